@@ -287,6 +287,26 @@ void kvo_quantize(const double* Y, int T, int d, int bits, const double* a16, co
     free(Zp);
 }
 
+/* Codes for a given grid (m, delta) and stored scales: t = (Y/(a c) - m)/delta,
+ * q = clamp(round-half-even(t), 0, 2^b-1). Used to check another implementation's
+ * codes against its own metadata. */
+void kvo_codes_for_grid(const double* Y, int T, int d, int bits, const double* a16, const double* c16,
+                        double m, double delta, uint8_t* codes, double* t_out) {
+    int L = (1 << bits) - 1;
+    for (int i = 0; i < T; ++i)
+        for (int j = 0; j < d; ++j) {
+            size_t e = (size_t)i * d + j;
+            double s = a16[i] * c16[j];
+            double z = s != 0.0 ? Y[e] / s : 0.0;
+            double t = (z - m) / delta;
+            if (t_out) t_out[e] = t;
+            double q = nearbyint(t);
+            if (q < 0) q = 0;
+            if (q > L) q = L;
+            codes[e] = (uint8_t)q;
+        }
+}
+
 /* ------------------------------------------------------------------------- */
 /* The group seal: rotate, normalise, store scales, quantise, pack.           */
 /* x: T x d fp16 bit patterns (token rows). side 0 = K, 1 = V.                */

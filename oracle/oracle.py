@@ -31,7 +31,7 @@ ITERS = 16
 
 __all__ = [
     "build", "lib", "half_to_double", "double_to_half", "hadamard", "rotate", "sinkhorn",
-    "record_bytes", "header_bytes", "pack", "unpack", "seal", "read_header", "quantize",
+    "record_bytes", "header_bytes", "pack", "unpack", "seal", "codes_for_grid", "read_header", "quantize",
     "dequant", "attention", "OracleCache", "bits_per_element", "GROUP", "SINK", "ITERS",
 ]
 
@@ -75,6 +75,7 @@ def lib():
             L.kvo_unpack.argtypes = [P, I, I, I, I, P]
             L.kvo_read_header.argtypes = [P, I, I, P, P, P, P]
             L.kvo_quantize.argtypes = [P, I, I, I, P, P, P, P, P, P]
+            L.kvo_codes_for_grid.argtypes = [P, I, I, I, P, P, D, D, P, P]
             L.kvo_seal.argtypes = [P, I, I, I, I, I, P, P, P]
             L.kvo_seal.restype = I
             L.kvo_dequant.argtypes = [P, I, I, I, I, I, P]
@@ -178,6 +179,17 @@ def quantize(Y: np.ndarray, bits: int, a16: np.ndarray, c16: np.ndarray):
     lib().kvo_quantize(_p(Y), T, d, bits, _p(a16), _p(c16), ctypes.byref(dl), ctypes.byref(m),
                        _p(codes), _p(t))
     return dl.value, m.value, codes, t
+
+
+def codes_for_grid(Y: np.ndarray, bits: int, a16, c16, m: float, delta: float):
+    """(codes, t) for a given grid and stored scales."""
+    Y = _c(Y, np.float64)
+    T, d = Y.shape
+    codes = np.empty((T, d), np.uint8)
+    t = np.empty((T, d))
+    lib().kvo_codes_for_grid(_p(Y), T, d, bits, _p(_c(a16, np.float64)), _p(_c(c16, np.float64)),
+                             float(m), float(delta), _p(codes), _p(t))
+    return codes, t
 
 
 def seal(x_half: np.ndarray, bits: int, side: int, iters: int = ITERS, return_scales: bool = False):

@@ -1,0 +1,820 @@
+// KVarN decode step for sm_103a: append, seal and split-K decode attention in one
+// persistent launch.
+//
+// Method (anbeeld.com "KVarN KV Cache: Implementation and Benchmarks", sections 1
+// and 2.1): the first 128 tokens (sink) and the partial newest group (tail) are read
+// exact in fp16 with the unrotated query; every sealed group is read straight from
+// its packed record with the query rotated by the same Hadamard matrix; the sealed
+// part of the output is accumulated in the rotated frame and rotated back once per
+// output row. A group is sealed at the moment its last token arrives, so a step whose
+// new token completes a group seals it first and attends to the sealed record.
+//
+// Work split. Every (sequence, KV head) pair is a block of scheduling units: one
+// exact item, one seal item if the step seals a group, and one unit per sealed group.
+// The units of all blocks are cut into equal contiguous ranges, one per CTA, so that
+// every CTA streams the same number of records. Each CTA writes one partial softmax
+// state (running max, sum, accumulator) per block it touches; the last CTA to finish a
+// block (atomic ticket, no waiting) merges the partials, rotates the sealed
+// accumulator back, adds the exact part and writes the fp16 output.
+//
+// Sealed-group stream. One producer thread copies whole group-pair records (K record
+// then V record, contiguous in the pool) into a ring of shared-memory stages with
+// cp.async.bulk; eight consumer warps take the stages round robin. For a group with
+// codes q, token scales a, channel scales c and grid (m, delta), the score of token t
+// is  scale * a_t * (delta * sum_j (q'_j c_j) q_tj + m * sum_j q'_j c_j)  with q' the
+// rotated query, and the rotated output accumulates
+//   c_j * (delta_V * sum_t w_t qV_jt + m_V * sum_t w_t),  w_t = p_t aV_t.
+// Both inner sums are dense 128 x 128 x (4 heads) contractions on the raw integer
+// codes, done with mma.sync m16n8k16 (f16 in, f32 accumulate). The codes become f16
+// operands by masking alone: a code placed in the low mantissa bits of a half is
+// the exact subnormal value code * 2^(e-24); the power of two is folded into the
+// other operand. The query side is split into f16 high and low parts in the eight
+// columns of the MMA (4 heads x 2), which keeps the logits at about fp32 accuracy.
+#include <cuda_fp16.h>
+#include <cuda_runtime.h>
+
+#include "kvarn_dev.cuh"
+
+namespace kvarn {
+
+namespace {
+
+constexpr int kE = 14;       // query operand exponent: |B| <= 2^14
+constexpr int kEV = 14;      // weight operand exponent
+constexpr int kXbHead = 88;  // exchange buffer words per head (bank-conflict-free stride)
+constexpr int kXbWarp = 4 * kXbHead;
+constexpr int kMrgFloats = 8 + 512;  // per warp: m[4], l[4], acc[4][128]
+constexpr int kConsumers = 256;
+#define kNegInf (-__int_as_float(0x7f800000))
+
+template <int B>
+struct Codes {
+    static constexpr int CPW = 32 / B;   // codes per 32-bit word
+    static constexpr int HALF = CPW / 2; // partner code distance (low half -> high half)
+    static constexpr int NWIN = 10 / B;  // codes of a 16-bit half that fit in the f16 mantissa
+    __host__ __device__ static constexpr int sh(int x) { return (x / NWIN) * NWIN * B; }
+    __host__ __device__ static constexpr int ex(int x) { return (x % NWIN) * B; }
+    __host__ __device__ static constexpr uint32_t mask(int x) { return (((1u << B) - 1u) << ex(x)) * 0x10001u; }
+};
+
+// pair P (0..15) of a thread's 32-code chunk: word P / HALF, position x = P % HALF;
+// the pair holds codes x and x + HALF of that word.
+template <int B>
+__device__ __forceinline__ void unpack16(const uint32_t (&w)[B], uint32_t (&a)[16]) {
+    using C = Codes<B>;
+#pragma unroll
+    for (int P = 0; P < 16; ++P) {
+        const int word = P / C::HALF, x = P % C::HALF;
+        a[P] = (w[word] >> C::sh(x)) & C::mask(x);
+    }
+}
+
+template <int B>
+__device__ __forceinline__ void load_chunk(const uint8_t* p, uint32_t (&w)[B]) {
+    if constexpr (B == 2) {
+        uint2 v = *reinterpret_cast<const uint2*>(p);
+        w[0] = v.x;
+        w[1] = v.y;
+    } else if constexpr (B == 4) {
+        uint4 v = *reinterpret_cast<const uint4*>(p);
+        w[0] = v.x; w[1] = v.y; w[2] = v.z; w[3] = v.w;
+    } else {
+        uint4 v0 = reinterpret_cast<const uint4*>(p)[0];
+        uint4 v1 = reinterpret_cast<const uint4*>(p)[1];
+        w[0] = v0.x; w[1] = v0.y; w[2] = v0.z; w[3] = v0.w;
+        w[4] = v1.x; w[5] = v1.y; w[6] = v1.z; w[7] = v1.w;
+    }
+}
+
+__device__ __forceinline__ void mma16816(float (&d)[4], uint32_t a0, uint32_t a1, uint32_t a2, uint32_t a3,
+                                         uint32_t b0, uint32_t b1) {
+    asm volatile(
+        "mma.sync.aligned.m16n8k16.row.col.f32.f16.f16.f32 {%0,%1,%2,%3}, {%4,%5,%6,%7}, {%8,%9}, "
+        "{%0,%1,%2,%3};\n"
+        : "+f"(d[0]), "+f"(d[1]), "+f"(d[2]), "+f"(d[3])
+        : "r"(a0), "r"(a1), "r"(a2), "r"(a3), "r"(b0), "r"(b1));
+}
+
+__device__ __forceinline__ uint32_t h2_bits(__half2 h) { return *reinterpret_cast<uint32_t*>(&h); }
+__device__ __forceinline__ __half2 bits_h2(uint32_t u) { return *reinterpret_cast<__half2*>(&u); }
+
+// QK row mapping: row g (0..7) of M tile mt holds token tok_row(mt, g) and row g + 8
+// holds that token + HALF_V, so the two scores of a thread are a V code pair.
+template <int VB>
+__device__ __forceinline__ int tok_row(int mt, int g) {
+    constexpr int CPW = 32 / VB, HALF = CPW / 2;
+    return CPW * (mt * (16 / CPW) + g / HALF) + g % HALF;
+}
+
+__device__ __forceinline__ int64_t covering(int64_t u, int64_t U, int64_t P) { return ((u + 1) * P + U - 1) / U - 1; }
+
+struct Item {
+    int type;  // 1 exact, 2 seal, 3 chunk of sealed groups
+    int ci;    // index of the sequence in the call
+    int kvh;
+    int g0, g1;
+};
+
+// Next item of this CTA's unit range [u, hi); advances u.
+__device__ bool next_item(const DecodeParams& p, int64_t& u, int64_t hi, Item& it) {
+    while (u < hi) {
+        int lo = 0, up = p.n_seqs - 1;
+        while (lo < up) {
+            int mid = (lo + up + 1) >> 1;
+            if (p.seqs[mid].unit_begin <= u) lo = mid; else up = mid - 1;
+        }
+        const SeqEntry& e = p.seqs[lo];
+        const int per = e.w_exact + e.w_seal + e.n_groups;
+        const int64_t rel = u - e.unit_begin;
+        const int kvh = (int)(rel / per);
+        const int off = (int)(rel % per);
+        const int64_t blk0 = e.unit_begin + (int64_t)kvh * per;
+        if (off < e.w_exact) {
+            u = blk0 + e.w_exact;
+            if (off == 0) { it = Item{1, lo, kvh, 0, 0}; return true; }
+            continue;
+        }
+        if (off < e.w_exact + e.w_seal) {
+            u = blk0 + e.w_exact + e.w_seal;
+            if (off == e.w_exact) { it = Item{2, lo, kvh, e.seal_group, e.seal_group + 1}; return true; }
+            continue;
+        }
+        const int gs = off - e.w_exact - e.w_seal;
+        const int64_t end = min(hi, blk0 + per);
+        it = Item{3, lo, kvh, gs, gs + (int)(end - u)};
+        u = end;
+        return true;
+    }
+    return false;
+}
+
+struct Smem {
+    uint8_t* stages;
+    uint64_t* full;
+    uint64_t* empty;
+    uint64_t* seal_done;
+    float* qrot;    // [4][128] rotated query / its max
+    float* qmax;    // [4]
+    float* xbuf;    // [8 warps][kXbWarp] (half2 words)
+    float* mrg;     // [8 warps][kMrgFloats], also exact-part and final-merge scratch
+    int* flag;
+    SealSmem* seal;
+};
+
+__device__ __forceinline__ float* partial_ptr(const DecodeParams& p, int blk, int slot) {
+    return reinterpret_cast<float*>(p.base + p.lay.partials) + ((size_t)blk * kPartialSlots + slot) * kPartialFloats;
+}
+
+__device__ __forceinline__ int32_t* err_word(const DecodeParams& p) {
+    return reinterpret_cast<int32_t*>(p.base + p.lay.err);
+}
+
+// 128-point Hadamard transform of a vector held by one warp, 4 consecutive values
+// per lane; scaled by 1/sqrt(128).
+__device__ __forceinline__ void warp_fwht128(float (&v)[4], int lane) {
+    float a0 = v[0] + v[1], a1 = v[0] - v[1], a2 = v[2] + v[3], a3 = v[2] - v[3];
+    v[0] = a0 + a2; v[2] = a0 - a2; v[1] = a1 + a3; v[3] = a1 - a3;
+#pragma unroll
+    for (int b = 1; b < 32; b <<= 1) {
+#pragma unroll
+        for (int e = 0; e < 4; ++e) {
+            float o = __shfl_xor_sync(0xffffffffu, v[e], b);
+            v[e] = (lane & b) ? (o - v[e]) : (v[e] + o);
+        }
+    }
+#pragma unroll
+    for (int e = 0; e < 4; ++e) v[e] *= kInvSqrt128;
+}
+
+// Expected number of partials of block (entry e, kvh) in this call.
+__device__ int expected_partials(const DecodeParams& p, const SeqEntry& e, int kvh, int64_t* first_cta) {
+    const int per = e.w_exact + e.w_seal + e.n_groups;
+    const int64_t g0u = e.unit_begin + (int64_t)kvh * per + e.w_exact + e.w_seal;
+    int n = 1 + (e.w_seal > 0 ? 1 : 0);
+    int64_t f = covering(g0u, p.units_total, p.grid);
+    if (e.n_groups > 0) n += (int)(covering(g0u + e.n_groups - 1, p.units_total, p.grid) - f + 1);
+    if (first_cta) *first_cta = f;
+    return n;
+}
+
+// Last CTA of a block: merge every partial of this call, rotate back, write out.
+__device__ void final_merge(const DecodeParams& p, const Smem& sm, int ci, int kvh) {
+    const int t = threadIdx.x;
+    const SeqEntry& e = p.seqs[ci];
+    const int blk = e.seq * p.hkv + kvh;
+    const int h = t >> 6, jj = 2 * (t & 63);
+    float M = kNegInf;
+    for (int s = 0; s < kPartialSlots; ++s) {
+        const float* P = partial_ptr(p, blk, s);
+        if ((uint32_t)__float_as_int(__ldcg(P)) != p.epoch) continue;
+        M = fmaxf(M, __ldcg(P + 4 + h));
+    }
+    float l = 0.f, r0 = 0.f, r1 = 0.f, x0 = 0.f, x1 = 0.f;
+    if (M != kNegInf) {
+        for (int s = 0; s < kPartialSlots; ++s) {
+            const float* P = partial_ptr(p, blk, s);
+            if ((uint32_t)__float_as_int(__ldcg(P)) != p.epoch) continue;
+            const float ms = __ldcg(P + 4 + h);
+            if (ms == kNegInf) continue;
+            const float w = exp2f(ms - M);
+            l += w * __ldcg(P + 8 + h);
+            const float2 a = __ldcg(reinterpret_cast<const float2*>(P + 12 + 128 * h + jj));
+            if (s == kSlotExact) {
+                x0 += w * a.x;
+                x1 += w * a.y;
+            } else {
+                r0 += w * a.x;
+                r1 += w * a.y;
+            }
+        }
+    }
+    float* rot = sm.mrg;        // [4][128]
+    float* ex = sm.mrg + 512;   // [4][128]
+    float* ls = sm.mrg + 1024;  // [4]
+    rot[128 * h + jj] = r0;
+    rot[128 * h + jj + 1] = r1;
+    ex[128 * h + jj] = x0;
+    ex[128 * h + jj + 1] = x1;
+    if ((t & 63) == 0) ls[h] = l;
+    named_bar(1, kConsumers);
+    const int w = t >> 5, lane = t & 31;
+    if (w < 4) {
+        float v[4];
+#pragma unroll
+        for (int k = 0; k < 4; ++k) v[k] = rot[128 * w + 4 * lane + k];
+        warp_fwht128(v, lane);
+#pragma unroll
+        for (int k = 0; k < 4; ++k) rot[128 * w + 4 * lane + k] = v[k];
+    }
+    named_bar(1, kConsumers);
+    if (h < p.r) {
+        const float lh = ls[h];
+        const float inv = lh > 0.f ? 1.0f / lh : 0.f;
+        __half2 o = __floats2half2_rn((ex[128 * h + jj] + rot[128 * h + jj]) * inv,
+                                      (ex[128 * h + jj + 1] + rot[128 * h + jj + 1]) * inv);
+        uint16_t* out = p.out + ((size_t)ci * p.hq + (size_t)kvh * p.r + h) * 128 + jj;
+        *reinterpret_cast<__half2*>(out) = o;
+    }
+}
+
+// Publish a partial (written by all consumer threads before the call) and merge if last.
+__device__ void publish(const DecodeParams& p, const Smem& sm, int ci, int kvh) {
+    __threadfence();
+    named_bar(1, kConsumers);
+    const SeqEntry& e = p.seqs[ci];
+    const int blk = e.seq * p.hkv + kvh;
+    if (threadIdx.x == 0) {
+        int expect = expected_partials(p, e, kvh, nullptr);
+        int32_t* tickets = reinterpret_cast<int32_t*>(p.base + p.lay.tickets);
+        int old = atomicAdd(tickets + blk, 1);
+        int last = (old == expect - 1);
+        if (last) tickets[blk] = 0;
+        __threadfence();
+        *sm.flag = last;
+    }
+    named_bar(1, kConsumers);
+    if (*sm.flag) final_merge(p, sm, ci, kvh);
+    named_bar(1, kConsumers);
+}
+
+// Exact part (sink + tail) of one block on CUDA cores; in a decode step the new token
+// is first written to the sink or tail (unless it completes a group).
+__device__ void exact_item(const DecodeParams& p, const Smem& sm, int ci, int kvh) {
+    const int t = threadIdx.x;
+    const SeqEntry& e = p.seqs[ci];
+    const size_t sl = (size_t)e.seq * p.num_layers + p.layer;
+    const size_t rows0 = (sl * p.hkv + kvh) * 128;  // first row of this (seq, layer, kv head)
+    const uint16_t* sink_k = reinterpret_cast<const uint16_t*>(p.base + p.lay.sink_k) + rows0 * 128;
+    const uint16_t* sink_v = reinterpret_cast<const uint16_t*>(p.base + p.lay.sink_v) + rows0 * 128;
+    const uint16_t* tail_k = reinterpret_cast<const uint16_t*>(p.base + p.lay.tail_k) + rows0 * 128;
+    const uint16_t* tail_v = reinterpret_cast<const uint16_t*>(p.base + p.lay.tail_v) + rows0 * 128;
+    if (e.new_pos >= 0 && e.seal_group < 0 && t < 32) {
+        const int side = t >> 4, chunk = t & 15;
+        const uint16_t* src = (side ? p.v_new : p.k_new) + ((size_t)ci * p.hkv + kvh) * 128;
+        size_t row = e.new_pos < kSink ? (size_t)e.new_pos : (size_t)((e.new_pos - kSink) % kGroup);
+        size_t off = (e.new_pos < kSink ? (side ? p.lay.sink_v : p.lay.sink_k) : (side ? p.lay.tail_v : p.lay.tail_k)) +
+                     (rows0 + row) * 256;
+        reinterpret_cast<uint4*>(p.base + off)[chunk] = reinterpret_cast<const uint4*>(src)[chunk];
+    }
+    float* qraw = sm.mrg;         // [4][128]
+    float* sc = sm.mrg + 512;     // [4][256]
+    float* red = sm.mrg + 1536;   // [4][2] max, [4][2] sum
+    for (int k = t; k < 512; k += kConsumers) {
+        const int h = k >> 7, j = k & 127;
+        qraw[k] = h < p.r ? half_bits_to_float(p.q[((size_t)ci * p.hq + (size_t)kvh * p.r + h) * 128 + j]) : 0.f;
+    }
+    named_bar(1, kConsumers);
+    const int n_ex = e.n_sink + e.n_tail;
+    float s[4] = {kNegInf, kNegInf, kNegInf, kNegInf};
+    if (t < n_ex) {
+        const uint16_t* row = t < e.n_sink ? sink_k + (size_t)t * 128 : tail_k + (size_t)(t - e.n_sink) * 128;
+        float d[4] = {0.f, 0.f, 0.f, 0.f};
+#pragma unroll 4
+        for (int c = 0; c < 16; ++c) {
+            uint4 kv = reinterpret_cast<const uint4*>(row)[c];
+            const __half2* hp = reinterpret_cast<const __half2*>(&kv);
+            float kf[8];
+#pragma unroll
+            for (int q2 = 0; q2 < 4; ++q2) {
+                float2 f = __half22float2(hp[q2]);
+                kf[2 * q2] = f.x;
+                kf[2 * q2 + 1] = f.y;
+            }
+#pragma unroll
+            for (int h = 0; h < 4; ++h) {
+                const float4 qa = reinterpret_cast<const float4*>(qraw + 128 * h + 8 * c)[0];
+                const float4 qb = reinterpret_cast<const float4*>(qraw + 128 * h + 8 * c)[1];
+                d[h] = fmaf(kf[0], qa.x, d[h]); d[h] = fmaf(kf[1], qa.y, d[h]);
+                d[h] = fmaf(kf[2], qa.z, d[h]); d[h] = fmaf(kf[3], qa.w, d[h]);
+                d[h] = fmaf(kf[4], qb.x, d[h]); d[h] = fmaf(kf[5], qb.y, d[h]);
+                d[h] = fmaf(kf[6], qb.z, d[h]); d[h] = fmaf(kf[7], qb.w, d[h]);
+            }
+        }
+#pragma unroll
+        for (int h = 0; h < 4; ++h) s[h] = d[h] * p.scale_log2;
+    }
+#pragma unroll
+    for (int h = 0; h < 4; ++h) sc[256 * h + t] = s[h];
+    named_bar(1, kConsumers);
+    // per-head max and sum: 64 threads per head, 4 entries each
+    {
+        const int h = t >> 6, k0 = 4 * (t & 63);
+        float m = fmaxf(fmaxf(sc[256 * h + k0], sc[256 * h + k0 + 1]), fmaxf(sc[256 * h + k0 + 2], sc[256 * h + k0 + 3]));
+#pragma unroll
+        for (int o = 16; o > 0; o >>= 1) m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, o));
+        if ((t & 31) == 0) red[2 * h + ((t >> 5) & 1)] = m;
+        named_bar(1, kConsumers);
+        m = fmaxf(red[2 * h], red[2 * h + 1]);
+        float sum = 0.f;
+#pragma unroll
+        for (int k = 0; k < 4; ++k) {
+            float v = sc[256 * h + k0 + k];
+            float pv = (m == kNegInf) ? 0.f : exp2f(v - m);
+            sc[256 * h + k0 + k] = pv;
+            sum += pv;
+        }
+#pragma unroll
+        for (int o = 16; o > 0; o >>= 1) sum += __shfl_xor_sync(0xffffffffu, sum, o);
+        if ((t & 31) == 0) red[8 + 2 * h + ((t >> 5) & 1)] = sum;
+        named_bar(1, kConsumers);
+        if ((t & 63) == 0) {
+            float* P = partial_ptr(p, e.seq * p.hkv + kvh, kSlotExact);
+            P[4 + h] = m;
+            P[8 + h] = red[8 + 2 * h] + red[8 + 2 * h + 1];
+        }
+    }
+    // P V: thread = channel j, two heads
+    {
+        const int j = t & 127, hp = t >> 7;
+        float a0 = 0.f, a1 = 0.f;
+        const float* p0 = sc + 256 * (2 * hp);
+        const float* p1 = sc + 256 * (2 * hp + 1);
+#pragma unroll 4
+        for (int k = 0; k < n_ex; ++k) {
+            const uint16_t* row = k < e.n_sink ? sink_v + (size_t)k * 128 : tail_v + (size_t)(k - e.n_sink) * 128;
+            const float v = half_bits_to_float(row[j]);
+            a0 = fmaf(p0[k], v, a0);
+            a1 = fmaf(p1[k], v, a1);
+        }
+        float* P = partial_ptr(p, e.seq * p.hkv + kvh, kSlotExact);
+        P[12 + 128 * (2 * hp) + j] = a0;
+        P[12 + 128 * (2 * hp + 1) + j] = a1;
+        if (t == 0) P[0] = __int_as_float((int)p.epoch);
+    }
+    publish(p, sm, ci, kvh);
+}
+
+// Rotate the query of a block: qrot = (q H) / max|q H| per head, qmax = that max.
+__device__ void setup_query(const DecodeParams& p, const Smem& sm, int ci, int kvh) {
+    const int t = threadIdx.x, w = t >> 5, lane = t & 31;
+    if (w < 4) {
+        float v[4] = {0.f, 0.f, 0.f, 0.f};
+        if (w < p.r) {
+            const uint16_t* q = p.q + ((size_t)ci * p.hq + (size_t)kvh * p.r + w) * 128 + 4 * lane;
+            uint2 raw = *reinterpret_cast<const uint2*>(q);
+            float2 f0 = __half22float2(bits_h2(raw.x)), f1 = __half22float2(bits_h2(raw.y));
+            v[0] = f0.x; v[1] = f0.y; v[2] = f1.x; v[3] = f1.y;
+        }
+        warp_fwht128(v, lane);
+        float mx = fmaxf(fmaxf(fabsf(v[0]), fabsf(v[1])), fmaxf(fabsf(v[2]), fabsf(v[3])));
+#pragma unroll
+        for (int o = 16; o > 0; o >>= 1) mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, o));
+        if (mx == 0.f) mx = 1.f;
+        const float inv = 1.0f / mx;
+#pragma unroll
+        for (int k = 0; k < 4; ++k) sm.qrot[128 * w + 4 * lane + k] = v[k] * inv;
+        if (lane == 0) sm.qmax[w] = mx;
+    }
+    named_bar(1, kConsumers);
+}
+
+struct WarpState {
+    float m, l;
+    float acc[8][2];
+};
+
+// Process one sealed group pair held in shared memory (K record, then V record).
+template <int KB, int VB>
+__device__ __forceinline__ void process_group(const DecodeParams& p, const uint8_t* rec, const float (&bq)[16][2],
+                                              float qm, float* xb, WarpState& st, int g, int tq) {
+    using CK = Codes<KB>;
+    using CV = Codes<VB>;
+    const uint8_t* krec = rec;
+    const uint8_t* vrec = rec + p.rec_k;
+    const float dK = *reinterpret_cast<const float*>(krec);
+    const float mK = *reinterpret_cast<const float*>(krec + 4);
+    const float dV = *reinterpret_cast<const float*>(vrec);
+    const float mV = *reinterpret_cast<const float*>(vrec + 4);
+    const uint16_t* aK = reinterpret_cast<const uint16_t*>(krec + 16);
+    const uint16_t* aV = reinterpret_cast<const uint16_t*>(vrec + 16);
+    const uint16_t* cV = reinterpret_cast<const uint16_t*>(vrec + 272);
+    // ---- query operand of this group: q' c_K, scaled, split into f16 high/low parts
+    uint32_t bk[16];
+    float kappa, sumqc;
+    {
+        const uint4* cp = reinterpret_cast<const uint4*>(krec + 272 + 64 * tq);
+        uint32_t cw[16];
+#pragma unroll
+        for (int k = 0; k < 4; ++k) {
+            uint4 v = cp[k];
+            cw[4 * k] = v.x; cw[4 * k + 1] = v.y; cw[4 * k + 2] = v.z; cw[4 * k + 3] = v.w;
+        }
+        float cf[32];
+#pragma unroll
+        for (int k = 0; k < 16; ++k) {
+            float2 f = __half22float2(bits_h2(cw[k]));
+            cf[2 * k] = f.x;
+            cf[2 * k + 1] = f.y;
+        }
+        float mc = cf[0];
+#pragma unroll
+        for (int k = 1; k < 32; ++k) mc = fmaxf(mc, cf[k]);
+        mc = fmaxf(mc, __shfl_xor_sync(0xffffffffu, mc, 1));
+        mc = fmaxf(mc, __shfl_xor_sync(0xffffffffu, mc, 2));
+        kappa = 1.0f / mc;
+        const bool lo_part = (g & 1) != 0;
+        float sum = 0.f;
+#pragma unroll
+        for (int P = 0; P < 16; ++P) {
+            const int x = P % CK::HALF;
+            const int c0 = CK::CPW * (P / CK::HALF) + x;
+            const float f0 = bq[P][0] * cf[c0] * kappa;
+            const float f1 = bq[P][1] * cf[c0 + CK::HALF] * kappa;
+            const __half2 hi = __floats2half2_rn(f0, f1);
+            if (lo_part) {
+                const float2 hf = __half22float2(hi);
+                bk[P] = h2_bits(__floats2half2_rn(f0 - hf.x, f1 - hf.y));
+            } else {
+                bk[P] = h2_bits(hi);
+            }
+            const float s = __int_as_float((127 + CK::ex(x) - kE) << 23);  // 2^(ex - E)
+            sum = fmaf(f0 + f1, s, sum);
+        }
+        sum += __shfl_xor_sync(0xffffffffu, sum, 1);
+        sum += __shfl_xor_sync(0xffffffffu, sum, 2);
+        // lane 8 tq holds the sum of head tq (its column head is (2 tq) >> 1 = tq)
+        sumqc = __shfl_sync(0xffffffffu, sum, 8 * tq) / kappa;
+    }
+    // ---- scores of the 16 tokens this thread holds (head tq)
+    float S[8][2];
+    {
+#pragma unroll
+        for (int mt = 0; mt < 8; ++mt) {
+            const int t0 = tok_row<VB>(mt, g), t1 = t0 + CV::HALF;
+            uint32_t w0[KB], w1[KB];
+            load_chunk<KB>(krec + 528 + t0 * 16 * KB + 4 * KB * tq, w0);
+            load_chunk<KB>(krec + 528 + t1 * 16 * KB + 4 * KB * tq, w1);
+            uint32_t a0[16], a1[16];
+            unpack16<KB>(w0, a0);
+            unpack16<KB>(w1, a1);
+            float c[4] = {0.f, 0.f, 0.f, 0.f};
+#pragma unroll
+            for (int ks = 0; ks < 8; ++ks) mma16816(c, a0[2 * ks], a1[2 * ks], a0[2 * ks + 1], a1[2 * ks + 1],
+                                                    bk[2 * ks], bk[2 * ks + 1]);
+            S[mt][0] = c[0] + c[1];
+            S[mt][1] = c[2] + c[3];
+        }
+    }
+    const float alpha = p.scale_log2 * qm * dK * (float)(1 << (24 - kE)) / kappa;
+    const float beta = p.scale_log2 * qm * mK * sumqc;
+    float gmax = kNegInf, amax = 0.f;
+    float av[8][2];
+#pragma unroll
+    for (int mt = 0; mt < 8; ++mt) {
+        const int t0 = tok_row<VB>(mt, g), t1 = t0 + CV::HALF;
+        S[mt][0] = half_bits_to_float(aK[t0]) * fmaf(alpha, S[mt][0], beta);
+        S[mt][1] = half_bits_to_float(aK[t1]) * fmaf(alpha, S[mt][1], beta);
+        gmax = fmaxf(gmax, fmaxf(S[mt][0], S[mt][1]));
+        av[mt][0] = half_bits_to_float(aV[t0]);
+        av[mt][1] = half_bits_to_float(aV[t1]);
+        amax = fmaxf(amax, fmaxf(av[mt][0], av[mt][1]));
+    }
+#pragma unroll
+    for (int o = 4; o < 32; o <<= 1) {
+        gmax = fmaxf(gmax, __shfl_xor_sync(0xffffffffu, gmax, o));
+        amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, o));
+    }
+    const float mnew = fmaxf(st.m, gmax);
+    const float corr = exp2f(st.m - mnew);
+    st.m = mnew;
+    const float rho = amax > 0.f ? 1.0f / amax : 1.0f;
+    const int xv = g % CV::HALF;
+    const float sv = __int_as_float((127 + kEV - CV::ex(xv)) << 23);    // 2^(EV - ex)
+    const float svi = __int_as_float((127 - kEV + CV::ex(xv)) << 23);   // 2^(ex - EV)
+    float lsum = 0.f, wsum = 0.f;
+#pragma unroll
+    for (int mt = 0; mt < 8; ++mt) {
+        const float p0 = exp2f(S[mt][0] - mnew), p1 = exp2f(S[mt][1] - mnew);
+        lsum += p0 + p1;
+        const __half2 wh = __floats2half2_rn(p0 * av[mt][0] * rho * sv, p1 * av[mt][1] * rho * sv);
+        const float2 wf = __half22float2(wh);
+        wsum = fmaf(wf.x + wf.y, svi, wsum);
+        reinterpret_cast<uint32_t*>(xb)[kXbHead * tq + 20 * (mt >> 1) + 8 * (mt & 1) + g] = h2_bits(wh);
+    }
+    st.l = fmaf(st.l, corr, lsum);
+#pragma unroll
+    for (int o = 4; o < 32; o <<= 1) wsum += __shfl_xor_sync(0xffffffffu, wsum, o);
+    __syncwarp();
+    uint32_t bv[16];
+    {
+        const uint4* src = reinterpret_cast<const uint4*>(xb + kXbHead * (g >> 1) + 20 * tq);
+#pragma unroll
+        for (int k = 0; k < 4; ++k) {
+            uint4 v = src[k];
+            bv[4 * k] = v.x; bv[4 * k + 1] = v.y; bv[4 * k + 2] = v.z; bv[4 * k + 3] = v.w;
+        }
+    }
+    __syncwarp();
+    // ---- P V in the rotated frame
+    const float gam = dV * (float)(1 << (24 - kEV)) / rho;
+    const float del = mV * wsum / rho;
+#pragma unroll
+    for (int mt = 0; mt < 8; ++mt) {
+        const int c0 = 16 * mt + g, c1 = c0 + 8;
+        uint32_t w0[VB], w1[VB];
+        load_chunk<VB>(vrec + 528 + c0 * 16 * VB + 4 * VB * tq, w0);
+        load_chunk<VB>(vrec + 528 + c1 * 16 * VB + 4 * VB * tq, w1);
+        uint32_t a0[16], a1[16];
+        unpack16<VB>(w0, a0);
+        unpack16<VB>(w1, a1);
+        float d[4] = {0.f, 0.f, 0.f, 0.f};
+#pragma unroll
+        for (int ks = 0; ks < 8; ++ks) mma16816(d, a0[2 * ks], a1[2 * ks], a0[2 * ks + 1], a1[2 * ks + 1],
+                                                bv[2 * ks], bv[2 * ks + 1]);
+        st.acc[mt][0] = fmaf(st.acc[mt][0], corr, half_bits_to_float(cV[c0]) * fmaf(gam, d[0], del));
+        st.acc[mt][1] = fmaf(st.acc[mt][1], corr, half_bits_to_float(cV[c1]) * fmaf(gam, d[2], del));
+    }
+}
+
+// Merge the eight warps' states of one item into a partial in global memory.
+__device__ void write_item_partial(const DecodeParams& p, const Smem& sm, const WarpState& st, int blk, int slot) {
+    const int t = threadIdx.x, w = t >> 5, lane = t & 31, g = lane >> 2, tq = lane & 3;
+    float l = st.l;
+#pragma unroll
+    for (int o = 4; o < 32; o <<= 1) l += __shfl_xor_sync(0xffffffffu, l, o);
+    float* M = sm.mrg + w * kMrgFloats;
+    if (g == 0) {
+        M[tq] = st.m;
+        M[4 + tq] = l;
+    }
+#pragma unroll
+    for (int mt = 0; mt < 8; ++mt) {
+        M[8 + 128 * tq + 16 * mt + g] = st.acc[mt][0];
+        M[8 + 128 * tq + 16 * mt + g + 8] = st.acc[mt][1];
+    }
+    named_bar(1, kConsumers);
+    const int h = t >> 6, jj = 2 * (t & 63);
+    float mx = kNegInf;
+#pragma unroll
+    for (int k = 0; k < 8; ++k) mx = fmaxf(mx, sm.mrg[k * kMrgFloats + h]);
+    float ls = 0.f, a0 = 0.f, a1 = 0.f;
+#pragma unroll
+    for (int k = 0; k < 8; ++k) {
+        const float* Mk = sm.mrg + k * kMrgFloats;
+        const float mk = Mk[h];
+        if (mk == kNegInf) continue;
+        const float wgt = exp2f(mk - mx);
+        ls = fmaf(wgt, Mk[4 + h], ls);
+        a0 = fmaf(wgt, Mk[8 + 128 * h + jj], a0);
+        a1 = fmaf(wgt, Mk[8 + 128 * h + jj + 1], a1);
+    }
+    float* P = partial_ptr(p, blk, slot);
+    *reinterpret_cast<float2*>(P + 12 + 128 * h + jj) = make_float2(a0, a1);
+    if ((t & 63) == 0) {
+        P[4 + h] = mx;
+        P[8 + h] = ls;
+    }
+    if (t == 0) P[0] = __int_as_float((int)p.epoch);
+}
+
+__device__ __forceinline__ const uint8_t* group_src(const DecodeParams& p, int seq, int kvh, int g) {
+    const int32_t* table = reinterpret_cast<const int32_t*>(p.base + p.lay.block_table);
+    int slot = table[((size_t)seq * p.num_layers + p.layer) * p.max_groups + g];
+    if (slot < 0 || slot >= p.pool_slots) {
+        atomicOr(err_word(p), kErrBadSlot);
+        slot = 0;
+    }
+    return p.base + p.lay.pool + (size_t)slot * p.slot_bytes + (size_t)kvh * (p.rec_k + p.rec_v);
+}
+
+struct SealRows {
+    const uint16_t* tail;  // rows 0..126
+    const uint16_t* last;  // row 127: the new token
+    __device__ const uint16_t* operator()(int i) const { return i < 127 ? tail + 128 * i : last; }
+};
+
+template <int KB, int VB>
+__global__ void __launch_bounds__(kDecodeThreads, 1) decode_kernel(const __grid_constant__ DecodeParams p) {
+    extern __shared__ __align__(128) uint8_t smem_raw[];
+    Smem sm;
+    const int pair = p.rec_k + p.rec_v;
+    {
+        size_t off = 0;
+        sm.stages = smem_raw;
+        off += (size_t)p.stages * pair;
+        off = (off + 15) & ~(size_t)15;
+        sm.full = reinterpret_cast<uint64_t*>(smem_raw + off);
+        off += 16 * 8;
+        sm.empty = reinterpret_cast<uint64_t*>(smem_raw + off);
+        off += 16 * 8;
+        sm.seal_done = reinterpret_cast<uint64_t*>(smem_raw + off);
+        off += 16;
+        sm.qrot = reinterpret_cast<float*>(smem_raw + off);
+        off += 512 * 4;
+        sm.qmax = reinterpret_cast<float*>(smem_raw + off);
+        off += 16;
+        sm.flag = reinterpret_cast<int*>(smem_raw + off);
+        off += 16;
+        sm.xbuf = reinterpret_cast<float*>(smem_raw + off);
+        off += 8 * kXbWarp * 4;
+        sm.mrg = reinterpret_cast<float*>(smem_raw + off);
+        off += 8 * kMrgFloats * 4;
+        sm.seal = reinterpret_cast<SealSmem*>(smem_raw + off);
+    }
+    const int t = threadIdx.x, w = t >> 5, lane = t & 31;
+    if (t == 0) {
+        for (int s = 0; s < p.stages; ++s) {
+            mbar_init(sm.full + s, 1);
+            mbar_init(sm.empty + s, 1);
+        }
+        mbar_init(sm.seal_done, 1);
+        asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+    }
+    __syncthreads();
+    const int64_t U = p.units_total, P = p.grid, b = blockIdx.x;
+    const int64_t lo = b * U / P, hi = (b + 1) * U / P;
+    int32_t* err = err_word(p);
+
+    if (w == 8) {
+        // ---------------- producer: stream the records of this CTA's groups
+        if (lane == 0) {
+            int64_t u = lo;
+            Item it;
+            uint32_t n = 0, sd = 0;
+            while (next_item(p, u, hi, it)) {
+                if (it.type == 1) continue;
+                const SeqEntry& e = p.seqs[it.ci];
+                if (it.type == 2) {
+                    mbar_wait(sm.seal_done, sd, err);
+                    sd ^= 1;
+                    fence_proxy_async_global();
+                }
+                for (int g = it.g0; g < it.g1; ++g) {
+                    const uint32_t s = n % p.stages;
+                    if (n >= (uint32_t)p.stages) mbar_wait(sm.empty + s, ((n / p.stages) - 1) & 1, err);
+                    const uint8_t* src;
+                    if (it.type == 2)
+                        src = p.base + p.lay.pool + (size_t)e.seal_slot * p.slot_bytes + (size_t)it.kvh * pair;
+                    else
+                        src = group_src(p, e.seq, it.kvh, g);
+                    mbar_arrive_expect_tx(sm.full + s, pair);
+                    bulk_g2s(sm.stages + (size_t)s * pair, src, pair, sm.full + s);
+                    ++n;
+                }
+            }
+            // drain: wait until the consumers have released every stage still in flight
+            const uint32_t first = n > (uint32_t)p.stages ? n - p.stages : 0;
+            for (uint32_t k = first; k < n; ++k) mbar_wait(sm.empty + (k % p.stages), (k / p.stages) & 1, err);
+        }
+        return;
+    }
+
+    // ---------------- consumers: 8 warps
+    const int g = lane >> 2, tq = lane & 3;
+    int64_t u = lo;
+    Item it;
+    uint32_t n = 0;
+    using CK = Codes<KB>;
+    while (next_item(p, u, hi, it)) {
+        const SeqEntry& e = p.seqs[it.ci];
+        const int blk = e.seq * p.hkv + it.kvh;
+        if (it.type == 1) {
+            exact_item(p, sm, it.ci, it.kvh);
+            continue;
+        }
+        int slot;
+        if (it.type == 2) {
+            // seal K and V of the completed group: rows 0..126 from the tail, row 127 new
+            const size_t sl = (size_t)e.seq * p.num_layers + p.layer;
+            const size_t rows0 = (sl * p.hkv + it.kvh) * 128;
+            uint8_t* dst = p.base + p.lay.pool + (size_t)e.seal_slot * p.slot_bytes + (size_t)it.kvh * pair;
+            SealRows rk{reinterpret_cast<const uint16_t*>(p.base + p.lay.tail_k) + rows0 * 128,
+                        p.k_new + ((size_t)it.ci * p.hkv + it.kvh) * 128};
+            seal_matrix(rk, p.k_bits, 0, p.iters, dst, nullptr, *sm.seal, 1);
+            SealRows rv{reinterpret_cast<const uint16_t*>(p.base + p.lay.tail_v) + rows0 * 128,
+                        p.v_new + ((size_t)it.ci * p.hkv + it.kvh) * 128};
+            seal_matrix(rv, p.v_bits, 1, p.iters, dst + p.rec_k, nullptr, *sm.seal, 1);
+            if (t == 0 && it.kvh == 0) {
+                int32_t* table = reinterpret_cast<int32_t*>(p.base + p.lay.block_table);
+                table[sl * p.max_groups + e.seal_group] = e.seal_slot;
+            }
+            fence_proxy_async_global();
+            named_bar(1, kConsumers);
+            if (t == 0) mbar_arrive(sm.seal_done);
+            slot = kSlotSeal;
+        } else {
+            int64_t first;
+            expected_partials(p, e, it.kvh, &first);
+            slot = kSlotChunk0 + (int)(b - first);
+            if (slot >= kPartialSlots) {  // cannot happen with the host's schedule
+                if (t == 0) atomicOr(err, kErrSpan);
+                slot = kPartialSlots - 1;
+            }
+        }
+        setup_query(p, sm, it.ci, it.kvh);
+        // loop-invariant query operand base: q_hat(head g>>1, channel) * 2^(E - ex)
+        float bq[16][2];
+        {
+            const float* qh = sm.qrot + 128 * (g >> 1);
+#pragma unroll
+            for (int P2 = 0; P2 < 16; ++P2) {
+                const int x = P2 % CK::HALF;
+                const int c0 = 32 * tq + CK::CPW * (P2 / CK::HALF) + x;
+                const float s = __int_as_float((127 + kE - CK::ex(x)) << 23);
+                bq[P2][0] = qh[c0] * s;
+                bq[P2][1] = qh[c0 + CK::HALF] * s;
+            }
+        }
+        const float qm = sm.qmax[tq];
+        WarpState st;
+        st.m = kNegInf;
+        st.l = 0.f;
+#pragma unroll
+        for (int mt = 0; mt < 8; ++mt) st.acc[mt][0] = st.acc[mt][1] = 0.f;
+        float* xb = sm.xbuf + w * kXbWarp;
+        const uint32_t cnt = (uint32_t)(it.g1 - it.g0);
+        for (uint32_t k = (w + 8 - (n & 7)) & 7; k < cnt; k += 8) {
+            const uint32_t gn = n + k;
+            const uint32_t s = gn % p.stages;
+            mbar_wait(sm.full + s, (gn / p.stages) & 1, err);
+            process_group<KB, VB>(p, sm.stages + (size_t)s * pair, bq, qm, xb, st, g, tq);
+            __syncwarp();
+            if (lane == 0) mbar_arrive(sm.empty + s);
+        }
+        n += cnt;
+        write_item_partial(p, sm, st, blk, slot);
+        publish(p, sm, it.ci, it.kvh);
+    }
+}
+
+template <int KB, int VB>
+int launch_t(const DecodeParams& p, int smem, cudaStream_t s) {
+    static bool attr = false;
+    if (!attr) {
+        cudaError_t e = cudaFuncSetAttribute(decode_kernel<KB, VB>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                             max_optin_smem());
+        if (e != cudaSuccess) return (int)e;
+        attr = true;
+    }
+    decode_kernel<KB, VB><<<p.grid, kDecodeThreads, smem, s>>>(p);
+    return (int)cudaGetLastError();
+}
+
+}  // namespace
+
+int decode_smem_bytes(int k_bits, int v_bits, int stages, bool with_seal) {
+    size_t pair = record_bytes(k_bits) + record_bytes(v_bits);
+    size_t off = (size_t)stages * pair;
+    off = (off + 15) & ~(size_t)15;
+    off += 16 * 8 * 2 + 16 + 512 * 4 + 16 + 16 + 8 * kXbWarp * 4 + 8 * kMrgFloats * 4;
+    if (with_seal) off += sizeof(SealSmem);
+    return (int)off;
+}
+
+int launch_decode(const DecodeParams& p, int smem, void* stream) {
+    cudaStream_t s = (cudaStream_t)stream;
+    switch (p.k_bits * 16 + p.v_bits) {
+        case 0x22: return launch_t<2, 2>(p, smem, s);
+        case 0x24: return launch_t<2, 4>(p, smem, s);
+        case 0x28: return launch_t<2, 8>(p, smem, s);
+        case 0x42: return launch_t<4, 2>(p, smem, s);
+        case 0x44: return launch_t<4, 4>(p, smem, s);
+        case 0x48: return launch_t<4, 8>(p, smem, s);
+        case 0x82: return launch_t<8, 2>(p, smem, s);
+        case 0x84: return launch_t<8, 4>(p, smem, s);
+        case 0x88: return launch_t<8, 8>(p, smem, s);
+    }
+    return (int)cudaErrorInvalidValue;
+}
+
+}  // namespace kvarn

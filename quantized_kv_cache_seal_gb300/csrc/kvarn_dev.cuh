@@ -1,0 +1,315 @@
+// Device helpers and the KVarN group seal, shared by the kernels of this library.
+//
+// The seal follows fig1.dev "KVarN: Variance-Normalized KV-Cache Quantization ...",
+// "What it is", and anbeeld.com "KVarN KV Cache: Implementation and Benchmarks",
+// sections 1 and 2.1: rotate each token row of a 128 x 128 group by the Hadamard
+// matrix, run 16 Sinkhorn iterations that rescale the token axis and then the
+// channel axis to unit mean square, store the scales, round to nearest on one
+// min/max grid and pack the codes next to the scale metadata.
+#pragma once
+#include <cuda_fp16.h>
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+#include "kvarn_internal.h"
+
+namespace kvarn {
+
+constexpr float kInvSqrt128 = 0.08838834764831845f;
+constexpr uint64_t kWaitLimitNs = 2000000000ull;  // a bounded wait gives up after 2 s
+
+__device__ __forceinline__ uint32_t smem_addr(const void* p) {
+    return (uint32_t)__cvta_generic_to_shared(p);
+}
+
+__device__ __forceinline__ uint64_t global_ns() {
+    uint64_t t;
+    asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(t));
+    return t;
+}
+
+__device__ __forceinline__ void mbar_init(uint64_t* bar, uint32_t count) {
+    asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" ::"r"(smem_addr(bar)), "r"(count) : "memory");
+}
+
+__device__ __forceinline__ void mbar_arrive(uint64_t* bar) {
+    asm volatile("mbarrier.arrive.release.cta.shared::cta.b64 _, [%0];" ::"r"(smem_addr(bar)) : "memory");
+}
+
+__device__ __forceinline__ void mbar_arrive_expect_tx(uint64_t* bar, uint32_t bytes) {
+    asm volatile("mbarrier.arrive.expect_tx.release.cta.shared::cta.b64 _, [%0], %1;" ::"r"(smem_addr(bar)),
+                 "r"(bytes)
+                 : "memory");
+}
+
+__device__ __forceinline__ bool mbar_try_wait(uint64_t* bar, uint32_t parity) {
+    uint32_t ok;
+    asm volatile(
+        "{\n .reg .pred p;\n mbarrier.try_wait.parity.acquire.cta.shared::cta.b64 p, [%1], %2;\n"
+        " selp.u32 %0, 1, 0, p;\n}\n"
+        : "=r"(ok)
+        : "r"(smem_addr(bar)), "r"(parity)
+        : "memory");
+    return ok != 0;
+}
+
+// Wait for the phase with the given parity to complete; give up after kWaitLimitNs,
+// record kErrTimeout in the error word and return false.
+// A wait that starts after any wait of the launch has given up returns at once, so a
+// failure ends the kernel within one time limit.
+__device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity, int32_t* err) {
+    if (mbar_try_wait(bar, parity)) return true;
+    if (*reinterpret_cast<volatile int32_t*>(err) & kErrTimeout) return false;
+    const uint64_t t0 = global_ns();
+    for (;;) {
+        for (int i = 0; i < 32; ++i)
+            if (mbar_try_wait(bar, parity)) return true;
+        if (global_ns() - t0 > kWaitLimitNs) {
+            atomicOr(err, kErrTimeout);
+            return false;
+        }
+    }
+}
+
+// One-dimensional bulk copy global -> shared, completing on an mbarrier.
+__device__ __forceinline__ void bulk_g2s(void* dst, const void* src, uint32_t bytes, uint64_t* bar) {
+    asm volatile(
+        "cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];" ::"r"(
+            smem_addr(dst)),
+        "l"(src), "r"(bytes), "r"(smem_addr(bar))
+        : "memory");
+}
+
+__device__ __forceinline__ void fence_proxy_async_global() {
+    asm volatile("fence.proxy.async.global;" ::: "memory");
+}
+
+__device__ __forceinline__ void named_bar(int id, int n) {
+    asm volatile("bar.sync %0, %1;" ::"r"(id), "r"(n) : "memory");
+}
+
+__device__ __forceinline__ uint16_t f16_bits_sat(float x) {
+    // round to nearest even; values beyond the largest finite half saturate
+    return __half_as_ushort(__float2half_rn(fminf(x, 65504.0f)));
+}
+
+__device__ __forceinline__ float half_bits_to_float(uint16_t b) { return __half2float(__ushort_as_half(b)); }
+
+// ---------------------------------------------------------------------------
+// Seal of one 128 x 128 group matrix by 256 threads.
+// ---------------------------------------------------------------------------
+struct SealSmem {
+    float Y[128 * 136];   // rotated group: row i at 136 i, channel j at j + 4 (j >= 64)
+    float u[136];         // 1 / c^2, same padding as a row
+    float v[136];         // 1 / a^2
+    float ra[128];        // 1 / a16
+    float rc[128];        // 1 / c16
+    float red[2][8];
+    uint16_t a16[128];
+    uint16_t c16[128];
+};
+
+__device__ __forceinline__ int ypad(int j) { return j + ((j >> 6) << 2); }
+
+template <int B>
+__device__ __forceinline__ void pack64_store(const int (&q)[64], uint8_t* dst) {
+    // 64 codes of B bits, least significant first, into 2B little-endian words
+    constexpr int CPW = 32 / B;
+    uint32_t w[2 * B];
+#pragma unroll
+    for (int k = 0; k < 2 * B; ++k) w[k] = 0;
+#pragma unroll
+    for (int e = 0; e < 64; ++e) w[e / CPW] |= (uint32_t)q[e] << ((e % CPW) * B);
+    uint4* d = reinterpret_cast<uint4*>(dst);
+#pragma unroll
+    for (int k = 0; k < B / 2; ++k) d[k] = make_uint4(w[4 * k], w[4 * k + 1], w[4 * k + 2], w[4 * k + 3]);
+}
+
+// Row pointer functor: rows(i) returns a 16-byte aligned pointer to 128 fp16 values.
+// which: 0 = K (token-major codes), 1 = V (channel-major codes).
+// bar_id: named barrier used among the 256 participating threads (threads 0..255).
+template <class Rows>
+__device__ void seal_matrix(const Rows& rows, int bits, int which, int iters, uint8_t* rec, float* dbg,
+                            SealSmem& S, int bar_id) {
+    const int t = threadIdx.x;
+    const int i = t >> 1, h = t & 1;  // row role: token row i, channel half h
+    const int j = t >> 1, hc = t & 1; // column role: channel j, token half hc
+    // 1. rotation Y = X H of every token row: 6 butterfly stages in registers,
+    //    the seventh across the partner thread, then the 1/sqrt(128) scaling.
+    float x[64];
+    {
+        const uint4* src = reinterpret_cast<const uint4*>(rows(i) + 64 * h);
+#pragma unroll
+        for (int q = 0; q < 8; ++q) {
+            uint4 w = src[q];
+            const __half2* hp = reinterpret_cast<const __half2*>(&w);
+#pragma unroll
+            for (int e = 0; e < 4; ++e) {
+                float2 f = __half22float2(hp[e]);
+                x[8 * q + 2 * e] = f.x;
+                x[8 * q + 2 * e + 1] = f.y;
+            }
+        }
+    }
+#pragma unroll
+    for (int len = 1; len < 64; len <<= 1) {
+#pragma unroll
+        for (int k = 0; k < 64; ++k) {
+            if (!(k & len)) {
+                float a = x[k], b = x[k + len];
+                x[k] = a + b;
+                x[k + len] = a - b;
+            }
+        }
+    }
+    float arow[64];
+#pragma unroll
+    for (int k = 0; k < 64; ++k) {
+        float o = __shfl_xor_sync(0xffffffffu, x[k], 1);
+        float y = (h ? (o - x[k]) : (x[k] + o)) * kInvSqrt128;
+        x[k] = y;
+        arow[k] = y * y;
+    }
+    {
+        float4* dst = reinterpret_cast<float4*>(S.Y + 136 * i + 68 * h);
+#pragma unroll
+        for (int q = 0; q < 16; ++q) dst[q] = make_float4(x[4 * q], x[4 * q + 1], x[4 * q + 2], x[4 * q + 3]);
+    }
+    if (t < 128) S.u[ypad(t)] = 1.0f;
+    named_bar(bar_id, 256);
+    float acol[64];
+#pragma unroll
+    for (int k = 0; k < 64; ++k) {
+        float y = S.Y[136 * (64 * hc + k) + ypad(j)];
+        acol[k] = y * y;
+    }
+    // 2. Sinkhorn on A = Y*Y in its matrix-vector form: a_i^2 = mean_j A_ij / c_j^2,
+    //    then c_j^2 = mean_i A_ij / a_i^2 (equal to rescaling the rows and columns of
+    //    Y in turn; a zero row or column keeps the factor 1).
+    float a2 = 1.0f, c2 = 1.0f;
+    for (int it = 0; it < iters; ++it) {
+        float p0 = 0.f, p1 = 0.f;
+        const float4* up = reinterpret_cast<const float4*>(S.u + 68 * h);
+#pragma unroll
+        for (int q = 0; q < 16; ++q) {
+            float4 uu = up[q];
+            p0 = fmaf(arow[4 * q], uu.x, p0);
+            p1 = fmaf(arow[4 * q + 1], uu.y, p1);
+            p0 = fmaf(arow[4 * q + 2], uu.z, p0);
+            p1 = fmaf(arow[4 * q + 3], uu.w, p1);
+        }
+        float p = p0 + p1;
+        p += __shfl_xor_sync(0xffffffffu, p, 1);
+        a2 = p * (1.0f / 128.0f);
+        if (a2 == 0.0f) a2 = 1.0f;
+        if (h == 0) S.v[ypad(i)] = 1.0f / a2;
+        named_bar(bar_id, 256);
+        p0 = 0.f;
+        p1 = 0.f;
+        const float4* vp = reinterpret_cast<const float4*>(S.v + 68 * hc);
+#pragma unroll
+        for (int q = 0; q < 16; ++q) {
+            float4 vv = vp[q];
+            p0 = fmaf(acol[4 * q], vv.x, p0);
+            p1 = fmaf(acol[4 * q + 1], vv.y, p1);
+            p0 = fmaf(acol[4 * q + 2], vv.z, p0);
+            p1 = fmaf(acol[4 * q + 3], vv.w, p1);
+        }
+        p = p0 + p1;
+        p += __shfl_xor_sync(0xffffffffu, p, 1);
+        c2 = p * (1.0f / 128.0f);
+        if (c2 == 0.0f) c2 = 1.0f;
+        if (hc == 0) S.u[ypad(j)] = 1.0f / c2;
+        named_bar(bar_id, 256);
+    }
+    // 3. stored scales: fp16, round to nearest even, saturating
+    if (h == 0) {
+        float a = sqrtf(a2);
+        uint16_t ab = f16_bits_sat(a);
+        S.a16[i] = ab;
+        S.ra[i] = 1.0f / half_bits_to_float(ab);
+        if (dbg) dbg[i] = a;
+    }
+    if (hc == 0) {
+        float c = sqrtf(c2);
+        uint16_t cb = f16_bits_sat(c);
+        S.c16[j] = cb;
+        S.rc[j] = 1.0f / half_bits_to_float(cb);
+        if (dbg) dbg[128 + j] = c;
+    }
+    named_bar(bar_id, 256);
+    // 4. normalised values Z' = Y / (a16 c16) from the packing perspective of this side
+    float z[64];
+    if (which == 0) {
+        const float4* src = reinterpret_cast<const float4*>(S.Y + 136 * i + 68 * h);
+        const float rai = S.ra[i];
+#pragma unroll
+        for (int q = 0; q < 16; ++q) {
+            float4 y = src[q];
+            z[4 * q + 0] = y.x * rai * S.rc[64 * h + 4 * q + 0];
+            z[4 * q + 1] = y.y * rai * S.rc[64 * h + 4 * q + 1];
+            z[4 * q + 2] = y.z * rai * S.rc[64 * h + 4 * q + 2];
+            z[4 * q + 3] = y.w * rai * S.rc[64 * h + 4 * q + 3];
+        }
+    } else {
+        const float rcj = S.rc[j];
+#pragma unroll
+        for (int k = 0; k < 64; ++k) z[k] = S.Y[136 * (64 * hc + k) + ypad(j)] * S.ra[64 * hc + k] * rcj;
+    }
+    float mn = z[0], mx = z[0];
+#pragma unroll
+    for (int k = 1; k < 64; ++k) {
+        mn = fminf(mn, z[k]);
+        mx = fmaxf(mx, z[k]);
+    }
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) {
+        mn = fminf(mn, __shfl_xor_sync(0xffffffffu, mn, o));
+        mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, o));
+    }
+    if ((t & 31) == 0) {
+        S.red[0][t >> 5] = mn;
+        S.red[1][t >> 5] = mx;
+    }
+    named_bar(bar_id, 256);
+    mn = S.red[0][0];
+    mx = S.red[1][0];
+#pragma unroll
+    for (int w = 1; w < 8; ++w) {
+        mn = fminf(mn, S.red[0][w]);
+        mx = fmaxf(mx, S.red[1][w]);
+    }
+    const int L = (1 << bits) - 1;
+    float delta = (mx - mn) / (float)L;
+    if (delta == 0.0f) delta = 1.0f;
+    const float inv = 1.0f / delta;
+    // 5. round to nearest (ties to even), clamp, pack
+    int qv[64];
+#pragma unroll
+    for (int k = 0; k < 64; ++k) {
+        int c = __float2int_rn((z[k] - mn) * inv);
+        qv[k] = min(max(c, 0), L);
+    }
+    const int row = (which == 0) ? i : j;  // token row (K) or channel row (V)
+    const int half = (which == 0) ? h : hc;
+    uint8_t* codes = rec + 528;
+    if (bits == 2)
+        pack64_store<2>(qv, codes + 32 * row + 16 * half);
+    else if (bits == 4)
+        pack64_store<4>(qv, codes + 64 * row + 32 * half);
+    else
+        pack64_store<8>(qv, codes + 128 * row + 64 * half);
+    // 6. header: delta, m, zero, a16[128], c16[128]
+    uint16_t* r16 = reinterpret_cast<uint16_t*>(rec);
+    if (t == 0) {
+        uint4 hdr = make_uint4(__float_as_uint(delta), __float_as_uint(mn), 0u, 0u);
+        *reinterpret_cast<uint4*>(rec) = hdr;
+    }
+    if (t < 128)
+        r16[8 + t] = S.a16[t];
+    else
+        r16[8 + 128 + (t - 128)] = S.c16[t - 128];
+    named_bar(bar_id, 256);
+}
+
+}  // namespace kvarn

@@ -1,0 +1,552 @@
+// Host side of the KVarN cache: argument checks, the host mirror of sequence
+// lengths and pool slots, scheduling of the decode kernel, and the C ABI.
+//
+// Region rules (anbeeld.com "KVarN KV Cache: Implementation and Benchmarks", 2.1):
+// positions 0..127 form the sink; body group g covers positions [128 + 128 g,
+// 256 + 128 g) and is sealed when its last token arrives; the partial newest group
+// (the tail) stays exact. The host mirror decides every seal and slot without
+// reading anything back from the device.
+#include <algorithm>
+#include <cmath>
+#include <cstdio>
+#include <cstring>
+#include <new>
+#include <vector>
+
+#include "../../include/kvarn.h"
+#include "kvarn_internal.h"
+
+using namespace kvarn;
+
+namespace {
+thread_local char g_last_error[256] = "";
+
+void set_cuda_error(int code, const char* what) {
+    std::snprintf(g_last_error, sizeof(g_last_error), "%s: %s (%d)", what, cuda_error_string(code), code);
+}
+
+size_t align_up(size_t x, size_t a) { return (x + a - 1) / a * a; }
+
+bool bits_ok(int b) { return b == 2 || b == 4 || b == 8; }
+
+int64_t groups_sealed(int64_t n) { return n > kSink ? (n - kSink) / kGroup : 0; }
+}  // namespace
+
+struct kvarn_cache {
+    kvarn_config cfg;
+    Layout lay;
+    uint8_t* base = nullptr;
+    size_t bytes = 0;
+    int r = 1;
+    int max_groups = 0;
+    size_t rec_k = 0, rec_v = 0, slot_bytes = 0;
+    std::vector<int64_t> len;          // [max_seqs][num_layers]
+    std::vector<int32_t> table;        // [max_seqs][num_layers][max_groups]
+    std::vector<int32_t> free_slots;   // stack of free pool slots
+    bool initialized = false;
+    uint32_t epoch = 0;
+    int sms = 152;
+    int max_smem = 227 * 1024;
+    bool host_only = false;
+
+    int64_t& L(int seq, int layer) { return len[(size_t)seq * cfg.num_layers + layer]; }
+    int64_t Lc(int seq, int layer) const { return len[(size_t)seq * cfg.num_layers + layer]; }
+    int32_t& T(int seq, int layer, int g) {
+        return table[((size_t)seq * cfg.num_layers + layer) * max_groups + g];
+    }
+    int32_t Tc(int seq, int layer, int g) const {
+        return table[((size_t)seq * cfg.num_layers + layer) * max_groups + g];
+    }
+};
+
+namespace {
+
+kvarn_status check_config(const kvarn_config* c) {
+    if (!c) return KVARN_EINVAL;
+    if (c->head_dim != kHeadDim || c->group_size != kGroup || c->sink_tokens != kSink) return KVARN_EINVAL;
+    if (c->num_layers <= 0 || c->max_seqs <= 0 || c->num_kv_heads <= 0 || c->num_q_heads <= 0) return KVARN_EINVAL;
+    if (c->num_q_heads % c->num_kv_heads) return KVARN_EINVAL;
+    int r = c->num_q_heads / c->num_kv_heads;
+    if (r != 1 && r != 2 && r != 4) return KVARN_EINVAL;
+    if (!bits_ok(c->k_bits) || !bits_ok(c->v_bits)) return KVARN_EINVAL;
+    if (c->sinkhorn_iters < 0 || c->sinkhorn_iters > 64) return KVARN_EINVAL;
+    if (c->max_seq_len <= 0 || c->pool_groups < 0) return KVARN_EINVAL;
+    if ((int64_t)c->max_seqs * c->num_kv_heads > (1 << 24)) return KVARN_EINVAL;
+    return KVARN_OK;
+}
+
+Layout make_layout(const kvarn_config& c, size_t* slot_bytes_out, int* max_groups_out) {
+    Layout l{};
+    int max_groups = (int)std::max<int64_t>(1, groups_sealed(c.max_seq_len));
+    size_t rk = record_bytes(c.k_bits), rv = record_bytes(c.v_bits);
+    size_t slot_bytes = align_up((size_t)c.num_kv_heads * (rk + rv), 256);
+    size_t off = 0;
+    auto take = [&](size_t n) { size_t o = off; off = align_up(off + n, 256); return o; };
+    size_t seq_layers = (size_t)c.max_seqs * c.num_layers;
+    size_t exact = seq_layers * c.num_kv_heads * kSink * kHeadDim * 2;
+    l.err = take(16);
+    l.tickets = take((size_t)c.max_seqs * c.num_kv_heads * 4);
+    l.block_table = take(seq_layers * max_groups * 4);
+    l.sink_k = take(exact);
+    l.sink_v = take(exact);
+    l.tail_k = take(exact);
+    l.tail_v = take(exact);
+    l.partials = take((size_t)c.max_seqs * c.num_kv_heads * kPartialSlots * kPartialFloats * 4);
+    l.pool = take((size_t)c.pool_groups * slot_bytes);
+    l.total = off;
+    if (slot_bytes_out) *slot_bytes_out = slot_bytes;
+    if (max_groups_out) *max_groups_out = max_groups;
+    return l;
+}
+
+kvarn_status ensure_init(kvarn_cache* c, void* stream) {
+    if (c->host_only || c->initialized) return KVARN_OK;
+    int rc = launch_init(c->base, c->lay, stream);
+    if (rc) { set_cuda_error(rc, "cache init"); return KVARN_ECUDA; }
+    c->initialized = true;
+    return KVARN_OK;
+}
+
+kvarn_status check_ids(const kvarn_cache* c, int32_t layer, int32_t n, const int32_t* ids) {
+    if (!c || layer < 0 || layer >= c->cfg.num_layers || n < 0 || (n > 0 && !ids)) return KVARN_EINVAL;
+    std::vector<char> seen(c->cfg.max_seqs, 0);
+    for (int i = 0; i < n; ++i) {
+        if (ids[i] < 0 || ids[i] >= c->cfg.max_seqs || seen[ids[i]]) return KVARN_EINVAL;
+        seen[ids[i]] = 1;
+    }
+    return KVARN_OK;
+}
+
+// Units charged for an exact item (sink + tail tokens) relative to one sealed group
+// pair: the exact tokens move 512 bytes each (K and V fp16) on the CUDA cores.
+int exact_units(const kvarn_cache* c, int n_exact) {
+    double pair = (double)(c->rec_k + c->rec_v);
+    return std::max(1, (int)std::ceil(n_exact * 512.0 / pair * 0.6));
+}
+
+int seal_units(const kvarn_cache* c) {
+    // a K + V seal costs roughly as much as this many group pairs on one SM
+    (void)c;
+    return 40;
+}
+
+// covering CTA of unit u when U units are split evenly over P CTAs
+inline int64_t covering(int64_t u, int64_t U, int64_t P) { return ((u + 1) * P + U - 1) / U - 1; }
+
+// Fill the schedule of a decode call: per sequence unit offsets, grid size.
+kvarn_status schedule(kvarn_cache* c, DecodeParams& p) {
+    int64_t U = 0;
+    int64_t max_groups = 0;
+    for (int i = 0; i < p.n_seqs; ++i) {
+        SeqEntry& e = p.seqs[i];
+        e.unit_begin = (int32_t)U;
+        int we = exact_units(c, e.n_sink + e.n_tail);
+        int ws = e.seal_group >= 0 ? seal_units(c) : 0;
+        e.w_exact = we;
+        e.w_seal = ws;
+        U += (int64_t)p.hkv * (we + ws + e.n_groups);
+        max_groups = std::max<int64_t>(max_groups, e.n_groups);
+    }
+    if (U >= (1ll << 31)) return KVARN_ECAPACITY;
+    p.units_total = U;
+    int64_t P = std::min<int64_t>(c->sms, std::max<int64_t>(1, U / 24));
+    // every block's sealed groups must fit in kMaxSpan partial slots
+    for (;;) {
+        bool ok = true;
+        for (int i = 0; i < p.n_seqs && ok; ++i) {
+            const SeqEntry& e = p.seqs[i];
+            if (e.n_groups == 0) continue;
+            for (int h = 0; h < p.hkv && ok; ++h) {
+                int64_t g0 = e.unit_begin + (int64_t)h * (e.w_exact + e.w_seal + e.n_groups) + e.w_exact + e.w_seal;
+                int64_t g1 = g0 + e.n_groups - 1;
+                if (covering(g1, U, P) - covering(g0, U, P) + 1 > kMaxSpan) ok = false;
+            }
+        }
+        if (ok) break;
+        P = std::max<int64_t>(1, P * 3 / 4);
+    }
+    p.grid = (int)P;
+    return KVARN_OK;
+}
+
+kvarn_status run_decode(kvarn_cache* c, int32_t layer, int32_t n_seqs, const int32_t* seq_ids, const void* k,
+                        const void* v, const void* q, void* out, float scale, void* stream, bool step) {
+    kvarn_status st = check_ids(c, layer, n_seqs, seq_ids);
+    if (st) return st;
+    if (n_seqs > kMaxBatch) return KVARN_ECAPACITY;
+    if (n_seqs > 0 && (!q || !out)) return KVARN_EINVAL;
+    if (step && n_seqs > 0 && (!k || !v)) return KVARN_EINVAL;
+    if (!std::isfinite(scale)) return KVARN_EINVAL;
+    if (n_seqs == 0) return KVARN_OK;
+    const kvarn_config& cfg = c->cfg;
+    // capacity checks before any state change
+    int need_slots = 0;
+    if (step) {
+        for (int i = 0; i < n_seqs; ++i) {
+            int64_t pos = c->Lc(seq_ids[i], layer);
+            if (pos + 1 > cfg.max_seq_len) return KVARN_ECAPACITY;
+            if (pos >= kSink && (pos - kSink) % kGroup == kGroup - 1) ++need_slots;
+        }
+        if ((size_t)need_slots > c->free_slots.size()) return KVARN_ECAPACITY;
+    }
+    static thread_local DecodeParams p;  // ~10 KB: keep it off the stack
+    std::memset(&p, 0, sizeof(p));
+    p.base = c->base;
+    p.lay = c->lay;
+    p.q = (const uint16_t*)q;
+    p.out = (uint16_t*)out;
+    p.k_new = step ? (const uint16_t*)k : nullptr;
+    p.v_new = step ? (const uint16_t*)v : nullptr;
+    p.n_seqs = n_seqs;
+    p.hq = cfg.num_q_heads;
+    p.hkv = cfg.num_kv_heads;
+    p.r = c->r;
+    p.k_bits = cfg.k_bits;
+    p.v_bits = cfg.v_bits;
+    p.iters = cfg.sinkhorn_iters;
+    p.layer = layer;
+    p.num_layers = cfg.num_layers;
+    p.max_seqs = cfg.max_seqs;
+    p.max_groups = c->max_groups;
+    p.rec_k = (int32_t)c->rec_k;
+    p.rec_v = (int32_t)c->rec_v;
+    p.slot_bytes = (int32_t)c->slot_bytes;
+    p.pool_slots = cfg.pool_groups;
+    p.scale_log2 = scale * 1.4426950408889634f;
+    bool any_seal = false;
+    std::vector<int32_t> taken;
+    for (int i = 0; i < n_seqs; ++i) {
+        SeqEntry& e = p.seqs[i];
+        int s = seq_ids[i];
+        int64_t n = c->Lc(s, layer);
+        e.seq = s;
+        e.new_pos = -1;
+        e.seal_group = -1;
+        e.seal_slot = -1;
+        if (step) {
+            e.new_pos = (int32_t)n;
+            if (n >= kSink && (n - kSink) % kGroup == kGroup - 1) {
+                e.seal_group = (int32_t)((n - kSink) / kGroup);
+                e.seal_slot = c->free_slots.back();
+                c->free_slots.pop_back();
+                taken.push_back(e.seal_slot);
+                any_seal = true;
+            }
+            n += 1;
+        }
+        e.n_sink = (int32_t)std::min<int64_t>(n, kSink);
+        e.n_groups = (int32_t)groups_sealed(n) - (e.seal_group >= 0 ? 1 : 0);
+        e.n_tail = n > kSink ? (int32_t)((n - kSink) % kGroup) : 0;
+    }
+    st = schedule(c, p);
+    if (st) {
+        for (int32_t s : taken) c->free_slots.push_back(s);
+        return st;
+    }
+    int pair = (int)(c->rec_k + c->rec_v);
+    int base_smem = decode_smem_bytes(cfg.k_bits, cfg.v_bits, 0, any_seal);
+    int stages = std::min(16, (c->max_smem - base_smem) / pair);
+    if (stages < 2) {
+        for (int32_t s : taken) c->free_slots.push_back(s);
+        return KVARN_ECAPACITY;
+    }
+    p.stages = stages;
+    p.epoch = ++c->epoch;
+    if (!c->host_only) {
+        st = ensure_init(c, stream);
+        if (st) return st;
+        int rc = launch_decode(p, decode_smem_bytes(cfg.k_bits, cfg.v_bits, stages, any_seal), stream);
+        if (rc) { set_cuda_error(rc, "decode launch"); return KVARN_ECUDA; }
+    }
+    if (step) {
+        for (int i = 0; i < n_seqs; ++i) {
+            const SeqEntry& e = p.seqs[i];
+            if (e.seal_group >= 0) c->T(e.seq, layer, e.seal_group) = e.seal_slot;
+            c->L(e.seq, layer) += 1;
+        }
+    }
+    return KVARN_OK;
+}
+
+}  // namespace
+
+extern "C" {
+
+size_t kvarn_record_bytes(int32_t bits) { return bits_ok(bits) ? record_bytes(bits) : 0; }
+
+kvarn_status kvarn_cache_required_bytes(const kvarn_config* cfg, size_t* bytes) {
+    kvarn_status st = check_config(cfg);
+    if (st) return st;
+    if (!bytes) return KVARN_EINVAL;
+    *bytes = make_layout(*cfg, nullptr, nullptr).total;
+    return KVARN_OK;
+}
+
+kvarn_status kvarn_cache_create(const kvarn_config* cfg, void* dev_mem, size_t bytes, kvarn_cache** out) {
+    kvarn_status st = check_config(cfg);
+    if (st) return st;
+    if (!out || !dev_mem || ((uintptr_t)dev_mem & 255)) return KVARN_EINVAL;
+    kvarn_cache* c = new (std::nothrow) kvarn_cache();
+    if (!c) return KVARN_ENOMEM;
+    c->cfg = *cfg;
+    c->lay = make_layout(*cfg, &c->slot_bytes, &c->max_groups);
+    if (bytes < c->lay.total) { delete c; return KVARN_ENOMEM; }
+    c->base = (uint8_t*)dev_mem;
+    c->bytes = bytes;
+    c->r = cfg->num_q_heads / cfg->num_kv_heads;
+    c->rec_k = record_bytes(cfg->k_bits);
+    c->rec_v = record_bytes(cfg->v_bits);
+    c->host_only = (cfg->flags & KVARN_FLAG_HOST_ONLY) != 0;
+    c->len.assign((size_t)cfg->max_seqs * cfg->num_layers, 0);
+    c->table.assign((size_t)cfg->max_seqs * cfg->num_layers * c->max_groups, -1);
+    c->free_slots.resize(cfg->pool_groups);
+    for (int i = 0; i < cfg->pool_groups; ++i) c->free_slots[i] = cfg->pool_groups - 1 - i;  // pop gives 0,1,2..
+    if (!c->host_only) {
+        c->sms = sm_count();
+        c->max_smem = max_optin_smem();
+        if (c->sms <= 0 || c->max_smem <= 0) {
+            std::snprintf(g_last_error, sizeof(g_last_error), "no CUDA device");
+            delete c;
+            return KVARN_ECUDA;
+        }
+    }
+    *out = c;
+    return KVARN_OK;
+}
+
+void kvarn_cache_destroy(kvarn_cache* cache) { delete cache; }
+
+kvarn_status kvarn_append(kvarn_cache* c, int32_t layer, int32_t n_seqs, const int32_t* seq_ids,
+                          const int32_t* n_tokens, const void* k, const void* v, void* stream) {
+    kvarn_status st = check_ids(c, layer, n_seqs, seq_ids);
+    if (st) return st;
+    if (n_seqs > kMaxBatch) return KVARN_ECAPACITY;
+    if (n_seqs > 0 && !n_tokens) return KVARN_EINVAL;
+    int64_t total = 0, new_groups = 0;
+    for (int i = 0; i < n_seqs; ++i) {
+        if (n_tokens[i] < 0) return KVARN_EINVAL;
+        int64_t n0 = c->Lc(seq_ids[i], layer), n1 = n0 + n_tokens[i];
+        if (n1 > c->cfg.max_seq_len) return KVARN_ECAPACITY;
+        total += n_tokens[i];
+        new_groups += groups_sealed(n1) - groups_sealed(n0);
+    }
+    if (total > 0 && (!k || !v)) return KVARN_EINVAL;
+    if (total >= (1ll << 31) / (c->cfg.num_kv_heads * 32)) return KVARN_ECAPACITY;
+    if ((size_t)new_groups > c->free_slots.size()) return KVARN_ECAPACITY;
+    if (total == 0) return KVARN_OK;
+    const kvarn_config& cfg = c->cfg;
+    static thread_local SealParams sp;
+    static thread_local AppendParams ap;
+    std::memset(&sp, 0, sizeof(sp));
+    std::memset(&ap, 0, sizeof(ap));
+    sp.base = ap.base = c->base;
+    sp.lay = ap.lay = c->lay;
+    sp.k_in = ap.k_in = (const uint16_t*)k;
+    sp.v_in = ap.v_in = (const uint16_t*)v;
+    sp.n_seqs = ap.n_seqs = n_seqs;
+    sp.hkv = ap.hkv = cfg.num_kv_heads;
+    sp.k_bits = cfg.k_bits;
+    sp.v_bits = cfg.v_bits;
+    sp.iters = cfg.sinkhorn_iters;
+    sp.layer = ap.layer = layer;
+    sp.num_layers = ap.num_layers = cfg.num_layers;
+    sp.max_groups = c->max_groups;
+    sp.rec_k = (int32_t)c->rec_k;
+    sp.rec_v = (int32_t)c->rec_v;
+    sp.slot_bytes = (int32_t)c->slot_bytes;
+    int64_t jobs = 0, row = 0, toks = 0;
+    for (int i = 0; i < n_seqs; ++i) {
+        int s = seq_ids[i];
+        int64_t n0 = c->Lc(s, layer), n1 = n0 + n_tokens[i];
+        int64_t g0 = groups_sealed(n0), g1 = groups_sealed(n1);
+        SealJobSeq& j = sp.seqs[i];
+        j.seq = s;
+        j.g_first = (int32_t)g0;
+        j.n_new = (int32_t)(g1 - g0);
+        j.n_before = (int32_t)n0;
+        j.in_row = (int32_t)row;
+        j.job_begin = (int32_t)jobs;
+        jobs += (g1 - g0) * cfg.num_kv_heads * 2;
+        AppendSeq& a = ap.seqs[i];
+        a.seq = s;
+        a.n_before = (int32_t)n0;
+        a.n_new = n_tokens[i];
+        a.keep_from = (int32_t)(kSink + g1 * kGroup);
+        a.in_row = (int32_t)row;
+        a.tok_begin = (int32_t)toks;
+        row += n_tokens[i];
+        toks += n_tokens[i];
+    }
+    if (jobs >= (1ll << 31)) return KVARN_ECAPACITY;
+    sp.jobs_total = (int32_t)jobs;
+    ap.tokens_total = (int32_t)toks;
+    if (!c->host_only) {
+        st = ensure_init(c, stream);
+        if (st) return st;
+    }
+    // take slots and publish the new block-table entries
+    for (int i = 0; i < n_seqs; ++i) {
+        const SealJobSeq& j = sp.seqs[i];
+        for (int g = 0; g < j.n_new; ++g) {
+            c->T(j.seq, layer, j.g_first + g) = c->free_slots.back();
+            c->free_slots.pop_back();
+        }
+        if (j.n_new && !c->host_only) {
+            size_t off = c->lay.block_table +
+                         (((size_t)j.seq * cfg.num_layers + layer) * c->max_groups + j.g_first) * 4;
+            int rc = memcpy_h2d_async(c->base + off, &c->T(j.seq, layer, j.g_first), (size_t)j.n_new * 4, stream);
+            if (rc) { set_cuda_error(rc, "block table copy"); return KVARN_ECUDA; }
+        }
+    }
+    if (!c->host_only) {
+        if (jobs > 0) {
+            int rc = launch_seal_jobs(sp, stream);
+            if (rc) { set_cuda_error(rc, "seal launch"); return KVARN_ECUDA; }
+        }
+        int rc = launch_append(ap, stream);
+        if (rc) { set_cuda_error(rc, "append launch"); return KVARN_ECUDA; }
+    }
+    for (int i = 0; i < n_seqs; ++i) c->L(seq_ids[i], layer) += n_tokens[i];
+    return KVARN_OK;
+}
+
+kvarn_status kvarn_decode_attention(kvarn_cache* c, int32_t layer, int32_t n_seqs, const int32_t* seq_ids,
+                                    const void* q, void* out, float softmax_scale, void* stream) {
+    return run_decode(c, layer, n_seqs, seq_ids, nullptr, nullptr, q, out, softmax_scale, stream, false);
+}
+
+kvarn_status kvarn_decode_step(kvarn_cache* c, int32_t layer, int32_t n_seqs, const int32_t* seq_ids,
+                               const void* k, const void* v, const void* q, void* out, float softmax_scale,
+                               void* stream) {
+    return run_decode(c, layer, n_seqs, seq_ids, k, v, q, out, softmax_scale, stream, true);
+}
+
+kvarn_status kvarn_group_record(const kvarn_cache* c, int32_t layer, int32_t seq_id, int32_t group,
+                                int32_t kv_head, int32_t which, const void** dev_ptr, size_t* bytes) {
+    if (!c || layer < 0 || layer >= c->cfg.num_layers || seq_id < 0 || seq_id >= c->cfg.max_seqs) return KVARN_EINVAL;
+    if (kv_head < 0 || kv_head >= c->cfg.num_kv_heads || (which != 0 && which != 1) || group < 0) return KVARN_EINVAL;
+    if (group >= groups_sealed(c->Lc(seq_id, layer))) return KVARN_ESTATE;
+    int32_t slot = c->Tc(seq_id, layer, group);
+    if (slot < 0) return KVARN_ESTATE;
+    size_t off = c->lay.pool + (size_t)slot * c->slot_bytes + (size_t)kv_head * (c->rec_k + c->rec_v) +
+                 (which ? c->rec_k : 0);
+    if (dev_ptr) *dev_ptr = c->base + off;
+    if (bytes) *bytes = which ? c->rec_v : c->rec_k;
+    return KVARN_OK;
+}
+
+kvarn_status kvarn_exact_regions(const kvarn_cache* c, int32_t layer, int32_t seq_id, const void** sink_k,
+                                 const void** sink_v, const void** tail_k, const void** tail_v) {
+    if (!c || layer < 0 || layer >= c->cfg.num_layers || seq_id < 0 || seq_id >= c->cfg.max_seqs) return KVARN_EINVAL;
+    size_t per = (size_t)c->cfg.num_kv_heads * kSink * kHeadDim * 2;
+    size_t off = ((size_t)seq_id * c->cfg.num_layers + layer) * per;
+    if (sink_k) *sink_k = c->base + c->lay.sink_k + off;
+    if (sink_v) *sink_v = c->base + c->lay.sink_v + off;
+    if (tail_k) *tail_k = c->base + c->lay.tail_k + off;
+    if (tail_v) *tail_v = c->base + c->lay.tail_v + off;
+    return KVARN_OK;
+}
+
+kvarn_status kvarn_dequant_group(kvarn_cache* c, int32_t layer, int32_t seq_id, int32_t group, int32_t kv_head,
+                                 int32_t which, int32_t frame, int32_t out_fp32, void* out, void* stream) {
+    const void* rec = nullptr;
+    kvarn_status st = kvarn_group_record(c, layer, seq_id, group, kv_head, which, &rec, nullptr);
+    if (st) return st;
+    if (!out || (frame != 0 && frame != 1)) return KVARN_EINVAL;
+    if (c->host_only) return KVARN_OK;
+    st = ensure_init(c, stream);
+    if (st) return st;
+    int rc = launch_dequant((const uint8_t*)rec, which ? c->cfg.v_bits : c->cfg.k_bits, which, frame, out_fp32 != 0,
+                            out, stream);
+    if (rc) { set_cuda_error(rc, "dequant launch"); return KVARN_ECUDA; }
+    return KVARN_OK;
+}
+
+kvarn_status kvarn_seq_release(kvarn_cache* c, int32_t seq_id) {
+    if (!c || seq_id < 0 || seq_id >= c->cfg.max_seqs) return KVARN_EINVAL;
+    for (int l = 0; l < c->cfg.num_layers; ++l) {
+        int64_t ng = groups_sealed(c->L(seq_id, l));
+        for (int64_t g = 0; g < ng; ++g) {
+            int32_t& s = c->T(seq_id, l, (int)g);
+            if (s >= 0) c->free_slots.push_back(s);
+            s = -1;
+        }
+        c->L(seq_id, l) = 0;
+    }
+    return KVARN_OK;
+}
+
+kvarn_status kvarn_seq_length(const kvarn_cache* c, int32_t layer, int32_t seq_id, int64_t* len) {
+    if (!c || !len || layer < 0 || layer >= c->cfg.num_layers || seq_id < 0 || seq_id >= c->cfg.max_seqs)
+        return KVARN_EINVAL;
+    *len = c->Lc(seq_id, layer);
+    return KVARN_OK;
+}
+
+kvarn_status kvarn_cache_stats(const kvarn_cache* c, kvarn_stats* o) {
+    if (!c || !o) return KVARN_EINVAL;
+    std::memset(o, 0, sizeof(*o));
+    const kvarn_config& cfg = c->cfg;
+    o->device_bytes = c->lay.total;
+    o->record_bytes_k = c->rec_k;
+    o->record_bytes_v = c->rec_v;
+    o->slot_bytes = c->slot_bytes;
+    o->pool_slots_total = cfg.pool_groups;
+    o->pool_slots_used = cfg.pool_groups - c->free_slots.size();
+    for (int s = 0; s < cfg.max_seqs; ++s)
+        for (int l = 0; l < cfg.num_layers; ++l) {
+            int64_t n = c->Lc(s, l);
+            o->tokens_cached += n;
+            o->sealed_tokens += groups_sealed(n) * kGroup;
+        }
+    o->exact_tokens = o->tokens_cached - o->sealed_tokens;
+    double elems_per_token = (double)cfg.num_kv_heads * kHeadDim;  // per side
+    o->sealed_bytes = (o->sealed_tokens / kGroup) * (uint64_t)cfg.num_kv_heads * (c->rec_k + c->rec_v);
+    o->exact_bytes = o->exact_tokens * (uint64_t)cfg.num_kv_heads * kHeadDim * 2 * 2;
+    o->body_bits_per_element = (double)(c->rec_k + c->rec_v) * 8.0 / (2.0 * kGroup * kHeadDim);
+    o->all_in_bits_per_element =
+        o->tokens_cached ? (double)(o->sealed_bytes + o->exact_bytes) * 8.0 / (o->tokens_cached * elems_per_token * 2)
+                         : 0.0;
+    return KVARN_OK;
+}
+
+kvarn_status kvarn_seal_groups(const void* x, int32_t n, int32_t bits, int32_t which, int32_t iters, void* records,
+                               float* scales, void* stream) {
+    if (n < 0 || !bits_ok(bits) || (which != 0 && which != 1) || iters < 0 || iters > 64) return KVARN_EINVAL;
+    if (n == 0) return KVARN_OK;
+    if (!x || !records || ((uintptr_t)x & 15) || ((uintptr_t)records & 15)) return KVARN_EINVAL;
+    int rc = launch_seal_groups(x, n, bits, which, iters, records, scales, stream);
+    if (rc) { set_cuda_error(rc, "seal launch"); return KVARN_ECUDA; }
+    return KVARN_OK;
+}
+
+kvarn_status kvarn_check_device_error(kvarn_cache* c, void* stream) {
+    if (!c) return KVARN_EINVAL;
+    if (c->host_only || !c->initialized) return KVARN_OK;
+    int32_t err[4] = {0, 0, 0, 0};
+    int rc = memcpy_d2h_sync(err, c->base + c->lay.err, sizeof(err), stream);
+    if (rc) { set_cuda_error(rc, "error word read"); return KVARN_ECUDA; }
+    int32_t zero[4] = {0, 0, 0, 0};
+    rc = memcpy_h2d_async(c->base + c->lay.err, zero, sizeof(zero), stream);
+    if (rc) { set_cuda_error(rc, "error word clear"); return KVARN_ECUDA; }
+    if (err[0] & kErrTimeout) return KVARN_ETIMEOUT;
+    if (err[0]) return KVARN_ESTATE;
+    return KVARN_OK;
+}
+
+const char* kvarn_status_string(kvarn_status s) {
+    switch (s) {
+        case KVARN_OK: return "ok";
+        case KVARN_EINVAL: return "invalid argument";
+        case KVARN_ENOMEM: return "device block too small";
+        case KVARN_ECAPACITY: return "capacity exceeded";
+        case KVARN_ECUDA: return "CUDA error";
+        case KVARN_ESTATE: return "invalid state";
+        case KVARN_ETIMEOUT: return "device wait timed out";
+    }
+    return "unknown status";
+}
+
+const char* kvarn_last_error(void) { return g_last_error; }
+
+}  // extern "C"

@@ -1,0 +1,144 @@
+"""CPU tests of the C ABI: the library loads, exports every entry point that
+include/kvarn.h declares, validates arguments on the host, and keeps the cache
+bookkeeping right (region rules of anbeeld.com "KVarN KV Cache: Implementation and
+Benchmarks", 2.1). No kernel is launched: caches here use KVARN_FLAG_HOST_ONLY."""
+import os
+import re
+
+import pytest
+
+from quantized_kv_cache_seal_gb300 import kvarn as K
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+FAKE = 1 << 30  # a device address that is never dereferenced in host-only mode
+
+
+def header_functions():
+    text = open(os.path.join(ROOT, "include", "kvarn.h")).read()
+    text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
+    return sorted(set(re.findall(r"\b(kvarn_[a-z_]+)\s*\(", text)))
+
+
+def test_library_exports_every_declared_function():
+    L = K.load()
+    names = header_functions()
+    assert len(names) >= 15
+    missing = [n for n in names if not hasattr(L, n)]
+    assert missing == []
+    assert sorted(K.EXPORTS) == names
+
+
+def host_cache(**kw):
+    args = dict(num_layers=2, max_seqs=4, num_q_heads=8, num_kv_heads=2, max_seq_len=2048,
+                flags=K.KVARN_FLAG_HOST_ONLY)
+    args.update(kw)
+    cfg = K.make_config(**args)
+    n = K.kvarn_cache_required_bytes(cfg)
+    return K.kvarn_cache_create(cfg, FAKE, n), cfg
+
+
+def test_status_strings_and_record_sizes():
+    assert K.kvarn_status_string(0) == "ok"
+    assert K.kvarn_status_string(3) == "capacity exceeded"
+    for b in (2, 4, 8):
+        assert K.kvarn_record_bytes(b) == 528 + 2048 * b
+    assert K.kvarn_record_bytes(3) == 0 and K.kvarn_record_bytes(16) == 0
+
+
+@pytest.mark.parametrize("field,value", [("head_dim", 64), ("group_size", 64), ("sink_tokens", 0),
+                                         ("k_bits", 3), ("v_bits", 1), ("num_q_heads", 24),
+                                         ("sinkhorn_iters", -1), ("max_seq_len", 0)])
+def test_bad_config_rejected(field, value):
+    cfg = K.make_config(flags=K.KVARN_FLAG_HOST_ONLY)
+    setattr(cfg, field, value)
+    with pytest.raises(K.KVarNError) as e:
+        K.kvarn_cache_required_bytes(cfg)
+    assert e.value.status == 1
+
+
+def test_create_checks_size_and_alignment():
+    cfg = K.make_config(max_seqs=2, max_seq_len=1024, flags=K.KVARN_FLAG_HOST_ONLY)
+    n = K.kvarn_cache_required_bytes(cfg)
+    with pytest.raises(K.KVarNError) as e:
+        K.kvarn_cache_create(cfg, FAKE, n - 1)
+    assert e.value.status == 2
+    with pytest.raises(K.KVarNError) as e:
+        K.kvarn_cache_create(cfg, FAKE + 16, n)
+    assert e.value.status == 1
+
+
+def test_seal_timing_and_regions_streaming():
+    """A group seals exactly when its 128th token arrives; tail grows 0..127."""
+    h, cfg = host_cache()
+    for n in range(1, 600):
+        K.kvarn_decode_step(h, 0, [1], FAKE, FAKE, FAKE, FAKE, 0.1)
+        assert K.kvarn_seq_length(h, 0, 1) == n
+        s = K.kvarn_cache_stats(h)
+        sealed = max(n - 128, 0) // 128
+        assert s.pool_slots_used == sealed
+        assert s.sealed_tokens == 128 * sealed
+        assert s.exact_tokens == n - 128 * sealed
+        for g in range(sealed):
+            K.kvarn_group_record(h, 0, 1, g, 0, 0)
+        with pytest.raises(K.KVarNError) as e:
+            K.kvarn_group_record(h, 0, 1, sealed, 0, 0)
+        assert e.value.status == 5
+    assert K.kvarn_seq_length(h, 1, 1) == 0  # other layer untouched
+
+
+def test_bulk_append_equals_streaming_bookkeeping():
+    h, _ = host_cache()
+    K.kvarn_append(h, 0, [0, 2], [700, 129], FAKE, FAKE)
+    assert K.kvarn_seq_length(h, 0, 0) == 700 and K.kvarn_seq_length(h, 0, 2) == 129
+    s = K.kvarn_cache_stats(h)
+    assert s.pool_slots_used == (700 - 128) // 128 + (129 - 128) // 128
+    K.kvarn_seq_release(h, 0)
+    assert K.kvarn_seq_length(h, 0, 0) == 0
+    assert K.kvarn_cache_stats(h).pool_slots_used == 0
+
+
+def test_capacity_errors_leave_state_unchanged():
+    h, _ = host_cache(pool_groups=3, max_seq_len=1024)
+    K.kvarn_append(h, 0, [0], [128 + 2 * 128], FAKE, FAKE)
+    before = (K.kvarn_seq_length(h, 0, 0), K.kvarn_cache_stats(h).pool_slots_used)
+    with pytest.raises(K.KVarNError) as e:       # needs 2 more slots, 1 left
+        K.kvarn_append(h, 0, [0], [256], FAKE, FAKE)
+    assert e.value.status == 3
+    with pytest.raises(K.KVarNError) as e:       # longer than max_seq_len
+        K.kvarn_append(h, 0, [1], [1025], FAKE, FAKE)
+    assert e.value.status == 3
+    assert (K.kvarn_seq_length(h, 0, 0), K.kvarn_cache_stats(h).pool_slots_used) == before
+    # a decode step that would need a slot when none is left
+    K.kvarn_append(h, 0, [1], [128 + 127], FAKE, FAKE)      # takes the last slot? no: 0 sealed
+    K.kvarn_append(h, 1, [1], [128 + 128], FAKE, FAKE)      # takes the third slot
+    assert K.kvarn_cache_stats(h).pool_slots_used == 3
+    with pytest.raises(K.KVarNError) as e:
+        K.kvarn_decode_step(h, 0, [1], FAKE, FAKE, FAKE, FAKE, 0.1)
+    assert e.value.status == 3
+    assert K.kvarn_seq_length(h, 0, 1) == 255
+
+
+def test_argument_validation():
+    h, _ = host_cache()
+    for args in ([h, 2, [0], [1], FAKE, FAKE], [h, 0, [4], [1], FAKE, FAKE], [h, 0, [0, 0], [1, 1], FAKE, FAKE],
+                 [h, 0, [0], [-1], FAKE, FAKE], [h, 0, [0], [5], 0, FAKE]):
+        with pytest.raises(K.KVarNError) as e:
+            K.kvarn_append(*args)
+        assert e.value.status == 1
+    with pytest.raises(K.KVarNError):
+        K.kvarn_decode_attention(h, 0, [0], FAKE, FAKE, float("nan"))
+    with pytest.raises(K.KVarNError):
+        K.kvarn_seq_length(h, 0, 9)
+
+
+def test_bits_per_element_formula():
+    """Body bits/element = b + 528*8/16384 per side (fig1.dev: about 2.3 at two bits)."""
+    for kb, vb in [(2, 2), (4, 2), (4, 4), (8, 8)]:
+        h, _ = host_cache(k_bits=kb, v_bits=vb)
+        s = K.kvarn_cache_stats(h)
+        assert abs(s.body_bits_per_element - ((kb + vb) / 2 + 528 * 8 / 16384)) < 1e-12
+        K.kvarn_append(h, 0, [0], [128 + 128 * 10], FAKE, FAKE)
+        s = K.kvarn_cache_stats(h)
+        elems = (128 + 1280) * 2 * 128 * 2
+        expect = (10 * 2 * (K.kvarn_record_bytes(kb) + K.kvarn_record_bytes(vb)) + 128 * 2 * 128 * 2 * 2) * 8 / elems
+        assert abs(s.all_in_bits_per_element - expect) < 1e-9
