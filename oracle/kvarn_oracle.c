@@ -114,17 +114,22 @@ void kvo_hadamard(int d, double* H) {
         }
 }
 
-/* Y = X * H for X of T rows and d columns (each token row rotated). */
+/* Y = X * H for X of T rows and d columns (each token row rotated). The sum runs
+ * over the +-1 entries of the Sylvester matrix and the result is divided by sqrt(d)
+ * once: for fp16 inputs every partial sum is exact in binary64 (fp16 values are
+ * multiples of 2^-24 below 2^16, so 128 of them need at most 47 significant bits),
+ * hence Y is exact up to that single division and zero stays zero. */
 void kvo_rotate(const double* X, int T, int d, double* Y) {
-    double* H = (double*)malloc(sizeof(double) * (size_t)d * d);
-    kvo_hadamard(d, H);
+    double s = sqrt((double)d);
     for (int i = 0; i < T; ++i)
         for (int j = 0; j < d; ++j) {
             double acc = 0.0;
-            for (int k = 0; k < d; ++k) acc += X[(size_t)i * d + k] * H[(size_t)k * d + j];
-            Y[(size_t)i * d + j] = acc;
+            for (int k = 0; k < d; ++k) {
+                int neg = __builtin_popcount((unsigned)(k & j)) & 1;
+                acc += neg ? -X[(size_t)i * d + k] : X[(size_t)i * d + k];
+            }
+            Y[(size_t)i * d + j] = acc / s;
         }
-    free(H);
 }
 
 /* ------------------------------------------------------------------------- */
@@ -393,8 +398,6 @@ int kvo_attention(int d, int T, int r, int kbits, int vbits, const uint16_t* q, 
     size_t kb = kvo_record_bytes(T, d, kbits), vb = kvo_record_bytes(T, d, vbits);
     size_t ns = (size_t)n_groups * T;
     int n_all = n_sink + (int)ns + n_tail;
-    double* H = (double*)malloc(sizeof(double) * (size_t)d * d);
-    kvo_hadamard(d, H);
     double* YK = (double*)malloc(sizeof(double) * (ns ? ns : 1) * d);
     double* YV = (double*)malloc(sizeof(double) * (ns ? ns : 1) * d);
     for (int g = 0; g < n_groups; ++g) {
@@ -406,13 +409,10 @@ int kvo_attention(int d, int T, int r, int kbits, int vbits, const uint16_t* q, 
     double* qr = (double*)malloc(sizeof(double) * d);
     double* oe = (double*)malloc(sizeof(double) * d);
     double* orot = (double*)malloc(sizeof(double) * d);
+    double* ob = (double*)malloc(sizeof(double) * d);
     for (int h = 0; h < r; ++h) {
         for (int j = 0; j < d; ++j) qd[j] = kvo_half_to_double(q[(size_t)h * d + j]);
-        for (int j = 0; j < d; ++j) {
-            double acc = 0.0;
-            for (int k = 0; k < d; ++k) acc += qd[k] * H[(size_t)k * d + j];
-            qr[j] = acc;
-        }
+        kvo_rotate(qd, 1, d, qr);
         int t = 0;
         for (int i = 0; i < n_sink; ++i, ++t) {
             double acc = 0.0;
@@ -441,13 +441,10 @@ int kvo_attention(int d, int T, int r, int kbits, int vbits, const uint16_t* q, 
             for (int j = 0; j < d; ++j) orot[j] += s[t] * YV[i * d + j];
         for (int i = 0; i < n_tail; ++i, ++t)
             for (int j = 0; j < d; ++j) oe[j] += s[t] * kvo_half_to_double(tail_v[(size_t)i * d + j]);
-        for (int j = 0; j < d; ++j) {
-            double acc = 0.0;
-            for (int k = 0; k < d; ++k) acc += orot[k] * H[(size_t)k * d + j];
-            out[(size_t)h * d + j] = n_all ? (oe[j] + acc) / l : 0.0;
-        }
+        kvo_rotate(orot, 1, d, ob);
+        for (int j = 0; j < d; ++j) out[(size_t)h * d + j] = n_all ? (oe[j] + ob[j]) / l : 0.0;
         if (lse) lse[h] = n_all ? mx + log(l) : -INFINITY;
     }
-    free(H); free(YK); free(YV); free(s); free(qd); free(qr); free(oe); free(orot);
+    free(YK); free(YV); free(s); free(qd); free(qr); free(oe); free(orot); free(ob);
     return 0;
 }

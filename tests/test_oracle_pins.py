@@ -383,3 +383,20 @@ def test_streaming_append_equals_bulk_append():
     for g in range(2):
         assert np.array_equal(a.seqs[0]["krec"][g], b.seqs[0]["krec"][g])
         assert np.array_equal(a.seqs[0]["vrec"][g], b.seqs[0]["vrec"][g])
+
+
+def test_rotation_of_fp16_rows_is_exact_before_the_scaling():
+    """fp16 inputs are integers times 2^-24, so X * (+-1 Sylvester matrix) is an exact
+    integer sum (Python ints here); the oracle's Y must equal that sum divided by
+    sqrt(128) with a single rounding, and exact zeros (a constant row) stay zero."""
+    x = workloads.tiny_matrix(21, 3, 128, 300.0)
+    x[2] = np.float16(1.5)
+    ints = (x.astype(np.float64) * 2.0 ** 24).astype(np.int64)
+    S = scipy.linalg.hadamard(128).astype(np.int64)
+    exact = [[int(sum(int(ints[i, k]) * int(S[k, j]) for k in range(128))) for j in range(128)] for i in range(3)]
+    Y = oracle.rotate(x.astype(np.float64))
+    for i in range(3):
+        for j in range(128):
+            ref = exact[i][j] * 2.0 ** -24 / math.sqrt(128)
+            assert abs(Y[i, j] - ref) <= abs(ref) * 2.0 ** -52
+    assert np.count_nonzero(Y[2]) == 1
