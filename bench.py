@@ -1,0 +1,504 @@
+"""KVarN decode-step benchmark on GB300.
+
+One step = one pass of the whole hot path for every sequence of the batch: append the
+new token's K/V, seal the group it completes (Hadamard rotation, 16 Sinkhorn
+iterations, rounding, packing), rotate the query, attend over sink + sealed records +
+tail, merge the split partials and rotate the output back -- one kvarn_decode_step
+call (one kernel launch).
+
+Workload (default): Llama-3.1-8B attention shape -- 32 query heads, 8 KV heads,
+head_dim 128 -- batch 16, context 32768 + U{0..127} tail tokens per sequence, 2-bit K
+and V. Synthetic data (seeded), generated on the device.
+
+  python bench.py [--gpus N] [--steps K] [--warmup W] [--impl reference]
+
+Prints one JSON line (rank 0). Under torchrun each rank runs its own replica of the
+workload on its GPU (weak scaling; the path has no exchange step).
+"""
+from __future__ import annotations
+
+import argparse
+import json
+import math
+import os
+import statistics
+import subprocess
+import sys
+import threading
+import time
+
+import numpy as np
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+METRIC = "KVarN decode-attn tokens/s, achieved HBM GB/s (% roofline); seal groups/s"
+WORKLOAD = "llama31_8b_gqa32x8_b16_ctx32k_k2v2"
+HQ, HKV, BATCH, KB, VB, SEED = 32, 8, 16, 2, 2, 2
+
+
+def c3_lengths():
+    from quantized_kv_cache_seal_gb300 import workloads
+    return list(workloads.workloads()["c3_llama31_8b_32k"].context)
+
+
+def rec_bytes(b):
+    return 528 + 2048 * b
+
+
+def step_bytes(lengths):
+    """Algorithmic HBM bytes of one decode step at the given lengths (before the step):
+    sealed records read + exact fp16 K/V read + q read + out written + new token written,
+    plus, for a sequence whose token completes a group, the 127 tail tokens read and the
+    new records written and read."""
+    pair = rec_bytes(KB) + rec_bytes(VB)
+    total = 0
+    for n in lengths:
+        n1 = n + 1
+        sealing = n >= 128 and (n - 128) % 128 == 127
+        groups = max(n1 - 128, 0) // 128 - (1 if sealing else 0)
+        n_sink = min(n1, 128)
+        n_tail = max(n1 - 128, 0) % 128
+        total += HKV * (groups * pair + (n_sink + n_tail) * 512)
+        total += HQ * 256 * 2 + HKV * 512
+        if sealing:
+            total += HKV * (127 * 512 + 2 * pair)
+    return total
+
+
+def sealing_count(lengths):
+    return sum(1 for n in lengths if n >= 128 and (n - 128) % 128 == 127)
+
+
+class ClockSampler:
+    """nvidia-smi sampling of SM clocks and throttle reasons during the timed region."""
+
+    FIELDS = ("clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, index: int):
+        self.index = index
+        self.proc = None
+        self.lines = []
+
+    def start(self):
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", f"--query-gpu={self.FIELDS}", "--format=csv,noheader,nounits", "-lms", "50",
+                 "-i", str(self.index)], stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+            self.reader = threading.Thread(target=self._read, daemon=True)
+            self.reader.start()
+        except OSError:
+            self.proc = None
+
+    def _read(self):
+        for line in self.proc.stdout:
+            self.lines.append((time.time(), line.strip()))
+
+    def stop(self):
+        if self.proc is not None:
+            self.proc.terminate()
+            try:
+                self.proc.wait(timeout=5)
+            except subprocess.TimeoutExpired:
+                self.proc.kill()
+
+    def summary(self, t0, t1):
+        sm, mx, reasons = [], None, set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for ts, line in self.lines:
+            parts = [p.strip() for p in line.split(",")]
+            if len(parts) < 8:
+                continue
+            try:
+                mx = float(parts[1])
+                if t0 - 0.05 <= ts <= t1 + 0.05:
+                    sm.append(float(parts[0]))
+                    for name, val in zip(names, parts[4:8]):
+                        if val.lower().startswith("active"):
+                            reasons.add(name)
+            except ValueError:
+                continue
+        return {"sm_mhz": statistics.median(sm) if sm else None, "sm_max_mhz": mx, "reasons": sorted(reasons),
+                "samples": len(sm)}
+
+
+def measured_hbm_peak():
+    try:
+        with open(os.path.join(ROOT, "MEASURED_PEAKS.json")) as fh:
+            return float(json.load(fh)["hbm_gbs"]), "measured"
+    except (OSError, KeyError, ValueError):
+        return 6800.0, "fallback"
+
+
+def dist_info():
+    rank = int(os.environ.get("RANK", "0"))
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    return rank, world, local
+
+
+def build_cache(torch, device, extra):
+    from quantized_kv_cache_seal_gb300 import workloads
+    from quantized_kv_cache_seal_gb300.cache import KVarNCache
+
+    lengths = c3_lengths()
+    cache = KVarNCache(num_layers=1, max_seqs=BATCH, num_q_heads=HQ, num_kv_heads=HKV, k_bits=KB, v_bits=VB,
+                       max_seq_len=max(lengths) + extra, device=device)
+    ids = list(range(BATCH))
+    chunk = 4096
+    done = [0] * BATCH
+    while any(d < n for d, n in zip(done, lengths)):
+        ks, vs, counts = [], [], []
+        for i, n in enumerate(lengths):
+            c = min(chunk, n - done[i])
+            counts.append(c)
+            if c > 0:
+                k, v = workloads.torch_tokens(SEED, i, done[i], c, HKV, device=device)
+                ks.append(k)
+                vs.append(v)
+        cache.append(0, ids, counts, torch.cat(ks), torch.cat(vs))
+        done = [d + c for d, c in zip(done, counts)]
+    torch.cuda.synchronize()
+    torch.cuda.empty_cache()
+    return cache, ids, lengths
+
+
+def run_ours(args):
+    import torch
+
+    from quantized_kv_cache_seal_gb300 import kvarn as K
+    from quantized_kv_cache_seal_gb300 import workloads
+
+    rank, world, local = dist_info()
+    torch.cuda.set_device(local)
+    device = torch.device("cuda", local)
+    pg = None
+    if world > 1:
+        import torch.distributed as dist
+        dist.init_process_group("nccl" if torch.cuda.is_available() else "gloo")
+        pg = dist
+    K_, W = args.steps, args.warmup
+    reps_max = max(3, min(args.reps, 8192 // max(K_, 1)))
+    total_steps = W + K_ * (reps_max + 2) + 8
+    cache, ids, lengths = build_cache(torch, device, total_steps + 256)
+    q_all = workloads.torch_queries(SEED + 100 * rank, total_steps, BATCH, HQ, device=device)
+    kn_all, vn_all = [], []
+    for i in range(BATCH):
+        k, v = workloads.torch_tokens(SEED, i, lengths[i], total_steps, HKV, device=device)
+        kn_all.append(k)
+        vn_all.append(v)
+    kn_all = torch.stack(kn_all, 1).contiguous()  # [steps][B][Hkv][d]
+    vn_all = torch.stack(vn_all, 1).contiguous()
+    out = torch.empty((BATCH, HQ, 128), dtype=torch.float16, device=device)
+    stream = torch.cuda.current_stream()
+    scale = 1.0 / math.sqrt(128)
+    h = cache.handle
+    sp = stream.cuda_stream
+    cur = [0]
+    lens = list(lengths)
+
+    def step():
+        s = cur[0]
+        K.kvarn_decode_step(h, 0, ids, kn_all[s], vn_all[s], q_all[s], out, scale, sp)
+        cur[0] += 1
+
+    def lens_at(s):
+        return [n + s for n in lengths]
+
+    for _ in range(W):
+        step()
+    torch.cuda.synchronize()
+
+    def barrier():
+        if pg is not None:
+            pg.barrier()
+        torch.cuda.synchronize()
+
+    sampler = ClockSampler(local)
+    sampler.start()
+    time.sleep(0.3)
+    rep_ms, rep_bytes = [], []
+    ev0 = torch.cuda.Event(enable_timing=True)
+    ev1 = torch.cuda.Event(enable_timing=True)
+    t_begin = time.time()
+    rep = 0
+    while True:
+        start = cur[0]
+        bytes_rep = sum(step_bytes(lens_at(s)) for s in range(start, start + K_))
+        barrier()
+        ev0.record(stream)
+        for _ in range(K_):
+            step()
+        ev1.record(stream)
+        barrier()
+        rep_ms.append(ev0.elapsed_time(ev1))
+        rep_bytes.append(bytes_rep)
+        rep += 1
+        if rep >= reps_max or (rep >= 3 and time.time() - t_begin > args.min_seconds):
+            break
+    t_end = time.time()
+    sampler.stop()
+    clocks = sampler.summary(t_begin, t_end)
+    err = cache.check_device_error()
+    if err != 0:
+        raise RuntimeError(f"device error word: {err}")
+    order = sorted(range(len(rep_ms)), key=lambda i: rep_ms[i])
+    mid = order[len(order) // 2]
+    ms = rep_ms[mid]
+    if pg is not None:
+        t = torch.tensor([ms], dtype=torch.float64, device=device)
+        pg.all_reduce(t, op=pg.ReduceOp.MAX)
+        ms = float(t.item())
+    ms_per_step = ms / K_
+    value = BATCH * world * K_ / (ms / 1e3)
+    launch_us = ms_per_step * 1e3
+    alg_bytes = rep_bytes[mid] / K_
+    achieved = alg_bytes / (launch_us * 1e-6) / 1e9
+    peak, peak_kind = measured_hbm_peak()
+
+    # seal share: per-step events over K steps; steps that seal vs steps that do not
+    evs = [torch.cuda.Event(enable_timing=True) for _ in range(K_ + 1)]
+    seal_flags = []
+    barrier()
+    evs[0].record(stream)
+    for k in range(K_):
+        seal_flags.append(sealing_count(lens_at(cur[0])) > 0)
+        step()
+        evs[k + 1].record(stream)
+    barrier()
+    per = [evs[k].elapsed_time(evs[k + 1]) for k in range(K_)]
+    plain = [t for t, f in zip(per, seal_flags) if not f]
+    seal_share = None
+    if plain and any(seal_flags):
+        base = statistics.median(plain)
+        seal_share = max(0.0, (sum(per) - base * len(per)) / sum(per))
+
+    # end to end through the C ABI with host buffers: H2D inputs, step, D2H output
+    e2e = None
+    if not args.no_e2e:
+        hk = kn_all[cur[0]:cur[0] + K_].cpu().pin_memory()
+        hv = vn_all[cur[0]:cur[0] + K_].cpu().pin_memory()
+        hq = q_all[cur[0]:cur[0] + K_].cpu().pin_memory()
+        hout = torch.empty((K_, BATCH, HQ, 128), dtype=torch.float16).pin_memory()
+        dk = torch.empty_like(kn_all[0])
+        dv = torch.empty_like(vn_all[0])
+        dq = torch.empty_like(q_all[0])
+        barrier()
+        e0 = torch.cuda.Event(enable_timing=True)
+        e1 = torch.cuda.Event(enable_timing=True)
+        e0.record(stream)
+        for k in range(K_):
+            dk.copy_(hk[k], non_blocking=True)
+            dv.copy_(hv[k], non_blocking=True)
+            dq.copy_(hq[k], non_blocking=True)
+            K.kvarn_decode_step(h, 0, ids, dk, dv, dq, out, scale, sp)
+            hout[k].copy_(out, non_blocking=True)
+            cur[0] += 1
+        e1.record(stream)
+        barrier()
+        ems = e0.elapsed_time(e1)
+        if pg is not None:
+            t = torch.tensor([ems], dtype=torch.float64, device=device)
+            pg.all_reduce(t, op=pg.ReduceOp.MAX)
+            ems = float(t.item())
+        e2e = {"value": BATCH * world * K_ / (ems / 1e3), "unit": "tokens/s",
+               "h2d_bytes_per_step": int(dk.numel() * 2 + dv.numel() * 2 + dq.numel() * 2),
+               "d2h_bytes_per_step": int(out.numel() * 2)}
+
+    # bulk seal throughput (kvarn_seal_groups on 16384 group matrices, 512 MiB in)
+    seal_gps = None
+    if not args.no_seal:
+        from quantized_kv_cache_seal_gb300.cache import seal_groups
+        n = 16384
+        x, _ = workloads.torch_tokens(SEED + 7, 99, 0, n * 128 // HKV, HKV, device=device)
+        x = x.view(n, 128, 128)
+        seal_groups(x[:256], 2, 0)
+        barrier()
+        s0 = torch.cuda.Event(enable_timing=True)
+        s1 = torch.cuda.Event(enable_timing=True)
+        s0.record(stream)
+        seal_groups(x, 2, 0)
+        s1.record(stream)
+        barrier()
+        seal_gps = n / (s0.elapsed_time(s1) / 1e3) * world
+        del x
+
+    result = {
+        "metric": METRIC, "value": value, "unit": "tokens/s", "n_gpus": world, "steps": K_, "warmup": W,
+        "ms_per_step": ms_per_step, "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
+        "dtype": "f16 mma / f32 accum on 2-bit codes", "data": "synthetic",
+        "config": {"workload": WORKLOAD, "global_batch": BATCH * world, "seq_len": int(statistics.mean(lengths)),
+                   "num_q_heads": HQ, "num_kv_heads": HKV, "head_dim": 128, "k_bits": KB, "v_bits": VB,
+                   "parallelism": f"replicas{world}", "l2": "working set ~315 MB per step > 129 MB L2 (no flush)",
+                   "reps": len(rep_ms), "rep_ms": [round(x, 4) for x in rep_ms]},
+        "gpu_launches": K_,
+        "roofline": {"bound": "hbm", "achieved": achieved, "peak": peak, "unit": "GB/s", "frac": achieved / peak,
+                     "traffic": args.traffic, "peak_kind": peak_kind, "kernel": "decode_kernel<2,2>",
+                     "alg_bytes_per_launch": alg_bytes, "launch_us": launch_us},
+        "seal_groups_per_s": seal_gps,
+        "seal_share": seal_share,
+        "clocks": clocks,
+        "e2e": e2e,
+    }
+    if rank == 0 and world == 1 and not args.no_cpu_baseline:
+        result["cpu_baseline"] = cpu_baseline(cache, lengths, cur[0], q_all, args.cpu_pairs)
+    if pg is not None:
+        pg.destroy_process_group()
+    cache.close()
+    if rank == 0:
+        print(json.dumps(result), flush=True)
+
+
+def _oracle_step_sample(cache, q_np, pairs):
+    """Time the oracle's attention for the given (seq, kv head) pairs on host threads."""
+    import concurrent.futures
+
+    import oracle
+
+    jobs = []
+    mem = cache.mem.cpu().numpy()
+    base = cache.mem.data_ptr()
+    from quantized_kv_cache_seal_gb300 import kvarn as K
+    for (s, h) in pairs:
+        n = cache.length(0, s)
+        ng = max(n - 128, 0) // 128
+        nt = max(n - 128, 0) % 128
+        kr = np.stack([mem[(p - base):(p - base) + nb] for p, nb in
+                       (K.kvarn_group_record(cache.handle, 0, s, g, h, 0) for g in range(ng))])
+        vr = np.stack([mem[(p - base):(p - base) + nb] for p, nb in
+                       (K.kvarn_group_record(cache.handle, 0, s, g, h, 1) for g in range(ng))])
+        sk, sv, tk, tv = [mem[(p - base):(p - base) + HKV * 128 * 128 * 2].view(np.float16).reshape(HKV, 128, 128)
+                          for p in K.kvarn_exact_regions(cache.handle, 0, s)]
+        r = HQ // HKV
+        jobs.append((q_np[s, h * r:(h + 1) * r], sk[h], sv[h], kr, vr, tk[h, :nt], tv[h, :nt]))
+    cores = os.cpu_count() or 1
+
+    def one(j):
+        q, sk, sv, kr, vr, tk, tv = j
+        return oracle.attention(q, 1.0 / math.sqrt(128), sk, sv, kr, vr, tk, tv, KB, VB)
+
+    t0 = time.perf_counter()
+    with concurrent.futures.ThreadPoolExecutor(max_workers=min(cores, len(jobs))) as ex:
+        list(ex.map(one, jobs))
+    return time.perf_counter() - t0, min(cores, len(jobs))
+
+
+def cpu_baseline(cache, lengths, s_now, q_all, n_pairs):
+    """The oracle timed on this host's cores on a bounded sample of the same workload:
+    decode attention for n_pairs (sequence, KV head) pairs of the current cache state."""
+    import oracle
+
+    oracle.build()
+    q_np = q_all[s_now - 1].cpu().numpy()
+    pairs = [(i % BATCH, (i * 3) % HKV) for i in range(n_pairs)]
+    t, used = _oracle_step_sample(cache, q_np, pairs)
+    step_s = t * (BATCH * HKV) / len(pairs)
+    # oracle seal throughput on 2 * cores group matrices
+    from quantized_kv_cache_seal_gb300 import workloads
+    import concurrent.futures
+    cores = os.cpu_count() or 1
+    xs = workloads.group_matrices(SEED + 11, 2 * cores)
+    t0 = time.perf_counter()
+    with concurrent.futures.ThreadPoolExecutor(max_workers=cores) as ex:
+        list(ex.map(lambda x: oracle.seal(x, KB, 0), list(xs)))
+    seal_gps = len(xs) / (time.perf_counter() - t0)
+    return {"value": BATCH / step_s, "unit": "tokens/s", "cores": used, "kind": "oracle",
+            "sample": f"decode attention of {len(pairs)} of {BATCH * HKV} (sequence, KV head) pairs at ~32k "
+                      f"context over the cache's records, scaled to the whole step; seal: {len(xs)} group matrices",
+            "seal_groups_per_s": seal_gps}
+
+
+def run_reference(args):
+    """The oracle (plain fp64 C) on the host cores: each step appends one token to a
+    sample of (sequence, KV head) pairs of the workload (sealing when a group fills),
+    then attends, one pair per core; scaled to the whole batch."""
+    import concurrent.futures
+
+    import oracle
+    from quantized_kv_cache_seal_gb300 import workloads
+
+    rank, world, local = dist_info()
+    if rank != 0:
+        return
+    oracle.build()
+    cores = os.cpu_count() or 1
+    n_pairs = max(1, min(cores, args.ref_pairs))
+    lengths = c3_lengths()
+    pairs = [(i % BATCH, (i * 3) % HKV) for i in range(n_pairs)]
+    caches, srcs = [], []
+    setup0 = time.perf_counter()
+
+    def setup(pair):
+        s, h = pair
+        src = workloads.TokenSource(SEED, s, HKV)
+        oc = oracle.OracleCache(1, KB, VB)
+        k, v = src.tokens(0, lengths[s])
+        oc.append(0, k[:, h:h + 1], v[:, h:h + 1])
+        return oc, src
+
+    with concurrent.futures.ThreadPoolExecutor(max_workers=n_pairs) as ex:
+        res = list(ex.map(setup, pairs))
+    caches = [r[0] for r in res]
+    srcs = [r[1] for r in res]
+    setup_s = time.perf_counter() - setup0
+    r = HQ // HKV
+    scale = 1.0 / math.sqrt(128)
+
+    def one_step(idx, step):
+        s, h = pairs[idx]
+        pos = lengths[s] + step
+        k, v = srcs[idx].tokens(pos, 1)
+        caches[idx].append(0, k[:, h:h + 1], v[:, h:h + 1])
+        q = workloads.queries(SEED, step, BATCH, HQ)[s, h * r:(h + 1) * r]
+        caches[idx].attend(0, q, scale)
+
+    times = []
+    with concurrent.futures.ThreadPoolExecutor(max_workers=n_pairs) as ex:
+        for step in range(args.warmup + args.steps):
+            t0 = time.perf_counter()
+            list(ex.map(lambda i: one_step(i, step), range(n_pairs)))
+            if step >= args.warmup:
+                times.append(time.perf_counter() - t0)
+    per_step = statistics.mean(times) * (BATCH * HKV) / n_pairs
+    value = BATCH / per_step
+    line = {"impl": "reference", "metric": METRIC, "value": value, "unit": "tokens/s", "n_gpus": world,
+            "steps": args.steps, "warmup": args.warmup, "ms_per_step": per_step * 1e3, "higher_is_better": True,
+            "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+            "config": {"workload": WORKLOAD, "global_batch": BATCH, "seq_len": int(statistics.mean(lengths)),
+                       "num_q_heads": HQ, "num_kv_heads": HKV, "head_dim": 128, "k_bits": KB, "v_bits": VB,
+                       "parallelism": "host threads", "setup_s": setup_s},
+            "cpu_baseline": {"value": value, "unit": "tokens/s", "cores": n_pairs, "kind": "oracle",
+                             "sample": f"{n_pairs} of {BATCH * HKV} (sequence, KV head) pairs per step, "
+                                       f"append + seal + attention, scaled to the whole batch"},
+            "e2e": {"value": value, "unit": "tokens/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
+    print(json.dumps(line), flush=True)
+
+
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=256)
+    ap.add_argument("--warmup", type=int, default=8)
+    ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
+    ap.add_argument("--reps", type=int, default=20, help="timed repetitions of K steps (median reported)")
+    ap.add_argument("--min-seconds", type=float, default=1.0)
+    ap.add_argument("--no-e2e", action="store_true")
+    ap.add_argument("--no-seal", action="store_true")
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--cpu-pairs", type=int, default=32)
+    ap.add_argument("--ref-pairs", type=int, default=16)
+    ap.add_argument("--traffic", type=float, default=None,
+                    help="ncu dram bytes per launch of the decode kernel, if captured for this build")
+    args = ap.parse_args()
+    if args.warmup < 3:
+        args.warmup = 3
+    if args.impl == "reference":
+        run_reference(args)
+    else:
+        run_ours(args)
+
+
+if __name__ == "__main__":
+    main()

@@ -198,33 +198,59 @@ __device__ int expected_partials(const DecodeParams& p, const SeqEntry& e, int k
 }
 
 // Last CTA of a block: merge every partial of this call, rotate back, write out.
+// The partial headers are read in one parallel round (one thread per slot); the
+// accumulators of the valid slots are then read with independent loads.
 __device__ void final_merge(const DecodeParams& p, const Smem& sm, int ci, int kvh) {
     const int t = threadIdx.x;
     const SeqEntry& e = p.seqs[ci];
     const int blk = e.seq * p.hkv + kvh;
+    float* hdr = sm.mrg + 1536;           // [kPartialSlots][8]: m[4], l[4]
+    int* list = reinterpret_cast<int*>(sm.mrg + 1536 + 8 * kPartialSlots);  // [kPartialSlots + 1]
+    bool valid = false;
+    if (t < kPartialSlots) {
+        const float* P = partial_ptr(p, blk, t);
+        valid = (uint32_t)__float_as_int(__ldcg(P)) == p.epoch;
+        const float4 m4 = __ldcg(reinterpret_cast<const float4*>(P + 4));
+        const float4 l4 = __ldcg(reinterpret_cast<const float4*>(P + 8));
+        float* H = hdr + 8 * t;
+        H[0] = valid ? m4.x : kNegInf; H[1] = valid ? m4.y : kNegInf;
+        H[2] = valid ? m4.z : kNegInf; H[3] = valid ? m4.w : kNegInf;
+        H[4] = l4.x; H[5] = l4.y; H[6] = l4.z; H[7] = l4.w;
+    }
+    if (t < 32) {  // warp 0 lists the valid slots among 0..31
+        const unsigned vm = __ballot_sync(0xffffffffu, valid);
+        if (t == 0) {
+            int n = 0;
+            for (int k = 0; k < 32; ++k)
+                if (vm >> k & 1) list[1 + n++] = k;
+            list[0] = n;
+        }
+    }
+    named_bar(1, kConsumers);
+    if (t >= 32 && t < kPartialSlots && valid) {  // slots beyond the first warp (rare)
+        const int k = atomicAdd(&list[0], 1);
+        list[1 + k] = t;
+    }
+    named_bar(1, kConsumers);
+    const int nv = list[0];
     const int h = t >> 6, jj = 2 * (t & 63);
     float M = kNegInf;
-    for (int s = 0; s < kPartialSlots; ++s) {
-        const float* P = partial_ptr(p, blk, s);
-        if ((uint32_t)__float_as_int(__ldcg(P)) != p.epoch) continue;
-        M = fmaxf(M, __ldcg(P + 4 + h));
-    }
+    for (int k = 0; k < nv; ++k) M = fmaxf(M, hdr[8 * list[1 + k] + h]);
     float l = 0.f, r0 = 0.f, r1 = 0.f, x0 = 0.f, x1 = 0.f;
     if (M != kNegInf) {
-        for (int s = 0; s < kPartialSlots; ++s) {
-            const float* P = partial_ptr(p, blk, s);
-            if ((uint32_t)__float_as_int(__ldcg(P)) != p.epoch) continue;
-            const float ms = __ldcg(P + 4 + h);
-            if (ms == kNegInf) continue;
-            const float w = exp2f(ms - M);
-            l += w * __ldcg(P + 8 + h);
-            const float2 a = __ldcg(reinterpret_cast<const float2*>(P + 12 + 128 * h + jj));
-            if (s == kSlotExact) {
-                x0 += w * a.x;
-                x1 += w * a.y;
+#pragma unroll 4
+        for (int k = 0; k < nv; ++k) {
+            const int sl = list[1 + k];
+            const float ms = hdr[8 * sl + h];
+            const float w = ms == kNegInf ? 0.f : exp2f(ms - M);
+            const float2 a = __ldcg(reinterpret_cast<const float2*>(partial_ptr(p, blk, sl) + 12 + 128 * h + jj));
+            l = fmaf(w, hdr[8 * sl + 4 + h], l);
+            if (sl == kSlotExact) {
+                x0 = fmaf(w, a.x, x0);
+                x1 = fmaf(w, a.y, x1);
             } else {
-                r0 += w * a.x;
-                r1 += w * a.y;
+                r0 = fmaf(w, a.x, r0);
+                r1 = fmaf(w, a.y, r1);
             }
         }
     }
@@ -278,9 +304,12 @@ __device__ void publish(const DecodeParams& p, const Smem& sm, int ci, int kvh) 
 }
 
 // Exact part (sink + tail) of one block on CUDA cores; in a decode step the new token
-// is first written to the sink or tail (unless it completes a group).
+// is first written to the sink or tail (unless it completes a group). Scores: one
+// thread per token, sixteen independent 16-byte loads of its K row. P V: warp w takes
+// tokens w, w+8, ...; lane l holds channels 4l..4l+3 of all four heads, so every V row
+// is one coalesced 256-byte warp load; the eight warps' sums meet in shared memory.
 __device__ void exact_item(const DecodeParams& p, const Smem& sm, int ci, int kvh) {
-    const int t = threadIdx.x;
+    const int t = threadIdx.x, w = t >> 5, lane = t & 31;
     const SeqEntry& e = p.seqs[ci];
     const size_t sl = (size_t)e.seq * p.num_layers + p.layer;
     const size_t rows0 = (sl * p.hkv + kvh) * 128;  // first row of this (seq, layer, kv head)
@@ -296,9 +325,10 @@ __device__ void exact_item(const DecodeParams& p, const Smem& sm, int ci, int kv
                      (rows0 + row) * 256;
         reinterpret_cast<uint4*>(p.base + off)[chunk] = reinterpret_cast<const uint4*>(src)[chunk];
     }
-    float* qraw = sm.mrg;         // [4][128]
-    float* sc = sm.mrg + 512;     // [4][256]
-    float* red = sm.mrg + 1536;   // [4][2] max, [4][2] sum
+    float* qraw = sm.xbuf;           // [4][128]
+    float* sc = sm.xbuf + 512;       // [4][256]
+    float* red = sm.xbuf + 1536;     // [16]
+    float* part = sm.mrg;            // [8 warps][4][128]
     for (int k = t; k < 512; k += kConsumers) {
         const int h = k >> 7, j = k & 127;
         qraw[k] = h < p.r ? half_bits_to_float(p.q[((size_t)ci * p.hq + (size_t)kvh * p.r + h) * 128 + j]) : 0.f;
@@ -307,27 +337,34 @@ __device__ void exact_item(const DecodeParams& p, const Smem& sm, int ci, int kv
     const int n_ex = e.n_sink + e.n_tail;
     float s[4] = {kNegInf, kNegInf, kNegInf, kNegInf};
     if (t < n_ex) {
-        const uint16_t* row = t < e.n_sink ? sink_k + (size_t)t * 128 : tail_k + (size_t)(t - e.n_sink) * 128;
+        const uint4* row = reinterpret_cast<const uint4*>(t < e.n_sink ? sink_k + (size_t)t * 128
+                                                                      : tail_k + (size_t)(t - e.n_sink) * 128);
         float d[4] = {0.f, 0.f, 0.f, 0.f};
-#pragma unroll 4
-        for (int c = 0; c < 16; ++c) {
-            uint4 kv = reinterpret_cast<const uint4*>(row)[c];
-            const __half2* hp = reinterpret_cast<const __half2*>(&kv);
-            float kf[8];
 #pragma unroll
-            for (int q2 = 0; q2 < 4; ++q2) {
-                float2 f = __half22float2(hp[q2]);
-                kf[2 * q2] = f.x;
-                kf[2 * q2 + 1] = f.y;
-            }
+        for (int half = 0; half < 2; ++half) {
+            uint4 kv[8];
 #pragma unroll
-            for (int h = 0; h < 4; ++h) {
-                const float4 qa = reinterpret_cast<const float4*>(qraw + 128 * h + 8 * c)[0];
-                const float4 qb = reinterpret_cast<const float4*>(qraw + 128 * h + 8 * c)[1];
-                d[h] = fmaf(kf[0], qa.x, d[h]); d[h] = fmaf(kf[1], qa.y, d[h]);
-                d[h] = fmaf(kf[2], qa.z, d[h]); d[h] = fmaf(kf[3], qa.w, d[h]);
-                d[h] = fmaf(kf[4], qb.x, d[h]); d[h] = fmaf(kf[5], qb.y, d[h]);
-                d[h] = fmaf(kf[6], qb.z, d[h]); d[h] = fmaf(kf[7], qb.w, d[h]);
+            for (int c = 0; c < 8; ++c) kv[c] = row[8 * half + c];
+#pragma unroll
+            for (int c = 0; c < 8; ++c) {
+                const __half2* hp = reinterpret_cast<const __half2*>(&kv[c]);
+                float kf[8];
+#pragma unroll
+                for (int q2 = 0; q2 < 4; ++q2) {
+                    float2 f = __half22float2(hp[q2]);
+                    kf[2 * q2] = f.x;
+                    kf[2 * q2 + 1] = f.y;
+                }
+                const int cc = 8 * half + c;
+#pragma unroll
+                for (int h = 0; h < 4; ++h) {
+                    const float4 qa = reinterpret_cast<const float4*>(qraw + 128 * h + 8 * cc)[0];
+                    const float4 qb = reinterpret_cast<const float4*>(qraw + 128 * h + 8 * cc)[1];
+                    d[h] = fmaf(kf[0], qa.x, d[h]); d[h] = fmaf(kf[1], qa.y, d[h]);
+                    d[h] = fmaf(kf[2], qa.z, d[h]); d[h] = fmaf(kf[3], qa.w, d[h]);
+                    d[h] = fmaf(kf[4], qb.x, d[h]); d[h] = fmaf(kf[5], qb.y, d[h]);
+                    d[h] = fmaf(kf[6], qb.z, d[h]); d[h] = fmaf(kf[7], qb.w, d[h]);
+                }
             }
         }
 #pragma unroll
@@ -342,7 +379,7 @@ __device__ void exact_item(const DecodeParams& p, const Smem& sm, int ci, int kv
         float m = fmaxf(fmaxf(sc[256 * h + k0], sc[256 * h + k0 + 1]), fmaxf(sc[256 * h + k0 + 2], sc[256 * h + k0 + 3]));
 #pragma unroll
         for (int o = 16; o > 0; o >>= 1) m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, o));
-        if ((t & 31) == 0) red[2 * h + ((t >> 5) & 1)] = m;
+        if (lane == 0) red[2 * h + (w & 1)] = m;
         named_bar(1, kConsumers);
         m = fmaxf(red[2 * h], red[2 * h + 1]);
         float sum = 0.f;
@@ -355,7 +392,7 @@ __device__ void exact_item(const DecodeParams& p, const Smem& sm, int ci, int kv
         }
 #pragma unroll
         for (int o = 16; o > 0; o >>= 1) sum += __shfl_xor_sync(0xffffffffu, sum, o);
-        if ((t & 31) == 0) red[8 + 2 * h + ((t >> 5) & 1)] = sum;
+        if (lane == 0) red[8 + 2 * h + (w & 1)] = sum;
         named_bar(1, kConsumers);
         if ((t & 63) == 0) {
             float* P = partial_ptr(p, e.seq * p.hkv + kvh, kSlotExact);
@@ -363,22 +400,54 @@ __device__ void exact_item(const DecodeParams& p, const Smem& sm, int ci, int kv
             P[8 + h] = red[8 + 2 * h] + red[8 + 2 * h + 1];
         }
     }
-    // P V: thread = channel j, two heads
+    // P V
     {
-        const int j = t & 127, hp = t >> 7;
+        float acc[4][4];
+#pragma unroll
+        for (int h = 0; h < 4; ++h)
+#pragma unroll
+            for (int c = 0; c < 4; ++c) acc[h][c] = 0.f;
+        for (int k0 = w; k0 < n_ex; k0 += 32) {
+            uint2 vv[4];
+#pragma unroll
+            for (int u = 0; u < 4; ++u) {
+                const int k = k0 + 8 * u;
+                vv[u] = make_uint2(0u, 0u);
+                if (k < n_ex) {
+                    const uint16_t* row = k < e.n_sink ? sink_v + (size_t)k * 128 : tail_v + (size_t)(k - e.n_sink) * 128;
+                    vv[u] = reinterpret_cast<const uint2*>(row)[lane];
+                }
+            }
+#pragma unroll
+            for (int u = 0; u < 4; ++u) {
+                const int k = k0 + 8 * u;
+                if (k < n_ex) {
+                    const float2 va = __half22float2(bits_h2(vv[u].x)), vb = __half22float2(bits_h2(vv[u].y));
+#pragma unroll
+                    for (int h = 0; h < 4; ++h) {
+                        const float pk = sc[256 * h + k];
+                        acc[h][0] = fmaf(pk, va.x, acc[h][0]);
+                        acc[h][1] = fmaf(pk, va.y, acc[h][1]);
+                        acc[h][2] = fmaf(pk, vb.x, acc[h][2]);
+                        acc[h][3] = fmaf(pk, vb.y, acc[h][3]);
+                    }
+                }
+            }
+        }
+#pragma unroll
+        for (int h = 0; h < 4; ++h)
+            *reinterpret_cast<float4*>(part + (w * 4 + h) * 128 + 4 * lane) =
+                make_float4(acc[h][0], acc[h][1], acc[h][2], acc[h][3]);
+        named_bar(1, kConsumers);
+        const int h = t >> 6, jj = 2 * (t & 63);
         float a0 = 0.f, a1 = 0.f;
-        const float* p0 = sc + 256 * (2 * hp);
-        const float* p1 = sc + 256 * (2 * hp + 1);
-#pragma unroll 4
-        for (int k = 0; k < n_ex; ++k) {
-            const uint16_t* row = k < e.n_sink ? sink_v + (size_t)k * 128 : tail_v + (size_t)(k - e.n_sink) * 128;
-            const float v = half_bits_to_float(row[j]);
-            a0 = fmaf(p0[k], v, a0);
-            a1 = fmaf(p1[k], v, a1);
+#pragma unroll
+        for (int k = 0; k < 8; ++k) {
+            a0 += part[(k * 4 + h) * 128 + jj];
+            a1 += part[(k * 4 + h) * 128 + jj + 1];
         }
         float* P = partial_ptr(p, e.seq * p.hkv + kvh, kSlotExact);
-        P[12 + 128 * (2 * hp) + j] = a0;
-        P[12 + 128 * (2 * hp + 1) + j] = a1;
+        *reinterpret_cast<float2*>(P + 12 + 128 * h + jj) = make_float2(a0, a1);
         if (t == 0) P[0] = __int_as_float((int)p.epoch);
     }
     publish(p, sm, ci, kvh);

@@ -176,3 +176,50 @@ def tiny_matrix(seed: int, rows: int, cols: int, scale: Optional[float] = 1.0):
     """Small fp16 matrix for brute-force checks."""
     rng = np.random.default_rng([seed, 49979687])
     return (rng.standard_normal(size=(rows, cols)) * scale).astype(np.float16)
+
+
+def torch_tokens(seed: int, seq: int, start: int, count: int, num_kv_heads: int, head_dim: int = HEAD_DIM,
+                 spike_frac: float = 0.0, spike_factor: float = 10.0, device="cuda"):
+    """Same value recipe as TokenSource, drawn on the device with torch (for the
+    multi-gigabyte prefills of the full-size workloads). Token t of sequence ``seq``
+    depends only on (seed, seq, t // 4096), so chunked generation is reproducible.
+    Returns fp16 (K, V), each [count][Hkv][d]."""
+    import torch
+
+    g = torch.Generator(device=device)
+    g.manual_seed(int(seed) * 1000003 + int(seq) * 7919 + 17)
+    s = torch.empty((2, num_kv_heads, head_dim), device=device).log_normal_(0.0, 0.5, generator=g)
+    for side in range(2):
+        for h in range(num_kv_heads):
+            out = torch.randperm(head_dim, generator=g, device=device)[:2]
+            s[side, h, out] *= 20.0
+    blk = 4096
+    ks, vs = [], []
+    pos = start
+    end = start + count
+    while pos < end:
+        b = pos // blk
+        gb = torch.Generator(device=device)
+        gb.manual_seed(int(seed) * 1000003 + int(seq) * 7919 + 104729 * (b + 1))
+        norms = torch.empty((blk,), device=device).log_normal_(0.0, 0.7, generator=gb)
+        if spike_frac > 0:
+            spikes = torch.rand((blk,), device=device, generator=gb) < spike_frac
+            norms = torch.where(spikes, norms * spike_factor, norms)
+        lo = pos - b * blk
+        hi = min(blk, end - b * blk)
+        x = torch.randn((2, blk, num_kv_heads, head_dim), device=device, generator=gb)[:, lo:hi]
+        x = x * s[:, None] * norms[None, lo:hi, None, None]
+        x = x.clamp_(-65504.0, 65504.0).to(torch.float16)
+        ks.append(x[0])
+        vs.append(x[1])
+        pos = b * blk + hi
+    return torch.cat(ks).contiguous(), torch.cat(vs).contiguous()
+
+
+def torch_queries(seed: int, steps: int, batch: int, num_q_heads: int, head_dim: int = HEAD_DIM, device="cuda"):
+    """N(0,1) fp16 queries [steps][batch][Hq][d] drawn on the device."""
+    import torch
+
+    g = torch.Generator(device=device)
+    g.manual_seed(int(seed) * 15485863 + 3)
+    return torch.randn((steps, batch, num_q_heads, head_dim), device=device, generator=g).to(torch.float16)
