@@ -151,8 +151,6 @@ __device__ bool next_item(const DecodeParams& p, int64_t& u, int64_t hi, Item& i
 struct Smem {
     uint8_t* stages;
     uint64_t* full;
-    uint64_t* empty;
-    uint64_t* seal_done;
     float* qrot;    // [4][128] rotated query / its max
     float* qmax;    // [4]
     float* xbuf;    // [8 warps][kXbWarp] (half2 words)
@@ -482,6 +480,28 @@ struct WarpState {
     float acc[8][2];
 };
 
+__device__ __forceinline__ float fast_exp2(float x) {
+    float y;
+    asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
+    return y;
+}
+
+// Operand of pair P from a thread's code words (the pair of codes x, x + HALF of
+// word P / HALF, masked into the low mantissa bits of two halves).
+template <int B>
+__device__ __forceinline__ uint32_t pair_operand(const uint32_t* w, int P) {
+    using C = Codes<B>;
+    const int word = P / C::HALF, x = P % C::HALF;
+    return (w[word] >> C::sh(x)) & C::mask(x);
+}
+
+// Tiles processed together, k-step outer: TG independent MMA chains, TG * 2 * B
+// code words live in registers.
+template <int B>
+struct TileGroup {
+    static constexpr int TG = B == 2 ? 8 : (B == 4 ? 4 : 2);
+};
+
 // Process one sealed group pair held in shared memory (K record, then V record).
 template <int KB, int VB>
 __device__ __forceinline__ void process_group(const DecodeParams& p, const uint8_t* rec, const float (&bq)[16][2],
@@ -508,16 +528,10 @@ __device__ __forceinline__ void process_group(const DecodeParams& p, const uint8
             uint4 v = cp[k];
             cw[4 * k] = v.x; cw[4 * k + 1] = v.y; cw[4 * k + 2] = v.z; cw[4 * k + 3] = v.w;
         }
-        float cf[32];
+        __half2 mh = bits_h2(cw[0]);
 #pragma unroll
-        for (int k = 0; k < 16; ++k) {
-            float2 f = __half22float2(bits_h2(cw[k]));
-            cf[2 * k] = f.x;
-            cf[2 * k + 1] = f.y;
-        }
-        float mc = cf[0];
-#pragma unroll
-        for (int k = 1; k < 32; ++k) mc = fmaxf(mc, cf[k]);
+        for (int k = 1; k < 16; ++k) mh = __hmax2(mh, bits_h2(cw[k]));
+        float mc = fmaxf(__low2float(mh), __high2float(mh));
         mc = fmaxf(mc, __shfl_xor_sync(0xffffffffu, mc, 1));
         mc = fmaxf(mc, __shfl_xor_sync(0xffffffffu, mc, 2));
         kappa = 1.0f / mc;
@@ -527,8 +541,11 @@ __device__ __forceinline__ void process_group(const DecodeParams& p, const uint8
         for (int P = 0; P < 16; ++P) {
             const int x = P % CK::HALF;
             const int c0 = CK::CPW * (P / CK::HALF) + x;
-            const float f0 = bq[P][0] * cf[c0] * kappa;
-            const float f1 = bq[P][1] * cf[c0 + CK::HALF] * kappa;
+            const int c1 = c0 + CK::HALF;
+            const float cf0 = __half2float(reinterpret_cast<const __half*>(cw)[c0]);
+            const float cf1 = __half2float(reinterpret_cast<const __half*>(cw)[c1]);
+            const float f0 = bq[P][0] * cf0 * kappa;
+            const float f1 = bq[P][1] * cf1 * kappa;
             const __half2 hi = __floats2half2_rn(f0, f1);
             if (lo_part) {
                 const float2 hf = __half22float2(hi);
@@ -536,8 +553,8 @@ __device__ __forceinline__ void process_group(const DecodeParams& p, const uint8
             } else {
                 bk[P] = h2_bits(hi);
             }
-            const float s = __int_as_float((127 + CK::ex(x) - kE) << 23);  // 2^(ex - E)
-            sum = fmaf(f0 + f1, s, sum);
+            const float sc = __int_as_float((127 + CK::ex(x) - kE) << 23);  // 2^(ex - E)
+            sum = fmaf(f0 + f1, sc, sum);
         }
         sum += __shfl_xor_sync(0xffffffffu, sum, 1);
         sum += __shfl_xor_sync(0xffffffffu, sum, 2);
@@ -547,21 +564,32 @@ __device__ __forceinline__ void process_group(const DecodeParams& p, const uint8
     // ---- scores of the 16 tokens this thread holds (head tq)
     float S[8][2];
     {
+        constexpr int TG = TileGroup<KB>::TG;
 #pragma unroll
-        for (int mt = 0; mt < 8; ++mt) {
-            const int t0 = tok_row<VB>(mt, g), t1 = t0 + CV::HALF;
-            uint32_t w0[KB], w1[KB];
-            load_chunk<KB>(krec + 528 + t0 * 16 * KB + 4 * KB * tq, w0);
-            load_chunk<KB>(krec + 528 + t1 * 16 * KB + 4 * KB * tq, w1);
-            uint32_t a0[16], a1[16];
-            unpack16<KB>(w0, a0);
-            unpack16<KB>(w1, a1);
-            float c[4] = {0.f, 0.f, 0.f, 0.f};
+        for (int t0g = 0; t0g < 8; t0g += TG) {
+            uint32_t w0[TG][KB], w1[TG][KB];
 #pragma unroll
-            for (int ks = 0; ks < 8; ++ks) mma16816(c, a0[2 * ks], a1[2 * ks], a0[2 * ks + 1], a1[2 * ks + 1],
-                                                    bk[2 * ks], bk[2 * ks + 1]);
-            S[mt][0] = c[0] + c[1];
-            S[mt][1] = c[2] + c[3];
+            for (int i = 0; i < TG; ++i) {
+                const int t0 = tok_row<VB>(t0g + i, g), t1 = t0 + CV::HALF;
+                load_chunk<KB>(krec + 528 + t0 * 16 * KB + 4 * KB * tq, w0[i]);
+                load_chunk<KB>(krec + 528 + t1 * 16 * KB + 4 * KB * tq, w1[i]);
+            }
+            float c[TG][4];
+#pragma unroll
+            for (int i = 0; i < TG; ++i) c[i][0] = c[i][1] = c[i][2] = c[i][3] = 0.f;
+#pragma unroll
+            for (int ks = 0; ks < 8; ++ks) {
+#pragma unroll
+                for (int i = 0; i < TG; ++i)
+                    mma16816(c[i], pair_operand<KB>(w0[i], 2 * ks), pair_operand<KB>(w1[i], 2 * ks),
+                             pair_operand<KB>(w0[i], 2 * ks + 1), pair_operand<KB>(w1[i], 2 * ks + 1), bk[2 * ks],
+                             bk[2 * ks + 1]);
+            }
+#pragma unroll
+            for (int i = 0; i < TG; ++i) {
+                S[t0g + i][0] = c[i][0] + c[i][1];
+                S[t0g + i][1] = c[i][2] + c[i][3];
+            }
         }
     }
     const float alpha = p.scale_log2 * qm * dK * (float)(1 << (24 - kE)) / kappa;
@@ -584,18 +612,18 @@ __device__ __forceinline__ void process_group(const DecodeParams& p, const uint8
         amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, o));
     }
     const float mnew = fmaxf(st.m, gmax);
-    const float corr = exp2f(st.m - mnew);
+    const float corr = fast_exp2(st.m - mnew);
     st.m = mnew;
     const float rho = amax > 0.f ? 1.0f / amax : 1.0f;
     const int xv = g % CV::HALF;
-    const float sv = __int_as_float((127 + kEV - CV::ex(xv)) << 23);    // 2^(EV - ex)
-    const float svi = __int_as_float((127 - kEV + CV::ex(xv)) << 23);   // 2^(ex - EV)
+    const float sv = __int_as_float((127 + kEV - CV::ex(xv)) << 23) * rho;  // 2^(EV - ex) / max aV
+    const float svi = __int_as_float((127 - kEV + CV::ex(xv)) << 23);       // 2^(ex - EV)
     float lsum = 0.f, wsum = 0.f;
 #pragma unroll
     for (int mt = 0; mt < 8; ++mt) {
-        const float p0 = exp2f(S[mt][0] - mnew), p1 = exp2f(S[mt][1] - mnew);
+        const float p0 = fast_exp2(S[mt][0] - mnew), p1 = fast_exp2(S[mt][1] - mnew);
         lsum += p0 + p1;
-        const __half2 wh = __floats2half2_rn(p0 * av[mt][0] * rho * sv, p1 * av[mt][1] * rho * sv);
+        const __half2 wh = __floats2half2_rn(p0 * av[mt][0] * sv, p1 * av[mt][1] * sv);
         const float2 wf = __half22float2(wh);
         wsum = fmaf(wf.x + wf.y, svi, wsum);
         reinterpret_cast<uint32_t*>(xb)[kXbHead * tq + 20 * (mt >> 1) + 8 * (mt & 1) + g] = h2_bits(wh);
@@ -617,21 +645,36 @@ __device__ __forceinline__ void process_group(const DecodeParams& p, const uint8
     // ---- P V in the rotated frame
     const float gam = dV * (float)(1 << (24 - kEV)) / rho;
     const float del = mV * wsum / rho;
+    {
+        constexpr int TG = TileGroup<VB>::TG;
 #pragma unroll
-    for (int mt = 0; mt < 8; ++mt) {
-        const int c0 = 16 * mt + g, c1 = c0 + 8;
-        uint32_t w0[VB], w1[VB];
-        load_chunk<VB>(vrec + 528 + c0 * 16 * VB + 4 * VB * tq, w0);
-        load_chunk<VB>(vrec + 528 + c1 * 16 * VB + 4 * VB * tq, w1);
-        uint32_t a0[16], a1[16];
-        unpack16<VB>(w0, a0);
-        unpack16<VB>(w1, a1);
-        float d[4] = {0.f, 0.f, 0.f, 0.f};
+        for (int m0 = 0; m0 < 8; m0 += TG) {
+            uint32_t w0[TG][VB], w1[TG][VB];
 #pragma unroll
-        for (int ks = 0; ks < 8; ++ks) mma16816(d, a0[2 * ks], a1[2 * ks], a0[2 * ks + 1], a1[2 * ks + 1],
-                                                bv[2 * ks], bv[2 * ks + 1]);
-        st.acc[mt][0] = fmaf(st.acc[mt][0], corr, half_bits_to_float(cV[c0]) * fmaf(gam, d[0], del));
-        st.acc[mt][1] = fmaf(st.acc[mt][1], corr, half_bits_to_float(cV[c1]) * fmaf(gam, d[2], del));
+            for (int i = 0; i < TG; ++i) {
+                const int c0 = 16 * (m0 + i) + g;
+                load_chunk<VB>(vrec + 528 + c0 * 16 * VB + 4 * VB * tq, w0[i]);
+                load_chunk<VB>(vrec + 528 + (c0 + 8) * 16 * VB + 4 * VB * tq, w1[i]);
+            }
+            float d[TG][4];
+#pragma unroll
+            for (int i = 0; i < TG; ++i) d[i][0] = d[i][1] = d[i][2] = d[i][3] = 0.f;
+#pragma unroll
+            for (int ks = 0; ks < 8; ++ks) {
+#pragma unroll
+                for (int i = 0; i < TG; ++i)
+                    mma16816(d[i], pair_operand<VB>(w0[i], 2 * ks), pair_operand<VB>(w1[i], 2 * ks),
+                             pair_operand<VB>(w0[i], 2 * ks + 1), pair_operand<VB>(w1[i], 2 * ks + 1), bv[2 * ks],
+                             bv[2 * ks + 1]);
+            }
+#pragma unroll
+            for (int i = 0; i < TG; ++i) {
+                const int mt = m0 + i;
+                const int c0 = 16 * mt + g;
+                st.acc[mt][0] = fmaf(st.acc[mt][0], corr, half_bits_to_float(cV[c0]) * fmaf(gam, d[i][0], del));
+                st.acc[mt][1] = fmaf(st.acc[mt][1], corr, half_bits_to_float(cV[c0 + 8]) * fmaf(gam, d[i][2], del));
+            }
+        }
     }
 }
 
@@ -692,6 +735,51 @@ struct SealRows {
     __device__ const uint16_t* operator()(int i) const { return i < 127 ? tail + 128 * i : last; }
 };
 
+// Walks the CTA's sealed groups in stream order to find the record of group number gn
+// (0, 1, ... over the chunk and seal items of the CTA's unit range, in item order).
+struct GroupCursor {
+    int64_t u;       // unit cursor of the item walk
+    Item it;         // current chunk / seal item
+    uint32_t base;   // group number of the item's first group
+    bool valid;
+    __device__ void init(int64_t lo) { u = lo; base = 0; valid = false; it.g0 = it.g1 = 0; }
+    // record address of group gn (gn never decreases between calls); null past the end
+    __device__ const uint8_t* src(const DecodeParams& p, int64_t hi, uint32_t gn) {
+        for (;;) {
+            if (valid && gn < base + (uint32_t)(it.g1 - it.g0)) break;
+            if (valid) base += (uint32_t)(it.g1 - it.g0);
+            valid = false;
+            Item n;
+            bool found = false;
+            while (next_item(p, u, hi, n)) {
+                if (n.type != 1) { found = true; break; }
+            }
+            if (!found) return nullptr;
+            it = n;
+            valid = true;
+        }
+        const SeqEntry& e = p.seqs[it.ci];
+        const int pair = p.rec_k + p.rec_v;
+        if (it.type == 2)
+            return p.base + p.lay.pool + (size_t)e.seal_slot * p.slot_bytes + (size_t)it.kvh * pair;
+        return group_src(p, e.seq, it.kvh, it.g0 + (int)(gn - base));
+    }
+};
+
+__device__ __forceinline__ void issue_group(const DecodeParams& p, const Smem& sm, GroupCursor& cur, int64_t hi,
+                                            uint32_t gn) {
+    const uint8_t* src = cur.src(p, hi, gn);
+    if (!src) return;
+    const uint32_t pair = (uint32_t)(p.rec_k + p.rec_v);
+    const uint32_t s = gn % p.stages;
+    mbar_arrive_expect_tx(sm.full + s, pair);
+    bulk_g2s(sm.stages + (size_t)s * pair, src, pair, sm.full + s);
+}
+
+// One CTA of 8 warps per SM. Stage ring: group gn lives in stage gn % S and is
+// processed by warp gn % 8; the warp that finishes with a stage issues the copy of
+// group gn + S into it, so no stage needs a release barrier. Seal items of the CTA run
+// first, with their scratch aliased onto the (still empty) stage ring.
 template <int KB, int VB>
 __global__ void __launch_bounds__(kDecodeThreads, 1) decode_kernel(const __grid_constant__ DecodeParams p) {
     extern __shared__ __align__(128) uint8_t smem_raw[];
@@ -700,14 +788,12 @@ __global__ void __launch_bounds__(kDecodeThreads, 1) decode_kernel(const __grid_
     {
         size_t off = 0;
         sm.stages = smem_raw;
-        off += (size_t)p.stages * pair;
+        size_t ring = (size_t)p.stages * pair;
+        if (ring < sizeof(SealSmem)) ring = sizeof(SealSmem);
+        off += ring;
         off = (off + 15) & ~(size_t)15;
         sm.full = reinterpret_cast<uint64_t*>(smem_raw + off);
-        off += 16 * 8;
-        sm.empty = reinterpret_cast<uint64_t*>(smem_raw + off);
-        off += 16 * 8;
-        sm.seal_done = reinterpret_cast<uint64_t*>(smem_raw + off);
-        off += 16;
+        off += 32 * 8;
         sm.qrot = reinterpret_cast<float*>(smem_raw + off);
         off += 512 * 4;
         sm.qmax = reinterpret_cast<float*>(smem_raw + off);
@@ -717,16 +803,11 @@ __global__ void __launch_bounds__(kDecodeThreads, 1) decode_kernel(const __grid_
         sm.xbuf = reinterpret_cast<float*>(smem_raw + off);
         off += 8 * kXbWarp * 4;
         sm.mrg = reinterpret_cast<float*>(smem_raw + off);
-        off += 8 * kMrgFloats * 4;
-        sm.seal = reinterpret_cast<SealSmem*>(smem_raw + off);
+        sm.seal = reinterpret_cast<SealSmem*>(smem_raw);
     }
     const int t = threadIdx.x, w = t >> 5, lane = t & 31;
     if (t == 0) {
-        for (int s = 0; s < p.stages; ++s) {
-            mbar_init(sm.full + s, 1);
-            mbar_init(sm.empty + s, 1);
-        }
-        mbar_init(sm.seal_done, 1);
+        for (int s = 0; s < p.stages; ++s) mbar_init(sm.full + s, 1);
         asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
     }
     __syncthreads();
@@ -734,41 +815,44 @@ __global__ void __launch_bounds__(kDecodeThreads, 1) decode_kernel(const __grid_
     const int64_t lo = b * U / P, hi = (b + 1) * U / P;
     int32_t* err = err_word(p);
 
-    if (w == 8) {
-        // ---------------- producer: stream the records of this CTA's groups
-        if (lane == 0) {
-            int64_t u = lo;
-            Item it;
-            uint32_t n = 0, sd = 0;
-            while (next_item(p, u, hi, it)) {
-                if (it.type == 1) continue;
-                const SeqEntry& e = p.seqs[it.ci];
-                if (it.type == 2) {
-                    mbar_wait(sm.seal_done, sd, err);
-                    sd ^= 1;
-                    fence_proxy_async_global();
-                }
-                for (int g = it.g0; g < it.g1; ++g) {
-                    const uint32_t s = n % p.stages;
-                    if (n >= (uint32_t)p.stages) mbar_wait(sm.empty + s, ((n / p.stages) - 1) & 1, err);
-                    const uint8_t* src;
-                    if (it.type == 2)
-                        src = p.base + p.lay.pool + (size_t)e.seal_slot * p.slot_bytes + (size_t)it.kvh * pair;
-                    else
-                        src = group_src(p, e.seq, it.kvh, g);
-                    mbar_arrive_expect_tx(sm.full + s, pair);
-                    bulk_g2s(sm.stages + (size_t)s * pair, src, pair, sm.full + s);
-                    ++n;
-                }
+    // ---- 1. seal the groups completed by this step's tokens (before any prefetch)
+    bool sealed_any = false;
+    {
+        int64_t u = lo;
+        Item it;
+        while (next_item(p, u, hi, it)) {
+            if (it.type != 2) continue;
+            const SeqEntry& e = p.seqs[it.ci];
+            const size_t sl = (size_t)e.seq * p.num_layers + p.layer;
+            const size_t rows0 = (sl * p.hkv + it.kvh) * 128;
+            uint8_t* dst = p.base + p.lay.pool + (size_t)e.seal_slot * p.slot_bytes + (size_t)it.kvh * pair;
+            SealRows rk{reinterpret_cast<const uint16_t*>(p.base + p.lay.tail_k) + rows0 * 128,
+                        p.k_new + ((size_t)it.ci * p.hkv + it.kvh) * 128};
+            seal_matrix(rk, p.k_bits, 0, p.iters, dst, nullptr, *sm.seal, 1);
+            SealRows rv{reinterpret_cast<const uint16_t*>(p.base + p.lay.tail_v) + rows0 * 128,
+                        p.v_new + ((size_t)it.ci * p.hkv + it.kvh) * 128};
+            seal_matrix(rv, p.v_bits, 1, p.iters, dst + p.rec_k, nullptr, *sm.seal, 1);
+            if (t == 0 && it.kvh == 0) {
+                int32_t* table = reinterpret_cast<int32_t*>(p.base + p.lay.block_table);
+                table[sl * p.max_groups + e.seal_group] = e.seal_slot;
             }
-            // drain: wait until the consumers have released every stage still in flight
-            const uint32_t first = n > (uint32_t)p.stages ? n - p.stages : 0;
-            for (uint32_t k = first; k < n; ++k) mbar_wait(sm.empty + (k % p.stages), (k / p.stages) & 1, err);
+            sealed_any = true;
         }
-        return;
+    }
+    if (sealed_any) {
+        fence_proxy_async_global();  // the records just written are read by bulk copies
+        __syncthreads();
     }
 
-    // ---------------- consumers: 8 warps
+    // ---- 2. prologue: the first S groups of the stream
+    GroupCursor cur;
+    cur.init(lo);
+    for (uint32_t gn = w; gn < (uint32_t)p.stages; gn += 8) {
+        if (lane == 0) issue_group(p, sm, cur, hi, gn);
+        __syncwarp();
+    }
+
+    // ---- 3. items in order
     const int g = lane >> 2, tq = lane & 3;
     int64_t u = lo;
     Item it;
@@ -783,23 +867,6 @@ __global__ void __launch_bounds__(kDecodeThreads, 1) decode_kernel(const __grid_
         }
         int slot;
         if (it.type == 2) {
-            // seal K and V of the completed group: rows 0..126 from the tail, row 127 new
-            const size_t sl = (size_t)e.seq * p.num_layers + p.layer;
-            const size_t rows0 = (sl * p.hkv + it.kvh) * 128;
-            uint8_t* dst = p.base + p.lay.pool + (size_t)e.seal_slot * p.slot_bytes + (size_t)it.kvh * pair;
-            SealRows rk{reinterpret_cast<const uint16_t*>(p.base + p.lay.tail_k) + rows0 * 128,
-                        p.k_new + ((size_t)it.ci * p.hkv + it.kvh) * 128};
-            seal_matrix(rk, p.k_bits, 0, p.iters, dst, nullptr, *sm.seal, 1);
-            SealRows rv{reinterpret_cast<const uint16_t*>(p.base + p.lay.tail_v) + rows0 * 128,
-                        p.v_new + ((size_t)it.ci * p.hkv + it.kvh) * 128};
-            seal_matrix(rv, p.v_bits, 1, p.iters, dst + p.rec_k, nullptr, *sm.seal, 1);
-            if (t == 0 && it.kvh == 0) {
-                int32_t* table = reinterpret_cast<int32_t*>(p.base + p.lay.block_table);
-                table[sl * p.max_groups + e.seal_group] = e.seal_slot;
-            }
-            fence_proxy_async_global();
-            named_bar(1, kConsumers);
-            if (t == 0) mbar_arrive(sm.seal_done);
             slot = kSlotSeal;
         } else {
             int64_t first;
@@ -819,9 +886,9 @@ __global__ void __launch_bounds__(kDecodeThreads, 1) decode_kernel(const __grid_
             for (int P2 = 0; P2 < 16; ++P2) {
                 const int x = P2 % CK::HALF;
                 const int c0 = 32 * tq + CK::CPW * (P2 / CK::HALF) + x;
-                const float s = __int_as_float((127 + kE - CK::ex(x)) << 23);
-                bq[P2][0] = qh[c0] * s;
-                bq[P2][1] = qh[c0 + CK::HALF] * s;
+                const float sc = __int_as_float((127 + kE - CK::ex(x)) << 23);
+                bq[P2][0] = qh[c0] * sc;
+                bq[P2][1] = qh[c0 + CK::HALF] * sc;
             }
         }
         const float qm = sm.qmax[tq];
@@ -838,11 +905,20 @@ __global__ void __launch_bounds__(kDecodeThreads, 1) decode_kernel(const __grid_
             mbar_wait(sm.full + s, (gn / p.stages) & 1, err);
             process_group<KB, VB>(p, sm.stages + (size_t)s * pair, bq, qm, xb, st, g, tq);
             __syncwarp();
-            if (lane == 0) mbar_arrive(sm.empty + s);
+            if (lane == 0) issue_group(p, sm, cur, hi, gn + p.stages);
+            __syncwarp();
         }
         n += cnt;
         write_item_partial(p, sm, st, blk, slot);
         publish(p, sm, it.ci, it.kvh);
+    }
+    // Normally every copy was waited for above. After a wait that gave up, let the
+    // copies still in flight land (bounded) before the CTA's shared memory goes away.
+    if (t == 0 && (*reinterpret_cast<volatile int32_t*>(err) & kErrTimeout)) {
+        const uint64_t t0 = global_ns();
+        for (uint32_t k = n > (uint32_t)p.stages ? n - p.stages : 0; k < n; ++k)
+            while (!mbar_try_wait(sm.full + (k % p.stages), (k / p.stages) & 1) && global_ns() - t0 < kWaitLimitNs) {
+            }
     }
 }
 
@@ -862,11 +938,12 @@ int launch_t(const DecodeParams& p, int smem, cudaStream_t s) {
 }  // namespace
 
 int decode_smem_bytes(int k_bits, int v_bits, int stages, bool with_seal) {
+    (void)with_seal;  // the seal scratch aliases the stage ring
     size_t pair = record_bytes(k_bits) + record_bytes(v_bits);
     size_t off = (size_t)stages * pair;
+    if (off < sizeof(SealSmem)) off = sizeof(SealSmem);
     off = (off + 15) & ~(size_t)15;
-    off += 16 * 8 * 2 + 16 + 512 * 4 + 16 + 16 + 8 * kXbWarp * 4 + 8 * kMrgFloats * 4;
-    if (with_seal) off += sizeof(SealSmem);
+    off += 32 * 8 + 512 * 4 + 16 + 16 + 8 * kXbWarp * 4 + 8 * kMrgFloats * 4;
     return (int)off;
 }
 

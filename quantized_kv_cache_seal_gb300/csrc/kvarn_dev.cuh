@@ -227,14 +227,16 @@ __device__ void seal_matrix(const Rows& rows, int bits, int which, int iters, ui
         float a = sqrtf(a2);
         uint16_t ab = f16_bits_sat(a);
         S.a16[i] = ab;
-        S.ra[i] = 1.0f / half_bits_to_float(ab);
+        const float af = half_bits_to_float(ab);
+        S.ra[i] = af != 0.0f ? 1.0f / af : 0.0f;  // a zero scale maps the row to 0
         if (dbg) dbg[i] = a;
     }
     if (hc == 0) {
         float c = sqrtf(c2);
         uint16_t cb = f16_bits_sat(c);
         S.c16[j] = cb;
-        S.rc[j] = 1.0f / half_bits_to_float(cb);
+        const float cf = half_bits_to_float(cb);
+        S.rc[j] = cf != 0.0f ? 1.0f / cf : 0.0f;
         if (dbg) dbg[128 + j] = c;
     }
     named_bar(bar_id, 256);

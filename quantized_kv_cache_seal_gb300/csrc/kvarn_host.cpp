@@ -244,9 +244,9 @@ kvarn_status run_decode(kvarn_cache* c, int32_t layer, int32_t n_seqs, const int
         return st;
     }
     int pair = (int)(c->rec_k + c->rec_v);
-    int base_smem = decode_smem_bytes(cfg.k_bits, cfg.v_bits, 0, any_seal);
-    int stages = std::min(16, (c->max_smem - base_smem) / pair);
-    if (stages < 2) {
+    int stages = 32;
+    while (stages > 1 && decode_smem_bytes(cfg.k_bits, cfg.v_bits, stages, any_seal) > c->max_smem) --stages;
+    if (decode_smem_bytes(cfg.k_bits, cfg.v_bits, stages, any_seal) > c->max_smem) {
         for (int32_t s : taken) c->free_slots.push_back(s);
         return KVARN_ECAPACITY;
     }
