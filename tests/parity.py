@@ -52,10 +52,14 @@ def check_seal(x_half: np.ndarray, rec_gpu: np.ndarray, bits: int, side: int, sc
     rec_o, a_o, c_o = oracle.seal(x_half, bits, side, iters=iters, return_scales=True)
     delta_g, m_g, a16_g, c16_g = oracle.read_header(rec_gpu)
     if scales_gpu is not None:
+        # Only values that fp16 can hold matter: beyond 65504 the stored scale saturates and
+        # below 2^-24 it flushes to zero (degenerate inputs on which Sinkhorn diverges drive
+        # the unrounded fp32 scales out of range). Those are checked through the stored fp16.
         a_g = np.asarray(scales_gpu[:128], np.float64)
         c_g = np.asarray(scales_gpu[128:], np.float64)
-        assert np.all(np.abs(a_g - a_o) <= SCALE_RTOL * np.abs(a_o)), f"{label}: token scales"
-        assert np.all(np.abs(c_g - c_o) <= SCALE_RTOL * np.abs(c_o)), f"{label}: channel scales"
+        for name, got, ref in (("token", a_g, a_o), ("channel", c_g, c_o)):
+            inr = (ref >= 2.0 ** -24) & (ref <= 65504.0)
+            assert np.all(np.abs(got[inr] - ref[inr]) <= SCALE_RTOL * np.abs(ref[inr])), f"{label}: {name} scales"
     for name, got, ref in (("a", a16_g, a_o), ("c", c16_g, c_o)):
         want = np.minimum(ref, 65504.0).astype(np.float16).astype(np.float64)
         bad = got != want
