@@ -151,6 +151,24 @@ kvarn_status kvarn_decode_step(kvarn_cache* cache, int32_t layer, int32_t n_seqs
                                const void* k, const void* v, const void* q, void* out, float softmax_scale,
                                void* stream);
 
+/* Decode attention as kvarn_decode_attention, for callers that cannot allocate device
+ * memory: a plugin inside a serving engine that owns all device memory through its own
+ * pool and forbids cudaMalloc, or a process under a hard device-memory cap, still has
+ * the cache's block and its q/out buffers, but cannot get a fresh allocation for the
+ * split-K scratch (partial softmax states and merge tickets). This call places that scratch in a fixed
+ * static device array of the library instead; it allocates and frees nothing.
+ * The KVarN pages have no counterpart of this call; it is an interface addition.
+ * Limit: max_seqs * num_kv_heads of the cache <= 128 (the array holds 128 blocks of
+ * 34 partial states, 9.2 MB per GPU, kept until the process exits); a larger cache is
+ * rejected with KVARN_ECAPACITY and a message in kvarn_last_error.
+ * The first call on a device looks up the array's device address (cudaGetSymbolAddress,
+ * with that device current); make that first call before any stream capture.
+ * Every call clears the array's tickets (an async memset on `stream`) and then reuses
+ * the partials left by the previous call, so calls that overlap on the GPU (other
+ * streams, other caches, other threads) race: order them on one stream. */
+kvarn_status kvarn_decode_attention_noalloc(kvarn_cache* cache, int32_t layer, int32_t n_seqs, const int32_t* seq_ids,
+                                            const void* q, void* out, float softmax_scale, void* stream);
+
 /* Convert one sealed group matrix to a standard layout ("others convert to a
  * standard cache layout first", anbeeld.com 2.1): out = yhat (frame 1, rotated) or
  * yhat * H (frame 0, original), [128 tokens][128 channels], fp32 if out_fp32 else

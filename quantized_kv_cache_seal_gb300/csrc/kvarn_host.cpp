@@ -7,6 +7,7 @@
 // (the tail) stays exact. The host mirror decides every seal and slot without
 // reading anything back from the device.
 #include <algorithm>
+#include <atomic>
 #include <cmath>
 #include <cstdio>
 #include <cstring>
@@ -169,8 +170,16 @@ kvarn_status schedule(kvarn_cache* c, DecodeParams& p) {
     return KVARN_OK;
 }
 
+// Split-K workspace placed outside the cache's device block (the allocation-free call).
+struct WorkspaceOverride {
+    void* partials;
+    void* tickets;
+    uint32_t epoch;
+};
+
 kvarn_status run_decode(kvarn_cache* c, int32_t layer, int32_t n_seqs, const int32_t* seq_ids, const void* k,
-                        const void* v, const void* q, void* out, float scale, void* stream, bool step) {
+                        const void* v, const void* q, void* out, float scale, void* stream, bool step,
+                        const WorkspaceOverride* ws = nullptr) {
     kvarn_status st = check_ids(c, layer, n_seqs, seq_ids);
     if (st) return st;
     if (n_seqs > kMaxBatch) return KVARN_ECAPACITY;
@@ -251,7 +260,14 @@ kvarn_status run_decode(kvarn_cache* c, int32_t layer, int32_t n_seqs, const int
         return KVARN_ECAPACITY;
     }
     p.stages = stages;
-    p.epoch = ++c->epoch;
+    if (ws) {
+        // offsets from the cache base that land on the static workspace (modulo 2^64)
+        p.lay.partials = (size_t)((uintptr_t)ws->partials - (uintptr_t)c->base);
+        p.lay.tickets = (size_t)((uintptr_t)ws->tickets - (uintptr_t)c->base);
+        p.epoch = ws->epoch;
+    } else {
+        p.epoch = ++c->epoch;
+    }
     if (!c->host_only) {
         st = ensure_init(c, stream);
         if (st) return st;
@@ -419,6 +435,33 @@ kvarn_status kvarn_decode_step(kvarn_cache* c, int32_t layer, int32_t n_seqs, co
                                const void* k, const void* v, const void* q, void* out, float softmax_scale,
                                void* stream) {
     return run_decode(c, layer, n_seqs, seq_ids, k, v, q, out, softmax_scale, stream, true);
+}
+
+// Decode attention whose split-K scratch lives in the library's static device array
+// (see kvarn_decode_attention_noalloc in kvarn.h). Nothing is allocated: the array is
+// fetched per device, its tickets cleared with an async memset, and every call gets an
+// epoch of its own so that partials left by earlier calls are never merged.
+kvarn_status kvarn_decode_attention_noalloc(kvarn_cache* c, int32_t layer, int32_t n_seqs, const int32_t* seq_ids,
+                                            const void* q, void* out, float softmax_scale, void* stream) {
+    if (!c) return KVARN_EINVAL;
+    int max_blocks = static_workspace_blocks();
+    if ((int64_t)c->cfg.max_seqs * c->cfg.num_kv_heads > max_blocks) {
+        std::snprintf(g_last_error, sizeof(g_last_error),
+                      "max_seqs * num_kv_heads = %lld exceeds the static workspace (%d blocks)",
+                      (long long)c->cfg.max_seqs * c->cfg.num_kv_heads, max_blocks);
+        return KVARN_ECAPACITY;
+    }
+    if (c->host_only) return KVARN_EINVAL;
+    WorkspaceOverride ws{};
+    int rc = static_workspace(&ws.partials, &ws.tickets);
+    if (rc) { set_cuda_error(rc, "static workspace address"); return KVARN_ECUDA; }
+    kvarn_status st = check_ids(c, layer, n_seqs, seq_ids);
+    if (st) return st;
+    rc = clear_static_tickets(ws.tickets, stream);
+    if (rc) { set_cuda_error(rc, "static workspace clear"); return KVARN_ECUDA; }
+    static std::atomic<uint32_t> epochs{0x80000000u};
+    ws.epoch = epochs.fetch_add(1) + 1;
+    return run_decode(c, layer, n_seqs, seq_ids, nullptr, nullptr, q, out, softmax_scale, stream, false, &ws);
 }
 
 kvarn_status kvarn_group_record(const kvarn_cache* c, int32_t layer, int32_t seq_id, int32_t group,

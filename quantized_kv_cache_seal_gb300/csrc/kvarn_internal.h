@@ -129,5 +129,9 @@ int sm_count();
 const char* cuda_error_string(int code);
 int memcpy_h2d_async(void* dst, const void* src, size_t bytes, void* stream);
 int memcpy_d2h_sync(void* dst, const void* src, size_t bytes, void* stream);
+// static split-K workspace for the allocation-free decode call (kvarn_decode.cu)
+int static_workspace_blocks();
+int static_workspace(void** partials, void** tickets);
+int clear_static_tickets(void* tickets, void* stream);
 
 }  // namespace kvarn

@@ -21,7 +21,7 @@ KVARN_FLAG_HOST_ONLY = 1
 # every entry point declared in include/kvarn.h
 EXPORTS = [
     "kvarn_record_bytes", "kvarn_cache_required_bytes", "kvarn_cache_create", "kvarn_cache_destroy",
-    "kvarn_append", "kvarn_decode_attention", "kvarn_decode_step", "kvarn_dequant_group",
+    "kvarn_append", "kvarn_decode_attention", "kvarn_decode_attention_noalloc", "kvarn_decode_step", "kvarn_dequant_group",
     "kvarn_seq_release", "kvarn_seq_length", "kvarn_group_record", "kvarn_exact_regions",
     "kvarn_cache_stats", "kvarn_seal_groups", "kvarn_check_device_error", "kvarn_status_string",
     "kvarn_last_error",
@@ -77,6 +77,7 @@ def load(build_if_missing: bool = True):
     L.kvarn_cache_destroy.restype = None
     L.kvarn_append.argtypes = [P, I32, I32, IP, IP, P, P, P]
     L.kvarn_decode_attention.argtypes = [P, I32, I32, IP, P, P, F, P]
+    L.kvarn_decode_attention_noalloc.argtypes = [P, I32, I32, IP, P, P, F, P]
     L.kvarn_decode_step.argtypes = [P, I32, I32, IP, P, P, P, P, F, P]
     L.kvarn_dequant_group.argtypes = [P, I32, I32, I32, I32, I32, I32, I32, P, P]
     L.kvarn_seq_release.argtypes = [P, I32]
@@ -165,6 +166,12 @@ def kvarn_append(handle, layer, seq_ids, n_tokens, k, v, stream=None):
 def kvarn_decode_attention(handle, layer, seq_ids, q, out, softmax_scale, stream=None):
     _check(load().kvarn_decode_attention(handle, layer, len(seq_ids), _ints(seq_ids), _ptr(q), _ptr(out),
                                          float(softmax_scale), _stream(stream)), "kvarn_decode_attention")
+
+
+def kvarn_decode_attention_noalloc(handle, layer, seq_ids, q, out, softmax_scale, stream=None):
+    _check(load().kvarn_decode_attention_noalloc(handle, layer, len(seq_ids), _ints(seq_ids), _ptr(q), _ptr(out),
+                                                 float(softmax_scale), _stream(stream)),
+           "kvarn_decode_attention_noalloc")
 
 
 def kvarn_decode_step(handle, layer, seq_ids, k, v, q, out, softmax_scale, stream=None):
