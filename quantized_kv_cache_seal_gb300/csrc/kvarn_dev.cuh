@@ -111,6 +111,13 @@ struct SealSmem {
 
 __device__ __forceinline__ int ypad(int j) { return j + ((j >> 6) << 2); }
 
+// Bounds on the squared Sinkhorn scales kept in fp32. Rows of fp16 data have squared
+// scales far inside them; only inputs on which the alternating normalisation diverges
+// (every row with a single non-zero rotated entry) reach them, and there the stored
+// fp16 scales saturate or flush either way. With A = Y^2 < 2^40, A / bound stays finite.
+constexpr float kSqMax = 1.2089258196146292e24f;   // 2^80
+constexpr float kSqMin = 8.271806125530277e-25f;   // 2^-80
+
 template <int B>
 __device__ __forceinline__ void pack64_store(const int (&q)[64], uint8_t* dst) {
     // 64 codes of B bits, least significant first, into 2B little-endian words
@@ -201,7 +208,8 @@ __device__ void seal_matrix(const Rows& rows, int bits, int which, int iters, ui
         float p = p0 + p1;
         p += __shfl_xor_sync(0xffffffffu, p, 1);
         a2 = p * (1.0f / 128.0f);
-        if (a2 == 0.0f) a2 = 1.0f;
+        // zero row keeps factor 1; the clamp only binds on divergent inputs (see kSqMax)
+        a2 = a2 == 0.0f ? 1.0f : fminf(fmaxf(a2, kSqMin), kSqMax);
         if (h == 0) S.v[ypad(i)] = 1.0f / a2;
         named_bar(bar_id, 256);
         p0 = 0.f;
@@ -218,7 +226,7 @@ __device__ void seal_matrix(const Rows& rows, int bits, int which, int iters, ui
         p = p0 + p1;
         p += __shfl_xor_sync(0xffffffffu, p, 1);
         c2 = p * (1.0f / 128.0f);
-        if (c2 == 0.0f) c2 = 1.0f;
+        c2 = c2 == 0.0f ? 1.0f : fminf(fmaxf(c2, kSqMin), kSqMax);
         if (hc == 0) S.u[ypad(j)] = 1.0f / c2;
         named_bar(bar_id, 256);
     }
