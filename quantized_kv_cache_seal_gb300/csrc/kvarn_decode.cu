@@ -41,12 +41,12 @@ namespace kvarn {
 
 namespace {
 
-constexpr int kE = 14;       // query operand exponent: |B| <= 2^14
-constexpr int kEV = 14;      // weight operand exponent
+constexpr int kEV = 13;      // weight operand exponent: |B| < 2^14
 constexpr int kXbHead = 88;  // exchange buffer words per head (bank-conflict-free stride)
 constexpr int kXbWarp = 4 * kXbHead;
 constexpr int kMrgFloats = 8 + 512;  // per warp: m[4], l[4], acc[4][128]
-constexpr int kConsumers = 256;
+constexpr int kWarps = kDecodeThreads / 32;  // 12
+constexpr int kConsumers = kDecodeThreads;
 constexpr int kMaxDevices = 64;
 #define kNegInf (-__int_as_float(0x7f800000))
 
@@ -155,6 +155,7 @@ struct Smem {
     uint8_t* stages;
     uint64_t* full;
     float* qrot;    // [4][128] rotated query / its max
+    float4* bqs;    // [8][32]: lane l's query operand base, q_hat * 2^-ex, in fragment order
     float* qmax;    // [4]
     float* xbuf;    // [8 warps][kXbWarp] (half2 words)
     float* mrg;     // [8 warps][kMrgFloats], also exact-part and final-merge scratch
@@ -234,7 +235,7 @@ __device__ void final_merge(const DecodeParams& p, const Smem& sm, int ci, int k
     }
     named_bar(1, kConsumers);
     const int nv = list[0];
-    const int h = t >> 6, jj = 2 * (t & 63);
+    const int h = (t >> 6) & 3, jj = 2 * (t & 63);
     float M = kNegInf;
     for (int k = 0; k < nv; ++k) M = fmaxf(M, hdr[8 * list[1 + k] + h]);
     float l = 0.f, r0 = 0.f, r1 = 0.f, x0 = 0.f, x1 = 0.f;
@@ -258,11 +259,13 @@ __device__ void final_merge(const DecodeParams& p, const Smem& sm, int ci, int k
     float* rot = sm.mrg;        // [4][128]
     float* ex = sm.mrg + 512;   // [4][128]
     float* ls = sm.mrg + 1024;  // [4]
-    rot[128 * h + jj] = r0;
-    rot[128 * h + jj + 1] = r1;
-    ex[128 * h + jj] = x0;
-    ex[128 * h + jj + 1] = x1;
-    if ((t & 63) == 0) ls[h] = l;
+    if (t < 256) {
+        rot[128 * h + jj] = r0;
+        rot[128 * h + jj + 1] = r1;
+        ex[128 * h + jj] = x0;
+        ex[128 * h + jj + 1] = x1;
+        if ((t & 63) == 0) ls[h] = l;
+    }
     named_bar(1, kConsumers);
     const int w = t >> 5, lane = t & 31;
     if (w < 4) {
@@ -274,7 +277,7 @@ __device__ void final_merge(const DecodeParams& p, const Smem& sm, int ci, int k
         for (int k = 0; k < 4; ++k) rot[128 * w + 4 * lane + k] = v[k];
     }
     named_bar(1, kConsumers);
-    if (h < p.r) {
+    if (t < 256 && h < p.r) {
         const float lh = ls[h];
         const float inv = lh > 0.f ? 1.0f / lh : 0.f;
         __half2 o = __floats2half2_rn((ex[128 * h + jj] + rot[128 * h + jj]) * inv,
@@ -329,7 +332,7 @@ __device__ void exact_item(const DecodeParams& p, const Smem& sm, int ci, int kv
     float* qraw = sm.xbuf;           // [4][128]
     float* sc = sm.xbuf + 512;       // [4][256]
     float* red = sm.xbuf + 1536;     // [16]
-    float* part = sm.mrg;            // [8 warps][4][128]
+    float* part = sm.mrg;            // [kWarps][4][128]
     for (int k = t; k < 512; k += kConsumers) {
         const int h = k >> 7, j = k & 127;
         qraw[k] = h < p.r ? half_bits_to_float(p.q[((size_t)ci * p.hq + (size_t)kvh * p.r + h) * 128 + j]) : 0.f;
@@ -371,16 +374,18 @@ __device__ void exact_item(const DecodeParams& p, const Smem& sm, int ci, int kv
 #pragma unroll
         for (int h = 0; h < 4; ++h) s[h] = d[h] * p.scale_log2;
     }
+    if (t < 256) {
 #pragma unroll
-    for (int h = 0; h < 4; ++h) sc[256 * h + t] = s[h];
+        for (int h = 0; h < 4; ++h) sc[256 * h + t] = s[h];
+    }
     named_bar(1, kConsumers);
-    // per-head max and sum: 64 threads per head, 4 entries each
+    // per-head max and sum: 64 threads per head, 4 entries each (threads >= 256 idle)
     {
-        const int h = t >> 6, k0 = 4 * (t & 63);
+        const int h = (t >> 6) & 3, k0 = 4 * (t & 63);
         float m = fmaxf(fmaxf(sc[256 * h + k0], sc[256 * h + k0 + 1]), fmaxf(sc[256 * h + k0 + 2], sc[256 * h + k0 + 3]));
 #pragma unroll
         for (int o = 16; o > 0; o >>= 1) m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, o));
-        if (lane == 0) red[2 * h + (w & 1)] = m;
+        if (lane == 0 && t < 256) red[2 * h + (w & 1)] = m;
         named_bar(1, kConsumers);
         m = fmaxf(red[2 * h], red[2 * h + 1]);
         float sum = 0.f;
@@ -388,14 +393,14 @@ __device__ void exact_item(const DecodeParams& p, const Smem& sm, int ci, int kv
         for (int k = 0; k < 4; ++k) {
             float v = sc[256 * h + k0 + k];
             float pv = (m == kNegInf) ? 0.f : exp2f(v - m);
-            sc[256 * h + k0 + k] = pv;
+            if (t < 256) sc[256 * h + k0 + k] = pv;
             sum += pv;
         }
 #pragma unroll
         for (int o = 16; o > 0; o >>= 1) sum += __shfl_xor_sync(0xffffffffu, sum, o);
-        if (lane == 0) red[8 + 2 * h + (w & 1)] = sum;
+        if (lane == 0 && t < 256) red[8 + 2 * h + (w & 1)] = sum;
         named_bar(1, kConsumers);
-        if ((t & 63) == 0) {
+        if ((t & 63) == 0 && t < 256) {
             float* P = partial_ptr(p, e.seq * p.hkv + kvh, kSlotExact);
             P[4 + h] = m;
             P[8 + h] = red[8 + 2 * h] + red[8 + 2 * h + 1];
@@ -408,11 +413,11 @@ __device__ void exact_item(const DecodeParams& p, const Smem& sm, int ci, int kv
         for (int h = 0; h < 4; ++h)
 #pragma unroll
             for (int c = 0; c < 4; ++c) acc[h][c] = 0.f;
-        for (int k0 = w; k0 < n_ex; k0 += 32) {
+        for (int k0 = w; k0 < n_ex; k0 += 4 * kWarps) {
             uint2 vv[4];
 #pragma unroll
             for (int u = 0; u < 4; ++u) {
-                const int k = k0 + 8 * u;
+                const int k = k0 + kWarps * u;
                 vv[u] = make_uint2(0u, 0u);
                 if (k < n_ex) {
                     const uint16_t* row = k < e.n_sink ? sink_v + (size_t)k * 128 : tail_v + (size_t)(k - e.n_sink) * 128;
@@ -421,7 +426,7 @@ __device__ void exact_item(const DecodeParams& p, const Smem& sm, int ci, int kv
             }
 #pragma unroll
             for (int u = 0; u < 4; ++u) {
-                const int k = k0 + 8 * u;
+                const int k = k0 + kWarps * u;
                 if (k < n_ex) {
                     const float2 va = __half22float2(bits_h2(vv[u].x)), vb = __half22float2(bits_h2(vv[u].y));
 #pragma unroll
@@ -440,22 +445,28 @@ __device__ void exact_item(const DecodeParams& p, const Smem& sm, int ci, int kv
             *reinterpret_cast<float4*>(part + (w * 4 + h) * 128 + 4 * lane) =
                 make_float4(acc[h][0], acc[h][1], acc[h][2], acc[h][3]);
         named_bar(1, kConsumers);
-        const int h = t >> 6, jj = 2 * (t & 63);
-        float a0 = 0.f, a1 = 0.f;
+        if (t < 256) {
+            const int h = t >> 6, jj = 2 * (t & 63);
+            float a0 = 0.f, a1 = 0.f;
 #pragma unroll
-        for (int k = 0; k < 8; ++k) {
-            a0 += part[(k * 4 + h) * 128 + jj];
-            a1 += part[(k * 4 + h) * 128 + jj + 1];
+            for (int k = 0; k < kWarps; ++k) {
+                a0 += part[(k * 4 + h) * 128 + jj];
+                a1 += part[(k * 4 + h) * 128 + jj + 1];
+            }
+            float* P = partial_ptr(p, e.seq * p.hkv + kvh, kSlotExact);
+            *reinterpret_cast<float2*>(P + 12 + 128 * h + jj) = make_float2(a0, a1);
+            if (t == 0) P[0] = __int_as_float((int)p.epoch);
         }
-        float* P = partial_ptr(p, e.seq * p.hkv + kvh, kSlotExact);
-        *reinterpret_cast<float2*>(P + 12 + 128 * h + jj) = make_float2(a0, a1);
-        if (t == 0) P[0] = __int_as_float((int)p.epoch);
     }
     publish(p, sm, ci, kvh);
 }
 
-// Rotate the query of a block: qrot = (q H) / max|q H| per head, qmax = that max.
+// Rotate the query of a block: qrot = (q H) / max|q H| per head, qmax = that max; then
+// the table of each lane's query operand base q_hat(head g>>1, channel) * 2^-ex in the
+// pair order of its MMA fragments (the codes' power-of-two offsets folded in).
+template <int KB>
 __device__ void setup_query(const DecodeParams& p, const Smem& sm, int ci, int kvh) {
+    using CK = Codes<KB>;
     const int t = threadIdx.x, w = t >> 5, lane = t & 31;
     if (w < 4) {
         float v[4] = {0.f, 0.f, 0.f, 0.f};
@@ -474,6 +485,23 @@ __device__ void setup_query(const DecodeParams& p, const Smem& sm, int ci, int k
 #pragma unroll
         for (int k = 0; k < 4; ++k) sm.qrot[128 * w + 4 * lane + k] = v[k] * inv;
         if (lane == 0) sm.qmax[w] = mx;
+    }
+    named_bar(1, kConsumers);
+    if (t < 256) {
+        // entry q (0..7) of lane l: pairs P = 2q, 2q+1 of lane l = (g, tq)
+        const int q = t >> 5, g = lane >> 2, tq = lane & 3;
+        const float* qh = sm.qrot + 128 * (g >> 1);
+        float vals[4];
+#pragma unroll
+        for (int e = 0; e < 2; ++e) {
+            const int P = 2 * q + e;
+            const int x = P % CK::HALF;
+            const int c0 = 32 * tq + CK::CPW * (P / CK::HALF) + x;
+            const float sc = __int_as_float((127 - CK::ex(x)) << 23);  // 2^-ex
+            vals[2 * e] = qh[c0] * sc;
+            vals[2 * e + 1] = qh[c0 + CK::HALF] * sc;
+        }
+        sm.bqs[q * 32 + lane] = make_float4(vals[0], vals[1], vals[2], vals[3]);
     }
     named_bar(1, kConsumers);
 }
@@ -502,13 +530,13 @@ __device__ __forceinline__ uint32_t pair_operand(const uint32_t* w, int P) {
 // code words live in registers.
 template <int B>
 struct TileGroup {
-    static constexpr int TG = B == 2 ? 8 : (B == 4 ? 4 : 2);
+    static constexpr int TG = B == 8 ? 2 : 4;
 };
 
 // Process one sealed group pair held in shared memory (K record, then V record).
 template <int KB, int VB>
-__device__ __forceinline__ void process_group(const DecodeParams& p, const uint8_t* rec, const float (&bq)[16][2],
-                                              float qm, float* xb, WarpState& st, int g, int tq) {
+__device__ __forceinline__ void process_group(const DecodeParams& p, const uint8_t* rec, const float4* bqs,
+                                              float qm, float* xb, WarpState& st, int g, int tq, int lane) {
     using CK = Codes<KB>;
     using CV = Codes<VB>;
     const uint8_t* krec = rec;
@@ -520,9 +548,10 @@ __device__ __forceinline__ void process_group(const DecodeParams& p, const uint8
     const uint16_t* aK = reinterpret_cast<const uint16_t*>(krec + 16);
     const uint16_t* aV = reinterpret_cast<const uint16_t*>(vrec + 16);
     const uint16_t* cV = reinterpret_cast<const uint16_t*>(vrec + 272);
-    // ---- query operand of this group: q' c_K, scaled, split into f16 high/low parts
+    // ---- query operand of this group: q_hat * c_K * 2^-ex, split into f16 high / low parts.
+    // |q_hat| <= 1, c_K <= 65504 and 2^-ex <= 1, so the operand can never overflow f16.
     uint32_t bk[16];
-    float kappa, sumqc;
+    float sumqc;
     {
         const uint4* cp = reinterpret_cast<const uint4*>(krec + 272 + 64 * tq);
         uint32_t cw[16];
@@ -531,13 +560,12 @@ __device__ __forceinline__ void process_group(const DecodeParams& p, const uint8
             uint4 v = cp[k];
             cw[4 * k] = v.x; cw[4 * k + 1] = v.y; cw[4 * k + 2] = v.z; cw[4 * k + 3] = v.w;
         }
-        __half2 mh = bits_h2(cw[0]);
+        float bq[32];
 #pragma unroll
-        for (int k = 1; k < 16; ++k) mh = __hmax2(mh, bits_h2(cw[k]));
-        float mc = fmaxf(__low2float(mh), __high2float(mh));
-        mc = fmaxf(mc, __shfl_xor_sync(0xffffffffu, mc, 1));
-        mc = fmaxf(mc, __shfl_xor_sync(0xffffffffu, mc, 2));
-        kappa = 1.0f / mc;
+        for (int q = 0; q < 8; ++q) {
+            const float4 v = bqs[q * 32 + lane];
+            bq[4 * q] = v.x; bq[4 * q + 1] = v.y; bq[4 * q + 2] = v.z; bq[4 * q + 3] = v.w;
+        }
         const bool lo_part = (g & 1) != 0;
         float sum = 0.f;
 #pragma unroll
@@ -545,24 +573,19 @@ __device__ __forceinline__ void process_group(const DecodeParams& p, const uint8
             const int x = P % CK::HALF;
             const int c0 = CK::CPW * (P / CK::HALF) + x;
             const int c1 = c0 + CK::HALF;
-            const float cf0 = __half2float(reinterpret_cast<const __half*>(cw)[c0]);
-            const float cf1 = __half2float(reinterpret_cast<const __half*>(cw)[c1]);
-            const float f0 = bq[P][0] * cf0 * kappa;
-            const float f1 = bq[P][1] * cf1 * kappa;
+            const float f0 = bq[2 * P] * __half2float(reinterpret_cast<const __half*>(cw)[c0]);
+            const float f1 = bq[2 * P + 1] * __half2float(reinterpret_cast<const __half*>(cw)[c1]);
             const __half2 hi = __floats2half2_rn(f0, f1);
-            if (lo_part) {
-                const float2 hf = __half22float2(hi);
-                bk[P] = h2_bits(__floats2half2_rn(f0 - hf.x, f1 - hf.y));
-            } else {
-                bk[P] = h2_bits(hi);
-            }
-            const float sc = __int_as_float((127 + CK::ex(x) - kE) << 23);  // 2^(ex - E)
+            const float2 hf = __half22float2(hi);
+            const uint32_t lo = h2_bits(__floats2half2_rn(f0 - hf.x, f1 - hf.y));
+            bk[P] = lo_part ? lo : h2_bits(hi);
+            const float sc = __int_as_float((127 + CK::ex(x)) << 23);  // 2^ex: back to q_hat * c_K
             sum = fmaf(f0 + f1, sc, sum);
         }
         sum += __shfl_xor_sync(0xffffffffu, sum, 1);
         sum += __shfl_xor_sync(0xffffffffu, sum, 2);
         // lane 8 tq holds the sum of head tq (its column head is (2 tq) >> 1 = tq)
-        sumqc = __shfl_sync(0xffffffffu, sum, 8 * tq) / kappa;
+        sumqc = __shfl_sync(0xffffffffu, sum, 8 * tq);
     }
     // ---- scores of the 16 tokens this thread holds (head tq)
     float S[8][2];
@@ -595,9 +618,9 @@ __device__ __forceinline__ void process_group(const DecodeParams& p, const uint8
             }
         }
     }
-    const float alpha = p.scale_log2 * qm * dK * (float)(1 << (24 - kE)) / kappa;
+    const float alpha = p.scale_log2 * qm * dK * 16777216.0f;  // codes enter as code * 2^(ex-24)
     const float beta = p.scale_log2 * qm * mK * sumqc;
-    float gmax = kNegInf, amax = 0.f;
+    float gmax = kNegInf;
     float av[8][2];
 #pragma unroll
     for (int mt = 0; mt < 8; ++mt) {
@@ -607,19 +630,26 @@ __device__ __forceinline__ void process_group(const DecodeParams& p, const uint8
         gmax = fmaxf(gmax, fmaxf(S[mt][0], S[mt][1]));
         av[mt][0] = half_bits_to_float(aV[t0]);
         av[mt][1] = half_bits_to_float(aV[t1]);
-        amax = fmaxf(amax, fmaxf(av[mt][0], av[mt][1]));
+    }
+    // largest V token scale of the group from its bit patterns (all >= 0): lane l reads 4
+    uint32_t amaxb;
+    {
+        const uint2 ab = reinterpret_cast<const uint2*>(aV)[lane];
+        amaxb = __vmaxu2(ab.x, ab.y);
+        amaxb = max(amaxb & 0xffffu, amaxb >> 16);
     }
 #pragma unroll
-    for (int o = 4; o < 32; o <<= 1) {
-        gmax = fmaxf(gmax, __shfl_xor_sync(0xffffffffu, gmax, o));
-        amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, o));
-    }
+    for (int o = 1; o < 32; o <<= 1) amaxb = max(amaxb, __shfl_xor_sync(0xffffffffu, amaxb, o));
+#pragma unroll
+    for (int o = 4; o < 32; o <<= 1) gmax = fmaxf(gmax, __shfl_xor_sync(0xffffffffu, gmax, o));
     const float mnew = fmaxf(st.m, gmax);
     const float corr = fast_exp2(st.m - mnew);
     st.m = mnew;
-    const float rho = amax > 0.f ? 1.0f / amax : 1.0f;
+    // rho = 2^(15 - e) puts every aV * rho in [0, 2): e = biased exponent of the largest aV
+    const int ebits = max((int)(amaxb >> 10) & 31, 1);
+    const float rho = __int_as_float((127 + 15 - ebits) << 23);
     const int xv = g % CV::HALF;
-    const float sv = __int_as_float((127 + kEV - CV::ex(xv)) << 23) * rho;  // 2^(EV - ex) / max aV
+    const float sv = __int_as_float((127 + kEV - CV::ex(xv)) << 23) * rho;  // 2^(EV - ex) * rho
     const float svi = __int_as_float((127 - kEV + CV::ex(xv)) << 23);       // 2^(ex - EV)
     float lsum = 0.f, wsum = 0.f;
 #pragma unroll
@@ -698,28 +728,30 @@ __device__ void write_item_partial(const DecodeParams& p, const Smem& sm, const 
         M[8 + 128 * tq + 16 * mt + g + 8] = st.acc[mt][1];
     }
     named_bar(1, kConsumers);
-    const int h = t >> 6, jj = 2 * (t & 63);
-    float mx = kNegInf;
+    if (t < 256) {
+        const int h = t >> 6, jj = 2 * (t & 63);
+        float mx = kNegInf;
 #pragma unroll
-    for (int k = 0; k < 8; ++k) mx = fmaxf(mx, sm.mrg[k * kMrgFloats + h]);
-    float ls = 0.f, a0 = 0.f, a1 = 0.f;
+        for (int k = 0; k < kWarps; ++k) mx = fmaxf(mx, sm.mrg[k * kMrgFloats + h]);
+        float ls = 0.f, a0 = 0.f, a1 = 0.f;
 #pragma unroll
-    for (int k = 0; k < 8; ++k) {
-        const float* Mk = sm.mrg + k * kMrgFloats;
-        const float mk = Mk[h];
-        if (mk == kNegInf) continue;
-        const float wgt = exp2f(mk - mx);
-        ls = fmaf(wgt, Mk[4 + h], ls);
-        a0 = fmaf(wgt, Mk[8 + 128 * h + jj], a0);
-        a1 = fmaf(wgt, Mk[8 + 128 * h + jj + 1], a1);
+        for (int k = 0; k < kWarps; ++k) {
+            const float* Mk = sm.mrg + k * kMrgFloats;
+            const float mk = Mk[h];
+            if (mk == kNegInf) continue;
+            const float wgt = exp2f(mk - mx);
+            ls = fmaf(wgt, Mk[4 + h], ls);
+            a0 = fmaf(wgt, Mk[8 + 128 * h + jj], a0);
+            a1 = fmaf(wgt, Mk[8 + 128 * h + jj + 1], a1);
+        }
+        float* P = partial_ptr(p, blk, slot);
+        *reinterpret_cast<float2*>(P + 12 + 128 * h + jj) = make_float2(a0, a1);
+        if ((t & 63) == 0) {
+            P[4 + h] = mx;
+            P[8 + h] = ls;
+        }
+        if (t == 0) P[0] = __int_as_float((int)p.epoch);
     }
-    float* P = partial_ptr(p, blk, slot);
-    *reinterpret_cast<float2*>(P + 12 + 128 * h + jj) = make_float2(a0, a1);
-    if ((t & 63) == 0) {
-        P[4 + h] = mx;
-        P[8 + h] = ls;
-    }
-    if (t == 0) P[0] = __int_as_float((int)p.epoch);
 }
 
 __device__ __forceinline__ const uint8_t* group_src(const DecodeParams& p, int seq, int kvh, int g) {
@@ -779,8 +811,8 @@ __device__ __forceinline__ void issue_group(const DecodeParams& p, const Smem& s
     bulk_g2s(sm.stages + (size_t)s * pair, src, pair, sm.full + s);
 }
 
-// One CTA of 8 warps per SM. Stage ring: group gn lives in stage gn % S and is
-// processed by warp gn % 8; the warp that finishes with a stage issues the copy of
+// One CTA of 12 warps per SM. Stage ring: group gn lives in stage gn % S and is
+// processed by warp gn % 12; the warp that finishes with a stage issues the copy of
 // group gn + S into it, so no stage needs a release barrier. Seal items of the CTA run
 // first, with their scratch aliased onto the (still empty) stage ring.
 template <int KB, int VB>
@@ -803,8 +835,10 @@ __global__ void __launch_bounds__(kDecodeThreads, 1) decode_kernel(const __grid_
         off += 16;
         sm.flag = reinterpret_cast<int*>(smem_raw + off);
         off += 16;
+        sm.bqs = reinterpret_cast<float4*>(smem_raw + off);
+        off += 8 * 32 * 16;
         sm.xbuf = reinterpret_cast<float*>(smem_raw + off);
-        off += 8 * kXbWarp * 4;
+        off += kWarps * kXbWarp * 4;
         sm.mrg = reinterpret_cast<float*>(smem_raw + off);
         sm.seal = reinterpret_cast<SealSmem*>(smem_raw);
     }
@@ -829,12 +863,14 @@ __global__ void __launch_bounds__(kDecodeThreads, 1) decode_kernel(const __grid_
             const size_t sl = (size_t)e.seq * p.num_layers + p.layer;
             const size_t rows0 = (sl * p.hkv + it.kvh) * 128;
             uint8_t* dst = p.base + p.lay.pool + (size_t)e.seal_slot * p.slot_bytes + (size_t)it.kvh * pair;
-            SealRows rk{reinterpret_cast<const uint16_t*>(p.base + p.lay.tail_k) + rows0 * 128,
-                        p.k_new + ((size_t)it.ci * p.hkv + it.kvh) * 128};
-            seal_matrix(rk, p.k_bits, 0, p.iters, dst, nullptr, *sm.seal, 1);
-            SealRows rv{reinterpret_cast<const uint16_t*>(p.base + p.lay.tail_v) + rows0 * 128,
-                        p.v_new + ((size_t)it.ci * p.hkv + it.kvh) * 128};
-            seal_matrix(rv, p.v_bits, 1, p.iters, dst + p.rec_k, nullptr, *sm.seal, 1);
+            if (t < kSealThreads) {  // the seal runs on 8 warps (barrier 2); the others wait below
+                SealRows rk{reinterpret_cast<const uint16_t*>(p.base + p.lay.tail_k) + rows0 * 128,
+                            p.k_new + ((size_t)it.ci * p.hkv + it.kvh) * 128};
+                seal_matrix(rk, p.k_bits, 0, p.iters, dst, nullptr, *sm.seal, 2);
+                SealRows rv{reinterpret_cast<const uint16_t*>(p.base + p.lay.tail_v) + rows0 * 128,
+                            p.v_new + ((size_t)it.ci * p.hkv + it.kvh) * 128};
+                seal_matrix(rv, p.v_bits, 1, p.iters, dst + p.rec_k, nullptr, *sm.seal, 2);
+            }
             if (t == 0 && it.kvh == 0) {
                 int32_t* table = reinterpret_cast<int32_t*>(p.base + p.lay.block_table);
                 table[sl * p.max_groups + e.seal_group] = e.seal_slot;
@@ -850,7 +886,7 @@ __global__ void __launch_bounds__(kDecodeThreads, 1) decode_kernel(const __grid_
     // ---- 2. prologue: the first S groups of the stream
     GroupCursor cur;
     cur.init(lo);
-    for (uint32_t gn = w; gn < (uint32_t)p.stages; gn += 8) {
+    for (uint32_t gn = w; gn < (uint32_t)p.stages; gn += kWarps) {
         if (lane == 0) issue_group(p, sm, cur, hi, gn);
         __syncwarp();
     }
@@ -860,7 +896,6 @@ __global__ void __launch_bounds__(kDecodeThreads, 1) decode_kernel(const __grid_
     int64_t u = lo;
     Item it;
     uint32_t n = 0;
-    using CK = Codes<KB>;
     while (next_item(p, u, hi, it)) {
         const SeqEntry& e = p.seqs[it.ci];
         const int blk = e.seq * p.hkv + it.kvh;
@@ -880,20 +915,7 @@ __global__ void __launch_bounds__(kDecodeThreads, 1) decode_kernel(const __grid_
                 slot = kPartialSlots - 1;
             }
         }
-        setup_query(p, sm, it.ci, it.kvh);
-        // loop-invariant query operand base: q_hat(head g>>1, channel) * 2^(E - ex)
-        float bq[16][2];
-        {
-            const float* qh = sm.qrot + 128 * (g >> 1);
-#pragma unroll
-            for (int P2 = 0; P2 < 16; ++P2) {
-                const int x = P2 % CK::HALF;
-                const int c0 = 32 * tq + CK::CPW * (P2 / CK::HALF) + x;
-                const float sc = __int_as_float((127 + kE - CK::ex(x)) << 23);
-                bq[P2][0] = qh[c0] * sc;
-                bq[P2][1] = qh[c0 + CK::HALF] * sc;
-            }
-        }
+        setup_query<KB>(p, sm, it.ci, it.kvh);
         const float qm = sm.qmax[tq];
         WarpState st;
         st.m = kNegInf;
@@ -902,11 +924,11 @@ __global__ void __launch_bounds__(kDecodeThreads, 1) decode_kernel(const __grid_
         for (int mt = 0; mt < 8; ++mt) st.acc[mt][0] = st.acc[mt][1] = 0.f;
         float* xb = sm.xbuf + w * kXbWarp;
         const uint32_t cnt = (uint32_t)(it.g1 - it.g0);
-        for (uint32_t k = (w + 8 - (n & 7)) & 7; k < cnt; k += 8) {
+        for (uint32_t k = (w + kWarps - (n % kWarps)) % kWarps; k < cnt; k += kWarps) {
             const uint32_t gn = n + k;
             const uint32_t s = gn % p.stages;
             mbar_wait(sm.full + s, (gn / p.stages) & 1, err);
-            process_group<KB, VB>(p, sm.stages + (size_t)s * pair, bq, qm, xb, st, g, tq);
+            process_group<KB, VB>(p, sm.stages + (size_t)s * pair, sm.bqs, qm, xb, st, g, tq, lane);
             __syncwarp();
             if (lane == 0) issue_group(p, sm, cur, hi, gn + p.stages);
             __syncwarp();
@@ -946,7 +968,7 @@ int decode_smem_bytes(int k_bits, int v_bits, int stages, bool with_seal) {
     size_t off = (size_t)stages * pair;
     if (off < sizeof(SealSmem)) off = sizeof(SealSmem);
     off = (off + 15) & ~(size_t)15;
-    off += 32 * 8 + 512 * 4 + 16 + 16 + 8 * kXbWarp * 4 + 8 * kMrgFloats * 4;
+    off += 32 * 8 + 512 * 4 + 16 + 16 + 8 * 32 * 16 + kWarps * kXbWarp * 4 + kWarps * kMrgFloats * 4;
     return (int)off;
 }
 

@@ -23,7 +23,7 @@ constexpr int kSlotSeal = 1;     // partial slot of the group sealed inside a de
 constexpr int kSlotChunk0 = 2;   // first partial slot of sealed-group chunks
 constexpr int kPartialSlots = kSlotChunk0 + kMaxSpan;
 constexpr int kPartialFloats = 528;  // [0] epoch bits, [4..8) m, [8..12) l, [12..524) acc
-constexpr int kDecodeThreads = 256;  // 8 warps
+constexpr int kDecodeThreads = 384;  // 12 warps
 constexpr int kSealThreads = 256;
 
 // device error word bits
