@@ -17,7 +17,7 @@ constexpr int kHeadDim = 128;
 constexpr int kGroup = 128;
 constexpr int kSink = 128;
 constexpr int kMaxBatch = 256;   // sequences per decode call (kernel parameter table size)
-constexpr int kMaxSpan = 32;     // CTAs that may share the sealed groups of one (seq, kv head)
+constexpr int kMaxSpan = 48;     // worker warps that may share the sealed groups of one (seq, kv head)
 constexpr int kSlotExact = 0;    // partial slot of the exact (sink + tail) part
 constexpr int kSlotSeal = 1;     // partial slot of the group sealed inside a decode step
 constexpr int kSlotChunk0 = 2;   // first partial slot of sealed-group chunks
@@ -68,7 +68,7 @@ struct DecodeParams {
     const uint16_t* v_new;
     int32_t n_seqs, hq, hkv, r, k_bits, v_bits, iters, layer, num_layers, max_seqs, max_groups;
     int32_t rec_k, rec_v, slot_bytes, pool_slots;
-    int32_t stages;             // smem ring stages
+    int32_t warps;              // worker warps per CTA (<= 12)
     int32_t grid;               // CTAs
     int64_t units_total;
     uint32_t epoch;
@@ -123,7 +123,7 @@ int launch_seal_groups(const void* x, int n, int bits, int which, int iters, voi
                        void* stream);
 int launch_dequant(const uint8_t* rec, int bits, int which, int frame, int out_fp32, void* out, void* stream);
 int launch_init(uint8_t* base, const Layout& lay, void* stream);
-int decode_smem_bytes(int k_bits, int v_bits, int stages, bool with_seal);
+int decode_smem_bytes(int k_bits, int v_bits, int warps, bool with_seal);
 int max_optin_smem();
 int sm_count();
 const char* cuda_error_string(int code);
