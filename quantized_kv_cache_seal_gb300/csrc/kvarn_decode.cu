@@ -118,9 +118,10 @@ __device__ bool next_item(const DecodeParams& p, int64_t& u, int64_t hi, Item& i
         const int kvh = (int)(rel / per);
         const int off = (int)(rel % per);
         const int64_t blk0 = e.unit_begin + (int64_t)kvh * per;
-        if (off < e.w_exact) {
-            u = blk0 + e.w_exact;
-            if (off == 0) { it = Item{1, lo, kvh, 0, 0}; return true; }
+        if (off < e.w_exact) {  // exact sub-item off / w_sub (g0 holds its index)
+            const int sub = off / e.w_sub;
+            u = blk0 + (int64_t)(sub + 1) * e.w_sub;
+            if (off % e.w_sub == 0) { it = Item{1, lo, kvh, sub, 0}; return true; }
             continue;
         }
         if (off < e.w_exact + e.w_seal) {
@@ -184,7 +185,7 @@ __device__ int expected_partials(const DecodeParams& p, const SeqEntry& e, int k
     const int per = e.w_exact + e.w_seal + e.n_groups;
     const int64_t g0u = e.unit_begin + (int64_t)kvh * per + e.w_exact + e.w_seal;
     const int64_t W = workers(p);
-    int n = 1 + (e.w_seal > 0 ? 1 : 0);
+    int n = e.w_exact / e.w_sub + (e.w_seal > 0 ? 1 : 0);
     const int64_t f = covering(g0u, p.units_total, W);
     if (e.n_groups > 0) n += (int)(covering(g0u + e.n_groups - 1, p.units_total, W) - f + 1);
     if (first_worker) *first_worker = f;
@@ -254,7 +255,7 @@ __device__ void final_merge_warp(const DecodeParams& p, int ci, int kvh, int lan
             for (int h = 0; h < 4; ++h) {
                 const float w = __shfl_sync(0xffffffffu, wt[k][h], src);
                 const float4 a = __ldcg(reinterpret_cast<const float4*>(P + 12 + 128 * h + 4 * lane));
-                if (sidx == kSlotExact) {
+                if (sidx < kMaxExactSubs) {
                     ex[h][0] = fmaf(w, a.x, ex[h][0]); ex[h][1] = fmaf(w, a.y, ex[h][1]);
                     ex[h][2] = fmaf(w, a.z, ex[h][2]); ex[h][3] = fmaf(w, a.w, ex[h][3]);
                 } else {
@@ -296,12 +297,13 @@ __device__ void publish_warp(const DecodeParams& p, int ci, int kvh, int lane) {
     if (last) final_merge_warp(p, ci, kvh, lane);
 }
 
-// Exact part (sink + tail) of one block on one warp, CUDA cores. In a decode step the
-// new token is first written to the sink or tail (unless it completes a group).
-// Scores: lane = token, its K row read with sixteen 16-byte loads, the query from
-// shared memory. P V: lane l owns channels 4l..4l+3, every V row is one coalesced
-// 256-byte warp load and the probabilities come by shuffle.
-__device__ void exact_item_warp(const DecodeParams& p, const WarpSmem& ws, int ci, int kvh, int lane) {
+// Exact part (sink + tail) of one block, one sub-item of up to 64 tokens on one warp's
+// CUDA cores. In a decode step the sub-item holding the new token first writes it to the
+// sink or tail (unless it completes a group). Scores: lane = token, its K row read with
+// sixteen 16-byte loads, the query from shared memory. P V: lane l owns channels
+// 4l..4l+3; the V rows of a 32-token chunk are all requested before use, each a
+// coalesced 256-byte warp load, and the probabilities come by shuffle.
+__device__ void exact_item_warp(const DecodeParams& p, const WarpSmem& ws, int ci, int kvh, int sub, int lane) {
     const SeqEntry& e = p.seqs[ci];
     const size_t sl = (size_t)e.seq * p.num_layers + p.layer;
     const size_t rows0 = (sl * p.hkv + kvh) * 128;
@@ -309,14 +311,19 @@ __device__ void exact_item_warp(const DecodeParams& p, const WarpSmem& ws, int c
     const uint16_t* sink_v = reinterpret_cast<const uint16_t*>(p.base + p.lay.sink_v) + rows0 * 128;
     const uint16_t* tail_k = reinterpret_cast<const uint16_t*>(p.base + p.lay.tail_k) + rows0 * 128;
     const uint16_t* tail_v = reinterpret_cast<const uint16_t*>(p.base + p.lay.tail_v) + rows0 * 128;
+    const int n_ex = e.n_sink + e.n_tail;
+    const int t_beg = kExactSub * sub, t_end = min(t_beg + kExactSub, n_ex);
     if (e.new_pos >= 0 && e.seal_group < 0) {
-        const int side = lane >> 4, chunk = lane & 15;
-        const uint16_t* src = (side ? p.v_new : p.k_new) + ((size_t)ci * p.hkv + kvh) * 128;
-        const size_t row = e.new_pos < kSink ? (size_t)e.new_pos : (size_t)((e.new_pos - kSink) % kGroup);
-        const size_t off =
-            (e.new_pos < kSink ? (side ? p.lay.sink_v : p.lay.sink_k) : (side ? p.lay.tail_v : p.lay.tail_k)) +
-            (rows0 + row) * 256;
-        reinterpret_cast<uint4*>(p.base + off)[chunk] = reinterpret_cast<const uint4*>(src)[chunk];
+        const int x_new = e.new_pos < kSink ? e.new_pos : e.n_sink + (e.new_pos - kSink) % kGroup;
+        if (x_new >= t_beg && x_new < t_end) {
+            const int side = lane >> 4, chunk = lane & 15;
+            const uint16_t* src = (side ? p.v_new : p.k_new) + ((size_t)ci * p.hkv + kvh) * 128;
+            const size_t row = e.new_pos < kSink ? (size_t)e.new_pos : (size_t)((e.new_pos - kSink) % kGroup);
+            const size_t off =
+                (e.new_pos < kSink ? (side ? p.lay.sink_v : p.lay.sink_k) : (side ? p.lay.tail_v : p.lay.tail_k)) +
+                (rows0 + row) * 256;
+            reinterpret_cast<uint4*>(p.base + off)[chunk] = reinterpret_cast<const uint4*>(src)[chunk];
+        }
     }
     float* qraw = ws.qrot;  // [4][128]
 #pragma unroll
@@ -331,7 +338,6 @@ __device__ void exact_item_warp(const DecodeParams& p, const WarpSmem& ws, int c
         reinterpret_cast<float4*>(qraw + 128 * h)[lane] = v;
     }
     __syncwarp();  // also orders the new token's global write before the reads below
-    const int n_ex = e.n_sink + e.n_tail;
     float m[4] = {kNegInf, kNegInf, kNegInf, kNegInf};
     float lsum[4] = {0.f, 0.f, 0.f, 0.f};
     float acc[4][4];
@@ -339,10 +345,10 @@ __device__ void exact_item_warp(const DecodeParams& p, const WarpSmem& ws, int c
     for (int h = 0; h < 4; ++h)
 #pragma unroll
         for (int c = 0; c < 4; ++c) acc[h][c] = 0.f;
-    for (int c0 = 0; c0 < n_ex; c0 += 32) {
+    for (int c0 = t_beg; c0 < t_end; c0 += 32) {
         const int t = c0 + lane;
         float s[4] = {kNegInf, kNegInf, kNegInf, kNegInf};
-        if (t < n_ex) {
+        if (t < t_end) {
             const uint4* row = reinterpret_cast<const uint4*>(t < e.n_sink ? sink_k + (size_t)t * 128
                                                                           : tail_k + (size_t)(t - e.n_sink) * 128);
             float d[4] = {0.f, 0.f, 0.f, 0.f};
@@ -385,29 +391,33 @@ __device__ void exact_item_warp(const DecodeParams& p, const WarpSmem& ws, int c
             const float mn = fmaxf(m[h], cm);
             const float corr = (m[h] == kNegInf) ? 0.f : exp2f(m[h] - mn);
             m[h] = mn;
-            pr[h] = (t < n_ex) ? exp2f(s[h] - mn) : 0.f;
+            pr[h] = (t < t_end) ? exp2f(s[h] - mn) : 0.f;
             lsum[h] = fmaf(lsum[h], corr, pr[h]);
 #pragma unroll
             for (int c = 0; c < 4; ++c) acc[h][c] *= corr;
         }
-        const int nt = min(32, n_ex - c0);
-        for (int j0 = 0; j0 < nt; j0 += 4) {
-            uint2 vv[4];
+        const int nt = min(32, t_end - c0);
+        // V rows of the chunk, 16 requests in flight at a time
 #pragma unroll
-            for (int u = 0; u < 4; ++u) {
-                const int tt = c0 + j0 + u;
-                vv[u] = make_uint2(0u, 0u);
-                if (j0 + u < nt) {
-                    const uint16_t* row = tt < e.n_sink ? sink_v + (size_t)tt * 128 : tail_v + (size_t)(tt - e.n_sink) * 128;
-                    vv[u] = reinterpret_cast<const uint2*>(row)[lane];
+        for (int j0 = 0; j0 < 32; j0 += 16) {
+            if (j0 >= nt) break;
+            uint2 vv[16];
+#pragma unroll
+            for (int j = 0; j < 16; ++j) {
+                const int tt = c0 + j0 + j;
+                vv[j] = make_uint2(0u, 0u);
+                if (j0 + j < nt) {
+                    const uint16_t* row =
+                        tt < e.n_sink ? sink_v + (size_t)tt * 128 : tail_v + (size_t)(tt - e.n_sink) * 128;
+                    vv[j] = reinterpret_cast<const uint2*>(row)[lane];
                 }
             }
 #pragma unroll
-            for (int u = 0; u < 4; ++u) {
-                const float2 va = __half22float2(bits_h2(vv[u].x)), vb = __half22float2(bits_h2(vv[u].y));
+            for (int j = 0; j < 16; ++j) {
+                const float2 va = __half22float2(bits_h2(vv[j].x)), vb = __half22float2(bits_h2(vv[j].y));
 #pragma unroll
                 for (int h = 0; h < 4; ++h) {
-                    const float pj = __shfl_sync(0xffffffffu, pr[h], (j0 + u) & 31);
+                    const float pj = __shfl_sync(0xffffffffu, pr[h], j0 + j);
                     acc[h][0] = fmaf(pj, va.x, acc[h][0]);
                     acc[h][1] = fmaf(pj, va.y, acc[h][1]);
                     acc[h][2] = fmaf(pj, vb.x, acc[h][2]);
@@ -416,7 +426,7 @@ __device__ void exact_item_warp(const DecodeParams& p, const WarpSmem& ws, int c
             }
         }
     }
-    float* P = partial_ptr(p, e.seq * p.hkv + kvh, kSlotExact);
+    float* P = partial_ptr(p, e.seq * p.hkv + kvh, sub);
 #pragma unroll
     for (int h = 0; h < 4; ++h) {
         float l = lsum[h];
@@ -848,7 +858,7 @@ __global__ void __launch_bounds__(kDecodeThreads, 1) decode_kernel(const __grid_
         const SeqEntry& e = p.seqs[it.ci];
         const int blk = e.seq * p.hkv + it.kvh;
         if (it.type == 1) {
-            exact_item_warp(p, ws, it.ci, it.kvh, lane);
+            exact_item_warp(p, ws, it.ci, it.kvh, it.g0, lane);
             continue;
         }
         int slot;
@@ -933,7 +943,7 @@ int decode_smem_bytes(int k_bits, int v_bits, int warps, bool with_seal) {
 
 // ---------------------------------------------------------------------------
 // Static split-K workspace for kvarn_decode_attention_noalloc: partial softmax states
-// and merge tickets of up to kStaticBlocks (sequence, KV head) blocks, 9.2 MB per GPU
+// and merge tickets of up to kStaticBlocks (sequence, KV head) blocks, 14.3 MB per GPU
 // that loads the library, held until the process exits. Host code must not pass the
 // symbol itself to a kernel (in host code it names a host-side shadow): the device
 // address is fetched once per device with cudaGetSymbolAddress, with that device

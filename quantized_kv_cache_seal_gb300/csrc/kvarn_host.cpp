@@ -118,11 +118,11 @@ kvarn_status check_ids(const kvarn_cache* c, int32_t layer, int32_t n, const int
     return KVARN_OK;
 }
 
-// Units charged for an exact item (sink + tail tokens) relative to one sealed group
-// pair: the exact tokens move 512 bytes each (K and V fp16) on the CUDA cores.
-int exact_units(const kvarn_cache* c, int n_exact) {
-    double pair = (double)(c->rec_k + c->rec_v);
-    return std::max(1, (int)std::ceil(n_exact * 512.0 / pair * 0.6));
+// Units charged for one exact sub-item (up to 64 sink/tail tokens on one warp's CUDA
+// cores) relative to one sealed group pair: about two group pairs at 2/2 bits.
+int exact_sub_units(const kvarn_cache* c) {
+    const double pair = (double)(c->rec_k + c->rec_v);
+    return std::max(1, (int)std::lround(2.0 * 9248.0 / pair));
 }
 
 int seal_units(const kvarn_cache* c) {
@@ -141,7 +141,10 @@ kvarn_status schedule(kvarn_cache* c, DecodeParams& p) {
     for (int i = 0; i < p.n_seqs; ++i) {
         SeqEntry& e = p.seqs[i];
         e.unit_begin = (int32_t)U;
-        int we = exact_units(c, e.n_sink + e.n_tail);
+        const int n_ex = e.n_sink + e.n_tail;
+        const int n_sub = std::max(1, (n_ex + kExactSub - 1) / kExactSub);
+        e.w_sub = exact_sub_units(c);
+        int we = n_sub * e.w_sub;
         int ws = e.seal_group >= 0 ? seal_units(c) : 0;
         e.w_exact = we;
         e.w_seal = ws;
