@@ -44,7 +44,9 @@ namespace {
 constexpr int kEV = 13;      // weight operand exponent: |B| < 2^14
 constexpr int kXbHead = 88;  // exchange buffer words per head (bank-conflict-free stride)
 constexpr int kXbWarp = 4 * kXbHead;
+constexpr int kMrgFloats = 8 + 512;  // per warp: m[4], l[4], acc[4][128]
 constexpr int kWarps = kDecodeThreads / 32;  // 12
+constexpr int kConsumers = kDecodeThreads;
 constexpr int kMaxDevices = 64;
 #define kNegInf (-__int_as_float(0x7f800000))
 
@@ -57,6 +59,18 @@ struct Codes {
     __host__ __device__ static constexpr int ex(int x) { return (x % NWIN) * B; }
     __host__ __device__ static constexpr uint32_t mask(int x) { return (((1u << B) - 1u) << ex(x)) * 0x10001u; }
 };
+
+// pair P (0..15) of a thread's 32-code chunk: word P / HALF, position x = P % HALF;
+// the pair holds codes x and x + HALF of that word.
+template <int B>
+__device__ __forceinline__ void unpack16(const uint32_t (&w)[B], uint32_t (&a)[16]) {
+    using C = Codes<B>;
+#pragma unroll
+    for (int P = 0; P < 16; ++P) {
+        const int word = P / C::HALF, x = P % C::HALF;
+        a[P] = (w[word] >> C::sh(x)) & C::mask(x);
+    }
+}
 
 template <int B>
 __device__ __forceinline__ void load_chunk(const uint8_t* p, uint32_t (&w)[B]) {
@@ -118,10 +132,9 @@ __device__ bool next_item(const DecodeParams& p, int64_t& u, int64_t hi, Item& i
         const int kvh = (int)(rel / per);
         const int off = (int)(rel % per);
         const int64_t blk0 = e.unit_begin + (int64_t)kvh * per;
-        if (off < e.w_exact) {  // exact sub-item off / w_sub (g0 holds its index)
-            const int sub = off / e.w_sub;
-            u = blk0 + (int64_t)(sub + 1) * e.w_sub;
-            if (off % e.w_sub == 0) { it = Item{1, lo, kvh, sub, 0}; return true; }
+        if (off < e.w_exact) {
+            u = blk0 + e.w_exact;
+            if (off == 0) { it = Item{1, lo, kvh, 0, 0}; return true; }
             continue;
         }
         if (off < e.w_exact + e.w_seal) {
@@ -138,19 +151,16 @@ __device__ bool next_item(const DecodeParams& p, int64_t& u, int64_t hi, Item& i
     return false;
 }
 
-// Per-warp shared memory of a worker warp: exchange buffer, query operand table,
-// rotated (or, in the exact part, raw) query, per-head query maxima.
-constexpr int kWarpRegion = kXbWarp * 4 + 8 * 32 * 16 + 512 * 4 + 16;
-
-struct WarpSmem {
-    uint8_t* kstage;   // K record of the warp's current group
-    uint8_t* vstage;   // V record of the warp's current group
-    uint64_t* full_k;  // completes when a K record has landed
-    uint64_t* full_v;
-    float* xb;         // [4][kXbHead] half2 words
-    float4* bqs;       // [8][32] lane operand bases
-    float* qrot;       // [4][128]
-    float* qmax;       // [4]
+struct Smem {
+    uint8_t* stages;
+    uint64_t* full;
+    float* qrot;    // [4][128] rotated query / its max
+    float4* bqs;    // [8][32]: lane l's query operand base, q_hat * 2^-ex, in fragment order
+    float* qmax;    // [4]
+    float* xbuf;    // [8 warps][kXbWarp] (half2 words)
+    float* mrg;     // [8 warps][kMrgFloats], also exact-part and final-merge scratch
+    int* flag;
+    SealSmem* seal;
 };
 
 __device__ __forceinline__ float* partial_ptr(const DecodeParams& p, int blk, int slot) {
@@ -178,283 +188,292 @@ __device__ __forceinline__ void warp_fwht128(float (&v)[4], int lane) {
     for (int e = 0; e < 4; ++e) v[e] *= kInvSqrt128;
 }
 
-__device__ __forceinline__ int64_t workers(const DecodeParams& p) { return (int64_t)p.grid * p.warps; }
-
-// Expected number of partials of block (entry e, kvh) in this call; first worker of its groups.
-__device__ int expected_partials(const DecodeParams& p, const SeqEntry& e, int kvh, int64_t* first_worker) {
+// Expected number of partials of block (entry e, kvh) in this call.
+__device__ int expected_partials(const DecodeParams& p, const SeqEntry& e, int kvh, int64_t* first_cta) {
     const int per = e.w_exact + e.w_seal + e.n_groups;
     const int64_t g0u = e.unit_begin + (int64_t)kvh * per + e.w_exact + e.w_seal;
-    const int64_t W = workers(p);
-    int n = e.w_exact / e.w_sub + (e.w_seal > 0 ? 1 : 0);
-    const int64_t f = covering(g0u, p.units_total, W);
-    if (e.n_groups > 0) n += (int)(covering(g0u + e.n_groups - 1, p.units_total, W) - f + 1);
-    if (first_worker) *first_worker = f;
+    int n = 1 + (e.w_seal > 0 ? 1 : 0);
+    int64_t f = covering(g0u, p.units_total, p.grid);
+    if (e.n_groups > 0) n += (int)(covering(g0u + e.n_groups - 1, p.units_total, p.grid) - f + 1);
+    if (first_cta) *first_cta = f;
     return n;
 }
 
-// The last worker of a block merges every partial of this call, rotates the sealed
-// accumulator back once and writes the fp16 output. One warp; lane l owns channels
-// 4l..4l+3 of every head.
-__device__ void final_merge_warp(const DecodeParams& p, int ci, int kvh, int lane) {
+// Last CTA of a block: merge every partial of this call, rotate back, write out.
+// The partial headers are read in one parallel round (one thread per slot); the
+// accumulators of the valid slots are then read with independent loads.
+__device__ void final_merge(const DecodeParams& p, const Smem& sm, int ci, int kvh) {
+    const int t = threadIdx.x;
     const SeqEntry& e = p.seqs[ci];
     const int blk = e.seq * p.hkv + kvh;
-    // headers of slots lane and 32 + lane
-    float mh[2][4], lh[2][4];
-    bool val[2];
-#pragma unroll
-    for (int k = 0; k < 2; ++k) {
-        const int sidx = 32 * k + lane;
-        val[k] = false;
-#pragma unroll
-        for (int h = 0; h < 4; ++h) { mh[k][h] = kNegInf; lh[k][h] = 0.f; }
-        if (sidx < kPartialSlots) {
-            const float* P = partial_ptr(p, blk, sidx);
-            val[k] = (uint32_t)__float_as_int(__ldcg(P)) == p.epoch;
-            if (val[k]) {
-                const float4 m4 = __ldcg(reinterpret_cast<const float4*>(P + 4));
-                const float4 l4 = __ldcg(reinterpret_cast<const float4*>(P + 8));
-                mh[k][0] = m4.x; mh[k][1] = m4.y; mh[k][2] = m4.z; mh[k][3] = m4.w;
-                lh[k][0] = l4.x; lh[k][1] = l4.y; lh[k][2] = l4.z; lh[k][3] = l4.w;
+    float* hdr = sm.mrg + 1536;           // [kPartialSlots][8]: m[4], l[4]
+    int* list = reinterpret_cast<int*>(sm.mrg + 1536 + 8 * kPartialSlots);  // [kPartialSlots + 1]
+    bool valid = false;
+    if (t < kPartialSlots) {
+        const float* P = partial_ptr(p, blk, t);
+        valid = (uint32_t)__float_as_int(__ldcg(P)) == p.epoch;
+        const float4 m4 = __ldcg(reinterpret_cast<const float4*>(P + 4));
+        const float4 l4 = __ldcg(reinterpret_cast<const float4*>(P + 8));
+        float* H = hdr + 8 * t;
+        H[0] = valid ? m4.x : kNegInf; H[1] = valid ? m4.y : kNegInf;
+        H[2] = valid ? m4.z : kNegInf; H[3] = valid ? m4.w : kNegInf;
+        H[4] = l4.x; H[5] = l4.y; H[6] = l4.z; H[7] = l4.w;
+    }
+    if (t < 32) {  // warp 0 lists the valid slots among 0..31
+        const unsigned vm = __ballot_sync(0xffffffffu, valid);
+        if (t == 0) {
+            int n = 0;
+            for (int k = 0; k < 32; ++k)
+                if (vm >> k & 1) list[1 + n++] = k;
+            list[0] = n;
+        }
+    }
+    named_bar(1, kConsumers);
+    if (t >= 32 && t < kPartialSlots && valid) {  // slots beyond the first warp (rare)
+        const int k = atomicAdd(&list[0], 1);
+        list[1 + k] = t;
+    }
+    named_bar(1, kConsumers);
+    const int nv = list[0];
+    const int h = (t >> 6) & 3, jj = 2 * (t & 63);
+    float M = kNegInf;
+    for (int k = 0; k < nv; ++k) M = fmaxf(M, hdr[8 * list[1 + k] + h]);
+    float l = 0.f, r0 = 0.f, r1 = 0.f, x0 = 0.f, x1 = 0.f;
+    if (M != kNegInf) {
+#pragma unroll 4
+        for (int k = 0; k < nv; ++k) {
+            const int sl = list[1 + k];
+            const float ms = hdr[8 * sl + h];
+            const float w = ms == kNegInf ? 0.f : exp2f(ms - M);
+            const float2 a = __ldcg(reinterpret_cast<const float2*>(partial_ptr(p, blk, sl) + 12 + 128 * h + jj));
+            l = fmaf(w, hdr[8 * sl + 4 + h], l);
+            if (sl == kSlotExact) {
+                x0 = fmaf(w, a.x, x0);
+                x1 = fmaf(w, a.y, x1);
+            } else {
+                r0 = fmaf(w, a.x, r0);
+                r1 = fmaf(w, a.y, r1);
             }
         }
     }
-    float M[4], L[4];
-#pragma unroll
-    for (int h = 0; h < 4; ++h) {
-        float m = fmaxf(mh[0][h], mh[1][h]);
-#pragma unroll
-        for (int o = 16; o > 0; o >>= 1) m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, o));
-        M[h] = m;
+    float* rot = sm.mrg;        // [4][128]
+    float* ex = sm.mrg + 512;   // [4][128]
+    float* ls = sm.mrg + 1024;  // [4]
+    if (t < 256) {
+        rot[128 * h + jj] = r0;
+        rot[128 * h + jj + 1] = r1;
+        ex[128 * h + jj] = x0;
+        ex[128 * h + jj + 1] = x1;
+        if ((t & 63) == 0) ls[h] = l;
     }
-    float wt[2][4];
+    named_bar(1, kConsumers);
+    const int w = t >> 5, lane = t & 31;
+    if (w < 4) {
+        float v[4];
 #pragma unroll
-    for (int k = 0; k < 2; ++k)
+        for (int k = 0; k < 4; ++k) v[k] = rot[128 * w + 4 * lane + k];
+        warp_fwht128(v, lane);
 #pragma unroll
-        for (int h = 0; h < 4; ++h) wt[k][h] = (mh[k][h] == kNegInf) ? 0.f : exp2f(mh[k][h] - M[h]);
-#pragma unroll
-    for (int h = 0; h < 4; ++h) {
-        float l = wt[0][h] * lh[0][h] + wt[1][h] * lh[1][h];
-#pragma unroll
-        for (int o = 16; o > 0; o >>= 1) l += __shfl_xor_sync(0xffffffffu, l, o);
-        L[h] = l;
+        for (int k = 0; k < 4; ++k) rot[128 * w + 4 * lane + k] = v[k];
     }
-    float ex[4][4], rot[4][4];
-#pragma unroll
-    for (int h = 0; h < 4; ++h)
-#pragma unroll
-        for (int c = 0; c < 4; ++c) ex[h][c] = rot[h][c] = 0.f;
-#pragma unroll
-    for (int k = 0; k < 2; ++k) {
-        unsigned mask = __ballot_sync(0xffffffffu, val[k]);
-        while (mask) {
-            const int src = __ffs(mask) - 1;
-            mask &= mask - 1;
-            const int sidx = 32 * k + src;
-            const float* P = partial_ptr(p, blk, sidx);
-#pragma unroll
-            for (int h = 0; h < 4; ++h) {
-                const float w = __shfl_sync(0xffffffffu, wt[k][h], src);
-                const float4 a = __ldcg(reinterpret_cast<const float4*>(P + 12 + 128 * h + 4 * lane));
-                if (sidx < kMaxExactSubs) {
-                    ex[h][0] = fmaf(w, a.x, ex[h][0]); ex[h][1] = fmaf(w, a.y, ex[h][1]);
-                    ex[h][2] = fmaf(w, a.z, ex[h][2]); ex[h][3] = fmaf(w, a.w, ex[h][3]);
-                } else {
-                    rot[h][0] = fmaf(w, a.x, rot[h][0]); rot[h][1] = fmaf(w, a.y, rot[h][1]);
-                    rot[h][2] = fmaf(w, a.z, rot[h][2]); rot[h][3] = fmaf(w, a.w, rot[h][3]);
-                }
-            }
-        }
-    }
-#pragma unroll
-    for (int h = 0; h < 4; ++h) {
-        warp_fwht128(rot[h], lane);
-        if (h < p.r) {
-            const float inv = L[h] > 0.f ? 1.0f / L[h] : 0.f;
-            const __half2 o0 = __floats2half2_rn((ex[h][0] + rot[h][0]) * inv, (ex[h][1] + rot[h][1]) * inv);
-            const __half2 o1 = __floats2half2_rn((ex[h][2] + rot[h][2]) * inv, (ex[h][3] + rot[h][3]) * inv);
-            uint16_t* out = p.out + ((size_t)ci * p.hq + (size_t)kvh * p.r + h) * 128 + 4 * lane;
-            *reinterpret_cast<uint2*>(out) = make_uint2(h2_bits(o0), h2_bits(o1));
-        }
+    named_bar(1, kConsumers);
+    if (t < 256 && h < p.r) {
+        const float lh = ls[h];
+        const float inv = lh > 0.f ? 1.0f / lh : 0.f;
+        __half2 o = __floats2half2_rn((ex[128 * h + jj] + rot[128 * h + jj]) * inv,
+                                      (ex[128 * h + jj + 1] + rot[128 * h + jj + 1]) * inv);
+        uint16_t* out = p.out + ((size_t)ci * p.hq + (size_t)kvh * p.r + h) * 128 + jj;
+        *reinterpret_cast<__half2*>(out) = o;
     }
 }
 
-// Publish a partial written by this warp; the last of the block's partials merges.
-__device__ void publish_warp(const DecodeParams& p, int ci, int kvh, int lane) {
+// Publish a partial (written by all consumer threads before the call) and merge if last.
+__device__ void publish(const DecodeParams& p, const Smem& sm, int ci, int kvh) {
     __threadfence();
-    __syncwarp();
+    named_bar(1, kConsumers);
     const SeqEntry& e = p.seqs[ci];
     const int blk = e.seq * p.hkv + kvh;
-    int last = 0;
-    if (lane == 0) {
-        const int expect = expected_partials(p, e, kvh, nullptr);
+    if (threadIdx.x == 0) {
+        int expect = expected_partials(p, e, kvh, nullptr);
         int32_t* tickets = reinterpret_cast<int32_t*>(p.base + p.lay.tickets);
-        const int old = atomicAdd(tickets + blk, 1);
-        last = (old == expect - 1);
+        int old = atomicAdd(tickets + blk, 1);
+        int last = (old == expect - 1);
         if (last) tickets[blk] = 0;
         __threadfence();
+        *sm.flag = last;
     }
-    last = __shfl_sync(0xffffffffu, last, 0);
-    if (last) final_merge_warp(p, ci, kvh, lane);
+    named_bar(1, kConsumers);
+    if (*sm.flag) final_merge(p, sm, ci, kvh);
+    named_bar(1, kConsumers);
 }
 
-// Exact part (sink + tail) of one block, one sub-item of up to 64 tokens on one warp's
-// CUDA cores. In a decode step the sub-item holding the new token first writes it to the
-// sink or tail (unless it completes a group). Scores: lane = token, its K row read with
-// sixteen 16-byte loads, the query from shared memory. P V: lane l owns channels
-// 4l..4l+3; the V rows of a 32-token chunk are all requested before use, each a
-// coalesced 256-byte warp load, and the probabilities come by shuffle.
-__device__ void exact_item_warp(const DecodeParams& p, const WarpSmem& ws, int ci, int kvh, int sub, int lane) {
+// Exact part (sink + tail) of one block on CUDA cores; in a decode step the new token
+// is first written to the sink or tail (unless it completes a group). Scores: one
+// thread per token, sixteen independent 16-byte loads of its K row. P V: warp w takes
+// tokens w, w+8, ...; lane l holds channels 4l..4l+3 of all four heads, so every V row
+// is one coalesced 256-byte warp load; the eight warps' sums meet in shared memory.
+__device__ void exact_item(const DecodeParams& p, const Smem& sm, int ci, int kvh) {
+    const int t = threadIdx.x, w = t >> 5, lane = t & 31;
     const SeqEntry& e = p.seqs[ci];
     const size_t sl = (size_t)e.seq * p.num_layers + p.layer;
-    const size_t rows0 = (sl * p.hkv + kvh) * 128;
+    const size_t rows0 = (sl * p.hkv + kvh) * 128;  // first row of this (seq, layer, kv head)
     const uint16_t* sink_k = reinterpret_cast<const uint16_t*>(p.base + p.lay.sink_k) + rows0 * 128;
     const uint16_t* sink_v = reinterpret_cast<const uint16_t*>(p.base + p.lay.sink_v) + rows0 * 128;
     const uint16_t* tail_k = reinterpret_cast<const uint16_t*>(p.base + p.lay.tail_k) + rows0 * 128;
     const uint16_t* tail_v = reinterpret_cast<const uint16_t*>(p.base + p.lay.tail_v) + rows0 * 128;
+    if (e.new_pos >= 0 && e.seal_group < 0 && t < 32) {
+        const int side = t >> 4, chunk = t & 15;
+        const uint16_t* src = (side ? p.v_new : p.k_new) + ((size_t)ci * p.hkv + kvh) * 128;
+        size_t row = e.new_pos < kSink ? (size_t)e.new_pos : (size_t)((e.new_pos - kSink) % kGroup);
+        size_t off = (e.new_pos < kSink ? (side ? p.lay.sink_v : p.lay.sink_k) : (side ? p.lay.tail_v : p.lay.tail_k)) +
+                     (rows0 + row) * 256;
+        reinterpret_cast<uint4*>(p.base + off)[chunk] = reinterpret_cast<const uint4*>(src)[chunk];
+    }
+    float* qraw = sm.xbuf;           // [4][128]
+    float* sc = sm.xbuf + 512;       // [4][256]
+    float* red = sm.xbuf + 1536;     // [16]
+    float* part = sm.mrg;            // [kWarps][4][128]
+    for (int k = t; k < 512; k += kConsumers) {
+        const int h = k >> 7, j = k & 127;
+        qraw[k] = h < p.r ? half_bits_to_float(p.q[((size_t)ci * p.hq + (size_t)kvh * p.r + h) * 128 + j]) : 0.f;
+    }
+    named_bar(1, kConsumers);
     const int n_ex = e.n_sink + e.n_tail;
-    const int t_beg = kExactSub * sub, t_end = min(t_beg + kExactSub, n_ex);
-    if (e.new_pos >= 0 && e.seal_group < 0) {
-        const int x_new = e.new_pos < kSink ? e.new_pos : e.n_sink + (e.new_pos - kSink) % kGroup;
-        if (x_new >= t_beg && x_new < t_end) {
-            const int side = lane >> 4, chunk = lane & 15;
-            const uint16_t* src = (side ? p.v_new : p.k_new) + ((size_t)ci * p.hkv + kvh) * 128;
-            const size_t row = e.new_pos < kSink ? (size_t)e.new_pos : (size_t)((e.new_pos - kSink) % kGroup);
-            const size_t off =
-                (e.new_pos < kSink ? (side ? p.lay.sink_v : p.lay.sink_k) : (side ? p.lay.tail_v : p.lay.tail_k)) +
-                (rows0 + row) * 256;
-            reinterpret_cast<uint4*>(p.base + off)[chunk] = reinterpret_cast<const uint4*>(src)[chunk];
-        }
-    }
-    float* qraw = ws.qrot;  // [4][128]
+    float s[4] = {kNegInf, kNegInf, kNegInf, kNegInf};
+    if (t < n_ex) {
+        const uint4* row = reinterpret_cast<const uint4*>(t < e.n_sink ? sink_k + (size_t)t * 128
+                                                                      : tail_k + (size_t)(t - e.n_sink) * 128);
+        float d[4] = {0.f, 0.f, 0.f, 0.f};
 #pragma unroll
-    for (int h = 0; h < 4; ++h) {
-        float4 v = make_float4(0.f, 0.f, 0.f, 0.f);
-        if (h < p.r) {
-            const uint2 raw = *reinterpret_cast<const uint2*>(p.q + ((size_t)ci * p.hq + (size_t)kvh * p.r + h) * 128 +
-                                                                4 * lane);
-            const float2 f0 = __half22float2(bits_h2(raw.x)), f1 = __half22float2(bits_h2(raw.y));
-            v = make_float4(f0.x, f0.y, f1.x, f1.y);
-        }
-        reinterpret_cast<float4*>(qraw + 128 * h)[lane] = v;
-    }
-    __syncwarp();  // also orders the new token's global write before the reads below
-    float m[4] = {kNegInf, kNegInf, kNegInf, kNegInf};
-    float lsum[4] = {0.f, 0.f, 0.f, 0.f};
-    float acc[4][4];
+        for (int half = 0; half < 2; ++half) {
+            uint4 kv[8];
 #pragma unroll
-    for (int h = 0; h < 4; ++h)
+            for (int c = 0; c < 8; ++c) kv[c] = row[8 * half + c];
 #pragma unroll
-        for (int c = 0; c < 4; ++c) acc[h][c] = 0.f;
-    for (int c0 = t_beg; c0 < t_end; c0 += 32) {
-        const int t = c0 + lane;
-        float s[4] = {kNegInf, kNegInf, kNegInf, kNegInf};
-        if (t < t_end) {
-            const uint4* row = reinterpret_cast<const uint4*>(t < e.n_sink ? sink_k + (size_t)t * 128
-                                                                          : tail_k + (size_t)(t - e.n_sink) * 128);
-            float d[4] = {0.f, 0.f, 0.f, 0.f};
+            for (int c = 0; c < 8; ++c) {
+                const __half2* hp = reinterpret_cast<const __half2*>(&kv[c]);
+                float kf[8];
 #pragma unroll
-            for (int half = 0; half < 2; ++half) {
-                uint4 kv[8];
-#pragma unroll
-                for (int c = 0; c < 8; ++c) kv[c] = row[8 * half + c];
-#pragma unroll
-                for (int c = 0; c < 8; ++c) {
-                    const __half2* hp = reinterpret_cast<const __half2*>(&kv[c]);
-                    float kf[8];
-#pragma unroll
-                    for (int q2 = 0; q2 < 4; ++q2) {
-                        const float2 f = __half22float2(hp[q2]);
-                        kf[2 * q2] = f.x;
-                        kf[2 * q2 + 1] = f.y;
-                    }
-                    const int cc = 8 * half + c;
-#pragma unroll
-                    for (int h = 0; h < 4; ++h) {
-                        const float4 qa = reinterpret_cast<const float4*>(qraw + 128 * h + 8 * cc)[0];
-                        const float4 qb = reinterpret_cast<const float4*>(qraw + 128 * h + 8 * cc)[1];
-                        d[h] = fmaf(kf[0], qa.x, d[h]); d[h] = fmaf(kf[1], qa.y, d[h]);
-                        d[h] = fmaf(kf[2], qa.z, d[h]); d[h] = fmaf(kf[3], qa.w, d[h]);
-                        d[h] = fmaf(kf[4], qb.x, d[h]); d[h] = fmaf(kf[5], qb.y, d[h]);
-                        d[h] = fmaf(kf[6], qb.z, d[h]); d[h] = fmaf(kf[7], qb.w, d[h]);
-                    }
+                for (int q2 = 0; q2 < 4; ++q2) {
+                    float2 f = __half22float2(hp[q2]);
+                    kf[2 * q2] = f.x;
+                    kf[2 * q2 + 1] = f.y;
                 }
-            }
-#pragma unroll
-            for (int h = 0; h < 4; ++h) s[h] = d[h] * p.scale_log2;
-        }
-        float pr[4];
-#pragma unroll
-        for (int h = 0; h < 4; ++h) {
-            float cm = s[h];
-#pragma unroll
-            for (int o = 16; o > 0; o >>= 1) cm = fmaxf(cm, __shfl_xor_sync(0xffffffffu, cm, o));
-            const float mn = fmaxf(m[h], cm);
-            const float corr = (m[h] == kNegInf) ? 0.f : exp2f(m[h] - mn);
-            m[h] = mn;
-            pr[h] = (t < t_end) ? exp2f(s[h] - mn) : 0.f;
-            lsum[h] = fmaf(lsum[h], corr, pr[h]);
-#pragma unroll
-            for (int c = 0; c < 4; ++c) acc[h][c] *= corr;
-        }
-        const int nt = min(32, t_end - c0);
-        // V rows of the chunk, 16 requests in flight at a time
-#pragma unroll
-        for (int j0 = 0; j0 < 32; j0 += 16) {
-            if (j0 >= nt) break;
-            uint2 vv[16];
-#pragma unroll
-            for (int j = 0; j < 16; ++j) {
-                const int tt = c0 + j0 + j;
-                vv[j] = make_uint2(0u, 0u);
-                if (j0 + j < nt) {
-                    const uint16_t* row =
-                        tt < e.n_sink ? sink_v + (size_t)tt * 128 : tail_v + (size_t)(tt - e.n_sink) * 128;
-                    vv[j] = reinterpret_cast<const uint2*>(row)[lane];
-                }
-            }
-#pragma unroll
-            for (int j = 0; j < 16; ++j) {
-                const float2 va = __half22float2(bits_h2(vv[j].x)), vb = __half22float2(bits_h2(vv[j].y));
+                const int cc = 8 * half + c;
 #pragma unroll
                 for (int h = 0; h < 4; ++h) {
-                    const float pj = __shfl_sync(0xffffffffu, pr[h], j0 + j);
-                    acc[h][0] = fmaf(pj, va.x, acc[h][0]);
-                    acc[h][1] = fmaf(pj, va.y, acc[h][1]);
-                    acc[h][2] = fmaf(pj, vb.x, acc[h][2]);
-                    acc[h][3] = fmaf(pj, vb.y, acc[h][3]);
+                    const float4 qa = reinterpret_cast<const float4*>(qraw + 128 * h + 8 * cc)[0];
+                    const float4 qb = reinterpret_cast<const float4*>(qraw + 128 * h + 8 * cc)[1];
+                    d[h] = fmaf(kf[0], qa.x, d[h]); d[h] = fmaf(kf[1], qa.y, d[h]);
+                    d[h] = fmaf(kf[2], qa.z, d[h]); d[h] = fmaf(kf[3], qa.w, d[h]);
+                    d[h] = fmaf(kf[4], qb.x, d[h]); d[h] = fmaf(kf[5], qb.y, d[h]);
+                    d[h] = fmaf(kf[6], qb.z, d[h]); d[h] = fmaf(kf[7], qb.w, d[h]);
                 }
             }
         }
+#pragma unroll
+        for (int h = 0; h < 4; ++h) s[h] = d[h] * p.scale_log2;
     }
-    float* P = partial_ptr(p, e.seq * p.hkv + kvh, sub);
+    if (t < 256) {
 #pragma unroll
-    for (int h = 0; h < 4; ++h) {
-        float l = lsum[h];
+        for (int h = 0; h < 4; ++h) sc[256 * h + t] = s[h];
+    }
+    named_bar(1, kConsumers);
+    // per-head max and sum: 64 threads per head, 4 entries each (threads >= 256 idle)
+    {
+        const int h = (t >> 6) & 3, k0 = 4 * (t & 63);
+        float m = fmaxf(fmaxf(sc[256 * h + k0], sc[256 * h + k0 + 1]), fmaxf(sc[256 * h + k0 + 2], sc[256 * h + k0 + 3]));
 #pragma unroll
-        for (int o = 16; o > 0; o >>= 1) l += __shfl_xor_sync(0xffffffffu, l, o);
-        reinterpret_cast<float4*>(P + 12 + 128 * h)[lane] = make_float4(acc[h][0], acc[h][1], acc[h][2], acc[h][3]);
-        if (lane == 0) {
-            P[4 + h] = m[h];
-            P[8 + h] = l;
+        for (int o = 16; o > 0; o >>= 1) m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, o));
+        if (lane == 0 && t < 256) red[2 * h + (w & 1)] = m;
+        named_bar(1, kConsumers);
+        m = fmaxf(red[2 * h], red[2 * h + 1]);
+        float sum = 0.f;
+#pragma unroll
+        for (int k = 0; k < 4; ++k) {
+            float v = sc[256 * h + k0 + k];
+            float pv = (m == kNegInf) ? 0.f : exp2f(v - m);
+            if (t < 256) sc[256 * h + k0 + k] = pv;
+            sum += pv;
+        }
+#pragma unroll
+        for (int o = 16; o > 0; o >>= 1) sum += __shfl_xor_sync(0xffffffffu, sum, o);
+        if (lane == 0 && t < 256) red[8 + 2 * h + (w & 1)] = sum;
+        named_bar(1, kConsumers);
+        if ((t & 63) == 0 && t < 256) {
+            float* P = partial_ptr(p, e.seq * p.hkv + kvh, kSlotExact);
+            P[4 + h] = m;
+            P[8 + h] = red[8 + 2 * h] + red[8 + 2 * h + 1];
         }
     }
-    if (lane == 0) P[0] = __int_as_float((int)p.epoch);
-    publish_warp(p, ci, kvh, lane);
+    // P V
+    {
+        float acc[4][4];
+#pragma unroll
+        for (int h = 0; h < 4; ++h)
+#pragma unroll
+            for (int c = 0; c < 4; ++c) acc[h][c] = 0.f;
+        for (int k0 = w; k0 < n_ex; k0 += 4 * kWarps) {
+            uint2 vv[4];
+#pragma unroll
+            for (int u = 0; u < 4; ++u) {
+                const int k = k0 + kWarps * u;
+                vv[u] = make_uint2(0u, 0u);
+                if (k < n_ex) {
+                    const uint16_t* row = k < e.n_sink ? sink_v + (size_t)k * 128 : tail_v + (size_t)(k - e.n_sink) * 128;
+                    vv[u] = reinterpret_cast<const uint2*>(row)[lane];
+                }
+            }
+#pragma unroll
+            for (int u = 0; u < 4; ++u) {
+                const int k = k0 + kWarps * u;
+                if (k < n_ex) {
+                    const float2 va = __half22float2(bits_h2(vv[u].x)), vb = __half22float2(bits_h2(vv[u].y));
+#pragma unroll
+                    for (int h = 0; h < 4; ++h) {
+                        const float pk = sc[256 * h + k];
+                        acc[h][0] = fmaf(pk, va.x, acc[h][0]);
+                        acc[h][1] = fmaf(pk, va.y, acc[h][1]);
+                        acc[h][2] = fmaf(pk, vb.x, acc[h][2]);
+                        acc[h][3] = fmaf(pk, vb.y, acc[h][3]);
+                    }
+                }
+            }
+        }
+#pragma unroll
+        for (int h = 0; h < 4; ++h)
+            *reinterpret_cast<float4*>(part + (w * 4 + h) * 128 + 4 * lane) =
+                make_float4(acc[h][0], acc[h][1], acc[h][2], acc[h][3]);
+        named_bar(1, kConsumers);
+        if (t < 256) {
+            const int h = t >> 6, jj = 2 * (t & 63);
+            float a0 = 0.f, a1 = 0.f;
+#pragma unroll
+            for (int k = 0; k < kWarps; ++k) {
+                a0 += part[(k * 4 + h) * 128 + jj];
+                a1 += part[(k * 4 + h) * 128 + jj + 1];
+            }
+            float* P = partial_ptr(p, e.seq * p.hkv + kvh, kSlotExact);
+            *reinterpret_cast<float2*>(P + 12 + 128 * h + jj) = make_float2(a0, a1);
+            if (t == 0) P[0] = __int_as_float((int)p.epoch);
+        }
+    }
+    publish(p, sm, ci, kvh);
 }
 
-// Rotate the query of a block (one warp): qrot = (q H) / max|q H| per head, qmax = that
-// max; then the table of each lane's query operand base q_hat(head g>>1, channel) * 2^-ex
-// in the pair order of its MMA fragments.
+// Rotate the query of a block: qrot = (q H) / max|q H| per head, qmax = that max; then
+// the table of each lane's query operand base q_hat(head g>>1, channel) * 2^-ex in the
+// pair order of its MMA fragments (the codes' power-of-two offsets folded in).
 template <int KB>
-__device__ void setup_query_warp(const DecodeParams& p, const WarpSmem& ws, int ci, int kvh, int lane) {
+__device__ void setup_query(const DecodeParams& p, const Smem& sm, int ci, int kvh) {
     using CK = Codes<KB>;
-#pragma unroll
-    for (int h = 0; h < 4; ++h) {
+    const int t = threadIdx.x, w = t >> 5, lane = t & 31;
+    if (w < 4) {
         float v[4] = {0.f, 0.f, 0.f, 0.f};
-        if (h < p.r) {
-            const uint16_t* q = p.q + ((size_t)ci * p.hq + (size_t)kvh * p.r + h) * 128 + 4 * lane;
-            const uint2 raw = *reinterpret_cast<const uint2*>(q);
-            const float2 f0 = __half22float2(bits_h2(raw.x)), f1 = __half22float2(bits_h2(raw.y));
+        if (w < p.r) {
+            const uint16_t* q = p.q + ((size_t)ci * p.hq + (size_t)kvh * p.r + w) * 128 + 4 * lane;
+            uint2 raw = *reinterpret_cast<const uint2*>(q);
+            float2 f0 = __half22float2(bits_h2(raw.x)), f1 = __half22float2(bits_h2(raw.y));
             v[0] = f0.x; v[1] = f0.y; v[2] = f1.x; v[3] = f1.y;
         }
         warp_fwht128(v, lane);
@@ -463,27 +482,28 @@ __device__ void setup_query_warp(const DecodeParams& p, const WarpSmem& ws, int 
         for (int o = 16; o > 0; o >>= 1) mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, o));
         if (mx == 0.f) mx = 1.f;
         const float inv = 1.0f / mx;
-        reinterpret_cast<float4*>(ws.qrot + 128 * h)[lane] = make_float4(v[0] * inv, v[1] * inv, v[2] * inv, v[3] * inv);
-        if (lane == 0) ws.qmax[h] = mx;
-    }
-    __syncwarp();
-    const int g = lane >> 2, tq = lane & 3;
-    const float* qh = ws.qrot + 128 * (g >> 1);
 #pragma unroll
-    for (int q = 0; q < 8; ++q) {
+        for (int k = 0; k < 4; ++k) sm.qrot[128 * w + 4 * lane + k] = v[k] * inv;
+        if (lane == 0) sm.qmax[w] = mx;
+    }
+    named_bar(1, kConsumers);
+    if (t < 256) {
+        // entry q (0..7) of lane l: pairs P = 2q, 2q+1 of lane l = (g, tq)
+        const int q = t >> 5, g = lane >> 2, tq = lane & 3;
+        const float* qh = sm.qrot + 128 * (g >> 1);
         float vals[4];
 #pragma unroll
-        for (int e2 = 0; e2 < 2; ++e2) {
-            const int P = 2 * q + e2;
+        for (int e = 0; e < 2; ++e) {
+            const int P = 2 * q + e;
             const int x = P % CK::HALF;
             const int c0 = 32 * tq + CK::CPW * (P / CK::HALF) + x;
             const float sc = __int_as_float((127 - CK::ex(x)) << 23);  // 2^-ex
-            vals[2 * e2] = qh[c0] * sc;
-            vals[2 * e2 + 1] = qh[c0 + CK::HALF] * sc;
+            vals[2 * e] = qh[c0] * sc;
+            vals[2 * e + 1] = qh[c0 + CK::HALF] * sc;
         }
-        ws.bqs[q * 32 + lane] = make_float4(vals[0], vals[1], vals[2], vals[3]);
+        sm.bqs[q * 32 + lane] = make_float4(vals[0], vals[1], vals[2], vals[3]);
     }
-    __syncwarp();
+    named_bar(1, kConsumers);
 }
 
 struct WarpState {
@@ -513,18 +533,21 @@ struct TileGroup {
     static constexpr int TG = B == 8 ? 2 : 4;
 };
 
-// Process one sealed group: K record at krec, V record at vrec (both in shared memory).
-// k_done() is called once the K record has been read completely (its stage may then be
-// refilled); v_wait() waits for the V record before it is first read.
-template <int KB, int VB, class KDone, class VWait>
-__device__ __forceinline__ void process_group(const DecodeParams& p, const uint8_t* krec, const uint8_t* vrec,
-                                              const float4* bqs, float qm, float* xb, WarpState& st, int g, int tq,
-                                              int lane, KDone k_done, VWait v_wait) {
+// Process one sealed group pair held in shared memory (K record, then V record).
+template <int KB, int VB>
+__device__ __forceinline__ void process_group(const DecodeParams& p, const uint8_t* rec, const float4* bqs,
+                                              float qm, float* xb, WarpState& st, int g, int tq, int lane) {
     using CK = Codes<KB>;
     using CV = Codes<VB>;
+    const uint8_t* krec = rec;
+    const uint8_t* vrec = rec + p.rec_k;
     const float dK = *reinterpret_cast<const float*>(krec);
     const float mK = *reinterpret_cast<const float*>(krec + 4);
+    const float dV = *reinterpret_cast<const float*>(vrec);
+    const float mV = *reinterpret_cast<const float*>(vrec + 4);
     const uint16_t* aK = reinterpret_cast<const uint16_t*>(krec + 16);
+    const uint16_t* aV = reinterpret_cast<const uint16_t*>(vrec + 16);
+    const uint16_t* cV = reinterpret_cast<const uint16_t*>(vrec + 272);
     // ---- query operand of this group: q_hat * c_K * 2^-ex, split into f16 high / low parts.
     // |q_hat| <= 1, c_K <= 65504 and 2^-ex <= 1, so the operand can never overflow f16.
     uint32_t bk[16];
@@ -598,24 +621,13 @@ __device__ __forceinline__ void process_group(const DecodeParams& p, const uint8
     const float alpha = p.scale_log2 * qm * dK * 16777216.0f;  // codes enter as code * 2^(ex-24)
     const float beta = p.scale_log2 * qm * mK * sumqc;
     float gmax = kNegInf;
+    float av[8][2];
 #pragma unroll
     for (int mt = 0; mt < 8; ++mt) {
         const int t0 = tok_row<VB>(mt, g), t1 = t0 + CV::HALF;
         S[mt][0] = half_bits_to_float(aK[t0]) * fmaf(alpha, S[mt][0], beta);
         S[mt][1] = half_bits_to_float(aK[t1]) * fmaf(alpha, S[mt][1], beta);
         gmax = fmaxf(gmax, fmaxf(S[mt][0], S[mt][1]));
-    }
-    __syncwarp();
-    k_done();   // the K record is no longer read
-    v_wait();
-    const float dV = *reinterpret_cast<const float*>(vrec);
-    const float mV = *reinterpret_cast<const float*>(vrec + 4);
-    const uint16_t* aV = reinterpret_cast<const uint16_t*>(vrec + 16);
-    const uint16_t* cV = reinterpret_cast<const uint16_t*>(vrec + 272);
-    float av[8][2];
-#pragma unroll
-    for (int mt = 0; mt < 8; ++mt) {
-        const int t0 = tok_row<VB>(mt, g), t1 = t0 + CV::HALF;
         av[mt][0] = half_bits_to_float(aV[t0]);
         av[mt][1] = half_bits_to_float(aV[t1]);
     }
@@ -699,24 +711,47 @@ __device__ __forceinline__ void process_group(const DecodeParams& p, const uint8
     }
 }
 
-// Write one warp's softmax state of an item as a partial (lane (g, tq) holds head tq at
-// channels 16 mt + g and 16 mt + g + 8).
-__device__ void write_partial_warp(const DecodeParams& p, const WarpState& st, int blk, int slot, int lane) {
-    const int g = lane >> 2, tq = lane & 3;
+// Merge the eight warps' states of one item into a partial in global memory.
+__device__ void write_item_partial(const DecodeParams& p, const Smem& sm, const WarpState& st, int blk, int slot) {
+    const int t = threadIdx.x, w = t >> 5, lane = t & 31, g = lane >> 2, tq = lane & 3;
     float l = st.l;
 #pragma unroll
     for (int o = 4; o < 32; o <<= 1) l += __shfl_xor_sync(0xffffffffu, l, o);
-    float* P = partial_ptr(p, blk, slot);
+    float* M = sm.mrg + w * kMrgFloats;
+    if (g == 0) {
+        M[tq] = st.m;
+        M[4 + tq] = l;
+    }
 #pragma unroll
     for (int mt = 0; mt < 8; ++mt) {
-        P[12 + 128 * tq + 16 * mt + g] = st.acc[mt][0];
-        P[12 + 128 * tq + 16 * mt + g + 8] = st.acc[mt][1];
+        M[8 + 128 * tq + 16 * mt + g] = st.acc[mt][0];
+        M[8 + 128 * tq + 16 * mt + g + 8] = st.acc[mt][1];
     }
-    if (g == 0) {
-        P[4 + tq] = st.m;
-        P[8 + tq] = l;
+    named_bar(1, kConsumers);
+    if (t < 256) {
+        const int h = t >> 6, jj = 2 * (t & 63);
+        float mx = kNegInf;
+#pragma unroll
+        for (int k = 0; k < kWarps; ++k) mx = fmaxf(mx, sm.mrg[k * kMrgFloats + h]);
+        float ls = 0.f, a0 = 0.f, a1 = 0.f;
+#pragma unroll
+        for (int k = 0; k < kWarps; ++k) {
+            const float* Mk = sm.mrg + k * kMrgFloats;
+            const float mk = Mk[h];
+            if (mk == kNegInf) continue;
+            const float wgt = exp2f(mk - mx);
+            ls = fmaf(wgt, Mk[4 + h], ls);
+            a0 = fmaf(wgt, Mk[8 + 128 * h + jj], a0);
+            a1 = fmaf(wgt, Mk[8 + 128 * h + jj + 1], a1);
+        }
+        float* P = partial_ptr(p, blk, slot);
+        *reinterpret_cast<float2*>(P + 12 + 128 * h + jj) = make_float2(a0, a1);
+        if ((t & 63) == 0) {
+            P[4 + h] = mx;
+            P[8 + h] = ls;
+        }
+        if (t == 0) P[0] = __int_as_float((int)p.epoch);
     }
-    if (lane == 0) P[0] = __int_as_float((int)p.epoch);
 }
 
 __device__ __forceinline__ const uint8_t* group_src(const DecodeParams& p, int seq, int kvh, int g) {
@@ -735,15 +770,15 @@ struct SealRows {
     __device__ const uint16_t* operator()(int i) const { return i < 127 ? tail + 128 * i : last; }
 };
 
-// Walks a worker's sealed groups in stream order to find the record of group number gn
-// (0, 1, ... over the chunk and seal items of the worker's unit range, in item order).
+// Walks the CTA's sealed groups in stream order to find the record of group number gn
+// (0, 1, ... over the chunk and seal items of the CTA's unit range, in item order).
 struct GroupCursor {
     int64_t u;       // unit cursor of the item walk
     Item it;         // current chunk / seal item
     uint32_t base;   // group number of the item's first group
     bool valid;
     __device__ void init(int64_t lo) { u = lo; base = 0; valid = false; it.g0 = it.g1 = 0; }
-    // record pair address of group gn (gn never decreases between calls); null past the end
+    // record address of group gn (gn never decreases between calls); null past the end
     __device__ const uint8_t* src(const DecodeParams& p, int64_t hi, uint32_t gn) {
         for (;;) {
             if (valid && gn < base + (uint32_t)(it.g1 - it.g0)) break;
@@ -766,50 +801,75 @@ struct GroupCursor {
     }
 };
 
-// One CTA of up to 12 worker warps per SM. Every warp is an independent worker with its
-// own contiguous range of scheduling units and a one-group stage split into a K half and
-// a V half: the next group's K record is requested as soon as the current QK is done,
-// its V record as soon as the current PV is done. The CTA only synchronises once, after
-// the seal items of its range (run first by 8 warps, their scratch on the stage area).
+__device__ __forceinline__ void issue_group(const DecodeParams& p, const Smem& sm, GroupCursor& cur, int64_t hi,
+                                            uint32_t gn) {
+    const uint8_t* src = cur.src(p, hi, gn);
+    if (!src) return;
+    const uint32_t pair = (uint32_t)(p.rec_k + p.rec_v);
+    const uint32_t s = gn % p.stages;
+    mbar_arrive_expect_tx(sm.full + s, pair);
+    bulk_g2s(sm.stages + (size_t)s * pair, src, pair, sm.full + s);
+}
+
+// One CTA of 12 warps per SM. Stage ring: group gn lives in stage gn % S and is
+// processed by warp gn % 12; the warp that finishes with a stage issues the copy of
+// group gn + S into it, so no stage needs a release barrier. Seal items of the CTA run
+// first, with their scratch aliased onto the (still empty) stage ring.
 template <int KB, int VB>
 __global__ void __launch_bounds__(kDecodeThreads, 1) decode_kernel(const __grid_constant__ DecodeParams p) {
     extern __shared__ __align__(128) uint8_t smem_raw[];
+    Smem sm;
     const int pair = p.rec_k + p.rec_v;
-    const int nw = p.warps;
-    size_t ring = (size_t)nw * pair;
-    if (ring < sizeof(SealSmem)) ring = sizeof(SealSmem);
-    ring = (ring + 127) & ~(size_t)127;
-    uint64_t* bars = reinterpret_cast<uint64_t*>(smem_raw + ring);  // full_k[12], full_v[12]
-    uint8_t* regions = smem_raw + ring + 256;
+    {
+        size_t off = 0;
+        sm.stages = smem_raw;
+        size_t ring = (size_t)p.stages * pair;
+        if (ring < sizeof(SealSmem)) ring = sizeof(SealSmem);
+        off += ring;
+        off = (off + 15) & ~(size_t)15;
+        sm.full = reinterpret_cast<uint64_t*>(smem_raw + off);
+        off += 32 * 8;
+        sm.qrot = reinterpret_cast<float*>(smem_raw + off);
+        off += 512 * 4;
+        sm.qmax = reinterpret_cast<float*>(smem_raw + off);
+        off += 16;
+        sm.flag = reinterpret_cast<int*>(smem_raw + off);
+        off += 16;
+        sm.bqs = reinterpret_cast<float4*>(smem_raw + off);
+        off += 8 * 32 * 16;
+        sm.xbuf = reinterpret_cast<float*>(smem_raw + off);
+        off += kWarps * kXbWarp * 4;
+        sm.mrg = reinterpret_cast<float*>(smem_raw + off);
+        sm.seal = reinterpret_cast<SealSmem*>(smem_raw);
+    }
     const int t = threadIdx.x, w = t >> 5, lane = t & 31;
     if (t == 0) {
-        for (int k = 0; k < 2 * kWarps; ++k) mbar_init(bars + k, 1);
+        for (int s = 0; s < p.stages; ++s) mbar_init(sm.full + s, 1);
         asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
     }
     __syncthreads();
-    const int64_t U = p.units_total, W = workers(p), b = blockIdx.x;
+    const int64_t U = p.units_total, P = p.grid, b = blockIdx.x;
+    const int64_t lo = b * U / P, hi = (b + 1) * U / P;
     int32_t* err = err_word(p);
 
     // ---- 1. seal the groups completed by this step's tokens (before any prefetch)
+    bool sealed_any = false;
     {
-        const int64_t clo = b * nw * U / W, chi = (b + 1) * nw * U / W;
-        SealSmem& S = *reinterpret_cast<SealSmem*>(smem_raw);
-        bool sealed_any = false;
-        int64_t u = clo;
+        int64_t u = lo;
         Item it;
-        while (next_item(p, u, chi, it)) {
+        while (next_item(p, u, hi, it)) {
             if (it.type != 2) continue;
             const SeqEntry& e = p.seqs[it.ci];
             const size_t sl = (size_t)e.seq * p.num_layers + p.layer;
             const size_t rows0 = (sl * p.hkv + it.kvh) * 128;
             uint8_t* dst = p.base + p.lay.pool + (size_t)e.seal_slot * p.slot_bytes + (size_t)it.kvh * pair;
-            if (t < kSealThreads) {  // the seal runs on 8 warps (barrier 2)
+            if (t < kSealThreads) {  // the seal runs on 8 warps (barrier 2); the others wait below
                 SealRows rk{reinterpret_cast<const uint16_t*>(p.base + p.lay.tail_k) + rows0 * 128,
                             p.k_new + ((size_t)it.ci * p.hkv + it.kvh) * 128};
-                seal_matrix(rk, p.k_bits, 0, p.iters, dst, nullptr, S, 2);
+                seal_matrix(rk, p.k_bits, 0, p.iters, dst, nullptr, *sm.seal, 2);
                 SealRows rv{reinterpret_cast<const uint16_t*>(p.base + p.lay.tail_v) + rows0 * 128,
                             p.v_new + ((size_t)it.ci * p.hkv + it.kvh) * 128};
-                seal_matrix(rv, p.v_bits, 1, p.iters, dst + p.rec_k, nullptr, S, 2);
+                seal_matrix(rv, p.v_bits, 1, p.iters, dst + p.rec_k, nullptr, *sm.seal, 2);
             }
             if (t == 0 && it.kvh == 0) {
                 int32_t* table = reinterpret_cast<int32_t*>(p.base + p.lay.block_table);
@@ -817,48 +877,30 @@ __global__ void __launch_bounds__(kDecodeThreads, 1) decode_kernel(const __grid_
             }
             sealed_any = true;
         }
-        if (sealed_any) fence_proxy_async_global();  // the records just written are read by bulk copies
+    }
+    if (sealed_any) {
+        fence_proxy_async_global();  // the records just written are read by bulk copies
         __syncthreads();
     }
-    if (w >= nw) return;
 
-    // ---- 2. this warp's worker range
-    const int64_t gw = b * nw + w;
-    const int64_t lo = gw * U / W, hi = (gw + 1) * U / W;
-    WarpSmem ws;
-    ws.kstage = smem_raw + (size_t)w * pair;
-    ws.vstage = ws.kstage + p.rec_k;
-    ws.full_k = bars + w;
-    ws.full_v = bars + kWarps + w;
-    {
-        uint8_t* r = regions + (size_t)w * kWarpRegion;
-        ws.xb = reinterpret_cast<float*>(r);
-        ws.bqs = reinterpret_cast<float4*>(r + kXbWarp * 4);
-        ws.qrot = reinterpret_cast<float*>(r + kXbWarp * 4 + 8 * 32 * 16);
-        ws.qmax = reinterpret_cast<float*>(r + kXbWarp * 4 + 8 * 32 * 16 + 512 * 4);
-    }
+    // ---- 2. prologue: the first S groups of the stream
     GroupCursor cur;
     cur.init(lo);
-    const uint8_t* next_src = nullptr;  // lane 0: record pair of the next group to request
-    if (lane == 0) {
-        next_src = cur.src(p, hi, 0);
-        if (next_src) {
-            mbar_arrive_expect_tx(ws.full_k, p.rec_k);
-            bulk_g2s(ws.kstage, next_src, p.rec_k, ws.full_k);
-            mbar_arrive_expect_tx(ws.full_v, p.rec_v);
-            bulk_g2s(ws.vstage, next_src + p.rec_k, p.rec_v, ws.full_v);
-        }
+    for (uint32_t gn = w; gn < (uint32_t)p.stages; gn += kWarps) {
+        if (lane == 0) issue_group(p, sm, cur, hi, gn);
+        __syncwarp();
     }
 
+    // ---- 3. items in order
     const int g = lane >> 2, tq = lane & 3;
     int64_t u = lo;
     Item it;
-    uint32_t n = 0;  // groups consumed by this warp
+    uint32_t n = 0;
     while (next_item(p, u, hi, it)) {
         const SeqEntry& e = p.seqs[it.ci];
         const int blk = e.seq * p.hkv + it.kvh;
         if (it.type == 1) {
-            exact_item_warp(p, ws, it.ci, it.kvh, it.g0, lane);
+            exact_item(p, sm, it.ci, it.kvh);
             continue;
         }
         int slot;
@@ -867,53 +909,41 @@ __global__ void __launch_bounds__(kDecodeThreads, 1) decode_kernel(const __grid_
         } else {
             int64_t first;
             expected_partials(p, e, it.kvh, &first);
-            slot = kSlotChunk0 + (int)(gw - first);
+            slot = kSlotChunk0 + (int)(b - first);
             if (slot >= kPartialSlots) {  // cannot happen with the host's schedule
-                if (lane == 0) atomicOr(err, kErrSpan);
+                if (t == 0) atomicOr(err, kErrSpan);
                 slot = kPartialSlots - 1;
             }
         }
-        setup_query_warp<KB>(p, ws, it.ci, it.kvh, lane);
-        const float qm = ws.qmax[tq];
+        setup_query<KB>(p, sm, it.ci, it.kvh);
+        const float qm = sm.qmax[tq];
         WarpState st;
         st.m = kNegInf;
         st.l = 0.f;
 #pragma unroll
         for (int mt = 0; mt < 8; ++mt) st.acc[mt][0] = st.acc[mt][1] = 0.f;
+        float* xb = sm.xbuf + w * kXbWarp;
         const uint32_t cnt = (uint32_t)(it.g1 - it.g0);
-        for (uint32_t k = 0; k < cnt; ++k, ++n) {
-            const uint32_t par = n & 1;
-            mbar_wait(ws.full_k, par, err);
-            auto k_done = [&]() {
-                if (lane == 0) {
-                    next_src = cur.src(p, hi, n + 1);
-                    if (next_src) {
-                        mbar_arrive_expect_tx(ws.full_k, p.rec_k);
-                        bulk_g2s(ws.kstage, next_src, p.rec_k, ws.full_k);
-                    }
-                }
-            };
-            auto v_wait = [&]() { mbar_wait(ws.full_v, par, err); };
-            process_group<KB, VB>(p, ws.kstage, ws.vstage, ws.bqs, qm, ws.xb, st, g, tq, lane, k_done, v_wait);
+        for (uint32_t k = (w + kWarps - (n % kWarps)) % kWarps; k < cnt; k += kWarps) {
+            const uint32_t gn = n + k;
+            const uint32_t s = gn % p.stages;
+            mbar_wait(sm.full + s, (gn / p.stages) & 1, err);
+            process_group<KB, VB>(p, sm.stages + (size_t)s * pair, sm.bqs, qm, xb, st, g, tq, lane);
             __syncwarp();
-            if (lane == 0 && next_src) {
-                mbar_arrive_expect_tx(ws.full_v, p.rec_v);
-                bulk_g2s(ws.vstage, next_src + p.rec_k, p.rec_v, ws.full_v);
-            }
+            if (lane == 0) issue_group(p, sm, cur, hi, gn + p.stages);
+            __syncwarp();
         }
-        write_partial_warp(p, st, blk, slot, lane);
-        publish_warp(p, it.ci, it.kvh, lane);
+        n += cnt;
+        write_item_partial(p, sm, st, blk, slot);
+        publish(p, sm, it.ci, it.kvh);
     }
     // Normally every copy was waited for above. After a wait that gave up, let the
     // copies still in flight land (bounded) before the CTA's shared memory goes away.
-    if (lane == 0 && (*reinterpret_cast<volatile int32_t*>(err) & kErrTimeout)) {
+    if (t == 0 && (*reinterpret_cast<volatile int32_t*>(err) & kErrTimeout)) {
         const uint64_t t0 = global_ns();
-        if (n > 0) {
-            while (!mbar_try_wait(ws.full_k, (n - 1) & 1) && global_ns() - t0 < kWaitLimitNs) {
+        for (uint32_t k = n > (uint32_t)p.stages ? n - p.stages : 0; k < n; ++k)
+            while (!mbar_try_wait(sm.full + (k % p.stages), (k / p.stages) & 1) && global_ns() - t0 < kWaitLimitNs) {
             }
-            while (!mbar_try_wait(ws.full_v, (n - 1) & 1) && global_ns() - t0 < kWaitLimitNs) {
-            }
-        }
     }
 }
 
@@ -932,18 +962,19 @@ int launch_t(const DecodeParams& p, int smem, cudaStream_t s) {
 
 }  // namespace
 
-int decode_smem_bytes(int k_bits, int v_bits, int warps, bool with_seal) {
-    (void)with_seal;  // the seal scratch aliases the stage area
+int decode_smem_bytes(int k_bits, int v_bits, int stages, bool with_seal) {
+    (void)with_seal;  // the seal scratch aliases the stage ring
     size_t pair = record_bytes(k_bits) + record_bytes(v_bits);
-    size_t ring = (size_t)warps * pair;
-    if (ring < sizeof(SealSmem)) ring = sizeof(SealSmem);
-    ring = (ring + 127) & ~(size_t)127;
-    return (int)(ring + 256 + (size_t)warps * kWarpRegion);
+    size_t off = (size_t)stages * pair;
+    if (off < sizeof(SealSmem)) off = sizeof(SealSmem);
+    off = (off + 15) & ~(size_t)15;
+    off += 32 * 8 + 512 * 4 + 16 + 16 + 8 * 32 * 16 + kWarps * kXbWarp * 4 + kWarps * kMrgFloats * 4;
+    return (int)off;
 }
 
 // ---------------------------------------------------------------------------
 // Static split-K workspace for kvarn_decode_attention_noalloc: partial softmax states
-// and merge tickets of up to kStaticBlocks (sequence, KV head) blocks, 14.3 MB per GPU
+// and merge tickets of up to kStaticBlocks (sequence, KV head) blocks, 9.2 MB per GPU
 // that loads the library, held until the process exits. Host code must not pass the
 // symbol itself to a kernel (in host code it names a host-side shadow): the device
 // address is fetched once per device with cudaGetSymbolAddress, with that device

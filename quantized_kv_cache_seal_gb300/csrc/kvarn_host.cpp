@@ -118,11 +118,11 @@ kvarn_status check_ids(const kvarn_cache* c, int32_t layer, int32_t n, const int
     return KVARN_OK;
 }
 
-// Units charged for one exact sub-item (up to 64 sink/tail tokens on one warp's CUDA
-// cores) relative to one sealed group pair: about two group pairs at 2/2 bits.
-int exact_sub_units(const kvarn_cache* c) {
-    const double pair = (double)(c->rec_k + c->rec_v);
-    return std::max(1, (int)std::lround(2.0 * 9248.0 / pair));
+// Units charged for an exact item (sink + tail tokens) relative to one sealed group
+// pair: the exact tokens move 512 bytes each (K and V fp16) on the CUDA cores.
+int exact_units(const kvarn_cache* c, int n_exact) {
+    double pair = (double)(c->rec_k + c->rec_v);
+    return std::max(1, (int)std::ceil(n_exact * 512.0 / pair * 0.6));
 }
 
 int seal_units(const kvarn_cache* c) {
@@ -134,29 +134,25 @@ int seal_units(const kvarn_cache* c) {
 // covering CTA of unit u when U units are split evenly over P CTAs
 inline int64_t covering(int64_t u, int64_t U, int64_t P) { return ((u + 1) * P + U - 1) / U - 1; }
 
-// Fill the schedule of a decode call: per sequence unit offsets, grid size. The units
-// are split evenly over P CTAs x nw worker warps.
+// Fill the schedule of a decode call: per sequence unit offsets, grid size.
 kvarn_status schedule(kvarn_cache* c, DecodeParams& p) {
     int64_t U = 0;
+    int64_t max_groups = 0;
     for (int i = 0; i < p.n_seqs; ++i) {
         SeqEntry& e = p.seqs[i];
         e.unit_begin = (int32_t)U;
-        const int n_ex = e.n_sink + e.n_tail;
-        const int n_sub = std::max(1, (n_ex + kExactSub - 1) / kExactSub);
-        e.w_sub = exact_sub_units(c);
-        int we = n_sub * e.w_sub;
+        int we = exact_units(c, e.n_sink + e.n_tail);
         int ws = e.seal_group >= 0 ? seal_units(c) : 0;
         e.w_exact = we;
         e.w_seal = ws;
         U += (int64_t)p.hkv * (we + ws + e.n_groups);
+        max_groups = std::max<int64_t>(max_groups, e.n_groups);
     }
     if (U >= (1ll << 31)) return KVARN_ECAPACITY;
     p.units_total = U;
-    const int64_t nw = p.warps;
-    int64_t P = std::min<int64_t>(c->sms, std::max<int64_t>(1, (U + 6 * nw - 1) / (6 * nw)));
+    int64_t P = std::min<int64_t>(c->sms, std::max<int64_t>(1, U / 24));
     // every block's sealed groups must fit in kMaxSpan partial slots
     for (;;) {
-        const int64_t W = P * nw;
         bool ok = true;
         for (int i = 0; i < p.n_seqs && ok; ++i) {
             const SeqEntry& e = p.seqs[i];
@@ -164,10 +160,10 @@ kvarn_status schedule(kvarn_cache* c, DecodeParams& p) {
             for (int h = 0; h < p.hkv && ok; ++h) {
                 int64_t g0 = e.unit_begin + (int64_t)h * (e.w_exact + e.w_seal + e.n_groups) + e.w_exact + e.w_seal;
                 int64_t g1 = g0 + e.n_groups - 1;
-                if (covering(g1, U, W) - covering(g0, U, W) + 1 > kMaxSpan) ok = false;
+                if (covering(g1, U, P) - covering(g0, U, P) + 1 > kMaxSpan) ok = false;
             }
         }
-        if (ok || P == 1) break;
+        if (ok) break;
         P = std::max<int64_t>(1, P * 3 / 4);
     }
     p.grid = (int)P;
@@ -251,18 +247,19 @@ kvarn_status run_decode(kvarn_cache* c, int32_t layer, int32_t n_seqs, const int
         e.n_groups = (int32_t)groups_sealed(n) - (e.seal_group >= 0 ? 1 : 0);
         e.n_tail = n > kSink ? (int32_t)((n - kSink) % kGroup) : 0;
     }
-    int warps = kDecodeThreads / 32;
-    while (warps > 1 && decode_smem_bytes(cfg.k_bits, cfg.v_bits, warps, any_seal) > c->max_smem) --warps;
-    if (decode_smem_bytes(cfg.k_bits, cfg.v_bits, warps, any_seal) > c->max_smem) {
-        for (int32_t s : taken) c->free_slots.push_back(s);
-        return KVARN_ECAPACITY;
-    }
-    p.warps = warps;
     st = schedule(c, p);
     if (st) {
         for (int32_t s : taken) c->free_slots.push_back(s);
         return st;
     }
+    int pair = (int)(c->rec_k + c->rec_v);
+    int stages = 32;
+    while (stages > 1 && decode_smem_bytes(cfg.k_bits, cfg.v_bits, stages, any_seal) > c->max_smem) --stages;
+    if (decode_smem_bytes(cfg.k_bits, cfg.v_bits, stages, any_seal) > c->max_smem) {
+        for (int32_t s : taken) c->free_slots.push_back(s);
+        return KVARN_ECAPACITY;
+    }
+    p.stages = stages;
     if (ws) {
         // offsets from the cache base that land on the static workspace (modulo 2^64)
         p.lay.partials = (size_t)((uintptr_t)ws->partials - (uintptr_t)c->base);
@@ -274,7 +271,7 @@ kvarn_status run_decode(kvarn_cache* c, int32_t layer, int32_t n_seqs, const int
     if (!c->host_only) {
         st = ensure_init(c, stream);
         if (st) return st;
-        int rc = launch_decode(p, decode_smem_bytes(cfg.k_bits, cfg.v_bits, warps, any_seal), stream);
+        int rc = launch_decode(p, decode_smem_bytes(cfg.k_bits, cfg.v_bits, stages, any_seal), stream);
         if (rc) { set_cuda_error(rc, "decode launch"); return KVARN_ECUDA; }
     }
     if (step) {

@@ -17,11 +17,10 @@ constexpr int kHeadDim = 128;
 constexpr int kGroup = 128;
 constexpr int kSink = 128;
 constexpr int kMaxBatch = 256;   // sequences per decode call (kernel parameter table size)
-constexpr int kMaxSpan = 48;     // worker warps that may share the sealed groups of one (seq, kv head)
-constexpr int kExactSub = 64;    // exact (sink + tail) tokens per exact sub-item
-constexpr int kMaxExactSubs = 4; // partial slots 0..3: exact sub-items (original frame)
-constexpr int kSlotSeal = 4;     // partial slot of the group sealed inside a decode step
-constexpr int kSlotChunk0 = 5;   // first partial slot of sealed-group chunks
+constexpr int kMaxSpan = 32;     // CTAs that may share the sealed groups of one (seq, kv head)
+constexpr int kSlotExact = 0;    // partial slot of the exact (sink + tail) part
+constexpr int kSlotSeal = 1;     // partial slot of the group sealed inside a decode step
+constexpr int kSlotChunk0 = 2;   // first partial slot of sealed-group chunks
 constexpr int kPartialSlots = kSlotChunk0 + kMaxSpan;
 constexpr int kPartialFloats = 528;  // [0] epoch bits, [4..8) m, [8..12) l, [12..524) acc
 constexpr int kDecodeThreads = 384;  // 12 warps
@@ -55,8 +54,7 @@ struct SeqEntry {
     int32_t seal_group;  // group completed by the new token, -1 if none
     int32_t seal_slot;   // pool slot taken for it
     int32_t unit_begin;  // first scheduling unit of this sequence
-    int32_t w_exact;     // units of the exact part of each (seq, kv head): n_sub * w_sub
-    int32_t w_sub;       // units charged per exact sub-item (up to 64 exact tokens)
+    int32_t w_exact;     // units charged for the exact item of each (seq, kv head)
     int32_t w_seal;      // units charged for the seal item (0 if none)
 };
 
@@ -70,7 +68,7 @@ struct DecodeParams {
     const uint16_t* v_new;
     int32_t n_seqs, hq, hkv, r, k_bits, v_bits, iters, layer, num_layers, max_seqs, max_groups;
     int32_t rec_k, rec_v, slot_bytes, pool_slots;
-    int32_t warps;              // worker warps per CTA (<= 12)
+    int32_t stages;             // smem ring stages
     int32_t grid;               // CTAs
     int64_t units_total;
     uint32_t epoch;
@@ -125,7 +123,7 @@ int launch_seal_groups(const void* x, int n, int bits, int which, int iters, voi
                        void* stream);
 int launch_dequant(const uint8_t* rec, int bits, int which, int frame, int out_fp32, void* out, void* stream);
 int launch_init(uint8_t* base, const Layout& lay, void* stream);
-int decode_smem_bytes(int k_bits, int v_bits, int warps, bool with_seal);
+int decode_smem_bytes(int k_bits, int v_bits, int stages, bool with_seal);
 int max_optin_smem();
 int sm_count();
 const char* cuda_error_string(int code);
