@@ -155,7 +155,7 @@ struct Smem {
     uint8_t* stages;
     uint64_t* full;
     float* qrot;    // [4][128] rotated query / its max
-    float4* bqs;    // [8][32]: lane l's query operand base, q_hat * 2^-ex, in fragment order
+    uint4* qtab;    // [3 kinds][4][32 lanes]: query operand table (setup_query)
     float* qmax;    // [4]
     float* xbuf;    // [8 warps][kXbWarp] (half2 words)
     float* mrg;     // [8 warps][kMrgFloats], also exact-part and final-merge scratch
@@ -462,8 +462,11 @@ __device__ void exact_item(const DecodeParams& p, const Smem& sm, int ci, int kv
 }
 
 // Rotate the query of a block: qrot = (q H) / max|q H| per head, qmax = that max; then
-// the table of each lane's query operand base q_hat(head g>>1, channel) * 2^-ex in the
-// pair order of its MMA fragments (the codes' power-of-two offsets folded in).
+// the table from which every lane builds its query operand for a group. Lane (g, tq)
+// holds column g of the MMA (head g >> 1, part g & 1) for the channels of pair P of
+// chunk tq; with v = q_hat * 2^-ex (the codes' power-of-two offset folded in) split
+// into f16 parts v = vh + vl, the table holds per pair: vh, -vh on a low-part lane
+// (0 on a high-part lane) and vl on a low-part lane (0 on a high-part lane).
 template <int KB>
 __device__ void setup_query(const DecodeParams& p, const Smem& sm, int ci, int kvh) {
     using CK = Codes<KB>;
@@ -488,27 +491,40 @@ __device__ void setup_query(const DecodeParams& p, const Smem& sm, int ci, int k
     }
     named_bar(1, kConsumers);
     if (t < 256) {
-        // entry q (0..7) of lane l: pairs P = 2q, 2q+1 of lane l = (g, tq)
+        // thread (q, lane) writes pairs P = 2q, 2q + 1 of lane (g, tq)
         const int q = t >> 5, g = lane >> 2, tq = lane & 3;
+        const bool lo_lane = (g & 1) != 0;
         const float* qh = sm.qrot + 128 * (g >> 1);
-        float vals[4];
+        uint32_t hi2[2], neg2[2], lo2[2];
 #pragma unroll
         for (int e = 0; e < 2; ++e) {
             const int P = 2 * q + e;
             const int x = P % CK::HALF;
             const int c0 = 32 * tq + CK::CPW * (P / CK::HALF) + x;
             const float sc = __int_as_float((127 - CK::ex(x)) << 23);  // 2^-ex
-            vals[2 * e] = qh[c0] * sc;
-            vals[2 * e + 1] = qh[c0 + CK::HALF] * sc;
+            const float v0 = qh[c0] * sc, v1 = qh[c0 + CK::HALF] * sc;
+            const __half2 h = __floats2half2_rn(v0, v1);
+            const float2 hf = __half22float2(h);
+            const __half2 l = __floats2half2_rn(v0 - hf.x, v1 - hf.y);
+            hi2[e] = h2_bits(h);
+            neg2[e] = lo_lane ? h2_bits(__hneg2(h)) : 0u;
+            lo2[e] = lo_lane ? h2_bits(l) : 0u;
         }
-        sm.bqs[q * 32 + lane] = make_float4(vals[0], vals[1], vals[2], vals[3]);
+        uint32_t* tab = reinterpret_cast<uint32_t*>(sm.qtab);
+        const int word = 2 * (q & 1);  // pairs 4k .. 4k + 3 share one 16-byte entry
+#pragma unroll
+        for (int kind = 0; kind < 3; ++kind) {
+            const uint32_t* src = kind == 0 ? hi2 : (kind == 1 ? neg2 : lo2);
+            uint32_t* dst = tab + 4 * ((kind * 4 + (q >> 1)) * 32 + lane) + word;
+            *reinterpret_cast<uint2*>(dst) = make_uint2(src[0], src[1]);
+        }
     }
     named_bar(1, kConsumers);
 }
 
 struct WarpState {
     float m, l;
-    float acc[8][2];
+    float2 acc[8];  // channels 16 mt + g and 16 mt + g + 8 of head tq
 };
 
 __device__ __forceinline__ float fast_exp2(float x) {
@@ -526,6 +542,26 @@ __device__ __forceinline__ uint32_t pair_operand(const uint32_t* w, int P) {
     return (w[word] >> C::sh(x)) & C::mask(x);
 }
 
+// f16 pair (c[c0], c[c0 + HALF]) of the channel scales of pair P, from the scales of a
+// 32-channel chunk held as 16 half2 words.
+template <int B>
+__device__ __forceinline__ __half2 pair_scales(const uint32_t* cw, int P) {
+    using C = Codes<B>;
+    const int c0 = C::CPW * (P / C::HALF) + P % C::HALF, c1 = c0 + C::HALF;
+    const int b0 = 2 * (c0 & 1), b1 = 4 + 2 * (c1 & 1);
+    return bits_h2(__byte_perm(cw[c0 >> 1], cw[c1 >> 1], b0 | (b0 + 1) << 4 | b1 << 8 | (b1 + 1) << 12));
+}
+
+// A operand whose every element is 2^e (rows identical): multiplies a B fragment into
+// its per-column sum, undoing the power-of-two offsets folded into B.
+__host__ __device__ constexpr uint32_t pow2_pair(int e) { return (uint32_t)((15 + e) << 10) * 0x10001u; }
+
+__device__ __forceinline__ float fmax3(float a, float b, float c) {
+    float d;
+    asm("max.f32 %0, %1, %2, %3;" : "=f"(d) : "f"(a), "f"(b), "f"(c));
+    return d;
+}
+
 // Tiles processed together, k-step outer: TG independent MMA chains, TG * 2 * B
 // code words live in registers.
 template <int B>
@@ -535,7 +571,7 @@ struct TileGroup {
 
 // Process one sealed group pair held in shared memory (K record, then V record).
 template <int KB, int VB>
-__device__ __forceinline__ void process_group(const DecodeParams& p, const uint8_t* rec, const float4* bqs,
+__device__ __forceinline__ void process_group(const DecodeParams& p, const uint8_t* rec, const uint4* qtab,
                                               float qm, float* xb, WarpState& st, int g, int tq, int lane) {
     using CK = Codes<KB>;
     using CV = Codes<VB>;
@@ -548,10 +584,10 @@ __device__ __forceinline__ void process_group(const DecodeParams& p, const uint8
     const uint16_t* aK = reinterpret_cast<const uint16_t*>(krec + 16);
     const uint16_t* aV = reinterpret_cast<const uint16_t*>(vrec + 16);
     const uint16_t* cV = reinterpret_cast<const uint16_t*>(vrec + 272);
-    // ---- query operand of this group: q_hat * c_K * 2^-ex, split into f16 high / low parts.
-    // |q_hat| <= 1, c_K <= 65504 and 2^-ex <= 1, so the operand can never overflow f16.
+    // ---- query operand of this group, (v c_K) split into f16 high / low parts:
+    // high lane: RN(vh c); low lane: RN(vl c + (vh c - RN(vh c))), the residual being
+    // exact in f16. |v| <= 1 and c_K <= 65504, so nothing overflows.
     uint32_t bk[16];
-    float sumqc;
     {
         const uint4* cp = reinterpret_cast<const uint4*>(krec + 272 + 64 * tq);
         uint32_t cw[16];
@@ -560,35 +596,36 @@ __device__ __forceinline__ void process_group(const DecodeParams& p, const uint8
             uint4 v = cp[k];
             cw[4 * k] = v.x; cw[4 * k + 1] = v.y; cw[4 * k + 2] = v.z; cw[4 * k + 3] = v.w;
         }
-        float bq[32];
 #pragma unroll
-        for (int q = 0; q < 8; ++q) {
-            const float4 v = bqs[q * 32 + lane];
-            bq[4 * q] = v.x; bq[4 * q + 1] = v.y; bq[4 * q + 2] = v.z; bq[4 * q + 3] = v.w;
-        }
-        const bool lo_part = (g & 1) != 0;
-        float sum = 0.f;
+        for (int k = 0; k < 4; ++k) {
+            const uint4 th = qtab[k * 32 + lane];
+            const uint4 tn = qtab[(4 + k) * 32 + lane];
+            const uint4 tl = qtab[(8 + k) * 32 + lane];
+            const uint32_t vh[4] = {th.x, th.y, th.z, th.w};
+            const uint32_t vn[4] = {tn.x, tn.y, tn.z, tn.w};
+            const uint32_t vl[4] = {tl.x, tl.y, tl.z, tl.w};
 #pragma unroll
-        for (int P = 0; P < 16; ++P) {
-            const int x = P % CK::HALF;
-            const int c0 = CK::CPW * (P / CK::HALF) + x;
-            const int c1 = c0 + CK::HALF;
-            const float f0 = bq[2 * P] * __half2float(reinterpret_cast<const __half*>(cw)[c0]);
-            const float f1 = bq[2 * P + 1] * __half2float(reinterpret_cast<const __half*>(cw)[c1]);
-            const __half2 hi = __floats2half2_rn(f0, f1);
-            const float2 hf = __half22float2(hi);
-            const uint32_t lo = h2_bits(__floats2half2_rn(f0 - hf.x, f1 - hf.y));
-            bk[P] = lo_part ? lo : h2_bits(hi);
-            const float sc = __int_as_float((127 + CK::ex(x)) << 23);  // 2^ex: back to q_hat * c_K
-            sum = fmaf(f0 + f1, sc, sum);
+            for (int e = 0; e < 4; ++e) {
+                const __half2 c2 = pair_scales<KB>(cw, 4 * k + e);
+                const __half2 r = __hfma2(bits_h2(vh[e]), c2, __hmul2(bits_h2(vn[e]), c2));
+                bk[4 * k + e] = h2_bits(__hfma2(bits_h2(vl[e]), c2, r));
+            }
         }
-        sum += __shfl_xor_sync(0xffffffffu, sum, 1);
-        sum += __shfl_xor_sync(0xffffffffu, sum, 2);
-        // lane 8 tq holds the sum of head tq (its column head is (2 tq) >> 1 = tq)
-        sumqc = __shfl_sync(0xffffffffu, sum, 8 * tq);
     }
-    // ---- scores of the 16 tokens this thread holds (head tq)
-    float S[8][2];
+    // sum_j q_hat_j c_j of head tq: the high and low columns of the operand times 2^ex
+    float sumqc;
+    {
+        float s4[4] = {0.f, 0.f, 0.f, 0.f};
+#pragma unroll
+        for (int ks = 0; ks < 8; ++ks) {
+            const uint32_t a0 = pow2_pair(CK::ex((2 * ks) % CK::HALF));
+            const uint32_t a2 = pow2_pair(CK::ex((2 * ks + 1) % CK::HALF));
+            mma16816(s4, a0, a0, a2, a2, bk[2 * ks], bk[2 * ks + 1]);
+        }
+        sumqc = s4[0] + s4[1];
+    }
+    // ---- raw scores of the 16 tokens this thread holds (head tq): high + low columns
+    float2 S[8];
     {
         constexpr int TG = TileGroup<KB>::TG;
 #pragma unroll
@@ -612,24 +649,22 @@ __device__ __forceinline__ void process_group(const DecodeParams& p, const uint8
                              bk[2 * ks + 1]);
             }
 #pragma unroll
-            for (int i = 0; i < TG; ++i) {
-                S[t0g + i][0] = c[i][0] + c[i][1];
-                S[t0g + i][1] = c[i][2] + c[i][3];
-            }
+            for (int i = 0; i < TG; ++i) S[t0g + i] = make_float2(c[i][0] + c[i][1], c[i][2] + c[i][3]);
         }
     }
+    // ---- scores: scale * a_t * (delta * raw + m * sum_j q_hat_j c_j), log2 domain
     const float alpha = p.scale_log2 * qm * dK * 16777216.0f;  // codes enter as code * 2^(ex-24)
     const float beta = p.scale_log2 * qm * mK * sumqc;
+    const float2 alpha2 = make_float2(alpha, alpha), beta2 = make_float2(beta, beta);
     float gmax = kNegInf;
-    float av[8][2];
+    float2 av[8];
 #pragma unroll
     for (int mt = 0; mt < 8; ++mt) {
         const int t0 = tok_row<VB>(mt, g), t1 = t0 + CV::HALF;
-        S[mt][0] = half_bits_to_float(aK[t0]) * fmaf(alpha, S[mt][0], beta);
-        S[mt][1] = half_bits_to_float(aK[t1]) * fmaf(alpha, S[mt][1], beta);
-        gmax = fmaxf(gmax, fmaxf(S[mt][0], S[mt][1]));
-        av[mt][0] = half_bits_to_float(aV[t0]);
-        av[mt][1] = half_bits_to_float(aV[t1]);
+        const float2 ak = make_float2(half_bits_to_float(aK[t0]), half_bits_to_float(aK[t1]));
+        S[mt] = __fmul2_rn(ak, __ffma2_rn(alpha2, S[mt], beta2));
+        gmax = fmax3(gmax, S[mt].x, S[mt].y);
+        av[mt] = make_float2(half_bits_to_float(aV[t0]), half_bits_to_float(aV[t1]));
     }
     // largest V token scale of the group from its bit patterns (all >= 0): lane l reads 4
     uint32_t amaxb;
@@ -650,20 +685,17 @@ __device__ __forceinline__ void process_group(const DecodeParams& p, const uint8
     const float rho = __int_as_float((127 + 15 - ebits) << 23);
     const int xv = g % CV::HALF;
     const float sv = __int_as_float((127 + kEV - CV::ex(xv)) << 23) * rho;  // 2^(EV - ex) * rho
-    const float svi = __int_as_float((127 - kEV + CV::ex(xv)) << 23);       // 2^(ex - EV)
-    float lsum = 0.f, wsum = 0.f;
+    const float2 sv2 = make_float2(sv, sv), mneg = make_float2(-mnew, -mnew);
+    float2 l2 = make_float2(0.f, 0.f);
 #pragma unroll
     for (int mt = 0; mt < 8; ++mt) {
-        const float p0 = fast_exp2(S[mt][0] - mnew), p1 = fast_exp2(S[mt][1] - mnew);
-        lsum += p0 + p1;
-        const __half2 wh = __floats2half2_rn(p0 * av[mt][0] * sv, p1 * av[mt][1] * sv);
-        const float2 wf = __half22float2(wh);
-        wsum = fmaf(wf.x + wf.y, svi, wsum);
+        const float2 d = __fadd2_rn(S[mt], mneg);
+        const float2 pr = make_float2(fast_exp2(d.x), fast_exp2(d.y));
+        l2 = __fadd2_rn(l2, pr);
+        const __half2 wh = __float22half2_rn(__fmul2_rn(__fmul2_rn(pr, av[mt]), sv2));
         reinterpret_cast<uint32_t*>(xb)[kXbHead * tq + 20 * (mt >> 1) + 8 * (mt & 1) + g] = h2_bits(wh);
     }
-    st.l = fmaf(st.l, corr, lsum);
-#pragma unroll
-    for (int o = 4; o < 32; o <<= 1) wsum += __shfl_xor_sync(0xffffffffu, wsum, o);
+    st.l = fmaf(st.l, corr, l2.x + l2.y);
     __syncwarp();
     uint32_t bv[16];
     {
@@ -675,9 +707,22 @@ __device__ __forceinline__ void process_group(const DecodeParams& p, const uint8
         }
     }
     __syncwarp();
+    // sum_t w_t rho of head tq: the weight operand times 2^(ex - EV)
+    float wsum;
+    {
+        float s4[4] = {0.f, 0.f, 0.f, 0.f};
+#pragma unroll
+        for (int ks = 0; ks < 8; ++ks) {
+            const uint32_t a0 = pow2_pair(CV::ex((2 * ks) % CV::HALF) - kEV);
+            const uint32_t a2 = pow2_pair(CV::ex((2 * ks + 1) % CV::HALF) - kEV);
+            mma16816(s4, a0, a0, a2, a2, bv[2 * ks], bv[2 * ks + 1]);
+        }
+        wsum = s4[0];
+    }
     // ---- P V in the rotated frame
     const float gam = dV * (float)(1 << (24 - kEV)) / rho;
     const float del = mV * wsum / rho;
+    const float2 corr2 = make_float2(corr, corr);
     {
         constexpr int TG = TileGroup<VB>::TG;
 #pragma unroll
@@ -704,8 +749,9 @@ __device__ __forceinline__ void process_group(const DecodeParams& p, const uint8
             for (int i = 0; i < TG; ++i) {
                 const int mt = m0 + i;
                 const int c0 = 16 * mt + g;
-                st.acc[mt][0] = fmaf(st.acc[mt][0], corr, half_bits_to_float(cV[c0]) * fmaf(gam, d[i][0], del));
-                st.acc[mt][1] = fmaf(st.acc[mt][1], corr, half_bits_to_float(cV[c0 + 8]) * fmaf(gam, d[i][2], del));
+                const float2 cv = make_float2(half_bits_to_float(cV[c0]), half_bits_to_float(cV[c0 + 8]));
+                const float2 x = make_float2(fmaf(gam, d[i][0], del), fmaf(gam, d[i][2], del));
+                st.acc[mt] = __ffma2_rn(st.acc[mt], corr2, __fmul2_rn(cv, x));
             }
         }
     }
@@ -724,8 +770,8 @@ __device__ void write_item_partial(const DecodeParams& p, const Smem& sm, const 
     }
 #pragma unroll
     for (int mt = 0; mt < 8; ++mt) {
-        M[8 + 128 * tq + 16 * mt + g] = st.acc[mt][0];
-        M[8 + 128 * tq + 16 * mt + g + 8] = st.acc[mt][1];
+        M[8 + 128 * tq + 16 * mt + g] = st.acc[mt].x;
+        M[8 + 128 * tq + 16 * mt + g + 8] = st.acc[mt].y;
     }
     named_bar(1, kConsumers);
     if (t < 256) {
@@ -754,20 +800,18 @@ __device__ void write_item_partial(const DecodeParams& p, const Smem& sm, const 
     }
 }
 
-__device__ __forceinline__ const uint8_t* group_src(const DecodeParams& p, int seq, int kvh, int g) {
-    const int32_t* table = reinterpret_cast<const int32_t*>(p.base + p.lay.block_table);
-    int slot = table[((size_t)seq * p.num_layers + p.layer) * p.max_groups + g];
-    if (slot < 0 || slot >= p.pool_slots) {
-        atomicOr(err_word(p), kErrBadSlot);
-        slot = 0;
-    }
-    return p.base + p.lay.pool + (size_t)slot * p.slot_bytes + (size_t)kvh * (p.rec_k + p.rec_v);
-}
-
 struct SealRows {
     const uint16_t* tail;  // rows 0..126
     const uint16_t* last;  // row 127: the new token
     __device__ const uint16_t* operator()(int i) const { return i < 127 ? tail + 128 * i : last; }
+};
+
+// Source of a copy being resolved. For a sealed group the block-table entry is loaded
+// one round ahead of the copy, so that its latency overlaps a group's processing.
+struct PendingCopy {
+    const uint8_t* base;  // seal record: its address; sealed group: pool + kv head offset
+    int32_t slot;         // block-table entry of a sealed group (possibly still in flight)
+    bool direct, valid;
 };
 
 // Walks the CTA's sealed groups in stream order to find the record of group number gn
@@ -778,8 +822,13 @@ struct GroupCursor {
     uint32_t base;   // group number of the item's first group
     bool valid;
     __device__ void init(int64_t lo) { u = lo; base = 0; valid = false; it.g0 = it.g1 = 0; }
-    // record address of group gn (gn never decreases between calls); null past the end
-    __device__ const uint8_t* src(const DecodeParams& p, int64_t hi, uint32_t gn) {
+    // source of group gn (gn never decreases between calls); invalid past the end
+    __device__ PendingCopy resolve(const DecodeParams& p, int64_t hi, uint32_t gn) {
+        PendingCopy pc;
+        pc.valid = false;
+        pc.direct = false;
+        pc.slot = 0;
+        pc.base = nullptr;
         for (;;) {
             if (valid && gn < base + (uint32_t)(it.g1 - it.g0)) break;
             if (valid) base += (uint32_t)(it.g1 - it.g0);
@@ -789,22 +838,36 @@ struct GroupCursor {
             while (next_item(p, u, hi, n)) {
                 if (n.type != 1) { found = true; break; }
             }
-            if (!found) return nullptr;
+            if (!found) return pc;
             it = n;
             valid = true;
         }
         const SeqEntry& e = p.seqs[it.ci];
-        const int pair = p.rec_k + p.rec_v;
-        if (it.type == 2)
-            return p.base + p.lay.pool + (size_t)e.seal_slot * p.slot_bytes + (size_t)it.kvh * pair;
-        return group_src(p, e.seq, it.kvh, it.g0 + (int)(gn - base));
+        const size_t pair = (size_t)(p.rec_k + p.rec_v);
+        pc.valid = true;
+        if (it.type == 2) {
+            pc.direct = true;
+            pc.base = p.base + p.lay.pool + (size_t)e.seal_slot * p.slot_bytes + (size_t)it.kvh * pair;
+        } else {
+            const int32_t* table = reinterpret_cast<const int32_t*>(p.base + p.lay.block_table);
+            pc.base = p.base + p.lay.pool + (size_t)it.kvh * pair;
+            pc.slot = table[((size_t)e.seq * p.num_layers + p.layer) * p.max_groups + it.g0 + (int)(gn - base)];
+        }
+        return pc;
     }
 };
 
-__device__ __forceinline__ void issue_group(const DecodeParams& p, const Smem& sm, GroupCursor& cur, int64_t hi,
-                                            uint32_t gn) {
-    const uint8_t* src = cur.src(p, hi, gn);
-    if (!src) return;
+__device__ __forceinline__ void issue_copy(const DecodeParams& p, const Smem& sm, const PendingCopy& pc, uint32_t gn) {
+    if (!pc.valid) return;
+    const uint8_t* src = pc.base;
+    if (!pc.direct) {
+        int slot = pc.slot;
+        if (slot < 0 || slot >= p.pool_slots) {
+            atomicOr(err_word(p), kErrBadSlot);
+            slot = 0;
+        }
+        src += (size_t)slot * p.slot_bytes;
+    }
     const uint32_t pair = (uint32_t)(p.rec_k + p.rec_v);
     const uint32_t s = gn % p.stages;
     mbar_arrive_expect_tx(sm.full + s, pair);
@@ -835,8 +898,8 @@ __global__ void __launch_bounds__(kDecodeThreads, 1) decode_kernel(const __grid_
         off += 16;
         sm.flag = reinterpret_cast<int*>(smem_raw + off);
         off += 16;
-        sm.bqs = reinterpret_cast<float4*>(smem_raw + off);
-        off += 8 * 32 * 16;
+        sm.qtab = reinterpret_cast<uint4*>(smem_raw + off);
+        off += 12 * 32 * 16;
         sm.xbuf = reinterpret_cast<float*>(smem_raw + off);
         off += kWarps * kXbWarp * 4;
         sm.mrg = reinterpret_cast<float*>(smem_raw + off);
@@ -886,10 +949,13 @@ __global__ void __launch_bounds__(kDecodeThreads, 1) decode_kernel(const __grid_
     // ---- 2. prologue: the first S groups of the stream
     GroupCursor cur;
     cur.init(lo);
-    for (uint32_t gn = w; gn < (uint32_t)p.stages; gn += kWarps) {
-        if (lane == 0) issue_group(p, sm, cur, hi, gn);
-        __syncwarp();
+    PendingCopy pend;
+    pend.valid = false;
+    if (lane == 0) {
+        for (uint32_t gn = w; gn < (uint32_t)p.stages; gn += kWarps) issue_copy(p, sm, cur.resolve(p, hi, gn), gn);
+        pend = cur.resolve(p, hi, w + p.stages);  // this warp's first copy inside the loop
     }
+    __syncwarp();
 
     // ---- 3. items in order
     const int g = lane >> 2, tq = lane & 3;
@@ -921,16 +987,19 @@ __global__ void __launch_bounds__(kDecodeThreads, 1) decode_kernel(const __grid_
         st.m = kNegInf;
         st.l = 0.f;
 #pragma unroll
-        for (int mt = 0; mt < 8; ++mt) st.acc[mt][0] = st.acc[mt][1] = 0.f;
+        for (int mt = 0; mt < 8; ++mt) st.acc[mt] = make_float2(0.f, 0.f);
         float* xb = sm.xbuf + w * kXbWarp;
         const uint32_t cnt = (uint32_t)(it.g1 - it.g0);
         for (uint32_t k = (w + kWarps - (n % kWarps)) % kWarps; k < cnt; k += kWarps) {
             const uint32_t gn = n + k;
             const uint32_t s = gn % p.stages;
             mbar_wait(sm.full + s, (gn / p.stages) & 1, err);
-            process_group<KB, VB>(p, sm.stages + (size_t)s * pair, sm.bqs, qm, xb, st, g, tq, lane);
+            process_group<KB, VB>(p, sm.stages + (size_t)s * pair, sm.qtab, qm, xb, st, g, tq, lane);
             __syncwarp();
-            if (lane == 0) issue_group(p, sm, cur, hi, gn + p.stages);
+            if (lane == 0) {
+                issue_copy(p, sm, pend, gn + p.stages);
+                pend = cur.resolve(p, hi, gn + kWarps + p.stages);
+            }
             __syncwarp();
         }
         n += cnt;
@@ -968,7 +1037,7 @@ int decode_smem_bytes(int k_bits, int v_bits, int stages, bool with_seal) {
     size_t off = (size_t)stages * pair;
     if (off < sizeof(SealSmem)) off = sizeof(SealSmem);
     off = (off + 15) & ~(size_t)15;
-    off += 32 * 8 + 512 * 4 + 16 + 16 + 8 * 32 * 16 + kWarps * kXbWarp * 4 + kWarps * kMrgFloats * 4;
+    off += 32 * 8 + 512 * 4 + 16 + 16 + 12 * 32 * 16 + kWarps * kXbWarp * 4 + kWarps * kMrgFloats * 4;
     return (int)off;
 }
 
