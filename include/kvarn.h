@@ -159,7 +159,7 @@ kvarn_status kvarn_decode_step(kvarn_cache* cache, int32_t layer, int32_t n_seqs
  * static device array of the library instead; it allocates and frees nothing.
  * The KVarN pages have no counterpart of this call; it is an interface addition.
  * Limit: max_seqs * num_kv_heads of the cache <= 128 (the array holds 128 blocks of
- * 34 partial states, 9.2 MB per GPU, kept until the process exits); a larger cache is
+ * 32 partial states, 8.7 MB per GPU, kept until the process exits); a larger cache is
  * rejected with KVARN_ECAPACITY and a message in kvarn_last_error.
  * The first call on a device looks up the array's device address (cudaGetSymbolAddress,
  * with that device current); make that first call before any stream capture.

@@ -44,9 +44,10 @@ namespace {
 constexpr int kEV = 13;      // weight operand exponent: |B| < 2^14
 constexpr int kXbHead = 88;  // exchange buffer words per head (bank-conflict-free stride)
 constexpr int kXbWarp = 4 * kXbHead;
-constexpr int kMrgFloats = 8 + 512;  // per warp: m[4], l[4], acc[4][128]
 constexpr int kWarps = kDecodeThreads / 32;  // 12
-constexpr int kConsumers = kDecodeThreads;
+constexpr int kRowPitch = 272;                // shared-memory pitch of an exact fp16 row (conflict-free ldmatrix)
+constexpr int kExactVOff = kExactRows * kRowPitch;  // V rows of an exact sub-group follow its K rows
+constexpr int kTabWords = 12 * 32;            // uint4 entries of one query operand table
 constexpr int kMaxDevices = 64;
 #define kNegInf (-__int_as_float(0x7f800000))
 
@@ -111,55 +112,73 @@ __device__ __forceinline__ int tok_row(int mt, int g) {
 
 __device__ __forceinline__ int64_t covering(int64_t u, int64_t U, int64_t P) { return ((u + 1) * P + U - 1) / U - 1; }
 
+// The part of one (sequence, KV head) block that a CTA's unit range covers. Its stream
+// entries, in order: n_ex exact sub-groups (the CTA that covers the block's first unit
+// owns the exact part), the group sealed in this step (if the CTA covers the seal unit),
+// then sealed groups g0 .. g1.
 struct Item {
-    int type;  // 1 exact, 2 seal, 3 chunk of sealed groups
     int ci;    // index of the sequence in the call
     int kvh;
+    int owner;  // covers the block's first unit (and so its exact part)
+    int n_ex, seal;
     int g0, g1;
+    __device__ int count() const { return n_ex + seal + g1 - g0; }
 };
 
-// Next item of this CTA's unit range [u, hi); advances u.
+// Next item of this CTA's unit range [u, hi); advances u. Every block the range touches
+// is an item, even one without stream entries: it still writes a (neutral) partial.
 __device__ bool next_item(const DecodeParams& p, int64_t& u, int64_t hi, Item& it) {
-    while (u < hi) {
-        int lo = 0, up = p.n_seqs - 1;
-        while (lo < up) {
-            int mid = (lo + up + 1) >> 1;
-            if (p.seqs[mid].unit_begin <= u) lo = mid; else up = mid - 1;
-        }
-        const SeqEntry& e = p.seqs[lo];
-        const int per = e.w_exact + e.w_seal + e.n_groups;
-        const int64_t rel = u - e.unit_begin;
-        const int kvh = (int)(rel / per);
-        const int off = (int)(rel % per);
-        const int64_t blk0 = e.unit_begin + (int64_t)kvh * per;
-        if (off < e.w_exact) {
-            u = blk0 + e.w_exact;
-            if (off == 0) { it = Item{1, lo, kvh, 0, 0}; return true; }
-            continue;
-        }
-        if (off < e.w_exact + e.w_seal) {
-            u = blk0 + e.w_exact + e.w_seal;
-            if (off == e.w_exact) { it = Item{2, lo, kvh, e.seal_group, e.seal_group + 1}; return true; }
-            continue;
-        }
-        const int gs = off - e.w_exact - e.w_seal;
-        const int64_t end = min(hi, blk0 + per);
-        it = Item{3, lo, kvh, gs, gs + (int)(end - u)};
-        u = end;
-        return true;
+    if (u >= hi) return false;
+    int lo = 0, up = p.n_seqs - 1;
+    while (lo < up) {
+        int mid = (lo + up + 1) >> 1;
+        if (p.seqs[mid].unit_begin <= u) lo = mid; else up = mid - 1;
     }
-    return false;
+    const SeqEntry& e = p.seqs[lo];
+    const int per = e.w_exact + e.w_seal + e.n_groups;
+    const int64_t rel = u - e.unit_begin;
+    const int kvh = (int)(rel / per);
+    const int off = (int)(rel % per);
+    const int64_t blk0 = e.unit_begin + (int64_t)kvh * per;
+    const int end = (int)(min(hi, blk0 + per) - blk0);  // one past the last covered unit
+    const int gu = e.w_exact + e.w_seal;                   // unit of group 0
+    it.ci = lo;
+    it.kvh = kvh;
+    it.owner = off == 0;
+    it.n_ex = off == 0 ? exact_subs(e.n_sink, e.n_tail) : 0;
+    it.seal = (e.w_seal > 0 && off <= e.w_exact && e.w_exact < end) ? 1 : 0;
+    it.g0 = max(off - gu, 0);
+    it.g1 = max(end - gu, it.g0);
+    u = blk0 + end;
+    return true;
 }
+
+struct WarpRegion {
+    float2 acc[8][32];
+    float m[4], l[4];
+};
+
+// Arrivals at the end of an item (two slots, by item parity).
+struct ItemCtl {
+    int tag;     // item number the slot currently takes
+    int count;   // warps arrived
+    int mask;    // warps that parked a state
+    int pad;
+};
 
 struct Smem {
     uint8_t* stages;
     uint64_t* full;
-    float* qrot;    // [4][128] rotated query / its max
-    uint4* qtab;    // [3 kinds][4][32 lanes]: query operand table (setup_query)
-    float* qmax;    // [4]
-    float* xbuf;    // [8 warps][kXbWarp] (half2 words)
-    float* mrg;     // [8 warps][kMrgFloats], also exact-part and final-merge scratch
-    int* flag;
+    uint32_t* gen;    // [32]: number of the group whose copy was last issued into each stage
+    uint4* qtab;      // [2][kTabWords]: query operand tables (by block parity)
+    float* qrot;      // [2][4][128]: rotated query of the table builder
+    float* qmax;      // [2][4]
+    float* xbuf;      // [kWarps][kXbWarp] (half2 words)
+    WarpRegion* region;  // [kWarps]
+    ItemCtl* ictl;       // [2]
+    int* busy;           // [kWarps]: item number parked in a warp's region, -1 if free
+    int* ctl;            // [6]: table ready generation, claims and departures per table slot
+    struct GroupCursor* cursor;  // [kWarps]: each warp's copy cursor (all its lanes keep it in step)
     SealSmem* seal;
 };
 
@@ -188,338 +207,150 @@ __device__ __forceinline__ void warp_fwht128(float (&v)[4], int lane) {
     for (int e = 0; e < 4; ++e) v[e] *= kInvSqrt128;
 }
 
-// Expected number of partials of block (entry e, kvh) in this call.
-__device__ int expected_partials(const DecodeParams& p, const SeqEntry& e, int kvh, int64_t* first_cta) {
+// CTAs whose unit ranges cover block (entry e, kvh) in this call (each writes one
+// partial); the first of them in *first_cta.
+__device__ int block_ctas(const DecodeParams& p, const SeqEntry& e, int kvh, int64_t* first_cta) {
     const int per = e.w_exact + e.w_seal + e.n_groups;
-    const int64_t g0u = e.unit_begin + (int64_t)kvh * per + e.w_exact + e.w_seal;
-    int n = 1 + (e.w_seal > 0 ? 1 : 0);
-    int64_t f = covering(g0u, p.units_total, p.grid);
-    if (e.n_groups > 0) n += (int)(covering(g0u + e.n_groups - 1, p.units_total, p.grid) - f + 1);
+    const int64_t blk0 = e.unit_begin + (int64_t)kvh * per;
+    const int64_t f = covering(blk0, p.units_total, p.grid);
     if (first_cta) *first_cta = f;
-    return n;
+    return (int)(covering(blk0 + per - 1, p.units_total, p.grid) - f + 1);
 }
 
-// Last CTA of a block: merge every partial of this call, rotate back, write out.
-// The partial headers are read in one parallel round (one thread per slot); the
-// accumulators of the valid slots are then read with independent loads.
-__device__ void final_merge(const DecodeParams& p, const Smem& sm, int ci, int kvh) {
-    const int t = threadIdx.x;
-    const SeqEntry& e = p.seqs[ci];
-    const int blk = e.seq * p.hkv + kvh;
-    float* hdr = sm.mrg + 1536;           // [kPartialSlots][8]: m[4], l[4]
-    int* list = reinterpret_cast<int*>(sm.mrg + 1536 + 8 * kPartialSlots);  // [kPartialSlots + 1]
-    bool valid = false;
-    if (t < kPartialSlots) {
-        const float* P = partial_ptr(p, blk, t);
-        valid = (uint32_t)__float_as_int(__ldcg(P)) == p.epoch;
-        const float4 m4 = __ldcg(reinterpret_cast<const float4*>(P + 4));
-        const float4 l4 = __ldcg(reinterpret_cast<const float4*>(P + 8));
-        float* H = hdr + 8 * t;
-        H[0] = valid ? m4.x : kNegInf; H[1] = valid ? m4.y : kNegInf;
-        H[2] = valid ? m4.z : kNegInf; H[3] = valid ? m4.w : kNegInf;
-        H[4] = l4.x; H[5] = l4.y; H[6] = l4.z; H[7] = l4.w;
-    }
-    if (t < 32) {  // warp 0 lists the valid slots among 0..31
-        const unsigned vm = __ballot_sync(0xffffffffu, valid);
-        if (t == 0) {
-            int n = 0;
-            for (int k = 0; k < 32; ++k)
-                if (vm >> k & 1) list[1 + n++] = k;
-            list[0] = n;
+// ldmatrix of four 8 x 8 b16 matrices (row addresses from lanes 8i .. 8i + 7 for matrix i).
+__device__ __forceinline__ void ldsm_x4(uint32_t addr, uint32_t& a0, uint32_t& a1, uint32_t& a2, uint32_t& a3) {
+    asm volatile("ldmatrix.sync.aligned.m8n8.x4.shared.b16 {%0,%1,%2,%3}, [%4];"
+                 : "=r"(a0), "=r"(a1), "=r"(a2), "=r"(a3)
+                 : "r"(addr));
+}
+__device__ __forceinline__ void ldsm_x4_t(uint32_t addr, uint32_t& a0, uint32_t& a1, uint32_t& a2, uint32_t& a3) {
+    asm volatile("ldmatrix.sync.aligned.m8n8.x4.trans.shared.b16 {%0,%1,%2,%3}, [%4];"
+                 : "=r"(a0), "=r"(a1), "=r"(a2), "=r"(a3)
+                 : "r"(addr));
+}
+
+// Bounded spin until *w == v (or >= v with at_least); records kErrTimeout on giving up.
+__device__ __forceinline__ void spin_until(const int* w, int v, bool at_least, int32_t* err) {
+    volatile const int* vw = w;
+    auto ok = [&]() { return at_least ? (*vw >= v) : (*vw == v); };
+    if (ok()) return;
+    const uint64_t t0 = global_ns();
+    while (!ok()) {
+        if (global_ns() - t0 > kWaitLimitNs) {
+            atomicOr(err, kErrTimeout);
+            return;
         }
-    }
-    named_bar(1, kConsumers);
-    if (t >= 32 && t < kPartialSlots && valid) {  // slots beyond the first warp (rare)
-        const int k = atomicAdd(&list[0], 1);
-        list[1 + k] = t;
-    }
-    named_bar(1, kConsumers);
-    const int nv = list[0];
-    const int h = (t >> 6) & 3, jj = 2 * (t & 63);
-    float M = kNegInf;
-    for (int k = 0; k < nv; ++k) M = fmaxf(M, hdr[8 * list[1 + k] + h]);
-    float l = 0.f, r0 = 0.f, r1 = 0.f, x0 = 0.f, x1 = 0.f;
-    if (M != kNegInf) {
-#pragma unroll 4
-        for (int k = 0; k < nv; ++k) {
-            const int sl = list[1 + k];
-            const float ms = hdr[8 * sl + h];
-            const float w = ms == kNegInf ? 0.f : exp2f(ms - M);
-            const float2 a = __ldcg(reinterpret_cast<const float2*>(partial_ptr(p, blk, sl) + 12 + 128 * h + jj));
-            l = fmaf(w, hdr[8 * sl + 4 + h], l);
-            if (sl == kSlotExact) {
-                x0 = fmaf(w, a.x, x0);
-                x1 = fmaf(w, a.y, x1);
-            } else {
-                r0 = fmaf(w, a.x, r0);
-                r1 = fmaf(w, a.y, r1);
-            }
-        }
-    }
-    float* rot = sm.mrg;        // [4][128]
-    float* ex = sm.mrg + 512;   // [4][128]
-    float* ls = sm.mrg + 1024;  // [4]
-    if (t < 256) {
-        rot[128 * h + jj] = r0;
-        rot[128 * h + jj + 1] = r1;
-        ex[128 * h + jj] = x0;
-        ex[128 * h + jj + 1] = x1;
-        if ((t & 63) == 0) ls[h] = l;
-    }
-    named_bar(1, kConsumers);
-    const int w = t >> 5, lane = t & 31;
-    if (w < 4) {
-        float v[4];
-#pragma unroll
-        for (int k = 0; k < 4; ++k) v[k] = rot[128 * w + 4 * lane + k];
-        warp_fwht128(v, lane);
-#pragma unroll
-        for (int k = 0; k < 4; ++k) rot[128 * w + 4 * lane + k] = v[k];
-    }
-    named_bar(1, kConsumers);
-    if (t < 256 && h < p.r) {
-        const float lh = ls[h];
-        const float inv = lh > 0.f ? 1.0f / lh : 0.f;
-        __half2 o = __floats2half2_rn((ex[128 * h + jj] + rot[128 * h + jj]) * inv,
-                                      (ex[128 * h + jj + 1] + rot[128 * h + jj + 1]) * inv);
-        uint16_t* out = p.out + ((size_t)ci * p.hq + (size_t)kvh * p.r + h) * 128 + jj;
-        *reinterpret_cast<__half2*>(out) = o;
     }
 }
 
-// Publish a partial (written by all consumer threads before the call) and merge if last.
-__device__ void publish(const DecodeParams& p, const Smem& sm, int ci, int kvh) {
-    __threadfence();
-    named_bar(1, kConsumers);
-    const SeqEntry& e = p.seqs[ci];
-    const int blk = e.seq * p.hkv + kvh;
-    if (threadIdx.x == 0) {
-        int expect = expected_partials(p, e, kvh, nullptr);
-        int32_t* tickets = reinterpret_cast<int32_t*>(p.base + p.lay.tickets);
-        int old = atomicAdd(tickets + blk, 1);
-        int last = (old == expect - 1);
-        if (last) tickets[blk] = 0;
-        __threadfence();
-        *sm.flag = last;
+// Query operand tables. For block (ci, kvh) the query is rotated per head:
+// q_hat = (q H) / max|q H|, qmax = that max. Lane (g, tq) of a warp holds column g of
+// the MMA (head g >> 1, part g & 1) for the channels of pair P of chunk tq; with
+// v = q_hat * 2^-ex (the codes' power-of-two offset folded in) split into f16 parts
+// v = vh + vl, the table holds per pair: vh, -vh on a low-part lane (0 on a high-part
+// lane) and vl on a low-part lane (0 on a high-part lane).
+
+// Rotate head h of block (ci, kvh) into table slot b (one warp).
+__device__ void rotate_head(const DecodeParams& p, const Smem& sm, int b, int ci, int kvh, int h, int lane) {
+    float v[4] = {0.f, 0.f, 0.f, 0.f};
+    if (h < p.r) {
+        const uint16_t* q = p.q + ((size_t)ci * p.hq + (size_t)kvh * p.r + h) * 128 + 4 * lane;
+        uint2 raw = *reinterpret_cast<const uint2*>(q);
+        float2 f0 = __half22float2(bits_h2(raw.x)), f1 = __half22float2(bits_h2(raw.y));
+        v[0] = f0.x; v[1] = f0.y; v[2] = f1.x; v[3] = f1.y;
     }
-    named_bar(1, kConsumers);
-    if (*sm.flag) final_merge(p, sm, ci, kvh);
-    named_bar(1, kConsumers);
+    warp_fwht128(v, lane);
+    float mx = fmaxf(fmaxf(fabsf(v[0]), fabsf(v[1])), fmaxf(fabsf(v[2]), fabsf(v[3])));
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, o));
+    if (mx == 0.f) mx = 1.f;
+    const float inv = 1.0f / mx;
+    float* qrot = sm.qrot + 512 * b + 128 * h;
+#pragma unroll
+    for (int k = 0; k < 4; ++k) qrot[4 * lane + k] = v[k] * inv;
+    if (lane == 0) sm.qmax[4 * b + h] = mx;
 }
 
-// Exact part (sink + tail) of one block on CUDA cores; in a decode step the new token
-// is first written to the sink or tail (unless it completes a group). Scores: one
-// thread per token, sixteen independent 16-byte loads of its K row. P V: warp w takes
-// tokens w, w+8, ...; lane l holds channels 4l..4l+3 of all four heads, so every V row
-// is one coalesced 256-byte warp load; the eight warps' sums meet in shared memory.
-__device__ void exact_item(const DecodeParams& p, const Smem& sm, int ci, int kvh) {
-    const int t = threadIdx.x, w = t >> 5, lane = t & 31;
-    const SeqEntry& e = p.seqs[ci];
-    const size_t sl = (size_t)e.seq * p.num_layers + p.layer;
-    const size_t rows0 = (sl * p.hkv + kvh) * 128;  // first row of this (seq, layer, kv head)
-    const uint16_t* sink_k = reinterpret_cast<const uint16_t*>(p.base + p.lay.sink_k) + rows0 * 128;
-    const uint16_t* sink_v = reinterpret_cast<const uint16_t*>(p.base + p.lay.sink_v) + rows0 * 128;
-    const uint16_t* tail_k = reinterpret_cast<const uint16_t*>(p.base + p.lay.tail_k) + rows0 * 128;
-    const uint16_t* tail_v = reinterpret_cast<const uint16_t*>(p.base + p.lay.tail_v) + rows0 * 128;
-    if (e.new_pos >= 0 && e.seal_group < 0 && t < 32) {
-        const int side = t >> 4, chunk = t & 15;
-        const uint16_t* src = (side ? p.v_new : p.k_new) + ((size_t)ci * p.hkv + kvh) * 128;
-        size_t row = e.new_pos < kSink ? (size_t)e.new_pos : (size_t)((e.new_pos - kSink) % kGroup);
-        size_t off = (e.new_pos < kSink ? (side ? p.lay.sink_v : p.lay.sink_k) : (side ? p.lay.tail_v : p.lay.tail_k)) +
-                     (rows0 + row) * 256;
-        reinterpret_cast<uint4*>(p.base + off)[chunk] = reinterpret_cast<const uint4*>(src)[chunk];
-    }
-    float* qraw = sm.xbuf;           // [4][128]
-    float* sc = sm.xbuf + 512;       // [4][256]
-    float* red = sm.xbuf + 1536;     // [16]
-    float* part = sm.mrg;            // [kWarps][4][128]
-    for (int k = t; k < 512; k += kConsumers) {
-        const int h = k >> 7, j = k & 127;
-        qraw[k] = h < p.r ? half_bits_to_float(p.q[((size_t)ci * p.hq + (size_t)kvh * p.r + h) * 128 + j]) : 0.f;
-    }
-    named_bar(1, kConsumers);
-    const int n_ex = e.n_sink + e.n_tail;
-    float s[4] = {kNegInf, kNegInf, kNegInf, kNegInf};
-    if (t < n_ex) {
-        const uint4* row = reinterpret_cast<const uint4*>(t < e.n_sink ? sink_k + (size_t)t * 128
-                                                                      : tail_k + (size_t)(t - e.n_sink) * 128);
-        float d[4] = {0.f, 0.f, 0.f, 0.f};
-#pragma unroll
-        for (int half = 0; half < 2; ++half) {
-            uint4 kv[8];
-#pragma unroll
-            for (int c = 0; c < 8; ++c) kv[c] = row[8 * half + c];
-#pragma unroll
-            for (int c = 0; c < 8; ++c) {
-                const __half2* hp = reinterpret_cast<const __half2*>(&kv[c]);
-                float kf[8];
-#pragma unroll
-                for (int q2 = 0; q2 < 4; ++q2) {
-                    float2 f = __half22float2(hp[q2]);
-                    kf[2 * q2] = f.x;
-                    kf[2 * q2 + 1] = f.y;
-                }
-                const int cc = 8 * half + c;
-#pragma unroll
-                for (int h = 0; h < 4; ++h) {
-                    const float4 qa = reinterpret_cast<const float4*>(qraw + 128 * h + 8 * cc)[0];
-                    const float4 qb = reinterpret_cast<const float4*>(qraw + 128 * h + 8 * cc)[1];
-                    d[h] = fmaf(kf[0], qa.x, d[h]); d[h] = fmaf(kf[1], qa.y, d[h]);
-                    d[h] = fmaf(kf[2], qa.z, d[h]); d[h] = fmaf(kf[3], qa.w, d[h]);
-                    d[h] = fmaf(kf[4], qb.x, d[h]); d[h] = fmaf(kf[5], qb.y, d[h]);
-                    d[h] = fmaf(kf[6], qb.z, d[h]); d[h] = fmaf(kf[7], qb.w, d[h]);
-                }
-            }
-        }
-#pragma unroll
-        for (int h = 0; h < 4; ++h) s[h] = d[h] * p.scale_log2;
-    }
-    if (t < 256) {
-#pragma unroll
-        for (int h = 0; h < 4; ++h) sc[256 * h + t] = s[h];
-    }
-    named_bar(1, kConsumers);
-    // per-head max and sum: 64 threads per head, 4 entries each (threads >= 256 idle)
-    {
-        const int h = (t >> 6) & 3, k0 = 4 * (t & 63);
-        float m = fmaxf(fmaxf(sc[256 * h + k0], sc[256 * h + k0 + 1]), fmaxf(sc[256 * h + k0 + 2], sc[256 * h + k0 + 3]));
-#pragma unroll
-        for (int o = 16; o > 0; o >>= 1) m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, o));
-        if (lane == 0 && t < 256) red[2 * h + (w & 1)] = m;
-        named_bar(1, kConsumers);
-        m = fmaxf(red[2 * h], red[2 * h + 1]);
-        float sum = 0.f;
-#pragma unroll
-        for (int k = 0; k < 4; ++k) {
-            float v = sc[256 * h + k0 + k];
-            float pv = (m == kNegInf) ? 0.f : exp2f(v - m);
-            if (t < 256) sc[256 * h + k0 + k] = pv;
-            sum += pv;
-        }
-#pragma unroll
-        for (int o = 16; o > 0; o >>= 1) sum += __shfl_xor_sync(0xffffffffu, sum, o);
-        if (lane == 0 && t < 256) red[8 + 2 * h + (w & 1)] = sum;
-        named_bar(1, kConsumers);
-        if ((t & 63) == 0 && t < 256) {
-            float* P = partial_ptr(p, e.seq * p.hkv + kvh, kSlotExact);
-            P[4 + h] = m;
-            P[8 + h] = red[8 + 2 * h] + red[8 + 2 * h + 1];
-        }
-    }
-    // P V
-    {
-        float acc[4][4];
-#pragma unroll
-        for (int h = 0; h < 4; ++h)
-#pragma unroll
-            for (int c = 0; c < 4; ++c) acc[h][c] = 0.f;
-        for (int k0 = w; k0 < n_ex; k0 += 4 * kWarps) {
-            uint2 vv[4];
-#pragma unroll
-            for (int u = 0; u < 4; ++u) {
-                const int k = k0 + kWarps * u;
-                vv[u] = make_uint2(0u, 0u);
-                if (k < n_ex) {
-                    const uint16_t* row = k < e.n_sink ? sink_v + (size_t)k * 128 : tail_v + (size_t)(k - e.n_sink) * 128;
-                    vv[u] = reinterpret_cast<const uint2*>(row)[lane];
-                }
-            }
-#pragma unroll
-            for (int u = 0; u < 4; ++u) {
-                const int k = k0 + kWarps * u;
-                if (k < n_ex) {
-                    const float2 va = __half22float2(bits_h2(vv[u].x)), vb = __half22float2(bits_h2(vv[u].y));
-#pragma unroll
-                    for (int h = 0; h < 4; ++h) {
-                        const float pk = sc[256 * h + k];
-                        acc[h][0] = fmaf(pk, va.x, acc[h][0]);
-                        acc[h][1] = fmaf(pk, va.y, acc[h][1]);
-                        acc[h][2] = fmaf(pk, vb.x, acc[h][2]);
-                        acc[h][3] = fmaf(pk, vb.y, acc[h][3]);
-                    }
-                }
-            }
-        }
-#pragma unroll
-        for (int h = 0; h < 4; ++h)
-            *reinterpret_cast<float4*>(part + (w * 4 + h) * 128 + 4 * lane) =
-                make_float4(acc[h][0], acc[h][1], acc[h][2], acc[h][3]);
-        named_bar(1, kConsumers);
-        if (t < 256) {
-            const int h = t >> 6, jj = 2 * (t & 63);
-            float a0 = 0.f, a1 = 0.f;
-#pragma unroll
-            for (int k = 0; k < kWarps; ++k) {
-                a0 += part[(k * 4 + h) * 128 + jj];
-                a1 += part[(k * 4 + h) * 128 + jj + 1];
-            }
-            float* P = partial_ptr(p, e.seq * p.hkv + kvh, kSlotExact);
-            *reinterpret_cast<float2*>(P + 12 + 128 * h + jj) = make_float2(a0, a1);
-            if (t == 0) P[0] = __int_as_float((int)p.epoch);
-        }
-    }
-    publish(p, sm, ci, kvh);
-}
-
-// Rotate the query of a block: qrot = (q H) / max|q H| per head, qmax = that max; then
-// the table from which every lane builds its query operand for a group. Lane (g, tq)
-// holds column g of the MMA (head g >> 1, part g & 1) for the channels of pair P of
-// chunk tq; with v = q_hat * 2^-ex (the codes' power-of-two offset folded in) split
-// into f16 parts v = vh + vl, the table holds per pair: vh, -vh on a low-part lane
-// (0 on a high-part lane) and vl on a low-part lane (0 on a high-part lane).
+// Table entries of pairs 2 q and 2 q + 1 of lane `lane` in slot b, from the rotated query.
 template <int KB>
-__device__ void setup_query(const DecodeParams& p, const Smem& sm, int ci, int kvh) {
+__device__ __forceinline__ void fill_table(const Smem& sm, int b, int q, int lane) {
     using CK = Codes<KB>;
-    const int t = threadIdx.x, w = t >> 5, lane = t & 31;
-    if (w < 4) {
-        float v[4] = {0.f, 0.f, 0.f, 0.f};
-        if (w < p.r) {
-            const uint16_t* q = p.q + ((size_t)ci * p.hq + (size_t)kvh * p.r + w) * 128 + 4 * lane;
-            uint2 raw = *reinterpret_cast<const uint2*>(q);
-            float2 f0 = __half22float2(bits_h2(raw.x)), f1 = __half22float2(bits_h2(raw.y));
-            v[0] = f0.x; v[1] = f0.y; v[2] = f1.x; v[3] = f1.y;
-        }
-        warp_fwht128(v, lane);
-        float mx = fmaxf(fmaxf(fabsf(v[0]), fabsf(v[1])), fmaxf(fabsf(v[2]), fabsf(v[3])));
+    const int g = lane >> 2, tq = lane & 3;
+    const bool lo_lane = (g & 1) != 0;
+    const float* qh = sm.qrot + 512 * b + 128 * (g >> 1);
+    uint32_t* tab = reinterpret_cast<uint32_t*>(sm.qtab + kTabWords * b);
+    uint32_t hi2[2], neg2[2], lo2[2];
 #pragma unroll
-        for (int o = 16; o > 0; o >>= 1) mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, o));
-        if (mx == 0.f) mx = 1.f;
-        const float inv = 1.0f / mx;
-#pragma unroll
-        for (int k = 0; k < 4; ++k) sm.qrot[128 * w + 4 * lane + k] = v[k] * inv;
-        if (lane == 0) sm.qmax[w] = mx;
+    for (int e = 0; e < 2; ++e) {
+        const int P = 2 * q + e;
+        const int x = P % CK::HALF;
+        const int c0 = 32 * tq + CK::CPW * (P / CK::HALF) + x;
+        const float sc = __int_as_float((127 - CK::ex(x)) << 23);  // 2^-ex
+        const float v0 = qh[c0] * sc, v1 = qh[c0 + CK::HALF] * sc;
+        const __half2 hh = __floats2half2_rn(v0, v1);
+        const float2 hf = __half22float2(hh);
+        const __half2 l = __floats2half2_rn(v0 - hf.x, v1 - hf.y);
+        hi2[e] = h2_bits(hh);
+        neg2[e] = lo_lane ? h2_bits(__hneg2(hh)) : 0u;
+        lo2[e] = lo_lane ? h2_bits(l) : 0u;
     }
-    named_bar(1, kConsumers);
-    if (t < 256) {
-        // thread (q, lane) writes pairs P = 2q, 2q + 1 of lane (g, tq)
-        const int q = t >> 5, g = lane >> 2, tq = lane & 3;
-        const bool lo_lane = (g & 1) != 0;
-        const float* qh = sm.qrot + 128 * (g >> 1);
-        uint32_t hi2[2], neg2[2], lo2[2];
-#pragma unroll
-        for (int e = 0; e < 2; ++e) {
-            const int P = 2 * q + e;
-            const int x = P % CK::HALF;
-            const int c0 = 32 * tq + CK::CPW * (P / CK::HALF) + x;
-            const float sc = __int_as_float((127 - CK::ex(x)) << 23);  // 2^-ex
-            const float v0 = qh[c0] * sc, v1 = qh[c0 + CK::HALF] * sc;
-            const __half2 h = __floats2half2_rn(v0, v1);
-            const float2 hf = __half22float2(h);
-            const __half2 l = __floats2half2_rn(v0 - hf.x, v1 - hf.y);
-            hi2[e] = h2_bits(h);
-            neg2[e] = lo_lane ? h2_bits(__hneg2(h)) : 0u;
-            lo2[e] = lo_lane ? h2_bits(l) : 0u;
-        }
-        uint32_t* tab = reinterpret_cast<uint32_t*>(sm.qtab);
-        const int word = 2 * (q & 1);  // pairs 4k .. 4k + 3 share one 16-byte entry
-#pragma unroll
-        for (int kind = 0; kind < 3; ++kind) {
-            const uint32_t* src = kind == 0 ? hi2 : (kind == 1 ? neg2 : lo2);
-            uint32_t* dst = tab + 4 * ((kind * 4 + (q >> 1)) * 32 + lane) + word;
-            *reinterpret_cast<uint2*>(dst) = make_uint2(src[0], src[1]);
-        }
+    const int word = 2 * (q & 1);  // pairs 4k .. 4k + 3 share one 16-byte entry
+    *reinterpret_cast<uint2*>(tab + 4 * ((0 * 4 + (q >> 1)) * 32 + lane) + word) = make_uint2(hi2[0], hi2[1]);
+    *reinterpret_cast<uint2*>(tab + 4 * ((1 * 4 + (q >> 1)) * 32 + lane) + word) = make_uint2(neg2[0], neg2[1]);
+    *reinterpret_cast<uint2*>(tab + 4 * ((2 * 4 + (q >> 1)) * 32 + lane) + word) = make_uint2(lo2[0], lo2[1]);
+}
+
+// The whole table of block (ci, kvh) in slot b, by one warp.
+template <int KB>
+__device__ void build_table(const DecodeParams& p, const Smem& sm, int b, int ci, int kvh, int lane) {
+#pragma unroll 1
+    for (int h = 0; h < 4; ++h) rotate_head(p, sm, b, ci, kvh, h, lane);
+    __syncwarp();
+#pragma unroll 1
+    for (int q = 0; q < 8; ++q) fill_table<KB>(sm, b, q, lane);
+}
+
+// Make the query table of the warp's kb-th table block available in slot kb & 1. The
+// first `prebuilt` blocks were built by the whole CTA before the item loop. For a later
+// block the first warp to reach it builds it once every warp has left block kb - 2 (the
+// slot's previous user); the others wait for it.
+template <int KB>
+__device__ void acquire_table(const DecodeParams& p, const Smem& sm, int kb, int prebuilt, int ci, int kvh, int lane,
+                              int32_t* err) {
+    if (kb < prebuilt) return;
+    const int b = kb & 1;
+    int* ready = sm.ctl;
+    int* claim = sm.ctl + 2;
+    int* left = sm.ctl + 4;
+    int old = 0;
+    if (lane == 0) old = atomicAdd(claim + b, 1);
+    old = __shfl_sync(0xffffffffu, old, 0);
+    if (old == kWarps * ((kb >> 1) - 1)) {  // claims of slot b count from block 2 + b on
+        if (lane == 0) spin_until(left + b, kWarps * (kb >> 1), true, err);
+        __syncwarp();
+        __threadfence_block();
+        build_table<KB>(p, sm, b, ci, kvh, lane);
+        __threadfence_block();
+        __syncwarp();
+        if (lane == 0) *reinterpret_cast<volatile int*>(ready + b) = kb + 1;
+    } else {
+        if (lane == 0) spin_until(ready + b, kb + 1, false, err);
+        __syncwarp();
+        __threadfence_block();
     }
-    named_bar(1, kConsumers);
+}
+
+// Exact query operand of a warp: column g holds head g >> 1 (both columns of a head
+// carry it), k pairs are channels 16 ks + 2 tq (+ 8).
+__device__ __forceinline__ void exact_query(const DecodeParams& p, int ci, int kvh, int g, int tq,
+                                            uint32_t (&bq)[16]) {
+    const int h = g >> 1;
+    const uint32_t* qw = reinterpret_cast<const uint32_t*>(p.q + ((size_t)ci * p.hq + (size_t)kvh * p.r + h) * 128);
+#pragma unroll
+    for (int ks = 0; ks < 8; ++ks) {
+        bq[2 * ks] = h < p.r ? qw[8 * ks + tq] : 0u;
+        bq[2 * ks + 1] = h < p.r ? qw[8 * ks + 4 + tq] : 0u;
+    }
 }
 
 struct WarpState {
@@ -569,102 +400,108 @@ struct TileGroup {
     static constexpr int TG = B == 8 ? 2 : 4;
 };
 
-// Process one sealed group pair held in shared memory (K record, then V record).
-template <int KB, int VB>
-__device__ __forceinline__ void process_group(const DecodeParams& p, const uint8_t* rec, const uint4* qtab,
-                                              float qm, float* xb, WarpState& st, int g, int tq, int lane) {
-    using CK = Codes<KB>;
-    using CV = Codes<VB>;
-    const uint8_t* krec = rec;
-    const uint8_t* vrec = rec + p.rec_k;
-    const float dK = *reinterpret_cast<const float*>(krec);
-    const float mK = *reinterpret_cast<const float*>(krec + 4);
-    const float dV = *reinterpret_cast<const float*>(vrec);
-    const float mV = *reinterpret_cast<const float*>(vrec + 4);
-    const uint16_t* aK = reinterpret_cast<const uint16_t*>(krec + 16);
-    const uint16_t* aV = reinterpret_cast<const uint16_t*>(vrec + 16);
-    const uint16_t* cV = reinterpret_cast<const uint16_t*>(vrec + 272);
-    // ---- query operand of this group, (v c_K) split into f16 high / low parts:
-    // high lane: RN(vh c); low lane: RN(vl c + (vh c - RN(vh c))), the residual being
-    // exact in f16. |v| <= 1 and c_K <= 65504, so nothing overflows.
-    uint32_t bk[16];
-    {
-        const uint4* cp = reinterpret_cast<const uint4*>(krec + 272 + 64 * tq);
-        uint32_t cw[16];
-#pragma unroll
-        for (int k = 0; k < 4; ++k) {
-            uint4 v = cp[k];
-            cw[4 * k] = v.x; cw[4 * k + 1] = v.y; cw[4 * k + 2] = v.z; cw[4 * k + 3] = v.w;
-        }
-#pragma unroll
-        for (int k = 0; k < 4; ++k) {
-            const uint4 th = qtab[k * 32 + lane];
-            const uint4 tn = qtab[(4 + k) * 32 + lane];
-            const uint4 tl = qtab[(8 + k) * 32 + lane];
-            const uint32_t vh[4] = {th.x, th.y, th.z, th.w};
-            const uint32_t vn[4] = {tn.x, tn.y, tn.z, tn.w};
-            const uint32_t vl[4] = {tl.x, tl.y, tl.z, tl.w};
-#pragma unroll
-            for (int e = 0; e < 4; ++e) {
-                const __half2 c2 = pair_scales<KB>(cw, 4 * k + e);
-                const __half2 r = __hfma2(bits_h2(vh[e]), c2, __hmul2(bits_h2(vn[e]), c2));
-                bk[4 * k + e] = h2_bits(__hfma2(bits_h2(vl[e]), c2, r));
-            }
-        }
-    }
-    // sum_j q_hat_j c_j of head tq: the high and low columns of the operand times 2^ex
-    float sumqc;
+// One record's 128 x 128 code matrix times a B fragment (8 columns), k-step outer.
+// Tile mt takes rows r = 16 mt + r0 and r + r1 of the matrix (the thread's row offset
+// r0 and the row distance r1 are folded into `rows` and `off1`); out[mt] holds, for
+// those two rows, the sum of the thread's columns 2 tq and 2 tq + 1. colsum is the
+// same column sum of B itself with each pair weighted by 2^ex (the power-of-two
+// offset of its codes), from eight MMAs with a constant A.
+template <int B>
+__device__ __forceinline__ void tiles_mma(const uint8_t* rows, int off1, const uint32_t (&bf)[16], float2 (&out)[8],
+                                          float& colsum) {
+    using C = Codes<B>;
     {
         float s4[4] = {0.f, 0.f, 0.f, 0.f};
 #pragma unroll
         for (int ks = 0; ks < 8; ++ks) {
-            const uint32_t a0 = pow2_pair(CK::ex((2 * ks) % CK::HALF));
-            const uint32_t a2 = pow2_pair(CK::ex((2 * ks + 1) % CK::HALF));
-            mma16816(s4, a0, a0, a2, a2, bk[2 * ks], bk[2 * ks + 1]);
+            const uint32_t a0 = pow2_pair(C::ex((2 * ks) % C::HALF));
+            const uint32_t a2 = pow2_pair(C::ex((2 * ks + 1) % C::HALF));
+            mma16816(s4, a0, a0, a2, a2, bf[2 * ks], bf[2 * ks + 1]);
         }
-        sumqc = s4[0] + s4[1];
+        colsum = s4[0] + s4[1];
     }
-    // ---- raw scores of the 16 tokens this thread holds (head tq): high + low columns
-    float2 S[8];
-    {
-        constexpr int TG = TileGroup<KB>::TG;
+    constexpr int TG = TileGroup<B>::TG;
 #pragma unroll
-        for (int t0g = 0; t0g < 8; t0g += TG) {
-            uint32_t w0[TG][KB], w1[TG][KB];
+    for (int t0g = 0; t0g < 8; t0g += TG) {
+        uint32_t w0[TG][B], w1[TG][B];
 #pragma unroll
-            for (int i = 0; i < TG; ++i) {
-                const int t0 = tok_row<VB>(t0g + i, g), t1 = t0 + CV::HALF;
-                load_chunk<KB>(krec + 528 + t0 * 16 * KB + 4 * KB * tq, w0[i]);
-                load_chunk<KB>(krec + 528 + t1 * 16 * KB + 4 * KB * tq, w1[i]);
-            }
-            float c[TG][4];
+        for (int i = 0; i < TG; ++i) {
+            const uint8_t* r = rows + (t0g + i) * 16 * 16 * B;
+            load_chunk<B>(r, w0[i]);
+            load_chunk<B>(r + off1, w1[i]);
+        }
+        float c[TG][4];
 #pragma unroll
-            for (int i = 0; i < TG; ++i) c[i][0] = c[i][1] = c[i][2] = c[i][3] = 0.f;
+        for (int i = 0; i < TG; ++i) c[i][0] = c[i][1] = c[i][2] = c[i][3] = 0.f;
 #pragma unroll
-            for (int ks = 0; ks < 8; ++ks) {
+        for (int ks = 0; ks < 8; ++ks) {
 #pragma unroll
-                for (int i = 0; i < TG; ++i)
-                    mma16816(c[i], pair_operand<KB>(w0[i], 2 * ks), pair_operand<KB>(w1[i], 2 * ks),
-                             pair_operand<KB>(w0[i], 2 * ks + 1), pair_operand<KB>(w1[i], 2 * ks + 1), bk[2 * ks],
-                             bk[2 * ks + 1]);
-            }
+            for (int i = 0; i < TG; ++i)
+                mma16816(c[i], pair_operand<B>(w0[i], 2 * ks), pair_operand<B>(w1[i], 2 * ks),
+                         pair_operand<B>(w0[i], 2 * ks + 1), pair_operand<B>(w1[i], 2 * ks + 1), bf[2 * ks],
+                         bf[2 * ks + 1]);
+        }
 #pragma unroll
-            for (int i = 0; i < TG; ++i) S[t0g + i] = make_float2(c[i][0] + c[i][1], c[i][2] + c[i][3]);
+        for (int i = 0; i < TG; ++i) out[t0g + i] = make_float2(c[i][0] + c[i][1], c[i][2] + c[i][3]);
+    }
+}
+
+// Query operand of a group: (v c_K) split into f16 high / low parts. High lane:
+// RN(vh c); low lane: RN(vl c + (vh c - RN(vh c))), the residual being exact in f16.
+// |v| <= 1 and c_K <= 65504, so nothing overflows.
+template <int KB>
+__device__ __forceinline__ void query_operand(const uint8_t* krec, const uint4* qtab, int tq, int lane,
+                                              uint32_t (&bk)[16]) {
+    const uint4* cp = reinterpret_cast<const uint4*>(krec + 272 + 64 * tq);
+    uint32_t cw[16];
+#pragma unroll
+    for (int k = 0; k < 4; ++k) {
+        uint4 v = cp[k];
+        cw[4 * k] = v.x; cw[4 * k + 1] = v.y; cw[4 * k + 2] = v.z; cw[4 * k + 3] = v.w;
+    }
+#pragma unroll
+    for (int k = 0; k < 4; ++k) {
+        const uint4 th = qtab[k * 32 + lane];
+        const uint4 tn = qtab[(4 + k) * 32 + lane];
+        const uint4 tl = qtab[(8 + k) * 32 + lane];
+        const uint32_t vh[4] = {th.x, th.y, th.z, th.w};
+        const uint32_t vn[4] = {tn.x, tn.y, tn.z, tn.w};
+        const uint32_t vl[4] = {tl.x, tl.y, tl.z, tl.w};
+#pragma unroll
+        for (int e = 0; e < 4; ++e) {
+            const __half2 c2 = pair_scales<KB>(cw, 4 * k + e);
+            const __half2 r = __hfma2(bits_h2(vh[e]), c2, __hmul2(bits_h2(vn[e]), c2));
+            bk[4 * k + e] = h2_bits(__hfma2(bits_h2(vl[e]), c2, r));
         }
     }
-    // ---- scores: scale * a_t * (delta * raw + m * sum_j q_hat_j c_j), log2 domain
+}
+
+// Scores of the group from the raw QK sums, online-softmax update of the warp state,
+// and the weight operand of P V: w = p * aV * rho * 2^(EV - ex) in f16, exchanged
+// through the warp's buffer into the B fragment layout (bf). Returns the correction
+// factor of the accumulator.
+template <int VB>
+__device__ __forceinline__ float softmax_weights(const DecodeParams& p, const uint8_t* krec, const uint8_t* vrec,
+                                                 float qm, float sumqc, const float2 (&raw)[8], float* xb,
+                                                 WarpState& st, int g, int tq, int lane, uint32_t (&bf)[16],
+                                                 float& rho) {
+    using CV = Codes<VB>;
+    const float dK = *reinterpret_cast<const float*>(krec);
+    const float mK = *reinterpret_cast<const float*>(krec + 4);
+    const uint16_t* aK = reinterpret_cast<const uint16_t*>(krec + 16);
+    const uint16_t* aV = reinterpret_cast<const uint16_t*>(vrec + 16);
+    // scores: scale * a_t * (delta * raw + m * sum_j q_hat_j c_j), log2 domain
     const float alpha = p.scale_log2 * qm * dK * 16777216.0f;  // codes enter as code * 2^(ex-24)
     const float beta = p.scale_log2 * qm * mK * sumqc;
     const float2 alpha2 = make_float2(alpha, alpha), beta2 = make_float2(beta, beta);
     float gmax = kNegInf;
-    float2 av[8];
+    float2 S[8];
 #pragma unroll
     for (int mt = 0; mt < 8; ++mt) {
         const int t0 = tok_row<VB>(mt, g), t1 = t0 + CV::HALF;
         const float2 ak = make_float2(half_bits_to_float(aK[t0]), half_bits_to_float(aK[t1]));
-        S[mt] = __fmul2_rn(ak, __ffma2_rn(alpha2, S[mt], beta2));
+        S[mt] = __fmul2_rn(ak, __ffma2_rn(alpha2, raw[mt], beta2));
         gmax = fmax3(gmax, S[mt].x, S[mt].y);
-        av[mt] = make_float2(half_bits_to_float(aV[t0]), half_bits_to_float(aV[t1]));
     }
     // largest V token scale of the group from its bit patterns (all >= 0): lane l reads 4
     uint32_t amaxb;
@@ -682,121 +519,355 @@ __device__ __forceinline__ void process_group(const DecodeParams& p, const uint8
     st.m = mnew;
     // rho = 2^(15 - e) puts every aV * rho in [0, 2): e = biased exponent of the largest aV
     const int ebits = max((int)(amaxb >> 10) & 31, 1);
-    const float rho = __int_as_float((127 + 15 - ebits) << 23);
+    rho = __int_as_float((127 + 15 - ebits) << 23);
     const int xv = g % CV::HALF;
     const float sv = __int_as_float((127 + kEV - CV::ex(xv)) << 23) * rho;  // 2^(EV - ex) * rho
     const float2 sv2 = make_float2(sv, sv), mneg = make_float2(-mnew, -mnew);
     float2 l2 = make_float2(0.f, 0.f);
 #pragma unroll
     for (int mt = 0; mt < 8; ++mt) {
+        const int t0 = tok_row<VB>(mt, g), t1 = t0 + CV::HALF;
+        const float2 av = make_float2(half_bits_to_float(aV[t0]), half_bits_to_float(aV[t1]));
         const float2 d = __fadd2_rn(S[mt], mneg);
         const float2 pr = make_float2(fast_exp2(d.x), fast_exp2(d.y));
         l2 = __fadd2_rn(l2, pr);
-        const __half2 wh = __float22half2_rn(__fmul2_rn(__fmul2_rn(pr, av[mt]), sv2));
+        const __half2 wh = __float22half2_rn(__fmul2_rn(__fmul2_rn(pr, av), sv2));
         reinterpret_cast<uint32_t*>(xb)[kXbHead * tq + 20 * (mt >> 1) + 8 * (mt & 1) + g] = h2_bits(wh);
     }
     st.l = fmaf(st.l, corr, l2.x + l2.y);
     __syncwarp();
-    uint32_t bv[16];
     {
         const uint4* src = reinterpret_cast<const uint4*>(xb + kXbHead * (g >> 1) + 20 * tq);
 #pragma unroll
         for (int k = 0; k < 4; ++k) {
             uint4 v = src[k];
-            bv[4 * k] = v.x; bv[4 * k + 1] = v.y; bv[4 * k + 2] = v.z; bv[4 * k + 3] = v.w;
+            bf[4 * k] = v.x; bf[4 * k + 1] = v.y; bf[4 * k + 2] = v.z; bf[4 * k + 3] = v.w;
         }
     }
     __syncwarp();
-    // sum_t w_t rho of head tq: the weight operand times 2^(ex - EV)
-    float wsum;
-    {
-        float s4[4] = {0.f, 0.f, 0.f, 0.f};
-#pragma unroll
-        for (int ks = 0; ks < 8; ++ks) {
-            const uint32_t a0 = pow2_pair(CV::ex((2 * ks) % CV::HALF) - kEV);
-            const uint32_t a2 = pow2_pair(CV::ex((2 * ks + 1) % CV::HALF) - kEV);
-            mma16816(s4, a0, a0, a2, a2, bv[2 * ks], bv[2 * ks + 1]);
-        }
-        wsum = s4[0];
-    }
-    // ---- P V in the rotated frame
-    const float gam = dV * (float)(1 << (24 - kEV)) / rho;
+    return corr;
+}
+
+// Rotated-frame P V update of the warp state from the raw P V sums. Both B columns of
+// a thread carry the same head's weights, so raw and colsum are twice the sums.
+__device__ __forceinline__ void pv_update(const uint8_t* vrec, const float2 (&raw)[8], float colsum, float corr,
+                                          float rho, WarpState& st, int g) {
+    const float dV = *reinterpret_cast<const float*>(vrec);
+    const float mV = *reinterpret_cast<const float*>(vrec + 4);
+    const uint16_t* cV = reinterpret_cast<const uint16_t*>(vrec + 272);
+    const float wsum = colsum * __int_as_float((127 - kEV - 1) << 23);  // sum_t w_t rho
+    const float gam = dV * (float)(1 << (24 - kEV - 1)) / rho;
     const float del = mV * wsum / rho;
-    const float2 corr2 = make_float2(corr, corr);
-    {
-        constexpr int TG = TileGroup<VB>::TG;
+    const float2 gam2 = make_float2(gam, gam), del2 = make_float2(del, del), corr2 = make_float2(corr, corr);
 #pragma unroll
-        for (int m0 = 0; m0 < 8; m0 += TG) {
-            uint32_t w0[TG][VB], w1[TG][VB];
-#pragma unroll
-            for (int i = 0; i < TG; ++i) {
-                const int c0 = 16 * (m0 + i) + g;
-                load_chunk<VB>(vrec + 528 + c0 * 16 * VB + 4 * VB * tq, w0[i]);
-                load_chunk<VB>(vrec + 528 + (c0 + 8) * 16 * VB + 4 * VB * tq, w1[i]);
-            }
-            float d[TG][4];
-#pragma unroll
-            for (int i = 0; i < TG; ++i) d[i][0] = d[i][1] = d[i][2] = d[i][3] = 0.f;
-#pragma unroll
-            for (int ks = 0; ks < 8; ++ks) {
-#pragma unroll
-                for (int i = 0; i < TG; ++i)
-                    mma16816(d[i], pair_operand<VB>(w0[i], 2 * ks), pair_operand<VB>(w1[i], 2 * ks),
-                             pair_operand<VB>(w0[i], 2 * ks + 1), pair_operand<VB>(w1[i], 2 * ks + 1), bv[2 * ks],
-                             bv[2 * ks + 1]);
-            }
-#pragma unroll
-            for (int i = 0; i < TG; ++i) {
-                const int mt = m0 + i;
-                const int c0 = 16 * mt + g;
-                const float2 cv = make_float2(half_bits_to_float(cV[c0]), half_bits_to_float(cV[c0 + 8]));
-                const float2 x = make_float2(fmaf(gam, d[i][0], del), fmaf(gam, d[i][2], del));
-                st.acc[mt] = __ffma2_rn(st.acc[mt], corr2, __fmul2_rn(cv, x));
-            }
-        }
+    for (int mt = 0; mt < 8; ++mt) {
+        const int c0 = 16 * mt + g;
+        const float2 cv = make_float2(half_bits_to_float(cV[c0]), half_bits_to_float(cV[c0 + 8]));
+        st.acc[mt] = __ffma2_rn(st.acc[mt], corr2, __fmul2_rn(cv, __ffma2_rn(gam2, raw[mt], del2)));
     }
 }
 
-// Merge the eight warps' states of one item into a partial in global memory.
-__device__ void write_item_partial(const DecodeParams& p, const Smem& sm, const WarpState& st, int blk, int slot) {
-    const int t = threadIdx.x, w = t >> 5, lane = t & 31, g = lane >> 2, tq = lane & 3;
-    float l = st.l;
+// Process one sealed group pair held in shared memory (K record, then V record).
+template <int KB, int VB>
+__device__ __forceinline__ void process_group(const DecodeParams& p, const uint8_t* rec, const uint4* qtab,
+                                              float qm, float* xb, WarpState& st, int g, int tq, int lane) {
+    using CV = Codes<VB>;
+    const uint8_t* krec = rec;
+    const uint8_t* vrec = rec + p.rec_k;
+    const uint8_t* rows_k = krec + 528 + tok_row<VB>(0, g) * 16 * KB + 4 * KB * tq;
+    const int off_k = CV::HALF * 16 * KB;
+    const uint8_t* rows_v = vrec + 528 + g * 16 * VB + 4 * VB * tq;
+    const int off_v = 8 * 16 * VB;
+    uint32_t bf[16];
+    query_operand<KB>(krec, qtab, tq, lane, bf);
+    float2 raw[8];
+    float colsum, corr, rho;
+    tiles_mma<KB>(rows_k, off_k, bf, raw, colsum);
+    corr = softmax_weights<VB>(p, krec, vrec, qm, colsum, raw, xb, st, g, tq, lane, bf, rho);
+    tiles_mma<VB>(rows_v, off_v, bf, raw, colsum);
+    pv_update(vrec, raw, colsum, corr, rho, st, g);
+}
+
+// 128-point Hadamard transform scaled by 1/sqrt(128) (the records' rotation) of a vector
+// held in the P V output layout: lane (g, tq) holds x[mt] = (channel 16 mt + g, channel
+// 16 mt + g + 8); channel bits 0..2 are lane bits 2..4, bit 3 the float2 half, bits 4..6
+// the tile.
+__device__ __forceinline__ void frag_fwht128(float2 (&x)[8], int lane) {
 #pragma unroll
-    for (int o = 4; o < 32; o <<= 1) l += __shfl_xor_sync(0xffffffffu, l, o);
-    float* M = sm.mrg + w * kMrgFloats;
-    if (g == 0) {
-        M[tq] = st.m;
-        M[4 + tq] = l;
+    for (int mt = 0; mt < 8; ++mt) x[mt] = make_float2(x[mt].x + x[mt].y, x[mt].x - x[mt].y);
+#pragma unroll
+    for (int len = 1; len < 8; len <<= 1) {
+#pragma unroll
+        for (int mt = 0; mt < 8; ++mt) {
+            if (mt & len) continue;
+            const float2 a = x[mt], b = x[mt + len];
+            x[mt] = make_float2(a.x + b.x, a.y + b.y);
+            x[mt + len] = make_float2(a.x - b.x, a.y - b.y);
+        }
     }
+#pragma unroll 1
+    for (int bt = 4; bt < 32; bt <<= 1) {
+        const float sg = (lane & bt) ? -1.f : 1.f;  // the lane holding the higher channel takes lo - hi
+#pragma unroll
+        for (int mt = 0; mt < 8; ++mt) {
+            const float ox = __shfl_xor_sync(0xffffffffu, x[mt].x, bt), oy = __shfl_xor_sync(0xffffffffu, x[mt].y, bt);
+            x[mt] = make_float2(fmaf(sg, x[mt].x, ox), fmaf(sg, x[mt].y, oy));
+        }
+    }
+#pragma unroll
+    for (int mt = 0; mt < 8; ++mt) x[mt] = make_float2(x[mt].x * kInvSqrt128, x[mt].y * kInvSqrt128);
+}
+
+// One exact sub-group (16 fp16 tokens of the sink or the tail, rows at pitch kRowPitch,
+// K rows then V rows; rows >= n_rows hold stale bytes) on the tensor cores: scores from
+// the unrotated query, P V with the weights split into f16 high and low columns (both
+// columns of a head), accumulated unrotated (the caller rotates the sum).
+__device__ __forceinline__ void process_exact(const uint8_t* stage, int n_rows, const uint32_t (&bq)[16],
+                                              float scale_log2, float* xb, WarpState& st, int g, int tq,
+                                              int lane) {
+    const uint32_t sK = smem_addr(stage), sV = sK + kExactVOff;
+    const int i4 = lane >> 3, r8 = lane & 7;
+    float d[4] = {0.f, 0.f, 0.f, 0.f};
+    {
+        // matrix i4: tokens r8 + 8 (i4 & 1), channels 16 ks + 8 (i4 >> 1)
+        const uint32_t a = sK + (r8 + 8 * (i4 & 1)) * kRowPitch + 16 * (i4 >> 1);
+#pragma unroll
+        for (int ks = 0; ks < 8; ++ks) {
+            uint32_t a0, a1, a2, a3;
+            ldsm_x4(a + 32 * ks, a0, a1, a2, a3);
+            mma16816(d, a0, a1, a2, a3, bq[2 * ks], bq[2 * ks + 1]);
+        }
+    }
+    const float s0 = g < n_rows ? d[0] * scale_log2 : kNegInf;
+    const float s1 = g + 8 < n_rows ? d[2] * scale_log2 : kNegInf;
+    float gmax = fmaxf(s0, s1);
+#pragma unroll
+    for (int o = 4; o < 32; o <<= 1) gmax = fmaxf(gmax, __shfl_xor_sync(0xffffffffu, gmax, o));
+    const float mnew = fmaxf(st.m, gmax);  // finite: every sub-group has a valid token
+    const float corr = fast_exp2(st.m - mnew);
+    st.m = mnew;
+    const float p0 = fast_exp2(s0 - mnew), p1 = fast_exp2(s1 - mnew);
+    st.l = fmaf(st.l, corr, p0 + p1);
+    {
+        const __half h0 = __float2half_rn(p0), h1 = __float2half_rn(p1);
+        const __half l0 = __float2half_rn(p0 - __half2float(h0)), l1 = __float2half_rn(p1 - __half2float(h1));
+        __half* xe = reinterpret_cast<__half*>(xb);  // [head][part][16 tokens]
+        xe[(2 * tq) * 16 + g] = h0;
+        xe[(2 * tq + 1) * 16 + g] = l0;
+        xe[(2 * tq) * 16 + g + 8] = h1;
+        xe[(2 * tq + 1) * 16 + g + 8] = l1;
+    }
+    __syncwarp();
+    const uint32_t* xw = reinterpret_cast<const uint32_t*>(xb);
+    const uint32_t b0 = xw[8 * g + tq], b1 = xw[8 * g + 4 + tq];  // column g: head g >> 1, part g & 1
+    __syncwarp();
+    uint32_t m01 = 0xffffffffu, m23 = 0xffffffffu;  // stale rows enter as zeros
+    if (n_rows < kExactRows) {
+        m01 = (2 * tq < n_rows ? 0x0000ffffu : 0u) | (2 * tq + 1 < n_rows ? 0xffff0000u : 0u);
+        m23 = (2 * tq + 8 < n_rows ? 0x0000ffffu : 0u) | (2 * tq + 9 < n_rows ? 0xffff0000u : 0u);
+    }
+    const float2 corr2 = make_float2(corr, corr);
+    // matrix i4 of tile mt: tokens r8 + 8 (i4 >> 1), channels 16 mt + 8 (i4 & 1), transposed
+    const uint32_t av = sV + (r8 + 8 * (i4 >> 1)) * kRowPitch + 16 * (i4 & 1);
 #pragma unroll
     for (int mt = 0; mt < 8; ++mt) {
-        M[8 + 128 * tq + 16 * mt + g] = st.acc[mt].x;
-        M[8 + 128 * tq + 16 * mt + g + 8] = st.acc[mt].y;
+        uint32_t a0, a1, a2, a3;
+        ldsm_x4_t(av + 32 * mt, a0, a1, a2, a3);
+        float e[4] = {0.f, 0.f, 0.f, 0.f};
+        mma16816(e, a0 & m01, a1 & m01, a2 & m23, a3 & m23, b0, b1);
+        st.acc[mt] = __ffma2_rn(st.acc[mt], corr2, make_float2(e[0] + e[1], e[2] + e[3]));
     }
-    named_bar(1, kConsumers);
-    if (t < 256) {
-        const int h = t >> 6, jj = 2 * (t & 63);
-        float mx = kNegInf;
+}
+
+// Last CTA of a block, by one warp: merge every partial of this call, rotate back
+// (128-point Hadamard transform split as 16 points in registers x 8 lanes) and write the
+// fp16 output. Lane l takes head l >> 3 and channels 16 (l & 7) .. + 15.
+__device__ __noinline__ void final_merge_warp(const DecodeParams& p, int ci, int kvh, int lane) {
+    const SeqEntry& e = p.seqs[ci];
+    const int blk = e.seq * p.hkv + kvh;
+    float mloc[2][4], lloc[2][4];
+    bool vloc[2];
 #pragma unroll
-        for (int k = 0; k < kWarps; ++k) mx = fmaxf(mx, sm.mrg[k * kMrgFloats + h]);
-        float ls = 0.f, a0 = 0.f, a1 = 0.f;
+    for (int r = 0; r < 2; ++r) {
+        const int sl = lane + 32 * r;
+        vloc[r] = false;
 #pragma unroll
-        for (int k = 0; k < kWarps; ++k) {
-            const float* Mk = sm.mrg + k * kMrgFloats;
-            const float mk = Mk[h];
-            if (mk == kNegInf) continue;
-            const float wgt = exp2f(mk - mx);
-            ls = fmaf(wgt, Mk[4 + h], ls);
-            a0 = fmaf(wgt, Mk[8 + 128 * h + jj], a0);
-            a1 = fmaf(wgt, Mk[8 + 128 * h + jj + 1], a1);
+        for (int h = 0; h < 4; ++h) mloc[r][h] = kNegInf, lloc[r][h] = 0.f;
+        if (sl < kPartialSlots) {
+            const float* P = partial_ptr(p, blk, sl);
+            vloc[r] = (uint32_t)__float_as_int(__ldcg(P)) == p.epoch;
+            if (vloc[r]) {
+                const float4 m4 = __ldcg(reinterpret_cast<const float4*>(P + 4));
+                const float4 l4 = __ldcg(reinterpret_cast<const float4*>(P + 8));
+                mloc[r][0] = m4.x; mloc[r][1] = m4.y; mloc[r][2] = m4.z; mloc[r][3] = m4.w;
+                lloc[r][0] = l4.x; lloc[r][1] = l4.y; lloc[r][2] = l4.z; lloc[r][3] = l4.w;
+            }
         }
-        float* P = partial_ptr(p, blk, slot);
-        *reinterpret_cast<float2*>(P + 12 + 128 * h + jj) = make_float2(a0, a1);
-        if ((t & 63) == 0) {
-            P[4 + h] = mx;
-            P[8 + h] = ls;
+    }
+    const int h = lane >> 3, c0 = 16 * (lane & 7);
+    float M = kNegInf;  // this lane's head
+#pragma unroll
+    for (int hh = 0; hh < 4; ++hh) {
+        float x = fmaxf(mloc[0][hh], mloc[1][hh]);
+#pragma unroll
+        for (int o = 16; o > 0; o >>= 1) x = fmaxf(x, __shfl_xor_sync(0xffffffffu, x, o));
+        if (hh == h) M = x;
+    }
+    float rot[16], L = 0.f;
+#pragma unroll
+    for (int k = 0; k < 16; ++k) rot[k] = 0.f;
+#pragma unroll 1
+    for (int r = 0; r < 2; ++r) {
+        unsigned vm = __ballot_sync(0xffffffffu, vloc[r]);
+        while (vm) {
+            const int src = __ffs(vm) - 1;
+            vm &= vm - 1;
+            const int sl = src + 32 * r;
+            float mh = kNegInf, lh = 0.f;
+#pragma unroll
+            for (int hh = 0; hh < 4; ++hh) {
+                const float mx = __shfl_sync(0xffffffffu, r ? mloc[1][hh] : mloc[0][hh], src);
+                const float lx = __shfl_sync(0xffffffffu, r ? lloc[1][hh] : lloc[0][hh], src);
+                if (hh == h) mh = mx, lh = lx;
+            }
+            const float wgt = (mh == kNegInf || M == kNegInf) ? 0.f : exp2f(mh - M);
+            L = fmaf(wgt, lh, L);
+            const float4* A = reinterpret_cast<const float4*>(partial_ptr(p, blk, sl) + 12 + 128 * h + c0);
+            float4 a[4];
+#pragma unroll
+            for (int k = 0; k < 4; ++k) a[k] = __ldcg(A + k);
+#pragma unroll
+            for (int k = 0; k < 4; ++k) {
+                rot[4 * k] = fmaf(wgt, a[k].x, rot[4 * k]); rot[4 * k + 1] = fmaf(wgt, a[k].y, rot[4 * k + 1]);
+                rot[4 * k + 2] = fmaf(wgt, a[k].z, rot[4 * k + 2]); rot[4 * k + 3] = fmaf(wgt, a[k].w, rot[4 * k + 3]);
+            }
         }
-        if (t == 0) P[0] = __int_as_float((int)p.epoch);
+    }
+    // Hadamard transform of the rotated part: channel c = 16 a + k with a = lane & 7
+#pragma unroll
+    for (int len = 1; len < 16; len <<= 1) {
+#pragma unroll
+        for (int k = 0; k < 16; ++k) {
+            if (k & len) continue;
+            const float x = rot[k], y = rot[k + len];
+            rot[k] = x + y;
+            rot[k + len] = x - y;
+        }
+    }
+#pragma unroll
+    for (int bt = 1; bt < 8; bt <<= 1) {
+#pragma unroll
+        for (int k = 0; k < 16; ++k) {
+            const float o = __shfl_xor_sync(0xffffffffu, rot[k], bt);
+            rot[k] = (lane & bt) ? (o - rot[k]) : (rot[k] + o);
+        }
+    }
+    if (h < p.r) {
+        const float inv = L > 0.f ? 1.0f / L : 0.f;
+        uint32_t w[8];
+#pragma unroll
+        for (int k = 0; k < 8; ++k)
+            w[k] = h2_bits(__floats2half2_rn(rot[2 * k] * kInvSqrt128 * inv, rot[2 * k + 1] * kInvSqrt128 * inv));
+        uint4* out = reinterpret_cast<uint4*>(p.out + ((size_t)ci * p.hq + (size_t)kvh * p.r + h) * 128 + c0);
+        out[0] = make_uint4(w[0], w[1], w[2], w[3]);
+        out[1] = make_uint4(w[4], w[5], w[6], w[7]);
+    }
+}
+
+// Merge the parked states of an item in warp order (deterministic whatever the order of
+// arrival), write the CTA's partial, count it, and merge the block if this is its last
+// partial (one warp).
+__device__ __noinline__ void finalize_item(const DecodeParams& p, const Smem& sm, uint32_t mask, int ci, int kvh, int pslot,
+                              int g, int tq, int lane) {
+    float M = kNegInf;
+    for (uint32_t mm = mask; mm; mm &= mm - 1) M = fmaxf(M, sm.region[__ffs(mm) - 1].m[tq]);
+    float L = 0.f;
+    float2 acc[8];
+#pragma unroll
+    for (int mt = 0; mt < 8; ++mt) acc[mt] = make_float2(0.f, 0.f);
+    for (uint32_t mm = mask; mm; mm &= mm - 1) {
+        const WarpRegion& R = sm.region[__ffs(mm) - 1];
+        const float mw = R.m[tq];
+        const float wgt = mw == kNegInf ? 0.f : exp2f(mw - M);
+        L = fmaf(wgt, R.l[tq], L);
+        const float2 w2 = make_float2(wgt, wgt);
+#pragma unroll
+        for (int mt = 0; mt < 8; ++mt) acc[mt] = __ffma2_rn(w2, R.acc[mt][lane], acc[mt]);
+    }
+    const SeqEntry& e = p.seqs[ci];
+    const int blk = e.seq * p.hkv + kvh;
+    float* P = partial_ptr(p, blk, pslot);
+#pragma unroll
+    for (int mt = 0; mt < 8; ++mt) {
+        P[12 + 128 * tq + 16 * mt + g] = acc[mt].x;
+        P[12 + 128 * tq + 16 * mt + g + 8] = acc[mt].y;
+    }
+    if (g == 0) {
+        P[4 + tq] = M;
+        P[8 + tq] = L;
+    }
+    __syncwarp();
+    if (lane == 0) P[0] = __int_as_float((int)p.epoch);
+    __threadfence();
+    __syncwarp();
+    int last = 0;
+    if (lane == 0) {
+        const int expect = block_ctas(p, e, kvh, nullptr);
+        int32_t* tickets = reinterpret_cast<int32_t*>(p.base + p.lay.tickets);
+        const int old = atomicAdd(tickets + blk, 1);
+        last = old == expect - 1;
+        if (last) tickets[blk] = 0;
+        __threadfence();
+    }
+    last = __shfl_sync(0xffffffffu, last, 0);
+    if (last) final_merge_warp(p, ci, kvh, lane);
+}
+
+// End of item number i for a warp: park its state (if it processed any group of the item)
+// in its region, then arrive; the warp that arrives last merges the parked states, writes
+// the partial and frees the regions and the arrival slot.
+__device__ void fold_item(const DecodeParams& p, const Smem& sm, const WarpState& st, uint32_t i, int ci, int kvh,
+                          int pslot, int w, int g, int tq, int lane, int32_t* err) {
+    ItemCtl& C = sm.ictl[i & 1];
+    const bool has = __any_sync(0xffffffffu, st.m != kNegInf);
+    if (has) {
+        float l = st.l;
+#pragma unroll
+        for (int o = 4; o < 32; o <<= 1) l += __shfl_xor_sync(0xffffffffu, l, o);
+        if (lane == 0) spin_until(sm.busy + w, -1, false, err);  // freed by the previous item's merge
+        __syncwarp();
+        __threadfence_block();
+        WarpRegion& R = sm.region[w];
+#pragma unroll
+        for (int mt = 0; mt < 8; ++mt) R.acc[mt][lane] = st.acc[mt];
+        if (g == 0) {
+            R.m[tq] = st.m;
+            R.l[tq] = l;
+        }
+        if (lane == 0) sm.busy[w] = (int)i;
+    }
+    __threadfence_block();
+    __syncwarp();
+    int c = 0;
+    if (lane == 0) {
+        spin_until(&C.tag, (int)i, false, err);
+        if (has) atomicOr(&C.mask, 1 << w);
+        __threadfence_block();
+        c = atomicAdd(&C.count, 1) + 1;
+    }
+    c = __shfl_sync(0xffffffffu, c, 0);
+    if (c == kWarps) {
+        __threadfence_block();
+        const uint32_t mask = (uint32_t)*reinterpret_cast<volatile int*>(&C.mask);
+        finalize_item(p, sm, mask, ci, kvh, pslot, g, tq, lane);
+        __syncwarp();
+        if (lane < kWarps && (mask >> lane & 1)) *reinterpret_cast<volatile int*>(sm.busy + lane) = -1;
+        if (lane == 0) {
+            *reinterpret_cast<volatile int*>(&C.count) = 0;
+            *reinterpret_cast<volatile int*>(&C.mask) = 0;
+            __threadfence_block();
+            *reinterpret_cast<volatile int*>(&C.tag) = (int)i + 2;
+        }
     }
 }
 
@@ -809,75 +880,138 @@ struct SealRows {
 // Source of a copy being resolved. For a sealed group the block-table entry is loaded
 // one round ahead of the copy, so that its latency overlaps a group's processing.
 struct PendingCopy {
-    const uint8_t* base;  // seal record: its address; sealed group: pool + kv head offset
-    int32_t slot;         // block-table entry of a sealed group (possibly still in flight)
-    bool direct, valid;
+    const uint8_t* base;  // seal record: its address; sealed group: pool + kv head offset;
+                          // exact sub-group: its first K row
+    int32_t aux;          // sealed group: its block-table entry (possibly still in flight);
+                          // exact sub-group: valid rows | 256 if in the tail
+    int32_t kind;         // 0 none, 1 exact sub-group, 2 seal record, 3 sealed group
 };
 
-// Walks the CTA's sealed groups in stream order to find the record of group number gn
-// (0, 1, ... over the chunk and seal items of the CTA's unit range, in item order).
-struct GroupCursor {
-    int64_t u;       // unit cursor of the item walk
-    Item it;         // current chunk / seal item
-    uint32_t base;   // group number of the item's first group
+// Walks the CTA's stream in order to find the source of entry number gn (0, 1, ... over
+// the entries of the CTA's items, in item order). Per item it keeps what a sealed group
+// needs, so that such an entry costs a compare, a subtraction and one load.
+struct __align__(16) GroupCursor {
+    int64_t u;             // unit cursor of the item walk
+    uint32_t first, end;   // entry numbers of the current item's first entry and one past its last
+    int32_t ci, kvh, n_ex, seal;
     bool valid;
-    __device__ void init(int64_t lo) { u = lo; base = 0; valid = false; it.g0 = it.g1 = 0; }
-    // source of group gn (gn never decreases between calls); invalid past the end
+    const uint8_t* base;   // pool + kv head offset
+    const int32_t* row;    // block-table entry of the item's first group
+    __device__ void init(int64_t lo) {
+        u = lo;
+        first = end = 0;
+        ci = kvh = n_ex = seal = 0;
+        valid = false;
+        base = nullptr;
+        row = nullptr;
+    }
+    // source of entry gn (gn never decreases between calls); kind 0 past the end
     __device__ PendingCopy resolve(const DecodeParams& p, int64_t hi, uint32_t gn) {
         PendingCopy pc;
-        pc.valid = false;
-        pc.direct = false;
-        pc.slot = 0;
+        pc.kind = 0;
+        pc.aux = 0;
         pc.base = nullptr;
-        for (;;) {
-            if (valid && gn < base + (uint32_t)(it.g1 - it.g0)) break;
-            if (valid) base += (uint32_t)(it.g1 - it.g0);
+        while (!valid || gn >= end) {
+            first = valid ? end : first;
             valid = false;
             Item n;
-            bool found = false;
-            while (next_item(p, u, hi, n)) {
-                if (n.type != 1) { found = true; break; }
-            }
-            if (!found) return pc;
-            it = n;
+            if (!next_item(p, u, hi, n)) return pc;
+            const SeqEntry& e = p.seqs[n.ci];
+            ci = n.ci;
+            kvh = n.kvh;
+            n_ex = n.n_ex;
+            seal = n.seal;
+            base = p.base + p.lay.pool + (size_t)n.kvh * (size_t)(p.rec_k + p.rec_v);
+            row = reinterpret_cast<const int32_t*>(p.base + p.lay.block_table) +
+                  ((size_t)e.seq * p.num_layers + p.layer) * p.max_groups + n.g0;
+            end = first + (uint32_t)n.count();
             valid = true;
         }
-        const SeqEntry& e = p.seqs[it.ci];
-        const size_t pair = (size_t)(p.rec_k + p.rec_v);
-        pc.valid = true;
-        if (it.type == 2) {
-            pc.direct = true;
-            pc.base = p.base + p.lay.pool + (size_t)e.seal_slot * p.slot_bytes + (size_t)it.kvh * pair;
+        const int j = (int)(gn - first);
+        if (j >= n_ex + seal) {
+            pc.kind = 3;
+            pc.base = base;
+            // issued here, first used when the copy is issued a group later: a volatile
+            // load keeps the compiler from sinking it to that use
+            asm volatile("ld.global.s32 %0, [%1];" : "=r"(pc.aux) : "l"(row + (j - n_ex - seal)));
+        } else if (j >= n_ex) {
+            const SeqEntry& e = p.seqs[ci];
+            pc.kind = 2;
+            pc.base = p.base + p.lay.pool + (size_t)e.seal_slot * p.slot_bytes + (size_t)kvh * (p.rec_k + p.rec_v);
         } else {
-            const int32_t* table = reinterpret_cast<const int32_t*>(p.base + p.lay.block_table);
-            pc.base = p.base + p.lay.pool + (size_t)it.kvh * pair;
-            pc.slot = table[((size_t)e.seq * p.num_layers + p.layer) * p.max_groups + it.g0 + (int)(gn - base)];
+            // exact sub-group j: sink rows 16 j .. or tail rows 16 (j - sink sub-groups) ..
+            const SeqEntry& e = p.seqs[ci];
+            const size_t rows0 = (((size_t)e.seq * p.num_layers + p.layer) * p.hkv + kvh) * 128;
+            const int js = (e.n_sink + kExactRows - 1) / kExactRows;
+            pc.kind = 1;
+            if (j < js) {
+                pc.base = p.base + p.lay.sink_k + (rows0 + (size_t)j * kExactRows) * 256;
+                pc.aux = min(kExactRows, e.n_sink - j * kExactRows);
+            } else {
+                pc.base = p.base + p.lay.tail_k + (rows0 + (size_t)(j - js) * kExactRows) * 256;
+                pc.aux = min(kExactRows, e.n_tail - (j - js) * kExactRows) | 256;
+            }
         }
         return pc;
     }
 };
 
-__device__ __forceinline__ void issue_copy(const DecodeParams& p, const Smem& sm, const PendingCopy& pc, uint32_t gn) {
-    if (!pc.valid) return;
-    const uint8_t* src = pc.base;
-    if (!pc.direct) {
-        int slot = pc.slot;
-        if (slot < 0 || slot >= p.pool_slots) {
-            atomicOr(err_word(p), kErrBadSlot);
-            slot = 0;
+// Issue the copy of a group into stage s (whole warp). A record is one bulk copy by lane
+// 0; an exact sub-group is one 256-byte copy per row (K rows by lanes 0..15, V rows by
+// lanes 16..31) into rows padded to kRowPitch.
+__device__ __forceinline__ void issue_copy(const DecodeParams& p, const Smem& sm, const PendingCopy& pc, uint32_t gn,
+                                           uint32_t s, int lane) {
+    if (pc.kind == 0) return;
+    uint8_t* dst = sm.stages + (size_t)s * (uint32_t)(p.rec_k + p.rec_v);
+    if (pc.kind == 1) {
+        const int rows = pc.aux & 255;
+        if (lane == 0) mbar_arrive_expect_tx(sm.full + s, (uint32_t)(2 * 256 * rows));
+        const int r = lane & 15;
+        if (r < rows) {
+            const size_t kv = (pc.aux & 256) ? p.lay.tail_v - p.lay.tail_k : p.lay.sink_v - p.lay.sink_k;
+            const uint8_t* src = pc.base + (lane < 16 ? 0 : kv) + (size_t)r * 256;
+            bulk_g2s(dst + (lane < 16 ? 0 : kExactVOff) + r * kRowPitch, src, 256, sm.full + s);
         }
-        src += (size_t)slot * p.slot_bytes;
+    } else if (lane == 0) {
+        const uint8_t* src = pc.base;
+        if (pc.kind == 3) {
+            int slot = pc.aux;
+            if (slot < 0 || slot >= p.pool_slots) {
+                atomicOr(err_word(p), kErrBadSlot);
+                slot = 0;
+            }
+            src += (size_t)slot * p.slot_bytes;
+        }
+        const uint32_t pair = (uint32_t)(p.rec_k + p.rec_v);
+        mbar_arrive_expect_tx(sm.full + s, pair);
+        bulk_g2s(dst, src, pair, sm.full + s);
     }
-    const uint32_t pair = (uint32_t)(p.rec_k + p.rec_v);
-    const uint32_t s = gn % p.stages;
-    mbar_arrive_expect_tx(sm.full + s, pair);
-    bulk_g2s(sm.stages + (size_t)s * pair, src, pair, sm.full + s);
+    if (lane == 0) *reinterpret_cast<volatile uint32_t*>(sm.gen + s) = gn;
+}
+
+// Wait until group gn has landed in its stage. A copy into a stage is issued only after
+// the stage's previous group was consumed, so once the stage's group number reads gn the
+// barrier's current phase is the one of gn and waiting on its parity is unambiguous; a
+// parity wait alone could match the phase of the group two rounds earlier when a warp
+// runs a full ring ahead of the copies.
+__device__ __forceinline__ void wait_group(const Smem& sm, uint32_t gn, uint32_t s, uint32_t parity, int32_t* err) {
+    volatile uint32_t* gp = sm.gen + s;
+    if (*gp != gn) {
+        const uint64_t t0 = global_ns();
+        while (*gp != gn) {
+            if (global_ns() - t0 > kWaitLimitNs) {
+                atomicOr(err, kErrTimeout);
+                return;
+            }
+        }
+    }
+    mbar_wait(sm.full + s, parity, err);
 }
 
 // One CTA of 12 warps per SM. Stage ring: group gn lives in stage gn % S and is
 // processed by warp gn % 12; the warp that finishes with a stage issues the copy of
-// group gn + S into it, so no stage needs a release barrier. Seal items of the CTA run
-// first, with their scratch aliased onto the (still empty) stage ring.
+// group gn + S into it. After the seal phase the warps never wait for each other as a
+// whole: an item's states are folded warp by warp and the last warp writes its partial.
 template <int KB, int VB>
 __global__ void __launch_bounds__(kDecodeThreads, 1) decode_kernel(const __grid_constant__ DecodeParams p) {
     extern __shared__ __align__(128) uint8_t smem_raw[];
@@ -892,20 +1026,36 @@ __global__ void __launch_bounds__(kDecodeThreads, 1) decode_kernel(const __grid_
         off = (off + 15) & ~(size_t)15;
         sm.full = reinterpret_cast<uint64_t*>(smem_raw + off);
         off += 32 * 8;
-        sm.qrot = reinterpret_cast<float*>(smem_raw + off);
-        off += 512 * 4;
-        sm.qmax = reinterpret_cast<float*>(smem_raw + off);
-        off += 16;
-        sm.flag = reinterpret_cast<int*>(smem_raw + off);
-        off += 16;
+        sm.gen = reinterpret_cast<uint32_t*>(smem_raw + off);
+        off += 32 * 4;
         sm.qtab = reinterpret_cast<uint4*>(smem_raw + off);
-        off += 12 * 32 * 16;
+        off += 2 * kTabWords * 16;
+        sm.qrot = reinterpret_cast<float*>(smem_raw + off);
+        off += 2 * 512 * 4;
+        sm.qmax = reinterpret_cast<float*>(smem_raw + off);
+        off += 2 * 4 * 4;
+        sm.region = reinterpret_cast<WarpRegion*>(smem_raw + off);
+        off += kWarps * sizeof(WarpRegion);
+        sm.ictl = reinterpret_cast<ItemCtl*>(smem_raw + off);
+        off += 2 * sizeof(ItemCtl);
+        sm.busy = reinterpret_cast<int*>(smem_raw + off);
+        off += 16 * 4;
+        sm.ctl = reinterpret_cast<int*>(smem_raw + off);
+        off += 8 * 4;
+        sm.cursor = reinterpret_cast<GroupCursor*>(smem_raw + off);
+        off += kWarps * sizeof(GroupCursor);
         sm.xbuf = reinterpret_cast<float*>(smem_raw + off);
-        off += kWarps * kXbWarp * 4;
-        sm.mrg = reinterpret_cast<float*>(smem_raw + off);
         sm.seal = reinterpret_cast<SealSmem*>(smem_raw);
     }
     const int t = threadIdx.x, w = t >> 5, lane = t & 31;
+    if (t < 32) sm.gen[t] = 0xffffffffu;
+    if (t < 8) sm.ctl[t] = 0;
+    if (t < 16) sm.busy[t] = -1;
+    if (t < 2) {
+        sm.ictl[t].tag = t;
+        sm.ictl[t].count = 0;
+        sm.ictl[t].mask = 0;
+    }
     if (t == 0) {
         for (int s = 0; s < p.stages; ++s) mbar_init(sm.full + s, 1);
         asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
@@ -915,16 +1065,25 @@ __global__ void __launch_bounds__(kDecodeThreads, 1) decode_kernel(const __grid_
     const int64_t lo = b * U / P, hi = (b + 1) * U / P;
     int32_t* err = err_word(p);
 
-    // ---- 1. seal the groups completed by this step's tokens (before any prefetch)
-    bool sealed_any = false;
+    // ---- 1. seal the groups completed by this step's tokens and write the other new
+    //      tokens into the sink or the tail, before any copy reads them
     {
         int64_t u = lo;
         Item it;
         while (next_item(p, u, hi, it)) {
-            if (it.type != 2) continue;
             const SeqEntry& e = p.seqs[it.ci];
             const size_t sl = (size_t)e.seq * p.num_layers + p.layer;
             const size_t rows0 = (sl * p.hkv + it.kvh) * 128;
+            if (it.owner && e.new_pos >= 0 && e.seal_group < 0 && t < 32) {
+                const int side = t >> 4, chunk = t & 15;
+                const uint16_t* src = (side ? p.v_new : p.k_new) + ((size_t)it.ci * p.hkv + it.kvh) * 128;
+                const size_t row = e.new_pos < kSink ? (size_t)e.new_pos : (size_t)((e.new_pos - kSink) % kGroup);
+                const size_t off = (e.new_pos < kSink ? (side ? p.lay.sink_v : p.lay.sink_k)
+                                                      : (side ? p.lay.tail_v : p.lay.tail_k)) +
+                                   (rows0 + row) * 256;
+                reinterpret_cast<uint4*>(p.base + off)[chunk] = reinterpret_cast<const uint4*>(src)[chunk];
+            }
+            if (!it.seal) continue;
             uint8_t* dst = p.base + p.lay.pool + (size_t)e.seal_slot * p.slot_bytes + (size_t)it.kvh * pair;
             if (t < kSealThreads) {  // the seal runs on 8 warps (barrier 2); the others wait below
                 SealRows rk{reinterpret_cast<const uint16_t*>(p.base + p.lay.tail_k) + rows0 * 128,
@@ -938,76 +1097,111 @@ __global__ void __launch_bounds__(kDecodeThreads, 1) decode_kernel(const __grid_
                 int32_t* table = reinterpret_cast<int32_t*>(p.base + p.lay.block_table);
                 table[sl * p.max_groups + e.seal_group] = e.seal_slot;
             }
-            sealed_any = true;
         }
     }
-    if (sealed_any) {
-        fence_proxy_async_global();  // the records just written are read by bulk copies
+    fence_proxy_async_global();  // the rows and records just written are read by bulk copies
+
+    // ---- query tables of the CTA's first two blocks, by the whole CTA
+    int prebuilt = 0;
+    {
+        int bci[2] = {-1, -1}, bkv[2] = {-1, -1};
+        int64_t u = lo;
+        Item it;
+        while (prebuilt < 2 && next_item(p, u, hi, it)) {
+            bci[prebuilt] = it.ci;
+            bkv[prebuilt] = it.kvh;
+            ++prebuilt;
+        }
+        if (w < 4 * prebuilt) rotate_head(p, sm, w >> 2, bci[w >> 2], bkv[w >> 2], w & 3, lane);
         __syncthreads();
+        for (int k = t; k < 256 * prebuilt; k += kDecodeThreads) fill_table<KB>(sm, k >> 8, (k >> 5) & 7, k & 31);
     }
+    __syncthreads();
 
-    // ---- 2. prologue: the first S groups of the stream
-    GroupCursor cur;
+    // ---- 2. prologue: the first S groups of the stream. Lane 0 of each warp resolves the
+    //      sources of the warp's copies; the source of its next copy is resolved one group
+    //      ahead and kept in registers, so the block-table load behind it is first waited
+    //      for when that copy is issued.
+    GroupCursor& cur = sm.cursor[w];
     cur.init(lo);
-    PendingCopy pend;
-    pend.valid = false;
-    if (lane == 0) {
-        for (uint32_t gn = w; gn < (uint32_t)p.stages; gn += kWarps) issue_copy(p, sm, cur.resolve(p, hi, gn), gn);
-        pend = cur.resolve(p, hi, w + p.stages);  // this warp's first copy inside the loop
-    }
     __syncwarp();
+    for (uint32_t gn = w; gn < (uint32_t)p.stages; gn += kWarps) issue_copy(p, sm, cur.resolve(p, hi, gn), gn, gn, lane);
+    PendingCopy pend = cur.resolve(p, hi, w + p.stages);  // this warp's first copy inside the loop
 
-    // ---- 3. items in order
+    // ---- 3. items in order, warp by warp
     const int g = lane >> 2, tq = lane & 3;
+    // this warp processes group numbers w, w + kWarps, ...: stage and phase parity of the next
+    uint32_t my_s = (uint32_t)w % (uint32_t)p.stages, my_par = ((uint32_t)w / (uint32_t)p.stages) & 1u;
+    float* xb = sm.xbuf + w * kXbWarp;
     int64_t u = lo;
     Item it;
-    uint32_t n = 0;
+    uint32_t n = 0, item_no = 0;
+    int kb = -1;
     while (next_item(p, u, hi, it)) {
         const SeqEntry& e = p.seqs[it.ci];
-        const int blk = e.seq * p.hkv + it.kvh;
-        if (it.type == 1) {
-            exact_item(p, sm, it.ci, it.kvh);
-            continue;
+        ++kb;
+        if (kb > 0 && lane == 0) atomicAdd(sm.ctl + 4 + ((kb - 1) & 1), 1);  // leaving block kb - 1
+        acquire_table<KB>(p, sm, kb, prebuilt, it.ci, it.kvh, lane, err);
+        const float qm = sm.qmax[4 * (kb & 1) + tq];
+        const uint4* qtab = sm.qtab + kTabWords * (kb & 1);
+        int64_t first;
+        block_ctas(p, e, it.kvh, &first);
+        int pslot = (int)(b - first);
+        if (pslot >= kPartialSlots) {  // cannot happen with the host's schedule
+            if (lane == 0) atomicOr(err, kErrSpan);
+            pslot = kPartialSlots - 1;
         }
-        int slot;
-        if (it.type == 2) {
-            slot = kSlotSeal;
-        } else {
-            int64_t first;
-            expected_partials(p, e, it.kvh, &first);
-            slot = kSlotChunk0 + (int)(b - first);
-            if (slot >= kPartialSlots) {  // cannot happen with the host's schedule
-                if (t == 0) atomicOr(err, kErrSpan);
-                slot = kPartialSlots - 1;
-            }
-        }
-        setup_query<KB>(p, sm, it.ci, it.kvh);
-        const float qm = sm.qmax[tq];
         WarpState st;
         st.m = kNegInf;
         st.l = 0.f;
 #pragma unroll
         for (int mt = 0; mt < 8; ++mt) st.acc[mt] = make_float2(0.f, 0.f);
-        float* xb = sm.xbuf + w * kXbWarp;
-        const uint32_t cnt = (uint32_t)(it.g1 - it.g0);
-        for (uint32_t k = (w + kWarps - (n % kWarps)) % kWarps; k < cnt; k += kWarps) {
-            const uint32_t gn = n + k;
-            const uint32_t s = gn % p.stages;
-            mbar_wait(sm.full + s, (gn / p.stages) & 1, err);
-            process_group<KB, VB>(p, sm.stages + (size_t)s * pair, sm.qtab, qm, xb, st, g, tq, lane);
-            __syncwarp();
-            if (lane == 0) {
-                issue_copy(p, sm, pend, gn + p.stages);
+        const uint32_t cnt = (uint32_t)it.count();
+        uint32_t k = (uint32_t)((w + kWarps - (int)(n % kWarps)) % kWarps);
+        if (k < (uint32_t)it.n_ex) {  // exact sub-groups come first
+            uint32_t bq[16];
+            exact_query(p, it.ci, it.kvh, g, tq, bq);
+            const int js = (e.n_sink + kExactRows - 1) / kExactRows;
+            for (; k < (uint32_t)it.n_ex; k += kWarps) {
+                const uint32_t gn = n + k;
+                wait_group(sm, gn, my_s, my_par, err);
+                const int j = (int)k;
+                const int rows = j < js ? min(kExactRows, e.n_sink - j * kExactRows)
+                                        : min(kExactRows, e.n_tail - (j - js) * kExactRows);
+                process_exact(sm.stages + (size_t)my_s * pair, rows, bq, p.scale_log2, xb, st, g, tq, lane);
+                __syncwarp();  // every lane is done with the stage before it is refilled
+                issue_copy(p, sm, pend, gn + p.stages, my_s, lane);
                 pend = cur.resolve(p, hi, gn + kWarps + p.stages);
+                my_s += kWarps;
+                while (my_s >= (uint32_t)p.stages) {
+                    my_s -= p.stages;
+                    my_par ^= 1u;
+                }
             }
-            __syncwarp();
+            // so far the state holds exact tokens only: rotate it like the records so that
+            // the block's sealed groups accumulate onto it
+            frag_fwht128(st.acc, lane);
+        }
+        for (; k < cnt; k += kWarps) {
+            const uint32_t gn = n + k;
+            wait_group(sm, gn, my_s, my_par, err);
+            process_group<KB, VB>(p, sm.stages + (size_t)my_s * pair, qtab, qm, xb, st, g, tq, lane);
+            __syncwarp();  // every lane is done with the stage before it is refilled
+            issue_copy(p, sm, pend, gn + p.stages, my_s, lane);
+            pend = cur.resolve(p, hi, gn + kWarps + p.stages);
+            my_s += kWarps;
+            while (my_s >= (uint32_t)p.stages) {
+                my_s -= p.stages;
+                my_par ^= 1u;
+            }
         }
         n += cnt;
-        write_item_partial(p, sm, st, blk, slot);
-        publish(p, sm, it.ci, it.kvh);
+        fold_item(p, sm, st, item_no, it.ci, it.kvh, pslot, w, g, tq, lane, err);
+        ++item_no;
     }
     // Normally every copy was waited for above. After a wait that gave up, let the
     // copies still in flight land (bounded) before the CTA's shared memory goes away.
+    __syncthreads();
     if (t == 0 && (*reinterpret_cast<volatile int32_t*>(err) & kErrTimeout)) {
         const uint64_t t0 = global_ns();
         for (uint32_t k = n > (uint32_t)p.stages ? n - p.stages : 0; k < n; ++k)
@@ -1037,13 +1231,14 @@ int decode_smem_bytes(int k_bits, int v_bits, int stages, bool with_seal) {
     size_t off = (size_t)stages * pair;
     if (off < sizeof(SealSmem)) off = sizeof(SealSmem);
     off = (off + 15) & ~(size_t)15;
-    off += 32 * 8 + 512 * 4 + 16 + 16 + 12 * 32 * 16 + kWarps * kXbWarp * 4 + kWarps * kMrgFloats * 4;
+    off += 32 * 8 + 32 * 4 + 2 * kTabWords * 16 + 2 * 512 * 4 + 2 * 4 * 4 + kWarps * sizeof(WarpRegion) + 2 * sizeof(ItemCtl) + 16 * 4 + 8 * 4 + kWarps * sizeof(GroupCursor) +
+           kWarps * kXbWarp * 4;
     return (int)off;
 }
 
 // ---------------------------------------------------------------------------
 // Static split-K workspace for kvarn_decode_attention_noalloc: partial softmax states
-// and merge tickets of up to kStaticBlocks (sequence, KV head) blocks, 9.2 MB per GPU
+// and merge tickets of up to kStaticBlocks (sequence, KV head) blocks, 8.7 MB per GPU
 // that loads the library, held until the process exits. Host code must not pass the
 // symbol itself to a kernel (in host code it names a host-side shadow): the device
 // address is fetched once per device with cudaGetSymbolAddress, with that device

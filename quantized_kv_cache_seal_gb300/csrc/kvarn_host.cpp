@@ -119,10 +119,11 @@ kvarn_status check_ids(const kvarn_cache* c, int32_t layer, int32_t n, const int
 }
 
 // Units charged for an exact item (sink + tail tokens) relative to one sealed group
-// pair: the exact tokens move 512 bytes each (K and V fp16) on the CUDA cores.
-int exact_units(const kvarn_cache* c, int n_exact) {
-    double pair = (double)(c->rec_k + c->rec_v);
-    return std::max(1, (int)std::ceil(n_exact * 512.0 / pair * 0.6));
+// pair: a 16-token fp16 sub-group moves about as many bytes as a 2-bit group pair but
+// needs far less arithmetic, so it is charged as half a group.
+int exact_units(const kvarn_cache* c, int n_sink, int n_tail) {
+    (void)c;
+    return std::max(1, (exact_subs(n_sink, n_tail) + 1) / 2);
 }
 
 int seal_units(const kvarn_cache* c) {
@@ -141,7 +142,7 @@ kvarn_status schedule(kvarn_cache* c, DecodeParams& p) {
     for (int i = 0; i < p.n_seqs; ++i) {
         SeqEntry& e = p.seqs[i];
         e.unit_begin = (int32_t)U;
-        int we = exact_units(c, e.n_sink + e.n_tail);
+        int we = exact_units(c, e.n_sink, e.n_tail);
         int ws = e.seal_group >= 0 ? seal_units(c) : 0;
         e.w_exact = we;
         e.w_seal = ws;
@@ -151,16 +152,16 @@ kvarn_status schedule(kvarn_cache* c, DecodeParams& p) {
     if (U >= (1ll << 31)) return KVARN_ECAPACITY;
     p.units_total = U;
     int64_t P = std::min<int64_t>(c->sms, std::max<int64_t>(1, U / 24));
-    // every block's sealed groups must fit in kMaxSpan partial slots
+    // the CTAs covering one (sequence, KV head) block must fit in its kMaxSpan partial slots
     for (;;) {
         bool ok = true;
         for (int i = 0; i < p.n_seqs && ok; ++i) {
             const SeqEntry& e = p.seqs[i];
-            if (e.n_groups == 0) continue;
+            const int per = e.w_exact + e.w_seal + e.n_groups;
             for (int h = 0; h < p.hkv && ok; ++h) {
-                int64_t g0 = e.unit_begin + (int64_t)h * (e.w_exact + e.w_seal + e.n_groups) + e.w_exact + e.w_seal;
-                int64_t g1 = g0 + e.n_groups - 1;
-                if (covering(g1, U, P) - covering(g0, U, P) + 1 > kMaxSpan) ok = false;
+                int64_t u0 = e.unit_begin + (int64_t)h * per;
+                int64_t u1 = u0 + per - 1;
+                if (covering(u1, U, P) - covering(u0, U, P) + 1 > kMaxSpan) ok = false;
             }
         }
         if (ok) break;

@@ -18,12 +18,10 @@ constexpr int kGroup = 128;
 constexpr int kSink = 128;
 constexpr int kMaxBatch = 256;   // sequences per decode call (kernel parameter table size)
 constexpr int kMaxSpan = 32;     // CTAs that may share the sealed groups of one (seq, kv head)
-constexpr int kSlotExact = 0;    // partial slot of the exact (sink + tail) part
-constexpr int kSlotSeal = 1;     // partial slot of the group sealed inside a decode step
-constexpr int kSlotChunk0 = 2;   // first partial slot of sealed-group chunks
-constexpr int kPartialSlots = kSlotChunk0 + kMaxSpan;
+constexpr int kPartialSlots = kMaxSpan;  // one partial per CTA covering a block
 constexpr int kPartialFloats = 528;  // [0] epoch bits, [4..8) m, [8..12) l, [12..524) acc
 constexpr int kDecodeThreads = 384;  // 12 warps
+constexpr int kExactRows = 16;       // tokens of an exact (sink or tail) sub-group of the decode stream
 constexpr int kSealThreads = 256;
 
 // device error word bits
@@ -32,6 +30,11 @@ constexpr int kErrBadSlot = 2;
 constexpr int kErrSpan = 4;
 
 KVARN_HD inline size_t record_bytes(int bits) { return 528 + 2048 * (size_t)bits; }
+
+// 16-token sub-groups of the exact part (sink then tail) of one (sequence, KV head).
+KVARN_HD inline int exact_subs(int n_sink, int n_tail) {
+    return (n_sink + kExactRows - 1) / kExactRows + (n_tail + kExactRows - 1) / kExactRows;
+}
 
 // Device memory layout of one cache (byte offsets into the caller's block).
 struct Layout {
