@@ -153,6 +153,35 @@ __device__ bool next_item(const DecodeParams& p, int64_t& u, int64_t hi, Item& i
     return true;
 }
 
+// The CTA's items, walked once at the start (the walk searches the sequence table in
+// kernel-parameter memory); every later walk reads this list. A range with more items
+// than fit walks the parameters again.
+constexpr int kMaxItems = 8;
+struct ItemList {
+    int n;  // items; kMaxItems + 1 if the list overflowed
+    int pad[3];
+    Item it[kMaxItems];
+};
+
+// Sources of the CTA's first kMaxEntries stream entries, resolved once by the whole CTA:
+// 8 bytes each, the low 48 bits an address (a record, or an exact sub-group's first K
+// row), bits 48..57 the exact sub-group's rows (| 256 in the tail), bits 62..63 the kind.
+constexpr int kMaxEntries = 256;
+
+struct ItemWalk {
+    int64_t u;  // unit cursor (overflowed list)
+    int idx;    // next list entry
+};
+
+__device__ __forceinline__ bool walk_next(const DecodeParams& p, const ItemList& L, ItemWalk& wk, int64_t hi, Item& it) {
+    if (L.n <= kMaxItems) {
+        if (wk.idx >= L.n) return false;
+        it = L.it[wk.idx++];
+        return true;
+    }
+    return next_item(p, wk.u, hi, it);
+}
+
 struct WarpRegion {
     float2 acc[8][32];
     float m[4], l[4];
@@ -179,6 +208,9 @@ struct Smem {
     int* busy;           // [kWarps]: item number parked in a warp's region, -1 if free
     int* ctl;            // [6]: table ready generation, claims and departures per table slot
     struct GroupCursor* cursor;  // [kWarps]: each warp's copy cursor (all its lanes keep it in step)
+    ItemList* items;
+    unsigned long long* ent;  // [kMaxEntries]
+    int* n_ent;               // entries in ent, or -1 if the stream does not fit
     SealSmem* seal;
 };
 
@@ -891,14 +923,15 @@ struct PendingCopy {
 // the entries of the CTA's items, in item order). Per item it keeps what a sealed group
 // needs, so that such an entry costs a compare, a subtraction and one load.
 struct __align__(16) GroupCursor {
-    int64_t u;             // unit cursor of the item walk
+    ItemWalk wk;           // item walk
     uint32_t first, end;   // entry numbers of the current item's first entry and one past its last
     int32_t ci, kvh, n_ex, seal;
     bool valid;
     const uint8_t* base;   // pool + kv head offset
     const int32_t* row;    // block-table entry of the item's first group
     __device__ void init(int64_t lo) {
-        u = lo;
+        wk.u = lo;
+        wk.idx = 0;
         first = end = 0;
         ci = kvh = n_ex = seal = 0;
         valid = false;
@@ -906,7 +939,7 @@ struct __align__(16) GroupCursor {
         row = nullptr;
     }
     // source of entry gn (gn never decreases between calls); kind 0 past the end
-    __device__ PendingCopy resolve(const DecodeParams& p, int64_t hi, uint32_t gn) {
+    __device__ PendingCopy resolve(const DecodeParams& p, const ItemList& L, int64_t hi, uint32_t gn) {
         PendingCopy pc;
         pc.kind = 0;
         pc.aux = 0;
@@ -915,7 +948,7 @@ struct __align__(16) GroupCursor {
             first = valid ? end : first;
             valid = false;
             Item n;
-            if (!next_item(p, u, hi, n)) return pc;
+            if (!walk_next(p, L, wk, hi, n)) return pc;
             const SeqEntry& e = p.seqs[n.ci];
             ci = n.ci;
             kvh = n.kvh;
@@ -989,6 +1022,21 @@ __device__ __forceinline__ void issue_copy(const DecodeParams& p, const Smem& sm
     if (lane == 0) *reinterpret_cast<volatile uint32_t*>(sm.gen + s) = gn;
 }
 
+// Source of stream entry gn from the CTA's entry table (kind 0 past the end).
+__device__ __forceinline__ PendingCopy table_copy(const Smem& sm, int n_ent, uint32_t gn) {
+    PendingCopy pc;
+    pc.kind = 0;
+    pc.aux = 0;
+    pc.base = nullptr;
+    if (gn < (uint32_t)n_ent) {
+        const unsigned long long v = sm.ent[gn];
+        pc.kind = (int)(v >> 62);
+        pc.aux = (int)((v >> 48) & 0x3ff);
+        pc.base = reinterpret_cast<const uint8_t*>(v & 0xffffffffffffull);
+    }
+    return pc;
+}
+
 // Wait until group gn has landed in its stage. A copy into a stage is issued only after
 // the stage's previous group was consumed, so once the stage's group number reads gn the
 // barrier's current phase is the one of gn and waiting on its parity is unambiguous; a
@@ -1044,6 +1092,13 @@ __global__ void __launch_bounds__(kDecodeThreads, 1) decode_kernel(const __grid_
         off += 8 * 4;
         sm.cursor = reinterpret_cast<GroupCursor*>(smem_raw + off);
         off += kWarps * sizeof(GroupCursor);
+        sm.items = reinterpret_cast<ItemList*>(smem_raw + off);
+        off += sizeof(ItemList);
+        sm.n_ent = reinterpret_cast<int*>(smem_raw + off);
+        off += 16;
+        sm.ent = reinterpret_cast<unsigned long long*>(smem_raw + off);
+        off += kMaxEntries * 8;
+
         sm.xbuf = reinterpret_cast<float*>(smem_raw + off);
         sm.seal = reinterpret_cast<SealSmem*>(smem_raw);
     }
@@ -1056,21 +1111,82 @@ __global__ void __launch_bounds__(kDecodeThreads, 1) decode_kernel(const __grid_
         sm.ictl[t].count = 0;
         sm.ictl[t].mask = 0;
     }
+    const int64_t U = p.units_total, P = p.grid, b = blockIdx.x;
+    const int64_t lo = b * U / P, hi = (b + 1) * U / P;
     if (t == 0) {
         for (int s = 0; s < p.stages; ++s) mbar_init(sm.full + s, 1);
         asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+        int64_t u = lo;
+        int n = 0;
+        Item it;
+        while (n <= kMaxItems && next_item(p, u, hi, it)) {
+            if (n < kMaxItems) sm.items->it[n] = it;
+            ++n;
+        }
+        sm.items->n = n;
     }
     __syncthreads();
-    const int64_t U = p.units_total, P = p.grid, b = blockIdx.x;
-    const int64_t lo = b * U / P, hi = (b + 1) * U / P;
     int32_t* err = err_word(p);
+    const ItemList& IL = *sm.items;
+    // ---- sources of the stream's entries, resolved once (block-table loads in parallel)
+    {
+        int total = 0;
+        if (IL.n <= kMaxItems)
+            for (int k = 0; k < IL.n; ++k) total += IL.it[k].count();
+        const bool fits = IL.n <= kMaxItems && total <= kMaxEntries;
+        if (fits) {
+            for (int e = t; e < total; e += kDecodeThreads) {
+                int k = 0, j = e;
+                while (j >= IL.it[k].count()) j -= IL.it[k++].count();
+                const Item& itm = IL.it[k];
+                const SeqEntry& se = p.seqs[itm.ci];
+                unsigned long long v;
+                if (j < itm.n_ex) {
+                    const size_t rows0 = (((size_t)se.seq * p.num_layers + p.layer) * p.hkv + itm.kvh) * 128;
+                    const int js = (se.n_sink + kExactRows - 1) / kExactRows;
+                    uintptr_t a;
+                    int aux;
+                    if (j < js) {
+                        a = (uintptr_t)(p.base + p.lay.sink_k + (rows0 + (size_t)j * kExactRows) * 256);
+                        aux = min(kExactRows, se.n_sink - j * kExactRows);
+                    } else {
+                        a = (uintptr_t)(p.base + p.lay.tail_k + (rows0 + (size_t)(j - js) * kExactRows) * 256);
+                        aux = min(kExactRows, se.n_tail - (j - js) * kExactRows) | 256;
+                    }
+                    v = (1ull << 62) | ((unsigned long long)aux << 48) | (unsigned long long)a;
+                } else {
+                    const uint8_t* src;
+                    if (j < itm.n_ex + itm.seal) {
+                        src = p.base + p.lay.pool + (size_t)se.seal_slot * p.slot_bytes;
+                    } else {
+                        const int32_t* table = reinterpret_cast<const int32_t*>(p.base + p.lay.block_table);
+                        int slot = table[((size_t)se.seq * p.num_layers + p.layer) * p.max_groups + itm.g0 +
+                                         (j - itm.n_ex - itm.seal)];
+                        if (slot < 0 || slot >= p.pool_slots) {
+                            atomicOr(err, kErrBadSlot);
+                            slot = 0;
+                        }
+                        src = p.base + p.lay.pool + (size_t)slot * p.slot_bytes;
+                    }
+                    src += (size_t)itm.kvh * (p.rec_k + p.rec_v);
+                    v = (2ull << 62) | (unsigned long long)(uintptr_t)src;
+                }
+                sm.ent[e] = v;
+            }
+        }
+        // addresses must fit the 48-bit field (they do on current GPUs; otherwise walk)
+        const bool wide = ((uintptr_t)(p.base + p.lay.total) >> 48) != 0;
+        if (t == 0) *sm.n_ent = (fits && !wide) ? total : -1;
+    }
+    __syncthreads();
+    const int n_ent = *sm.n_ent;
 
     // ---- 1. seal the groups completed by this step's tokens and write the other new
     //      tokens into the sink or the tail, before any copy reads them
     {
-        int64_t u = lo;
+        ItemWalk wk{lo, 0};
         Item it;
-        while (next_item(p, u, hi, it)) {
+        while (walk_next(p, IL, wk, hi, it)) {
             const SeqEntry& e = p.seqs[it.ci];
             const size_t sl = (size_t)e.seq * p.num_layers + p.layer;
             const size_t rows0 = (sl * p.hkv + it.kvh) * 128;
@@ -1105,9 +1221,9 @@ __global__ void __launch_bounds__(kDecodeThreads, 1) decode_kernel(const __grid_
     int prebuilt = 0;
     {
         int bci[2] = {-1, -1}, bkv[2] = {-1, -1};
-        int64_t u = lo;
+        ItemWalk wk{lo, 0};
         Item it;
-        while (prebuilt < 2 && next_item(p, u, hi, it)) {
+        while (prebuilt < 2 && walk_next(p, IL, wk, hi, it)) {
             bci[prebuilt] = it.ci;
             bkv[prebuilt] = it.kvh;
             ++prebuilt;
@@ -1125,19 +1241,35 @@ __global__ void __launch_bounds__(kDecodeThreads, 1) decode_kernel(const __grid_
     GroupCursor& cur = sm.cursor[w];
     cur.init(lo);
     __syncwarp();
-    for (uint32_t gn = w; gn < (uint32_t)p.stages; gn += kWarps) issue_copy(p, sm, cur.resolve(p, hi, gn), gn, gn, lane);
-    PendingCopy pend = cur.resolve(p, hi, w + p.stages);  // this warp's first copy inside the loop
+    {
+        // resolve this warp's prologue copies (at most three: gn = w, w + 12, w + 24 < 32)
+        // before issuing any, so that their block-table loads overlap
+        PendingCopy pro[3];
+#pragma unroll
+        for (int r = 0; r < 3; ++r) {
+            const uint32_t gn = (uint32_t)(w + kWarps * r);
+            pro[r].kind = 0;
+            if (gn < (uint32_t)p.stages) pro[r] = n_ent >= 0 ? table_copy(sm, n_ent, gn) : cur.resolve(p, IL, hi, gn);
+        }
+#pragma unroll
+        for (int r = 0; r < 3; ++r) {
+            const uint32_t gn = (uint32_t)(w + kWarps * r);
+            if (gn < (uint32_t)p.stages) issue_copy(p, sm, pro[r], gn, gn, lane);
+        }
+    }
+    // this warp's first copy inside the loop
+    PendingCopy pend = n_ent >= 0 ? table_copy(sm, n_ent, w + p.stages) : cur.resolve(p, IL, hi, w + p.stages);
 
     // ---- 3. items in order, warp by warp
     const int g = lane >> 2, tq = lane & 3;
     // this warp processes group numbers w, w + kWarps, ...: stage and phase parity of the next
     uint32_t my_s = (uint32_t)w % (uint32_t)p.stages, my_par = ((uint32_t)w / (uint32_t)p.stages) & 1u;
     float* xb = sm.xbuf + w * kXbWarp;
-    int64_t u = lo;
+    ItemWalk wk{lo, 0};
     Item it;
     uint32_t n = 0, item_no = 0;
     int kb = -1;
-    while (next_item(p, u, hi, it)) {
+    while (walk_next(p, IL, wk, hi, it)) {
         const SeqEntry& e = p.seqs[it.ci];
         ++kb;
         if (kb > 0 && lane == 0) atomicAdd(sm.ctl + 4 + ((kb - 1) & 1), 1);  // leaving block kb - 1
@@ -1171,7 +1303,8 @@ __global__ void __launch_bounds__(kDecodeThreads, 1) decode_kernel(const __grid_
                 process_exact(sm.stages + (size_t)my_s * pair, rows, bq, p.scale_log2, xb, st, g, tq, lane);
                 __syncwarp();  // every lane is done with the stage before it is refilled
                 issue_copy(p, sm, pend, gn + p.stages, my_s, lane);
-                pend = cur.resolve(p, hi, gn + kWarps + p.stages);
+                pend = n_ent >= 0 ? table_copy(sm, n_ent, gn + kWarps + p.stages)
+                                  : cur.resolve(p, IL, hi, gn + kWarps + p.stages);
                 my_s += kWarps;
                 while (my_s >= (uint32_t)p.stages) {
                     my_s -= p.stages;
@@ -1188,7 +1321,8 @@ __global__ void __launch_bounds__(kDecodeThreads, 1) decode_kernel(const __grid_
             process_group<KB, VB>(p, sm.stages + (size_t)my_s * pair, qtab, qm, xb, st, g, tq, lane);
             __syncwarp();  // every lane is done with the stage before it is refilled
             issue_copy(p, sm, pend, gn + p.stages, my_s, lane);
-            pend = cur.resolve(p, hi, gn + kWarps + p.stages);
+            pend = n_ent >= 0 ? table_copy(sm, n_ent, gn + kWarps + p.stages)
+                              : cur.resolve(p, IL, hi, gn + kWarps + p.stages);
             my_s += kWarps;
             while (my_s >= (uint32_t)p.stages) {
                 my_s -= p.stages;
@@ -1231,7 +1365,7 @@ int decode_smem_bytes(int k_bits, int v_bits, int stages, bool with_seal) {
     size_t off = (size_t)stages * pair;
     if (off < sizeof(SealSmem)) off = sizeof(SealSmem);
     off = (off + 15) & ~(size_t)15;
-    off += 32 * 8 + 32 * 4 + 2 * kTabWords * 16 + 2 * 512 * 4 + 2 * 4 * 4 + kWarps * sizeof(WarpRegion) + 2 * sizeof(ItemCtl) + 16 * 4 + 8 * 4 + kWarps * sizeof(GroupCursor) +
+    off += 32 * 8 + 32 * 4 + 2 * kTabWords * 16 + 2 * 512 * 4 + 2 * 4 * 4 + kWarps * sizeof(WarpRegion) + 2 * sizeof(ItemCtl) + 16 * 4 + 8 * 4 + kWarps * sizeof(GroupCursor) + sizeof(ItemList) + 16 + kMaxEntries * 8 +
            kWarps * kXbWarp * 4;
     return (int)off;
 }

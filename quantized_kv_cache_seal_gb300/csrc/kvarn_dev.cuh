@@ -194,40 +194,41 @@ __device__ void seal_matrix(const Rows& rows, int bits, int which, int iters, ui
     //    then c_j^2 = mean_i A_ij / a_i^2 (equal to rescaling the rows and columns of
     //    Y in turn; a zero row or column keeps the factor 1).
     float a2 = 1.0f, c2 = 1.0f;
+    // (four partial sums per pass keep the FMA chains short; __frcp_rn is the correctly
+    // rounded reciprocal, the same value as 1.0f / x)
     for (int it = 0; it < iters; ++it) {
-        float p0 = 0.f, p1 = 0.f;
+        float p0 = 0.f, p1 = 0.f, p2 = 0.f, p3 = 0.f;
         const float4* up = reinterpret_cast<const float4*>(S.u + 68 * h);
 #pragma unroll
         for (int q = 0; q < 16; ++q) {
             float4 uu = up[q];
             p0 = fmaf(arow[4 * q], uu.x, p0);
             p1 = fmaf(arow[4 * q + 1], uu.y, p1);
-            p0 = fmaf(arow[4 * q + 2], uu.z, p0);
-            p1 = fmaf(arow[4 * q + 3], uu.w, p1);
+            p2 = fmaf(arow[4 * q + 2], uu.z, p2);
+            p3 = fmaf(arow[4 * q + 3], uu.w, p3);
         }
-        float p = p0 + p1;
+        float p = (p0 + p2) + (p1 + p3);
         p += __shfl_xor_sync(0xffffffffu, p, 1);
         a2 = p * (1.0f / 128.0f);
         // zero row keeps factor 1; the clamp only binds on divergent inputs (see kSqMax)
         a2 = a2 == 0.0f ? 1.0f : fminf(fmaxf(a2, kSqMin), kSqMax);
-        if (h == 0) S.v[ypad(i)] = 1.0f / a2;
+        if (h == 0) S.v[ypad(i)] = __frcp_rn(a2);
         named_bar(bar_id, 256);
-        p0 = 0.f;
-        p1 = 0.f;
+        p0 = p1 = p2 = p3 = 0.f;
         const float4* vp = reinterpret_cast<const float4*>(S.v + 68 * hc);
 #pragma unroll
         for (int q = 0; q < 16; ++q) {
             float4 vv = vp[q];
             p0 = fmaf(acol[4 * q], vv.x, p0);
             p1 = fmaf(acol[4 * q + 1], vv.y, p1);
-            p0 = fmaf(acol[4 * q + 2], vv.z, p0);
-            p1 = fmaf(acol[4 * q + 3], vv.w, p1);
+            p2 = fmaf(acol[4 * q + 2], vv.z, p2);
+            p3 = fmaf(acol[4 * q + 3], vv.w, p3);
         }
-        p = p0 + p1;
+        p = (p0 + p2) + (p1 + p3);
         p += __shfl_xor_sync(0xffffffffu, p, 1);
         c2 = p * (1.0f / 128.0f);
         c2 = c2 == 0.0f ? 1.0f : fminf(fmaxf(c2, kSqMin), kSqMax);
-        if (hc == 0) S.u[ypad(j)] = 1.0f / c2;
+        if (hc == 0) S.u[ypad(j)] = __frcp_rn(c2);
         named_bar(bar_id, 256);
     }
     // 3. stored scales: fp16, round to nearest even, saturating

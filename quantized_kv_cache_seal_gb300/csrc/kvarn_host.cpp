@@ -127,9 +127,10 @@ int exact_units(const kvarn_cache* c, int n_sink, int n_tail) {
 }
 
 int seal_units(const kvarn_cache* c) {
-    // a K + V seal costs roughly as much as this many group pairs on one SM
-    (void)c;
-    return 40;
+    // a K + V seal inside the decode kernel costs about as much as 80 group pairs of
+    // 2-bit records on one SM (measured); wider records make a group pair dearer
+    const double pair2 = 2.0 * (528 + 2048 * 2);
+    return std::max(1, (int)std::lround(80.0 * pair2 / (double)(c->rec_k + c->rec_v)));
 }
 
 // covering CTA of unit u when U units are split evenly over P CTAs
