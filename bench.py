@@ -333,7 +333,7 @@ def run_ours(args):
                    "num_q_heads": HQ, "num_kv_heads": HKV, "head_dim": 128, "k_bits": KB, "v_bits": VB,
                    "parallelism": f"replicas{world}", "l2": "working set ~315 MB per step > 129 MB L2 (no flush)",
                    "reps": len(rep_ms), "rep_ms": [round(x, 4) for x in rep_ms]},
-        "gpu_launches": K_,
+        "gpu_launches": 2 * K_,  # per step: the decode kernel and its merge kernel
         "roofline": {"bound": "hbm", "achieved": achieved, "peak": peak, "unit": "GB/s", "frac": achieved / peak,
                      "traffic": args.traffic, "peak_kind": peak_kind, "kernel": "decode_kernel<2,2>",
                      "alg_bytes_per_launch": alg_bytes, "launch_us": launch_us},

@@ -711,104 +711,9 @@ __device__ __forceinline__ void process_exact(const uint8_t* stage, int n_rows, 
     }
 }
 
-// Last CTA of a block, by one warp: merge every partial of this call, rotate back
-// (128-point Hadamard transform split as 16 points in registers x 8 lanes) and write the
-// fp16 output. Lane l takes head l >> 3 and channels 16 (l & 7) .. + 15.
-__device__ __noinline__ void final_merge_warp(const DecodeParams& p, int ci, int kvh, int lane) {
-    const SeqEntry& e = p.seqs[ci];
-    const int blk = e.seq * p.hkv + kvh;
-    float mloc[2][4], lloc[2][4];
-    bool vloc[2];
-#pragma unroll
-    for (int r = 0; r < 2; ++r) {
-        const int sl = lane + 32 * r;
-        vloc[r] = false;
-#pragma unroll
-        for (int h = 0; h < 4; ++h) mloc[r][h] = kNegInf, lloc[r][h] = 0.f;
-        if (sl < kPartialSlots) {
-            const float* P = partial_ptr(p, blk, sl);
-            vloc[r] = (uint32_t)__float_as_int(__ldcg(P)) == p.epoch;
-            if (vloc[r]) {
-                const float4 m4 = __ldcg(reinterpret_cast<const float4*>(P + 4));
-                const float4 l4 = __ldcg(reinterpret_cast<const float4*>(P + 8));
-                mloc[r][0] = m4.x; mloc[r][1] = m4.y; mloc[r][2] = m4.z; mloc[r][3] = m4.w;
-                lloc[r][0] = l4.x; lloc[r][1] = l4.y; lloc[r][2] = l4.z; lloc[r][3] = l4.w;
-            }
-        }
-    }
-    const int h = lane >> 3, c0 = 16 * (lane & 7);
-    float M = kNegInf;  // this lane's head
-#pragma unroll
-    for (int hh = 0; hh < 4; ++hh) {
-        float x = fmaxf(mloc[0][hh], mloc[1][hh]);
-#pragma unroll
-        for (int o = 16; o > 0; o >>= 1) x = fmaxf(x, __shfl_xor_sync(0xffffffffu, x, o));
-        if (hh == h) M = x;
-    }
-    float rot[16], L = 0.f;
-#pragma unroll
-    for (int k = 0; k < 16; ++k) rot[k] = 0.f;
-#pragma unroll 1
-    for (int r = 0; r < 2; ++r) {
-        unsigned vm = __ballot_sync(0xffffffffu, vloc[r]);
-        while (vm) {
-            const int src = __ffs(vm) - 1;
-            vm &= vm - 1;
-            const int sl = src + 32 * r;
-            float mh = kNegInf, lh = 0.f;
-#pragma unroll
-            for (int hh = 0; hh < 4; ++hh) {
-                const float mx = __shfl_sync(0xffffffffu, r ? mloc[1][hh] : mloc[0][hh], src);
-                const float lx = __shfl_sync(0xffffffffu, r ? lloc[1][hh] : lloc[0][hh], src);
-                if (hh == h) mh = mx, lh = lx;
-            }
-            const float wgt = (mh == kNegInf || M == kNegInf) ? 0.f : exp2f(mh - M);
-            L = fmaf(wgt, lh, L);
-            const float4* A = reinterpret_cast<const float4*>(partial_ptr(p, blk, sl) + 12 + 128 * h + c0);
-            float4 a[4];
-#pragma unroll
-            for (int k = 0; k < 4; ++k) a[k] = __ldcg(A + k);
-#pragma unroll
-            for (int k = 0; k < 4; ++k) {
-                rot[4 * k] = fmaf(wgt, a[k].x, rot[4 * k]); rot[4 * k + 1] = fmaf(wgt, a[k].y, rot[4 * k + 1]);
-                rot[4 * k + 2] = fmaf(wgt, a[k].z, rot[4 * k + 2]); rot[4 * k + 3] = fmaf(wgt, a[k].w, rot[4 * k + 3]);
-            }
-        }
-    }
-    // Hadamard transform of the rotated part: channel c = 16 a + k with a = lane & 7
-#pragma unroll
-    for (int len = 1; len < 16; len <<= 1) {
-#pragma unroll
-        for (int k = 0; k < 16; ++k) {
-            if (k & len) continue;
-            const float x = rot[k], y = rot[k + len];
-            rot[k] = x + y;
-            rot[k + len] = x - y;
-        }
-    }
-#pragma unroll
-    for (int bt = 1; bt < 8; bt <<= 1) {
-#pragma unroll
-        for (int k = 0; k < 16; ++k) {
-            const float o = __shfl_xor_sync(0xffffffffu, rot[k], bt);
-            rot[k] = (lane & bt) ? (o - rot[k]) : (rot[k] + o);
-        }
-    }
-    if (h < p.r) {
-        const float inv = L > 0.f ? 1.0f / L : 0.f;
-        uint32_t w[8];
-#pragma unroll
-        for (int k = 0; k < 8; ++k)
-            w[k] = h2_bits(__floats2half2_rn(rot[2 * k] * kInvSqrt128 * inv, rot[2 * k + 1] * kInvSqrt128 * inv));
-        uint4* out = reinterpret_cast<uint4*>(p.out + ((size_t)ci * p.hq + (size_t)kvh * p.r + h) * 128 + c0);
-        out[0] = make_uint4(w[0], w[1], w[2], w[3]);
-        out[1] = make_uint4(w[4], w[5], w[6], w[7]);
-    }
-}
-
 // Merge the parked states of an item in warp order (deterministic whatever the order of
-// arrival), write the CTA's partial, count it, and merge the block if this is its last
-// partial (one warp).
+// arrival) and write the CTA's partial (one warp). The block's partials are merged by
+// merge_kernel after this kernel.
 __device__ __noinline__ void finalize_item(const DecodeParams& p, const Smem& sm, uint32_t mask, int ci, int kvh, int pslot,
                               int g, int tq, int lane) {
     float M = kNegInf;
@@ -838,21 +743,7 @@ __device__ __noinline__ void finalize_item(const DecodeParams& p, const Smem& sm
         P[4 + tq] = M;
         P[8 + tq] = L;
     }
-    __syncwarp();
     if (lane == 0) P[0] = __int_as_float((int)p.epoch);
-    __threadfence();
-    __syncwarp();
-    int last = 0;
-    if (lane == 0) {
-        const int expect = block_ctas(p, e, kvh, nullptr);
-        int32_t* tickets = reinterpret_cast<int32_t*>(p.base + p.lay.tickets);
-        const int old = atomicAdd(tickets + blk, 1);
-        last = old == expect - 1;
-        if (last) tickets[blk] = 0;
-        __threadfence();
-    }
-    last = __shfl_sync(0xffffffffu, last, 0);
-    if (last) final_merge_warp(p, ci, kvh, lane);
 }
 
 // End of item number i for a warp: park its state (if it processed any group of the item)
@@ -1126,6 +1017,8 @@ __global__ void __launch_bounds__(kDecodeThreads, 1) decode_kernel(const __grid_
         sm.items->n = n;
     }
     __syncthreads();
+    // the merge kernel that follows may be scheduled now; it waits for this grid to finish
+    asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
     int32_t* err = err_word(p);
     const ItemList& IL = *sm.items;
     // ---- sources of the stream's entries, resolved once (block-table loads in parallel)
@@ -1344,6 +1237,62 @@ __global__ void __launch_bounds__(kDecodeThreads, 1) decode_kernel(const __grid_
     }
 }
 
+// Merge of every (sequence, KV head) block of a decode call: one CTA per block, one warp
+// per query head. The partials of the CTAs that covered the block are merged (running
+// maxima, sums and rotated accumulators), the sum is rotated back with the 128-point
+// Hadamard transform and the fp16 output written. Launched right after the decode kernel
+// (programmatic dependent launch); it waits for that grid's completion before reading.
+__global__ void __launch_bounds__(128) merge_kernel(const __grid_constant__ DecodeParams p) {
+    asm volatile("griddepcontrol.wait;" ::: "memory");
+    const int ci = blockIdx.x / p.hkv, kvh = blockIdx.x % p.hkv;
+    const int h = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    if (h >= p.r) return;
+    const SeqEntry& e = p.seqs[ci];
+    const int blk = e.seq * p.hkv + kvh;
+    int64_t first;
+    const int nsl = min(block_ctas(p, e, kvh, &first), kPartialSlots);
+    float M = kNegInf;
+    for (int sl = 0; sl < nsl; ++sl) {
+        const float* P = partial_ptr(p, blk, sl);
+        if ((uint32_t)__float_as_int(__ldcg(P)) == p.epoch) M = fmaxf(M, __ldcg(P + 4 + h));
+    }
+    float L = 0.f, v[4] = {0.f, 0.f, 0.f, 0.f};
+    if (M != kNegInf) {
+        for (int sl = 0; sl < nsl; ++sl) {
+            const float* P = partial_ptr(p, blk, sl);
+            if ((uint32_t)__float_as_int(__ldcg(P)) != p.epoch) continue;
+            const float ms = __ldcg(P + 4 + h);
+            const float wgt = ms == kNegInf ? 0.f : exp2f(ms - M);
+            L = fmaf(wgt, __ldcg(P + 8 + h), L);
+            const float4 a = __ldcg(reinterpret_cast<const float4*>(P + 12 + 128 * h) + lane);
+            v[0] = fmaf(wgt, a.x, v[0]);
+            v[1] = fmaf(wgt, a.y, v[1]);
+            v[2] = fmaf(wgt, a.z, v[2]);
+            v[3] = fmaf(wgt, a.w, v[3]);
+        }
+    }
+    warp_fwht128(v, lane);
+    const float inv = L > 0.f ? 1.0f / L : 0.f;
+    uint2 o;
+    o.x = h2_bits(__floats2half2_rn(v[0] * inv, v[1] * inv));
+    o.y = h2_bits(__floats2half2_rn(v[2] * inv, v[3] * inv));
+    *reinterpret_cast<uint2*>(p.out + ((size_t)ci * p.hq + (size_t)kvh * p.r + h) * 128 + 4 * lane) = o;
+}
+
+int launch_merge(const DecodeParams& p, cudaStream_t s) {
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3((unsigned)(p.n_seqs * p.hkv));
+    cfg.blockDim = dim3(128);
+    cfg.dynamicSmemBytes = 0;
+    cfg.stream = s;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    return (int)cudaLaunchKernelEx(&cfg, merge_kernel, p);
+}
+
 template <int KB, int VB>
 int launch_t(const DecodeParams& p, int smem, cudaStream_t s) {
     static bool attr = false;
@@ -1354,7 +1303,9 @@ int launch_t(const DecodeParams& p, int smem, cudaStream_t s) {
         attr = true;
     }
     decode_kernel<KB, VB><<<p.grid, kDecodeThreads, smem, s>>>(p);
-    return (int)cudaGetLastError();
+    const int rc = (int)cudaGetLastError();
+    if (rc) return rc;
+    return launch_merge(p, s);
 }
 
 }  // namespace
