@@ -1251,25 +1251,44 @@ __global__ void __launch_bounds__(128) merge_kernel(const __grid_constant__ Deco
     const int blk = e.seq * p.hkv + kvh;
     int64_t first;
     const int nsl = min(block_ctas(p, e, kvh, &first), kPartialSlots);
-    float M = kNegInf;
-    for (int sl = 0; sl < nsl; ++sl) {
-        const float* P = partial_ptr(p, blk, sl);
-        if ((uint32_t)__float_as_int(__ldcg(P)) == p.epoch) M = fmaxf(M, __ldcg(P + 4 + h));
-    }
-    float L = 0.f, v[4] = {0.f, 0.f, 0.f, 0.f};
-    if (M != kNegInf) {
-        for (int sl = 0; sl < nsl; ++sl) {
-            const float* P = partial_ptr(p, blk, sl);
-            if ((uint32_t)__float_as_int(__ldcg(P)) != p.epoch) continue;
-            const float ms = __ldcg(P + 4 + h);
-            const float wgt = ms == kNegInf ? 0.f : exp2f(ms - M);
-            L = fmaf(wgt, __ldcg(P + 8 + h), L);
-            const float4 a = __ldcg(reinterpret_cast<const float4*>(P + 12 + 128 * h) + lane);
-            v[0] = fmaf(wgt, a.x, v[0]);
-            v[1] = fmaf(wgt, a.y, v[1]);
-            v[2] = fmaf(wgt, a.z, v[2]);
-            v[3] = fmaf(wgt, a.w, v[3]);
+    // partials four at a time, every load of a round issued before any is used, combined
+    // with the running maximum, sum and accumulator
+    float M = kNegInf, L = 0.f, v[4] = {0.f, 0.f, 0.f, 0.f};
+    for (int s0 = 0; s0 < nsl; s0 += 4) {
+        float ms[4], ls[4];
+        float4 a[4];
+#pragma unroll
+        for (int k = 0; k < 4; ++k) {
+            ms[k] = kNegInf;
+            ls[k] = 0.f;
+            a[k] = make_float4(0.f, 0.f, 0.f, 0.f);
+            if (s0 + k < nsl) {
+                const float* P = partial_ptr(p, blk, s0 + k);
+                const bool ok = (uint32_t)__float_as_int(__ldcg(P)) == p.epoch;
+                const float m = __ldcg(P + 4 + h), l = __ldcg(P + 8 + h);
+                a[k] = __ldcg(reinterpret_cast<const float4*>(P + 12 + 128 * h) + lane);
+                ms[k] = ok ? m : kNegInf;
+                ls[k] = l;
+            }
         }
+        float Mn = M;
+#pragma unroll
+        for (int k = 0; k < 4; ++k) Mn = fmaxf(Mn, ms[k]);
+        if (Mn == kNegInf) continue;
+        const float c = M == kNegInf ? 0.f : exp2f(M - Mn);
+        L *= c;
+#pragma unroll
+        for (int q = 0; q < 4; ++q) v[q] *= c;
+#pragma unroll
+        for (int k = 0; k < 4; ++k) {
+            const float wgt = ms[k] == kNegInf ? 0.f : exp2f(ms[k] - Mn);
+            L = fmaf(wgt, ls[k], L);
+            v[0] = fmaf(wgt, a[k].x, v[0]);
+            v[1] = fmaf(wgt, a[k].y, v[1]);
+            v[2] = fmaf(wgt, a[k].z, v[2]);
+            v[3] = fmaf(wgt, a[k].w, v[3]);
+        }
+        M = Mn;
     }
     warp_fwht128(v, lane);
     const float inv = L > 0.f ? 1.0f / L : 0.f;
