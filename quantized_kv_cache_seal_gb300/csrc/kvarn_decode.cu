@@ -9,20 +9,21 @@
 // output row. A group is sealed at the moment its last token arrives, so a step whose
 // new token completes a group seals it first and attends to the sealed record.
 //
-// Work split. Every (sequence, KV head) pair is a block of scheduling units: one
-// exact item, one seal item if the step seals a group, and one unit per sealed group.
-// The units of all blocks are cut into equal contiguous ranges, one per CTA, so that
-// every CTA streams the same number of records. Each CTA writes one partial softmax
-// state (running max, sum, accumulator) per block it touches; the last CTA to finish a
-// block (atomic ticket, no waiting) merges the partials, rotates the sealed
-// accumulator back, adds the exact part and writes the fp16 output.
+// Work split. Every (sequence, KV head) pair is a block of scheduling units: its exact
+// part, the seal of a group this step completes, and one unit per sealed group. The
+// units of all blocks are cut into equal contiguous ranges, one per CTA; the part of a
+// block that a CTA covers is an item, whose stream entries are the block's exact
+// sub-groups (16 fp16 tokens each, if the CTA owns the exact part), the record sealed in
+// this step, then sealed groups. Each CTA writes one partial softmax state (running
+// max, sum, rotated accumulator) per block it covers; merge_kernel, launched after the
+// decode kernel, merges each block's partials, rotates back and writes fp16.
 //
-// Sealed-group stream. One producer thread copies whole group-pair records (K record
-// then V record, contiguous in the pool) into a ring of shared-memory stages with
-// cp.async.bulk; eight consumer warps take the stages round robin. For a group with
-// codes q, token scales a, channel scales c and grid (m, delta), the score of token t
-// is  scale * a_t * (delta * sum_j (q'_j c_j) q_tj + m * sum_j q'_j c_j)  with q' the
-// rotated query, and the rotated output accumulates
+// Stream. Entries are copied with cp.async.bulk into a ring of shared-memory stages;
+// entry n is processed by warp n mod 12, which then issues the copy of entry n + S into
+// the stage it freed. For a group with codes q, token scales a, channel scales c and
+// grid (m, delta), the score of token t is
+//   scale * a_t * (delta * sum_j (q'_j c_j) q_tj + m * sum_j q'_j c_j)
+// with q' the rotated query, and the rotated output accumulates
 //   c_j * (delta_V * sum_t w_t qV_jt + m_V * sum_t w_t),  w_t = p_t aV_t.
 // Both inner sums are dense 128 x 128 x (4 heads) contractions on the raw integer
 // codes, done with mma.sync m16n8k16 (f16 in, f32 accumulate). The codes become f16
