@@ -203,6 +203,7 @@ struct Smem {
     uint4* qtab;      // [2][kTabWords]: query operand tables (by block parity)
     float* qrot;      // [2][4][128]: rotated query of the table builder
     float* qmax;      // [2][4]
+    uint32_t* qraw;   // [2][4][64]: the block's query as read (half2 words), for its exact part
     float* xbuf;      // [kWarps][kXbWarp] (half2 words)
     WarpRegion* region;  // [kWarps]
     ItemCtl* ictl;       // [2]
@@ -286,12 +287,14 @@ __device__ __forceinline__ void spin_until(const int* w, int v, bool at_least, i
 // Rotate head h of block (ci, kvh) into table slot b (one warp).
 __device__ void rotate_head(const DecodeParams& p, const Smem& sm, int b, int ci, int kvh, int h, int lane) {
     float v[4] = {0.f, 0.f, 0.f, 0.f};
+    uint2 raw = make_uint2(0u, 0u);
     if (h < p.r) {
         const uint16_t* q = p.q + ((size_t)ci * p.hq + (size_t)kvh * p.r + h) * 128 + 4 * lane;
-        uint2 raw = *reinterpret_cast<const uint2*>(q);
+        raw = *reinterpret_cast<const uint2*>(q);
         float2 f0 = __half22float2(bits_h2(raw.x)), f1 = __half22float2(bits_h2(raw.y));
         v[0] = f0.x; v[1] = f0.y; v[2] = f1.x; v[3] = f1.y;
     }
+    *reinterpret_cast<uint2*>(sm.qraw + 256 * b + 64 * h + 2 * lane) = raw;
     warp_fwht128(v, lane);
     float mx = fmaxf(fmaxf(fabsf(v[0]), fabsf(v[1])), fmaxf(fabsf(v[2]), fabsf(v[3])));
 #pragma unroll
@@ -374,15 +377,14 @@ __device__ void acquire_table(const DecodeParams& p, const Smem& sm, int kb, int
 }
 
 // Exact query operand of a warp: column g holds head g >> 1 (both columns of a head
-// carry it), k pairs are channels 16 ks + 2 tq (+ 8).
-__device__ __forceinline__ void exact_query(const DecodeParams& p, int ci, int kvh, int g, int tq,
-                                            uint32_t (&bq)[16]) {
-    const int h = g >> 1;
-    const uint32_t* qw = reinterpret_cast<const uint32_t*>(p.q + ((size_t)ci * p.hq + (size_t)kvh * p.r + h) * 128);
+// carry it), k pairs are channels 16 ks + 2 tq (+ 8); read from the copy of the query
+// kept with the block's table in slot b (zeros for heads the group does not have).
+__device__ __forceinline__ void exact_query(const Smem& sm, int b, int g, int tq, uint32_t (&bq)[16]) {
+    const uint32_t* qw = sm.qraw + 256 * b + 64 * (g >> 1);
 #pragma unroll
     for (int ks = 0; ks < 8; ++ks) {
-        bq[2 * ks] = h < p.r ? qw[8 * ks + tq] : 0u;
-        bq[2 * ks + 1] = h < p.r ? qw[8 * ks + 4 + tq] : 0u;
+        bq[2 * ks] = qw[8 * ks + tq];
+        bq[2 * ks + 1] = qw[8 * ks + 4 + tq];
     }
 }
 
@@ -974,6 +976,8 @@ __global__ void __launch_bounds__(kDecodeThreads, 1) decode_kernel(const __grid_
         off += 2 * 512 * 4;
         sm.qmax = reinterpret_cast<float*>(smem_raw + off);
         off += 2 * 4 * 4;
+        sm.qraw = reinterpret_cast<uint32_t*>(smem_raw + off);
+        off += 2 * 4 * 64 * 4;
         sm.region = reinterpret_cast<WarpRegion*>(smem_raw + off);
         off += kWarps * sizeof(WarpRegion);
         sm.ictl = reinterpret_cast<ItemCtl*>(smem_raw + off);
@@ -1186,7 +1190,7 @@ __global__ void __launch_bounds__(kDecodeThreads, 1) decode_kernel(const __grid_
         uint32_t k = (uint32_t)((w + kWarps - (int)(n % kWarps)) % kWarps);
         if (k < (uint32_t)it.n_ex) {  // exact sub-groups come first
             uint32_t bq[16];
-            exact_query(p, it.ci, it.kvh, g, tq, bq);
+            exact_query(sm, kb & 1, g, tq, bq);
             const int js = (e.n_sink + kExactRows - 1) / kExactRows;
             for (; k < (uint32_t)it.n_ex; k += kWarps) {
                 const uint32_t gn = n + k;
@@ -1336,7 +1340,7 @@ int decode_smem_bytes(int k_bits, int v_bits, int stages, bool with_seal) {
     size_t off = (size_t)stages * pair;
     if (off < sizeof(SealSmem)) off = sizeof(SealSmem);
     off = (off + 15) & ~(size_t)15;
-    off += 32 * 8 + 32 * 4 + 2 * kTabWords * 16 + 2 * 512 * 4 + 2 * 4 * 4 + kWarps * sizeof(WarpRegion) + 2 * sizeof(ItemCtl) + 16 * 4 + 8 * 4 + kWarps * sizeof(GroupCursor) + sizeof(ItemList) + 16 + kMaxEntries * 8 +
+    off += 32 * 8 + 32 * 4 + 2 * kTabWords * 16 + 2 * 512 * 4 + 2 * 4 * 4 + 2 * 4 * 64 * 4 + kWarps * sizeof(WarpRegion) + 2 * sizeof(ItemCtl) + 16 * 4 + 8 * 4 + kWarps * sizeof(GroupCursor) + sizeof(ItemList) + 16 + kMaxEntries * 8 +
            kWarps * kXbWarp * 4;
     return (int)off;
 }
