@@ -72,6 +72,12 @@ typedef enum {
 /* Flags for kvarn_config.flags. */
 #define KVARN_FLAG_HOST_ONLY 1 /* bookkeeping only: no CUDA call and no launch is made.
                                   For testing the cache logic on machines without a GPU. */
+#define KVARN_FLAG_TEST_STALL 2 /* testing the timeout path only: in every decode launch one
+                                   thread waits, before any copy is issued, on a word that
+                                   nothing sets; the bounded wait gives up after about 2 s,
+                                   records the timeout in the error word and the launch goes
+                                   on (its results stay correct). kvarn_check_device_error
+                                   then returns KVARN_ETIMEOUT. Not for production use. */
 
 typedef struct {
     int32_t num_layers;     /* attention layers held by this cache */

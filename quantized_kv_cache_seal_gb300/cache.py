@@ -13,10 +13,11 @@ from . import kvarn as K
 
 class KVarNCache:
     def __init__(self, num_layers=1, max_seqs=1, num_q_heads=32, num_kv_heads=8, k_bits=2, v_bits=2,
-                 sinkhorn_iters=16, max_seq_len=32768, pool_groups=None, device="cuda"):
+                 sinkhorn_iters=16, max_seq_len=32768, pool_groups=None, device="cuda", flags=0):
         self.cfg = K.make_config(num_layers=num_layers, max_seqs=max_seqs, num_q_heads=num_q_heads,
                                  num_kv_heads=num_kv_heads, k_bits=k_bits, v_bits=v_bits,
-                                 sinkhorn_iters=sinkhorn_iters, max_seq_len=max_seq_len, pool_groups=pool_groups)
+                                 sinkhorn_iters=sinkhorn_iters, max_seq_len=max_seq_len, pool_groups=pool_groups,
+                                 flags=flags)
         self.nbytes = K.kvarn_cache_required_bytes(self.cfg)
         self.mem = torch.empty(self.nbytes + 256, dtype=torch.uint8, device=device)
         base = self.mem.data_ptr()

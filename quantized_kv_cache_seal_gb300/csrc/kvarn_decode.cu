@@ -1025,6 +1025,10 @@ __global__ void __launch_bounds__(kDecodeThreads, 1) decode_kernel(const __grid_
     // the merge kernel that follows may be scheduled now; it waits for this grid to finish
     asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
     int32_t* err = err_word(p);
+    if (p.test_stall && b == 0) {  // a bounded wait on a word nothing sets (timeout path test)
+        if (t == 0) spin_until(sm.ctl + 6, 1, false, err);
+        __syncthreads();
+    }
     const ItemList& IL = *sm.items;
     // ---- sources of the stream's entries, resolved once (block-table loads in parallel)
     {

@@ -49,6 +49,7 @@ struct kvarn_cache {
     int sms = 152;
     int max_smem = 227 * 1024;
     bool host_only = false;
+    bool test_stall = false;
 
     int64_t& L(int seq, int layer) { return len[(size_t)seq * cfg.num_layers + layer]; }
     int64_t Lc(int seq, int layer) const { return len[(size_t)seq * cfg.num_layers + layer]; }
@@ -224,6 +225,7 @@ kvarn_status run_decode(kvarn_cache* c, int32_t layer, int32_t n_seqs, const int
     p.slot_bytes = (int32_t)c->slot_bytes;
     p.pool_slots = cfg.pool_groups;
     p.scale_log2 = scale * 1.4426950408889634f;
+    p.test_stall = c->test_stall ? 1 : 0;
     bool any_seal = false;
     std::vector<int32_t> taken;
     for (int i = 0; i < n_seqs; ++i) {
@@ -315,6 +317,7 @@ kvarn_status kvarn_cache_create(const kvarn_config* cfg, void* dev_mem, size_t b
     c->rec_k = record_bytes(cfg->k_bits);
     c->rec_v = record_bytes(cfg->v_bits);
     c->host_only = (cfg->flags & KVARN_FLAG_HOST_ONLY) != 0;
+    c->test_stall = (cfg->flags & KVARN_FLAG_TEST_STALL) != 0;
     c->len.assign((size_t)cfg->max_seqs * cfg->num_layers, 0);
     c->table.assign((size_t)cfg->max_seqs * cfg->num_layers * c->max_groups, -1);
     c->free_slots.resize(cfg->pool_groups);

@@ -75,6 +75,7 @@ struct DecodeParams {
     int32_t grid;               // CTAs
     int64_t units_total;
     uint32_t epoch;
+    int32_t test_stall;         // KVARN_FLAG_TEST_STALL: one bounded wait that runs out
     float scale_log2;           // softmax_scale * log2(e)
     SeqEntry seqs[kMaxBatch];
 };

@@ -17,6 +17,7 @@ from . import build as _build
 STATUS = {0: "KVARN_OK", 1: "KVARN_EINVAL", 2: "KVARN_ENOMEM", 3: "KVARN_ECAPACITY", 4: "KVARN_ECUDA",
           5: "KVARN_ESTATE", 6: "KVARN_ETIMEOUT"}
 KVARN_FLAG_HOST_ONLY = 1
+KVARN_FLAG_TEST_STALL = 2
 
 # every entry point declared in include/kvarn.h
 EXPORTS = [
