@@ -209,6 +209,22 @@ kvarn_status kvarn_cache_stats(const kvarn_cache* cache, kvarn_stats* out);
 kvarn_status kvarn_seal_groups(const void* x, int32_t n, int32_t bits, int32_t which, int32_t sinkhorn_iters,
                                void* records, float* scales, void* stream);
 
+/* Partition of a decode call's work over CTAs, the one every decode call uses
+ * (exposed to test and inspect schedules; host only, no CUDA call). The work is a
+ * line of n_blocks blocks, block k holding units[k] >= 1 scheduling units (one
+ * sealed group pair is one unit); the first head[k] units of block k
+ * (1 <= head[k] <= units[k]; a decode call's exact part and seal of a (sequence,
+ * KV head)) must go whole to one CTA. Writes the cut table cuts[0..n] (host array
+ * of max_ctas + 1 entries): cuts[0] = 0, cuts[n] = the total, CTA b takes units
+ * [cuts[b], cuts[b + 1]), n <= max_ctas, no range empty, no cut strictly inside a
+ * head, every block covered by at most max_span ranges; n in *n_ctas. The cuts are
+ * the greedy fill (each cut as late as a bound L and the heads allow) for the
+ * smallest L >= min_load found by bisection: when max_span does not bind, no valid
+ * partition into max_ctas ranges has a smaller largest range. KVARN_EINVAL for bad
+ * arguments, KVARN_ECAPACITY if the total reaches 2^31 or nothing fits. */
+kvarn_status kvarn_partition_units(int32_t n_blocks, const int32_t* units, const int32_t* head, int32_t max_ctas,
+                                   int32_t max_span, int32_t min_load, int32_t* cuts, int32_t* n_ctas);
+
 /* Read and clear the device error word of the cache (synchronises `stream`).
  * KVARN_OK, or KVARN_ETIMEOUT if a bounded wait in a kernel gave up. */
 kvarn_status kvarn_check_device_error(kvarn_cache* cache, void* stream);

@@ -111,7 +111,15 @@ __device__ __forceinline__ int tok_row(int mt, int g) {
     return CPW * (mt * (16 / CPW) + g / HALF) + g % HALF;
 }
 
-__device__ __forceinline__ int64_t covering(int64_t u, int64_t U, int64_t P) { return ((u + 1) * P + U - 1) / U - 1; }
+// CTA whose unit range holds unit u (the host's cut table: the last b with cta_begin[b] <= u).
+__device__ __forceinline__ int64_t covering(const DecodeParams& p, int64_t u) {
+    int lo = 0, hi = p.grid - 1;
+    while (lo < hi) {
+        const int mid = (lo + hi + 1) >> 1;
+        if (p.cta_begin[mid] <= u) lo = mid; else hi = mid - 1;
+    }
+    return lo;
+}
 
 // The part of one (sequence, KV head) block that a CTA's unit range covers. Its stream
 // entries, in order: n_ex exact sub-groups (the CTA that covers the block's first unit
@@ -246,9 +254,9 @@ __device__ __forceinline__ void warp_fwht128(float (&v)[4], int lane) {
 __device__ int block_ctas(const DecodeParams& p, const SeqEntry& e, int kvh, int64_t* first_cta) {
     const int per = e.w_exact + e.w_seal + e.n_groups;
     const int64_t blk0 = e.unit_begin + (int64_t)kvh * per;
-    const int64_t f = covering(blk0, p.units_total, p.grid);
+    const int64_t f = covering(p, blk0);
     if (first_cta) *first_cta = f;
-    return (int)(covering(blk0 + per - 1, p.units_total, p.grid) - f + 1);
+    return (int)(covering(p, blk0 + per - 1) - f + 1);
 }
 
 // ldmatrix of four 8 x 8 b16 matrices (row addresses from lanes 8i .. 8i + 7 for matrix i).
@@ -617,9 +625,25 @@ __device__ __forceinline__ void process_group(const DecodeParams& p, const uint8
     query_operand<KB>(krec, qtab, tq, lane, bf);
     float2 raw[8];
     float colsum, corr, rho;
-    tiles_mma<KB>(rows_k, off_k, bf, raw, colsum);
-    corr = softmax_weights<VB>(p, krec, vrec, qm, colsum, raw, xb, st, g, tq, lane, bf, rho);
-    tiles_mma<VB>(rows_v, off_v, bf, raw, colsum);
+    if constexpr (KB == VB) {
+        // One copy of the contraction code serves both records (a loop that is not
+        // unrolled): the group loop then fits the instruction cache far better.
+        const uint8_t* rows = rows_k;
+        int off = off_k;
+#pragma unroll 1
+        for (int side = 0; side < 2; ++side) {
+            tiles_mma<KB>(rows, off, bf, raw, colsum);
+            if (side == 0) {
+                corr = softmax_weights<VB>(p, krec, vrec, qm, colsum, raw, xb, st, g, tq, lane, bf, rho);
+                rows = rows_v;
+                off = off_v;
+            }
+        }
+    } else {
+        tiles_mma<KB>(rows_k, off_k, bf, raw, colsum);
+        corr = softmax_weights<VB>(p, krec, vrec, qm, colsum, raw, xb, st, g, tq, lane, bf, rho);
+        tiles_mma<VB>(rows_v, off_v, bf, raw, colsum);
+    }
     pv_update(vrec, raw, colsum, corr, rho, st, g);
 }
 
@@ -833,7 +857,7 @@ struct __align__(16) GroupCursor {
         row = nullptr;
     }
     // source of entry gn (gn never decreases between calls); kind 0 past the end
-    __device__ PendingCopy resolve(const DecodeParams& p, const ItemList& L, int64_t hi, uint32_t gn) {
+    __device__ __noinline__ PendingCopy resolve(const DecodeParams& p, const ItemList& L, int64_t hi, uint32_t gn) {
         PendingCopy pc;
         pc.kind = 0;
         pc.aux = 0;
@@ -883,22 +907,29 @@ struct __align__(16) GroupCursor {
     }
 };
 
+// Copies of an exact sub-group's rows (whole warp): K rows by lanes 0..15, V rows by
+// lanes 16..31, each into a row padded to kRowPitch. Kept out of line: the group loop
+// stays short.
+__device__ __noinline__ void issue_exact_rows(const DecodeParams& p, uint64_t* bar, uint8_t* dst, const uint8_t* base,
+                                              int aux, int lane) {
+    const int rows = aux & 255;
+    if (lane == 0) mbar_arrive_expect_tx(bar, (uint32_t)(2 * 256 * rows));
+    const int r = lane & 15;
+    if (r < rows) {
+        const size_t kv = (aux & 256) ? p.lay.tail_v - p.lay.tail_k : p.lay.sink_v - p.lay.sink_k;
+        const uint8_t* src = base + (lane < 16 ? 0 : kv) + (size_t)r * 256;
+        bulk_g2s(dst + (lane < 16 ? 0 : kExactVOff) + r * kRowPitch, src, 256, bar);
+    }
+}
+
 // Issue the copy of a group into stage s (whole warp). A record is one bulk copy by lane
-// 0; an exact sub-group is one 256-byte copy per row (K rows by lanes 0..15, V rows by
-// lanes 16..31) into rows padded to kRowPitch.
+// 0; an exact sub-group is one 256-byte copy per row (issue_exact_rows).
 __device__ __forceinline__ void issue_copy(const DecodeParams& p, const Smem& sm, const PendingCopy& pc, uint32_t gn,
                                            uint32_t s, int lane) {
     if (pc.kind == 0) return;
     uint8_t* dst = sm.stages + (size_t)s * (uint32_t)(p.rec_k + p.rec_v);
     if (pc.kind == 1) {
-        const int rows = pc.aux & 255;
-        if (lane == 0) mbar_arrive_expect_tx(sm.full + s, (uint32_t)(2 * 256 * rows));
-        const int r = lane & 15;
-        if (r < rows) {
-            const size_t kv = (pc.aux & 256) ? p.lay.tail_v - p.lay.tail_k : p.lay.sink_v - p.lay.sink_k;
-            const uint8_t* src = pc.base + (lane < 16 ? 0 : kv) + (size_t)r * 256;
-            bulk_g2s(dst + (lane < 16 ? 0 : kExactVOff) + r * kRowPitch, src, 256, sm.full + s);
-        }
+        issue_exact_rows(p, sm.full + s, dst, pc.base, pc.aux, lane);
     } else if (lane == 0) {
         const uint8_t* src = pc.base;
         if (pc.kind == 3) {
@@ -1007,8 +1038,8 @@ __global__ void __launch_bounds__(kDecodeThreads, 1) decode_kernel(const __grid_
         sm.ictl[t].count = 0;
         sm.ictl[t].mask = 0;
     }
-    const int64_t U = p.units_total, P = p.grid, b = blockIdx.x;
-    const int64_t lo = b * U / P, hi = (b + 1) * U / P;
+    const int64_t b = blockIdx.x;
+    const int64_t lo = p.cta_begin[b], hi = p.cta_begin[b + 1];
     if (t == 0) {
         for (int s = 0; s < p.stages; ++s) mbar_init(sm.full + s, 1);
         asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");

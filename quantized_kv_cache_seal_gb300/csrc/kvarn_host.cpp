@@ -128,19 +128,86 @@ int exact_units(const kvarn_cache* c, int n_sink, int n_tail) {
 }
 
 int seal_units(const kvarn_cache* c) {
-    // a K + V seal inside the decode kernel costs about as much as 80 group pairs of
-    // 2-bit records on one SM (measured); wider records make a group pair dearer
+    // a K + V seal inside the decode kernel costs about as much as 140 group pairs of
+    // 2-bit records on one SM (measured: ~43 us against ~0.31 us per group pair);
+    // wider records make a group pair dearer
     const double pair2 = 2.0 * (528 + 2048 * 2);
-    return std::max(1, (int)std::lround(80.0 * pair2 / (double)(c->rec_k + c->rec_v)));
+    return std::max(1, (int)std::lround(140.0 * pair2 / (double)(c->rec_k + c->rec_v)));
 }
 
-// covering CTA of unit u when U units are split evenly over P CTAs
-inline int64_t covering(int64_t u, int64_t U, int64_t P) { return ((u + 1) * P + U - 1) / U - 1; }
+// Greedy fill of the unit line with ranges of at most L units, each cut as late as the
+// indivisible block heads allow. begin[k] = first unit of block k (begin[nb] = total).
+// Returns the number of ranges (cuts in `cuts`, from 0 to the total).
+int greedy_cuts(const std::vector<int64_t>& begin, const int32_t* head, int64_t L, std::vector<int32_t>& cuts) {
+    const int nb = (int)begin.size() - 1;
+    const int64_t U = begin[nb];
+    cuts.clear();
+    cuts.push_back(0);
+    int64_t start = 0;
+    while (start < U) {
+        int64_t end = start + L;
+        if (end >= U) {
+            end = U;
+        } else {
+            // block holding unit `end`: the last k with begin[k] <= end
+            const int k = (int)(std::upper_bound(begin.begin(), begin.begin() + nb, end) - begin.begin()) - 1;
+            if (begin[k] < end && end < begin[k] + head[k]) end = begin[k];  // > start as L >= every head
+        }
+        cuts.push_back((int32_t)end);
+        start = end;
+    }
+    return (int)cuts.size() - 1;
+}
 
-// Fill the schedule of a decode call: per sequence unit offsets, grid size.
+// Ranges covering each block at most max_span.
+bool spans_ok(const std::vector<int64_t>& begin, const std::vector<int32_t>& cuts, int max_span) {
+    const int nb = (int)begin.size() - 1;
+    for (int k = 0; k < nb; ++k) {
+        const int64_t a = begin[k], z = begin[k + 1] - 1;
+        const int ca = (int)(std::upper_bound(cuts.begin(), cuts.end(), (int32_t)a) - cuts.begin()) - 1;
+        const int cz = (int)(std::upper_bound(cuts.begin(), cuts.end(), (int32_t)z) - cuts.begin()) - 1;
+        if (cz - ca + 1 > max_span) return false;
+    }
+    return true;
+}
+
+kvarn_status partition_units(int nb, const int32_t* units, const int32_t* head, int max_ctas, int max_span,
+                             int min_load, std::vector<int32_t>& cuts) {
+    if (nb < 1 || !units || !head || max_ctas < 1 || max_span < 1 || min_load < 1) return KVARN_EINVAL;
+    std::vector<int64_t> begin(nb + 1, 0);
+    int64_t lo = min_load;
+    for (int k = 0; k < nb; ++k) {
+        if (units[k] < 1 || head[k] < 1 || head[k] > units[k]) return KVARN_EINVAL;
+        begin[k + 1] = begin[k] + units[k];
+        lo = std::max<int64_t>(lo, head[k]);
+    }
+    const int64_t U = begin[nb];
+    if (U >= (1ll << 31)) return KVARN_ECAPACITY;
+    lo = std::max<int64_t>(lo, (U + max_ctas - 1) / max_ctas);
+    auto fits = [&](int64_t L) {
+        return greedy_cuts(begin, head, L, cuts) <= max_ctas && spans_ok(begin, cuts, max_span);
+    };
+    // smallest bound that fits, by bisection (the range count of the greedy fill only
+    // falls as L grows; the span limit, when it binds, is re-checked below)
+    int64_t hi = std::max(lo, U);
+    if (!fits(hi)) return KVARN_ECAPACITY;
+    while (lo < hi) {
+        const int64_t mid = lo + (hi - lo) / 2;
+        if (fits(mid)) hi = mid; else lo = mid + 1;
+    }
+    while (!fits(lo)) ++lo;  // terminates: the bound U fits
+    return KVARN_OK;
+}
+
+// Fill the schedule of a decode call: per sequence unit offsets, the CTA ranges. The
+// units of one (sequence, KV head) block are, in order: its exact part, the seal made
+// in this call (if any), its sealed groups. The exact part and the seal go whole to the
+// CTA that covers the block's first unit.
 kvarn_status schedule(kvarn_cache* c, DecodeParams& p) {
     int64_t U = 0;
-    int64_t max_groups = 0;
+    std::vector<int32_t> units, head;
+    units.reserve((size_t)p.n_seqs * p.hkv);
+    head.reserve((size_t)p.n_seqs * p.hkv);
     for (int i = 0; i < p.n_seqs; ++i) {
         SeqEntry& e = p.seqs[i];
         e.unit_begin = (int32_t)U;
@@ -148,28 +215,22 @@ kvarn_status schedule(kvarn_cache* c, DecodeParams& p) {
         int ws = e.seal_group >= 0 ? seal_units(c) : 0;
         e.w_exact = we;
         e.w_seal = ws;
-        U += (int64_t)p.hkv * (we + ws + e.n_groups);
-        max_groups = std::max<int64_t>(max_groups, e.n_groups);
-    }
-    if (U >= (1ll << 31)) return KVARN_ECAPACITY;
-    p.units_total = U;
-    int64_t P = std::min<int64_t>(c->sms, std::max<int64_t>(1, U / 24));
-    // the CTAs covering one (sequence, KV head) block must fit in its kMaxSpan partial slots
-    for (;;) {
-        bool ok = true;
-        for (int i = 0; i < p.n_seqs && ok; ++i) {
-            const SeqEntry& e = p.seqs[i];
-            const int per = e.w_exact + e.w_seal + e.n_groups;
-            for (int h = 0; h < p.hkv && ok; ++h) {
-                int64_t u0 = e.unit_begin + (int64_t)h * per;
-                int64_t u1 = u0 + per - 1;
-                if (covering(u1, U, P) - covering(u0, U, P) + 1 > kMaxSpan) ok = false;
-            }
+        const int64_t per = (int64_t)we + ws + e.n_groups;
+        if (U + (int64_t)p.hkv * per >= (1ll << 31)) return KVARN_ECAPACITY;
+        for (int h = 0; h < p.hkv; ++h) {
+            units.push_back((int32_t)per);
+            head.push_back(we + ws);
         }
-        if (ok) break;
-        P = std::max<int64_t>(1, P * 3 / 4);
+        U += (int64_t)p.hkv * per;
     }
-    p.grid = (int)P;
+    p.units_total = U;
+    std::vector<int32_t> cuts;
+    const int max_ctas = std::max(1, std::min(c->sms, kMaxGrid));
+    // at least 24 units per CTA: fewer would make the per-CTA start and merge dominate
+    kvarn_status st = partition_units((int)units.size(), units.data(), head.data(), max_ctas, kMaxSpan, 24, cuts);
+    if (st) return st;
+    p.grid = (int)cuts.size() - 1;
+    for (size_t b = 0; b < cuts.size(); ++b) p.cta_begin[b] = cuts[b];
     return KVARN_OK;
 }
 
@@ -293,6 +354,17 @@ kvarn_status run_decode(kvarn_cache* c, int32_t layer, int32_t n_seqs, const int
 extern "C" {
 
 size_t kvarn_record_bytes(int32_t bits) { return bits_ok(bits) ? record_bytes(bits) : 0; }
+
+kvarn_status kvarn_partition_units(int32_t n_blocks, const int32_t* units, const int32_t* head, int32_t max_ctas,
+                                   int32_t max_span, int32_t min_load, int32_t* cuts, int32_t* n_ctas) {
+    if (!cuts || !n_ctas) return KVARN_EINVAL;
+    std::vector<int32_t> c;
+    kvarn_status st = partition_units(n_blocks, units, head, max_ctas, max_span, min_load, c);
+    if (st) return st;
+    std::copy(c.begin(), c.end(), cuts);
+    *n_ctas = (int32_t)c.size() - 1;
+    return KVARN_OK;
+}
 
 kvarn_status kvarn_cache_required_bytes(const kvarn_config* cfg, size_t* bytes) {
     kvarn_status st = check_config(cfg);

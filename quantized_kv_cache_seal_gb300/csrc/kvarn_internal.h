@@ -18,6 +18,7 @@ constexpr int kGroup = 128;
 constexpr int kSink = 128;
 constexpr int kMaxBatch = 256;   // sequences per decode call (kernel parameter table size)
 constexpr int kMaxSpan = 32;     // CTAs that may share the sealed groups of one (seq, kv head)
+constexpr int kMaxGrid = 256;    // CTAs of a decode launch (at most one per SM)
 constexpr int kPartialSlots = kMaxSpan;  // one partial per CTA covering a block
 constexpr int kPartialFloats = 528;  // [0] epoch bits, [4..8) m, [8..12) l, [12..524) acc
 constexpr int kDecodeThreads = 384;  // 12 warps
@@ -74,6 +75,7 @@ struct DecodeParams {
     int32_t stages;             // smem ring stages
     int32_t grid;               // CTAs
     int64_t units_total;
+    int32_t cta_begin[kMaxGrid + 1];  // first scheduling unit of each CTA; [grid] = units_total
     uint32_t epoch;
     int32_t test_stall;         // KVARN_FLAG_TEST_STALL: one bounded wait that runs out
     float scale_log2;           // softmax_scale * log2(e)

@@ -25,7 +25,7 @@ EXPORTS = [
     "kvarn_append", "kvarn_decode_attention", "kvarn_decode_attention_noalloc", "kvarn_decode_step", "kvarn_dequant_group",
     "kvarn_seq_release", "kvarn_seq_length", "kvarn_group_record", "kvarn_exact_regions",
     "kvarn_cache_stats", "kvarn_seal_groups", "kvarn_check_device_error", "kvarn_status_string",
-    "kvarn_last_error",
+    "kvarn_last_error", "kvarn_partition_units",
 ]
 
 
@@ -92,6 +92,7 @@ def load(build_if_missing: bool = True):
     L.kvarn_status_string.restype = ctypes.c_char_p
     L.kvarn_last_error.argtypes = []
     L.kvarn_last_error.restype = ctypes.c_char_p
+    L.kvarn_partition_units.argtypes = [I32, IP, IP, I32, I32, I32, IP, IP]
     for name in EXPORTS:
         fn = getattr(L, name)
         if fn.restype is ctypes.c_int:  # default: status enum
@@ -222,6 +223,19 @@ def kvarn_seal_groups(x, n, bits, which, sinkhorn_iters, records, scales=None, s
 
 def kvarn_check_device_error(handle, stream=None) -> int:
     return int(load().kvarn_check_device_error(handle, _stream(stream)))
+
+
+def kvarn_partition_units(units, head, max_ctas: int, max_span: int, min_load: int):
+    """Cut table of the decode scheduler's partition (host only): list of n + 1 cuts."""
+    I32 = ctypes.c_int32
+    nb = len(units)
+    U = (I32 * max(nb, 1))(*units)
+    H = (I32 * max(nb, 1))(*head)
+    cuts = (I32 * (max_ctas + 1))()
+    n = I32()
+    _check(load().kvarn_partition_units(nb, U, H, max_ctas, max_span, min_load, cuts, ctypes.byref(n)),
+           "kvarn_partition_units")
+    return [int(cuts[i]) for i in range(n.value + 1)]
 
 
 def kvarn_status_string(status: int) -> str:
