@@ -1055,6 +1055,10 @@ __global__ void __launch_bounds__(kDecodeThreads, 1) decode_kernel(const __grid_
     __syncthreads();
     // the merge kernel that follows may be scheduled now; it waits for this grid to finish
     asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+    // this grid is itself a programmatic dependent of the work before it in the stream
+    // (the previous step's merge, or the kernel that wrote q, k or v): nothing above read
+    // global memory, everything below may read that work's output
+    asm volatile("griddepcontrol.wait;" ::: "memory");
     int32_t* err = err_word(p);
     if (p.test_stall && b == 0) {  // a bounded wait on a word nothing sets (timeout path test)
         if (t == 0) spin_until(sm.ctl + 6, 1, false, err);
@@ -1284,6 +1288,8 @@ __global__ void __launch_bounds__(kDecodeThreads, 1) decode_kernel(const __grid_
 // (programmatic dependent launch); it waits for that grid's completion before reading.
 __global__ void __launch_bounds__(128) merge_kernel(const __grid_constant__ DecodeParams p) {
     asm volatile("griddepcontrol.wait;" ::: "memory");
+    // the next decode launch may start its CTAs now (it waits for this grid before reading)
+    asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
     const int ci = blockIdx.x / p.hkv, kvh = blockIdx.x % p.hkv;
     const int h = threadIdx.x >> 5, lane = threadIdx.x & 31;
     if (h >= p.r) return;
@@ -1361,8 +1367,19 @@ int launch_t(const DecodeParams& p, int smem, cudaStream_t s) {
         if (e != cudaSuccess) return (int)e;
         attr = true;
     }
-    decode_kernel<KB, VB><<<p.grid, kDecodeThreads, smem, s>>>(p);
-    const int rc = (int)cudaGetLastError();
+    // programmatic dependent of the work before it in the stream: the CTAs start (and
+    // build their item lists) while that work drains, and wait for it before reading memory
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3((unsigned)p.grid);
+    cfg.blockDim = dim3(kDecodeThreads);
+    cfg.dynamicSmemBytes = (size_t)smem;
+    cfg.stream = s;
+    cudaLaunchAttribute la[1];
+    la[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    la[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = la;
+    cfg.numAttrs = 1;
+    const int rc = (int)cudaLaunchKernelEx(&cfg, decode_kernel<KB, VB>, p);
     if (rc) return rc;
     return launch_merge(p, s);
 }
