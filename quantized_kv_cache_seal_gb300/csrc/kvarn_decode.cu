@@ -292,14 +292,18 @@ __device__ __forceinline__ void spin_until(const int* w, int v, bool at_least, i
 // v = vh + vl, the table holds per pair: vh, -vh on a low-part lane (0 on a high-part
 // lane) and vl on a low-part lane (0 on a high-part lane).
 
-// Rotate head h of block (ci, kvh) into table slot b (one warp).
-__device__ void rotate_head(const DecodeParams& p, const Smem& sm, int b, int ci, int kvh, int h, int lane) {
-    float v[4] = {0.f, 0.f, 0.f, 0.f};
-    uint2 raw = make_uint2(0u, 0u);
-    if (h < p.r) {
-        const uint16_t* q = p.q + ((size_t)ci * p.hq + (size_t)kvh * p.r + h) * 128 + 4 * lane;
-        raw = *reinterpret_cast<const uint2*>(q);
-        float2 f0 = __half22float2(bits_h2(raw.x)), f1 = __half22float2(bits_h2(raw.y));
+// Lane's four query values of head h of block (ci, kvh) (zeros for a head the block's
+// KV head does not have).
+__device__ __forceinline__ uint2 load_query(const DecodeParams& p, int ci, int kvh, int h, int lane) {
+    if (h >= p.r) return make_uint2(0u, 0u);
+    return *reinterpret_cast<const uint2*>(p.q + ((size_t)ci * p.hq + (size_t)kvh * p.r + h) * 128 + 4 * lane);
+}
+
+// Rotate head h (its values `raw` as load_query read them) into table slot b (one warp).
+__device__ void rotate_loaded(const Smem& sm, int b, int h, int lane, uint2 raw) {
+    float v[4];
+    {
+        const float2 f0 = __half22float2(bits_h2(raw.x)), f1 = __half22float2(bits_h2(raw.y));
         v[0] = f0.x; v[1] = f0.y; v[2] = f1.x; v[3] = f1.y;
     }
     *reinterpret_cast<uint2*>(sm.qraw + 256 * b + 64 * h + 2 * lane) = raw;
@@ -313,6 +317,12 @@ __device__ void rotate_head(const DecodeParams& p, const Smem& sm, int b, int ci
 #pragma unroll
     for (int k = 0; k < 4; ++k) qrot[4 * lane + k] = v[k] * inv;
     if (lane == 0) sm.qmax[4 * b + h] = mx;
+}
+
+// Rotate head h of block (ci, kvh) into table slot b (one warp).
+__device__ __forceinline__ void rotate_head(const DecodeParams& p, const Smem& sm, int b, int ci, int kvh, int h,
+                                            int lane) {
+    rotate_loaded(sm, b, h, lane, load_query(p, ci, kvh, h, lane));
 }
 
 // Table entries of pairs 2 q and 2 q + 1 of lane `lane` in slot b, from the rotated query.
@@ -1065,6 +1075,22 @@ __global__ void __launch_bounds__(kDecodeThreads, 1) decode_kernel(const __grid_
         __syncthreads();
     }
     const ItemList& IL = *sm.items;
+    // the CTA's first two blocks: their query tables are built by the whole CTA; the query
+    // rows are loaded first, so that their latency overlaps the block-table loads below
+    int prebuilt = 0;
+    int bci[2] = {-1, -1}, bkv[2] = {-1, -1};
+    {
+        ItemWalk wk{lo, 0};
+        Item it;
+        while (prebuilt < 2 && walk_next(p, IL, wk, hi, it)) {
+            bci[prebuilt] = it.ci;
+            bkv[prebuilt] = it.kvh;
+            ++prebuilt;
+        }
+    }
+    const bool rotator = w < 4 * prebuilt;
+    uint2 qrow = make_uint2(0u, 0u);
+    if (rotator) qrow = load_query(p, bci[w >> 2], bkv[w >> 2], w & 3, lane);
     // ---- sources of the stream's entries, resolved once (block-table loads in parallel)
     {
         int total = 0;
@@ -1115,6 +1141,7 @@ __global__ void __launch_bounds__(kDecodeThreads, 1) decode_kernel(const __grid_
         const bool wide = ((uintptr_t)(p.base + p.lay.total) >> 48) != 0;
         if (t == 0) *sm.n_ent = (fits && !wide) ? total : -1;
     }
+    if (rotator) rotate_loaded(sm, w >> 2, w & 3, lane, qrow);
     __syncthreads();
     const int n_ent = *sm.n_ent;
 
@@ -1152,23 +1179,9 @@ __global__ void __launch_bounds__(kDecodeThreads, 1) decode_kernel(const __grid_
             }
         }
     }
+    // ---- query tables of the CTA's first two blocks (rotated above), by the whole CTA
+    for (int k = t; k < 256 * prebuilt; k += kDecodeThreads) fill_table<KB>(sm, k >> 8, (k >> 5) & 7, k & 31);
     fence_proxy_async_global();  // the rows and records just written are read by bulk copies
-
-    // ---- query tables of the CTA's first two blocks, by the whole CTA
-    int prebuilt = 0;
-    {
-        int bci[2] = {-1, -1}, bkv[2] = {-1, -1};
-        ItemWalk wk{lo, 0};
-        Item it;
-        while (prebuilt < 2 && walk_next(p, IL, wk, hi, it)) {
-            bci[prebuilt] = it.ci;
-            bkv[prebuilt] = it.kvh;
-            ++prebuilt;
-        }
-        if (w < 4 * prebuilt) rotate_head(p, sm, w >> 2, bci[w >> 2], bkv[w >> 2], w & 3, lane);
-        __syncthreads();
-        for (int k = t; k < 256 * prebuilt; k += kDecodeThreads) fill_table<KB>(sm, k >> 8, (k >> 5) & 7, k & 31);
-    }
     __syncthreads();
 
     // ---- 2. prologue: the first S groups of the stream. Lane 0 of each warp resolves the
