@@ -11,16 +11,17 @@
 //
 // Work split. Every (sequence, KV head) pair is a block of scheduling units: its exact
 // part, the seal of a group this step completes, and one unit per sealed group. The
-// units of all blocks are cut into equal contiguous ranges, one per CTA; the part of a
+// units of all blocks are cut into contiguous ranges of near-equal size, one per CTA
+// (a block's exact part and seal never split); the part of a
 // block that a CTA covers is an item, whose stream entries are the block's exact
 // sub-groups (16 fp16 tokens each, if the CTA owns the exact part), the record sealed in
 // this step, then sealed groups. Each CTA writes one partial softmax state (running
 // max, sum, rotated accumulator) per block it covers; merge_kernel, launched after the
 // decode kernel, merges each block's partials, rotates back and writes fp16.
 //
-// Stream. Entries are copied with cp.async.bulk into a ring of shared-memory stages;
-// entry n is processed by warp n mod 12, which then issues the copy of entry n + S into
-// the stage it freed. For a group with codes q, token scales a, channel scales c and
+// Stream. Entries are copied with cp.async.bulk into a ring of shared-memory stages by
+// one copy-issuing warp; entry n is processed by compute warp n mod 12, which releases
+// its stage (an mbarrier arrive) for the copy of entry n + S. For a group with codes q, token scales a, channel scales c and
 // grid (m, delta), the score of token t is
 //   scale * a_t * (delta * sum_j (q'_j c_j) q_tj + m * sum_j q'_j c_j)
 // with q' the rotated query, and the rotated output accumulates
@@ -45,7 +46,16 @@ namespace {
 constexpr int kEV = 13;      // weight operand exponent: |B| < 2^14
 constexpr int kXbHead = 88;  // exchange buffer words per head (bank-conflict-free stride)
 constexpr int kXbWarp = 4 * kXbHead;
-constexpr int kWarps = kDecodeThreads / 32;  // 12
+constexpr int kWarps = 12;  // compute warps (warpgroups 0..2); warpgroup 3 issues the copies
+static_assert(kDecodeThreads == 32 * (kWarps + 4), "three compute warpgroups and one copy-issuing warpgroup");
+// Registers per thread after the split: the kernel is launched with 65536 / 512 = 128;
+// the copy-issuing warpgroup gives back (128 - kRegsCopy) per thread, the compute
+// warpgroups take (kRegsCompute - 128). Per CTA 12 * 32 * 24 = 9216 taken, 4 * 32 * 72 =
+// 9216 given; per SM sub-partition (three compute warps, one copy warp) 2304 and 2304.
+constexpr int kRegsCompute = 152, kRegsCopy = 56;
+constexpr int kComputeThreads = 32 * kWarps;
+static_assert(kWarps * 32 * (kRegsCompute - 128) <= 4 * 32 * (128 - kRegsCopy), "register split exceeds the launch");
+static_assert(3 * 32 * (kRegsCompute - 128) <= 32 * (128 - kRegsCopy), "register split exceeds a sub-partition");
 constexpr int kRowPitch = 272;                // shared-memory pitch of an exact fp16 row (conflict-free ldmatrix)
 constexpr int kExactVOff = kExactRows * kRowPitch;  // V rows of an exact sub-group follow its K rows
 constexpr int kTabWords = 12 * 32;            // uint4 entries of one query operand table
@@ -206,7 +216,8 @@ struct ItemCtl {
 
 struct Smem {
     uint8_t* stages;
-    uint64_t* full;
+    uint64_t* full;   // [32]: copy of the stage's group landed
+    uint64_t* empty;  // [32]: the stage's group consumed (its stage may be refilled)
     uint32_t* gen;    // [32]: number of the group whose copy was last issued into each stage
     uint4* qtab;      // [2][kTabWords]: query operand tables (by block parity)
     float* qrot;      // [2][4][128]: rotated query of the table builder
@@ -217,7 +228,7 @@ struct Smem {
     ItemCtl* ictl;       // [2]
     int* busy;           // [kWarps]: item number parked in a warp's region, -1 if free
     int* ctl;            // [6]: table ready generation, claims and departures per table slot
-    struct GroupCursor* cursor;  // [kWarps]: each warp's copy cursor (all its lanes keep it in step)
+    struct GroupCursor* cursor;  // [4]: each copy warp's cursor (all its lanes keep it in step)
     ItemList* items;
     unsigned long long* ent;  // [kMaxEntries]
     int* n_ent;               // entries in ent, or -1 if the stream does not fit
@@ -991,10 +1002,12 @@ __device__ __forceinline__ void wait_group(const Smem& sm, uint32_t gn, uint32_t
     mbar_wait(sm.full + s, parity, err);
 }
 
-// One CTA of 12 warps per SM. Stage ring: group gn lives in stage gn % S and is
-// processed by warp gn % 12; the warp that finishes with a stage issues the copy of
-// group gn + S into it. After the seal phase the warps never wait for each other as a
-// whole: an item's states are folded warp by warp and the last warp writes its partial.
+// One CTA of four warpgroups per SM: three compute warpgroups (12 warps, 152 registers
+// per thread) and one copy-issuing warpgroup (56 registers; one warp issues). Stage
+// ring: group gn lives in stage gn % S and is processed by compute warp gn % 12, which
+// releases the stage; the copy warp then issues group gn + S into it. After the start
+// the compute warps never wait for each other as a whole: an item's states are folded
+// warp by warp and the last warp writes its partial.
 template <int KB, int VB>
 __global__ void __launch_bounds__(kDecodeThreads, 1) decode_kernel(const __grid_constant__ DecodeParams p) {
     extern __shared__ __align__(128) uint8_t smem_raw[];
@@ -1008,6 +1021,8 @@ __global__ void __launch_bounds__(kDecodeThreads, 1) decode_kernel(const __grid_
         off += ring;
         off = (off + 15) & ~(size_t)15;
         sm.full = reinterpret_cast<uint64_t*>(smem_raw + off);
+        off += 32 * 8;
+        sm.empty = reinterpret_cast<uint64_t*>(smem_raw + off);
         off += 32 * 8;
         sm.gen = reinterpret_cast<uint32_t*>(smem_raw + off);
         off += 32 * 4;
@@ -1028,7 +1043,7 @@ __global__ void __launch_bounds__(kDecodeThreads, 1) decode_kernel(const __grid_
         sm.ctl = reinterpret_cast<int*>(smem_raw + off);
         off += 8 * 4;
         sm.cursor = reinterpret_cast<GroupCursor*>(smem_raw + off);
-        off += kWarps * sizeof(GroupCursor);
+        off += 4 * sizeof(GroupCursor);
         sm.items = reinterpret_cast<ItemList*>(smem_raw + off);
         off += sizeof(ItemList);
         sm.n_ent = reinterpret_cast<int*>(smem_raw + off);
@@ -1051,7 +1066,10 @@ __global__ void __launch_bounds__(kDecodeThreads, 1) decode_kernel(const __grid_
     const int64_t b = blockIdx.x;
     const int64_t lo = p.cta_begin[b], hi = p.cta_begin[b + 1];
     if (t == 0) {
-        for (int s = 0; s < p.stages; ++s) mbar_init(sm.full + s, 1);
+        for (int s = 0; s < p.stages; ++s) {
+            mbar_init(sm.full + s, 1);
+            mbar_init(sm.empty + s, 1);
+        }
         asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
         int64_t u = lo;
         int n = 0;
@@ -1065,223 +1083,236 @@ __global__ void __launch_bounds__(kDecodeThreads, 1) decode_kernel(const __grid_
     __syncthreads();
     // the merge kernel that follows may be scheduled now; it waits for this grid to finish
     asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
-    // this grid is itself a programmatic dependent of the work before it in the stream
-    // (the previous step's merge, or the kernel that wrote q, k or v): nothing above read
-    // global memory, everything below may read that work's output
-    asm volatile("griddepcontrol.wait;" ::: "memory");
     int32_t* err = err_word(p);
-    if (p.test_stall && b == 0) {  // a bounded wait on a word nothing sets (timeout path test)
-        if (t == 0) spin_until(sm.ctl + 6, 1, false, err);
-        __syncthreads();
-    }
     const ItemList& IL = *sm.items;
-    // the CTA's first two blocks: their query tables are built by the whole CTA; the query
-    // rows are loaded first, so that their latency overlaps the block-table loads below
-    int prebuilt = 0;
-    int bci[2] = {-1, -1}, bkv[2] = {-1, -1};
-    {
-        ItemWalk wk{lo, 0};
-        Item it;
-        while (prebuilt < 2 && walk_next(p, IL, wk, hi, it)) {
-            bci[prebuilt] = it.ci;
-            bkv[prebuilt] = it.kvh;
-            ++prebuilt;
-        }
-    }
-    const bool rotator = w < 4 * prebuilt;
-    uint2 qrow = make_uint2(0u, 0u);
-    if (rotator) qrow = load_query(p, bci[w >> 2], bkv[w >> 2], w & 3, lane);
-    // ---- sources of the stream's entries, resolved once (block-table loads in parallel)
-    {
-        int total = 0;
-        if (IL.n <= kMaxItems)
-            for (int k = 0; k < IL.n; ++k) total += IL.it[k].count();
-        const bool fits = IL.n <= kMaxItems && total <= kMaxEntries;
-        if (fits) {
-            for (int e = t; e < total; e += kDecodeThreads) {
-                int k = 0, j = e;
-                while (j >= IL.it[k].count()) j -= IL.it[k++].count();
-                const Item& itm = IL.it[k];
-                const SeqEntry& se = p.seqs[itm.ci];
-                unsigned long long v;
-                if (j < itm.n_ex) {
-                    const size_t rows0 = (((size_t)se.seq * p.num_layers + p.layer) * p.hkv + itm.kvh) * 128;
-                    const int js = (se.n_sink + kExactRows - 1) / kExactRows;
-                    uintptr_t a;
-                    int aux;
-                    if (j < js) {
-                        a = (uintptr_t)(p.base + p.lay.sink_k + (rows0 + (size_t)j * kExactRows) * 256);
-                        aux = min(kExactRows, se.n_sink - j * kExactRows);
-                    } else {
-                        a = (uintptr_t)(p.base + p.lay.tail_k + (rows0 + (size_t)(j - js) * kExactRows) * 256);
-                        aux = min(kExactRows, se.n_tail - (j - js) * kExactRows) | 256;
-                    }
-                    v = (1ull << 62) | ((unsigned long long)aux << 48) | (unsigned long long)a;
-                } else {
-                    const uint8_t* src;
-                    if (j < itm.n_ex + itm.seal) {
-                        src = p.base + p.lay.pool + (size_t)se.seal_slot * p.slot_bytes;
-                    } else {
-                        const int32_t* table = reinterpret_cast<const int32_t*>(p.base + p.lay.block_table);
-                        int slot = table[((size_t)se.seq * p.num_layers + p.layer) * p.max_groups + itm.g0 +
-                                         (j - itm.n_ex - itm.seal)];
-                        if (slot < 0 || slot >= p.pool_slots) {
-                            atomicOr(err, kErrBadSlot);
-                            slot = 0;
-                        }
-                        src = p.base + p.lay.pool + (size_t)slot * p.slot_bytes;
-                    }
-                    src += (size_t)itm.kvh * (p.rec_k + p.rec_v);
-                    v = (2ull << 62) | (unsigned long long)(uintptr_t)src;
+    uint32_t n = 0;  // stream entries of the CTA (counted by the compute warps)
+    if (w >= kWarps) {
+        // ---- 2. the copy-issuing warpgroup. It hands registers to the compute warpgroups;
+        //      its warps issue every copy of the stream, entry n into stage n % S once the
+        //      consumer of entry n - S has released that stage, from
+        //      the moment the compute warps have written this step's tokens and seals and
+        //      resolved the stream's sources (named barrier 3).
+        asm volatile("setmaxnreg.dec.sync.aligned.u32 %0;" ::"n"(kRegsCopy));
+        asm volatile("griddepcontrol.wait;" ::: "memory");
+        named_bar(3, kDecodeThreads);
+        // copy warp k issues the entries of the stages s with s % 4 == k, in entry order
+        // (a stage's entries all come from one warp, so each waits on the stage's release
+        // of the entry before it and its phase parity is unambiguous)
+        const uint32_t k = (uint32_t)(w - kWarps);
+        const int n_ent = *sm.n_ent;
+        GroupCursor& cur = sm.cursor[k];
+        cur.init(lo);
+        __syncwarp();
+        uint32_t s = 0, round = 0;
+        for (uint32_t gn = 0; k < (uint32_t)p.stages; ++gn) {  // (a ring of fewer than 4 stages idles some)
+            if ((s & 3u) == k) {
+                const PendingCopy pc = n_ent >= 0 ? table_copy(sm, n_ent, gn) : cur.resolve(p, IL, hi, gn);
+                if (pc.kind == 0) break;
+                if (round > 0) {
+                    int ok = 1;
+                    if (lane == 0) ok = mbar_wait(sm.empty + s, (round - 1) & 1u, err);
+                    ok = __shfl_sync(0xffffffffu, ok, 0);
+                    __syncwarp();
+                    if (!ok) break;  // a consumer stopped: the error word has the timeout
                 }
-                sm.ent[e] = v;
+                issue_copy(p, sm, pc, gn, s, lane);
+            } else if (n_ent >= 0 && gn >= (uint32_t)n_ent) {
+                break;
+            }
+            if (++s == (uint32_t)p.stages) {
+                s = 0;
+                ++round;
             }
         }
-        // addresses must fit the 48-bit field (they do on current GPUs; otherwise walk)
-        const bool wide = ((uintptr_t)(p.base + p.lay.total) >> 48) != 0;
-        if (t == 0) *sm.n_ent = (fits && !wide) ? total : -1;
-    }
-    if (rotator) rotate_loaded(sm, w >> 2, w & 3, lane, qrow);
-    __syncthreads();
-    const int n_ent = *sm.n_ent;
+    } else {
+        asm volatile("setmaxnreg.inc.sync.aligned.u32 %0;" ::"n"(kRegsCompute));
+        // this grid is itself a programmatic dependent of the work before it in the stream
+        // (the previous step's merge, or the kernel that wrote q, k or v): nothing above read
+        // global memory, everything below may read that work's output
+        asm volatile("griddepcontrol.wait;" ::: "memory");
+        if (p.test_stall && b == 0) {  // a bounded wait on a word nothing sets (timeout path test)
+            if (t == 0) spin_until(sm.ctl + 6, 1, false, err);
+            named_bar(1, kComputeThreads);
+        }
+        // the CTA's first two blocks: their query tables are built by the whole CTA; the query
+        // rows are loaded first, so that their latency overlaps the block-table loads below
+        int prebuilt = 0;
+        int bci[2] = {-1, -1}, bkv[2] = {-1, -1};
+        {
+            ItemWalk wk{lo, 0};
+            Item it;
+            while (prebuilt < 2 && walk_next(p, IL, wk, hi, it)) {
+                bci[prebuilt] = it.ci;
+                bkv[prebuilt] = it.kvh;
+                ++prebuilt;
+            }
+        }
+        const bool rotator = w < 4 * prebuilt;
+        uint2 qrow = make_uint2(0u, 0u);
+        if (rotator) qrow = load_query(p, bci[w >> 2], bkv[w >> 2], w & 3, lane);
+        // ---- sources of the stream's entries, resolved once (block-table loads in parallel)
+        {
+            int total = 0;
+            if (IL.n <= kMaxItems)
+                for (int k = 0; k < IL.n; ++k) total += IL.it[k].count();
+            const bool fits = IL.n <= kMaxItems && total <= kMaxEntries;
+            if (fits) {
+                for (int e = t; e < total; e += kComputeThreads) {
+                    int k = 0, j = e;
+                    while (j >= IL.it[k].count()) j -= IL.it[k++].count();
+                    const Item& itm = IL.it[k];
+                    const SeqEntry& se = p.seqs[itm.ci];
+                    unsigned long long v;
+                    if (j < itm.n_ex) {
+                        const size_t rows0 = (((size_t)se.seq * p.num_layers + p.layer) * p.hkv + itm.kvh) * 128;
+                        const int js = (se.n_sink + kExactRows - 1) / kExactRows;
+                        uintptr_t a;
+                        int aux;
+                        if (j < js) {
+                            a = (uintptr_t)(p.base + p.lay.sink_k + (rows0 + (size_t)j * kExactRows) * 256);
+                            aux = min(kExactRows, se.n_sink - j * kExactRows);
+                        } else {
+                            a = (uintptr_t)(p.base + p.lay.tail_k + (rows0 + (size_t)(j - js) * kExactRows) * 256);
+                            aux = min(kExactRows, se.n_tail - (j - js) * kExactRows) | 256;
+                        }
+                        v = (1ull << 62) | ((unsigned long long)aux << 48) | (unsigned long long)a;
+                    } else {
+                        const uint8_t* src;
+                        if (j < itm.n_ex + itm.seal) {
+                            src = p.base + p.lay.pool + (size_t)se.seal_slot * p.slot_bytes;
+                        } else {
+                            const int32_t* table = reinterpret_cast<const int32_t*>(p.base + p.lay.block_table);
+                            int slot = table[((size_t)se.seq * p.num_layers + p.layer) * p.max_groups + itm.g0 +
+                                             (j - itm.n_ex - itm.seal)];
+                            if (slot < 0 || slot >= p.pool_slots) {
+                                atomicOr(err, kErrBadSlot);
+                                slot = 0;
+                            }
+                            src = p.base + p.lay.pool + (size_t)slot * p.slot_bytes;
+                        }
+                        src += (size_t)itm.kvh * (p.rec_k + p.rec_v);
+                        v = (2ull << 62) | (unsigned long long)(uintptr_t)src;
+                    }
+                    sm.ent[e] = v;
+                }
+            }
+            // addresses must fit the 48-bit field (they do on current GPUs; otherwise walk)
+            const bool wide = ((uintptr_t)(p.base + p.lay.total) >> 48) != 0;
+            if (t == 0) *sm.n_ent = (fits && !wide) ? total : -1;
+        }
+        if (rotator) rotate_loaded(sm, w >> 2, w & 3, lane, qrow);
+        named_bar(1, kComputeThreads);
+        const int n_ent = *sm.n_ent;
 
-    // ---- 1. seal the groups completed by this step's tokens and write the other new
-    //      tokens into the sink or the tail, before any copy reads them
-    {
+        // ---- 1. seal the groups completed by this step's tokens and write the other new
+        //      tokens into the sink or the tail, before any copy reads them
+        {
+            ItemWalk wk{lo, 0};
+            Item it;
+            while (walk_next(p, IL, wk, hi, it)) {
+                const SeqEntry& e = p.seqs[it.ci];
+                const size_t sl = (size_t)e.seq * p.num_layers + p.layer;
+                const size_t rows0 = (sl * p.hkv + it.kvh) * 128;
+                if (it.owner && e.new_pos >= 0 && e.seal_group < 0 && t < 32) {
+                    const int side = t >> 4, chunk = t & 15;
+                    const uint16_t* src = (side ? p.v_new : p.k_new) + ((size_t)it.ci * p.hkv + it.kvh) * 128;
+                    const size_t row = e.new_pos < kSink ? (size_t)e.new_pos : (size_t)((e.new_pos - kSink) % kGroup);
+                    const size_t off = (e.new_pos < kSink ? (side ? p.lay.sink_v : p.lay.sink_k)
+                                                          : (side ? p.lay.tail_v : p.lay.tail_k)) +
+                                       (rows0 + row) * 256;
+                    reinterpret_cast<uint4*>(p.base + off)[chunk] = reinterpret_cast<const uint4*>(src)[chunk];
+                }
+                if (!it.seal) continue;
+                uint8_t* dst = p.base + p.lay.pool + (size_t)e.seal_slot * p.slot_bytes + (size_t)it.kvh * pair;
+                if (t < kSealThreads) {  // the seal runs on 8 warps (barrier 2); the others wait below
+                    SealRows rk{reinterpret_cast<const uint16_t*>(p.base + p.lay.tail_k) + rows0 * 128,
+                                p.k_new + ((size_t)it.ci * p.hkv + it.kvh) * 128};
+                    seal_matrix(rk, p.k_bits, 0, p.iters, dst, nullptr, *sm.seal, 2);
+                    SealRows rv{reinterpret_cast<const uint16_t*>(p.base + p.lay.tail_v) + rows0 * 128,
+                                p.v_new + ((size_t)it.ci * p.hkv + it.kvh) * 128};
+                    seal_matrix(rv, p.v_bits, 1, p.iters, dst + p.rec_k, nullptr, *sm.seal, 2);
+                }
+                if (t == 0 && it.kvh == 0) {
+                    int32_t* table = reinterpret_cast<int32_t*>(p.base + p.lay.block_table);
+                    table[sl * p.max_groups + e.seal_group] = e.seal_slot;
+                }
+            }
+        }
+        // ---- query tables of the CTA's first two blocks (rotated above), by the whole CTA
+        for (int k = t; k < 256 * prebuilt; k += kComputeThreads) fill_table<KB>(sm, k >> 8, (k >> 5) & 7, k & 31);
+        fence_proxy_async_global();  // the rows and records just written are read by bulk copies
+        named_bar(1, kComputeThreads);
+        bar_arrive(3, kDecodeThreads);  // the copy-issuing warp may start
+
+        // ---- 3. items in order, warp by warp
+        const int g = lane >> 2, tq = lane & 3;
+        // this warp processes group numbers w, w + kWarps, ...: stage and phase parity of the next
+        uint32_t my_s = (uint32_t)w % (uint32_t)p.stages, my_par = ((uint32_t)w / (uint32_t)p.stages) & 1u;
+        float* xb = sm.xbuf + w * kXbWarp;
         ItemWalk wk{lo, 0};
         Item it;
+        uint32_t item_no = 0;
+        int kb = -1;
         while (walk_next(p, IL, wk, hi, it)) {
             const SeqEntry& e = p.seqs[it.ci];
-            const size_t sl = (size_t)e.seq * p.num_layers + p.layer;
-            const size_t rows0 = (sl * p.hkv + it.kvh) * 128;
-            if (it.owner && e.new_pos >= 0 && e.seal_group < 0 && t < 32) {
-                const int side = t >> 4, chunk = t & 15;
-                const uint16_t* src = (side ? p.v_new : p.k_new) + ((size_t)it.ci * p.hkv + it.kvh) * 128;
-                const size_t row = e.new_pos < kSink ? (size_t)e.new_pos : (size_t)((e.new_pos - kSink) % kGroup);
-                const size_t off = (e.new_pos < kSink ? (side ? p.lay.sink_v : p.lay.sink_k)
-                                                      : (side ? p.lay.tail_v : p.lay.tail_k)) +
-                                   (rows0 + row) * 256;
-                reinterpret_cast<uint4*>(p.base + off)[chunk] = reinterpret_cast<const uint4*>(src)[chunk];
+            ++kb;
+            if (kb > 0 && lane == 0) atomicAdd(sm.ctl + 4 + ((kb - 1) & 1), 1);  // leaving block kb - 1
+            acquire_table<KB>(p, sm, kb, prebuilt, it.ci, it.kvh, lane, err);
+            const float qm = sm.qmax[4 * (kb & 1) + tq];
+            const uint4* qtab = sm.qtab + kTabWords * (kb & 1);
+            int64_t first;
+            block_ctas(p, e, it.kvh, &first);
+            int pslot = (int)(b - first);
+            if (pslot >= kPartialSlots) {  // cannot happen with the host's schedule
+                if (lane == 0) atomicOr(err, kErrSpan);
+                pslot = kPartialSlots - 1;
             }
-            if (!it.seal) continue;
-            uint8_t* dst = p.base + p.lay.pool + (size_t)e.seal_slot * p.slot_bytes + (size_t)it.kvh * pair;
-            if (t < kSealThreads) {  // the seal runs on 8 warps (barrier 2); the others wait below
-                SealRows rk{reinterpret_cast<const uint16_t*>(p.base + p.lay.tail_k) + rows0 * 128,
-                            p.k_new + ((size_t)it.ci * p.hkv + it.kvh) * 128};
-                seal_matrix(rk, p.k_bits, 0, p.iters, dst, nullptr, *sm.seal, 2);
-                SealRows rv{reinterpret_cast<const uint16_t*>(p.base + p.lay.tail_v) + rows0 * 128,
-                            p.v_new + ((size_t)it.ci * p.hkv + it.kvh) * 128};
-                seal_matrix(rv, p.v_bits, 1, p.iters, dst + p.rec_k, nullptr, *sm.seal, 2);
+            WarpState st;
+            st.m = kNegInf;
+            st.l = 0.f;
+#pragma unroll
+            for (int mt = 0; mt < 8; ++mt) st.acc[mt] = make_float2(0.f, 0.f);
+            const uint32_t cnt = (uint32_t)it.count();
+            uint32_t k = (uint32_t)((w + kWarps - (int)(n % kWarps)) % kWarps);
+            if (k < (uint32_t)it.n_ex) {  // exact sub-groups come first
+                uint32_t bq[16];
+                exact_query(sm, kb & 1, g, tq, bq);
+                const int js = (e.n_sink + kExactRows - 1) / kExactRows;
+                for (; k < (uint32_t)it.n_ex; k += kWarps) {
+                    const uint32_t gn = n + k;
+                    wait_group(sm, gn, my_s, my_par, err);
+                    const int j = (int)k;
+                    const int rows = j < js ? min(kExactRows, e.n_sink - j * kExactRows)
+                                            : min(kExactRows, e.n_tail - (j - js) * kExactRows);
+                    process_exact(sm.stages + (size_t)my_s * pair, rows, bq, p.scale_log2, xb, st, g, tq, lane);
+                    __syncwarp();  // every lane is done with the stage before it is released
+                    if (lane == 0) mbar_arrive(sm.empty + my_s);
+                    my_s += kWarps;
+                    while (my_s >= (uint32_t)p.stages) {
+                        my_s -= p.stages;
+                        my_par ^= 1u;
+                    }
+                }
+                // so far the state holds exact tokens only: rotate it like the records so that
+                // the block's sealed groups accumulate onto it
+                frag_fwht128(st.acc, lane);
             }
-            if (t == 0 && it.kvh == 0) {
-                int32_t* table = reinterpret_cast<int32_t*>(p.base + p.lay.block_table);
-                table[sl * p.max_groups + e.seal_group] = e.seal_slot;
-            }
-        }
-    }
-    // ---- query tables of the CTA's first two blocks (rotated above), by the whole CTA
-    for (int k = t; k < 256 * prebuilt; k += kDecodeThreads) fill_table<KB>(sm, k >> 8, (k >> 5) & 7, k & 31);
-    fence_proxy_async_global();  // the rows and records just written are read by bulk copies
-    __syncthreads();
-
-    // ---- 2. prologue: the first S groups of the stream. Lane 0 of each warp resolves the
-    //      sources of the warp's copies; the source of its next copy is resolved one group
-    //      ahead and kept in registers, so the block-table load behind it is first waited
-    //      for when that copy is issued.
-    GroupCursor& cur = sm.cursor[w];
-    cur.init(lo);
-    __syncwarp();
-    {
-        // resolve this warp's prologue copies (at most three: gn = w, w + 12, w + 24 < 32)
-        // before issuing any, so that their block-table loads overlap
-        PendingCopy pro[3];
-#pragma unroll
-        for (int r = 0; r < 3; ++r) {
-            const uint32_t gn = (uint32_t)(w + kWarps * r);
-            pro[r].kind = 0;
-            if (gn < (uint32_t)p.stages) pro[r] = n_ent >= 0 ? table_copy(sm, n_ent, gn) : cur.resolve(p, IL, hi, gn);
-        }
-#pragma unroll
-        for (int r = 0; r < 3; ++r) {
-            const uint32_t gn = (uint32_t)(w + kWarps * r);
-            if (gn < (uint32_t)p.stages) issue_copy(p, sm, pro[r], gn, gn, lane);
-        }
-    }
-    // this warp's first copy inside the loop
-    PendingCopy pend = n_ent >= 0 ? table_copy(sm, n_ent, w + p.stages) : cur.resolve(p, IL, hi, w + p.stages);
-
-    // ---- 3. items in order, warp by warp
-    const int g = lane >> 2, tq = lane & 3;
-    // this warp processes group numbers w, w + kWarps, ...: stage and phase parity of the next
-    uint32_t my_s = (uint32_t)w % (uint32_t)p.stages, my_par = ((uint32_t)w / (uint32_t)p.stages) & 1u;
-    float* xb = sm.xbuf + w * kXbWarp;
-    ItemWalk wk{lo, 0};
-    Item it;
-    uint32_t n = 0, item_no = 0;
-    int kb = -1;
-    while (walk_next(p, IL, wk, hi, it)) {
-        const SeqEntry& e = p.seqs[it.ci];
-        ++kb;
-        if (kb > 0 && lane == 0) atomicAdd(sm.ctl + 4 + ((kb - 1) & 1), 1);  // leaving block kb - 1
-        acquire_table<KB>(p, sm, kb, prebuilt, it.ci, it.kvh, lane, err);
-        const float qm = sm.qmax[4 * (kb & 1) + tq];
-        const uint4* qtab = sm.qtab + kTabWords * (kb & 1);
-        int64_t first;
-        block_ctas(p, e, it.kvh, &first);
-        int pslot = (int)(b - first);
-        if (pslot >= kPartialSlots) {  // cannot happen with the host's schedule
-            if (lane == 0) atomicOr(err, kErrSpan);
-            pslot = kPartialSlots - 1;
-        }
-        WarpState st;
-        st.m = kNegInf;
-        st.l = 0.f;
-#pragma unroll
-        for (int mt = 0; mt < 8; ++mt) st.acc[mt] = make_float2(0.f, 0.f);
-        const uint32_t cnt = (uint32_t)it.count();
-        uint32_t k = (uint32_t)((w + kWarps - (int)(n % kWarps)) % kWarps);
-        if (k < (uint32_t)it.n_ex) {  // exact sub-groups come first
-            uint32_t bq[16];
-            exact_query(sm, kb & 1, g, tq, bq);
-            const int js = (e.n_sink + kExactRows - 1) / kExactRows;
-            for (; k < (uint32_t)it.n_ex; k += kWarps) {
+            for (; k < cnt; k += kWarps) {
                 const uint32_t gn = n + k;
                 wait_group(sm, gn, my_s, my_par, err);
-                const int j = (int)k;
-                const int rows = j < js ? min(kExactRows, e.n_sink - j * kExactRows)
-                                        : min(kExactRows, e.n_tail - (j - js) * kExactRows);
-                process_exact(sm.stages + (size_t)my_s * pair, rows, bq, p.scale_log2, xb, st, g, tq, lane);
-                __syncwarp();  // every lane is done with the stage before it is refilled
-                issue_copy(p, sm, pend, gn + p.stages, my_s, lane);
-                pend = n_ent >= 0 ? table_copy(sm, n_ent, gn + kWarps + p.stages)
-                                  : cur.resolve(p, IL, hi, gn + kWarps + p.stages);
+                process_group<KB, VB>(p, sm.stages + (size_t)my_s * pair, qtab, qm, xb, st, g, tq, lane);
+                __syncwarp();  // every lane is done with the stage before it is released
+                if (lane == 0) mbar_arrive(sm.empty + my_s);
                 my_s += kWarps;
                 while (my_s >= (uint32_t)p.stages) {
                     my_s -= p.stages;
                     my_par ^= 1u;
                 }
             }
-            // so far the state holds exact tokens only: rotate it like the records so that
-            // the block's sealed groups accumulate onto it
-            frag_fwht128(st.acc, lane);
+            n += cnt;
+            fold_item(p, sm, st, item_no, it.ci, it.kvh, pslot, w, g, tq, lane, err);
+            ++item_no;
         }
-        for (; k < cnt; k += kWarps) {
-            const uint32_t gn = n + k;
-            wait_group(sm, gn, my_s, my_par, err);
-            process_group<KB, VB>(p, sm.stages + (size_t)my_s * pair, qtab, qm, xb, st, g, tq, lane);
-            __syncwarp();  // every lane is done with the stage before it is refilled
-            issue_copy(p, sm, pend, gn + p.stages, my_s, lane);
-            pend = n_ent >= 0 ? table_copy(sm, n_ent, gn + kWarps + p.stages)
-                              : cur.resolve(p, IL, hi, gn + kWarps + p.stages);
-            my_s += kWarps;
-            while (my_s >= (uint32_t)p.stages) {
-                my_s -= p.stages;
-                my_par ^= 1u;
-            }
-        }
-        n += cnt;
-        fold_item(p, sm, st, item_no, it.ci, it.kvh, pslot, w, g, tq, lane, err);
-        ++item_no;
     }
     // Normally every copy was waited for above. After a wait that gave up, let the
     // copies still in flight land (bounded) before the CTA's shared memory goes away.
@@ -1405,7 +1436,7 @@ int decode_smem_bytes(int k_bits, int v_bits, int stages, bool with_seal) {
     size_t off = (size_t)stages * pair;
     if (off < sizeof(SealSmem)) off = sizeof(SealSmem);
     off = (off + 15) & ~(size_t)15;
-    off += 32 * 8 + 32 * 4 + 2 * kTabWords * 16 + 2 * 512 * 4 + 2 * 4 * 4 + 2 * 4 * 64 * 4 + kWarps * sizeof(WarpRegion) + 2 * sizeof(ItemCtl) + 16 * 4 + 8 * 4 + kWarps * sizeof(GroupCursor) + sizeof(ItemList) + 16 + kMaxEntries * 8 +
+    off += 2 * 32 * 8 + 32 * 4 + 2 * kTabWords * 16 + 2 * 512 * 4 + 2 * 4 * 4 + 2 * 4 * 64 * 4 + kWarps * sizeof(WarpRegion) + 2 * sizeof(ItemCtl) + 16 * 4 + 8 * 4 + 4 * sizeof(GroupCursor) + sizeof(ItemList) + 16 + kMaxEntries * 8 +
            kWarps * kXbWarp * 4;
     return (int)off;
 }

@@ -88,6 +88,11 @@ __device__ __forceinline__ void named_bar(int id, int n) {
     asm volatile("bar.sync %0, %1;" ::"r"(id), "r"(n) : "memory");
 }
 
+// Arrive at named barrier id (n threads in all) without waiting for it.
+__device__ __forceinline__ void bar_arrive(int id, int n) {
+    asm volatile("bar.arrive %0, %1;" ::"r"(id), "r"(n) : "memory");
+}
+
 __device__ __forceinline__ uint16_t f16_bits_sat(float x) {
     // round to nearest even; values beyond the largest finite half saturate
     return __half_as_ushort(__float2half_rn(fminf(x, 65504.0f)));

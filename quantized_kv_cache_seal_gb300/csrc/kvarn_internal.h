@@ -21,7 +21,7 @@ constexpr int kMaxSpan = 32;     // CTAs that may share the sealed groups of one
 constexpr int kMaxGrid = 256;    // CTAs of a decode launch (at most one per SM)
 constexpr int kPartialSlots = kMaxSpan;  // one partial per CTA covering a block
 constexpr int kPartialFloats = 528;  // [0] epoch bits, [4..8) m, [8..12) l, [12..524) acc
-constexpr int kDecodeThreads = 384;  // 12 warps
+constexpr int kDecodeThreads = 512;  // 3 compute warpgroups + 1 copy-issuing warpgroup
 constexpr int kExactRows = 16;       // tokens of an exact (sink or tail) sub-group of the decode stream
 constexpr int kSealThreads = 256;
 
