@@ -124,6 +124,25 @@ class ClockSampler:
                 "samples": len(sm)}
 
 
+def profiled_traffic(alg_bytes):
+    """DRAM bytes per decode launch from the committed ncu capture of this kernel build,
+    scaled to this launch's algorithmic bytes (the capture ran the same workload a few
+    steps earlier); None if the kernel sources changed since the capture."""
+    import hashlib
+    try:
+        with open(os.path.join(ROOT, "profiles", "decode_kernel_llama31_8b_b16_ctx32k_k2v2_traffic.json")) as fh:
+            rec = json.load(fh)
+        h = hashlib.sha256()
+        for f in rec["sources"]:
+            with open(os.path.join(ROOT, f), "rb") as fh:
+                h.update(fh.read())
+        if h.hexdigest() != rec["sources_sha256"]:
+            return None
+        return float(rec["dram_bytes_per_launch"]) * alg_bytes / float(rec["alg_bytes_per_launch"])
+    except (OSError, KeyError, ValueError):
+        return None
+
+
 def measured_hbm_peak():
     try:
         with open(os.path.join(ROOT, "MEASURED_PEAKS.json")) as fh:
@@ -339,7 +358,8 @@ def run_ours(args):
                    "reps": len(rep_ms), "rep_ms": [round(x, 4) for x in rep_ms]},
         "gpu_launches": 2 * K_,  # per step: the decode kernel and its merge kernel
         "roofline": {"bound": "hbm", "achieved": achieved, "peak": peak, "unit": "GB/s", "frac": achieved / peak,
-                     "traffic": args.traffic, "peak_kind": peak_kind, "kernel": "decode_kernel<2,2>",
+                     "traffic": args.traffic if args.traffic is not None else profiled_traffic(alg_bytes),
+                     "peak_kind": peak_kind, "kernel": "decode_kernel<2,2>",
                      "alg_bytes_per_launch": alg_bytes, "launch_us": launch_us},
         "seal_groups_per_s": seal_gps,
         "seal_share": seal_share,
