@@ -136,22 +136,26 @@ int seal_units(const kvarn_cache* c) {
 }
 
 // Greedy fill of the unit line with ranges of at most L units, each cut as late as the
-// indivisible block heads allow. begin[k] = first unit of block k (begin[nb] = total).
+// indivisible block heads allow (a cut inside a head moves back to the head's start,
+// which lies past the previous cut because L >= every head). begin[k] = first unit of
+// block k (begin[nb] = total). Stops once more than max_ranges ranges are needed.
 // Returns the number of ranges (cuts in `cuts`, from 0 to the total).
-int greedy_cuts(const std::vector<int64_t>& begin, const int32_t* head, int64_t L, std::vector<int32_t>& cuts) {
+int greedy_cuts(const std::vector<int64_t>& begin, const int32_t* head, int64_t L, int max_ranges,
+                std::vector<int32_t>& cuts) {
     const int nb = (int)begin.size() - 1;
     const int64_t U = begin[nb];
     cuts.clear();
     cuts.push_back(0);
     int64_t start = 0;
+    int k = 0;  // block holding the current cut position (cuts only move forward)
     while (start < U) {
+        if ((int)cuts.size() > max_ranges) return max_ranges + 1;
         int64_t end = start + L;
         if (end >= U) {
             end = U;
         } else {
-            // block holding unit `end`: the last k with begin[k] <= end
-            const int k = (int)(std::upper_bound(begin.begin(), begin.begin() + nb, end) - begin.begin()) - 1;
-            if (begin[k] < end && end < begin[k] + head[k]) end = begin[k];  // > start as L >= every head
+            while (begin[k + 1] <= end) ++k;
+            if (begin[k] < end && end < begin[k] + head[k]) end = begin[k];
         }
         cuts.push_back((int32_t)end);
         start = end;
@@ -159,14 +163,16 @@ int greedy_cuts(const std::vector<int64_t>& begin, const int32_t* head, int64_t 
     return (int)cuts.size() - 1;
 }
 
-// Ranges covering each block at most max_span.
+// Ranges covering each block at most max_span (one walk over blocks and cuts together).
 bool spans_ok(const std::vector<int64_t>& begin, const std::vector<int32_t>& cuts, int max_span) {
     const int nb = (int)begin.size() - 1;
+    const int n = (int)cuts.size() - 1;
+    int c = 0;  // range holding the block's first unit
     for (int k = 0; k < nb; ++k) {
-        const int64_t a = begin[k], z = begin[k + 1] - 1;
-        const int ca = (int)(std::upper_bound(cuts.begin(), cuts.end(), (int32_t)a) - cuts.begin()) - 1;
-        const int cz = (int)(std::upper_bound(cuts.begin(), cuts.end(), (int32_t)z) - cuts.begin()) - 1;
-        if (cz - ca + 1 > max_span) return false;
+        while (c + 1 < n && cuts[c + 1] <= begin[k]) ++c;
+        int z = c;  // range holding the block's last unit
+        while (z + 1 < n && cuts[z + 1] <= begin[k + 1] - 1) ++z;
+        if (z - c + 1 > max_span) return false;
     }
     return true;
 }
@@ -175,27 +181,36 @@ kvarn_status partition_units(int nb, const int32_t* units, const int32_t* head, 
                              int min_load, std::vector<int32_t>& cuts) {
     if (nb < 1 || !units || !head || max_ctas < 1 || max_span < 1 || min_load < 1) return KVARN_EINVAL;
     std::vector<int64_t> begin(nb + 1, 0);
-    int64_t lo = min_load;
+    int64_t lo = min_load, max_head = 1;
     for (int k = 0; k < nb; ++k) {
         if (units[k] < 1 || head[k] < 1 || head[k] > units[k]) return KVARN_EINVAL;
         begin[k + 1] = begin[k] + units[k];
-        lo = std::max<int64_t>(lo, head[k]);
+        max_head = std::max<int64_t>(max_head, head[k]);
     }
     const int64_t U = begin[nb];
     if (U >= (1ll << 31)) return KVARN_ECAPACITY;
+    lo = std::max(lo, max_head);
     lo = std::max<int64_t>(lo, (U + max_ctas - 1) / max_ctas);
     auto fits = [&](int64_t L) {
-        return greedy_cuts(begin, head, L, cuts) <= max_ctas && spans_ok(begin, cuts, max_span);
+        return greedy_cuts(begin, head, L, max_ctas, cuts) <= max_ctas && spans_ok(begin, cuts, max_span);
     };
+    // A bound of lo + max_head always fits the CTA count (a cut loses less than one head,
+    // so every range but the last holds more than U / max_ctas units); the span limit can
+    // ask for more, then the bound doubles until it fits (the whole line, one range, does).
+    int64_t hi = std::min(U, lo + max_head);
+    if (hi < lo) hi = lo;
+    while (!fits(hi)) {
+        if (hi >= U) return KVARN_ECAPACITY;
+        lo = hi + 1;
+        hi = std::min(U, 2 * hi);
+    }
     // smallest bound that fits, by bisection (the range count of the greedy fill only
     // falls as L grows; the span limit, when it binds, is re-checked below)
-    int64_t hi = std::max(lo, U);
-    if (!fits(hi)) return KVARN_ECAPACITY;
     while (lo < hi) {
         const int64_t mid = lo + (hi - lo) / 2;
         if (fits(mid)) hi = mid; else lo = mid + 1;
     }
-    while (!fits(lo)) ++lo;  // terminates: the bound U fits
+    while (!fits(lo)) ++lo;  // terminates: hi fitted
     return KVARN_OK;
 }
 
