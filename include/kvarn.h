@@ -31,7 +31,11 @@
  * Conventions for every call below:
  *   - Memory: the caller allocates the device memory of the cache (one block,
  *     sized by kvarn_cache_required_bytes) and every q/k/v/out buffer. No call
- *     allocates or frees device memory. Host pointers are marked "host".
+ *     allocates or frees device memory. Host pointers are marked "host". A buffer
+ *     marked "device" may also be pinned host memory that kernels reach at the same
+ *     address (cudaHostAlloc under unified addressing; on Grace systems the GPU reads
+ *     and writes it over NVLink-C2C): the kernels then move the data themselves.
+ *     kvarn_device_accessible tells which pointers qualify.
  *   - Streams: `stream` is a cudaStream_t passed as void* (NULL = legacy default
  *     stream). Calls enqueue work and return without synchronising. All calls on
  *     one cache handle must be ordered on the GPU (issue them to one stream):
@@ -228,6 +232,12 @@ kvarn_status kvarn_partition_units(int32_t n_blocks, const int32_t* units, const
 /* Read and clear the device error word of the cache (synchronises `stream`).
  * KVARN_OK, or KVARN_ETIMEOUT if a bounded wait in a kernel gave up. */
 kvarn_status kvarn_check_device_error(kvarn_cache* cache, void* stream);
+
+/* *accessible = 1 if kernels can dereference ptr as given: device or managed memory, or
+ * pinned host memory mapped at the same address (see Memory above); 0 otherwise (also
+ * for ordinary pageable host memory and unknown pointers). KVARN_ECUDA only if the
+ * CUDA runtime cannot answer. Host only; launches nothing. */
+kvarn_status kvarn_device_accessible(const void* ptr, int32_t* accessible);
 
 /* Static text for a status code. */
 const char* kvarn_status_string(kvarn_status status);

@@ -374,6 +374,18 @@ extern "C" {
 
 size_t kvarn_record_bytes(int32_t bits) { return bits_ok(bits) ? record_bytes(bits) : 0; }
 
+kvarn_status kvarn_device_accessible(const void* ptr, int32_t* accessible) {
+    if (!accessible) return KVARN_EINVAL;
+    int a = 0;
+    const int rc = pointer_device_accessible(ptr, &a);
+    if (rc) {
+        set_cuda_error(rc, "cudaPointerGetAttributes");
+        return KVARN_ECUDA;
+    }
+    *accessible = a;
+    return KVARN_OK;
+}
+
 kvarn_status kvarn_partition_units(int32_t n_blocks, const int32_t* units, const int32_t* head, int32_t max_ctas,
                                    int32_t max_span, int32_t min_load, int32_t* cuts, int32_t* n_ctas) {
     if (!cuts || !n_ctas) return KVARN_EINVAL;

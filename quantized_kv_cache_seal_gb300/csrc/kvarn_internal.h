@@ -133,6 +133,7 @@ int decode_smem_bytes(int k_bits, int v_bits, int stages, bool with_seal);
 int max_optin_smem();
 int sm_count();
 const char* cuda_error_string(int code);
+int pointer_device_accessible(const void* ptr, int* accessible);  // 0 or a cudaError_t value
 int memcpy_h2d_async(void* dst, const void* src, size_t bytes, void* stream);
 int memcpy_d2h_sync(void* dst, const void* src, size_t bytes, void* stream);
 // static split-K workspace for the allocation-free decode call (kvarn_decode.cu)

@@ -225,6 +225,20 @@ int max_optin_smem() {
 
 const char* cuda_error_string(int code) { return cudaGetErrorString((cudaError_t)code); }
 
+int pointer_device_accessible(const void* ptr, int* accessible) {
+    *accessible = 0;
+    cudaPointerAttributes a;
+    cudaError_t e = cudaPointerGetAttributes(&a, ptr);
+    if (e != cudaSuccess) {
+        cudaGetLastError();  // an unknown pointer is an answer, not a sticky error
+        return 0;
+    }
+    if (a.type == cudaMemoryTypeDevice || a.type == cudaMemoryTypeManaged) *accessible = 1;
+    // pinned host memory that kernels reach at the same address (unified addressing)
+    if (a.type == cudaMemoryTypeHost && a.devicePointer == ptr) *accessible = 1;
+    return 0;
+}
+
 int memcpy_h2d_async(void* dst, const void* src, size_t bytes, void* stream) {
     return (int)cudaMemcpyAsync(dst, src, bytes, cudaMemcpyHostToDevice, (cudaStream_t)stream);
 }

@@ -25,7 +25,7 @@ EXPORTS = [
     "kvarn_append", "kvarn_decode_attention", "kvarn_decode_attention_noalloc", "kvarn_decode_step", "kvarn_dequant_group",
     "kvarn_seq_release", "kvarn_seq_length", "kvarn_group_record", "kvarn_exact_regions",
     "kvarn_cache_stats", "kvarn_seal_groups", "kvarn_check_device_error", "kvarn_status_string",
-    "kvarn_last_error", "kvarn_partition_units",
+    "kvarn_last_error", "kvarn_partition_units", "kvarn_device_accessible",
 ]
 
 
@@ -93,6 +93,7 @@ def load(build_if_missing: bool = True):
     L.kvarn_last_error.argtypes = []
     L.kvarn_last_error.restype = ctypes.c_char_p
     L.kvarn_partition_units.argtypes = [I32, IP, IP, I32, I32, I32, IP, IP]
+    L.kvarn_device_accessible.argtypes = [P, IP]
     for name in EXPORTS:
         fn = getattr(L, name)
         if fn.restype is ctypes.c_int:  # default: status enum
@@ -236,6 +237,14 @@ def kvarn_partition_units(units, head, max_ctas: int, max_span: int, min_load: i
     _check(load().kvarn_partition_units(nb, U, H, max_ctas, max_span, min_load, cuts, ctypes.byref(n)),
            "kvarn_partition_units")
     return [int(cuts[i]) for i in range(n.value + 1)]
+
+
+def kvarn_device_accessible(ptr) -> bool:
+    """Can kernels dereference this pointer as given (device memory, or pinned host
+    memory mapped at the same address)?"""
+    a = ctypes.c_int32()
+    _check(load().kvarn_device_accessible(_ptr(ptr), ctypes.byref(a)), "kvarn_device_accessible")
+    return bool(a.value)
 
 
 def kvarn_status_string(status: int) -> str:
