@@ -35,6 +35,7 @@ sys.path.insert(0, ROOT)
 METRIC = "KVarN decode-attn tokens/s, achieved HBM GB/s (% roofline); seal groups/s"
 WORKLOAD = "llama31_8b_gqa32x8_b16_ctx32k_k2v2"
 HQ, HKV, BATCH, KB, VB, SEED = 32, 8, 16, 2, 2, 2
+FLOOR = 0  # tail floor in groups (--tail-floor; 0 = the published design)
 
 
 def c3_lengths():
@@ -46,28 +47,34 @@ def rec_bytes(b):
     return 528 + 2048 * b
 
 
+def sealed_groups(n):
+    """Body groups sealed at length n: group g seals when group g + FLOOR fills."""
+    return max(max(n - 128, 0) // 128 - FLOOR, 0)
+
+
 def step_bytes(lengths):
     """Algorithmic HBM bytes of one decode step at the given lengths (before the step):
     sealed records read + exact fp16 K/V read + q read + out written + new token written,
-    plus, for a sequence whose token completes a group, the 127 tail tokens read and the
-    new records written and read."""
+    plus, for a sequence whose step seals a group, that group's tail tokens read (127
+    and the new token, or all 128 with a tail floor) and the new records written and
+    read."""
     pair = rec_bytes(KB) + rec_bytes(VB)
     total = 0
     for n in lengths:
         n1 = n + 1
-        sealing = n >= 128 and (n - 128) % 128 == 127
-        groups = max(n1 - 128, 0) // 128 - (1 if sealing else 0)
+        sealing = sealed_groups(n1) > sealed_groups(n)
+        groups = sealed_groups(n1) - (1 if sealing else 0)
         n_sink = min(n1, 128)
-        n_tail = max(n1 - 128, 0) % 128
+        n_tail = max(n1 - 128, 0) - 128 * sealed_groups(n1)
         total += HKV * (groups * pair + (n_sink + n_tail) * 512)
         total += HQ * 256 * 2 + HKV * 512
         if sealing:
-            total += HKV * (127 * 512 + 2 * pair)
+            total += HKV * ((127 if FLOOR == 0 else 128) * 512 + 2 * pair)
     return total
 
 
 def sealing_count(lengths):
-    return sum(1 for n in lengths if n >= 128 and (n - 128) % 128 == 127)
+    return sum(1 for n in lengths if sealed_groups(n + 1) > sealed_groups(n))
 
 
 class ClockSampler:
@@ -164,6 +171,7 @@ def build_cache(torch, device, extra):
 
     lengths = c3_lengths()
     cache = KVarNCache(num_layers=1, max_seqs=BATCH, num_q_heads=HQ, num_kv_heads=HKV, k_bits=KB, v_bits=VB,
+                       tail_floor=FLOOR,
                        max_seq_len=max(lengths) + extra, device=device)
     ids = list(range(BATCH))
     chunk = 4096
@@ -419,7 +427,8 @@ def run_ours(args):
                    "reps": len(rep_ms), "rep_ms": [round(x, 4) for x in rep_ms]},
         "gpu_launches": 2 * K_,  # per step: the decode kernel and its merge kernel
         "roofline": {"bound": "hbm", "achieved": achieved, "peak": peak, "unit": "GB/s", "frac": achieved / peak,
-                     "traffic": args.traffic if args.traffic is not None else profiled_traffic(alg_bytes),
+                     "traffic": args.traffic if args.traffic is not None else
+                     (profiled_traffic(alg_bytes) if FLOOR == 0 else None),
                      "peak_kind": peak_kind, "kernel": "decode_kernel<2,2>",
                      "alg_bytes_per_launch": alg_bytes, "launch_us": launch_us},
         "seal_groups_per_s": seal_gps,
@@ -450,16 +459,21 @@ def _oracle_step_sample(cache, q_np, pairs):
     from quantized_kv_cache_seal_gb300 import kvarn as K
     for (s, h) in pairs:
         n = cache.length(0, s)
-        ng = max(n - 128, 0) // 128
-        nt = max(n - 128, 0) % 128
+        ng = sealed_groups(n)
+        nt = max(n - 128, 0) - 128 * ng
         kr = np.stack([mem[(p - base):(p - base) + nb] for p, nb in
                        (K.kvarn_group_record(cache.handle, 0, s, g, h, 0) for g in range(ng))])
         vr = np.stack([mem[(p - base):(p - base) + nb] for p, nb in
                        (K.kvarn_group_record(cache.handle, 0, s, g, h, 1) for g in range(ng))])
-        sk, sv, tk, tv = [mem[(p - base):(p - base) + HKV * 128 * 128 * 2].view(np.float16).reshape(HKV, 128, 128)
-                          for p in K.kvarn_exact_regions(cache.handle, 0, s)]
+        ring = 128 * (FLOOR + 1)  # tail ring rows; slot = (position - 128) mod ring
+        regions = K.kvarn_exact_regions(cache.handle, 0, s)
+        sk, sv = [mem[(p - base):(p - base) + HKV * 128 * 128 * 2].view(np.float16).reshape(HKV, 128, 128)
+                  for p in regions[:2]]
+        tk, tv = [mem[(p - base):(p - base) + HKV * ring * 128 * 2].view(np.float16).reshape(HKV, ring, 128)
+                  for p in regions[2:]]
+        idx = (128 * ng + np.arange(nt)) % ring
         r = HQ // HKV
-        jobs.append((q_np[s, h * r:(h + 1) * r], sk[h], sv[h], kr, vr, tk[h, :nt], tv[h, :nt]))
+        jobs.append((q_np[s, h * r:(h + 1) * r], sk[h], sv[h], kr, vr, tk[h, idx], tv[h, idx]))
     cores = os.cpu_count() or 1
 
     def one(j):
@@ -520,7 +534,7 @@ def run_reference(args):
     def setup(pair):
         s, h = pair
         src = workloads.TokenSource(SEED, s, HKV)
-        oc = oracle.OracleCache(1, KB, VB)
+        oc = oracle.OracleCache(1, KB, VB, tail_floor=FLOOR)
         k, v = src.tokens(0, lengths[s])
         oc.append(0, k[:, h:h + 1], v[:, h:h + 1])
         return oc, src
@@ -576,11 +590,18 @@ def main():
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--cpu-pairs", type=int, default=32)
     ap.add_argument("--ref-pairs", type=int, default=16)
+    ap.add_argument("--tail-floor", type=int, default=0,
+                    help="keep this many full groups exact beyond the partial one (BeeLlama: 1); "
+                         "the headline workload is the published design, 0")
     ap.add_argument("--traffic", type=float, default=None,
                     help="ncu dram bytes per launch of the decode kernel, if captured for this build")
     args = ap.parse_args()
     if args.warmup < 3:
         args.warmup = 3
+    global FLOOR, WORKLOAD
+    if args.tail_floor:
+        FLOOR = args.tail_floor
+        WORKLOAD = f"{WORKLOAD}_tail_floor{FLOOR}"
     if args.impl == "reference":
         run_reference(args)
     else:

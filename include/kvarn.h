@@ -98,6 +98,13 @@ typedef struct {
     int32_t pool_groups;    /* slots in the sealed-group pool; one slot holds one
                                (sequence, layer, group) for all KV heads, K and V */
     int32_t flags;          /* KVARN_FLAG_* */
+    int32_t tail_floor;     /* groups of recent tokens kept exact beyond the partial one:
+                               0 = the published design (the tail is the partial newest
+                               group, 0..127 tokens); F = 1..3 = a floor of F groups, as
+                               BeeLlama does with F = 1 (anbeeld.com 2.1): group g is sealed
+                               when group g + F fills, so once the body starts at least
+                               128 F recent tokens stay exact (the tail holds 128 F ..
+                               128 F + 127 of them) */
 } kvarn_config;
 
 typedef struct {
@@ -198,7 +205,8 @@ kvarn_status kvarn_group_record(const kvarn_cache* cache, int32_t layer, int32_t
                                 int32_t kv_head, int32_t which, const void** dev_ptr, size_t* bytes);
 
 /* Device addresses of the exact regions of (layer, seq): fp16 [kv_head][128][128]
- * each for the sink K/V and the tail K/V (tail slot = (position - 128) mod 128). */
+ * for the sink K/V and [kv_head][128 (tail_floor + 1)][128] for the tail K/V (a ring:
+ * tail slot = (position - 128) mod (128 (tail_floor + 1))). */
 kvarn_status kvarn_exact_regions(const kvarn_cache* cache, int32_t layer, int32_t seq_id, const void** sink_k,
                                  const void** sink_v, const void** tail_k, const void** tail_v);
 

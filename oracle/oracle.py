@@ -250,16 +250,20 @@ class OracleCache:
     Region rules (anbeeld.com, 2.1): positions 0..127 are the sink (exact fp16);
     body group g covers positions [128 + 128 g, 256 + 128 g) and is sealed when its
     last token arrives; the partial newest group (the tail) stays exact fp16.
+    With tail_floor F > 0 (the BeeLlama floor of the same section, F = 1 there) the
+    exact tail never drops below F full groups: the oldest exact group is sealed only
+    once F + 1 full groups are exact, i.e. group g seals when group g + F fills.
     K and V of each KV head are sealed as separate 128 x d matrices.
     """
 
     def __init__(self, num_kv_heads: int, k_bits: int, v_bits: int, head_dim: int = HEAD_DIM,
-                 iters: int = ITERS):
+                 iters: int = ITERS, tail_floor: int = 0):
         self.hkv = num_kv_heads
         self.kb = k_bits
         self.vb = v_bits
         self.d = head_dim
         self.iters = iters
+        self.floor = tail_floor
         self.seqs = {}
 
     def _seq(self, s):
@@ -268,15 +272,15 @@ class OracleCache:
                 "n": 0,
                 "sink_k": np.zeros((SINK, self.hkv, self.d), np.float16),
                 "sink_v": np.zeros((SINK, self.hkv, self.d), np.float16),
-                "tail_k": np.zeros((GROUP, self.hkv, self.d), np.float16),
-                "tail_v": np.zeros((GROUP, self.hkv, self.d), np.float16),
+                "tail_k": [],  # exact tail tokens in position order, each [Hkv][d]
+                "tail_v": [],
                 "krec": [],  # per group: [Hkv][record] uint8
                 "vrec": [],
             }
         return self.seqs[s]
 
     def append(self, s, k, v):
-        """Append tokens k, v [n][Hkv][d] fp16 to sequence s, sealing each filled group."""
+        """Append tokens k, v [n][Hkv][d] fp16 to sequence s, sealing each group due."""
         st = self._seq(s)
         for t in range(k.shape[0]):
             p = st["n"]
@@ -284,17 +288,24 @@ class OracleCache:
                 st["sink_k"][p] = k[t]
                 st["sink_v"][p] = v[t]
             else:
-                slot = (p - SINK) % GROUP
-                st["tail_k"][slot] = k[t]
-                st["tail_v"][slot] = v[t]
-                if slot == GROUP - 1:
-                    kr = np.stack([seal(st["tail_k"][:, h, :], self.kb, 0, self.iters)
-                                   for h in range(self.hkv)])
-                    vr = np.stack([seal(st["tail_v"][:, h, :], self.vb, 1, self.iters)
-                                   for h in range(self.hkv)])
-                    st["krec"].append(kr)
-                    st["vrec"].append(vr)
+                st["tail_k"].append(np.asarray(k[t], np.float16))
+                st["tail_v"].append(np.asarray(v[t], np.float16))
+                if len(st["tail_k"]) == GROUP * (self.floor + 1):
+                    gk = np.stack(st["tail_k"][:GROUP])  # the oldest exact group [T][Hkv][d]
+                    gv = np.stack(st["tail_v"][:GROUP])
+                    st["krec"].append(np.stack([seal(gk[:, h, :], self.kb, 0, self.iters) for h in range(self.hkv)]))
+                    st["vrec"].append(np.stack([seal(gv[:, h, :], self.vb, 1, self.iters) for h in range(self.hkv)]))
+                    del st["tail_k"][:GROUP]
+                    del st["tail_v"][:GROUP]
             st["n"] = p + 1
+
+    def tail(self, s):
+        """Exact tail tokens of sequence s, (k, v) [n_tail][Hkv][d] fp16."""
+        st = self._seq(s)
+        if not st["tail_k"]:
+            z = np.zeros((0, self.hkv, self.d), np.float16)
+            return z, z
+        return np.stack(st["tail_k"]), np.stack(st["tail_v"])
 
     def length(self, s):
         return self._seq(s)["n"]
@@ -304,7 +315,8 @@ class OracleCache:
         n = st["n"]
         n_sink = min(n, SINK)
         n_groups = len(st["krec"])
-        n_tail = max(n - SINK, 0) - GROUP * n_groups
+        n_tail = len(st["tail_k"])
+        assert n_tail == max(n - SINK, 0) - GROUP * n_groups
         return n_sink, n_groups, n_tail
 
     def attend(self, s, q, scale, kv_heads=None):
@@ -315,11 +327,12 @@ class OracleCache:
         r = hq // self.hkv
         out = np.full((hq, self.d), np.nan)
         heads = range(self.hkv) if kv_heads is None else kv_heads
+        tk, tv = self.tail(s)
         for h in heads:
             kr = np.stack([g[h] for g in st["krec"]]) if n_groups else np.zeros((0,), np.uint8)
             vr = np.stack([g[h] for g in st["vrec"]]) if n_groups else np.zeros((0,), np.uint8)
             out[h * r:(h + 1) * r] = attention(
                 q[h * r:(h + 1) * r], scale,
                 st["sink_k"][:n_sink, h], st["sink_v"][:n_sink, h], kr, vr,
-                st["tail_k"][:n_tail, h], st["tail_v"][:n_tail, h], self.kb, self.vb)
+                tk[:, h], tv[:, h], self.kb, self.vb)
         return out

@@ -13,11 +13,11 @@ from . import kvarn as K
 
 class KVarNCache:
     def __init__(self, num_layers=1, max_seqs=1, num_q_heads=32, num_kv_heads=8, k_bits=2, v_bits=2,
-                 sinkhorn_iters=16, max_seq_len=32768, pool_groups=None, device="cuda", flags=0):
+                 sinkhorn_iters=16, max_seq_len=32768, pool_groups=None, device="cuda", flags=0, tail_floor=0):
         self.cfg = K.make_config(num_layers=num_layers, max_seqs=max_seqs, num_q_heads=num_q_heads,
                                  num_kv_heads=num_kv_heads, k_bits=k_bits, v_bits=v_bits,
                                  sinkhorn_iters=sinkhorn_iters, max_seq_len=max_seq_len, pool_groups=pool_groups,
-                                 flags=flags)
+                                 flags=flags, tail_floor=tail_floor)
         self.nbytes = K.kvarn_cache_required_bytes(self.cfg)
         self.mem = torch.empty(self.nbytes + 256, dtype=torch.uint8, device=device)
         base = self.mem.data_ptr()
@@ -73,14 +73,28 @@ class KVarNCache:
         return self.mem[off:off + n].clone()
 
     def exact_regions(self, layer, seq_id):
-        """(sink_k, sink_v, tail_k, tail_v) fp16 views [Hkv][128][128]."""
+        """(sink_k, sink_v, tail_k, tail_v) fp16 views: sink [Hkv][128][128], tail ring
+        [Hkv][128 (tail_floor + 1)][128] (slot = (position - 128) mod ring rows)."""
         ptrs = K.kvarn_exact_regions(self.handle, layer, seq_id)
-        n = self.cfg.num_kv_heads * 128 * 128 * 2
+        ring = 128 * (self.cfg.tail_floor + 1)
         views = []
-        for ptr in ptrs:
+        for i, ptr in enumerate(ptrs):
+            rows = 128 if i < 2 else ring
             off = ptr - self.mem.data_ptr()
-            views.append(self.mem[off:off + n].view(torch.float16).view(self.cfg.num_kv_heads, 128, 128))
+            n = self.cfg.num_kv_heads * rows * 128 * 2
+            views.append(self.mem[off:off + n].view(torch.float16).view(self.cfg.num_kv_heads, rows, 128))
         return tuple(views)
+
+    def exact_tail(self, layer, seq_id):
+        """The exact tail tokens in position order: (tail_k, tail_v) fp16 [Hkv][n_tail][128]."""
+        n = self.length(layer, seq_id)
+        F = self.cfg.tail_floor
+        sealed = max(0, (n - 128) // 128 - F) if n > 128 else 0
+        n_tail = n - 128 - 128 * sealed if n > 128 else 0
+        ring = 128 * (F + 1)
+        _, _, tk, tv = self.exact_regions(layer, seq_id)
+        idx = (128 * sealed + torch.arange(n_tail, device=tk.device)) % ring
+        return tk[:, idx], tv[:, idx]
 
     def length(self, layer, seq_id) -> int:
         return K.kvarn_seq_length(self.handle, layer, seq_id)

@@ -144,6 +144,14 @@ struct Item {
     __device__ int count() const { return n_ex + seal + g1 - g0; }
 };
 
+// Row (in units of 128 halves, from the tail region's start) of the first token of exact
+// tail sub-group jt of block blk (sequence entry e): the tail is a ring of p.tail_cap rows
+// per block whose tokens start at slot e.tail_first; a 16-row sub-group never wraps (the
+// ring holds whole groups and the first slot is a multiple of 128).
+__device__ __forceinline__ size_t tail_row(const DecodeParams& p, const SeqEntry& e, size_t blk, int jt) {
+    return blk * (size_t)p.tail_cap + (size_t)((e.tail_first + jt * kExactRows) % p.tail_cap);
+}
+
 // Next item of this CTA's unit range [u, hi); advances u. Every block the range touches
 // is an item, even one without stream entries: it still writes a (neutral) partial.
 __device__ bool next_item(const DecodeParams& p, int64_t& u, int64_t hi, Item& it) {
@@ -842,10 +850,14 @@ __device__ void fold_item(const DecodeParams& p, const Smem& sm, const WarpState
     }
 }
 
+// Rows of the group sealed in a decode step: from the tail ring (contiguous there: the
+// group starts at a multiple of 128 rows), the last one from the step's input when the
+// step's token completes the group (no tail floor).
 struct SealRows {
-    const uint16_t* tail;  // rows 0..126
-    const uint16_t* last;  // row 127: the new token
-    __device__ const uint16_t* operator()(int i) const { return i < 127 ? tail + 128 * i : last; }
+    const uint16_t* tail;  // row 0 of the group in the tail ring
+    const uint16_t* last;  // the new token
+    int from_tail;         // rows read from the ring: 127 (then row 127 is the new token) or 128
+    __device__ const uint16_t* operator()(int i) const { return i < from_tail ? tail + 128 * i : last; }
 };
 
 // Source of a copy being resolved. For a sealed group the block-table entry is loaded
@@ -913,14 +925,14 @@ struct __align__(16) GroupCursor {
         } else {
             // exact sub-group j: sink rows 16 j .. or tail rows 16 (j - sink sub-groups) ..
             const SeqEntry& e = p.seqs[ci];
-            const size_t rows0 = (((size_t)e.seq * p.num_layers + p.layer) * p.hkv + kvh) * 128;
+            const size_t blk = ((size_t)e.seq * p.num_layers + p.layer) * p.hkv + kvh;
             const int js = (e.n_sink + kExactRows - 1) / kExactRows;
             pc.kind = 1;
             if (j < js) {
-                pc.base = p.base + p.lay.sink_k + (rows0 + (size_t)j * kExactRows) * 256;
+                pc.base = p.base + p.lay.sink_k + (blk * 128 + (size_t)j * kExactRows) * 256;
                 pc.aux = min(kExactRows, e.n_sink - j * kExactRows);
             } else {
-                pc.base = p.base + p.lay.tail_k + (rows0 + (size_t)(j - js) * kExactRows) * 256;
+                pc.base = p.base + p.lay.tail_k + tail_row(p, e, blk, j - js) * 256;
                 pc.aux = min(kExactRows, e.n_tail - (j - js) * kExactRows) | 256;
             }
         }
@@ -1164,15 +1176,15 @@ __global__ void __launch_bounds__(kDecodeThreads, 1) decode_kernel(const __grid_
                     const SeqEntry& se = p.seqs[itm.ci];
                     unsigned long long v;
                     if (j < itm.n_ex) {
-                        const size_t rows0 = (((size_t)se.seq * p.num_layers + p.layer) * p.hkv + itm.kvh) * 128;
+                        const size_t blk = ((size_t)se.seq * p.num_layers + p.layer) * p.hkv + itm.kvh;
                         const int js = (se.n_sink + kExactRows - 1) / kExactRows;
                         uintptr_t a;
                         int aux;
                         if (j < js) {
-                            a = (uintptr_t)(p.base + p.lay.sink_k + (rows0 + (size_t)j * kExactRows) * 256);
+                            a = (uintptr_t)(p.base + p.lay.sink_k + (blk * 128 + (size_t)j * kExactRows) * 256);
                             aux = min(kExactRows, se.n_sink - j * kExactRows);
                         } else {
-                            a = (uintptr_t)(p.base + p.lay.tail_k + (rows0 + (size_t)(j - js) * kExactRows) * 256);
+                            a = (uintptr_t)(p.base + p.lay.tail_k + tail_row(p, se, blk, j - js) * 256);
                             aux = min(kExactRows, se.n_tail - (j - js) * kExactRows) | 256;
                         }
                         v = (1ull << 62) | ((unsigned long long)aux << 48) | (unsigned long long)a;
@@ -1212,24 +1224,29 @@ __global__ void __launch_bounds__(kDecodeThreads, 1) decode_kernel(const __grid_
             while (walk_next(p, IL, wk, hi, it)) {
                 const SeqEntry& e = p.seqs[it.ci];
                 const size_t sl = (size_t)e.seq * p.num_layers + p.layer;
-                const size_t rows0 = (sl * p.hkv + it.kvh) * 128;
-                if (it.owner && e.new_pos >= 0 && e.seal_group < 0 && t < 32) {
+                const size_t blk = sl * p.hkv + it.kvh;
+                const size_t rows0 = blk * (size_t)p.tail_cap;  // tail ring rows of the block
+                // the new token goes to the sink or the tail ring, unless it completes the
+                // group sealed now (no tail floor): then it is that group's last row
+                const bool in_seal = e.seal_group >= 0 && p.tail_cap == kGroup;
+                if (it.owner && e.new_pos >= 0 && !in_seal && t < 32) {
                     const int side = t >> 4, chunk = t & 15;
                     const uint16_t* src = (side ? p.v_new : p.k_new) + ((size_t)it.ci * p.hkv + it.kvh) * 128;
-                    const size_t row = e.new_pos < kSink ? (size_t)e.new_pos : (size_t)((e.new_pos - kSink) % kGroup);
-                    const size_t off = (e.new_pos < kSink ? (side ? p.lay.sink_v : p.lay.sink_k)
-                                                          : (side ? p.lay.tail_v : p.lay.tail_k)) +
-                                       (rows0 + row) * 256;
+                    const size_t off = e.new_pos < kSink
+                                           ? (side ? p.lay.sink_v : p.lay.sink_k) + (blk * 128 + e.new_pos) * 256
+                                           : (side ? p.lay.tail_v : p.lay.tail_k) +
+                                                 (rows0 + (size_t)((e.new_pos - kSink) % p.tail_cap)) * 256;
                     reinterpret_cast<uint4*>(p.base + off)[chunk] = reinterpret_cast<const uint4*>(src)[chunk];
                 }
                 if (!it.seal) continue;
                 uint8_t* dst = p.base + p.lay.pool + (size_t)e.seal_slot * p.slot_bytes + (size_t)it.kvh * pair;
                 if (t < kSealThreads) {  // the seal runs on 8 warps (barrier 2); the others wait below
-                    SealRows rk{reinterpret_cast<const uint16_t*>(p.base + p.lay.tail_k) + rows0 * 128,
-                                p.k_new + ((size_t)it.ci * p.hkv + it.kvh) * 128};
+                    const int first = (kGroup * e.seal_group) % p.tail_cap, from_tail = in_seal ? 127 : 128;
+                    SealRows rk{reinterpret_cast<const uint16_t*>(p.base + p.lay.tail_k) + (rows0 + first) * 128,
+                                p.k_new + ((size_t)it.ci * p.hkv + it.kvh) * 128, from_tail};
                     seal_matrix(rk, p.k_bits, 0, p.iters, dst, nullptr, *sm.seal, 2);
-                    SealRows rv{reinterpret_cast<const uint16_t*>(p.base + p.lay.tail_v) + rows0 * 128,
-                                p.v_new + ((size_t)it.ci * p.hkv + it.kvh) * 128};
+                    SealRows rv{reinterpret_cast<const uint16_t*>(p.base + p.lay.tail_v) + (rows0 + first) * 128,
+                                p.v_new + ((size_t)it.ci * p.hkv + it.kvh) * 128, from_tail};
                     seal_matrix(rv, p.v_bits, 1, p.iters, dst + p.rec_k, nullptr, *sm.seal, 2);
                 }
                 if (t == 0 && it.kvh == 0) {

@@ -30,7 +30,9 @@ size_t align_up(size_t x, size_t a) { return (x + a - 1) / a * a; }
 
 bool bits_ok(int b) { return b == 2 || b == 4 || b == 8; }
 
-int64_t groups_sealed(int64_t n) { return n > kSink ? (n - kSink) / kGroup : 0; }
+// Body groups sealed once a sequence holds n tokens: group g seals when group g + F
+// fills (F = the tail floor in groups; 0 = the published design).
+int64_t groups_sealed(int64_t n, int F) { return n > kSink ? std::max<int64_t>(0, (n - kSink) / kGroup - F) : 0; }
 }  // namespace
 
 struct kvarn_cache {
@@ -50,6 +52,7 @@ struct kvarn_cache {
     int max_smem = 227 * 1024;
     bool host_only = false;
     bool test_stall = false;
+    int tail_cap = kGroup;  // rows of the tail ring per (sequence, layer, KV head)
 
     int64_t& L(int seq, int layer) { return len[(size_t)seq * cfg.num_layers + layer]; }
     int64_t Lc(int seq, int layer) const { return len[(size_t)seq * cfg.num_layers + layer]; }
@@ -73,13 +76,14 @@ kvarn_status check_config(const kvarn_config* c) {
     if (!bits_ok(c->k_bits) || !bits_ok(c->v_bits)) return KVARN_EINVAL;
     if (c->sinkhorn_iters < 0 || c->sinkhorn_iters > 64) return KVARN_EINVAL;
     if (c->max_seq_len <= 0 || c->pool_groups < 0) return KVARN_EINVAL;
+    if (c->tail_floor < 0 || c->tail_floor > 3) return KVARN_EINVAL;
     if ((int64_t)c->max_seqs * c->num_kv_heads > (1 << 24)) return KVARN_EINVAL;
     return KVARN_OK;
 }
 
 Layout make_layout(const kvarn_config& c, size_t* slot_bytes_out, int* max_groups_out) {
     Layout l{};
-    int max_groups = (int)std::max<int64_t>(1, groups_sealed(c.max_seq_len));
+    int max_groups = (int)std::max<int64_t>(1, groups_sealed(c.max_seq_len, c.tail_floor));
     size_t rk = record_bytes(c.k_bits), rv = record_bytes(c.v_bits);
     size_t slot_bytes = align_up((size_t)c.num_kv_heads * (rk + rv), 256);
     size_t off = 0;
@@ -91,8 +95,8 @@ Layout make_layout(const kvarn_config& c, size_t* slot_bytes_out, int* max_group
     l.block_table = take(seq_layers * max_groups * 4);
     l.sink_k = take(exact);
     l.sink_v = take(exact);
-    l.tail_k = take(exact);
-    l.tail_v = take(exact);
+    l.tail_k = take(exact * (c.tail_floor + 1));  // a ring of 128 (F + 1) rows per head
+    l.tail_v = take(exact * (c.tail_floor + 1));
     l.partials = take((size_t)c.max_seqs * c.num_kv_heads * kPartialSlots * kPartialFloats * 4);
     l.pool = take((size_t)c.pool_groups * slot_bytes);
     l.total = off;
@@ -273,7 +277,8 @@ kvarn_status run_decode(kvarn_cache* c, int32_t layer, int32_t n_seqs, const int
         for (int i = 0; i < n_seqs; ++i) {
             int64_t pos = c->Lc(seq_ids[i], layer);
             if (pos + 1 > cfg.max_seq_len) return KVARN_ECAPACITY;
-            if (pos >= kSink && (pos - kSink) % kGroup == kGroup - 1) ++need_slots;
+            if (pos >= kSink && (pos - kSink) % kGroup == kGroup - 1 && (pos - kSink) / kGroup >= cfg.tail_floor)
+                ++need_slots;
         }
         if ((size_t)need_slots > c->free_slots.size()) return KVARN_ECAPACITY;
     }
@@ -302,6 +307,7 @@ kvarn_status run_decode(kvarn_cache* c, int32_t layer, int32_t n_seqs, const int
     p.pool_slots = cfg.pool_groups;
     p.scale_log2 = scale * 1.4426950408889634f;
     p.test_stall = c->test_stall ? 1 : 0;
+    p.tail_cap = c->tail_cap;
     bool any_seal = false;
     std::vector<int32_t> taken;
     for (int i = 0; i < n_seqs; ++i) {
@@ -314,8 +320,10 @@ kvarn_status run_decode(kvarn_cache* c, int32_t layer, int32_t n_seqs, const int
         e.seal_slot = -1;
         if (step) {
             e.new_pos = (int32_t)n;
-            if (n >= kSink && (n - kSink) % kGroup == kGroup - 1) {
-                e.seal_group = (int32_t)((n - kSink) / kGroup);
+            // the token completes group (n - 128) / 128; with a tail floor of F groups
+            // the group F before it seals
+            if (n >= kSink && (n - kSink) % kGroup == kGroup - 1 && (n - kSink) / kGroup >= cfg.tail_floor) {
+                e.seal_group = (int32_t)((n - kSink) / kGroup - cfg.tail_floor);
                 e.seal_slot = c->free_slots.back();
                 c->free_slots.pop_back();
                 taken.push_back(e.seal_slot);
@@ -323,9 +331,11 @@ kvarn_status run_decode(kvarn_cache* c, int32_t layer, int32_t n_seqs, const int
             }
             n += 1;
         }
+        const int64_t sealed = groups_sealed(n, cfg.tail_floor);
         e.n_sink = (int32_t)std::min<int64_t>(n, kSink);
-        e.n_groups = (int32_t)groups_sealed(n) - (e.seal_group >= 0 ? 1 : 0);
-        e.n_tail = n > kSink ? (int32_t)((n - kSink) % kGroup) : 0;
+        e.n_groups = (int32_t)sealed - (e.seal_group >= 0 ? 1 : 0);
+        e.n_tail = n > kSink ? (int32_t)(n - kSink - kGroup * sealed) : 0;
+        e.tail_first = (int32_t)((kGroup * sealed) % c->tail_cap);
     }
     st = schedule(c, p);
     if (st) {
@@ -419,6 +429,7 @@ kvarn_status kvarn_cache_create(const kvarn_config* cfg, void* dev_mem, size_t b
     c->r = cfg->num_q_heads / cfg->num_kv_heads;
     c->rec_k = record_bytes(cfg->k_bits);
     c->rec_v = record_bytes(cfg->v_bits);
+    c->tail_cap = kGroup * (cfg->tail_floor + 1);
     c->host_only = (cfg->flags & KVARN_FLAG_HOST_ONLY) != 0;
     c->test_stall = (cfg->flags & KVARN_FLAG_TEST_STALL) != 0;
     c->len.assign((size_t)cfg->max_seqs * cfg->num_layers, 0);
@@ -452,7 +463,7 @@ kvarn_status kvarn_append(kvarn_cache* c, int32_t layer, int32_t n_seqs, const i
         int64_t n0 = c->Lc(seq_ids[i], layer), n1 = n0 + n_tokens[i];
         if (n1 > c->cfg.max_seq_len) return KVARN_ECAPACITY;
         total += n_tokens[i];
-        new_groups += groups_sealed(n1) - groups_sealed(n0);
+        new_groups += groups_sealed(n1, c->cfg.tail_floor) - groups_sealed(n0, c->cfg.tail_floor);
     }
     if (total > 0 && (!k || !v)) return KVARN_EINVAL;
     if (total >= (1ll << 31) / (c->cfg.num_kv_heads * 32)) return KVARN_ECAPACITY;
@@ -478,11 +489,12 @@ kvarn_status kvarn_append(kvarn_cache* c, int32_t layer, int32_t n_seqs, const i
     sp.rec_k = (int32_t)c->rec_k;
     sp.rec_v = (int32_t)c->rec_v;
     sp.slot_bytes = (int32_t)c->slot_bytes;
+    sp.tail_cap = ap.tail_cap = c->tail_cap;
     int64_t jobs = 0, row = 0, toks = 0;
     for (int i = 0; i < n_seqs; ++i) {
         int s = seq_ids[i];
         int64_t n0 = c->Lc(s, layer), n1 = n0 + n_tokens[i];
-        int64_t g0 = groups_sealed(n0), g1 = groups_sealed(n1);
+        int64_t g0 = groups_sealed(n0, cfg.tail_floor), g1 = groups_sealed(n1, cfg.tail_floor);
         SealJobSeq& j = sp.seqs[i];
         j.seq = s;
         j.g_first = (int32_t)g0;
@@ -576,7 +588,7 @@ kvarn_status kvarn_group_record(const kvarn_cache* c, int32_t layer, int32_t seq
                                 int32_t kv_head, int32_t which, const void** dev_ptr, size_t* bytes) {
     if (!c || layer < 0 || layer >= c->cfg.num_layers || seq_id < 0 || seq_id >= c->cfg.max_seqs) return KVARN_EINVAL;
     if (kv_head < 0 || kv_head >= c->cfg.num_kv_heads || (which != 0 && which != 1) || group < 0) return KVARN_EINVAL;
-    if (group >= groups_sealed(c->Lc(seq_id, layer))) return KVARN_ESTATE;
+    if (group >= groups_sealed(c->Lc(seq_id, layer), c->cfg.tail_floor)) return KVARN_ESTATE;
     int32_t slot = c->Tc(seq_id, layer, group);
     if (slot < 0) return KVARN_ESTATE;
     size_t off = c->lay.pool + (size_t)slot * c->slot_bytes + (size_t)kv_head * (c->rec_k + c->rec_v) +
@@ -591,10 +603,11 @@ kvarn_status kvarn_exact_regions(const kvarn_cache* c, int32_t layer, int32_t se
     if (!c || layer < 0 || layer >= c->cfg.num_layers || seq_id < 0 || seq_id >= c->cfg.max_seqs) return KVARN_EINVAL;
     size_t per = (size_t)c->cfg.num_kv_heads * kSink * kHeadDim * 2;
     size_t off = ((size_t)seq_id * c->cfg.num_layers + layer) * per;
+    size_t toff = off * (size_t)(c->cfg.tail_floor + 1);  // the tail ring is F + 1 groups long
     if (sink_k) *sink_k = c->base + c->lay.sink_k + off;
     if (sink_v) *sink_v = c->base + c->lay.sink_v + off;
-    if (tail_k) *tail_k = c->base + c->lay.tail_k + off;
-    if (tail_v) *tail_v = c->base + c->lay.tail_v + off;
+    if (tail_k) *tail_k = c->base + c->lay.tail_k + toff;
+    if (tail_v) *tail_v = c->base + c->lay.tail_v + toff;
     return KVARN_OK;
 }
 
@@ -616,7 +629,7 @@ kvarn_status kvarn_dequant_group(kvarn_cache* c, int32_t layer, int32_t seq_id, 
 kvarn_status kvarn_seq_release(kvarn_cache* c, int32_t seq_id) {
     if (!c || seq_id < 0 || seq_id >= c->cfg.max_seqs) return KVARN_EINVAL;
     for (int l = 0; l < c->cfg.num_layers; ++l) {
-        int64_t ng = groups_sealed(c->L(seq_id, l));
+        int64_t ng = groups_sealed(c->L(seq_id, l), c->cfg.tail_floor);
         for (int64_t g = 0; g < ng; ++g) {
             int32_t& s = c->T(seq_id, l, (int)g);
             if (s >= 0) c->free_slots.push_back(s);
@@ -648,7 +661,7 @@ kvarn_status kvarn_cache_stats(const kvarn_cache* c, kvarn_stats* o) {
         for (int l = 0; l < cfg.num_layers; ++l) {
             int64_t n = c->Lc(s, l);
             o->tokens_cached += n;
-            o->sealed_tokens += groups_sealed(n) * kGroup;
+            o->sealed_tokens += groups_sealed(n, cfg.tail_floor) * kGroup;
         }
     o->exact_tokens = o->tokens_cached - o->sealed_tokens;
     double elems_per_token = (double)cfg.num_kv_heads * kHeadDim;  // per side

@@ -60,6 +60,7 @@ struct SeqEntry {
     int32_t unit_begin;  // first scheduling unit of this sequence
     int32_t w_exact;     // units charged for the exact item of each (seq, kv head)
     int32_t w_seal;      // units charged for the seal item (0 if none)
+    int32_t tail_first;  // tail ring slot of the first exact tail token
 };
 
 // Parameters of the decode kernel (append + seal + attention).
@@ -78,6 +79,7 @@ struct DecodeParams {
     int32_t cta_begin[kMaxGrid + 1];  // first scheduling unit of each CTA; [grid] = units_total
     uint32_t epoch;
     int32_t test_stall;         // KVARN_FLAG_TEST_STALL: one bounded wait that runs out
+    int32_t tail_cap;           // rows of the tail ring per (sequence, layer, KV head)
     float scale_log2;           // softmax_scale * log2(e)
     SeqEntry seqs[kMaxBatch];
 };
@@ -100,6 +102,7 @@ struct SealParams {
     int32_t n_seqs, hkv, k_bits, v_bits, iters, layer, num_layers, max_groups;
     int32_t rec_k, rec_v, slot_bytes;
     int32_t jobs_total;
+    int32_t tail_cap;
     SealJobSeq seqs[kMaxBatch];
 };
 
@@ -118,6 +121,7 @@ struct AppendParams {
     const uint16_t* k_in;
     const uint16_t* v_in;
     int32_t n_seqs, hkv, layer, num_layers, tokens_total;
+    int32_t tail_cap;
     AppendSeq seqs[kMaxBatch];
 };
 

@@ -33,14 +33,15 @@ __global__ void __launch_bounds__(256) seal_groups_kernel(const uint16_t* x, int
 }
 
 struct JobRows {
-    const uint16_t* tail;  // tail rows of (seq, layer, kv head)
+    const uint16_t* tail;  // tail ring of (seq, layer, kv head)
     const uint16_t* in;    // input row of position n_before, this kv head
     int first_pos;         // position of row 0 of the group
     int n_before;
     int hkv;
+    int cap;               // rows of the tail ring
     __device__ const uint16_t* operator()(int i) const {
         int p = first_pos + i;
-        if (p < n_before) return tail + 128 * i;
+        if (p < n_before) return tail + 128 * ((p - kSink) % cap);
         return in + (size_t)(p - n_before) * hkv * 128;
     }
 };
@@ -66,9 +67,9 @@ __global__ void __launch_bounds__(256) seal_jobs_kernel(const __grid_constant__ 
     uint8_t* rec = p.base + p.lay.pool + (size_t)slot * p.slot_bytes + (size_t)kvh * (p.rec_k + p.rec_v) +
                    (side ? p.rec_k : 0);
     const uint16_t* tail = reinterpret_cast<const uint16_t*>(p.base + (side ? p.lay.tail_v : p.lay.tail_k)) +
-                           (sl * p.hkv + kvh) * 128 * 128;
+                           (sl * p.hkv + kvh) * (size_t)p.tail_cap * 128;
     const uint16_t* in = (side ? p.v_in : p.k_in) + ((size_t)e.in_row * p.hkv + kvh) * 128;
-    JobRows rows{tail, in, kSink + kGroup * g, e.n_before, p.hkv};
+    JobRows rows{tail, in, kSink + kGroup * g, e.n_before, p.hkv, p.tail_cap};
     seal_matrix(rows, side ? p.v_bits : p.k_bits, side, p.iters, rec, nullptr, S, 1);
 }
 
@@ -96,7 +97,8 @@ __global__ void append_kernel(const __grid_constant__ AppendParams p) {
         if (pos < kSink) {
             dst_off = (side ? p.lay.sink_v : p.lay.sink_k) + ((sl * p.hkv + kvh) * 128 + pos) * 256;
         } else if (pos >= e.keep_from) {
-            dst_off = (side ? p.lay.tail_v : p.lay.tail_k) + ((sl * p.hkv + kvh) * 128 + (pos - kSink) % kGroup) * 256;
+            dst_off = (side ? p.lay.tail_v : p.lay.tail_k) +
+                      ((sl * p.hkv + kvh) * (size_t)p.tail_cap + (pos - kSink) % p.tail_cap) * 256;
         } else {
             continue;  // sealed by this call
         }

@@ -41,7 +41,7 @@ class KVarNError(RuntimeError):
 class kvarn_config(ctypes.Structure):
     _fields_ = [(n, ctypes.c_int32) for n in (
         "num_layers", "max_seqs", "num_q_heads", "num_kv_heads", "head_dim", "k_bits", "v_bits",
-        "group_size", "sink_tokens", "sinkhorn_iters", "max_seq_len", "pool_groups", "flags")]
+        "group_size", "sink_tokens", "sinkhorn_iters", "max_seq_len", "pool_groups", "flags", "tail_floor")]
 
 
 class kvarn_stats(ctypes.Structure):
@@ -133,11 +133,11 @@ def _check(rc: int, where: str):
 
 def make_config(num_layers=1, max_seqs=1, num_q_heads=32, num_kv_heads=8, k_bits=2, v_bits=2,
                 sinkhorn_iters=16, max_seq_len=32768, pool_groups=None, flags=0, head_dim=128,
-                group_size=128, sink_tokens=128) -> kvarn_config:
+                group_size=128, sink_tokens=128, tail_floor=0) -> kvarn_config:
     if pool_groups is None:
-        pool_groups = max_seqs * num_layers * max(0, (max_seq_len - 128) // 128)
+        pool_groups = max_seqs * num_layers * max(0, (max_seq_len - 128) // 128 - tail_floor)
     return kvarn_config(num_layers, max_seqs, num_q_heads, num_kv_heads, head_dim, k_bits, v_bits,
-                        group_size, sink_tokens, sinkhorn_iters, max_seq_len, pool_groups, flags)
+                        group_size, sink_tokens, sinkhorn_iters, max_seq_len, pool_groups, flags, tail_floor)
 
 
 def kvarn_record_bytes(bits: int) -> int:

@@ -86,6 +86,42 @@ def test_seal_timing_and_regions_streaming():
     assert K.kvarn_seq_length(h, 1, 1) == 0  # other layer untouched
 
 
+@pytest.mark.parametrize("floor", [1, 3])
+def test_tail_floor_seal_timing_streaming_and_bulk(floor):
+    """With a tail floor of F groups (anbeeld.com 2.1, BeeLlama's F = 1) group g seals
+    when group g + F fills: decode steps and a bulk append agree, and once the body has
+    started at least 128 F recent tokens stay exact."""
+    h, cfg = host_cache(tail_floor=floor)
+    for n in range(1, 128 + 128 * (floor + 2) + 3):
+        K.kvarn_decode_step(h, 0, [1], FAKE, FAKE, FAKE, FAKE, 0.1)
+        s = K.kvarn_cache_stats(h)
+        sealed = max(max(n - 128, 0) // 128 - floor, 0)
+        assert s.pool_slots_used == sealed
+        assert s.sealed_tokens == 128 * sealed
+        assert s.exact_tokens == n - 128 * sealed
+        if n >= 128 + 128 * floor:
+            assert s.exact_tokens - 128 >= 128 * floor
+        for g in range(sealed):
+            K.kvarn_group_record(h, 0, 1, g, 0, 0)
+        with pytest.raises(K.KVarNError) as e:
+            K.kvarn_group_record(h, 0, 1, sealed, 0, 0)
+        assert e.value.status == 5
+    K.kvarn_append(h, 0, [2], [n], FAKE, FAKE)
+    assert K.kvarn_cache_stats(h).pool_slots_used == 2 * sealed
+
+
+def test_tail_floor_config_and_ring_size():
+    for bad in (-1, 4):
+        with pytest.raises(K.KVarNError) as e:
+            K.kvarn_cache_required_bytes(K.make_config(flags=K.KVARN_FLAG_HOST_ONLY, tail_floor=bad))
+        assert e.value.status == 1
+    base = K.make_config(max_seqs=2, max_seq_len=4096, pool_groups=8, flags=K.KVARN_FLAG_HOST_ONLY)
+    one = K.make_config(max_seqs=2, max_seq_len=4096, pool_groups=8, flags=K.KVARN_FLAG_HOST_ONLY, tail_floor=1)
+    # one more 128-row group of fp16 K and V per (sequence, KV head): 2 * 8 * 128 * 128 * 2 * 2 bytes
+    grow = K.kvarn_cache_required_bytes(one) - K.kvarn_cache_required_bytes(base)
+    assert 2 * 8 * 128 * 128 * 2 * 2 <= grow <= 2 * 8 * 128 * 128 * 2 * 2 + 2 * 256
+
+
 def test_bulk_append_equals_streaming_bookkeeping():
     h, _ = host_cache()
     K.kvarn_append(h, 0, [0, 2], [700, 129], FAKE, FAKE)

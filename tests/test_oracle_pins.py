@@ -367,7 +367,38 @@ def test_cache_regions_and_seal_timing():
     # sink and tail hold the input bits unchanged
     st = cache.seqs[0]
     assert np.array_equal(st["sink_k"][:, 0].view(np.uint16), k[:128, 0].view(np.uint16))
-    assert np.array_equal(st["tail_v"][:5, 0].view(np.uint16), v[384:389, 0].view(np.uint16))
+    assert np.array_equal(cache.tail(0)[1][:5, 0].view(np.uint16), v[384:389, 0].view(np.uint16))
+
+
+@pytest.mark.parametrize("floor", [1, 2])
+def test_tail_floor_seal_timing_and_records(floor):
+    """anbeeld.com 2.1 (BeeLlama): the exact tail never drops below `floor` full groups,
+    i.e. group g seals when group g + floor fills. The tail then holds exactly the input
+    tokens of the unsealed positions, and every sealed record equals the one the
+    published design (no floor) makes for the same group: a seal depends only on the
+    group's own tokens."""
+    src = workloads.TokenSource(10, 0, 1)
+    n_all = 128 + 128 * (floor + 3) + 7
+    k, v = src.tokens(0, n_all)
+    fl = oracle.OracleCache(1, 2, 2, tail_floor=floor)
+    pub = oracle.OracleCache(1, 2, 2)
+    for n in range(1, n_all + 1):
+        fl.append(0, k[n - 1:n], v[n - 1:n])
+        ns, ng, nt = fl.regions(0)
+        body = max(n - 128, 0)
+        assert ng == max(body // 128 - floor, 0)
+        assert nt == body - 128 * ng
+        if body >= 128 * floor:
+            assert nt >= 128 * floor
+        tk, tv = fl.tail(0)
+        assert np.array_equal(tk.view(np.uint16), k[128 + 128 * ng:n].view(np.uint16))
+        assert np.array_equal(tv.view(np.uint16), v[128 + 128 * ng:n].view(np.uint16))
+    pub.append(0, k, v)
+    ng = fl.regions(0)[1]
+    assert ng == (n_all - 128) // 128 - floor and ng >= 3
+    for g in range(ng):
+        assert np.array_equal(fl.seqs[0]["krec"][g], pub.seqs[0]["krec"][g])
+        assert np.array_equal(fl.seqs[0]["vrec"][g], pub.seqs[0]["vrec"][g])
 
 
 def test_streaming_append_equals_bulk_append():
