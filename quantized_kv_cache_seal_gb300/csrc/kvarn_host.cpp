@@ -124,11 +124,12 @@ kvarn_status check_ids(const kvarn_cache* c, int32_t layer, int32_t n, const int
 }
 
 // Units charged for an exact item (sink + tail tokens) relative to one sealed group
-// pair: a 16-token fp16 sub-group moves about as many bytes as a 2-bit group pair but
-// needs far less arithmetic, so it is charged as half a group.
+// pair: a 16-token fp16 sub-group moves about as many bytes as a 2-bit group pair and,
+// measured, costs a CTA about as much time (its rows are copied one by one), so it is
+// charged as one.
 int exact_units(const kvarn_cache* c, int n_sink, int n_tail) {
     (void)c;
-    return std::max(1, (exact_subs(n_sink, n_tail) + 1) / 2);
+    return std::max(1, exact_subs(n_sink, n_tail));
 }
 
 int seal_units(const kvarn_cache* c) {
