@@ -246,12 +246,115 @@ def run_ours(args):
     sampler = ClockSampler(local)
     sampler.start()
     time.sleep(0.3)
+    def run_e2e():
+        """e2e and e2e_copies (None, None with --no-e2e); run halfway through the timed
+        repetitions, so that the contexts match those of the median repetition."""
+        # end to end through the C ABI with host buffers: every step's k, v and q come from
+        # pinned host memory and its output goes back to pinned host memory, inside the
+        # timed region. Two ways, both reported: (1) the kernels read and write the pinned
+        # host buffers themselves (unified addressing; over NVLink-C2C on Grace), used as
+        # `e2e` when the library confirms the buffers are device-accessible; (2) explicit
+        # copies on a second stream, double buffered (step k + 1 goes up and step k - 1 comes
+        # down while step k runs), `e2e_copies`, and `e2e` when (1) is not available.
+        e2e, e2e_copies = None, None
+        if not args.no_e2e:
+            nk, nv, nq = kn_all[0].numel(), vn_all[0].numel(), q_all[0].numel()
+            h2d = int((nk + nv + nq) * 2)
+            d2h = int(out.numel() * 2)
+
+            def timed(run):
+                barrier()
+                e0 = torch.cuda.Event(enable_timing=True)
+                e1 = torch.cuda.Event(enable_timing=True)
+                e0.record(stream)
+                t_host = time.perf_counter()
+                run()
+                e1.record(stream)
+                t_host = time.perf_counter() - t_host
+                barrier()
+                ems = e0.elapsed_time(e1)
+                if pg is not None:
+                    t = torch.tensor([ems], dtype=torch.float64, device=device)
+                    pg.all_reduce(t, op=pg.ReduceOp.MAX)
+                    ems = float(t.item())
+                return ems, t_host
+
+            def entry(ems, path):
+                return {"value": BATCH * world * K_ / (ems / 1e3), "unit": "tokens/s", "h2d_bytes_per_step": h2d,
+                        "d2h_bytes_per_step": d2h, "path": path}
+
+            # (1) kernels on the pinned host buffers
+            hk = kn_all[cur[0]:cur[0] + K_].cpu().pin_memory()
+            hv = vn_all[cur[0]:cur[0] + K_].cpu().pin_memory()
+            hq = q_all[cur[0]:cur[0] + K_].cpu().pin_memory()
+            hout = torch.empty((K_, BATCH, HQ, 128), dtype=torch.float16).pin_memory()
+            mapped = all(K.kvarn_device_accessible(t) for t in (hk, hv, hq, hout))
+            if mapped:
+                def run_mapped():
+                    for k in range(K_):
+                        K.kvarn_decode_step(h, 0, ids, hk[k], hv[k], hq[k], hout[k], scale, sp)
+                        cur[0] += 1
+                ems, t_host = timed(run_mapped)
+                e2e = entry(ems, "kernels read and write pinned host buffers")
+                print(f"e2e mapped: host loop {t_host / K_ * 1e6:.1f} us per step, device {ems / K_ * 1e3:.1f} us per step",
+                      file=sys.stderr)
+
+            # (2) explicit copies, double buffered on a copy stream
+            hin = torch.cat([kn_all[cur[0]:cur[0] + K_].reshape(K_, -1), vn_all[cur[0]:cur[0] + K_].reshape(K_, -1),
+                             q_all[cur[0]:cur[0] + K_].reshape(K_, -1)], dim=1).cpu().pin_memory()
+            cs = torch.cuda.Stream(device=device)
+            din = [torch.empty(nk + nv + nq, dtype=torch.float16, device=device) for _ in range(2)]
+            dk = [d[:nk].view_as(kn_all[0]) for d in din]
+            dv = [d[nk:nk + nv].view_as(vn_all[0]) for d in din]
+            dq = [d[nk + nv:].view_as(q_all[0]) for d in din]
+            do = [torch.empty_like(out) for _ in range(2)]
+            up = [torch.cuda.Event() for _ in range(2)]    # inputs of the buffer set uploaded
+            done = [torch.cuda.Event() for _ in range(2)]  # step on the buffer set finished
+            down = [torch.cuda.Event() for _ in range(2)]  # output of the buffer set downloaded
+
+            def run_copies():
+                cs.wait_stream(stream)
+                for k in range(K_):
+                    b = k & 1
+                    torch.cuda.set_stream(cs)
+                    if k >= 2:
+                        cs.wait_event(done[b])
+                    din[b].copy_(hin[k], non_blocking=True)
+                    up[b].record(cs)
+                    torch.cuda.set_stream(stream)
+                    stream.wait_event(up[b])
+                    if k >= 2:
+                        stream.wait_event(down[b])
+                    K.kvarn_decode_step(h, 0, ids, dk[b], dv[b], dq[b], do[b], scale, sp)
+                    done[b].record(stream)
+                    torch.cuda.set_stream(cs)
+                    cs.wait_event(done[b])
+                    hout[k].copy_(do[b], non_blocking=True)
+                    down[b].record(cs)
+                    torch.cuda.set_stream(stream)
+                    cur[0] += 1
+                stream.wait_stream(cs)
+
+            ems, t_host = timed(run_copies)
+            e2e_copies = entry(ems, "copies on a second stream, double buffered")
+            print(f"e2e copies: host loop {t_host / K_ * 1e6:.1f} us per step, device {ems / K_ * 1e3:.1f} us per step",
+                  file=sys.stderr)
+            if e2e is None:
+                e2e = e2e_copies
+
+        return e2e, e2e_copies
+
     rep_ms, rep_bytes = [], []
     ev0 = torch.cuda.Event(enable_timing=True)
     ev1 = torch.cuda.Event(enable_timing=True)
     t_begin = time.time()
     rep = 0
+    e2e = e2e_copies = None
+    e2e_done = False
     while True:
+        if rep == reps_max // 2 and not e2e_done:
+            e2e, e2e_copies = run_e2e()
+            e2e_done = True
         start = cur[0]
         bytes_rep = sum(step_bytes(lens_at(s)) for s in range(start, start + K_))
         barrier()
@@ -267,6 +370,8 @@ def run_ours(args):
             break
     t_end = time.time()
     sampler.stop()
+    if not e2e_done:
+        e2e, e2e_copies = run_e2e()
     clocks = sampler.summary(t_begin, t_end)
     err = cache.check_device_error()
     if err != 0:
@@ -305,99 +410,6 @@ def run_ours(args):
         seal_share = max(0.0, extra / sum(per))
         seal_steps = {"sealing": len(sealing), "plain": len(plain),
                       "sealing_step_us": statistics.fmean(sealing) * 1e3, "plain_step_us": statistics.fmean(plain) * 1e3}
-
-    # end to end through the C ABI with host buffers: every step's k, v and q come from
-    # pinned host memory and its output goes back to pinned host memory, inside the
-    # timed region. Two ways, both reported: (1) the kernels read and write the pinned
-    # host buffers themselves (unified addressing; over NVLink-C2C on Grace), used as
-    # `e2e` when the library confirms the buffers are device-accessible; (2) explicit
-    # copies on a second stream, double buffered (step k + 1 goes up and step k - 1 comes
-    # down while step k runs), `e2e_copies`, and `e2e` when (1) is not available.
-    e2e, e2e_copies = None, None
-    if not args.no_e2e:
-        nk, nv, nq = kn_all[0].numel(), vn_all[0].numel(), q_all[0].numel()
-        h2d = int((nk + nv + nq) * 2)
-        d2h = int(out.numel() * 2)
-
-        def timed(run):
-            barrier()
-            e0 = torch.cuda.Event(enable_timing=True)
-            e1 = torch.cuda.Event(enable_timing=True)
-            e0.record(stream)
-            t_host = time.perf_counter()
-            run()
-            e1.record(stream)
-            t_host = time.perf_counter() - t_host
-            barrier()
-            ems = e0.elapsed_time(e1)
-            if pg is not None:
-                t = torch.tensor([ems], dtype=torch.float64, device=device)
-                pg.all_reduce(t, op=pg.ReduceOp.MAX)
-                ems = float(t.item())
-            return ems, t_host
-
-        def entry(ems, path):
-            return {"value": BATCH * world * K_ / (ems / 1e3), "unit": "tokens/s", "h2d_bytes_per_step": h2d,
-                    "d2h_bytes_per_step": d2h, "path": path}
-
-        # (1) kernels on the pinned host buffers
-        hk = kn_all[cur[0]:cur[0] + K_].cpu().pin_memory()
-        hv = vn_all[cur[0]:cur[0] + K_].cpu().pin_memory()
-        hq = q_all[cur[0]:cur[0] + K_].cpu().pin_memory()
-        hout = torch.empty((K_, BATCH, HQ, 128), dtype=torch.float16).pin_memory()
-        mapped = all(K.kvarn_device_accessible(t) for t in (hk, hv, hq, hout))
-        if mapped:
-            def run_mapped():
-                for k in range(K_):
-                    K.kvarn_decode_step(h, 0, ids, hk[k], hv[k], hq[k], hout[k], scale, sp)
-                    cur[0] += 1
-            ems, t_host = timed(run_mapped)
-            e2e = entry(ems, "kernels read and write pinned host buffers")
-            print(f"e2e mapped: host loop {t_host / K_ * 1e6:.1f} us per step, device {ems / K_ * 1e3:.1f} us per step",
-                  file=sys.stderr)
-
-        # (2) explicit copies, double buffered on a copy stream
-        hin = torch.cat([kn_all[cur[0]:cur[0] + K_].reshape(K_, -1), vn_all[cur[0]:cur[0] + K_].reshape(K_, -1),
-                         q_all[cur[0]:cur[0] + K_].reshape(K_, -1)], dim=1).cpu().pin_memory()
-        cs = torch.cuda.Stream(device=device)
-        din = [torch.empty(nk + nv + nq, dtype=torch.float16, device=device) for _ in range(2)]
-        dk = [d[:nk].view_as(kn_all[0]) for d in din]
-        dv = [d[nk:nk + nv].view_as(vn_all[0]) for d in din]
-        dq = [d[nk + nv:].view_as(q_all[0]) for d in din]
-        do = [torch.empty_like(out) for _ in range(2)]
-        up = [torch.cuda.Event() for _ in range(2)]    # inputs of the buffer set uploaded
-        done = [torch.cuda.Event() for _ in range(2)]  # step on the buffer set finished
-        down = [torch.cuda.Event() for _ in range(2)]  # output of the buffer set downloaded
-
-        def run_copies():
-            cs.wait_stream(stream)
-            for k in range(K_):
-                b = k & 1
-                torch.cuda.set_stream(cs)
-                if k >= 2:
-                    cs.wait_event(done[b])
-                din[b].copy_(hin[k], non_blocking=True)
-                up[b].record(cs)
-                torch.cuda.set_stream(stream)
-                stream.wait_event(up[b])
-                if k >= 2:
-                    stream.wait_event(down[b])
-                K.kvarn_decode_step(h, 0, ids, dk[b], dv[b], dq[b], do[b], scale, sp)
-                done[b].record(stream)
-                torch.cuda.set_stream(cs)
-                cs.wait_event(done[b])
-                hout[k].copy_(do[b], non_blocking=True)
-                down[b].record(cs)
-                torch.cuda.set_stream(stream)
-                cur[0] += 1
-            stream.wait_stream(cs)
-
-        ems, t_host = timed(run_copies)
-        e2e_copies = entry(ems, "copies on a second stream, double buffered")
-        print(f"e2e copies: host loop {t_host / K_ * 1e6:.1f} us per step, device {ems / K_ * 1e3:.1f} us per step",
-              file=sys.stderr)
-        if e2e is None:
-            e2e = e2e_copies
 
     # bulk seal throughput (kvarn_seal_groups on 16384 group matrices, 512 MiB in)
     seal_gps = None
