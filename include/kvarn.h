@@ -172,7 +172,7 @@ kvarn_status kvarn_decode_step(kvarn_cache* cache, int32_t layer, int32_t n_seqs
  * memory: a plugin inside a serving engine that owns all device memory through its own
  * pool and forbids cudaMalloc, or a process under a hard device-memory cap, still has
  * the cache's block and its q/out buffers, but cannot get a fresh allocation for the
- * split-K scratch (partial softmax states and merge tickets). This call places that scratch in a fixed
+ * split-K scratch (partial softmax states). This call places that scratch in a fixed
  * static device array of the library instead; it allocates and frees nothing.
  * The KVarN pages have no counterpart of this call; it is an interface addition.
  * Limit: max_seqs * num_kv_heads of the cache <= 128 (the array holds 128 blocks of
@@ -180,9 +180,9 @@ kvarn_status kvarn_decode_step(kvarn_cache* cache, int32_t layer, int32_t n_seqs
  * rejected with KVARN_ECAPACITY and a message in kvarn_last_error.
  * The first call on a device looks up the array's device address (cudaGetSymbolAddress,
  * with that device current); make that first call before any stream capture.
- * Every call clears the array's tickets (an async memset on `stream`) and then reuses
- * the partials left by the previous call, so calls that overlap on the GPU (other
- * streams, other caches, other threads) race: order them on one stream. */
+ * Every call reuses the partial states left by the previous call (each call tags its own
+ * with a fresh epoch), so calls that overlap on the GPU (other streams, other caches,
+ * other threads) race: order them on one stream. */
 kvarn_status kvarn_decode_attention_noalloc(kvarn_cache* cache, int32_t layer, int32_t n_seqs, const int32_t* seq_ids,
                                             const void* q, void* out, float softmax_scale, void* stream);
 

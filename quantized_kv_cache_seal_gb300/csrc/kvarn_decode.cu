@@ -1459,22 +1459,20 @@ int decode_smem_bytes(int k_bits, int v_bits, int stages, bool with_seal) {
 }
 
 // ---------------------------------------------------------------------------
-// Static split-K workspace for kvarn_decode_attention_noalloc: partial softmax states
-// and merge tickets of up to kStaticBlocks (sequence, KV head) blocks, 8.7 MB per GPU
+// Static split-K workspace for kvarn_decode_attention_noalloc: the partial softmax
+// states of up to kStaticBlocks (sequence, KV head) blocks, 8.7 MB per GPU
 // that loads the library, held until the process exits. Host code must not pass the
 // symbol itself to a kernel (in host code it names a host-side shadow): the device
 // address is fetched once per device with cudaGetSymbolAddress, with that device
 // current, on the first call made on it.
 constexpr int kStaticBlocks = 128;
 static __device__ __align__(256) float kvarn_static_partials[(size_t)kStaticBlocks * kPartialSlots * kPartialFloats];
-static __device__ __align__(256) int32_t kvarn_static_tickets[kStaticBlocks];
 
 int static_workspace_blocks() { return kStaticBlocks; }
 
-int static_workspace(void** partials, void** tickets) {
+int static_workspace(void** partials) {
     static std::mutex mu;
     static void* parts[kMaxDevices] = {};
-    static void* ticks[kMaxDevices] = {};
     int dev = 0;
     cudaError_t e = cudaGetDevice(&dev);
     if (e != cudaSuccess) return (int)e;
@@ -1482,21 +1480,12 @@ int static_workspace(void** partials, void** tickets) {
     std::lock_guard<std::mutex> lock(mu);
     if (!parts[dev]) {
         void* pp = nullptr;
-        void* tp = nullptr;
         e = cudaGetSymbolAddress(&pp, kvarn_static_partials);
         if (e != cudaSuccess) return (int)e;
-        e = cudaGetSymbolAddress(&tp, kvarn_static_tickets);
-        if (e != cudaSuccess) return (int)e;
         parts[dev] = pp;
-        ticks[dev] = tp;
     }
     *partials = parts[dev];
-    *tickets = ticks[dev];
     return 0;
-}
-
-int clear_static_tickets(void* tickets, void* stream) {
-    return (int)cudaMemsetAsync(tickets, 0, sizeof(int32_t) * kStaticBlocks, (cudaStream_t)stream);
 }
 
 int launch_decode(const DecodeParams& p, int smem, void* stream) {

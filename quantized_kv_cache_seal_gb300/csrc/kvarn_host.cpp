@@ -91,7 +91,6 @@ Layout make_layout(const kvarn_config& c, size_t* slot_bytes_out, int* max_group
     size_t seq_layers = (size_t)c.max_seqs * c.num_layers;
     size_t exact = seq_layers * c.num_kv_heads * kSink * kHeadDim * 2;
     l.err = take(16);
-    l.tickets = take((size_t)c.max_seqs * c.num_kv_heads * 4);
     l.block_table = take(seq_layers * max_groups * 4);
     l.sink_k = take(exact);
     l.sink_v = take(exact);
@@ -257,7 +256,6 @@ kvarn_status schedule(kvarn_cache* c, DecodeParams& p) {
 // Split-K workspace placed outside the cache's device block (the allocation-free call).
 struct WorkspaceOverride {
     void* partials;
-    void* tickets;
     uint32_t epoch;
 };
 
@@ -358,7 +356,6 @@ kvarn_status run_decode(kvarn_cache* c, int32_t layer, int32_t n_seqs, const int
     if (ws) {
         // offsets from the cache base that land on the static workspace (modulo 2^64)
         p.lay.partials = (size_t)((uintptr_t)ws->partials - (uintptr_t)c->base);
-        p.lay.tickets = (size_t)((uintptr_t)ws->tickets - (uintptr_t)c->base);
         p.epoch = ws->epoch;
     } else {
         p.epoch = ++c->epoch;
@@ -560,8 +557,8 @@ kvarn_status kvarn_decode_step(kvarn_cache* c, int32_t layer, int32_t n_seqs, co
 
 // Decode attention whose split-K scratch lives in the library's static device array
 // (see kvarn_decode_attention_noalloc in kvarn.h). Nothing is allocated: the array is
-// fetched per device, its tickets cleared with an async memset, and every call gets an
-// epoch of its own so that partials left by earlier calls are never merged.
+// fetched per device, and every call gets an epoch of its own so that partials left by
+// earlier calls are never merged.
 kvarn_status kvarn_decode_attention_noalloc(kvarn_cache* c, int32_t layer, int32_t n_seqs, const int32_t* seq_ids,
                                             const void* q, void* out, float softmax_scale, void* stream) {
     if (!c) return KVARN_EINVAL;
@@ -574,12 +571,10 @@ kvarn_status kvarn_decode_attention_noalloc(kvarn_cache* c, int32_t layer, int32
     }
     if (c->host_only) return KVARN_EINVAL;
     WorkspaceOverride ws{};
-    int rc = static_workspace(&ws.partials, &ws.tickets);
+    int rc = static_workspace(&ws.partials);
     if (rc) { set_cuda_error(rc, "static workspace address"); return KVARN_ECUDA; }
     kvarn_status st = check_ids(c, layer, n_seqs, seq_ids);
     if (st) return st;
-    rc = clear_static_tickets(ws.tickets, stream);
-    if (rc) { set_cuda_error(rc, "static workspace clear"); return KVARN_ECUDA; }
     static std::atomic<uint32_t> epochs{0x80000000u};
     ws.epoch = epochs.fetch_add(1) + 1;
     return run_decode(c, layer, n_seqs, seq_ids, nullptr, nullptr, q, out, softmax_scale, stream, false, &ws);

@@ -40,7 +40,6 @@ KVARN_HD inline int exact_subs(int n_sink, int n_tail) {
 // Device memory layout of one cache (byte offsets into the caller's block).
 struct Layout {
     size_t err;          // int32[4]
-    size_t tickets;      // int32[max_seqs * Hkv]
     size_t block_table;  // int32[max_seqs][num_layers][max_groups]
     size_t sink_k, sink_v, tail_k, tail_v;  // fp16[max_seqs][num_layers][Hkv][128][128]
     size_t partials;     // float[max_seqs][Hkv][kPartialSlots][kPartialFloats]
@@ -142,7 +141,6 @@ int memcpy_h2d_async(void* dst, const void* src, size_t bytes, void* stream);
 int memcpy_d2h_sync(void* dst, const void* src, size_t bytes, void* stream);
 // static split-K workspace for the allocation-free decode call (kvarn_decode.cu)
 int static_workspace_blocks();
-int static_workspace(void** partials, void** tickets);
-int clear_static_tickets(void* tickets, void* stream);
+int static_workspace(void** partials);
 
 }  // namespace kvarn

@@ -205,7 +205,7 @@ int launch_dequant(const uint8_t* rec, int bits, int which, int frame, int out_f
 
 int launch_init(uint8_t* base, const Layout& lay, void* stream) {
     cudaStream_t s = (cudaStream_t)stream;
-    cudaError_t e = cudaMemsetAsync(base + lay.err, 0, lay.block_table - lay.err, s);  // error word + tickets
+    cudaError_t e = cudaMemsetAsync(base + lay.err, 0, lay.block_table - lay.err, s);  // error word
     if (e == cudaSuccess) e = cudaMemsetAsync(base + lay.block_table, 0xff, lay.sink_k - lay.block_table, s);
     if (e == cudaSuccess) e = cudaMemsetAsync(base + lay.partials, 0, lay.pool - lay.partials, s);
     return (int)e;

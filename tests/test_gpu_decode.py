@@ -188,7 +188,7 @@ def test_decode_step_equals_append_then_attend():
                                           b.record(0, i, g, h, which).cpu().numpy())
 
 
-def test_repeated_calls_are_deterministic_and_reset_tickets():
+def test_repeated_calls_are_deterministic():
     cache = _cache(8, 2, 2, 2, 2, 2048)
     src = [workloads.TokenSource(5 + i, i, 2) for i in range(2)]
     toks = [s.tokens(0, 1500) for s in src]
