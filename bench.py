@@ -432,7 +432,7 @@ def run_ours(args):
     result = {
         "metric": METRIC, "value": value, "unit": "tokens/s", "n_gpus": world, "steps": K_, "warmup": W,
         "ms_per_step": ms_per_step, "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
-        "dtype": "f16 mma / f32 accum on 2-bit codes", "data": "synthetic",
+        "dtype": f"f16 mma / f32 accum on {KB}/{VB}-bit codes", "data": "synthetic",
         "config": {"workload": WORKLOAD, "global_batch": BATCH * world, "seq_len": int(statistics.mean(lengths)),
                    "num_q_heads": HQ, "num_kv_heads": HKV, "head_dim": 128, "k_bits": KB, "v_bits": VB,
                    "parallelism": f"replicas{world}", "l2": "working set ~315 MB per step > 129 MB L2 (no flush)",
@@ -440,8 +440,8 @@ def run_ours(args):
         "gpu_launches": 2 * K_,  # per step: the decode kernel and its merge kernel
         "roofline": {"bound": "hbm", "achieved": achieved, "peak": peak, "unit": "GB/s", "frac": achieved / peak,
                      "traffic": args.traffic if args.traffic is not None else
-                     (profiled_traffic(alg_bytes) if FLOOR == 0 else None),
-                     "peak_kind": peak_kind, "kernel": "decode_kernel<2,2>",
+                     (profiled_traffic(alg_bytes) if FLOOR == 0 and (KB, VB) == (2, 2) else None),
+                     "peak_kind": peak_kind, "kernel": f"decode_kernel<{KB},{VB}>",
                      "alg_bytes_per_launch": alg_bytes, "launch_us": launch_us},
         "seal_groups_per_s": seal_gps,
         "seal_share": seal_share,
@@ -602,6 +602,8 @@ def main():
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--cpu-pairs", type=int, default=32)
     ap.add_argument("--ref-pairs", type=int, default=16)
+    ap.add_argument("--k-bits", type=int, default=2, help="K code width (the headline workload: 2)")
+    ap.add_argument("--v-bits", type=int, default=2, help="V code width (the headline workload: 2)")
     ap.add_argument("--tail-floor", type=int, default=0,
                     help="keep this many full groups exact beyond the partial one (BeeLlama: 1); "
                          "the headline workload is the published design, 0")
@@ -610,7 +612,10 @@ def main():
     args = ap.parse_args()
     if args.warmup < 3:
         args.warmup = 3
-    global FLOOR, WORKLOAD
+    global FLOOR, WORKLOAD, KB, VB
+    if (args.k_bits, args.v_bits) != (KB, VB):
+        KB, VB = args.k_bits, args.v_bits
+        WORKLOAD = WORKLOAD.replace("_k2v2", f"_k{KB}v{VB}")
     if args.tail_floor:
         FLOOR = args.tail_floor
         WORKLOAD = f"{WORKLOAD}_tail_floor{FLOOR}"

@@ -48,7 +48,9 @@
  *     returned by kvarn_check_device_error after the stream has been synchronised.
  *   - Threads: a handle is not thread-safe; use one handle per host thread.
  *   - Sizes: head_dim, group size and sink length are 128; bits per side are
- *     2, 4 or 8; the number of query heads per KV head is 1, 2 or 4 (query head h
+ *     2, 4 or 8 in any K/V pair; 3, 5 or 6 with K and V alike (kvarn3, kvarn5, kvarn6);
+ *     or the pairs K6/V5, K5/V4, K3/V2 (anbeeld.com sections 4-6 name these widths and
+ *     presets); the number of query heads per KV head is 1, 2 or 4 (query head h
  *     reads KV head h / (num_q_heads / num_kv_heads)).
  */
 #ifndef KVARN_H
@@ -89,8 +91,8 @@ typedef struct {
     int32_t num_q_heads;    /* Hq */
     int32_t num_kv_heads;   /* Hkv; Hq / Hkv in {1, 2, 4} */
     int32_t head_dim;       /* must be 128 */
-    int32_t k_bits;         /* bits per K code: 2, 4 or 8 */
-    int32_t v_bits;         /* bits per V code: 2, 4 or 8 */
+    int32_t k_bits;         /* bits per K code: 2, 3, 4, 5, 6 or 8 (see Sizes above) */
+    int32_t v_bits;         /* bits per V code: 2, 3, 4, 5, 6 or 8 (see Sizes above) */
     int32_t group_size;     /* must be 128 (anbeeld.com 2.1) */
     int32_t sink_tokens;    /* must be 128 (anbeeld.com 2.1) */
     int32_t sinkhorn_iters; /* 16 in the method (anbeeld.com 1); 0..64 accepted */

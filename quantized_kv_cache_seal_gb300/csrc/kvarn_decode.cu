@@ -62,31 +62,46 @@ constexpr int kTabWords = 12 * 32;            // uint4 entries of one query oper
 constexpr int kMaxDevices = 64;
 #define kNegInf (-__int_as_float(0x7f800000))
 
+// A thread's 32-code chunk is taken as NVW words of CPW codes, HALF in each 16-bit half
+// at B-bit spacing from bit 0 of the half. For B = 2, 4, 8 these are the packed words
+// themselves; for the odd widths (the stream has codes straddling words) load_chunk
+// rebuilds them: 8 codes a word at 3 bits, 4 at 5 and 6 bits.
 template <int B>
 struct Codes {
-    static constexpr int CPW = 32 / B;   // codes per 32-bit word
-    static constexpr int HALF = CPW / 2; // partner code distance (low half -> high half)
-    static constexpr int NWIN = 10 / B;  // codes of a 16-bit half that fit in the f16 mantissa
+    static constexpr int CPW = B == 3 ? 8 : (B == 5 || B == 6) ? 4 : 32 / B;  // codes per word
+    static constexpr int NVW = 32 / CPW;  // words per 32-code chunk
+    static constexpr int HALF = CPW / 2;  // partner code distance (low half -> high half)
+    static constexpr int NWIN = 10 / B;   // codes of a 16-bit half that fit in the f16 mantissa
     __host__ __device__ static constexpr int sh(int x) { return (x / NWIN) * NWIN * B; }
     __host__ __device__ static constexpr int ex(int x) { return (x % NWIN) * B; }
     __host__ __device__ static constexpr uint32_t mask(int x) { return (((1u << B) - 1u) << ex(x)) * 0x10001u; }
 };
 
-// pair P (0..15) of a thread's 32-code chunk: word P / HALF, position x = P % HALF;
-// the pair holds codes x and x + HALF of that word.
-template <int B>
-__device__ __forceinline__ void unpack16(const uint32_t (&w)[B], uint32_t (&a)[16]) {
-    using C = Codes<B>;
-#pragma unroll
-    for (int P = 0; P < 16; ++P) {
-        const int word = P / C::HALF, x = P % C::HALF;
-        a[P] = (w[word] >> C::sh(x)) & C::mask(x);
-    }
+// Bits pos .. pos + width - 1 (width <= 24) of a little-endian word stream.
+template <int N>
+__device__ __forceinline__ uint32_t stream_bits(const uint32_t (&s)[N], int pos, int width) {
+    const int lo = pos / 32, sh = pos % 32;
+    uint32_t v = s[lo] >> sh;
+    if (sh + width > 32) v |= s[lo + 1] << (32 - sh);
+    return v & ((1u << width) - 1u);
 }
 
 template <int B>
-__device__ __forceinline__ void load_chunk(const uint8_t* p, uint32_t (&w)[B]) {
-    if constexpr (B == 2) {
+__device__ __forceinline__ void load_chunk(const uint8_t* p, uint32_t (&w)[Codes<B>::NVW]) {
+    using C = Codes<B>;
+    if constexpr (B == 3 || B == 5 || B == 6) {
+        // 32 codes = B packed words (4-byte aligned); word v of the result holds codes
+        // CPW v .. CPW v + CPW - 1: the first HALF in the low half, the others in the high
+        uint32_t s[B];
+#pragma unroll
+        for (int k = 0; k < B; ++k) s[k] = reinterpret_cast<const uint32_t*>(p)[k];
+        constexpr int HW = C::HALF * B;
+#pragma unroll
+        for (int v = 0; v < C::NVW; ++v) {
+            const uint32_t f = stream_bits(s, v * C::CPW * B, C::CPW * B);
+            w[v] = (f & ((1u << HW) - 1u)) | ((f >> HW) << 16);
+        }
+    } else if constexpr (B == 2) {
         uint2 v = *reinterpret_cast<const uint2*>(p);
         w[0] = v.x;
         w[1] = v.y;
@@ -117,7 +132,7 @@ __device__ __forceinline__ __half2 bits_h2(uint32_t u) { return *reinterpret_cas
 // holds that token + HALF_V, so the two scores of a thread are a V code pair.
 template <int VB>
 __device__ __forceinline__ int tok_row(int mt, int g) {
-    constexpr int CPW = 32 / VB, HALF = CPW / 2;
+    constexpr int CPW = Codes<VB>::CPW, HALF = Codes<VB>::HALF;
     return CPW * (mt * (16 / CPW) + g / HALF) + g % HALF;
 }
 
@@ -469,7 +484,7 @@ __device__ __forceinline__ float fmax3(float a, float b, float c) {
 // code words live in registers.
 template <int B>
 struct TileGroup {
-    static constexpr int TG = B == 8 ? 2 : 4;
+    static constexpr int TG = Codes<B>::NVW == 8 ? 2 : 4;
 };
 
 // One record's 128 x 128 code matrix times a B fragment (8 columns), k-step outer.
@@ -495,7 +510,7 @@ __device__ __forceinline__ void tiles_mma(const uint8_t* rows, int off1, const u
     constexpr int TG = TileGroup<B>::TG;
 #pragma unroll
     for (int t0g = 0; t0g < 8; t0g += TG) {
-        uint32_t w0[TG][B], w1[TG][B];
+        uint32_t w0[TG][C::NVW], w1[TG][C::NVW];
 #pragma unroll
         for (int i = 0; i < TG; ++i) {
             const uint8_t* r = rows + (t0g + i) * 16 * 16 * B;
@@ -1500,6 +1515,12 @@ int launch_decode(const DecodeParams& p, int smem, void* stream) {
         case 0x82: return launch_t<8, 2>(p, smem, s);
         case 0x84: return launch_t<8, 4>(p, smem, s);
         case 0x88: return launch_t<8, 8>(p, smem, s);
+        case 0x33: return launch_t<3, 3>(p, smem, s);
+        case 0x55: return launch_t<5, 5>(p, smem, s);
+        case 0x66: return launch_t<6, 6>(p, smem, s);
+        case 0x65: return launch_t<6, 5>(p, smem, s);
+        case 0x54: return launch_t<5, 4>(p, smem, s);
+        case 0x32: return launch_t<3, 2>(p, smem, s);
     }
     return (int)cudaErrorInvalidValue;
 }

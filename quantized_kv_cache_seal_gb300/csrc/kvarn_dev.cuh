@@ -125,16 +125,26 @@ constexpr float kSqMin = 8.271806125530277e-25f;   // 2^-80
 
 template <int B>
 __device__ __forceinline__ void pack64_store(const int (&q)[64], uint8_t* dst) {
-    // 64 codes of B bits, least significant first, into 2B little-endian words
-    constexpr int CPW = 32 / B;
+    // 64 codes of B bits into 2B little-endian words: code e at bits e B .. e B + B - 1
+    // of the stream, least significant first (a code may straddle two words)
     uint32_t w[2 * B];
 #pragma unroll
     for (int k = 0; k < 2 * B; ++k) w[k] = 0;
 #pragma unroll
-    for (int e = 0; e < 64; ++e) w[e / CPW] |= (uint32_t)q[e] << ((e % CPW) * B);
-    uint4* d = reinterpret_cast<uint4*>(dst);
+    for (int e = 0; e < 64; ++e) {
+        const int bit = e * B, word = bit / 32, s = bit % 32;
+        w[word] |= (uint32_t)q[e] << s;
+        if (s + B > 32) w[word + 1] |= (uint32_t)q[e] >> (32 - s);
+    }
+    if constexpr (B % 2 == 0) {  // 16-byte aligned (the stream of 64 codes starts at 8 B bytes)
+        uint4* d = reinterpret_cast<uint4*>(dst);
 #pragma unroll
-    for (int k = 0; k < B / 2; ++k) d[k] = make_uint4(w[4 * k], w[4 * k + 1], w[4 * k + 2], w[4 * k + 3]);
+        for (int k = 0; k < B / 2; ++k) d[k] = make_uint4(w[4 * k], w[4 * k + 1], w[4 * k + 2], w[4 * k + 3]);
+    } else {  // 8-byte aligned
+        uint2* d = reinterpret_cast<uint2*>(dst);
+#pragma unroll
+        for (int k = 0; k < B; ++k) d[k] = make_uint2(w[2 * k], w[2 * k + 1]);
+    }
 }
 
 // Row pointer functor: rows(i) returns a 16-byte aligned pointer to 128 fp16 values.
@@ -309,12 +319,15 @@ __device__ void seal_matrix(const Rows& rows, int bits, int which, int iters, ui
     const int row = (which == 0) ? i : j;  // token row (K) or channel row (V)
     const int half = (which == 0) ? h : hc;
     uint8_t* codes = rec + 528;
-    if (bits == 2)
-        pack64_store<2>(qv, codes + 32 * row + 16 * half);
-    else if (bits == 4)
-        pack64_store<4>(qv, codes + 64 * row + 32 * half);
-    else
-        pack64_store<8>(qv, codes + 128 * row + 64 * half);
+    uint8_t* dst = codes + 16 * bits * row + 8 * bits * half;  // 128 codes a row, 64 a half
+    switch (bits) {
+        case 2: pack64_store<2>(qv, dst); break;
+        case 3: pack64_store<3>(qv, dst); break;
+        case 4: pack64_store<4>(qv, dst); break;
+        case 5: pack64_store<5>(qv, dst); break;
+        case 6: pack64_store<6>(qv, dst); break;
+        default: pack64_store<8>(qv, dst); break;
+    }
     // 6. header: delta, m, zero, a16[128], c16[128]
     uint16_t* r16 = reinterpret_cast<uint16_t*>(rec);
     if (t == 0) {

@@ -28,7 +28,15 @@ void set_cuda_error(int code, const char* what) {
 
 size_t align_up(size_t x, size_t a) { return (x + a - 1) / a * a; }
 
-bool bits_ok(int b) { return b == 2 || b == 4 || b == 8; }
+bool bits_ok(int b) { return b == 2 || b == 3 || b == 4 || b == 5 || b == 6 || b == 8; }
+
+// K/V width pairs the decode kernel is built for: any of 2, 4, 8 with any; the odd widths
+// 3, 5, 6 symmetric; and the presets K6/V5, K5/V4, K3/V2 (anbeeld.com section 6)
+bool pair_ok(int kb, int vb) {
+    const bool even = (kb == 2 || kb == 4 || kb == 8) && (vb == 2 || vb == 4 || vb == 8);
+    const bool preset = (kb == 6 && vb == 5) || (kb == 5 && vb == 4) || (kb == 3 && vb == 2);
+    return even || preset || (kb == vb && bits_ok(kb));
+}
 
 // Body groups sealed once a sequence holds n tokens: group g seals when group g + F
 // fills (F = the tail floor in groups; 0 = the published design).
@@ -73,7 +81,7 @@ kvarn_status check_config(const kvarn_config* c) {
     if (c->num_q_heads % c->num_kv_heads) return KVARN_EINVAL;
     int r = c->num_q_heads / c->num_kv_heads;
     if (r != 1 && r != 2 && r != 4) return KVARN_EINVAL;
-    if (!bits_ok(c->k_bits) || !bits_ok(c->v_bits)) return KVARN_EINVAL;
+    if (!bits_ok(c->k_bits) || !bits_ok(c->v_bits) || !pair_ok(c->k_bits, c->v_bits)) return KVARN_EINVAL;
     if (c->sinkhorn_iters < 0 || c->sinkhorn_iters > 64) return KVARN_EINVAL;
     if (c->max_seq_len <= 0 || c->pool_groups < 0) return KVARN_EINVAL;
     if (c->tail_floor < 0 || c->tail_floor > 3) return KVARN_EINVAL;

@@ -109,9 +109,12 @@ __global__ void append_kernel(const __grid_constant__ AppendParams p) {
 
 template <int B>
 __device__ __forceinline__ int code_at(const uint8_t* codes, int e) {
+    // code e of the stream: bits e B .. e B + B - 1, least significant first
     const uint32_t* w = reinterpret_cast<const uint32_t*>(codes);
-    constexpr int CPW = 32 / B;
-    return (w[e / CPW] >> ((e % CPW) * B)) & ((1u << B) - 1);
+    const int bit = e * B, word = bit / 32, s = bit % 32;
+    uint32_t v = w[word] >> s;
+    if (s + B > 32) v |= w[word + 1] << (32 - s);
+    return (int)(v & ((1u << B) - 1));
 }
 
 __global__ void __launch_bounds__(256) dequant_kernel(const uint8_t* rec, int bits, int which, int frame, int out_fp32,
@@ -127,7 +130,15 @@ __global__ void __launch_bounds__(256) dequant_kernel(const uint8_t* rec, int bi
     for (int k = 0; k < 64; ++k) {
         const int j = 64 * h + k;
         const int e = which == 0 ? i * 128 + j : j * 128 + i;
-        int q = bits == 2 ? code_at<2>(codes, e) : bits == 4 ? code_at<4>(codes, e) : code_at<8>(codes, e);
+        int q;
+        switch (bits) {
+            case 2: q = code_at<2>(codes, e); break;
+            case 3: q = code_at<3>(codes, e); break;
+            case 4: q = code_at<4>(codes, e); break;
+            case 5: q = code_at<5>(codes, e); break;
+            case 6: q = code_at<6>(codes, e); break;
+            default: q = code_at<8>(codes, e); break;
+        }
         x[k] = ai * half_bits_to_float(r16[8 + 128 + j]) * fmaf(delta, (float)q, m);
     }
     if (frame == 0) {

@@ -40,13 +40,29 @@ def host_cache(**kw):
 def test_status_strings_and_record_sizes():
     assert K.kvarn_status_string(0) == "ok"
     assert K.kvarn_status_string(3) == "capacity exceeded"
-    for b in (2, 4, 8):
+    for b in (2, 3, 4, 5, 6, 8):
         assert K.kvarn_record_bytes(b) == 528 + 2048 * b
-    assert K.kvarn_record_bytes(3) == 0 and K.kvarn_record_bytes(16) == 0
+    for b in (0, 1, 7, 9, 16):
+        assert K.kvarn_record_bytes(b) == 0
+
+
+@pytest.mark.parametrize("kb,vb,ok", [(3, 3, True), (5, 5, True), (6, 6, True), (2, 8, True), (8, 4, True),
+                                      (6, 5, True), (5, 4, True), (3, 2, True),
+                                      (2, 3, False), (5, 6, False), (4, 6, False), (7, 7, False), (3, 4, False)])
+def test_width_pairs(kb, vb, ok):
+    """K/V widths: 2, 4 and 8 in any pair; 3, 5 and 6 symmetric; the presets K6/V5,
+    K5/V4 and K3/V2 (anbeeld.com section 6)."""
+    cfg = K.make_config(k_bits=kb, v_bits=vb, flags=K.KVARN_FLAG_HOST_ONLY)
+    if ok:
+        assert K.kvarn_cache_required_bytes(cfg) > 0
+    else:
+        with pytest.raises(K.KVarNError) as e:
+            K.kvarn_cache_required_bytes(cfg)
+        assert e.value.status == 1
 
 
 @pytest.mark.parametrize("field,value", [("head_dim", 64), ("group_size", 64), ("sink_tokens", 0),
-                                         ("k_bits", 3), ("v_bits", 1), ("num_q_heads", 24),
+                                         ("k_bits", 7), ("v_bits", 1), ("num_q_heads", 24),
                                          ("sinkhorn_iters", -1), ("max_seq_len", 0)])
 def test_bad_config_rejected(field, value):
     cfg = K.make_config(flags=K.KVARN_FLAG_HOST_ONLY)

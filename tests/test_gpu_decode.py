@@ -89,7 +89,8 @@ def test_c1_single_head_293_tokens():
 LENGTHS = [0, 1, 127, 128, 129, 255, 256, 300, 1000, 1535]
 
 
-@pytest.mark.parametrize("kb,vb", [(2, 2), (4, 2), (2, 4), (4, 4), (8, 8), (8, 2)])
+@pytest.mark.parametrize("kb,vb", [(2, 2), (4, 2), (2, 4), (4, 4), (8, 8), (8, 2), (3, 3), (5, 5), (6, 6), (6, 5),
+                                   (5, 4), (3, 2)])
 def test_mixed_lengths(kb, vb):
     """Sink only, group boundaries, several groups, ragged tails; r = 4."""
     hq, hkv = 8, 2

@@ -21,7 +21,7 @@ def _seal_gpu(x_np, bits, which, iters=16):
     return rec.cpu().numpy(), sc.cpu().numpy()
 
 
-@pytest.mark.parametrize("bits", [2, 4, 8])
+@pytest.mark.parametrize("bits", [2, 3, 4, 5, 6, 8])
 @pytest.mark.parametrize("which", [0, 1])
 def test_seal_parity(bits, which):
     xs = np.concatenate([workloads.group_matrices(100 + bits, 24),
@@ -69,10 +69,14 @@ def test_seal_degenerate_matrices():
             assert not rec[0][528:].any()
 
 
-@pytest.mark.parametrize("bits,which,frame", [(2, 0, 0), (2, 1, 1), (4, 0, 1), (4, 1, 0), (8, 0, 0), (8, 1, 1)])
+@pytest.mark.parametrize("bits,which,frame", [(2, 0, 0), (2, 1, 1), (4, 0, 1), (4, 1, 0), (8, 0, 0), (8, 1, 1),
+                                                (3, 0, 0), (3, 1, 1), (5, 0, 1), (6, 1, 0)])
 def test_dequant_group_parity(bits, which, frame):
     from quantized_kv_cache_seal_gb300.cache import KVarNCache
-    kb, vb = (bits, 2) if which == 0 else (2, bits)
+    if bits in (3, 5, 6):  # odd widths come in symmetric pairs
+        kb = vb = bits
+    else:
+        kb, vb = (bits, 2) if which == 0 else (2, bits)
     cache = KVarNCache(num_layers=1, max_seqs=1, num_q_heads=4, num_kv_heads=2, k_bits=kb, v_bits=vb,
                        max_seq_len=1024)
     src = workloads.TokenSource(31, 0, 2)
