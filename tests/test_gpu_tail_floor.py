@@ -28,9 +28,9 @@ SCALE = 1.0 / math.sqrt(128)
 HQ, HKV = 8, 2
 
 
-def _cache(floor, max_len=2048, seqs=2):
+def _cache(floor, max_len=2048, seqs=2, bits=2):
     from quantized_kv_cache_seal_gb300.cache import KVarNCache
-    return KVarNCache(num_layers=1, max_seqs=seqs, num_q_heads=HQ, num_kv_heads=HKV, k_bits=2, v_bits=2,
+    return KVarNCache(num_layers=1, max_seqs=seqs, num_q_heads=HQ, num_kv_heads=HKV, k_bits=bits, v_bits=bits,
                       max_seq_len=max_len, tail_floor=floor)
 
 
@@ -40,7 +40,7 @@ def _records(cache, seq, kvh, which, n_groups):
     return np.stack([cache.record(0, seq, g, kvh, which).cpu().numpy() for g in range(n_groups)])
 
 
-def _check_attention(cache, floor, seq, q, out, label):
+def _check_attention(cache, floor, seq, q, out, label, bits=2):
     n = cache.length(0, seq)
     n_sink = min(n, 128)
     n_groups = max(max(n - 128, 0) // 128 - floor, 0)
@@ -51,7 +51,7 @@ def _check_attention(cache, floor, seq, q, out, label):
     for h in range(HKV):
         ref = oracle.attention(q[h * r:(h + 1) * r], SCALE, sk[h, :n_sink], sv[h, :n_sink],
                                _records(cache, seq, h, 0, n_groups), _records(cache, seq, h, 1, n_groups),
-                               tk[h], tv[h], 2, 2)
+                               tk[h], tv[h], bits, bits)
         parity.check_attention(out[h * r:(h + 1) * r], ref, f"{label} seq {seq} kvh {h}")
 
 
@@ -60,10 +60,10 @@ def _tokens(seed, seq, start, count):
     return k.contiguous(), v.contiguous()
 
 
-@pytest.mark.parametrize("floor", [1, 2])
-def test_tail_floor_decode_parity(floor):
-    seed = 20 + floor
-    cache = _cache(floor)
+@pytest.mark.parametrize("floor,bits", [(1, 2), (2, 2), (1, 3)])
+def test_tail_floor_decode_parity(floor, bits):
+    seed = 20 + floor + 10 * bits
+    cache = _cache(floor, bits=bits)
     # seq 0: the body has started and sealed; seq 1: still inside the floor (nothing sealed)
     lengths = [128 + 128 * (floor + 2) + 120, 128 + 128 * floor - 3]
     for s, n in enumerate(lengths):
@@ -84,7 +84,7 @@ def test_tail_floor_decode_parity(floor):
             o = out.float().cpu().numpy()
             q = qs[step].cpu().numpy()
             for s in range(2):
-                _check_attention(cache, floor, s, q[s], o[s], f"floor {floor} step {step}")
+                _check_attention(cache, floor, s, q[s], o[s], f"floor {floor} b{bits} step {step}", bits)
     # the exact tail is the input, bit for bit, in position order
     for s in range(2):
         n = cache.length(0, s)
@@ -103,7 +103,7 @@ def test_tail_floor_decode_parity(floor):
     for h in range(HKV):
         for which, x in ((0, k), (1, v)):
             rec = cache.record(0, 0, 2, h, which).cpu().numpy()
-            parity.check_seal(x[:, h].cpu().numpy(), rec, 2, which, label=f"floor {floor} seal kvh {h} side {which}")
+            parity.check_seal(x[:, h].cpu().numpy(), rec, bits, which, label=f"floor {floor} seal kvh {h} side {which}")
 
 
 def test_tail_floor_bulk_seals_match_published_records():
