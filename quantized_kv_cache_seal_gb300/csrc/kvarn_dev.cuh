@@ -150,6 +150,15 @@ __device__ __forceinline__ void pack64_store(const int (&q)[64], uint8_t* dst) {
 // Row pointer functor: rows(i) returns a 16-byte aligned pointer to 128 fp16 values.
 // which: 0 = K (token-major codes), 1 = V (channel-major codes).
 // bar_id: named barrier used among the 256 participating threads (threads 0..255).
+// Hardware reciprocal (rcp.approx.ftz.f32, within an ulp or so): the Sinkhorn
+// iteration corrects its own rounding, and the squared scales stay inside
+// [kSqMin, kSqMax] (no denormals to flush).
+__device__ __forceinline__ float fast_rcp(float x) {
+    float r;
+    asm("rcp.approx.ftz.f32 %0, %1;" : "=f"(r) : "f"(x));
+    return r;
+}
+
 template <class Rows>
 __device__ void seal_matrix(const Rows& rows, int bits, int which, int iters, uint8_t* rec, float* dbg,
                             SealSmem& S, int bar_id) {
@@ -209,41 +218,44 @@ __device__ void seal_matrix(const Rows& rows, int bits, int which, int iters, ui
     //    then c_j^2 = mean_i A_ij / a_i^2 (equal to rescaling the rows and columns of
     //    Y in turn; a zero row or column keeps the factor 1).
     float a2 = 1.0f, c2 = 1.0f;
-    // (four partial sums per pass keep the FMA chains short; __frcp_rn is the correctly
-    // rounded reciprocal, the same value as 1.0f / x)
+    // (eight partial sums per pass keep the FMA chains short; the reciprocals are the
+    // hardware approximation, fast_rcp)
     for (int it = 0; it < iters; ++it) {
-        float p0 = 0.f, p1 = 0.f, p2 = 0.f, p3 = 0.f;
+        float pp[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
         const float4* up = reinterpret_cast<const float4*>(S.u + 68 * h);
 #pragma unroll
         for (int q = 0; q < 16; ++q) {
             float4 uu = up[q];
-            p0 = fmaf(arow[4 * q], uu.x, p0);
-            p1 = fmaf(arow[4 * q + 1], uu.y, p1);
-            p2 = fmaf(arow[4 * q + 2], uu.z, p2);
-            p3 = fmaf(arow[4 * q + 3], uu.w, p3);
+            const int o = 4 * (q & 1);
+            pp[o] = fmaf(arow[4 * q], uu.x, pp[o]);
+            pp[o + 1] = fmaf(arow[4 * q + 1], uu.y, pp[o + 1]);
+            pp[o + 2] = fmaf(arow[4 * q + 2], uu.z, pp[o + 2]);
+            pp[o + 3] = fmaf(arow[4 * q + 3], uu.w, pp[o + 3]);
         }
-        float p = (p0 + p2) + (p1 + p3);
+        float p = ((pp[0] + pp[4]) + (pp[2] + pp[6])) + ((pp[1] + pp[5]) + (pp[3] + pp[7]));
         p += __shfl_xor_sync(0xffffffffu, p, 1);
         a2 = p * (1.0f / 128.0f);
         // zero row keeps factor 1; the clamp only binds on divergent inputs (see kSqMax)
         a2 = a2 == 0.0f ? 1.0f : fminf(fmaxf(a2, kSqMin), kSqMax);
-        if (h == 0) S.v[ypad(i)] = __frcp_rn(a2);
+        if (h == 0) S.v[ypad(i)] = fast_rcp(a2);
         named_bar(bar_id, 256);
-        p0 = p1 = p2 = p3 = 0.f;
+#pragma unroll
+        for (int k = 0; k < 8; ++k) pp[k] = 0.f;
         const float4* vp = reinterpret_cast<const float4*>(S.v + 68 * hc);
 #pragma unroll
         for (int q = 0; q < 16; ++q) {
             float4 vv = vp[q];
-            p0 = fmaf(acol[4 * q], vv.x, p0);
-            p1 = fmaf(acol[4 * q + 1], vv.y, p1);
-            p2 = fmaf(acol[4 * q + 2], vv.z, p2);
-            p3 = fmaf(acol[4 * q + 3], vv.w, p3);
+            const int o = 4 * (q & 1);
+            pp[o] = fmaf(acol[4 * q], vv.x, pp[o]);
+            pp[o + 1] = fmaf(acol[4 * q + 1], vv.y, pp[o + 1]);
+            pp[o + 2] = fmaf(acol[4 * q + 2], vv.z, pp[o + 2]);
+            pp[o + 3] = fmaf(acol[4 * q + 3], vv.w, pp[o + 3]);
         }
-        p = (p0 + p2) + (p1 + p3);
+        p = ((pp[0] + pp[4]) + (pp[2] + pp[6])) + ((pp[1] + pp[5]) + (pp[3] + pp[7]));
         p += __shfl_xor_sync(0xffffffffu, p, 1);
         c2 = p * (1.0f / 128.0f);
         c2 = c2 == 0.0f ? 1.0f : fminf(fmaxf(c2, kSqMin), kSqMax);
-        if (hc == 0) S.u[ypad(j)] = __frcp_rn(c2);
+        if (hc == 0) S.u[ypad(j)] = fast_rcp(c2);
         named_bar(bar_id, 256);
     }
     // 3. stored scales: fp16, round to nearest even, saturating
