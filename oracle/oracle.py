@@ -32,7 +32,7 @@ ITERS = 16
 __all__ = [
     "build", "lib", "half_to_double", "double_to_half", "hadamard", "rotate", "sinkhorn",
     "record_bytes", "header_bytes", "pack", "unpack", "seal", "codes_for_grid", "read_header", "quantize",
-    "dequant", "attention", "OracleCache", "bits_per_element", "GROUP", "SINK", "ITERS",
+    "dequant", "attention", "prefill_attention", "OracleCache", "bits_per_element", "GROUP", "SINK", "ITERS",
 ]
 
 
@@ -239,6 +239,43 @@ def attention(q_half, scale, sink_k, sink_v, k_records, v_records, tail_k, tail_
     return (out, lse) if return_lse else out
 
 
+def prefill_attention(q_half, positions, scale, sink_k, sink_v, k_records, v_records, tail_k, tail_v,
+                      k_bits, v_bits, T: int = GROUP):
+    """Many-query (prefill) attention for one (sequence, KV head), by its plain definition.
+
+    q_half: [n_q][r][d] fp16, the queries of the tokens at `positions` (ints). The keys
+    are the cache as it stands: sink tokens at positions 0 .. n_sink - 1, sealed group g
+    at positions 128 + T g .. 128 + T g + T - 1 (its record dequantised and rotated back,
+    anbeeld.com "KVarN KV Cache: Implementation and Benchmarks", 2.1 and section 1), then
+    the exact tail. The query at position P attends to the keys at positions <= P
+    (causal), with a plain fp64 softmax. Returns [n_q][r][d] fp64.
+    """
+    q = np.asarray(q_half, np.float16).astype(np.float64)
+    n_q, r, d = q.shape
+    kr = np.asarray(k_records, np.uint8).reshape(-1, record_bytes(k_bits, T, d)) if np.size(k_records) else []
+    vr = np.asarray(v_records, np.uint8).reshape(-1, record_bytes(v_bits, T, d)) if np.size(v_records) else []
+    parts_k = [np.asarray(sink_k, np.float16).reshape(-1, d).astype(np.float64)]
+    parts_v = [np.asarray(sink_v, np.float16).reshape(-1, d).astype(np.float64)]
+    if len(kr):
+        assert parts_k[0].shape[0] == SINK, "sealed groups follow a full sink"
+    for g in range(len(kr)):
+        parts_k.append(dequant(kr[g], k_bits, 0, frame=0, T=T, d=d))
+        parts_v.append(dequant(vr[g], v_bits, 1, frame=0, T=T, d=d))
+    parts_k.append(np.asarray(tail_k, np.float16).reshape(-1, d).astype(np.float64))
+    parts_v.append(np.asarray(tail_v, np.float16).reshape(-1, d).astype(np.float64))
+    K = np.concatenate(parts_k)  # row j = the key at position j
+    V = np.concatenate(parts_v)
+    out = np.empty((n_q, r, d))
+    for i, P in enumerate(positions):
+        if not 0 <= P < K.shape[0]:
+            raise ValueError("query position outside the cache")
+        s = scale * (q[i] @ K[:P + 1].T)  # [r][P + 1]
+        s -= s.max(axis=1, keepdims=True)
+        w = np.exp(s)
+        out[i] = (w @ V[:P + 1]) / w.sum(axis=1, keepdims=True)
+    return out
+
+
 def bits_per_element(bits: int, T: int = GROUP, d: int = HEAD_DIM) -> float:
     """Body bits per cached element of the record format: payload plus metadata."""
     return record_bytes(bits, T, d) * 8.0 / (T * d)
@@ -318,6 +355,26 @@ class OracleCache:
         n_tail = len(st["tail_k"])
         assert n_tail == max(n - SINK, 0) - GROUP * n_groups
         return n_sink, n_groups, n_tail
+
+    def prefill_attend(self, s, q, scale, kv_heads=None):
+        """q: [n_q][Hq][d] fp16, the queries of the last n_q tokens of sequence s ->
+        out [n_q][Hq][d] fp64, each attending causally to the cache as it stands."""
+        st = self._seq(s)
+        n = st["n"]
+        n_sink, n_groups, n_tail = self.regions(s)
+        n_q, hq = q.shape[0], q.shape[1]
+        r = hq // self.hkv
+        pos = list(range(n - n_q, n))
+        out = np.full((n_q, hq, self.d), np.nan)
+        heads = range(self.hkv) if kv_heads is None else kv_heads
+        tk, tv = self.tail(s)
+        for h in heads:
+            kr = np.stack([g[h] for g in st["krec"]]) if n_groups else np.zeros((0,), np.uint8)
+            vr = np.stack([g[h] for g in st["vrec"]]) if n_groups else np.zeros((0,), np.uint8)
+            out[:, h * r:(h + 1) * r] = prefill_attention(
+                q[:, h * r:(h + 1) * r], pos, scale, st["sink_k"][:n_sink, h], st["sink_v"][:n_sink, h],
+                kr, vr, tk[:, h], tv[:, h], self.kb, self.vb)
+        return out
 
     def attend(self, s, q, scale, kv_heads=None):
         """q: [Hq][d] fp16 for sequence s -> out [Hq][d] fp64 (contiguous GQA grouping)."""

@@ -351,6 +351,81 @@ def test_attention_brute_force_over_dequantised_cache(kb, vb):
         assert np.abs(out - exact).max() < 0.05 * np.abs(exact).max()
 
 
+@pytest.mark.parametrize("kb,vb", [(2, 2), (4, 2), (3, 3)])
+def test_prefill_attention_reduces_to_decode_attention(kb, vb):
+    """Prefill (many-query) attention at the positions where the causal cut falls on a
+    region boundary equals the decode-attention oracle (the C restatement) over the
+    regions up to that cut: the last query over the whole cache; a query ending sealed
+    group g over the sink and groups 0..g; a query inside the sink over the sink up to
+    it; a query inside the tail over the sink, every group and the tail up to it."""
+    src = workloads.TokenSource(11, 0, 1)
+    n = 128 + 128 * 3 + 41
+    k, v = src.tokens(0, n)
+    k = k[:, 0]
+    v = v[:, 0]
+    kr = np.stack([oracle.seal(k[128 + 128 * g:256 + 128 * g], kb, 0) for g in range(3)])
+    vr = np.stack([oracle.seal(v[128 + 128 * g:256 + 128 * g], vb, 1) for g in range(3)])
+    positions = [0, 5, 127, 255, 383, 511, 512, 530, n - 1]
+    q = RNG.standard_normal((len(positions), 2, 128)).astype(np.float16)
+    scale = 1 / math.sqrt(128)
+    out = oracle.prefill_attention(q, positions, scale, k[:128], v[:128], kr, vr, k[512:], v[512:], kb, vb)
+    empty = np.zeros(0, np.uint8)
+    none = np.zeros((0, 128), np.float16)
+    for i, P in enumerate(positions):
+        if P < 128:
+            ref = oracle.attention(q[i], scale, k[:P + 1], v[:P + 1], empty, empty, none, none, kb, vb)
+        elif P < 512:
+            assert (P - 127) % 128 == 0
+            g = (P - 255) // 128
+            ref = oracle.attention(q[i], scale, k[:128], v[:128], kr[:g + 1], vr[:g + 1], none, none, kb, vb)
+        else:
+            ref = oracle.attention(q[i], scale, k[:128], v[:128], kr, vr, k[512:P + 1], v[512:P + 1], kb, vb)
+        assert np.allclose(out[i], ref, atol=1e-11, rtol=1e-11), P
+
+
+def test_prefill_attention_is_causal_and_matches_cache_helper():
+    """Keys after a query's position do not move its output: changing every token from
+    the next group boundary on leaves it bit-identical (a sealed record depends on all
+    128 tokens of its group, so the boundary, not the position, is the cut). The
+    cache-level helper over the last n_q tokens equals the per-head function."""
+    src = workloads.TokenSource(12, 0, 2)
+    n = 128 + 128 * 2 + 9
+    k, v = src.tokens(0, n)
+    cache = oracle.OracleCache(2, 2, 2)
+    cache.append(0, k, v)
+    q = RNG.standard_normal((20, 4, 128)).astype(np.float16)
+    scale = 1 / math.sqrt(128)
+    out = cache.prefill_attend(0, q, scale)
+    k2, v2 = k.copy(), v.copy()
+    k2[384:] = -k2[384:]
+    v2[384:] = v2[384:] * np.float16(2)
+    other = oracle.OracleCache(2, 2, 2)
+    other.append(0, k2, v2)
+    pos = np.arange(n - 20, n)
+    out2 = other.prefill_attend(0, q, scale)
+    seen = pos >= 384  # queries at or after the first changed token see it
+    assert seen.any() and (~seen).any()
+    assert np.array_equal(out[~seen], out2[~seen])
+    assert all(not np.array_equal(out[i], out2[i]) for i in np.nonzero(seen)[0])
+    q_early = RNG.standard_normal((2, 4, 128)).astype(np.float16)
+    for c in (cache, other):
+        st = c.seqs[0]
+        kr = np.stack([g[1] for g in st["krec"]])
+        vr = np.stack([g[1] for g in st["vrec"]])
+        tk, tv = c.tail(0)
+        c.early = oracle.prefill_attention(q_early[:, 2:], [299, 383], scale, st["sink_k"][:, 1], st["sink_v"][:, 1],
+                                           kr, vr, tk[:, 1], tv[:, 1], 2, 2)
+    assert np.array_equal(cache.early, other.early)
+    # the helper equals the per-head call (KV head 1 holds query heads 2, 3)
+    st = cache.seqs[0]
+    kr = np.stack([g[1] for g in st["krec"]])
+    vr = np.stack([g[1] for g in st["vrec"]])
+    tk, tv = cache.tail(0)
+    ref = oracle.prefill_attention(q[:, 2:], list(pos), scale, st["sink_k"][:, 1], st["sink_v"][:, 1], kr, vr,
+                                   tk[:, 1], tv[:, 1], 2, 2)
+    assert np.array_equal(out[:, 2:], ref)
+
+
 # --------------------------------------------------------------------------- regions
 def test_cache_regions_and_seal_timing():
     """anbeeld.com 2.1: sink = first 128 tokens; a group seals exactly when its 128th
