@@ -170,6 +170,28 @@ kvarn_status kvarn_decode_step(kvarn_cache* cache, int32_t layer, int32_t n_seqs
                                const void* k, const void* v, const void* q, void* out, float softmax_scale,
                                void* stream);
 
+/* Prefill (many-query) attention: the queries of the last q_lens[i] tokens of
+ * sequence seq_ids[i] (positions n - q_lens[i] .. n - 1, n its current length), each
+ * attending causally to the cached keys at positions up to its own. The cache is read
+ * as it stands (sink and tail exact; sealed groups from their records, the query
+ * rotated in and the sealed part rotated back, anbeeld.com 1 and 2.1), so a chunk
+ * appended by kvarn_append and then attended with this call reads its own tokens
+ * sealed wherever their group was sealed by that append.
+ * q: device fp16 [sum(q_lens)][num_q_heads][128], the sequences' query rows back to
+ * back in the order of seq_ids; out: device fp16, same shape (written, not read).
+ * seq_ids, q_lens: host arrays; 0 <= q_lens[i] <= n; n_seqs <= 256. EINVAL (nothing
+ * enqueued) on bad ids, lengths or pointers; sum(q_lens) * num_q_heads < 2^31. */
+kvarn_status kvarn_prefill_attention(kvarn_cache* cache, int32_t layer, int32_t n_seqs, const int32_t* seq_ids,
+                                     const int32_t* q_lens, const void* q, void* out, float softmax_scale,
+                                     void* stream);
+
+/* Prefill of a prompt chunk: kvarn_append(n_tokens, k, v) (which seals every group the
+ * chunk completes, many per launch) followed by kvarn_prefill_attention with
+ * q_lens = n_tokens. Arguments of both are checked before anything is enqueued. */
+kvarn_status kvarn_prefill(kvarn_cache* cache, int32_t layer, int32_t n_seqs, const int32_t* seq_ids,
+                           const int32_t* n_tokens, const void* k, const void* v, const void* q, void* out,
+                           float softmax_scale, void* stream);
+
 /* Decode attention as kvarn_decode_attention, for callers that cannot allocate device
  * memory: a plugin inside a serving engine that owns all device memory through its own
  * pool and forbids cudaMalloc, or a process under a hard device-memory cap, still has

@@ -60,6 +60,27 @@ class KVarNCache:
                             self._stream(stream))
         return out
 
+    def prefill_attention(self, layer: int, seq_ids: Sequence[int], q_lens: Sequence[int], q: torch.Tensor,
+                          out: Optional[torch.Tensor] = None, scale: Optional[float] = None,
+                          stream=None) -> torch.Tensor:
+        """Causal attention of the last q_lens[i] tokens of each sequence over the cache as
+        it stands; q, out: [sum(q_lens)][Hq][128] fp16."""
+        if out is None:
+            out = torch.empty_like(q)
+        K.kvarn_prefill_attention(self.handle, layer, list(seq_ids), list(q_lens), q, out,
+                                  self.scale if scale is None else scale, self._stream(stream))
+        return out
+
+    def prefill(self, layer: int, seq_ids: Sequence[int], n_tokens: Sequence[int], k: torch.Tensor, v: torch.Tensor,
+                q: torch.Tensor, out: Optional[torch.Tensor] = None, scale: Optional[float] = None,
+                stream=None) -> torch.Tensor:
+        """Append a prompt chunk (sealing the groups it completes) and attend its queries."""
+        if out is None:
+            out = torch.empty_like(q)
+        K.kvarn_prefill(self.handle, layer, list(seq_ids), list(n_tokens), k, v, q, out,
+                        self.scale if scale is None else scale, self._stream(stream))
+        return out
+
     def dequant_group(self, layer, seq_id, group, kv_head, which, frame=0, stream=None) -> torch.Tensor:
         out = torch.empty((128, 128), dtype=torch.float32, device=self.mem.device)
         K.kvarn_dequant_group(self.handle, layer, seq_id, group, kv_head, which, frame, out, True,

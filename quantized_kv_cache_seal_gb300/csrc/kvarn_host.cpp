@@ -384,6 +384,84 @@ kvarn_status run_decode(kvarn_cache* c, int32_t layer, int32_t n_seqs, const int
     return KVARN_OK;
 }
 
+// Checks of a prefill-attention call made before anything is enqueued. `added` (the
+// tokens a fused call appends first, or null) extends each sequence's length.
+kvarn_status check_prefill(const kvarn_cache* c, int32_t layer, int32_t n_seqs, const int32_t* seq_ids,
+                           const int32_t* q_lens, const int32_t* added, const void* q, const void* out,
+                           float scale) {
+    kvarn_status st = check_ids(c, layer, n_seqs, seq_ids);
+    if (st) return st;
+    if (n_seqs > kMaxBatch) return KVARN_ECAPACITY;
+    if (n_seqs > 0 && !q_lens) return KVARN_EINVAL;
+    if (!std::isfinite(scale)) return KVARN_EINVAL;
+    int64_t rows = 0, ctas = 0;
+    const int qt = kPrefillRows / c->r;
+    for (int i = 0; i < n_seqs; ++i) {
+        const int64_t n = c->Lc(seq_ids[i], layer) + (added ? (int64_t)added[i] : 0);
+        if (q_lens[i] < 0 || q_lens[i] > n) return KVARN_EINVAL;
+        rows += q_lens[i];
+        ctas += (int64_t)(q_lens[i] + qt - 1) / qt * c->cfg.num_kv_heads;
+    }
+    if (rows > 0 && (!q || !out)) return KVARN_EINVAL;
+    if (rows * c->cfg.num_q_heads >= (1ll << 31) || ctas >= (1ll << 31)) return KVARN_ECAPACITY;
+    if (!c->host_only && prefill_smem_bytes(c->cfg.k_bits, c->cfg.v_bits, 1) > c->max_smem) return KVARN_ECAPACITY;
+    return KVARN_OK;
+}
+
+// Prefill attention after check_prefill: one CTA per (sequence, KV head, query tile).
+kvarn_status run_prefill(kvarn_cache* c, int32_t layer, int32_t n_seqs, const int32_t* seq_ids,
+                         const int32_t* q_lens, const void* q, void* out, float scale, void* stream) {
+    const kvarn_config& cfg = c->cfg;
+    static thread_local PrefillParams p;
+    std::memset(&p, 0, sizeof(p));
+    p.base = c->base;
+    p.lay = c->lay;
+    p.q = (const uint16_t*)q;
+    p.out = (uint16_t*)out;
+    p.n_seqs = 0;
+    p.hq = cfg.num_q_heads;
+    p.hkv = cfg.num_kv_heads;
+    p.r = c->r;
+    p.k_bits = cfg.k_bits;
+    p.v_bits = cfg.v_bits;
+    p.layer = layer;
+    p.num_layers = cfg.num_layers;
+    p.max_groups = c->max_groups;
+    p.rec_k = (int32_t)c->rec_k;
+    p.rec_v = (int32_t)c->rec_v;
+    p.slot_bytes = (int32_t)c->slot_bytes;
+    p.tail_cap = c->tail_cap;
+    p.scale_log2 = scale * 1.4426950408889634f;
+    const int qt = kPrefillRows / c->r;
+    int64_t row = 0, ctas = 0;
+    for (int i = 0; i < n_seqs; ++i) {
+        const int64_t n = c->Lc(seq_ids[i], layer);
+        if (q_lens[i] > 0) {  // sequences without queries take no CTA
+            PrefillSeq& e = p.seqs[p.n_seqs++];
+            e.seq = seq_ids[i];
+            e.n = (int32_t)n;
+            e.q_len = q_lens[i];
+            e.q_row = (int32_t)row;
+            e.n_groups = (int32_t)groups_sealed(n, cfg.tail_floor);
+            e.n_tiles = (q_lens[i] + qt - 1) / qt;
+            e.cta_begin = (int32_t)ctas;
+            ctas += (int64_t)e.n_tiles * cfg.num_kv_heads;
+        }
+        row += q_lens[i];
+    }
+    if (ctas == 0) return KVARN_OK;
+    p.grid = (int32_t)ctas;
+    int stages = 8;
+    while (stages > 1 && prefill_smem_bytes(cfg.k_bits, cfg.v_bits, stages) > c->max_smem) --stages;
+    p.stages = stages;
+    if (c->host_only) return KVARN_OK;
+    kvarn_status st = ensure_init(c, stream);
+    if (st) return st;
+    const int rc = launch_prefill(p, prefill_smem_bytes(cfg.k_bits, cfg.v_bits, stages), stream);
+    if (rc) { set_cuda_error(rc, "prefill launch"); return KVARN_ECUDA; }
+    return KVARN_OK;
+}
+
 }  // namespace
 
 extern "C" {
@@ -555,6 +633,24 @@ kvarn_status kvarn_append(kvarn_cache* c, int32_t layer, int32_t n_seqs, const i
 kvarn_status kvarn_decode_attention(kvarn_cache* c, int32_t layer, int32_t n_seqs, const int32_t* seq_ids,
                                     const void* q, void* out, float softmax_scale, void* stream) {
     return run_decode(c, layer, n_seqs, seq_ids, nullptr, nullptr, q, out, softmax_scale, stream, false);
+}
+
+kvarn_status kvarn_prefill_attention(kvarn_cache* c, int32_t layer, int32_t n_seqs, const int32_t* seq_ids,
+                                     const int32_t* q_lens, const void* q, void* out, float softmax_scale,
+                                     void* stream) {
+    kvarn_status st = check_prefill(c, layer, n_seqs, seq_ids, q_lens, nullptr, q, out, softmax_scale);
+    if (st) return st;
+    return run_prefill(c, layer, n_seqs, seq_ids, q_lens, q, out, softmax_scale, stream);
+}
+
+kvarn_status kvarn_prefill(kvarn_cache* c, int32_t layer, int32_t n_seqs, const int32_t* seq_ids,
+                           const int32_t* n_tokens, const void* k, const void* v, const void* q, void* out,
+                           float softmax_scale, void* stream) {
+    kvarn_status st = check_prefill(c, layer, n_seqs, seq_ids, n_tokens, n_tokens, q, out, softmax_scale);
+    if (st) return st;
+    st = kvarn_append(c, layer, n_seqs, seq_ids, n_tokens, k, v, stream);
+    if (st) return st;
+    return run_prefill(c, layer, n_seqs, seq_ids, n_tokens, q, out, softmax_scale, stream);
 }
 
 kvarn_status kvarn_decode_step(kvarn_cache* c, int32_t layer, int32_t n_seqs, const int32_t* seq_ids,

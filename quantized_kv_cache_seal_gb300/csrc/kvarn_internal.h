@@ -24,6 +24,8 @@ constexpr int kPartialFloats = 528;  // [0] epoch bits, [4..8) m, [8..12) l, [12
 constexpr int kDecodeThreads = 512;  // 3 compute warpgroups + 1 copy-issuing warpgroup
 constexpr int kExactRows = 16;       // tokens of an exact (sink or tail) sub-group of the decode stream
 constexpr int kSealThreads = 256;
+constexpr int kPrefillThreads = 256;  // 8 warps, one 16-row MMA tile each
+constexpr int kPrefillRows = 128;     // query rows (token, head) of a prefill CTA
 
 // device error word bits
 constexpr int kErrTimeout = 1;
@@ -83,6 +85,31 @@ struct DecodeParams {
     SeqEntry seqs[kMaxBatch];
 };
 
+// One sequence of a prefill-attention call: its queries are those of the last q_len
+// tokens (positions n - q_len .. n - 1), rows q_row .. q_row + q_len - 1 of q and out.
+struct PrefillSeq {
+    int32_t seq;
+    int32_t n;          // tokens in the cache
+    int32_t q_len;
+    int32_t q_row;
+    int32_t n_groups;   // sealed groups of the sequence
+    int32_t n_tiles;    // query tiles (kPrefillRows / r tokens each)
+    int32_t cta_begin;  // first CTA of this sequence (n_tiles * Hkv CTAs)
+};
+
+struct PrefillParams {
+    uint8_t* base;
+    Layout lay;
+    const uint16_t* q;  // [rows][Hq][128]
+    uint16_t* out;
+    int32_t n_seqs, hq, hkv, r, k_bits, v_bits, layer, num_layers, max_groups;
+    int32_t rec_k, rec_v, slot_bytes, tail_cap;
+    int32_t stages;     // record ring stages
+    int32_t grid;
+    float scale_log2;
+    PrefillSeq seqs[kMaxBatch];
+};
+
 // Parameters of the bulk seal for kvarn_append.
 struct SealJobSeq {
     int32_t seq;
@@ -126,6 +153,8 @@ struct AppendParams {
 
 // Launchers (defined in the .cu files). Return 0 on success, else a cudaError_t value.
 int launch_decode(const DecodeParams& p, int smem_bytes, void* stream);
+int launch_prefill(const PrefillParams& p, int smem_bytes, void* stream);
+int prefill_smem_bytes(int k_bits, int v_bits, int stages);
 int launch_seal_jobs(const SealParams& p, void* stream);
 int launch_append(const AppendParams& p, void* stream);
 int launch_seal_groups(const void* x, int n, int bits, int which, int iters, void* records, float* scales,

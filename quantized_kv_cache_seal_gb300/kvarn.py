@@ -25,7 +25,8 @@ EXPORTS = [
     "kvarn_append", "kvarn_decode_attention", "kvarn_decode_attention_noalloc", "kvarn_decode_step", "kvarn_dequant_group",
     "kvarn_seq_release", "kvarn_seq_length", "kvarn_group_record", "kvarn_exact_regions",
     "kvarn_cache_stats", "kvarn_seal_groups", "kvarn_check_device_error", "kvarn_status_string",
-    "kvarn_last_error", "kvarn_partition_units", "kvarn_device_accessible",
+    "kvarn_last_error", "kvarn_partition_units", "kvarn_device_accessible", "kvarn_prefill_attention",
+    "kvarn_prefill",
 ]
 
 
@@ -80,6 +81,8 @@ def load(build_if_missing: bool = True):
     L.kvarn_decode_attention.argtypes = [P, I32, I32, IP, P, P, F, P]
     L.kvarn_decode_attention_noalloc.argtypes = [P, I32, I32, IP, P, P, F, P]
     L.kvarn_decode_step.argtypes = [P, I32, I32, IP, P, P, P, P, F, P]
+    L.kvarn_prefill_attention.argtypes = [P, I32, I32, IP, IP, P, P, F, P]
+    L.kvarn_prefill.argtypes = [P, I32, I32, IP, IP, P, P, P, P, F, P]
     L.kvarn_dequant_group.argtypes = [P, I32, I32, I32, I32, I32, I32, I32, P, P]
     L.kvarn_seq_release.argtypes = [P, I32]
     L.kvarn_seq_length.argtypes = [P, I32, I32, ctypes.POINTER(I64)]
@@ -180,6 +183,17 @@ def kvarn_decode_attention_noalloc(handle, layer, seq_ids, q, out, softmax_scale
 def kvarn_decode_step(handle, layer, seq_ids, k, v, q, out, softmax_scale, stream=None):
     _check(load().kvarn_decode_step(handle, layer, len(seq_ids), _ints(seq_ids), _ptr(k), _ptr(v), _ptr(q),
                                     _ptr(out), float(softmax_scale), _stream(stream)), "kvarn_decode_step")
+
+
+def kvarn_prefill_attention(handle, layer, seq_ids, q_lens, q, out, softmax_scale, stream=None):
+    _check(load().kvarn_prefill_attention(handle, layer, len(seq_ids), _ints(seq_ids), _ints(q_lens), _ptr(q),
+                                          _ptr(out), float(softmax_scale), _stream(stream)),
+           "kvarn_prefill_attention")
+
+
+def kvarn_prefill(handle, layer, seq_ids, n_tokens, k, v, q, out, softmax_scale, stream=None):
+    _check(load().kvarn_prefill(handle, layer, len(seq_ids), _ints(seq_ids), _ints(n_tokens), _ptr(k), _ptr(v),
+                                _ptr(q), _ptr(out), float(softmax_scale), _stream(stream)), "kvarn_prefill")
 
 
 def kvarn_dequant_group(handle, layer, seq_id, group, kv_head, which, frame, out, out_fp32=True, stream=None):

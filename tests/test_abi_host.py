@@ -183,6 +183,33 @@ def test_argument_validation():
         K.kvarn_seq_length(h, 0, 9)
 
 
+def test_prefill_argument_checks_and_fused_bookkeeping():
+    """kvarn_prefill_attention: q_lens within 0..length, pointers present when any query
+    row exists, finite scale; nothing changes on a rejected call. kvarn_prefill appends
+    first (sealing the groups the chunk completes) and checks q_lens against the
+    extended length; a rejected fused call appends nothing."""
+    h, _ = host_cache()
+    K.kvarn_append(h, 0, [0], [300], FAKE, FAKE)
+    K.kvarn_prefill_attention(h, 0, [0], [300], FAKE, FAKE, 0.1)   # every token's query
+    K.kvarn_prefill_attention(h, 0, [0], [0], 0, 0, 0.1)           # no rows: no pointers needed
+    K.kvarn_prefill_attention(h, 0, [0, 1], [1, 0], FAKE, FAKE, 0.1)
+    for args in ([h, 0, [0], [301], FAKE, FAKE, 0.1], [h, 0, [0], [-1], FAKE, FAKE, 0.1],
+                 [h, 0, [0], [5], 0, FAKE, 0.1], [h, 0, [0], [5], FAKE, 0, 0.1],
+                 [h, 0, [0], [5], FAKE, FAKE, float("inf")], [h, 0, [0, 0], [1, 1], FAKE, FAKE, 0.1],
+                 [h, 0, [1], [1], FAKE, FAKE, 0.1]):
+        with pytest.raises(K.KVarNError) as e:
+            K.kvarn_prefill_attention(*args)
+        assert e.value.status == 1
+    K.kvarn_prefill(h, 0, [1], [128 + 256 + 5], FAKE, FAKE, FAKE, FAKE, 0.1)
+    assert K.kvarn_seq_length(h, 0, 1) == 128 + 256 + 5
+    assert K.kvarn_cache_stats(h).pool_slots_used == 1 + 2  # seq 0: group 0; seq 1: groups 0, 1
+    with pytest.raises(K.KVarNError):
+        K.kvarn_prefill(h, 0, [2], [10], FAKE, FAKE, FAKE, FAKE, float("nan"))
+    with pytest.raises(K.KVarNError):
+        K.kvarn_prefill(h, 0, [2], [10], FAKE, FAKE, 0, FAKE, 0.1)
+    assert K.kvarn_seq_length(h, 0, 2) == 0
+
+
 def test_bits_per_element_formula():
     """Body bits/element = b + 528*8/16384 per side (fig1.dev: about 2.3 at two bits)."""
     for kb, vb in [(2, 2), (4, 2), (4, 4), (8, 8)]:
