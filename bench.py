@@ -10,7 +10,14 @@ Workload (default): Llama-3.1-8B attention shape -- 32 query heads, 8 KV heads,
 head_dim 128 -- batch 16, context 32768 + U{0..127} tail tokens per sequence, 2-bit K
 and V. Synthetic data (seeded), generated on the device.
 
+Beside it, the line carries the bulk-seal rate and a prompt-prefill leg: Qwen3-4B
+attention shape (32 query heads, 8 KV heads), one 4096-token prompt through
+kvarn_prefill (bulk append sealing 31 groups per KV head and side, then causal
+attention of all 4096 queries over the cache), with the tensor roofline of the
+attention kernel.
+
   python bench.py [--gpus N] [--steps K] [--warmup W] [--impl reference]
+  python bench.py --prefill-only
 
 Prints one JSON line (rank 0). Under torchrun each rank runs its own replica of the
 workload on its GPU (weak scaling; the path has no exchange step).
@@ -131,13 +138,14 @@ class ClockSampler:
                 "samples": len(sm)}
 
 
-def profiled_traffic(alg_bytes):
-    """DRAM bytes per decode launch from the committed ncu capture of this kernel build,
-    scaled to this launch's algorithmic bytes (the capture ran the same workload a few
-    steps earlier); None if the kernel sources changed since the capture."""
+def profiled_traffic(alg_bytes, record="decode_kernel_llama31_8b_b16_ctx32k_k2v2_traffic.json"):
+    """DRAM bytes per launch from the committed ncu capture of this kernel build, scaled
+    to this launch's algorithmic bytes when the record has them (the decode capture ran
+    the same workload a few steps earlier; the prefill capture ran this very launch);
+    None if the kernel sources changed since the capture."""
     import hashlib
     try:
-        with open(os.path.join(ROOT, "profiles", "decode_kernel_llama31_8b_b16_ctx32k_k2v2_traffic.json")) as fh:
+        with open(os.path.join(ROOT, "profiles", record)) as fh:
             rec = json.load(fh)
         h = hashlib.sha256()
         for f in rec["sources"]:
@@ -145,6 +153,8 @@ def profiled_traffic(alg_bytes):
                 h.update(fh.read())
         if h.hexdigest() != rec["sources_sha256"]:
             return None
+        if "alg_bytes_per_launch" not in rec:
+            return float(rec["dram_bytes_per_launch"])
         return float(rec["dram_bytes_per_launch"]) * alg_bytes / float(rec["alg_bytes_per_launch"])
     except (OSError, KeyError, ValueError):
         return None
@@ -190,6 +200,75 @@ def build_cache(torch, device, extra):
     torch.cuda.synchronize()
     torch.cuda.empty_cache()
     return cache, ids, lengths
+
+
+def measured_tensor_peak():
+    """Dense bf16 burst TFLOP/s from MEASURED_PEAKS.json (f16 mma has the same nominal
+    rate), else the fallback."""
+    try:
+        with open(os.path.join(ROOT, "MEASURED_PEAKS.json")) as fh:
+            v = float(json.load(fh)["bf16_tflops"])
+        return v, "measured bf16 dense (burst), MEASURED_PEAKS.json"
+    except (OSError, KeyError, ValueError):
+        return 1900.0, "fallback bf16 dense"
+
+
+PF_HQ, PF_HKV, PF_N = 32, 8, 4096  # prefill leg: Qwen3-4B attention shape, one 4096-token prompt
+
+
+def prefill_leg(torch, device, stream, barrier, reps=5):
+    """Prompt prefill: kvarn_prefill (bulk append of 4096 tokens, sealing 31 groups per
+    KV head and side, then causal many-query attention of all 4096 queries). Each rep
+    starts from an empty sequence; L2 is flushed (a 256 MiB write) before each timed call.
+    Also times kvarn_prefill_attention alone on the filled cache for its roofline."""
+    from quantized_kv_cache_seal_gb300 import workloads
+    from quantized_kv_cache_seal_gb300.cache import KVarNCache
+
+    cache = KVarNCache(num_layers=1, max_seqs=1, num_q_heads=PF_HQ, num_kv_heads=PF_HKV, k_bits=KB, v_bits=VB,
+                       tail_floor=FLOOR, max_seq_len=PF_N, device=device)
+    k, v = workloads.torch_tokens(SEED + 11, 0, 0, PF_N, PF_HKV, device=device)
+    k, v = k.contiguous(), v.contiguous()
+    q = workloads.torch_queries(SEED + 12, PF_N, 1, PF_HQ, device=device)[:, 0].contiguous()
+    out = torch.empty_like(q)
+    flush = torch.empty(256 << 20, dtype=torch.uint8, device=device)
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    fused, attn = [], []
+    for rep in range(reps + 2):  # the first two untimed
+        cache.release(0)
+        flush.fill_(rep & 255)
+        barrier()
+        e0.record(stream)
+        cache.prefill(0, [0], [PF_N], k, v, q, out)
+        e1.record(stream)
+        barrier()
+        if rep >= 2:
+            fused.append(e0.elapsed_time(e1))
+        flush.fill_((rep + 1) & 255)
+        barrier()
+        e0.record(stream)
+        cache.prefill_attention(0, [0], [PF_N], q, out)
+        e1.record(stream)
+        barrier()
+        if rep >= 2:
+            attn.append(e0.elapsed_time(e1))
+    err = cache.check_device_error()
+    cache.close()
+    if err:
+        raise RuntimeError(f"device error word after prefill: {err}")
+    f_ms, a_ms = statistics.median(fused), statistics.median(attn)
+    flops = PF_HQ * 4 * 128 * (PF_N * (PF_N + 1) / 2)  # causal QK + PV, 2 flops per MAC
+    peak, kind = measured_tensor_peak()
+    ach = flops / (a_ms * 1e-3) / 1e12
+    return {
+        "workload": f"qwen3_4b_gqa32x8_prompt{PF_N}_k{KB}v{VB}" + (f"_tail_floor{FLOOR}" if FLOOR else ""),
+        "tokens_per_s": PF_N / (f_ms * 1e-3), "fused_ms": f_ms, "attention_ms": a_ms, "append_seal_ms": f_ms - a_ms,
+        "l2": "flushed (256 MiB write) before each timed call",
+        "roofline": {"bound": "tensor", "achieved": ach, "peak": peak, "unit": "TFLOP/s", "frac": ach / peak,
+                     "traffic": profiled_traffic(None, "prefill_kernel_qwen3_4b_prompt4096_k2v2_traffic.json")
+                     if FLOOR == 0 and (KB, VB) == (2, 2) else None, "peak_kind": kind, "kernel": f"prefill_kernel<{KB},{VB}>",
+                     "alg_flops_per_launch": flops, "launch_us": a_ms * 1e3},
+        "gpu_launches_per_prefill": 3,  # seal_jobs_kernel, append_kernel, prefill_kernel
+    }
 
 
 def run_ours(args):
@@ -429,6 +508,8 @@ def run_ours(args):
         seal_gps = n / (s0.elapsed_time(s1) / 1e3) * world
         del x
 
+    prefill = None if args.no_prefill else prefill_leg(torch, device, stream, barrier)
+
     result = {
         "metric": METRIC, "value": value, "unit": "tokens/s", "n_gpus": world, "steps": K_, "warmup": W,
         "ms_per_step": ms_per_step, "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
@@ -444,6 +525,7 @@ def run_ours(args):
                      "peak_kind": peak_kind, "kernel": f"decode_kernel<{KB},{VB}>",
                      "alg_bytes_per_launch": alg_bytes, "launch_us": launch_us},
         "seal_groups_per_s": seal_gps,
+        "prefill": prefill,
         "seal_share": seal_share,
         "seal_steps": seal_steps,
         "clocks": clocks,
@@ -599,6 +681,8 @@ def main():
     ap.add_argument("--min-seconds", type=float, default=1.0)
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--no-seal", action="store_true")
+    ap.add_argument("--no-prefill", action="store_true")
+    ap.add_argument("--prefill-only", action="store_true", help="run the prompt-prefill leg alone (one JSON object)")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--cpu-pairs", type=int, default=32)
     ap.add_argument("--ref-pairs", type=int, default=16)
@@ -621,6 +705,12 @@ def main():
         WORKLOAD = f"{WORKLOAD}_tail_floor{FLOOR}"
     if args.impl == "reference":
         run_reference(args)
+    elif args.prefill_only:
+        import torch
+
+        torch.cuda.set_device(0)
+        res = prefill_leg(torch, torch.device("cuda", 0), torch.cuda.current_stream(), torch.cuda.synchronize)
+        print(json.dumps({"prefill": res}), flush=True)
     else:
         run_ours(args)
 
