@@ -9,7 +9,8 @@ themselves are checked against the oracle's seal in the seal and decode tests.
 Cases: prompts from scratch (queries in the sink, inside sealed groups, in the tail),
 chunks on top of a cache, every query head ratio (1, 2, 4), widths 2..8 with the odd
 ones and the presets, a tail floor, empty query lists, the fused append + attention,
-and sampled rows of the Qwen3-4B 4096-token prefill.
+a second layer with interleaved pool slots and norm spikes at the Phi-4 shape, and
+sampled rows of the Qwen3-4B 4096-token prefill.
 """
 import math
 
@@ -32,28 +33,28 @@ def _cache(hq, hkv, kb, vb, seqs=3, max_len=2048, floor=0):
                       max_seq_len=max_len, tail_floor=floor)
 
 
-def _records(cache, seq, kvh, which, n_groups):
+def _records(cache, seq, kvh, which, n_groups, layer=0):
     if n_groups == 0:
         return np.zeros(0, np.uint8)
-    return np.stack([cache.record(0, seq, g, kvh, which).cpu().numpy() for g in range(n_groups)])
+    return np.stack([cache.record(layer, seq, g, kvh, which).cpu().numpy() for g in range(n_groups)])
 
 
-def _check(cache, seq, q, out, kb, vb, floor=0, rows=None, label=""):
+def _check(cache, seq, q, out, kb, vb, floor=0, rows=None, label="", layer=0, heads=None):
     """q, out: [n_q][Hq][128] for the last n_q tokens of `seq`; rows: the query rows to
-    check (all by default)."""
-    n = cache.length(0, seq)
+    check (all by default); heads: the KV heads to check (all by default)."""
+    n = cache.length(layer, seq)
     n_q, hq = q.shape[0], q.shape[1]
     hkv = cache.cfg.num_kv_heads
     r = hq // hkv
     n_groups = max(max(n - 128, 0) // 128 - floor, 0)
-    sk, sv = [t.cpu().numpy() for t in cache.exact_regions(0, seq)[:2]]
-    tk, tv = [t.cpu().numpy() for t in cache.exact_tail(0, seq)]
+    sk, sv = [t.cpu().numpy() for t in cache.exact_regions(layer, seq)[:2]]
+    tk, tv = [t.cpu().numpy() for t in cache.exact_tail(layer, seq)]
     rows = list(range(n_q)) if rows is None else list(rows)
     pos = [n - n_q + i for i in rows]
-    for h in range(hkv):
+    for h in (range(hkv) if heads is None else heads):
         ref = oracle.prefill_attention(q[rows, h * r:(h + 1) * r], pos, SCALE, sk[h, :min(n, 128)],
-                                       sv[h, :min(n, 128)], _records(cache, seq, h, 0, n_groups),
-                                       _records(cache, seq, h, 1, n_groups), tk[h], tv[h], kb, vb)
+                                       sv[h, :min(n, 128)], _records(cache, seq, h, 0, n_groups, layer),
+                                       _records(cache, seq, h, 1, n_groups, layer), tk[h], tv[h], kb, vb)
         for j, i in enumerate(rows):
             parity.check_attention(out[i, h * r:(h + 1) * r], ref[j], f"{label} seq {seq} kvh {h} token {pos[j]}")
 
@@ -177,3 +178,43 @@ def test_qwen3_4b_prefill_4096_sampled_rows():
     assert bool(torch.isfinite(out.float()).all())
     rows = [0, 1, 127, 128, 200, 255, 1000, 2047, 3000, 3967, 3968, 4095]
     _check(cache, 0, q.cpu().numpy(), out.float().cpu().numpy(), 2, 2, rows=rows, label="qwen3-4b 4096")
+
+
+def test_phi4_shape_second_layer_interleaved_slots_spikes():
+    """Phi-4 attention shape (40 query heads, 10 KV heads), a cache of two layers whose
+    sequences were appended in interleaved rounds (the pool slots of a sequence are not
+    contiguous), 5 % of tokens with x10 K/V norms; prefill attention on layer 1."""
+    from quantized_kv_cache_seal_gb300.cache import KVarNCache
+    cache = KVarNCache(num_layers=2, max_seqs=3, num_q_heads=40, num_kv_heads=10, k_bits=4, v_bits=2,
+                       max_seq_len=2048)
+    lengths = [900, 1400, 700]
+    done = [0, 0, 0]
+    while any(d < n for d, n in zip(done, lengths)):
+        for layer in (0, 1):
+            ids, counts, ks, vs = [], [], [], []
+            for s, n in enumerate(lengths):
+                take = min(300, n - done[s])
+                if take <= 0:
+                    continue
+                k, v = workloads.torch_tokens(100 + layer, s, done[s], take, 10, spike_frac=0.05, spike_factor=10.0)
+                ids.append(s)
+                counts.append(take)
+                ks.append(k)
+                vs.append(v)
+            cache.append(layer, ids, counts, torch.cat(ks).contiguous(), torch.cat(vs).contiguous())
+        done = [min(n, d + 300) for d, n in zip(done, lengths)]
+    from quantized_kv_cache_seal_gb300 import kvarn as K
+    # group 0 of sequence 1 was sealed in the first round, group 1 in the second
+    p0, _ = K.kvarn_group_record(cache.handle, 1, 1, 0, 0, 0)
+    p1, _ = K.kvarn_group_record(cache.handle, 1, 1, 1, 0, 0)
+    assert p1 - p0 != K.kvarn_cache_stats(cache.handle).slot_bytes  # not adjacent in the pool
+    # one call over the sequences in the order 2, 0, 1; rows follow the call's order
+    q_lens = [200, 130, 64]
+    q = _queries(101, sum(q_lens), 40)
+    out = cache.prefill_attention(1, [2, 0, 1], q_lens, q)
+    torch.cuda.synchronize()
+    assert cache.check_device_error() == 0
+    qn, on = q.cpu().numpy(), out.float().cpu().numpy()
+    _check(cache, 2, qn[:200], on[:200], 4, 2, label="phi4 l1", layer=1, heads=[0, 9])
+    _check(cache, 0, qn[200:330], on[200:330], 4, 2, label="phi4 l1", layer=1, heads=[3])
+    _check(cache, 1, qn[330:], on[330:], 4, 2, label="phi4 l1", layer=1, heads=[5, 7])
