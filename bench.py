@@ -213,6 +213,30 @@ def measured_tensor_peak():
         return 1900.0, "fallback bf16 dense"
 
 
+def snapshot_leg(cache):
+    """Save the headline cache to a pinned host image and restore it (into the same cache,
+    which leaves its state as it was): bytes and host-clock times of both directions."""
+    import torch
+
+    from quantized_kv_cache_seal_gb300 import kvarn as K
+
+    n = K.kvarn_snapshot_bytes(cache.handle)
+    buf = torch.empty(n, dtype=torch.uint8, pin_memory=True)
+    torch.cuda.synchronize()
+    saves, loads = [], []
+    for _ in range(3):
+        t0 = time.perf_counter()
+        K.kvarn_snapshot_save(cache.handle, buf, n)
+        t1 = time.perf_counter()
+        K.kvarn_snapshot_load(cache.handle, buf, n)
+        t2 = time.perf_counter()
+        saves.append(t1 - t0)
+        loads.append(t2 - t1)
+    s, l = min(saves), min(loads)
+    return {"bytes": n, "save_ms": s * 1e3, "load_ms": l * 1e3, "save_gbs": n / s / 1e9, "load_gbs": n / l / 1e9,
+            "host_buffer": "pinned", "note": "records of every sealed group, exact regions, bookkeeping"}
+
+
 PF_HQ, PF_HKV, PF_N = 32, 8, 4096  # prefill leg: Qwen3-4B attention shape, one 4096-token prompt
 
 
@@ -509,6 +533,7 @@ def run_ours(args):
         del x
 
     prefill = None if args.no_prefill else prefill_leg(torch, device, stream, barrier)
+    snapshot = None if args.no_snapshot or world > 1 else snapshot_leg(cache)
 
     result = {
         "metric": METRIC, "value": value, "unit": "tokens/s", "n_gpus": world, "steps": K_, "warmup": W,
@@ -526,6 +551,7 @@ def run_ours(args):
                      "alg_bytes_per_launch": alg_bytes, "launch_us": launch_us},
         "seal_groups_per_s": seal_gps,
         "prefill": prefill,
+        "snapshot": snapshot,
         "seal_share": seal_share,
         "seal_steps": seal_steps,
         "clocks": clocks,
@@ -682,6 +708,7 @@ def main():
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--no-seal", action="store_true")
     ap.add_argument("--no-prefill", action="store_true")
+    ap.add_argument("--no-snapshot", action="store_true")
     ap.add_argument("--prefill-only", action="store_true", help="run the prompt-prefill leg alone (one JSON object)")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--cpu-pairs", type=int, default=32)

@@ -218,6 +218,28 @@ kvarn_status kvarn_dequant_group(kvarn_cache* cache, int32_t layer, int32_t seq_
                                  int32_t kv_head, int32_t which, int32_t frame, int32_t out_fp32, void* out,
                                  void* stream);
 
+/* Snapshot of a cache (checkpoint and restore). The KVarN pages have no counterpart of
+ * these calls; they are an interface addition for serving (moving or parking a cache).
+ * A snapshot holds the host bookkeeping (sequence lengths, block table) and the device
+ * state that attention reads: the exact sink and tail regions of every sequence and the
+ * pool slots in use (records of every sealed group), in one host byte image with a
+ * versioned header that records the cache's configuration.
+ * kvarn_snapshot_bytes: size of the image of the cache's current state.
+ * kvarn_snapshot_save: write the image into host memory `dst` (pageable or pinned, at
+ * least kvarn_snapshot_bytes). It is ordered after the work already enqueued on `stream`
+ * and returns once the copies are complete (the stream is synchronised); work on other
+ * streams that writes the cache must be complete before the call.
+ * kvarn_snapshot_load: replace the whole state of `cache` (created with the same
+ * configuration; flags may differ) by the image at `src`. The image is checked first
+ * (header, configuration, sizes, every table entry in range, no slot used twice, each
+ * sequence's sealed groups exactly those its length implies): EINVAL leaves the cache
+ * unchanged. Returns after the copies are complete. After a load, every call gives the
+ * results the saved cache would have given, bit for bit. With KVARN_FLAG_HOST_ONLY no
+ * device memory is touched: device sections are written as zeros and skipped on load. */
+kvarn_status kvarn_snapshot_bytes(const kvarn_cache* cache, size_t* bytes);
+kvarn_status kvarn_snapshot_save(kvarn_cache* cache, void* dst, size_t bytes, void* stream);
+kvarn_status kvarn_snapshot_load(kvarn_cache* cache, const void* src, size_t bytes, void* stream);
+
 /* Drop a sequence in every layer and return its pool slots. */
 kvarn_status kvarn_seq_release(kvarn_cache* cache, int32_t seq_id);
 

@@ -120,6 +120,25 @@ class KVarNCache:
     def length(self, layer, seq_id) -> int:
         return K.kvarn_seq_length(self.handle, layer, seq_id)
 
+    def snapshot(self, pinned: bool = True, stream=None) -> torch.Tensor:
+        """The cache's state as a host byte image (uint8 tensor, pinned by default)."""
+        n = K.kvarn_snapshot_bytes(self.handle)
+        buf = torch.empty(n, dtype=torch.uint8, pin_memory=pinned and self.mem.is_cuda)
+        K.kvarn_snapshot_save(self.handle, buf, n, self._stream(stream))
+        return buf
+
+    def restore(self, image, stream=None):
+        """Replace the cache's state by a host image from snapshot() (tensor or numpy array)."""
+        n = image.numel() if hasattr(image, "numel") else image.nbytes
+        K.kvarn_snapshot_load(self.handle, image, n, self._stream(stream))
+
+    def save(self, path, stream=None):
+        self.snapshot(pinned=False, stream=stream).numpy().tofile(path)
+
+    def load(self, path, stream=None):
+        import numpy as np
+        self.restore(np.fromfile(path, dtype=np.uint8), stream=stream)
+
     def release(self, seq_id):
         K.kvarn_seq_release(self.handle, seq_id)
 

@@ -19,6 +19,12 @@
 
 using namespace kvarn;
 
+namespace kvarn {
+// host-side copy helpers of the snapshot calls (kvarn_seal.cu)
+int memcpy_d2h_async(void* dst, const void* src, size_t bytes, void* stream);
+int stream_sync(void* stream);
+}  // namespace kvarn
+
 namespace {
 thread_local char g_last_error[256] = "";
 
@@ -462,6 +468,60 @@ kvarn_status run_prefill(kvarn_cache* c, int32_t layer, int32_t n_seqs, const in
     return KVARN_OK;
 }
 
+// ---- snapshot image: header, host bookkeeping, exact regions, used pool slots ----
+constexpr char kSnapMagic[8] = {'K', 'V', 'A', 'R', 'N', 'S', 'N', '1'};
+constexpr uint32_t kSnapVersion = 1;
+
+struct SnapHeader {
+    char magic[8];
+    uint32_t version;
+    uint32_t header_bytes;
+    kvarn_config cfg;
+    int32_t max_groups;
+    int32_t reserved;
+    uint64_t slot_bytes;
+    uint64_t sink_bytes;   // one of the sink K / sink V regions
+    uint64_t tail_bytes;   // one of the tail K / tail V regions
+    uint64_t n_used;       // pool slots in the image
+    uint64_t total_bytes;
+};
+
+struct SnapSizes {
+    size_t seq_layers, len_bytes, table_bytes, sink_bytes, tail_bytes, total;
+};
+
+SnapSizes snap_sizes(const kvarn_cache* c, uint64_t n_used) {
+    SnapSizes z{};
+    z.seq_layers = (size_t)c->cfg.max_seqs * c->cfg.num_layers;
+    z.len_bytes = z.seq_layers * sizeof(int64_t);
+    z.table_bytes = z.seq_layers * (size_t)c->max_groups * sizeof(int32_t);
+    z.sink_bytes = c->lay.sink_v - c->lay.sink_k;
+    z.tail_bytes = c->lay.tail_v - c->lay.tail_k;
+    z.total = sizeof(SnapHeader) + z.len_bytes + z.table_bytes + 2 * z.sink_bytes + 2 * z.tail_bytes +
+              (size_t)n_used * c->slot_bytes;
+    return z;
+}
+
+// Pool slots in use, ascending (every table entry of a sealed group).
+std::vector<int32_t> used_slots(const kvarn_cache* c) {
+    std::vector<int32_t> u;
+    for (int s = 0; s < c->cfg.max_seqs; ++s)
+        for (int l = 0; l < c->cfg.num_layers; ++l) {
+            const int64_t ng = groups_sealed(c->Lc(s, l), c->cfg.tail_floor);
+            for (int64_t g = 0; g < ng; ++g) u.push_back(c->Tc(s, l, (int)g));
+        }
+    std::sort(u.begin(), u.end());
+    return u;
+}
+
+bool same_config(const kvarn_config& a, const kvarn_config& b) {
+    return a.num_layers == b.num_layers && a.max_seqs == b.max_seqs && a.num_q_heads == b.num_q_heads &&
+           a.num_kv_heads == b.num_kv_heads && a.head_dim == b.head_dim && a.k_bits == b.k_bits &&
+           a.v_bits == b.v_bits && a.group_size == b.group_size && a.sink_tokens == b.sink_tokens &&
+           a.sinkhorn_iters == b.sinkhorn_iters && a.max_seq_len == b.max_seq_len &&
+           a.pool_groups == b.pool_groups && a.tail_floor == b.tail_floor;
+}
+
 }  // namespace
 
 extern "C" {
@@ -723,6 +783,136 @@ kvarn_status kvarn_dequant_group(kvarn_cache* c, int32_t layer, int32_t seq_id, 
     int rc = launch_dequant((const uint8_t*)rec, which ? c->cfg.v_bits : c->cfg.k_bits, which, frame, out_fp32 != 0,
                             out, stream);
     if (rc) { set_cuda_error(rc, "dequant launch"); return KVARN_ECUDA; }
+    return KVARN_OK;
+}
+
+kvarn_status kvarn_snapshot_bytes(const kvarn_cache* c, size_t* bytes) {
+    if (!c || !bytes) return KVARN_EINVAL;
+    *bytes = snap_sizes(c, used_slots(c).size()).total;
+    return KVARN_OK;
+}
+
+kvarn_status kvarn_snapshot_save(kvarn_cache* c, void* dst, size_t bytes, void* stream) {
+    if (!c || !dst) return KVARN_EINVAL;
+    const std::vector<int32_t> used = used_slots(c);
+    const SnapSizes z = snap_sizes(c, used.size());
+    if (bytes < z.total) return KVARN_EINVAL;
+    uint8_t* o = (uint8_t*)dst;
+    SnapHeader h;
+    std::memset(&h, 0, sizeof(h));
+    std::memcpy(h.magic, kSnapMagic, sizeof(h.magic));
+    h.version = kSnapVersion;
+    h.header_bytes = (uint32_t)sizeof(SnapHeader);
+    h.cfg = c->cfg;
+    h.max_groups = c->max_groups;
+    h.slot_bytes = c->slot_bytes;
+    h.sink_bytes = z.sink_bytes;
+    h.tail_bytes = z.tail_bytes;
+    h.n_used = used.size();
+    h.total_bytes = z.total;
+    std::memcpy(o, &h, sizeof(h));
+    size_t off = sizeof(h);
+    std::memcpy(o + off, c->len.data(), z.len_bytes);
+    off += z.len_bytes;
+    std::memcpy(o + off, c->table.data(), z.table_bytes);
+    off += z.table_bytes;
+    if (c->host_only) {
+        std::memset(o + off, 0, z.total - off);
+        return KVARN_OK;
+    }
+    kvarn_status st = ensure_init(c, stream);
+    if (st) return st;
+    const size_t regions[4] = {c->lay.sink_k, c->lay.sink_v, c->lay.tail_k, c->lay.tail_v};
+    const size_t sizes[4] = {z.sink_bytes, z.sink_bytes, z.tail_bytes, z.tail_bytes};
+    for (int i = 0; i < 4; ++i) {
+        int rc = memcpy_d2h_async(o + off, c->base + regions[i], sizes[i], stream);
+        if (rc) { set_cuda_error(rc, "snapshot copy"); return KVARN_ECUDA; }
+        off += sizes[i];
+    }
+    // used slots, runs of consecutive slots in one copy each
+    for (size_t i = 0; i < used.size();) {
+        size_t j = i + 1;
+        while (j < used.size() && used[j] == used[j - 1] + 1) ++j;
+        const size_t n = (j - i) * c->slot_bytes;
+        int rc = memcpy_d2h_async(o + off, c->base + c->lay.pool + (size_t)used[i] * c->slot_bytes, n, stream);
+        if (rc) { set_cuda_error(rc, "snapshot copy"); return KVARN_ECUDA; }
+        off += n;
+        i = j;
+    }
+    int rc = stream_sync(stream);
+    if (rc) { set_cuda_error(rc, "snapshot copy"); return KVARN_ECUDA; }
+    return KVARN_OK;
+}
+
+kvarn_status kvarn_snapshot_load(kvarn_cache* c, const void* src, size_t bytes, void* stream) {
+    if (!c || !src || bytes < sizeof(SnapHeader)) return KVARN_EINVAL;
+    const uint8_t* in = (const uint8_t*)src;
+    SnapHeader h;
+    std::memcpy(&h, in, sizeof(h));
+    if (std::memcmp(h.magic, kSnapMagic, sizeof(h.magic)) || h.version != kSnapVersion ||
+        h.header_bytes != sizeof(SnapHeader) || !same_config(h.cfg, c->cfg) || h.max_groups != c->max_groups ||
+        h.slot_bytes != c->slot_bytes)
+        return KVARN_EINVAL;
+    if (h.n_used > (uint64_t)c->cfg.pool_groups) return KVARN_EINVAL;
+    const SnapSizes z = snap_sizes(c, h.n_used);
+    if (h.sink_bytes != z.sink_bytes || h.tail_bytes != z.tail_bytes || h.total_bytes != z.total || bytes < z.total)
+        return KVARN_EINVAL;
+    // the bookkeeping, checked in full before anything changes
+    std::vector<int64_t> len(z.seq_layers);
+    std::vector<int32_t> table(z.table_bytes / sizeof(int32_t));
+    size_t off = sizeof(h);
+    std::memcpy(len.data(), in + off, z.len_bytes);
+    off += z.len_bytes;
+    std::memcpy(table.data(), in + off, z.table_bytes);
+    off += z.table_bytes;
+    std::vector<char> seen(c->cfg.pool_groups, 0);
+    std::vector<int32_t> used;
+    for (size_t sl = 0; sl < z.seq_layers; ++sl) {
+        if (len[sl] < 0 || len[sl] > c->cfg.max_seq_len) return KVARN_EINVAL;
+        const int64_t ng = groups_sealed(len[sl], c->cfg.tail_floor);
+        for (int g = 0; g < c->max_groups; ++g) {
+            const int32_t v = table[sl * c->max_groups + g];
+            if (g < ng) {
+                if (v < 0 || v >= c->cfg.pool_groups || seen[v]) return KVARN_EINVAL;
+                seen[v] = 1;
+                used.push_back(v);
+            } else if (v != -1) {
+                return KVARN_EINVAL;
+            }
+        }
+    }
+    if (used.size() != h.n_used) return KVARN_EINVAL;
+    std::sort(used.begin(), used.end());
+    if (!c->host_only) {
+        kvarn_status st = ensure_init(c, stream);
+        if (st) return st;
+        const size_t regions[4] = {c->lay.sink_k, c->lay.sink_v, c->lay.tail_k, c->lay.tail_v};
+        const size_t sizes[4] = {z.sink_bytes, z.sink_bytes, z.tail_bytes, z.tail_bytes};
+        size_t doff = off;
+        for (int i = 0; i < 4; ++i) {
+            int rc = memcpy_h2d_async(c->base + regions[i], in + doff, sizes[i], stream);
+            if (rc) { set_cuda_error(rc, "snapshot copy"); return KVARN_ECUDA; }
+            doff += sizes[i];
+        }
+        for (size_t i = 0; i < used.size();) {
+            size_t j = i + 1;
+            while (j < used.size() && used[j] == used[j - 1] + 1) ++j;
+            const size_t n = (j - i) * c->slot_bytes;
+            int rc = memcpy_h2d_async(c->base + c->lay.pool + (size_t)used[i] * c->slot_bytes, in + doff, n, stream);
+            if (rc) { set_cuda_error(rc, "snapshot copy"); return KVARN_ECUDA; }
+            doff += n;
+            i = j;
+        }
+        int rc = memcpy_h2d_async(c->base + c->lay.block_table, table.data(), z.table_bytes, stream);
+        if (rc == 0) rc = stream_sync(stream);  // `table` and the caller's image stay valid until here
+        if (rc) { set_cuda_error(rc, "snapshot copy"); return KVARN_ECUDA; }
+    }
+    c->len = std::move(len);
+    c->table = std::move(table);
+    // free slots in the order a fresh cache hands them out (lowest first)
+    c->free_slots.clear();
+    for (int i = c->cfg.pool_groups - 1; i >= 0; --i)
+        if (!seen[i]) c->free_slots.push_back(i);
     return KVARN_OK;
 }
 

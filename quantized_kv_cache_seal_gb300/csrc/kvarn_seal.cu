@@ -256,6 +256,12 @@ int memcpy_h2d_async(void* dst, const void* src, size_t bytes, void* stream) {
     return (int)cudaMemcpyAsync(dst, src, bytes, cudaMemcpyHostToDevice, (cudaStream_t)stream);
 }
 
+int memcpy_d2h_async(void* dst, const void* src, size_t bytes, void* stream) {
+    return (int)cudaMemcpyAsync(dst, src, bytes, cudaMemcpyDeviceToHost, (cudaStream_t)stream);
+}
+
+int stream_sync(void* stream) { return (int)cudaStreamSynchronize((cudaStream_t)stream); }
+
 int memcpy_d2h_sync(void* dst, const void* src, size_t bytes, void* stream) {
     cudaError_t e = cudaMemcpyAsync(dst, src, bytes, cudaMemcpyDeviceToHost, (cudaStream_t)stream);
     if (e == cudaSuccess) e = cudaStreamSynchronize((cudaStream_t)stream);

@@ -26,7 +26,7 @@ EXPORTS = [
     "kvarn_seq_release", "kvarn_seq_length", "kvarn_group_record", "kvarn_exact_regions",
     "kvarn_cache_stats", "kvarn_seal_groups", "kvarn_check_device_error", "kvarn_status_string",
     "kvarn_last_error", "kvarn_partition_units", "kvarn_device_accessible", "kvarn_prefill_attention",
-    "kvarn_prefill",
+    "kvarn_prefill", "kvarn_snapshot_bytes", "kvarn_snapshot_save", "kvarn_snapshot_load",
 ]
 
 
@@ -83,6 +83,9 @@ def load(build_if_missing: bool = True):
     L.kvarn_decode_step.argtypes = [P, I32, I32, IP, P, P, P, P, F, P]
     L.kvarn_prefill_attention.argtypes = [P, I32, I32, IP, IP, P, P, F, P]
     L.kvarn_prefill.argtypes = [P, I32, I32, IP, IP, P, P, P, P, F, P]
+    L.kvarn_snapshot_bytes.argtypes = [P, ctypes.POINTER(SZ)]
+    L.kvarn_snapshot_save.argtypes = [P, P, SZ, P]
+    L.kvarn_snapshot_load.argtypes = [P, P, SZ, P]
     L.kvarn_dequant_group.argtypes = [P, I32, I32, I32, I32, I32, I32, I32, P, P]
     L.kvarn_seq_release.argtypes = [P, I32]
     L.kvarn_seq_length.argtypes = [P, I32, I32, ctypes.POINTER(I64)]
@@ -199,6 +202,29 @@ def kvarn_prefill(handle, layer, seq_ids, n_tokens, k, v, q, out, softmax_scale,
 def kvarn_dequant_group(handle, layer, seq_id, group, kv_head, which, frame, out, out_fp32=True, stream=None):
     _check(load().kvarn_dequant_group(handle, layer, seq_id, group, kv_head, which, frame, int(bool(out_fp32)),
                                       _ptr(out), _stream(stream)), "kvarn_dequant_group")
+
+
+def _host_ptr(buf) -> int:
+    """Address of a host buffer: a numpy array, a (CPU, possibly pinned) torch tensor or an int."""
+    if isinstance(buf, int):
+        return buf
+    if hasattr(buf, "data_ptr"):
+        return buf.data_ptr()
+    return buf.ctypes.data
+
+
+def kvarn_snapshot_bytes(handle) -> int:
+    n = ctypes.c_size_t()
+    _check(load().kvarn_snapshot_bytes(handle, ctypes.byref(n)), "kvarn_snapshot_bytes")
+    return n.value
+
+
+def kvarn_snapshot_save(handle, dst, nbytes, stream=None):
+    _check(load().kvarn_snapshot_save(handle, _host_ptr(dst), nbytes, _stream(stream)), "kvarn_snapshot_save")
+
+
+def kvarn_snapshot_load(handle, src, nbytes, stream=None):
+    _check(load().kvarn_snapshot_load(handle, _host_ptr(src), nbytes, _stream(stream)), "kvarn_snapshot_load")
 
 
 def kvarn_seq_release(handle, seq_id):

@@ -210,6 +210,81 @@ def test_prefill_argument_checks_and_fused_bookkeeping():
     assert K.kvarn_seq_length(h, 0, 2) == 0
 
 
+def _snapshot(h):
+    import numpy as np
+    n = K.kvarn_snapshot_bytes(h)
+    buf = np.zeros(n, np.uint8)
+    K.kvarn_snapshot_save(h, buf, n)
+    return buf
+
+
+def _state(h, cfg):
+    """Lengths, slots used and the record pointer offsets of every sealed group."""
+    lens = [[K.kvarn_seq_length(h, l, s) for s in range(cfg.max_seqs)] for l in range(cfg.num_layers)]
+    recs = []
+    for l in range(cfg.num_layers):
+        for s in range(cfg.max_seqs):
+            for g in range(max(lens[l][s] - 128, 0) // 128 - cfg.tail_floor):
+                recs.append(K.kvarn_group_record(h, l, s, g, 1, 1)[0] - FAKE)
+    return lens, K.kvarn_cache_stats(h).pool_slots_used, recs
+
+
+@pytest.mark.parametrize("floor", [0, 1])
+def test_snapshot_round_trip_of_the_bookkeeping(floor):
+    """A snapshot restored into a fresh cache of the same configuration reproduces the
+    lengths, the slots in use and every group's record address; later appends then seal
+    into the lowest free slots."""
+    h, cfg = host_cache(tail_floor=floor, pool_groups=64)
+    K.kvarn_append(h, 0, [0, 2], [700, 300], FAKE, FAKE)
+    K.kvarn_append(h, 1, [1], [1000], FAKE, FAKE)
+    for _ in range(130):
+        K.kvarn_decode_step(h, 0, [0, 2], FAKE, FAKE, FAKE, FAKE, 0.1)
+    K.kvarn_seq_release(h, 2)  # leaves holes in the pool
+    img = _snapshot(h)
+    assert img.size == K.kvarn_snapshot_bytes(h) and bytes(img[:8]) == b"KVARNSN1"
+    h2, _ = host_cache(tail_floor=floor, pool_groups=64)
+    K.kvarn_append(h2, 0, [3], [500], FAKE, FAKE)  # state that the load replaces
+    K.kvarn_snapshot_load(h2, img, img.size)
+    assert _state(h2, cfg) == _state(h, cfg)
+    used = K.kvarn_cache_stats(h2).pool_slots_used
+    taken = {K.kvarn_group_record(h2, l, s, g, 0, 0)[0] for l in range(2) for s in range(4)
+             for g in range(max(K.kvarn_seq_length(h2, l, s) - 128, 0) // 128 - floor)}
+    K.kvarn_append(h2, 1, [3], [128 + 128 * (floor + 1)], FAKE, FAKE)  # seals one group
+    new = K.kvarn_group_record(h2, 1, 3, 0, 0, 0)[0]
+    assert new not in taken and K.kvarn_cache_stats(h2).pool_slots_used == used + 1
+    assert _snapshot(h2).size == K.kvarn_snapshot_bytes(h2)
+
+
+def test_snapshot_rejects_bad_images_and_leaves_the_cache_unchanged():
+    import numpy as np
+    h, cfg = host_cache(pool_groups=32)
+    K.kvarn_append(h, 0, [0], [600], FAKE, FAKE)
+    img = _snapshot(h)
+    h2, _ = host_cache(pool_groups=32)
+    K.kvarn_append(h2, 0, [1], [300], FAKE, FAKE)
+    before = _state(h2, cfg)
+    bad = []
+    b = img.copy(); b[0] = ord("X"); bad.append(b)                       # magic
+    b = img.copy(); b[8] = 9; bad.append(b)                              # version
+    bad.append(img[:-1].copy())                                          # truncated
+    hdr = 16 + 4 * 14 + 8 + 5 * 8                                        # header bytes
+    lens = np.frombuffer(img[hdr:hdr + 8 * 8].tobytes(), np.int64).copy()
+    b = img.copy(); l2 = lens.copy(); l2[0] = 5000; b[hdr:hdr + 64] = np.frombuffer(l2.tobytes(), np.uint8); bad.append(b)
+    tab = hdr + 8 * 8
+    b = img.copy(); b[tab:tab + 4] = np.frombuffer(np.int32(99).tobytes(), np.uint8); bad.append(b)   # slot out of range
+    b = img.copy(); b[tab + 4:tab + 8] = b[tab:tab + 4]; bad.append(b)   # a slot used twice
+    for b in bad:
+        with pytest.raises(K.KVarNError) as e:
+            K.kvarn_snapshot_load(h2, b, b.size)
+        assert e.value.status == 1
+    assert _state(h2, cfg) == before
+    other, _ = host_cache(pool_groups=32, k_bits=4)                     # another configuration
+    with pytest.raises(K.KVarNError):
+        K.kvarn_snapshot_load(other, img, img.size)
+    K.kvarn_snapshot_load(h2, img, img.size)
+    assert _state(h2, cfg) == _state(h, cfg)
+
+
 def test_bits_per_element_formula():
     """Body bits/element = b + 528*8/16384 per side (fig1.dev: about 2.3 at two bits)."""
     for kb, vb in [(2, 2), (4, 2), (4, 4), (8, 8)]:
