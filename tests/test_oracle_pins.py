@@ -426,6 +426,24 @@ def test_prefill_attention_is_causal_and_matches_cache_helper():
     assert np.array_equal(out[:, 2:], ref)
 
 
+@pytest.mark.parametrize("floor", [0, 1])
+def test_prefill_last_query_equals_cache_attend(floor):
+    """At the cache level, with and without a tail floor: the newest token's prefill
+    query equals the decode-attention oracle over the same cache (the floor only moves
+    groups from the records to the exact tail, which both read)."""
+    src = workloads.TokenSource(13, 0, 2)
+    n = 128 + 128 * 3 + 17
+    k, v = src.tokens(0, n)
+    cache = oracle.OracleCache(2, 2, 2, tail_floor=floor)
+    cache.append(0, k, v)
+    q = RNG.standard_normal((3, 4, 128)).astype(np.float16)
+    scale = 1 / math.sqrt(128)
+    out = cache.prefill_attend(0, q, scale)
+    ref = cache.attend(0, q[-1], scale)
+    assert np.allclose(out[-1], ref, atol=1e-11, rtol=1e-11)
+    assert cache.regions(0)[1] == 3 - floor
+
+
 # --------------------------------------------------------------------------- regions
 def test_cache_regions_and_seal_timing():
     """anbeeld.com 2.1: sink = first 128 tokens; a group seals exactly when its 128th
