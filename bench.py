@@ -168,6 +168,24 @@ def measured_hbm_peak():
         return 6800.0, "fallback"
 
 
+def max_over_ranks(ms, pg=None, device=None):
+    """The slowest rank's time for the timed region (every rank gets it); the identity
+    on one rank. pg: torch.distributed (initialised) or None."""
+    if pg is None:
+        return float(ms)
+    import torch
+
+    t = torch.tensor([float(ms)], dtype=torch.float64, device=device)
+    pg.all_reduce(t, op=pg.ReduceOp.MAX)
+    return float(t.item())
+
+
+def whole_job_rate(units_per_rank, world, ms):
+    """Units all ranks processed (each rank a replica of the workload: weak scaling)
+    per second of the slowest rank's time."""
+    return units_per_rank * world / (ms / 1e3)
+
+
 def dist_info():
     rank = int(os.environ.get("RANK", "0"))
     world = int(os.environ.get("WORLD_SIZE", "1"))
@@ -375,15 +393,11 @@ def run_ours(args):
                 e1.record(stream)
                 t_host = time.perf_counter() - t_host
                 barrier()
-                ems = e0.elapsed_time(e1)
-                if pg is not None:
-                    t = torch.tensor([ems], dtype=torch.float64, device=device)
-                    pg.all_reduce(t, op=pg.ReduceOp.MAX)
-                    ems = float(t.item())
+                ems = max_over_ranks(e0.elapsed_time(e1), pg, device)
                 return ems, t_host
 
             def entry(ems, path):
-                return {"value": BATCH * world * K_ / (ems / 1e3), "unit": "tokens/s", "h2d_bytes_per_step": h2d,
+                return {"value": whole_job_rate(BATCH * K_, world, ems), "unit": "tokens/s", "h2d_bytes_per_step": h2d,
                         "d2h_bytes_per_step": d2h, "path": path}
 
             # (1) kernels on the pinned host buffers
@@ -481,13 +495,9 @@ def run_ours(args):
         raise RuntimeError(f"device error word: {err}")
     order = sorted(range(len(rep_ms)), key=lambda i: rep_ms[i])
     mid = order[len(order) // 2]
-    ms = rep_ms[mid]
-    if pg is not None:
-        t = torch.tensor([ms], dtype=torch.float64, device=device)
-        pg.all_reduce(t, op=pg.ReduceOp.MAX)
-        ms = float(t.item())
+    ms = max_over_ranks(rep_ms[mid], pg, device)
     ms_per_step = ms / K_
-    value = BATCH * world * K_ / (ms / 1e3)
+    value = whole_job_rate(BATCH * K_, world, ms)
     launch_us = ms_per_step * 1e3
     alg_bytes = rep_bytes[mid] / K_
     achieved = alg_bytes / (launch_us * 1e-6) / 1e9
