@@ -795,6 +795,7 @@ kvarn_status kvarn_snapshot_bytes(const kvarn_cache* c, size_t* bytes) {
 kvarn_status kvarn_snapshot_save(kvarn_cache* c, void* dst, size_t bytes, void* stream) {
     if (!c || !dst) return KVARN_EINVAL;
     const std::vector<int32_t> used = used_slots(c);
+    if (!used.empty() && (used.front() < 0 || used.back() >= c->cfg.pool_groups)) return KVARN_ESTATE;
     const SnapSizes z = snap_sizes(c, used.size());
     if (bytes < z.total) return KVARN_EINVAL;
     uint8_t* o = (uint8_t*)dst;
