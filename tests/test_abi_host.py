@@ -210,6 +210,19 @@ def test_prefill_argument_checks_and_fused_bookkeeping():
     assert K.kvarn_seq_length(h, 0, 2) == 0
 
 
+def test_prefill_batch_limit():
+    """Up to 256 sequences per prefill call (the kernel parameter table); one more is a
+    capacity error, not a launch."""
+    h, _ = host_cache(max_seqs=300, num_layers=1, max_seq_len=256, pool_groups=8)
+    ids = list(range(256))
+    K.kvarn_append(h, 0, ids, [3] * 256, FAKE, FAKE)
+    K.kvarn_prefill_attention(h, 0, ids, [3] * 256, FAKE, FAKE, 0.1)
+    K.kvarn_append(h, 0, [256], [2], FAKE, FAKE)
+    with pytest.raises(K.KVarNError) as e:
+        K.kvarn_prefill_attention(h, 0, ids + [256], [1] * 257, FAKE, FAKE, 0.1)
+    assert e.value.status == 3
+
+
 def _snapshot(h):
     import numpy as np
     n = K.kvarn_snapshot_bytes(h)
