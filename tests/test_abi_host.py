@@ -309,3 +309,27 @@ def test_bits_per_element_formula():
         elems = (128 + 1280) * 2 * 128 * 2
         expect = (10 * 2 * (K.kvarn_record_bytes(kb) + K.kvarn_record_bytes(vb)) + 128 * 2 * 128 * 2 * 2) * 8 / elems
         assert abs(s.all_in_bits_per_element - expect) < 1e-9
+
+
+def test_bench_step_bytes_matches_the_cache_accounting():
+    """The roofline numerator of bench.py (algorithmic bytes of one decode step) equals
+    an independent count from the library's own accounting after the step: every sealed
+    record and exact fp16 token read, q read and out written, the new token written, and
+    for a sealing sequence its 127 older group tokens read and the new records written."""
+    import sys
+    sys.path.insert(0, ROOT)
+    import bench
+
+    lengths = [300, 383, 511, 1000, 127, 128, 255, 4096 + 127]
+    h, _ = host_cache(max_seqs=len(lengths), num_layers=1, num_q_heads=bench.HQ, num_kv_heads=bench.HKV,
+                      k_bits=bench.KB, v_bits=bench.VB, max_seq_len=8192, pool_groups=256)
+    ids = list(range(len(lengths)))
+    K.kvarn_append(h, 0, ids, lengths, FAKE, FAKE)
+    K.kvarn_decode_step(h, 0, ids, FAKE, FAKE, FAKE, FAKE, 0.1)
+    st = K.kvarn_cache_stats(h)
+    sealing = sum(1 for n in lengths if n >= 128 and (n + 1 - 128) % 128 == 0)
+    assert sealing == 4
+    pair = st.record_bytes_k + st.record_bytes_v
+    expected = (st.sealed_bytes + st.exact_bytes + len(lengths) * (bench.HQ * 512 + bench.HKV * 512)
+                + sealing * bench.HKV * (127 * 512 + pair))
+    assert bench.step_bytes(lengths) == expected
