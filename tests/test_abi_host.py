@@ -311,7 +311,8 @@ def test_bits_per_element_formula():
         assert abs(s.all_in_bits_per_element - expect) < 1e-9
 
 
-def test_bench_step_bytes_matches_the_cache_accounting():
+@pytest.mark.parametrize("floor", [0, 1])
+def test_bench_step_bytes_matches_the_cache_accounting(floor, monkeypatch):
     """The roofline numerator of bench.py (algorithmic bytes of one decode step) equals
     an independent count from the library's own accounting after the step: every sealed
     record and exact fp16 token read, q read and out written, the new token written, and
@@ -320,16 +321,21 @@ def test_bench_step_bytes_matches_the_cache_accounting():
     sys.path.insert(0, ROOT)
     import bench
 
+    monkeypatch.setattr(bench, "FLOOR", floor)
     lengths = [300, 383, 511, 1000, 127, 128, 255, 4096 + 127]
     h, _ = host_cache(max_seqs=len(lengths), num_layers=1, num_q_heads=bench.HQ, num_kv_heads=bench.HKV,
-                      k_bits=bench.KB, v_bits=bench.VB, max_seq_len=8192, pool_groups=256)
+                      k_bits=bench.KB, v_bits=bench.VB, max_seq_len=8192, pool_groups=256, tail_floor=floor)
     ids = list(range(len(lengths)))
     K.kvarn_append(h, 0, ids, lengths, FAKE, FAKE)
+    used = K.kvarn_cache_stats(h).pool_slots_used
     K.kvarn_decode_step(h, 0, ids, FAKE, FAKE, FAKE, FAKE, 0.1)
     st = K.kvarn_cache_stats(h)
-    sealing = sum(1 for n in lengths if n >= 128 and (n + 1 - 128) % 128 == 0)
-    assert sealing == 4
+    sealing = st.pool_slots_used - used  # groups sealed by the step
+    assert sealing == (4 if floor == 0 else 3)
     pair = st.record_bytes_k + st.record_bytes_v
+    # a sealing step reads the group's tokens from the tail: 127 and the new one without a
+    # floor, all 128 with one
+    tail_read = 127 if floor == 0 else 128
     expected = (st.sealed_bytes + st.exact_bytes + len(lengths) * (bench.HQ * 512 + bench.HKV * 512)
-                + sealing * bench.HKV * (127 * 512 + pair))
+                + sealing * bench.HKV * (tail_read * 512 + pair))
     assert bench.step_bytes(lengths) == expected
