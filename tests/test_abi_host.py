@@ -339,3 +339,32 @@ def test_bench_step_bytes_matches_the_cache_accounting(floor, monkeypatch):
     expected = (st.sealed_bytes + st.exact_bytes + len(lengths) * (bench.HQ * 512 + bench.HKV * 512)
                 + sealing * bench.HKV * (tail_read * 512 + pair))
     assert bench.step_bytes(lengths) == expected
+
+
+def test_every_entry_point_rejects_a_null_cache_handle():
+    import ctypes
+    L = K.load()
+    I = ctypes.c_int32
+    ids, cnt = (I * 1)(0), (I * 1)(1)
+    ptr, size, n64 = ctypes.c_void_p(), ctypes.c_size_t(), ctypes.c_int64()
+    calls = {
+        "kvarn_append": lambda: L.kvarn_append(None, 0, 1, ids, cnt, FAKE, FAKE, None),
+        "kvarn_decode_attention": lambda: L.kvarn_decode_attention(None, 0, 1, ids, FAKE, FAKE, 0.1, None),
+        "kvarn_decode_attention_noalloc": lambda: L.kvarn_decode_attention_noalloc(None, 0, 1, ids, FAKE, FAKE, 0.1,
+                                                                                   None),
+        "kvarn_decode_step": lambda: L.kvarn_decode_step(None, 0, 1, ids, FAKE, FAKE, FAKE, FAKE, 0.1, None),
+        "kvarn_prefill_attention": lambda: L.kvarn_prefill_attention(None, 0, 1, ids, cnt, FAKE, FAKE, 0.1, None),
+        "kvarn_prefill": lambda: L.kvarn_prefill(None, 0, 1, ids, cnt, FAKE, FAKE, FAKE, FAKE, 0.1, None),
+        "kvarn_dequant_group": lambda: L.kvarn_dequant_group(None, 0, 0, 0, 0, 0, 0, 1, FAKE, None),
+        "kvarn_seq_release": lambda: L.kvarn_seq_release(None, 0),
+        "kvarn_seq_length": lambda: L.kvarn_seq_length(None, 0, 0, ctypes.byref(n64)),
+        "kvarn_group_record": lambda: L.kvarn_group_record(None, 0, 0, 0, 0, 0, ctypes.byref(ptr), ctypes.byref(size)),
+        "kvarn_exact_regions": lambda: L.kvarn_exact_regions(None, 0, 0, *[ctypes.byref(ptr)] * 4),
+        "kvarn_cache_stats": lambda: L.kvarn_cache_stats(None, ctypes.byref(K.kvarn_stats())),
+        "kvarn_check_device_error": lambda: L.kvarn_check_device_error(None, None),
+        "kvarn_snapshot_bytes": lambda: L.kvarn_snapshot_bytes(None, ctypes.byref(size)),
+        "kvarn_snapshot_save": lambda: L.kvarn_snapshot_save(None, FAKE, 1000, None),
+        "kvarn_snapshot_load": lambda: L.kvarn_snapshot_load(None, FAKE, 1000, None),
+    }
+    for name, call in calls.items():
+        assert call() == 1, name
