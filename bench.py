@@ -258,7 +258,7 @@ def snapshot_leg(cache):
 PF_HQ, PF_HKV, PF_N = 32, 8, 4096  # prefill leg: Qwen3-4B attention shape, one 4096-token prompt
 
 
-def prefill_leg(torch, device, stream, barrier, reps=5):
+def prefill_leg(torch, device, stream, barrier, reps=5, cpu=False):
     """Prompt prefill: kvarn_prefill (bulk append of 4096 tokens, sealing 31 groups per
     KV head and side, then causal many-query attention of all 4096 queries). Each rep
     starts from an empty sequence; L2 is flushed (a 256 MiB write) before each timed call.
@@ -310,6 +310,8 @@ def prefill_leg(torch, device, stream, barrier, reps=5):
                      if FLOOR == 0 and (KB, VB) == (2, 2) else None, "peak_kind": kind, "kernel": f"prefill_kernel<{KB},{VB}>",
                      "alg_flops_per_launch": flops, "launch_us": a_ms * 1e3},
         "gpu_launches_per_prefill": 3,  # seal_jobs_kernel, append_kernel, prefill_kernel
+        "cpu_baseline": prefill_cpu_baseline(k.cpu().numpy(), v.cpu().numpy(), q.cpu().numpy(),
+                                             positions_sample=256) if cpu else None,
     }
 
 
@@ -542,7 +544,8 @@ def run_ours(args):
         seal_gps = n / (s0.elapsed_time(s1) / 1e3) * world
         del x
 
-    prefill = None if args.no_prefill else prefill_leg(torch, device, stream, barrier)
+    prefill = None if args.no_prefill else prefill_leg(
+        torch, device, stream, barrier, cpu=rank == 0 and world == 1 and not args.no_cpu_baseline)
     snapshot = None if args.no_snapshot or world > 1 else snapshot_leg(cache)
 
     result = {
@@ -639,6 +642,48 @@ def cpu_baseline(cache, lengths, s_now, q_all, n_pairs):
             "sample": f"decode attention of {len(pairs)} of {BATCH * HKV} (sequence, KV head) pairs at ~32k "
                       f"context over the cache's records, scaled to the whole step; seal: {len(xs)} group matrices",
             "seal_groups_per_s": seal_gps}
+
+
+def prefill_cpu_baseline(k, v, q, positions_sample=64, head=0):
+    """The oracle's prefill attention, as it stands, on this host's cores, on a bounded
+    sample of the prompt-prefill leg: one KV head's cache built by the oracle from the
+    same tokens (k, v: [n][Hkv][128] fp16 numpy), then the queries of `positions_sample`
+    positions spread over the prompt (its r query heads), timed and scaled by the causal
+    work (sum over queries of the keys each sees) to the whole prompt and all heads.
+    Returns the cpu_baseline object (prompt tokens/s)."""
+    import concurrent.futures
+
+    import oracle
+
+    oracle.build()
+    n, hkv = k.shape[0], k.shape[1]
+    hq = q.shape[1]
+    r = hq // hkv
+    oc = oracle.OracleCache(1, KB, VB, tail_floor=FLOOR)
+    oc.append(0, k[:, head:head + 1], v[:, head:head + 1])  # untimed setup (the oracle's seals)
+    st = oc.seqs[0]
+    n_sink, n_groups, _ = oc.regions(0)
+    kr = np.stack([g[0] for g in st["krec"]]) if n_groups else np.zeros((0,), np.uint8)
+    vr = np.stack([g[0] for g in st["vrec"]]) if n_groups else np.zeros((0,), np.uint8)
+    tk, tv = oc.tail(0)
+    pos = sorted({int(x) for x in np.linspace(0, n - 1, positions_sample)})
+    cores = os.cpu_count() or 1
+    chunks = [pos[i::cores] for i in range(min(cores, len(pos)))]
+
+    def run(ps):
+        oracle.prefill_attention(q[ps, head * r:(head + 1) * r], ps, 1.0 / math.sqrt(128), st["sink_k"][:n_sink, 0],
+                                 st["sink_v"][:n_sink, 0], kr, vr, tk[:, 0], tv[:, 0], KB, VB)
+
+    t0 = time.perf_counter()
+    with concurrent.futures.ThreadPoolExecutor(max_workers=len(chunks)) as ex:
+        list(ex.map(run, chunks))
+    t = time.perf_counter() - t0
+    work_sample = sum(p + 1 for p in pos) * r
+    work_all = (n * (n + 1) // 2) * hq
+    prompt_s = t * work_all / work_sample
+    return {"value": n / prompt_s, "unit": "prompt tokens/s", "cores": len(chunks), "kind": "oracle",
+            "sample": f"{len(pos)} query positions x {r} query heads of KV head {head}, scaled by causal work "
+                      f"to {n} positions x {hq} heads (the oracle's seals of the prompt are untimed setup)"}
 
 
 def run_reference(args):

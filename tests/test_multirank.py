@@ -66,3 +66,20 @@ def test_reference_arm_does_no_work_off_rank_zero():
                         "--warmup", "3"], env=env, capture_output=True, text=True, timeout=120)
     assert r.returncode == 0
     assert r.stdout.strip() == ""
+
+
+def test_prefill_cpu_baseline_runs_on_a_small_prompt():
+    """The prefill leg's CPU baseline (the oracle on host cores, sampled, scaled by the
+    causal work) on a small prompt: one object of the bench contract's cpu_baseline form."""
+    import numpy as np
+
+    sys.path.insert(0, ROOT)
+    import bench
+
+    rng = np.random.default_rng(0)
+    n = 128 + 128 * 2 + 40
+    k = rng.standard_normal((n, 2, 128)).astype(np.float16)
+    v = rng.standard_normal((n, 2, 128)).astype(np.float16)
+    q = rng.standard_normal((n, 8, 128)).astype(np.float16)
+    r = bench.prefill_cpu_baseline(k, v, q, positions_sample=16, head=1)
+    assert r["kind"] == "oracle" and r["unit"] == "prompt tokens/s" and r["value"] > 0 and r["cores"] >= 1
