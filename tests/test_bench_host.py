@@ -1,9 +1,11 @@
-"""The N > 1 path of the benchmark on CPU, as world-size-2 gloo process groups.
+"""Host-side logic of the benchmark, on CPU.
 
-The path has no exchange step (every (sequence, KV head) block is independent), so N
-GPUs run N replicas of the workload; the only collective is the maximum of the timed
-region over the ranks, and the reported value is the units all ranks processed per
-second of that slowest time (weak scaling). The reference arm runs on rank 0 alone.
+The N > 1 path as world-size-2 gloo process groups: the path has no exchange step
+(every (sequence, KV head) block is independent), so N GPUs run N replicas of the
+workload; the only collective is the maximum of the timed region over the ranks, and
+the reported value is the units all ranks processed per second of that slowest time
+(weak scaling). The reference arm runs on rank 0 alone. And the prefill leg's CPU
+baseline on a small prompt.
 """
 import json
 import os
