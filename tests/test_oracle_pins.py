@@ -187,6 +187,57 @@ def test_quantisation_half_step_bound_and_brute_force(bits):
     assert np.all(dist_own <= dist_best + 1e-12 * delta)
 
 
+def test_codes_for_grid_hand_worked_golden(golden_dir):
+    """Codes for a grid that is not the matrix's own: clamping at both ends, ties to
+    even, a zero scale product, token scales per row and channel scales per column
+    (hand-worked values in tests/golden/codes_for_grid.json)."""
+    g = json.load(open(os.path.join(golden_dir, "codes_for_grid.json")))
+    codes, t = oracle.codes_for_grid(np.array(g["Y"]), g["bits"], np.array(g["a16"]), np.array(g["c16"]),
+                                     g["m"], g["delta"])
+    assert t.tolist() == g["t"]
+    assert codes.tolist() == g["codes"]
+
+
+@pytest.mark.parametrize("bits", [2, 3, 4, 5, 6, 7, 8])
+def test_codes_for_grid_reproduces_quantize_on_its_own_grid(bits):
+    """Given the stored scales and the grid that kvo_quantize chose, the per-grid
+    re-derivation returns exactly kvo_quantize's codes and t (several seeds, K- and
+    V-like matrices, T != d so that a row/column swap of the scales cannot pass)."""
+    for seed in range(3):
+        x = workloads.group_matrices(40 + 7 * bits + seed, 1)[0]
+        Y = oracle.rotate(x.astype(np.float64))[:96]  # 96 tokens x 128 channels
+        rng = np.random.default_rng(seed)
+        a16 = rng.lognormal(0.0, 0.7, Y.shape[0]).astype(np.float16).astype(np.float64)
+        c16 = rng.lognormal(0.0, 0.5, Y.shape[1]).astype(np.float16).astype(np.float64)
+        delta, m, codes_q, t_q = oracle.quantize(Y, bits, a16, c16)
+        codes_g, t_g = oracle.codes_for_grid(Y, bits, a16, c16, m, delta)
+        assert np.array_equal(t_g, t_q)
+        assert np.array_equal(codes_g, codes_q)
+
+
+@pytest.mark.parametrize("bits", [2, 3, 4, 8])
+def test_codes_for_grid_is_the_nearest_clamped_grid_point(bits):
+    """Brute force: on a grid narrower than the data (values below m and above
+    m + L delta), each code is the nearest of the 2^b grid points m + q delta, found by
+    exhaustive search over q; values off the grid take code 0 or L."""
+    rng = np.random.default_rng(100 + bits)
+    T, d = 24, 40
+    a16 = rng.lognormal(0.0, 0.5, T).astype(np.float16).astype(np.float64)
+    c16 = rng.lognormal(0.0, 0.5, d).astype(np.float16).astype(np.float64)
+    Z = rng.uniform(-1.5, 1.5, (T, d))
+    Y = Z * np.outer(a16, c16)
+    L = 2 ** bits - 1
+    m = float(np.float32(-1.0))
+    delta = float(np.float32(2.0 / L))  # grid spans [-1, 1]; the data spans [-1.5, 1.5]
+    codes, t = oracle.codes_for_grid(Y, bits, a16, c16, m, delta)
+    z = Y / np.outer(a16, c16)
+    grid = m + delta * np.arange(L + 1)
+    nearest = np.argmin(np.abs(z[..., None] - grid), axis=-1)
+    assert np.array_equal(codes, nearest)
+    assert np.all(codes[z < m] == 0) and np.all(codes[z > m + L * delta] == L)
+    assert (z < m).any() and (z > m + L * delta).any()
+
+
 def test_tiny_seal_brute_force():
     """T=4, d=4: the seal equals a step-by-step restatement using numpy and scipy
     (library Hadamard, float16 casts, explicit loops), independent of the C code."""
