@@ -203,7 +203,9 @@ kvarn_status kvarn_prefill(kvarn_cache* cache, int32_t layer, int32_t n_seqs, co
  * 32 partial states, 8.7 MB per GPU, kept until the process exits); a larger cache is
  * rejected with KVARN_ECAPACITY and a message in kvarn_last_error.
  * The first call on a device looks up the array's device address (cudaGetSymbolAddress,
- * with that device current); make that first call before any stream capture.
+ * with that device current); make that first call before any stream capture. The
+ * current device must be the one that holds the cache (EINVAL otherwise): each device
+ * has its own copy of the array.
  * Every call reuses the partial states left by the previous call (each call tags its own
  * with a fresh epoch), so calls that overlap on the GPU (other streams, other caches,
  * other threads) race: order them on one stream. */
@@ -284,7 +286,11 @@ kvarn_status kvarn_partition_units(int32_t n_blocks, const int32_t* units, const
                                    int32_t max_span, int32_t min_load, int32_t* cuts, int32_t* n_ctas);
 
 /* Read and clear the device error word of the cache (synchronises `stream`).
- * KVARN_OK, or KVARN_ETIMEOUT if a bounded wait in a kernel gave up. */
+ * KVARN_OK; KVARN_ETIMEOUT if a bounded wait in a kernel gave up; KVARN_ESTATE for any
+ * other recorded fault: a block-table entry out of range, a block split over too many
+ * CTAs, or a split-K partial that the merge needed but that carried another call's
+ * epoch (overlapping calls on the shared workspace of kvarn_decode_attention_noalloc);
+ * such a partial is left out of the output instead of being mixed in. */
 kvarn_status kvarn_check_device_error(kvarn_cache* cache, void* stream);
 
 /* *accessible = 1 if kernels can dereference ptr as given: device or managed memory, or

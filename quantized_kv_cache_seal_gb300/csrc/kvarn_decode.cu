@@ -259,7 +259,7 @@ struct Smem {
 };
 
 __device__ __forceinline__ float* partial_ptr(const DecodeParams& p, int blk, int slot) {
-    return reinterpret_cast<float*>(p.base + p.lay.partials) + ((size_t)blk * kPartialSlots + slot) * kPartialFloats;
+    return p.partials + ((size_t)blk * kPartialSlots + slot) * kPartialFloats;
 }
 
 __device__ __forceinline__ int32_t* err_word(const DecodeParams& p) {
@@ -1376,6 +1376,7 @@ __global__ void __launch_bounds__(128) merge_kernel(const __grid_constant__ Deco
     // partials four at a time, every load of a round issued before any is used, combined
     // with the running maximum, sum and accumulator
     float M = kNegInf, L = 0.f, v[4] = {0.f, 0.f, 0.f, 0.f};
+    bool stale = false;
     for (int s0 = 0; s0 < nsl; s0 += 4) {
         float ms[4], ls[4];
         float4 a[4];
@@ -1388,9 +1389,13 @@ __global__ void __launch_bounds__(128) merge_kernel(const __grid_constant__ Deco
                 const float* P = partial_ptr(p, blk, s0 + k);
                 const bool ok = (uint32_t)__float_as_int(__ldcg(P)) == p.epoch;
                 const float m = __ldcg(P + 4 + h), l = __ldcg(P + 8 + h);
-                a[k] = __ldcg(reinterpret_cast<const float4*>(P + 12 + 128 * h) + lane);
+                const float4 av = __ldcg(reinterpret_cast<const float4*>(P + 12 + 128 * h) + lane);
+                // a partial of another call (missing or overwritten) enters as nothing and
+                // is reported; what its slot holds never reaches the sums
                 ms[k] = ok ? m : kNegInf;
-                ls[k] = l;
+                ls[k] = ok ? l : 0.f;
+                a[k] = ok ? av : make_float4(0.f, 0.f, 0.f, 0.f);
+                stale |= !ok;
             }
         }
         float Mn = M;
@@ -1412,6 +1417,7 @@ __global__ void __launch_bounds__(128) merge_kernel(const __grid_constant__ Deco
         }
         M = Mn;
     }
+    if (stale && lane == 0) atomicOr(err_word(p), kErrStalePartial);
     warp_fwht128(v, lane);
     const float inv = L > 0.f ? 1.0f / L : 0.f;
     uint2 o;

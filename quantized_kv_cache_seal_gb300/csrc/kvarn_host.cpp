@@ -67,6 +67,7 @@ struct kvarn_cache {
     bool host_only = false;
     bool test_stall = false;
     int tail_cap = kGroup;  // rows of the tail ring per (sequence, layer, KV head)
+    int device = -1;        // CUDA device holding the block (set at create unless host-only)
 
     int64_t& L(int seq, int layer) { return len[(size_t)seq * cfg.num_layers + layer]; }
     int64_t Lc(int seq, int layer) const { return len[(size_t)seq * cfg.num_layers + layer]; }
@@ -368,10 +369,10 @@ kvarn_status run_decode(kvarn_cache* c, int32_t layer, int32_t n_seqs, const int
     if (stages >= 8) stages &= ~3;
     p.stages = stages;
     if (ws) {
-        // offsets from the cache base that land on the static workspace (modulo 2^64)
-        p.lay.partials = (size_t)((uintptr_t)ws->partials - (uintptr_t)c->base);
+        p.partials = (float*)ws->partials;
         p.epoch = ws->epoch;
     } else {
+        p.partials = (float*)(c->base + c->lay.partials);
         p.epoch = ++c->epoch;
     }
     if (!c->host_only) {
@@ -583,7 +584,8 @@ kvarn_status kvarn_cache_create(const kvarn_config* cfg, void* dev_mem, size_t b
     if (!c->host_only) {
         c->sms = sm_count();
         c->max_smem = max_optin_smem();
-        if (c->sms <= 0 || c->max_smem <= 0) {
+        if (pointer_device(dev_mem, &c->device)) c->device = -1;
+        if (c->sms <= 0 || c->max_smem <= 0 || c->device < 0) {
             std::snprintf(g_last_error, sizeof(g_last_error), "no CUDA device");
             delete c;
             return KVARN_ECUDA;
@@ -734,8 +736,17 @@ kvarn_status kvarn_decode_attention_noalloc(kvarn_cache* c, int32_t layer, int32
         return KVARN_ECAPACITY;
     }
     if (c->host_only) return KVARN_EINVAL;
+    // the array used is the current device's: it must be the device that holds the cache
+    int cur = -1;
+    int rc = current_device(&cur);
+    if (rc) { set_cuda_error(rc, "current device"); return KVARN_ECUDA; }
+    if (cur != c->device) {
+        std::snprintf(g_last_error, sizeof(g_last_error),
+                      "the current device (%d) is not the cache's device (%d)", cur, c->device);
+        return KVARN_EINVAL;
+    }
     WorkspaceOverride ws{};
-    int rc = static_workspace(&ws.partials);
+    rc = static_workspace(&ws.partials);
     if (rc) { set_cuda_error(rc, "static workspace address"); return KVARN_ECUDA; }
     kvarn_status st = check_ids(c, layer, n_seqs, seq_ids);
     if (st) return st;

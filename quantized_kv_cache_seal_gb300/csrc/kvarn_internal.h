@@ -31,6 +31,7 @@ constexpr int kPrefillRows = 128;     // query rows (token, head) of a prefill C
 constexpr int kErrTimeout = 1;
 constexpr int kErrBadSlot = 2;
 constexpr int kErrSpan = 4;
+constexpr int kErrStalePartial = 8;  // a partial the merge needed carried another call's epoch
 
 KVARN_HD inline size_t record_bytes(int bits) { return 528 + 2048 * (size_t)bits; }
 
@@ -68,6 +69,7 @@ struct SeqEntry {
 struct DecodeParams {
     uint8_t* base;              // cache device block
     Layout lay;
+    float* partials;            // split-K partial states: the cache's own region or the static workspace
     const uint16_t* q;          // [n][Hq][128]
     uint16_t* out;              // [n][Hq][128]
     const uint16_t* k_new;      // [n][Hkv][128] or null
@@ -166,6 +168,8 @@ int max_optin_smem();
 int sm_count();
 const char* cuda_error_string(int code);
 int pointer_device_accessible(const void* ptr, int* accessible);  // 0 or a cudaError_t value
+int current_device(int* device);                        // 0 or a cudaError_t value
+int pointer_device(const void* ptr, int* device);       // device holding ptr (else the current one)
 int memcpy_h2d_async(void* dst, const void* src, size_t bytes, void* stream);
 int memcpy_d2h_sync(void* dst, const void* src, size_t bytes, void* stream);
 // static split-K workspace for the allocation-free decode call (kvarn_decode.cu)

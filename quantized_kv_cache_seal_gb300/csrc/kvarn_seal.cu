@@ -238,6 +238,19 @@ int max_optin_smem() {
 
 const char* cuda_error_string(int code) { return cudaGetErrorString((cudaError_t)code); }
 
+int current_device(int* device) { return (int)cudaGetDevice(device); }
+
+int pointer_device(const void* ptr, int* device) {
+    cudaPointerAttributes a;
+    cudaError_t e = cudaPointerGetAttributes(&a, ptr);
+    if (e != cudaSuccess || a.type != cudaMemoryTypeDevice) {
+        cudaGetLastError();  // not a device allocation this runtime knows: take the current device
+        return (int)cudaGetDevice(device);
+    }
+    *device = a.device;
+    return 0;
+}
+
 int pointer_device_accessible(const void* ptr, int* accessible) {
     *accessible = 0;
     cudaPointerAttributes a;
