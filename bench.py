@@ -10,11 +10,19 @@ Workload (default): Llama-3.1-8B attention shape -- 32 query heads, 8 KV heads,
 head_dim 128 -- batch 16, context 32768 + U{0..127} tail tokens per sequence, 2-bit K
 and V. Synthetic data (seeded), generated on the device.
 
-Beside it, the line carries the bulk-seal rate and a prompt-prefill leg: Qwen3-4B
-attention shape (32 query heads, 8 KV heads), one 4096-token prompt through
-kvarn_prefill (bulk append sealing 31 groups per KV head and side, then causal
-attention of all 4096 queries over the cache), with the tensor roofline of the
-attention kernel.
+Beside it, the line carries:
+- the bulk-seal rate and its FP32 roofline (`seal_roofline`), and the share of step time
+  the staggered fused seals take (`seal_share`, from a back-to-back run in which every
+  sequence seals several times);
+- the other decode workloads (`workloads`): Qwen3-4B attention shape at 4k for its 256
+  steps, the 64k long-reasoning shape at K4/V2 and K4/V4 for its 2048 steps, and the
+  ragged Phi-4-14B shape (batch 64, 1k-16k, norm spikes) at 2, 4 and 8 bits, each
+  through the same decode-step loop;
+- a prompt-prefill leg: Qwen3-4B attention shape (32 query heads, 8 KV heads), one
+  4096-token prompt through kvarn_prefill (bulk append sealing 31 groups per KV head and
+  side, then causal attention of all 4096 queries over the cache), with the tensor
+  roofline of the attention kernel;
+- the oracle on the host cores (`cpu_baseline`, all cores and one thread).
 
   python bench.py [--gpus N] [--steps K] [--warmup W] [--impl reference]
   python bench.py --prefill-only
@@ -59,13 +67,14 @@ def sealed_groups(n):
     return max(max(n - 128, 0) // 128 - FLOOR, 0)
 
 
-def step_bytes(lengths):
+def step_bytes(lengths, hq=None, hkv=None, kb=None, vb=None):
     """Algorithmic HBM bytes of one decode step at the given lengths (before the step):
     sealed records read + exact fp16 K/V read + q read + out written + new token written,
     plus, for a sequence whose step seals a group, that group's tail tokens read (127
     and the new token, or all 128 with a tail floor) and the new records written and
-    read."""
-    pair = rec_bytes(KB) + rec_bytes(VB)
+    read. Head counts and widths default to the headline workload's."""
+    hq, hkv = hq or HQ, hkv or HKV
+    pair = rec_bytes(kb or KB) + rec_bytes(vb or VB)
     total = 0
     for n in lengths:
         n1 = n + 1
@@ -73,10 +82,10 @@ def step_bytes(lengths):
         groups = sealed_groups(n1) - (1 if sealing else 0)
         n_sink = min(n1, 128)
         n_tail = max(n1 - 128, 0) - 128 * sealed_groups(n1)
-        total += HKV * (groups * pair + (n_sink + n_tail) * 512)
-        total += HQ * 256 * 2 + HKV * 512
+        total += hkv * (groups * pair + (n_sink + n_tail) * 512)
+        total += hq * 256 * 2 + hkv * 512
         if sealing:
-            total += HKV * ((127 if FLOOR == 0 else 128) * 512 + 2 * pair)
+            total += hkv * ((127 if FLOOR == 0 else 128) * 512 + 2 * pair)
     return total
 
 
@@ -256,6 +265,13 @@ def snapshot_leg(cache):
 
 
 PF_HQ, PF_HKV, PF_N = 32, 8, 4096  # prefill leg: Qwen3-4B attention shape, one 4096-token prompt
+SS_STEPS, SS_WIN = 1024, 8          # seal-share run: steps, steps per timed window
+# Seal roofline. FP32 work of sealing one 128 x 128 group matrix (an FMA counts 2): the
+# 128-point Hadamard transform, 7 add/subtract stages per element; Y * Y, 1; 16 Sinkhorn
+# iterations of two matrix-vector passes over Y * Y, 64; the normalised value and its
+# grid position (two multiplies and an FMA), 4. 76 FLOP per element.
+SEAL_FLOP = 76 * 128 * 128
+FP32_LANES_PER_SM = 128
 
 
 def prefill_leg(torch, device, stream, barrier, reps=5, cpu=False):
@@ -331,7 +347,7 @@ def run_ours(args):
         pg = dist
     K_, W = args.steps, args.warmup
     reps_max = max(3, min(args.reps, 8192 // max(K_, 1)))
-    total_steps = W + K_ * (reps_max + 3) + 8  # timed reps, per-step events, two e2e passes
+    total_steps = W + K_ * (reps_max + 2) + SS_STEPS + 8  # timed reps, two e2e passes, seal-share run
     cache, ids, lengths = build_cache(torch, device, total_steps + 256)
     q_all = workloads.torch_queries(SEED + 100 * rank, total_steps, BATCH, HQ, device=device)
     kn_all, vn_all = [], []
@@ -505,26 +521,40 @@ def run_ours(args):
     achieved = alg_bytes / (launch_us * 1e-6) / 1e9
     peak, peak_kind = measured_hbm_peak()
 
-    # seal share: per-step events over K steps; steps that seal vs steps that do not
-    evs = [torch.cuda.Event(enable_timing=True) for _ in range(K_ + 1)]
-    seal_flags = []
+    # seal share (fig1.dev "Why it matters" claims 0.18 % latency overhead): SS_STEPS
+    # consecutive steps, in which every sequence seals twice at staggered steps, timed back
+    # to back in windows of SS_WIN steps (one event pair per window: per-step events break
+    # the programmatic launch chain between steps). The number of fused seals per window
+    # varies; a least-squares fit of window time on it gives the time one seal adds to its
+    # step, and the share is what the run's seals add over the run's time. This is the
+    # difference between the run and the same steps with those groups already sealed.
+    n_win = SS_STEPS // SS_WIN
+    wev = [torch.cuda.Event(enable_timing=True) for _ in range(n_win + 1)]
+    seals_w = []
     barrier()
-    evs[0].record(stream)
-    for k in range(K_):
-        seal_flags.append(sealing_count(lens_at(cur[0])) > 0)
-        step()
-        evs[k + 1].record(stream)
+    wev[0].record(stream)
+    for wi in range(n_win):
+        ns = 0
+        for _ in range(SS_WIN):
+            ns += sealing_count(lens_at(cur[0]))
+            step()
+        wev[wi + 1].record(stream)
+        seals_w.append(ns)
     barrier()
-    per = [evs[k].elapsed_time(evs[k + 1]) for k in range(K_)]
-    plain = [t for t, f in zip(per, seal_flags) if not f]
-    sealing = [t for t, f in zip(per, seal_flags) if f]
+    tw = [wev[i].elapsed_time(wev[i + 1]) for i in range(n_win)]
     seal_share, seal_steps = None, None
-    if plain and sealing:
-        # time the sealing steps take beyond a plain step, as a share of all the time
-        extra = (statistics.fmean(sealing) - statistics.fmean(plain)) * len(sealing)
-        seal_share = max(0.0, extra / sum(per))
-        seal_steps = {"sealing": len(sealing), "plain": len(plain),
-                      "sealing_step_us": statistics.fmean(sealing) * 1e3, "plain_step_us": statistics.fmean(plain) * 1e3}
+    if len(set(seals_w)) > 1:
+        X = np.stack([np.ones(n_win), np.array(seals_w, np.float64)], 1)
+        coef, *_ = np.linalg.lstsq(X, np.array(tw, np.float64), rcond=None)
+        resid = np.array(tw) - X @ coef
+        dof = max(n_win - 2, 1)
+        cov = (resid @ resid / dof) * np.linalg.inv(X.T @ X)
+        per_seal_ms = float(coef[1])
+        seal_share = max(0.0, per_seal_ms * sum(seals_w) / sum(tw))
+        seal_steps = {"steps": SS_STEPS, "window": SS_WIN, "seals": int(sum(seals_w)),
+                      "us_per_seal": per_seal_ms * 1e3, "us_per_seal_stderr": float(math.sqrt(cov[1, 1])) * 1e3,
+                      "us_per_step": sum(tw) / SS_STEPS * 1e3,
+                      "method": "window time regressed on fused seals per window; share = fitted seal time / run time"}
 
     # bulk seal throughput (kvarn_seal_groups on 16384 group matrices, 512 MiB in)
     seal_gps = None
@@ -544,6 +574,8 @@ def run_ours(args):
         seal_gps = n / (s0.elapsed_time(s1) / 1e3) * world
         del x
 
+    workloads_res = None if args.no_workloads or (KB, VB, FLOOR) != (2, 2, 0) else workload_leg(
+        torch, device, stream, barrier, peak)
     prefill = None if args.no_prefill else prefill_leg(
         torch, device, stream, barrier, cpu=rank == 0 and world == 1 and not args.no_cpu_baseline)
     snapshot = None if args.no_snapshot or world > 1 else snapshot_leg(cache)
@@ -563,6 +595,8 @@ def run_ours(args):
                      "peak_kind": peak_kind, "kernel": f"decode_kernel<{KB},{VB}>",
                      "alg_bytes_per_launch": alg_bytes, "launch_us": launch_us},
         "seal_groups_per_s": seal_gps,
+        "seal_roofline": seal_roofline(seal_gps, clocks, torch),
+        "workloads": workloads_res,
         "prefill": prefill,
         "snapshot": snapshot,
         "seal_share": seal_share,
@@ -580,7 +614,117 @@ def run_ours(args):
         print(json.dumps(result), flush=True)
 
 
-def _oracle_step_sample(cache, q_np, pairs):
+def seal_roofline(seal_gps, clocks, torch):
+    """The bulk seal against the FP32 ALU peak of this GPU: SEAL_FLOP per group matrix
+    times groups/s, over SMs x 128 FP32 lanes x 2 FLOP per FMA x the SM clock (the
+    largest sampled, nvidia-smi's clocks.max.sm, else 2070 MHz)."""
+    if not seal_gps:
+        return None
+    sms = torch.cuda.get_device_properties(torch.cuda.current_device()).multi_processor_count
+    mhz = (clocks or {}).get("sm_max_mhz") or 2070.0
+    peak = sms * FP32_LANES_PER_SM * 2 * mhz * 1e6 / 1e12
+    achieved = seal_gps * SEAL_FLOP / 1e12
+    return {"bound": "alu", "achieved": achieved, "peak": peak, "unit": "TFLOP/s", "frac": achieved / peak,
+            "flop_per_group": SEAL_FLOP, "peak_kind": f"derived: {sms} SMs x {FP32_LANES_PER_SM} FP32 lanes x 2 x "
+                                                      f"{mhz:.0f} MHz", "kernel": "seal_groups_kernel"}
+
+
+WORKLOAD_LEG = [  # (workload name, steps timed, bit widths); C3 is the headline line itself
+    ("c2_qwen3_4b_4k", 256, None),
+    ("c4_long_64k_k4v2", 2048, None),
+    ("c4_long_64k_k4v4", 2048, None),
+    ("c5_phi4_14b_ragged_b2", 64, None),
+    ("c5_phi4_14b_ragged_b4", 64, None),
+    ("c5_phi4_14b_ragged_b8", 64, None),
+]
+
+
+def workload_leg(torch, device, stream, barrier, peak):
+    """The other decode workloads, each through the same kvarn_decode_step loop: the cache
+    prefilled by bulk append, a few untimed steps, then its stated number of decode steps
+    timed back to back (two passes from the same state, the faster kept). Reported per
+    workload: us per step, tokens/s, algorithmic HBM GB/s and the fraction of the
+    measured peak (for the single-sequence Qwen3-4B shape the step is launch- and
+    latency-bound: its fraction is not a meaningful roofline)."""
+    from quantized_kv_cache_seal_gb300 import workloads
+    from quantized_kv_cache_seal_gb300 import kvarn as K
+    from quantized_kv_cache_seal_gb300.cache import KVarNCache
+
+    wl = workloads.workloads()
+    out = {}
+    for name, steps, _ in WORKLOAD_LEG:
+        w = wl[name]
+        lengths = list(w.context)
+        warm = 4
+        cache = KVarNCache(num_layers=1, max_seqs=w.batch, num_q_heads=w.num_q_heads, num_kv_heads=w.num_kv_heads,
+                           k_bits=w.k_bits, v_bits=w.v_bits, max_seq_len=max(lengths) + 2 * (steps + warm),
+                           device=device)
+        done = [0] * w.batch
+        while any(d < n for d, n in zip(done, lengths)):
+            ids, counts, ks, vs = [], [], [], []
+            for i in range(w.batch):
+                c = min(8192, lengths[i] - done[i])
+                if c > 0:
+                    k, v = workloads.torch_tokens(w.seed, i, done[i], c, w.num_kv_heads, spike_frac=w.spike_frac,
+                                                  spike_factor=w.spike_factor, device=device)
+                    ids.append(i)
+                    counts.append(c)
+                    ks.append(k)
+                    vs.append(v)
+                    done[i] += c
+            cache.append(0, ids, counts, torch.cat(ks), torch.cat(vs))
+        total = warm + steps
+        kn, vn = [], []
+        for i in range(w.batch):
+            k, v = workloads.torch_tokens(w.seed, i, lengths[i], total, w.num_kv_heads, spike_frac=w.spike_frac,
+                                          spike_factor=w.spike_factor, device=device)
+            kn.append(k)
+            vn.append(v)
+        kn = torch.stack(kn, 1).contiguous()
+        vn = torch.stack(vn, 1).contiguous()
+        qs = workloads.torch_queries(w.seed, total, w.batch, w.num_q_heads, device=device)
+        outb = torch.empty((w.batch, w.num_q_heads, 128), dtype=torch.float16, device=device)
+        ids = list(range(w.batch))
+        scale = 1.0 / math.sqrt(128)
+        h, sp = cache.handle, stream.cuda_stream
+        img = cache.snapshot()
+        best = None
+        for rep in range(2):
+            if rep:
+                cache.restore(img)
+            base = 0
+            for k in range(warm):
+                K.kvarn_decode_step(h, 0, ids, kn[base + k], vn[base + k], qs[base + k], outb, scale, sp)
+            barrier()
+            e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            e0.record(stream)
+            for k in range(warm, total):
+                K.kvarn_decode_step(h, 0, ids, kn[base + k], vn[base + k], qs[base + k], outb, scale, sp)
+            e1.record(stream)
+            barrier()
+            ms = e0.elapsed_time(e1)
+            best = ms if best is None else min(best, ms)
+        err = cache.check_device_error()
+        cache.close()
+        if err:
+            raise RuntimeError(f"device error word in {name}: {err}")
+        nbytes = sum(step_bytes([n + warm + k for n in lengths], w.num_q_heads, w.num_kv_heads, w.k_bits, w.v_bits)
+                     for k in range(steps))
+        us = best / steps * 1e3
+        gbs = nbytes / (best * 1e-3) / 1e9
+        entry = {"steps": steps, "us_per_step": us, "tokens_per_s": w.batch * steps / (best * 1e-3),
+                 "hbm_gbs": gbs, "frac": gbs / peak, "alg_bytes_per_step": nbytes / steps,
+                 "batch": w.batch, "num_q_heads": w.num_q_heads, "num_kv_heads": w.num_kv_heads,
+                 "k_bits": w.k_bits, "v_bits": w.v_bits, "mean_context": int(statistics.mean(lengths))}
+        if w.batch == 1:
+            entry["note"] = "one sequence: launch- and latency-bound, the roofline fraction is not meaningful"
+        out[name] = entry
+        del kn, vn, qs, img
+        torch.cuda.empty_cache()
+    return out
+
+
+def _oracle_step_sample(cache, q_np, pairs, threads=None):
     """Time the oracle's attention for the given (seq, kv head) pairs on host threads."""
     import concurrent.futures
 
@@ -613,10 +757,11 @@ def _oracle_step_sample(cache, q_np, pairs):
         q, sk, sv, kr, vr, tk, tv = j
         return oracle.attention(q, 1.0 / math.sqrt(128), sk, sv, kr, vr, tk, tv, KB, VB)
 
+    n_threads = min(threads or cores, len(jobs))
     t0 = time.perf_counter()
-    with concurrent.futures.ThreadPoolExecutor(max_workers=min(cores, len(jobs))) as ex:
+    with concurrent.futures.ThreadPoolExecutor(max_workers=n_threads) as ex:
         list(ex.map(one, jobs))
-    return time.perf_counter() - t0, min(cores, len(jobs))
+    return time.perf_counter() - t0, n_threads
 
 
 def cpu_baseline(cache, lengths, s_now, q_all, n_pairs):
@@ -629,6 +774,8 @@ def cpu_baseline(cache, lengths, s_now, q_all, n_pairs):
     pairs = [(i % BATCH, (i * 3) % HKV) for i in range(n_pairs)]
     t, used = _oracle_step_sample(cache, q_np, pairs)
     step_s = t * (BATCH * HKV) / len(pairs)
+    t1, _ = _oracle_step_sample(cache, q_np, pairs[:2], threads=1)  # the oracle on one thread
+    single_s = t1 * (BATCH * HKV) / 2
     # oracle seal throughput on 2 * cores group matrices
     from quantized_kv_cache_seal_gb300 import workloads
     import concurrent.futures
@@ -641,7 +788,9 @@ def cpu_baseline(cache, lengths, s_now, q_all, n_pairs):
     return {"value": BATCH / step_s, "unit": "tokens/s", "cores": used, "kind": "oracle",
             "sample": f"decode attention of {len(pairs)} of {BATCH * HKV} (sequence, KV head) pairs at ~32k "
                       f"context over the cache's records, scaled to the whole step; seal: {len(xs)} group matrices",
-            "seal_groups_per_s": seal_gps}
+            "seal_groups_per_s": seal_gps,
+            "single_thread": {"value": BATCH / single_s, "unit": "tokens/s", "cores": 1,
+                              "sample": "decode attention of 2 pairs on one thread, scaled to the whole step"}}
 
 
 def prefill_cpu_baseline(k, v, q, positions_sample=64, head=0):
@@ -687,9 +836,11 @@ def prefill_cpu_baseline(k, v, q, positions_sample=64, head=0):
 
 
 def run_reference(args):
-    """The oracle (plain fp64 C) on the host cores: each step appends one token to a
-    sample of (sequence, KV head) pairs of the workload (sealing when a group fills),
-    then attends, one pair per core; scaled to the whole batch."""
+    """The oracle (plain fp64 C) on the host cores, on the headline workload: every step
+    appends one token to each of the 128 (sequence, KV head) pairs (sealing when a group
+    fills) and attends with their query heads, the pairs spread over one thread per core.
+    The whole batch is timed every step (nothing is scaled); beside it, one pair-step
+    timed on a single thread."""
     import concurrent.futures
 
     import oracle
@@ -700,54 +851,69 @@ def run_reference(args):
         return
     oracle.build()
     cores = os.cpu_count() or 1
-    n_pairs = max(1, min(cores, args.ref_pairs))
+    n_pairs = BATCH * HKV if args.ref_pairs <= 0 else max(1, min(BATCH * HKV, args.ref_pairs))
     lengths = c3_lengths()
-    pairs = [(i % BATCH, (i * 3) % HKV) for i in range(n_pairs)]
-    caches, srcs = [], []
+    pairs = [(i % BATCH, (i // BATCH + 3 * (i % BATCH)) % HKV) for i in range(n_pairs)]
+    if n_pairs == BATCH * HKV:
+        pairs = [(s, h) for s in range(BATCH) for h in range(HKV)]
     setup0 = time.perf_counter()
+    srcs = {s: workloads.TokenSource(SEED, s, HKV) for s in {p[0] for p in pairs}}
+    toks = {s: srcs[s].tokens(0, lengths[s] + args.warmup + args.steps + 1) for s in srcs}
 
     def setup(pair):
         s, h = pair
-        src = workloads.TokenSource(SEED, s, HKV)
         oc = oracle.OracleCache(1, KB, VB, tail_floor=FLOOR)
-        k, v = src.tokens(0, lengths[s])
-        oc.append(0, k[:, h:h + 1], v[:, h:h + 1])
-        return oc, src
+        k, v = toks[s]
+        oc.append(0, k[:lengths[s], h:h + 1], v[:lengths[s], h:h + 1])
+        return oc
 
-    with concurrent.futures.ThreadPoolExecutor(max_workers=n_pairs) as ex:
-        res = list(ex.map(setup, pairs))
-    caches = [r[0] for r in res]
-    srcs = [r[1] for r in res]
+    with concurrent.futures.ThreadPoolExecutor(max_workers=cores) as ex:
+        caches = list(ex.map(setup, pairs))
     setup_s = time.perf_counter() - setup0
     r = HQ // HKV
     scale = 1.0 / math.sqrt(128)
 
-    def one_step(idx, step):
+    def one_step(idx, step, q):
         s, h = pairs[idx]
         pos = lengths[s] + step
-        k, v = srcs[idx].tokens(pos, 1)
-        caches[idx].append(0, k[:, h:h + 1], v[:, h:h + 1])
-        q = workloads.queries(SEED, step, BATCH, HQ)[s, h * r:(h + 1) * r]
-        caches[idx].attend(0, q, scale)
+        k, v = toks[s]
+        caches[idx].append(0, k[pos:pos + 1, h:h + 1], v[pos:pos + 1, h:h + 1])
+        caches[idx].attend(0, q[s, h * r:(h + 1) * r], scale)
 
     times = []
-    with concurrent.futures.ThreadPoolExecutor(max_workers=n_pairs) as ex:
+    with concurrent.futures.ThreadPoolExecutor(max_workers=cores) as ex:
         for step in range(args.warmup + args.steps):
+            q = workloads.queries(SEED, step, BATCH, HQ)
             t0 = time.perf_counter()
-            list(ex.map(lambda i: one_step(i, step), range(n_pairs)))
+            list(ex.map(lambda i: one_step(i, step, q), range(n_pairs)))
             if step >= args.warmup:
                 times.append(time.perf_counter() - t0)
+    # one pair-step on one thread (the oracle's single-thread rate), on a fresh copy of a pair
+    step1 = args.warmup + args.steps
+    t1 = []
+    q1 = workloads.queries(SEED, step1, BATCH, HQ)
+    for idx in range(min(3, n_pairs)):
+        t0 = time.perf_counter()
+        one_step(idx, step1, q1)
+        t1.append(time.perf_counter() - t0)
+    single_step_s = statistics.median(t1) * BATCH * HKV
     per_step = statistics.mean(times) * (BATCH * HKV) / n_pairs
     value = BATCH / per_step
+    whole = n_pairs == BATCH * HKV
     line = {"impl": "reference", "metric": METRIC, "value": value, "unit": "tokens/s", "n_gpus": world,
             "steps": args.steps, "warmup": args.warmup, "ms_per_step": per_step * 1e3, "higher_is_better": True,
             "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
             "config": {"workload": WORKLOAD, "global_batch": BATCH, "seq_len": int(statistics.mean(lengths)),
                        "num_q_heads": HQ, "num_kv_heads": HKV, "head_dim": 128, "k_bits": KB, "v_bits": VB,
                        "parallelism": "host threads", "setup_s": setup_s},
-            "cpu_baseline": {"value": value, "unit": "tokens/s", "cores": n_pairs, "kind": "oracle",
-                             "sample": f"{n_pairs} of {BATCH * HKV} (sequence, KV head) pairs per step, "
-                                       f"append + seal + attention, scaled to the whole batch"},
+            "cpu_baseline": {"value": value, "unit": "tokens/s", "cores": min(cores, n_pairs), "kind": "oracle",
+                             "sample": (f"the whole batch every step: all {n_pairs} (sequence, KV head) pairs, "
+                                        f"append + seal + attention, timed (not scaled)") if whole else
+                                       (f"{n_pairs} of {BATCH * HKV} (sequence, KV head) pairs per step, "
+                                        f"append + seal + attention, scaled to the whole batch"),
+                             "single_thread": {"value": BATCH / single_step_s, "unit": "tokens/s", "cores": 1,
+                                               "sample": "median of 3 single pair-steps on one thread, "
+                                                         "times 128 pairs"}},
             "e2e": {"value": value, "unit": "tokens/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
     print(json.dumps(line), flush=True)
 
@@ -764,10 +930,11 @@ def main():
     ap.add_argument("--no-seal", action="store_true")
     ap.add_argument("--no-prefill", action="store_true")
     ap.add_argument("--no-snapshot", action="store_true")
+    ap.add_argument("--no-workloads", action="store_true", help="skip the Qwen3-4B / 64k / Phi-4 decode workloads")
     ap.add_argument("--prefill-only", action="store_true", help="run the prompt-prefill leg alone (one JSON object)")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--cpu-pairs", type=int, default=32)
-    ap.add_argument("--ref-pairs", type=int, default=16)
+    ap.add_argument("--ref-pairs", type=int, default=0, help="reference arm: pairs per step (0: the whole batch)")
     ap.add_argument("--k-bits", type=int, default=2, help="K code width (the headline workload: 2)")
     ap.add_argument("--v-bits", type=int, default=2, help="V code width (the headline workload: 2)")
     ap.add_argument("--tail-floor", type=int, default=0,
