@@ -955,23 +955,29 @@ struct __align__(16) GroupCursor {
     }
 };
 
-// Copies of an exact sub-group's rows (whole warp): K rows by lanes 0..15, V rows by
-// lanes 16..31, each into a row padded to kRowPitch. Kept out of line: the group loop
-// stays short.
+// Copies of an exact sub-group's rows (whole warp) into rows padded to kRowPitch (so
+// that the ldmatrix reads of process_exact are free of bank conflicts): 16-byte cp.async
+// copies, two 256-byte rows per warp instruction (K rows, then V rows), tracked by the
+// stage's full barrier (each lane's copies hold the barrier's phase open until they
+// land; lane 0 makes the phase's one expected arrival). Many small bulk copies cost the
+// copy warps far more issue time. Kept out of line: the group loop stays short.
 __device__ __noinline__ void issue_exact_rows(const DecodeParams& p, uint64_t* bar, uint8_t* dst, const uint8_t* base,
                                               int aux, int lane) {
     const int rows = aux & 255;
-    if (lane == 0) mbar_arrive_expect_tx(bar, (uint32_t)(2 * 256 * rows));
-    const int r = lane & 15;
-    if (r < rows) {
-        const size_t kv = (aux & 256) ? p.lay.tail_v - p.lay.tail_k : p.lay.sink_v - p.lay.sink_k;
-        const uint8_t* src = base + (lane < 16 ? 0 : kv) + (size_t)r * 256;
-        bulk_g2s(dst + (lane < 16 ? 0 : kExactVOff) + r * kRowPitch, src, 256, bar);
+    const size_t kv = (aux & 256) ? p.lay.tail_v - p.lay.tail_k : p.lay.sink_v - p.lay.sink_k;
+    for (int i = lane; i < 2 * 16 * kExactRows; i += 32) {  // (side, row, 16-byte chunk)
+        const int side = i / (16 * kExactRows), r = (i / 16) % kExactRows, c = i % 16;
+        if (r < rows)
+            cp_async_16(dst + (side ? kExactVOff : 0) + r * kRowPitch + 16 * c,
+                        base + (side ? kv : 0) + (size_t)r * 256 + 16 * c);
     }
+    cp_async_mbar_arrive(bar);
+    __syncwarp();
+    if (lane == 0) mbar_arrive(bar);
 }
 
 // Issue the copy of a group into stage s (whole warp). A record is one bulk copy by lane
-// 0; an exact sub-group is one 256-byte copy per row (issue_exact_rows).
+// 0; an exact sub-group is copied by the whole warp (issue_exact_rows).
 __device__ __forceinline__ void issue_copy(const DecodeParams& p, const Smem& sm, const PendingCopy& pc, uint32_t gn,
                                            uint32_t s, int lane) {
     if (pc.kind == 0) return;
