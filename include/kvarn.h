@@ -279,11 +279,15 @@ kvarn_status kvarn_seal_groups(const void* x, int32_t n, int32_t bits, int32_t w
  * [cuts[b], cuts[b + 1]), n <= max_ctas, no range empty, no cut strictly inside a
  * head, every block covered by at most max_span ranges; n in *n_ctas. The cuts are
  * the greedy fill (each cut as late as a bound L and the heads allow) for the
- * smallest L >= min_load found by bisection: when max_span does not bind, no valid
- * partition into max_ctas ranges has a smaller largest range. KVARN_EINVAL for bad
- * arguments, KVARN_ECAPACITY if the total reaches 2^31 or nothing fits. */
+ * smallest L >= min_load found by bisection; a range's cost is its units plus
+ * item_cost (>= 0) for every block it touches beyond its first two (a decode CTA
+ * builds the query tables of its first two blocks up front; a later block's is built
+ * while the CTA's warps wait). With item_cost 0 and when max_span does not bind, no
+ * valid partition into max_ctas ranges has a smaller largest range. KVARN_EINVAL for
+ * bad arguments, KVARN_ECAPACITY if the total reaches 2^31 or nothing fits. */
 kvarn_status kvarn_partition_units(int32_t n_blocks, const int32_t* units, const int32_t* head, int32_t max_ctas,
-                                   int32_t max_span, int32_t min_load, int32_t* cuts, int32_t* n_ctas);
+                                   int32_t max_span, int32_t min_load, int32_t item_cost, int32_t* cuts,
+                                   int32_t* n_ctas);
 
 /* Read and clear the device error word of the cache (synchronises `stream`).
  * KVARN_OK; KVARN_ETIMEOUT if a bounded wait in a kernel gave up; KVARN_ESTATE for any

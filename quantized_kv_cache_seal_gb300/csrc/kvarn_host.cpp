@@ -137,14 +137,23 @@ kvarn_status check_ids(const kvarn_cache* c, int32_t layer, int32_t n, const int
     return KVARN_OK;
 }
 
-// Units charged for an exact item (sink + tail tokens) relative to one sealed group
-// pair: a 16-token fp16 sub-group moves about as many bytes as a 2-bit group pair and,
-// measured, costs a CTA about as much time (its rows are copied one by one), so it is
-// charged as one.
-int exact_units(const kvarn_cache* c, int n_sink, int n_tail) {
-    (void)c;
-    return std::max(1, exact_subs(n_sink, n_tail));
+// Costs of the decode schedule relative to one sealed group pair (one unit), fitted on the
+// GPU from per-CTA times of decode steps over many blocks (ragged Phi-4 shape at 2 bits,
+// CTAs covering 3 to 11 blocks): a 2-bit group pair 0.283 us, a 16-token exact sub-group
+// 0.416 us (1.47 units), a block 3.86 us on average. A CTA's first two blocks have their
+// query tables built by the whole CTA at its start; a later block has its table built by
+// one warp while the others wait, so the fixed cost is charged per block beyond a CTA's
+// second (item_units). Wider records make a group pair dearer; the other costs stay, so
+// they shrink in units.
+double pair_scale(const kvarn_cache* c) {
+    return 2.0 * (528 + 2048 * 2) / (double)(c->rec_k + c->rec_v);
 }
+
+int exact_units(const kvarn_cache* c, int n_sink, int n_tail) {
+    return std::max(1, (int)std::lround(1.47 * exact_subs(n_sink, n_tail) * pair_scale(c)));
+}
+
+int item_units(const kvarn_cache* c) { return (int)std::lround(16.0 * pair_scale(c)); }
 
 int seal_units(const kvarn_cache* c) {
     // a K + V seal inside the decode kernel costs about as much as 140 group pairs of
@@ -154,12 +163,13 @@ int seal_units(const kvarn_cache* c) {
     return std::max(1, (int)std::lround(140.0 * pair2 / (double)(c->rec_k + c->rec_v)));
 }
 
-// Greedy fill of the unit line with ranges of at most L units, each cut as late as the
+// Greedy fill of the unit line with ranges of cost at most L, each cut as late as the
 // indivisible block heads allow (a cut inside a head moves back to the head's start,
-// which lies past the previous cut because L >= every head). begin[k] = first unit of
-// block k (begin[nb] = total). Stops once more than max_ranges ranges are needed.
+// which lies past the previous cut because L >= every head). A range's cost is its units
+// plus item_cost for every block it touches beyond its first two. begin[k] = first unit
+// of block k (begin[nb] = total). Stops once more than max_ranges ranges are needed.
 // Returns the number of ranges (cuts in `cuts`, from 0 to the total).
-int greedy_cuts(const std::vector<int64_t>& begin, const int32_t* head, int64_t L, int max_ranges,
+int greedy_cuts(const std::vector<int64_t>& begin, const int32_t* head, int64_t L, int max_ranges, int item_cost,
                 std::vector<int32_t>& cuts) {
     const int nb = (int)begin.size() - 1;
     const int64_t U = begin[nb];
@@ -169,12 +179,30 @@ int greedy_cuts(const std::vector<int64_t>& begin, const int32_t* head, int64_t 
     int k = 0;  // block holding the current cut position (cuts only move forward)
     while (start < U) {
         if ((int)cuts.size() > max_ranges) return max_ranges + 1;
-        int64_t end = start + L;
-        if (end >= U) {
-            end = U;
-        } else {
-            while (begin[k + 1] <= end) ++k;
-            if (begin[k] < end && end < begin[k] + head[k]) end = begin[k];
+        while (begin[k + 1] <= start) ++k;
+        int64_t budget = L, pos = start, end = U;
+        for (int kk = k, blocks = 1;; ++kk, ++blocks) {
+            if (blocks > 2) budget -= item_cost;
+            if (budget <= 0) {  // no room for another block (pos > start here)
+                end = pos;
+                break;
+            }
+            const int64_t bend = begin[kk + 1];
+            if (bend - pos <= budget) {  // the rest of block kk fits
+                budget -= bend - pos;
+                pos = bend;
+                if (pos >= U) {
+                    end = U;
+                    break;
+                }
+                continue;
+            }
+            end = pos + budget;  // cut inside block kk
+            if (begin[kk] < end && end < begin[kk] + head[kk]) {
+                end = begin[kk];
+                if (end <= start) end = begin[kk] + head[kk];  // a range takes at least its first head
+            }
+            break;
         }
         cuts.push_back((int32_t)end);
         start = end;
@@ -197,7 +225,7 @@ bool spans_ok(const std::vector<int64_t>& begin, const std::vector<int32_t>& cut
 }
 
 kvarn_status partition_units(int nb, const int32_t* units, const int32_t* head, int max_ctas, int max_span,
-                             int min_load, std::vector<int32_t>& cuts) {
+                             int min_load, std::vector<int32_t>& cuts, int item_cost = 0) {
     if (nb < 1 || !units || !head || max_ctas < 1 || max_span < 1 || min_load < 1) return KVARN_EINVAL;
     std::vector<int64_t> begin(nb + 1, 0);
     int64_t lo = min_load, max_head = 1;
@@ -211,17 +239,20 @@ kvarn_status partition_units(int nb, const int32_t* units, const int32_t* head, 
     lo = std::max(lo, max_head);
     lo = std::max<int64_t>(lo, (U + max_ctas - 1) / max_ctas);
     auto fits = [&](int64_t L) {
-        return greedy_cuts(begin, head, L, max_ctas, cuts) <= max_ctas && spans_ok(begin, cuts, max_span);
+        return greedy_cuts(begin, head, L, max_ctas, item_cost, cuts) <= max_ctas && spans_ok(begin, cuts, max_span);
     };
-    // A bound of lo + max_head always fits the CTA count (a cut loses less than one head,
-    // so every range but the last holds more than U / max_ctas units); the span limit can
-    // ask for more, then the bound doubles until it fits (the whole line, one range, does).
-    int64_t hi = std::min(U, lo + max_head);
+    // Without block costs a bound of lo + max_head always fits the CTA count (a cut loses
+    // less than one head, so every range but the last holds more than U / max_ctas units);
+    // block costs or the span limit can ask for more, then the bound doubles until it fits
+    // (the whole line, one range, does).
+    // the whole line as one range costs its units plus the blocks beyond its second
+    const int64_t whole = U + (int64_t)item_cost * std::max(0, nb - 2);
+    int64_t hi = std::min(whole, lo + max_head);
     if (hi < lo) hi = lo;
     while (!fits(hi)) {
-        if (hi >= U) return KVARN_ECAPACITY;
+        if (hi >= whole) return KVARN_ECAPACITY;
         lo = hi + 1;
-        hi = std::min(U, 2 * hi);
+        hi = std::min(whole, 2 * hi);
     }
     // smallest bound that fits, by bisection (the range count of the greedy fill only
     // falls as L grows; the span limit, when it binds, is re-checked below)
@@ -261,7 +292,8 @@ kvarn_status schedule(kvarn_cache* c, DecodeParams& p) {
     std::vector<int32_t> cuts;
     const int max_ctas = std::max(1, std::min(c->sms, kMaxGrid));
     // at least 24 units per CTA: fewer would make the per-CTA start and merge dominate
-    kvarn_status st = partition_units((int)units.size(), units.data(), head.data(), max_ctas, kMaxSpan, 24, cuts);
+    kvarn_status st =
+        partition_units((int)units.size(), units.data(), head.data(), max_ctas, kMaxSpan, 24, cuts, item_units(c));
     if (st) return st;
     p.grid = (int)cuts.size() - 1;
     for (size_t b = 0; b < cuts.size(); ++b) p.cta_begin[b] = cuts[b];
@@ -542,10 +574,11 @@ kvarn_status kvarn_device_accessible(const void* ptr, int32_t* accessible) {
 }
 
 kvarn_status kvarn_partition_units(int32_t n_blocks, const int32_t* units, const int32_t* head, int32_t max_ctas,
-                                   int32_t max_span, int32_t min_load, int32_t* cuts, int32_t* n_ctas) {
-    if (!cuts || !n_ctas) return KVARN_EINVAL;
+                                   int32_t max_span, int32_t min_load, int32_t item_cost, int32_t* cuts,
+                                   int32_t* n_ctas) {
+    if (!cuts || !n_ctas || item_cost < 0) return KVARN_EINVAL;
     std::vector<int32_t> c;
-    kvarn_status st = partition_units(n_blocks, units, head, max_ctas, max_span, min_load, c);
+    kvarn_status st = partition_units(n_blocks, units, head, max_ctas, max_span, min_load, c, item_cost);
     if (st) return st;
     std::copy(c.begin(), c.end(), cuts);
     *n_ctas = (int32_t)c.size() - 1;

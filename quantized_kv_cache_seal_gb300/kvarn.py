@@ -98,7 +98,7 @@ def load(build_if_missing: bool = True):
     L.kvarn_status_string.restype = ctypes.c_char_p
     L.kvarn_last_error.argtypes = []
     L.kvarn_last_error.restype = ctypes.c_char_p
-    L.kvarn_partition_units.argtypes = [I32, IP, IP, I32, I32, I32, IP, IP]
+    L.kvarn_partition_units.argtypes = [I32, IP, IP, I32, I32, I32, I32, IP, IP]
     L.kvarn_device_accessible.argtypes = [P, IP]
     for name in EXPORTS:
         fn = getattr(L, name)
@@ -266,7 +266,7 @@ def kvarn_check_device_error(handle, stream=None) -> int:
     return int(load().kvarn_check_device_error(handle, _stream(stream)))
 
 
-def kvarn_partition_units(units, head, max_ctas: int, max_span: int, min_load: int):
+def kvarn_partition_units(units, head, max_ctas: int, max_span: int, min_load: int, item_cost: int = 0):
     """Cut table of the decode scheduler's partition (host only): list of n + 1 cuts."""
     I32 = ctypes.c_int32
     nb = len(units)
@@ -274,7 +274,7 @@ def kvarn_partition_units(units, head, max_ctas: int, max_span: int, min_load: i
     H = (I32 * max(nb, 1))(*head)
     cuts = (I32 * (max_ctas + 1))()
     n = I32()
-    _check(load().kvarn_partition_units(nb, U, H, max_ctas, max_span, min_load, cuts, ctypes.byref(n)),
+    _check(load().kvarn_partition_units(nb, U, H, max_ctas, max_span, min_load, item_cost, cuts, ctypes.byref(n)),
            "kvarn_partition_units")
     return [int(cuts[i]) for i in range(n.value + 1)]
 

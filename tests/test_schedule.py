@@ -119,3 +119,42 @@ def test_partition_rejects_bad_arguments(units, head, max_ctas, max_span, min_lo
     with pytest.raises(K.KVarNError) as e:
         K.kvarn_partition_units(units, head, max_ctas, max_span, min_load)
     assert e.value.status == 1
+
+
+def _cost(begin, a, b, item_cost):
+    """Units of range [a, b) plus item_cost for every block it touches beyond its first two."""
+    blocks = sum(1 for k in range(len(begin) - 1) if begin[k] < b and begin[k + 1] > a)
+    return (b - a) + item_cost * max(0, blocks - 2)
+
+
+def _optimal_cost(units, head, max_ctas, item_cost):
+    """Smallest largest range cost over every valid cut set of at most max_ctas ranges."""
+    allowed, begin, total = _allowed(units, head)
+    pts = [0] + allowed + [total]
+
+    @functools.lru_cache(maxsize=None)
+    def best(i, c):
+        if pts[i] == total:
+            return 0
+        if c == 0:
+            return float("inf")
+        return min(max(_cost(begin, pts[i], pts[j], item_cost), best(j, c - 1)) for j in range(i + 1, len(pts)))
+
+    return best(0, max_ctas)
+
+
+@pytest.mark.parametrize("seed", range(60))
+def test_partition_with_block_cost_matches_exhaustive_optimum(seed):
+    """With a cost per block beyond a range's second (the decode CTA's on-demand query
+    tables), the greedy fill at the bisected bound is still the exhaustive optimum."""
+    rng = random.Random(1000 + seed)
+    nb = rng.randint(1, 9)
+    units = [rng.randint(1, 7) for _ in range(nb)]
+    head = [rng.randint(1, u) for u in units]
+    max_ctas = rng.randint(1, 5)
+    item_cost = rng.randint(1, 6)
+    cuts = K.kvarn_partition_units(units, head, max_ctas, 64, 1, item_cost)
+    _check_valid(units, head, cuts, max_ctas, 64)
+    _, begin, _ = _allowed(units, head)
+    got = max(_cost(begin, a, b, item_cost) for a, b in zip(cuts, cuts[1:]))
+    assert got == _optimal_cost(units, head, max_ctas, item_cost), (units, head, max_ctas, item_cost, cuts)
