@@ -157,6 +157,8 @@ struct AppendParams {
 int launch_decode(const DecodeParams& p, int smem_bytes, void* stream);
 int launch_prefill(const PrefillParams& p, int smem_bytes, void* stream);
 int prefill_smem_bytes(int k_bits, int v_bits, int stages);
+int launch_prefill_tc(const PrefillParams& p, void* stream);  // tcgen05 kernel (kvarn_prefill_tc.cu)
+int prefill_tc_smem_bytes();
 int launch_seal_jobs(const SealParams& p, void* stream);
 int launch_append(const AppendParams& p, void* stream);
 int launch_seal_groups(const void* x, int n, int bits, int which, int iters, void* records, float* scales,
