@@ -28,20 +28,24 @@
 // Warp roles (640 threads, 5 warpgroups; warp w reaches tensor-memory lanes
 // 32 (w % 4) .. 32 (w % 4) + 31, so thread 32 (w % 4) + lane of a warpgroup owns query
 // row 32 (w % 4) + lane):
-//   WG0, WG1  softmax: two threads per row, each with 64 of the unit's 128 keys; they
-//        load S, apply scales, mask, keep the running maximum (raised only when it grows
-//        by more than 8 in log2 units, with O and l rescaled then), write W (high and
-//        low f16 parts) over S, and at the end normalise O and write the output.
-//   WG2  query operand: rotates and scales its row once, then per group writes A (high
-//        and low parts) into tensor memory and the row sum sum_j v_ij c_j into shared memory;
-//        before the exact blocks it writes the raw query and rotates O back.
-//   WG3  expansion: turns each unit's records (or exact rows) into the two operand tiles
-//        in shared memory (canonical K-major layout, no swizzle): the K codes as f16
-//        integers, the dequantised V values (high and low parts), and the token scales.
-//   WG4  warp 16 owns tensor memory and one of its threads issues every MMA.
+//   WG0  softmax: one thread per row; loads S in 32-column chunks (a pass for the
+//        maximum, a pass for the weights), keeps the running maximum (raised only when
+//        it grows by more than 8 in log2 units, with O and l rescaled then), writes W
+//        (high and low f16 parts) over S, and at the end normalises O and writes the
+//        output.
+//   WG1  query operand: rotates and scales its row once, then per group writes A (high
+//        and low parts) into tensor memory and the row sum sum_j v_ij c_j into shared
+//        memory; before the exact blocks it writes the raw query and rotates O back.
+//   WG2  K expansion: the K codes of each group as f16 integers (or the exact K rows) in
+//        a canonical K-major tile (no swizzle) and the group's token scales.
+//   WG3  V expansion: the dequantised V values of each group as high and low parts (or
+//        the exact V rows, transposed) in a canonical K-major tile.
+//   WG4  warp 16 owns tensor memory and one of its threads issues every MMA, QK or PV,
+//        whichever is ready first.
 // Tensor memory (512 columns): A [0, 128), S0 [128, 256), S1 [256, 384), O [384, 512).
-// QK of unit u + 1 runs while the softmax of unit u does; the operand tiles and S are
-// double-buffered. Every wait is bounded (2 s) and sets the error word when it gives up.
+// QK of unit u + 1 runs while the softmax of unit u does; the K tiles, V tiles and S are
+// double-buffered and released separately (a K tile when its QK completes, a V tile when
+// its PV does). Every wait is bounded (2 s) and sets the error word when it gives up.
 #include <cuda_fp16.h>
 #include <cuda_runtime.h>
 
@@ -53,38 +57,40 @@ namespace {
 
 constexpr int kTcThreads = 640;      // five warpgroups
 constexpr int kRows = kPrefillRows;  // 128 query rows per CTA
-// registers a thread: 96 at launch (65536 / 640 rounded down to a multiple of 8); the
-// softmax warpgroups keep them, the query warpgroup takes what the expansion and the
-// issuing warpgroup give back (per scheduler: one warp of each warpgroup)
-constexpr int kRegsLaunch = 96, kRegsQuery = 176, kRegsExpand = 88, kRegsIssue = 24;
-static_assert(2 * kRegsLaunch + kRegsQuery + kRegsExpand + kRegsIssue <= 5 * kRegsLaunch,
+// registers a thread: 96 at launch (65536 / 640 rounded down to a multiple of 8), then
+// re-split per warpgroup (per scheduler: one warp of each warpgroup)
+constexpr int kRegsLaunch = 96, kRegsSoftmax = 128, kRegsQuery = 176, kRegsExpandK = 64, kRegsExpandV = 88,
+              kRegsIssue = 24;
+static_assert(kRegsSoftmax + kRegsQuery + kRegsExpandK + kRegsExpandV + kRegsIssue <= 5 * kRegsLaunch,
               "register split exceeds what a sub-partition holds at launch");
 static_assert(kRegsLaunch * kTcThreads <= 65536, "launch registers");
 
 // tensor memory columns
 constexpr uint32_t kColA = 0, kColS = 128, kColO = 384;
 
-// shared memory: two operand sets, then the small tables
+// shared memory: two operand sets (K tile, V tile, the V expansion's token factors),
+// the K-side tables of the last four units, then the small tables
 constexpr int kKTile = 128 * 128 * 2;           // N = 128 tokens, K = 128 channels
-constexpr int kVTile = 128 * 256 * 2;         // N = 128 channels, K = 128 tokens (high parts), 128 (low)
-constexpr int kOffK = 0, kOffV = kKTile, kOffAK = kOffV + kVTile;
-constexpr int kOffAlpha = kOffAK + 512, kOffBeta = kOffAlpha + 512;  // deltaV aV_t, mV aV_t
-constexpr int kOffScal = kOffBeta + 512;        // deltaK, mK, e
-constexpr int kSetBytes = kOffScal + 128;
-constexpr int kOffRs = 2 * kSetBytes;           // float[4][128] row sums, ring by unit
-constexpr int kOffRed = kOffRs + 4 * 128 * 4;  // float[2][8] expansion reductions
-constexpr int kOffCq = kOffRed + 64;            // float[2][128] channel scales of the next query operand
-constexpr int kOffXch = kOffCq + 1024;          // float[768] softmax exchange
-constexpr int kOffPos = kOffXch + 3072;         // int[128] row positions
+constexpr int kVTile = 128 * 256 * 2;           // N = 128 channels, K = 128 tokens (high parts), 128 (low)
+constexpr int kOffK = 0, kOffV = kKTile;
+constexpr int kOffAlpha = kOffV + kVTile, kOffBeta = kOffAlpha + 512;  // deltaV aV_t, mV aV_t
+constexpr int kSetBytes = kOffBeta + 512;
+constexpr int kOffKtab = 2 * kSetBytes;         // [4][aK float[128], deltaK, mK, e, pad]
+constexpr int kKtabBytes = 512 + 16;
+constexpr int kOffRs = kOffKtab + 4 * kKtabBytes;  // float[4][128] row sums, ring by unit
+constexpr int kOffRed = kOffRs + 4 * 128 * 4;   // float[2][2][8] expansion reductions (K, V warpgroups)
+constexpr int kOffCq = kOffRed + 128;           // float[2][128] channel scales of the next query operand
+constexpr int kOffPos = kOffCq + 1024;          // int[128] row positions
 constexpr int kOffQm = kOffPos + 512;           // float[128] row maxima of the rotated query
 constexpr int kOffBars = kOffQm + 512;
-// barriers: tiles_full[2], tiles_empty[2], a_full[4], a_empty, s_full[2], p_full[2],
-// o_done[2], drain
-constexpr int kNumBars = 16;
+// barriers: k_full[4], k_empty[2], v_full[2], v_empty[2], a_full[4], a_empty, s_full[2],
+// p_full[2], o_done[2], drain
+constexpr int kNumBars = 22;
 constexpr int kOffTmem = kOffBars + 8 * kNumBars;
 constexpr int kSmemTc = kOffTmem + 16;
 static_assert(kSmemTc <= 227 * 1024, "shared memory of one CTA");
-static_assert(kSetBytes % 128 == 0 && kOffV % 128 == 0, "operand tiles stay 128-byte aligned");
+static_assert(kSetBytes % 128 == 0 && kOffV % 128 == 0 && kOffKtab % 16 == 0 && kKtabBytes % 16 == 0,
+              "operand tiles stay 128-byte aligned");
 
 __device__ __forceinline__ void tc_fence_before() { asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory"); }
 __device__ __forceinline__ void tc_fence_after() { asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory"); }
@@ -237,65 +243,100 @@ __device__ __forceinline__ const uint4* exact_row(const PrefillParams& p, const 
     return reinterpret_cast<const uint4*>(p.base + off);
 }
 
-// bars: [0, 2) tiles_full, [2, 4) tiles_empty, [4, 8) a_full, 8 a_empty, [9, 11) s_full,
-// [11, 13) p_full, [13, 15) o_done (PV of unit v completes phase v / 2 of o_done[v % 2]),
-// 15 drain (used once).
+// bars: [0, 4) k_full (by unit % 4), [4, 6) k_empty, [6, 8) v_full, [8, 10) v_empty,
+// [10, 14) a_full (by unit % 4), 14 a_empty, [15, 17) s_full, [17, 19) p_full,
+// [19, 21) o_done (PV of unit v completes phase v / 2 of o_done[v % 2]), 21 drain (once).
 // A barrier is indexed so that its previous phase has always completed when a thread
 // waits for the next: a parity wait cannot then be satisfied by an older phase. For
 // o_done this follows from tcgen05.mma completing in issue order: every wait for PV(v)
-// comes after its thread has seen QK(v) or a later MMA complete, and PV(v - 2) was issued
-// before QK(v) (the issuer's step k issues QK(k), then PV(k - 1)).
-constexpr int kBarTilesFull = 0, kBarTilesEmpty = 2, kBarAFull = 4, kBarAEmpty = 8, kBarSFull = 9,
-              kBarPFull = 11, kBarODone = 13, kBarDrain = 15;
+// comes after its thread has seen QK(v) or a later MMA complete, and PV(v - 2) is issued
+// before QK(v) (QK(v) reuses the S buffer of PV(v - 2)'s weights).
+constexpr int kBarKFull = 0, kBarKEmpty = 4, kBarVFull = 6, kBarVEmpty = 8, kBarAFull = 10, kBarAEmpty = 14,
+              kBarSFull = 15, kBarPFull = 17, kBarODone = 19, kBarDrain = 21;
 
 // wait until PV of unit v has completed
 __device__ __forceinline__ void wait_pv(uint64_t* bars, int v, int32_t* err) {
     mbar_wait(bars + kBarODone + (v & 1), (uint32_t)((v >> 1) & 1), err);
 }
 
-// ---- WG3: the MMA issuer (one thread) ----
+// ---- WG4: the MMA issuer (one thread) ----
+// QK(u) into S[u % 2] once the K tile and the query operand of unit u are in place and
+// PV(u - 2), the last reader of that S buffer, has been issued; PV(u) into O once the
+// weights of unit u and its V tile are in place. Whichever is ready is issued first.
+__device__ __forceinline__ void issue_qk(const TcCta& c, uint32_t sbase, uint64_t* bars, uint32_t tmem, int u) {
+    const int b = u & 1;
+    const bool sealed = u < c.n_sealed;
+    tc_fence_after();
+    const uint32_t d = tmem + kColS + 128u * b;
+    const uint32_t kt = sbase + b * kSetBytes + kOffK;
+#pragma unroll
+    for (int ks = 0; ks < 8; ++ks) mma_ts(d, tmem + kColA + 8 * ks, smem_desc(kt + ks * 4096), ks > 0);
+    if (sealed) {
+#pragma unroll
+        for (int ks = 0; ks < 8; ++ks) mma_ts(d, tmem + kColA + 64 + 8 * ks, smem_desc(kt + ks * 4096), 1u);
+    }
+    mma_commit(bars + kBarSFull + b);
+    mma_commit(bars + kBarKEmpty + b);
+    if (sealed) mma_commit(bars + kBarAEmpty);
+}
+
+__device__ __forceinline__ void issue_pv(const TcCta& c, uint32_t sbase, uint64_t* bars, uint32_t tmem, int v) {
+    const int b = v & 1;
+    tc_fence_after();
+    const uint32_t a = tmem + kColS + 128u * b;
+    const uint32_t vt = sbase + b * kSetBytes + kOffV;
+    // W high x B high, W high x B low (sealed only), W low x B high; the weights of
+    // k-step ks sit in columns 16 ks (high) and 16 ks + 8 (low)
+    const int passes = v < c.n_sealed ? 3 : 2;
+    for (int ps = 0; ps < passes; ++ps) {
+        const uint32_t alo = ps == passes - 1 ? 8u : 0u;
+        const uint32_t bks = ps == 1 && passes == 3 ? 8u : 0u;
+#pragma unroll
+        for (int ks = 0; ks < 8; ++ks)
+            mma_ts(tmem + kColO, a + 16 * ks + alo, smem_desc(vt + (bks + ks) * 4096),
+                   (v > 0 || ps > 0 || ks > 0) ? 1u : 0u);
+    }
+    mma_commit(bars + kBarVEmpty + b);
+    mma_commit(bars + kBarODone + b);
+}
+
+// non-blocking test of a barrier phase (try_wait may suspend the thread for a while)
+__device__ __forceinline__ bool mbar_test(uint64_t* bar, uint32_t parity) {
+    uint32_t ok;
+    asm volatile(
+        "{\n .reg .pred p;\n mbarrier.test_wait.parity.acquire.cta.shared::cta.b64 p, [%1], %2;\n"
+        " selp.u32 %0, 1, 0, p;\n}\n"
+        : "=r"(ok)
+        : "r"(smem_addr(bar)), "r"(parity)
+        : "memory");
+    return ok != 0;
+}
+
 __device__ __forceinline__ void issue_role(const TcCta& c, uint8_t* smem, uint64_t* bars, uint32_t tmem,
                                            int32_t* err) {
     const uint32_t sbase = smem_addr(smem);
-    int pv = 0;
-    for (int u = 0; u <= c.units; ++u) {
-        if (u < c.units) {
-            const int b = u & 1;
-            const bool sealed = u < c.n_sealed;
-            mbar_wait(bars + kBarTilesFull + b, (uint32_t)((u >> 1) & 1), err);
-            if (u <= c.n_sealed) mbar_wait(bars + kBarAFull + (u & 3), (uint32_t)((u >> 2) & 1), err);
-            tc_fence_after();
-            const uint32_t d = tmem + kColS + 128u * b;
-            const uint32_t kt = sbase + b * kSetBytes + kOffK;
-#pragma unroll
-            for (int ks = 0; ks < 8; ++ks) mma_ts(d, tmem + kColA + 8 * ks, smem_desc(kt + ks * 4096), ks > 0);
-            if (sealed) {
-#pragma unroll
-                for (int ks = 0; ks < 8; ++ks) mma_ts(d, tmem + kColA + 64 + 8 * ks, smem_desc(kt + ks * 4096), 1u);
-            }
-            mma_commit(bars + kBarSFull + b);
-            if (sealed) mma_commit(bars + kBarAEmpty);
+    int nq = 0, np = 0;  // next QK, next PV
+    uint64_t t0 = global_ns();
+    while (np < c.units) {
+        bool did = false;
+        if (nq < c.units && nq <= np + 1 && mbar_test(bars + kBarKFull + (nq & 3), (uint32_t)((nq >> 2) & 1)) &&
+            (nq > c.n_sealed || mbar_test(bars + kBarAFull + (nq & 3), (uint32_t)((nq >> 2) & 1)))) {
+            issue_qk(c, sbase, bars, tmem, nq);
+            ++nq;
+            did = true;
+        } else if (np < nq && mbar_test(bars + kBarPFull + (np & 1), (uint32_t)((np >> 1) & 1)) &&
+                   mbar_test(bars + kBarVFull + (np & 1), (uint32_t)((np >> 1) & 1))) {
+            issue_pv(c, sbase, bars, tmem, np);
+            ++np;
+            did = true;
         }
-        if (u >= 1) {
-            const int v = u - 1, b = v & 1;
-            mbar_wait(bars + kBarPFull + b, (uint32_t)((v >> 1) & 1), err);
-            tc_fence_after();
-            const uint32_t a = tmem + kColS + 128u * b;
-            const uint32_t vt = sbase + b * kSetBytes + kOffV;
-            // W high x B high, W high x B low (sealed only), W low x B high; the weights of
-            // k-step ks sit in columns 16 ks (high) and 16 ks + 8 (low)
-            const int passes = v < c.n_sealed ? 3 : 2;
-            for (int ps = 0; ps < passes; ++ps) {
-                const uint32_t alo = ps == passes - 1 ? 8u : 0u;
-                const uint32_t bks = ps == 1 && passes == 3 ? 8u : 0u;
-#pragma unroll
-                for (int ks = 0; ks < 8; ++ks)
-                    mma_ts(tmem + kColO, a + 16 * ks + alo, smem_desc(vt + (bks + ks) * 4096),
-                           (pv > 0 || ps > 0 || ks > 0) ? 1u : 0u);
-            }
-            ++pv;
-            mma_commit(bars + kBarTilesEmpty + b);
-            mma_commit(bars + kBarODone + b);
+        if (did) {
+            t0 = global_ns();
+        } else if (global_ns() - t0 > kWaitLimitNs || (*reinterpret_cast<volatile int32_t*>(err) & kErrTimeout)) {
+            atomicOr(err, kErrTimeout);
+            return;
+        } else {
+            __nanosleep(32);  // leave the scheduler's issue slots to the softmax warp
         }
     }
 }
@@ -308,55 +349,107 @@ __device__ __forceinline__ float wg_max(float x, float* red, int et, int id) {
     return fmaxf(fmaxf(red[0], red[1]), fmaxf(red[2], red[3]));
 }
 
-// ---- WG2: operand tiles and per-token tables of every unit (thread et = 0..127) ----
+// The group's power of two e (its dequantised values times 2^-e stay below 2^15; the
+// weights take 2^e), computed alike by both expansion warpgroups from the V header.
+template <int VB>
+__device__ __forceinline__ int group_exponent(float aV, float cV, float dV, float mV, float* red, int et, int id) {
+    const float amax = wg_max(aV, red, et, id);
+    const float cmax = wg_max(cV, red + 4, et, id);
+    const float bound = amax * cmax * (fabsf(mV) + fabsf(dV) * (float)((1 << VB) - 1));
+    int e = 0;
+    if (bound > 32768.f) frexpf(bound * (1.0f / 32768.f), &e);
+    return e;
+}
+
+// ---- WG2: the K tile and the K-side tables of every unit (thread et = 0..127) ----
 template <int KB, int VB>
-__device__ __forceinline__ void expand_role(const PrefillParams& p, const TcCta& c, uint8_t* smem, uint64_t* bars,
-                                            int32_t* err, int et) {
-    const int lane = et & 31, wv = et >> 5;
+__device__ __forceinline__ void expand_k_role(const PrefillParams& p, const TcCta& c, uint8_t* smem, uint64_t* bars,
+                                              int32_t* err, int et) {
     float* red_all = reinterpret_cast<float*>(smem + kOffRed);
     for (int u = 0; u < c.units; ++u) {
         const int b = u & 1;
         const Unit x = unit_of(c, u);
         uint8_t* set = smem + b * kSetBytes;
+        float* kt = reinterpret_cast<float*>(smem + kOffKtab + (u & 3) * kKtabBytes);
         if (x.sealed) {
             const uint8_t* kr = tc_group_src(p, c, x.g);
             const uint8_t* vr = kr + p.rec_k;
-            uint32_t ks_[4 * KB], vs_[4 * VB];
+            uint32_t ks_[4 * KB];
 #pragma unroll
             for (int i = 0; i < KB; ++i) {
                 const uint4 v4 = reinterpret_cast<const uint4*>(kr + 528 + et * 16 * KB)[i];
                 ks_[4 * i] = v4.x; ks_[4 * i + 1] = v4.y; ks_[4 * i + 2] = v4.z; ks_[4 * i + 3] = v4.w;
-            }
-#pragma unroll
-            for (int i = 0; i < VB; ++i) {
-                const uint4 v4 = reinterpret_cast<const uint4*>(vr + 528 + et * 16 * VB)[i];
-                vs_[4 * i] = v4.x; vs_[4 * i + 1] = v4.y; vs_[4 * i + 2] = v4.z; vs_[4 * i + 3] = v4.w;
             }
             const float aK = __half2float(reinterpret_cast<const __half*>(kr + 16)[et]);
             const float aV = __half2float(reinterpret_cast<const __half*>(vr + 16)[et]);
             const float cV = __half2float(reinterpret_cast<const __half*>(vr + 272)[et]);
             const float dK = *reinterpret_cast<const float*>(kr), mK = *reinterpret_cast<const float*>(kr + 4);
             const float dV = *reinterpret_cast<const float*>(vr), mV = *reinterpret_cast<const float*>(vr + 4);
-            if (u >= 2) mbar_wait(bars + kBarTilesEmpty + b, (uint32_t)(((u >> 1) - 1) & 1), err);
-            // B = the dequantised value in the rotated frame, c_j aV_t (deltaV q_tj + mV),
-            // times 2^-e where e keeps it below 2^15 (the weights take 2^e)
+            // the set's K tile is free once QK(u - 2) has completed; the table slot u % 4 once
+            // the softmax of unit u - 4 is done, which QK(u - 2) being issued implies
+            if (u >= 2) mbar_wait(bars + kBarKEmpty + b, (uint32_t)(((u >> 1) - 1) & 1), err);
+            const int e = group_exponent<VB>(aV, cV, dV, mV, red_all + 8 * b, et, 5);
+#pragma unroll
+            for (int m = 0; m < 16; ++m)
+                *reinterpret_cast<uint4*>(set + kOffK + tile_off(et, 8 * m)) = codes8<KB>(ks_, m);
+            kt[et] = aK;
+            if (et == 0) {
+                kt[128] = dK;
+                kt[129] = mK;
+                kt[130] = (float)e;
+            }
+        } else {
+            // exact block: the K rows as they are (rows past the block's end are zeros)
+            const bool live = et < x.cnt;
+            const uint4* src = live ? exact_row(p, c, x.tail, 0, x.kp0 + et) : nullptr;
+            if (u >= 2) mbar_wait(bars + kBarKEmpty + b, (uint32_t)(((u >> 1) - 1) & 1), err);
+#pragma unroll 1
+            for (int i0 = 0; i0 < 16; i0 += 4) {
+                uint4 kr[4];
+#pragma unroll
+                for (int i = 0; i < 4; ++i) kr[i] = live ? src[i0 + i] : make_uint4(0u, 0u, 0u, 0u);
+#pragma unroll
+                for (int i = 0; i < 4; ++i)
+                    *reinterpret_cast<uint4*>(set + kOffK + tile_off(et, 8 * (i0 + i))) = kr[i];
+            }
+        }
+        fence_proxy_async_smem();
+        mbar_arrive(bars + kBarKFull + (u & 3));
+    }
+}
+
+// ---- WG3: the V tile of every unit (thread et = 0..127) ----
+template <int VB>
+__device__ __forceinline__ void expand_v_role(const PrefillParams& p, const TcCta& c, uint8_t* smem, uint64_t* bars,
+                                              int32_t* err, int et) {
+    const int lane = et & 31, wv = et >> 5;
+    float* red_all = reinterpret_cast<float*>(smem + kOffRed) + 16;
+    for (int u = 0; u < c.units; ++u) {
+        const int b = u & 1;
+        const Unit x = unit_of(c, u);
+        uint8_t* set = smem + b * kSetBytes;
+        if (x.sealed) {
+            const uint8_t* vr = tc_group_src(p, c, x.g) + p.rec_k;
+            uint32_t vs_[4 * VB];
+#pragma unroll
+            for (int i = 0; i < VB; ++i) {
+                const uint4 v4 = reinterpret_cast<const uint4*>(vr + 528 + et * 16 * VB)[i];
+                vs_[4 * i] = v4.x; vs_[4 * i + 1] = v4.y; vs_[4 * i + 2] = v4.z; vs_[4 * i + 3] = v4.w;
+            }
+            const float aV = __half2float(reinterpret_cast<const __half*>(vr + 16)[et]);
+            const float cV = __half2float(reinterpret_cast<const __half*>(vr + 272)[et]);
+            const float dV = *reinterpret_cast<const float*>(vr), mV = *reinterpret_cast<const float*>(vr + 4);
+            if (u >= 2) mbar_wait(bars + kBarVEmpty + b, (uint32_t)(((u >> 1) - 1) & 1), err);
+            // B = the dequantised value in the rotated frame, c_j aV_t (deltaV q_tj + mV), times 2^-e
             float* alpha = reinterpret_cast<float*>(set + kOffAlpha);
             float* beta = reinterpret_cast<float*>(set + kOffBeta);
             alpha[et] = dV * aV;
             beta[et] = mV * aV;
-            float* red = red_all + 8 * b;
-            const float amax = wg_max(aV, red, et, 1);  // (its barrier also publishes alpha, beta)
-            const float cmax = wg_max(cV, red + 4, et, 1);
-            const float bound = amax * cmax * (fabsf(mV) + fabsf(dV) * (float)((1 << VB) - 1));
-            int e = 0;
-            if (bound > 32768.f) frexpf(bound * (1.0f / 32768.f), &e);
+            // (the reductions' barriers also publish alpha and beta)
+            const int e = group_exponent<VB>(aV, cV, dV, mV, red_all + 8 * b, et, 1);
             const float cs = ldexpf(cV, -e);
-            // K tile: row = token et
-#pragma unroll
-            for (int m = 0; m < 16; ++m)
-                *reinterpret_cast<uint4*>(set + kOffK + tile_off(et, 8 * m)) = codes8<KB>(ks_, m);
-            // V tile: row = channel et, f16 high parts in k-steps 0..7, the f16 rounding of
-            // the residuals in k-steps 8..15
+            // row = channel et: f16 high parts in k-steps 0..7, the f16 rounding of the
+            // residuals in k-steps 8..15
             const float2* al2 = reinterpret_cast<const float2*>(alpha);
             const float2* be2 = reinterpret_cast<const float2*>(beta);
 #pragma unroll 4
@@ -378,27 +471,10 @@ __device__ __forceinline__ void expand_role(const PrefillParams& p, const TcCta&
                 *reinterpret_cast<uint4*>(set + kOffV + tile_off(et, 128 + 8 * m)) =
                     make_uint4(lo[0], lo[1], lo[2], lo[3]);
             }
-            reinterpret_cast<float*>(set + kOffAK)[et] = aK;
-            if (et == 0) {
-                reinterpret_cast<float*>(set + kOffScal)[0] = dK;
-                reinterpret_cast<float*>(set + kOffScal)[1] = mK;
-                reinterpret_cast<float*>(set + kOffScal)[2] = (float)e;
-            }
         } else {
-            // exact block: K rows as they are, V rows transposed (movmatrix) into channel rows
-            const bool live = et < x.cnt;
-            const uint4* src = live ? exact_row(p, c, x.tail, 0, x.kp0 + et) : nullptr;
-            if (u >= 2) mbar_wait(bars + kBarTilesEmpty + b, (uint32_t)(((u >> 1) - 1) & 1), err);
-#pragma unroll 1
-            for (int i0 = 0; i0 < 16; i0 += 4) {
-                uint4 kr[4];
-#pragma unroll
-                for (int i = 0; i < 4; ++i) kr[i] = live ? src[i0 + i] : make_uint4(0u, 0u, 0u, 0u);
-#pragma unroll
-                for (int i = 0; i < 4; ++i)
-                    *reinterpret_cast<uint4*>(set + kOffK + tile_off(et, 8 * (i0 + i))) = kr[i];
-            }
-            // core matrix cm = (ks 16 + rg) 2 + kc: channels 8 rg .., tokens 16 ks + 8 kc ..
+            // exact block: V rows transposed (movmatrix) into channel rows; core matrix
+            // cm = (ks 16 + rg) 2 + kc holds channels 8 rg .., tokens 16 ks + 8 kc ..
+            if (u >= 2) mbar_wait(bars + kBarVEmpty + b, (uint32_t)(((u >> 1) - 1) & 1), err);
 #pragma unroll 1
             for (int hh = 0; hh < 2; ++hh) {
                 uint32_t a[32];
@@ -421,7 +497,7 @@ __device__ __forceinline__ void expand_role(const PrefillParams& p, const TcCta&
             }
         }
         fence_proxy_async_smem();
-        mbar_arrive(bars + kBarTilesFull + b);
+        mbar_arrive(bars + kBarVFull + b);
     }
 }
 
@@ -558,101 +634,109 @@ __device__ __forceinline__ void query_role(const PrefillParams& p, const TcCta& 
         }
         tm_wait_st();
         tc_fence_before();
-        named_bar(4, 384);
+        named_bar(4, 256);
     }
 }
 
-// O *= f over columns [c0, c0 + 64) of the thread's row (O complete up to the last PV issued)
-__device__ __forceinline__ void scale_o(uint32_t to, int c0, float f) {
+// O *= f over the thread's row (O complete up to the last PV issued)
+__device__ __forceinline__ void scale_o(uint32_t to, float f) {
 #pragma unroll 1
-    for (int ch = 0; ch < 2; ++ch) {
+    for (int ch = 0; ch < 4; ++ch) {
         uint32_t r[32];
-        tm_ld32(to + c0 + 32 * ch, r);
+        tm_ld32(to + 32 * ch, r);
         tm_wait_ld();
 #pragma unroll
         for (int j = 0; j < 32; ++j) r[j] = __float_as_uint(__uint_as_float(r[j]) * f);
-        tm_st32(to + c0 + 32 * ch, r);
+        tm_st32(to + 32 * ch, r);
     }
     tm_wait_st();
 }
 
-// ---- WG0 and WG1: softmax, rescaling and the output. Thread (h, i) takes row i's key
-// columns 64 h .. 64 h + 63 of every unit (and the same columns of O); the two halves of
-// a row exchange their maxima through shared memory once per unit. ----
+// Logits (log2 units) of 32 keys of a chunk, minus `sub`: sealed aK_t (al S + be) - sub,
+// exact S al - sub; keys past the block's end or the row's position are -inf.
+__device__ __forceinline__ void chunk_logits(const uint32_t (&r)[32], float (&w)[32], bool sealed, const float* aK,
+                                             int ch, float al, float be, float sub, bool masked, int kcnt, int kbase,
+                                             int pi) {
+    if (sealed) {
+#pragma unroll
+        for (int j4 = 0; j4 < 8; ++j4) {
+            const float4 a4 = reinterpret_cast<const float4*>(aK)[8 * ch + j4];
+            w[4 * j4] = fmaf(a4.x, fmaf(al, __uint_as_float(r[4 * j4]), be), -sub);
+            w[4 * j4 + 1] = fmaf(a4.y, fmaf(al, __uint_as_float(r[4 * j4 + 1]), be), -sub);
+            w[4 * j4 + 2] = fmaf(a4.z, fmaf(al, __uint_as_float(r[4 * j4 + 2]), be), -sub);
+            w[4 * j4 + 3] = fmaf(a4.w, fmaf(al, __uint_as_float(r[4 * j4 + 3]), be), -sub);
+        }
+    } else {
+#pragma unroll
+        for (int j = 0; j < 32; ++j) w[j] = fmaf(__uint_as_float(r[j]), al, -sub);
+    }
+    if (masked) {
+#pragma unroll
+        for (int j = 0; j < 32; ++j)
+            if (32 * ch + j >= kcnt || kbase + 32 * ch + j > pi) w[j] = kNegInfT;
+    }
+}
+
+// Weights of 16 keys (one k-step) as f16 high parts then the f16 rounding of the residuals.
+__device__ __forceinline__ void split16(const float* w, uint32_t* o) {
+#pragma unroll
+    for (int q = 0; q < 8; ++q) {
+        const __half2 hv = __floats2half2_rn(w[2 * q], w[2 * q + 1]);
+        const float2 hf = __half22float2(hv);
+        o[q] = h2u(hv);
+        o[8 + q] = h2u(__floats2half2_rn(w[2 * q] - hf.x, w[2 * q + 1] - hf.y));
+    }
+}
+
+// ---- WG0: softmax, rescaling and the output (thread i = row i) ----
 __device__ __forceinline__ void softmax_role(const PrefillParams& p, const TcCta& c, uint8_t* smem, uint64_t* bars,
-                                             uint32_t tmem, int32_t* err, int h, int i, uint32_t lane_off) {
+                                             uint32_t tmem, int32_t* err, int i, uint32_t lane_off) {
     const int pi = reinterpret_cast<const int*>(smem + kOffPos)[i];
     const float* rsring = reinterpret_cast<const float*>(smem + kOffRs);
-    float* xch = reinterpret_cast<float*>(smem + kOffXch);  // maxima [2 units][2 halves][128], sums [2][128]
     const uint32_t to = tmem + lane_off + kColO;
     float m_used = kNegInfT, l = 0.f, qm = 0.f;
     for (int u = 0; u < c.units; ++u) {
         const int b = u & 1;
         const Unit x = unit_of(c, u);
-        const uint8_t* set = smem + b * kSetBytes;
         if (!x.sealed && u == c.n_sealed && u > 0) {
             // all sealed groups are in O: the query warpgroup rotates it back to the
             // original frame before any thread here touches O again
             tc_fence_before();
-            named_bar(4, 384);
+            named_bar(4, 256);
             tc_fence_after();
         }
         mbar_wait(bars + kBarSFull + b, (uint32_t)((u >> 1) & 1), err);
-        mbar_wait(bars + kBarTilesFull + b, (uint32_t)((u >> 1) & 1), err);
-        if (x.sealed) mbar_wait(bars + kBarAFull + (u & 3), (uint32_t)((u >> 2) & 1), err);
-        tc_fence_after();
-        const uint32_t ts = tmem + lane_off + kColS + 128u * b;
-        // logit of token t (log2 units): sealed aK_t (al S + be), exact S scale; masked
-        // tokens (past the row's position or the block's end) are -inf
         float al = p.scale_log2, be = 0.f, e = 0.f;
-        const float* aK = reinterpret_cast<const float*>(set + kOffAK);
+        const float* kt = reinterpret_cast<const float*>(smem + kOffKtab + (u & 3) * kKtabBytes);
         int kbase, kcnt;
         if (x.sealed) {
+            mbar_wait(bars + kBarKFull + (u & 3), (uint32_t)((u >> 2) & 1), err);
+            mbar_wait(bars + kBarAFull + (u & 3), (uint32_t)((u >> 2) & 1), err);
             if (u == 0) qm = reinterpret_cast<const float*>(smem + kOffQm)[i];
-            const float* sc = reinterpret_cast<const float*>(set + kOffScal);
-            al = p.scale_log2 * qm * sc[0];
-            be = p.scale_log2 * qm * sc[1] * rsring[128 * (u & 3) + i];
-            e = sc[2];
+            al = p.scale_log2 * qm * kt[128];
+            be = p.scale_log2 * qm * kt[129] * rsring[128 * (u & 3) + i];
+            e = kt[130];
             kbase = kSink + kGroup * x.g;
             kcnt = kGroup;
         } else {
             kbase = x.kp0;
             kcnt = x.cnt;
         }
+        tc_fence_after();
+        const uint32_t ts = tmem + lane_off + kColS + 128u * b;
         const bool masked = kcnt < kGroup || kbase + kGroup - 1 > c.pmin;
-        // pass 1: the unit's row maximum over this thread's 64 columns, then the row's
+        // pass 1: the unit's row maximum
         float mx = kNegInfT;
 #pragma unroll 1
-        for (int ch = 2 * h; ch < 2 * h + 2; ++ch) {
+        for (int ch = 0; ch < 4; ++ch) {
             uint32_t r[32];
             tm_ld32(ts + 32 * ch, r);
             tm_wait_ld();
-            float sv[32];
-            if (x.sealed) {
+            float w[32];
+            chunk_logits(r, w, x.sealed, kt, ch, al, be, 0.f, masked, kcnt, kbase, pi);
 #pragma unroll
-                for (int j4 = 0; j4 < 8; ++j4) {
-                    const float4 a4 = reinterpret_cast<const float4*>(aK)[8 * ch + j4];
-                    sv[4 * j4] = a4.x * fmaf(al, __uint_as_float(r[4 * j4]), be);
-                    sv[4 * j4 + 1] = a4.y * fmaf(al, __uint_as_float(r[4 * j4 + 1]), be);
-                    sv[4 * j4 + 2] = a4.z * fmaf(al, __uint_as_float(r[4 * j4 + 2]), be);
-                    sv[4 * j4 + 3] = a4.w * fmaf(al, __uint_as_float(r[4 * j4 + 3]), be);
-                }
-            } else {
-#pragma unroll
-                for (int j = 0; j < 32; ++j) sv[j] = __uint_as_float(r[j]) * al;
-            }
-            if (masked) {
-#pragma unroll
-                for (int j = 0; j < 32; ++j)
-                    if (32 * ch + j >= kcnt || kbase + 32 * ch + j > pi) sv[j] = kNegInfT;
-            }
-#pragma unroll
-            for (int j = 0; j < 32; ++j) mx = fmaxf(mx, sv[j]);
+            for (int j = 0; j < 32; ++j) mx = fmaxf(mx, w[j]);
         }
-        float* xu = xch + 256 * (u & 1);
-        xu[128 * h + i] = mx;
-        named_bar(3, 256);
-        mx = fmaxf(mx, xu[128 * (h ^ 1) + i]);
         // raise the reference maximum where it grew by more than 8; O and l follow (O
         // holds PV of every earlier unit). Tensor-memory accesses are warp-wide: the
         // whole warp rescales, by 1 in the rows that keep their maximum.
@@ -665,7 +749,7 @@ __device__ __forceinline__ void softmax_role(const PrefillParams& p, const TcCta
         if (u > 0 && __any_sync(0xffffffffu, raise)) {
             wait_pv(bars, u - 1, err);
             tc_fence_after();
-            scale_o(to, 64 * h, corr);
+            scale_o(to, corr);
         }
         // pass 2: weights W = 2^(logit - m + e) as f16 high and low parts, written over the
         // chunk's own columns: k-step ks (16 tokens) holds the high parts in columns
@@ -673,46 +757,20 @@ __device__ __forceinline__ void softmax_role(const PrefillParams& p, const TcCta
         const float sub = (m_used == kNegInfT ? 0.f : m_used) - e;
         float ws0 = 0.f, ws1 = 0.f;
 #pragma unroll 1
-        for (int ch = 2 * h; ch < 2 * h + 2; ++ch) {
+        for (int ch = 0; ch < 4; ++ch) {
             uint32_t r[32];
             tm_ld32(ts + 32 * ch, r);
             tm_wait_ld();
             float w[32];
-            if (x.sealed) {
-#pragma unroll
-                for (int j4 = 0; j4 < 8; ++j4) {
-                    const float4 a4 = reinterpret_cast<const float4*>(aK)[8 * ch + j4];
-                    w[4 * j4] = fmaf(a4.x, fmaf(al, __uint_as_float(r[4 * j4]), be), -sub);
-                    w[4 * j4 + 1] = fmaf(a4.y, fmaf(al, __uint_as_float(r[4 * j4 + 1]), be), -sub);
-                    w[4 * j4 + 2] = fmaf(a4.z, fmaf(al, __uint_as_float(r[4 * j4 + 2]), be), -sub);
-                    w[4 * j4 + 3] = fmaf(a4.w, fmaf(al, __uint_as_float(r[4 * j4 + 3]), be), -sub);
-                }
-            } else {
-#pragma unroll
-                for (int j = 0; j < 32; ++j) w[j] = fmaf(__uint_as_float(r[j]), al, -sub);
-            }
-            if (masked) {
-#pragma unroll
-                for (int j = 0; j < 32; ++j)
-                    if (32 * ch + j >= kcnt || kbase + 32 * ch + j > pi) w[j] = kNegInfT;
-            }
+            chunk_logits(r, w, x.sealed, kt, ch, al, be, sub, masked, kcnt, kbase, pi);
 #pragma unroll
             for (int j = 0; j < 32; ++j) {
                 w[j] = ex2f(w[j]);
                 if (j & 1) ws1 += w[j]; else ws0 += w[j];
             }
             uint32_t o[32];
-#pragma unroll
-            for (int kk = 0; kk < 2; ++kk) {
-#pragma unroll
-                for (int q = 0; q < 8; ++q) {
-                    const float w0 = w[16 * kk + 2 * q], w1 = w[16 * kk + 2 * q + 1];
-                    const __half2 hv = __floats2half2_rn(w0, w1);
-                    const float2 hf = __half22float2(hv);
-                    o[16 * kk + q] = h2u(hv);
-                    o[16 * kk + 8 + q] = h2u(__floats2half2_rn(w0 - hf.x, w1 - hf.y));
-                }
-            }
+            split16(w, o);
+            split16(w + 16, o + 16);
             tm_st32(ts + 32 * ch, o);
         }
         l += ldexpf(ws0 + ws1, -(int)e);
@@ -720,21 +778,18 @@ __device__ __forceinline__ void softmax_role(const PrefillParams& p, const TcCta
         tc_fence_before();
         mbar_arrive(bars + kBarPFull + b);
     }
-    // normalise and write the row's 64 columns of this half
-    xch[512 + 128 * h + i] = l;
+    // normalise and write the row
     wait_pv(bars, c.units - 1, err);
-    named_bar(3, 256);
     tc_fence_after();
-    const float lt = xch[512 + i] + xch[640 + i];
     const int tok = c.t0 + i / p.r;
-    const float inv = lt > 0.f ? 1.0f / lt : 0.f;
+    const float inv = l > 0.f ? 1.0f / l : 0.f;
     uint4* dst = nullptr;
     if (tok < c.e->q_len) {
         const size_t orow = (size_t)(c.e->q_row + tok) * p.hq + (size_t)c.kvh * p.r + i % p.r;
         dst = reinterpret_cast<uint4*>(p.out + orow * kHeadDim);
     }
 #pragma unroll 1
-    for (int ch = 2 * h; ch < 2 * h + 2; ++ch) {
+    for (int ch = 0; ch < 4; ++ch) {
         uint32_t r[32];
         tm_ld32(to + 32 * ch, r);
         tm_wait_ld();
@@ -790,18 +845,19 @@ __global__ void __launch_bounds__(kTcThreads, 1) prefill_tc_kernel(const __grid_
         }
     }
     if (t == 0) {
-        mbar_init(bars + kBarTilesFull, 128);
-        mbar_init(bars + kBarTilesFull + 1, 128);
-        mbar_init(bars + kBarTilesEmpty, 1);
-        mbar_init(bars + kBarTilesEmpty + 1, 1);
-        for (int k = 0; k < 4; ++k) mbar_init(bars + kBarAFull + k, 128);
+        for (int k = 0; k < 4; ++k) {
+            mbar_init(bars + kBarKFull + k, 128);
+            mbar_init(bars + kBarAFull + k, 128);
+        }
+        for (int k = 0; k < 2; ++k) {
+            mbar_init(bars + kBarKEmpty + k, 1);
+            mbar_init(bars + kBarVFull + k, 128);
+            mbar_init(bars + kBarVEmpty + k, 1);
+            mbar_init(bars + kBarSFull + k, 1);
+            mbar_init(bars + kBarPFull + k, 128);
+            mbar_init(bars + kBarODone + k, 1);
+        }
         mbar_init(bars + kBarAEmpty, 1);
-        mbar_init(bars + kBarSFull, 1);
-        mbar_init(bars + kBarSFull + 1, 1);
-        mbar_init(bars + kBarPFull, 256);
-        mbar_init(bars + kBarPFull + 1, 256);
-        mbar_init(bars + kBarODone, 1);
-        mbar_init(bars + kBarODone + 1, 1);
         mbar_init(bars + kBarDrain, 1);
         asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
     }
@@ -816,14 +872,18 @@ __global__ void __launch_bounds__(kTcThreads, 1) prefill_tc_kernel(const __grid_
     tc_fence_after();
     const uint32_t tmem = *reinterpret_cast<volatile uint32_t*>(smem + kOffTmem);
     const uint32_t lane_off = (uint32_t)(32 * (w & 3)) << 16;
-    if (wg <= 1) {
-        softmax_role(p, c, smem, bars, tmem, err, wg, t & 127, lane_off);
-    } else if (wg == 2) {
+    if (wg == 0) {
+        asm volatile("setmaxnreg.inc.sync.aligned.u32 %0;" ::"n"(kRegsSoftmax));
+        softmax_role(p, c, smem, bars, tmem, err, t, lane_off);
+    } else if (wg == 1) {
         asm volatile("setmaxnreg.inc.sync.aligned.u32 %0;" ::"n"(kRegsQuery));
-        query_role(p, c, smem, bars, tmem, err, t - 256, lane_off);
+        query_role(p, c, smem, bars, tmem, err, t - 128, lane_off);
+    } else if (wg == 2) {
+        asm volatile("setmaxnreg.dec.sync.aligned.u32 %0;" ::"n"(kRegsExpandK));
+        expand_k_role<KB, VB>(p, c, smem, bars, err, t - 256);
     } else if (wg == 3) {
-        asm volatile("setmaxnreg.dec.sync.aligned.u32 %0;" ::"n"(kRegsExpand));
-        expand_role<KB, VB>(p, c, smem, bars, err, t - 384);
+        asm volatile("setmaxnreg.dec.sync.aligned.u32 %0;" ::"n"(kRegsExpandV));
+        expand_v_role<VB>(p, c, smem, bars, err, t - 384);
     } else {
         asm volatile("setmaxnreg.dec.sync.aligned.u32 %0;" ::"n"(kRegsIssue));
         if (w == 16 && lane == 0) {
