@@ -59,7 +59,7 @@ constexpr int kTcThreads = 640;      // five warpgroups
 constexpr int kRows = kPrefillRows;  // 128 query rows per CTA
 // registers a thread: 96 at launch (65536 / 640 rounded down to a multiple of 8), then
 // re-split per warpgroup (per scheduler: one warp of each warpgroup)
-constexpr int kRegsLaunch = 96, kRegsSoftmax = 128, kRegsQuery = 176, kRegsExpandK = 64, kRegsExpandV = 88,
+constexpr int kRegsLaunch = 96, kRegsSoftmax = 112, kRegsQuery = 176, kRegsExpandK = 96, kRegsExpandV = 72,
               kRegsIssue = 24;
 static_assert(kRegsSoftmax + kRegsQuery + kRegsExpandK + kRegsExpandV + kRegsIssue <= 5 * kRegsLaunch,
               "register split exceeds what a sub-partition holds at launch");
@@ -80,12 +80,13 @@ constexpr int kKtabBytes = 512 + 16;
 constexpr int kOffRs = kOffKtab + 4 * kKtabBytes;  // float[4][128] row sums, ring by unit
 constexpr int kOffRed = kOffRs + 4 * 128 * 4;   // float[2][2][8] expansion reductions (K, V warpgroups)
 constexpr int kOffCq = kOffRed + 128;           // float[2][128] channel scales of the next query operand
-constexpr int kOffPos = kOffCq + 1024;          // int[128] row positions
+constexpr int kOffMx = kOffCq + 1024;           // float[4][128] row maxima of the logits, ring by unit
+constexpr int kOffPos = kOffMx + 2048;          // int[128] row positions
 constexpr int kOffQm = kOffPos + 512;           // float[128] row maxima of the rotated query
 constexpr int kOffBars = kOffQm + 512;
 // barriers: k_full[4], k_empty[2], v_full[2], v_empty[2], a_full[4], a_empty, s_full[2],
-// p_full[2], o_done[2], drain
-constexpr int kNumBars = 22;
+// p_full[2], o_done[2], drain, m_full[4]
+constexpr int kNumBars = 26;
 constexpr int kOffTmem = kOffBars + 8 * kNumBars;
 constexpr int kSmemTc = kOffTmem + 16;
 static_assert(kSmemTc <= 227 * 1024, "shared memory of one CTA");
@@ -245,14 +246,15 @@ __device__ __forceinline__ const uint4* exact_row(const PrefillParams& p, const 
 
 // bars: [0, 4) k_full (by unit % 4), [4, 6) k_empty, [6, 8) v_full, [8, 10) v_empty,
 // [10, 14) a_full (by unit % 4), 14 a_empty, [15, 17) s_full, [17, 19) p_full,
-// [19, 21) o_done (PV of unit v completes phase v / 2 of o_done[v % 2]), 21 drain (once).
+// [19, 21) o_done (PV of unit v completes phase v / 2 of o_done[v % 2]), 21 drain (once),
+// [22, 26) m_full (by unit % 4: the unit's logits and row maxima are in place).
 // A barrier is indexed so that its previous phase has always completed when a thread
 // waits for the next: a parity wait cannot then be satisfied by an older phase. For
 // o_done this follows from tcgen05.mma completing in issue order: every wait for PV(v)
 // comes after its thread has seen QK(v) or a later MMA complete, and PV(v - 2) is issued
 // before QK(v) (QK(v) reuses the S buffer of PV(v - 2)'s weights).
 constexpr int kBarKFull = 0, kBarKEmpty = 4, kBarVFull = 6, kBarVEmpty = 8, kBarAFull = 10, kBarAEmpty = 14,
-              kBarSFull = 15, kBarPFull = 17, kBarODone = 19, kBarDrain = 21;
+              kBarSFull = 15, kBarPFull = 17, kBarODone = 19, kBarDrain = 21, kBarMFull = 22;
 
 // wait until PV of unit v has completed
 __device__ __forceinline__ void wait_pv(uint64_t* bars, int v, int32_t* err) {
@@ -361,63 +363,6 @@ __device__ __forceinline__ int group_exponent(float aV, float cV, float dV, floa
     return e;
 }
 
-// ---- WG2: the K tile and the K-side tables of every unit (thread et = 0..127) ----
-template <int KB, int VB>
-__device__ __forceinline__ void expand_k_role(const PrefillParams& p, const TcCta& c, uint8_t* smem, uint64_t* bars,
-                                              int32_t* err, int et) {
-    float* red_all = reinterpret_cast<float*>(smem + kOffRed);
-    for (int u = 0; u < c.units; ++u) {
-        const int b = u & 1;
-        const Unit x = unit_of(c, u);
-        uint8_t* set = smem + b * kSetBytes;
-        float* kt = reinterpret_cast<float*>(smem + kOffKtab + (u & 3) * kKtabBytes);
-        if (x.sealed) {
-            const uint8_t* kr = tc_group_src(p, c, x.g);
-            const uint8_t* vr = kr + p.rec_k;
-            uint32_t ks_[4 * KB];
-#pragma unroll
-            for (int i = 0; i < KB; ++i) {
-                const uint4 v4 = reinterpret_cast<const uint4*>(kr + 528 + et * 16 * KB)[i];
-                ks_[4 * i] = v4.x; ks_[4 * i + 1] = v4.y; ks_[4 * i + 2] = v4.z; ks_[4 * i + 3] = v4.w;
-            }
-            const float aK = __half2float(reinterpret_cast<const __half*>(kr + 16)[et]);
-            const float aV = __half2float(reinterpret_cast<const __half*>(vr + 16)[et]);
-            const float cV = __half2float(reinterpret_cast<const __half*>(vr + 272)[et]);
-            const float dK = *reinterpret_cast<const float*>(kr), mK = *reinterpret_cast<const float*>(kr + 4);
-            const float dV = *reinterpret_cast<const float*>(vr), mV = *reinterpret_cast<const float*>(vr + 4);
-            // the set's K tile is free once QK(u - 2) has completed; the table slot u % 4 once
-            // the softmax of unit u - 4 is done, which QK(u - 2) being issued implies
-            if (u >= 2) mbar_wait(bars + kBarKEmpty + b, (uint32_t)(((u >> 1) - 1) & 1), err);
-            const int e = group_exponent<VB>(aV, cV, dV, mV, red_all + 8 * b, et, 5);
-#pragma unroll
-            for (int m = 0; m < 16; ++m)
-                *reinterpret_cast<uint4*>(set + kOffK + tile_off(et, 8 * m)) = codes8<KB>(ks_, m);
-            kt[et] = aK;
-            if (et == 0) {
-                kt[128] = dK;
-                kt[129] = mK;
-                kt[130] = (float)e;
-            }
-        } else {
-            // exact block: the K rows as they are (rows past the block's end are zeros)
-            const bool live = et < x.cnt;
-            const uint4* src = live ? exact_row(p, c, x.tail, 0, x.kp0 + et) : nullptr;
-            if (u >= 2) mbar_wait(bars + kBarKEmpty + b, (uint32_t)(((u >> 1) - 1) & 1), err);
-#pragma unroll 1
-            for (int i0 = 0; i0 < 16; i0 += 4) {
-                uint4 kr[4];
-#pragma unroll
-                for (int i = 0; i < 4; ++i) kr[i] = live ? src[i0 + i] : make_uint4(0u, 0u, 0u, 0u);
-#pragma unroll
-                for (int i = 0; i < 4; ++i)
-                    *reinterpret_cast<uint4*>(set + kOffK + tile_off(et, 8 * (i0 + i))) = kr[i];
-            }
-        }
-        fence_proxy_async_smem();
-        mbar_arrive(bars + kBarKFull + (u & 3));
-    }
-}
-
 // ---- WG3: the V tile of every unit (thread et = 0..127) ----
 template <int VB>
 __device__ __forceinline__ void expand_v_role(const PrefillParams& p, const TcCta& c, uint8_t* smem, uint64_t* bars,
@@ -448,6 +393,7 @@ __device__ __forceinline__ void expand_v_role(const PrefillParams& p, const TcCt
             // (the reductions' barriers also publish alpha and beta)
             const int e = group_exponent<VB>(aV, cV, dV, mV, red_all + 8 * b, et, 1);
             const float cs = ldexpf(cV, -e);
+            const float2 cs2 = make_float2(cs, cs), m1 = make_float2(-1.f, -1.f);
             // row = channel et: f16 high parts in k-steps 0..7, the f16 rounding of the
             // residuals in k-steps 8..15
             const float2* al2 = reinterpret_cast<const float2*>(alpha);
@@ -459,13 +405,10 @@ __device__ __forceinline__ void expand_v_role(const PrefillParams& p, const TcCt
                 uint32_t hi[4], lo[4];
 #pragma unroll
                 for (int j = 0; j < 4; ++j) {
-                    const float2 qf = __half22float2(u2h(qw[j]));
-                    const float2 a2 = al2[4 * m + j], b2 = be2[4 * m + j];
-                    const float x0 = cs * fmaf(qf.x, a2.x, b2.x), x1 = cs * fmaf(qf.y, a2.y, b2.y);
-                    const __half2 h = __floats2half2_rn(x0, x1);
-                    const float2 hf = __half22float2(h);
+                    const float2 x = __fmul2_rn(cs2, __ffma2_rn(__half22float2(u2h(qw[j])), al2[4 * m + j], be2[4 * m + j]));
+                    const __half2 h = __float22half2_rn(x);
                     hi[j] = h2u(h);
-                    lo[j] = h2u(__floats2half2_rn(x0 - hf.x, x1 - hf.y));
+                    lo[j] = h2u(__float22half2_rn(__ffma2_rn(__half22float2(h), m1, x)));
                 }
                 *reinterpret_cast<uint4*>(set + kOffV + tile_off(et, 8 * m)) = make_uint4(hi[0], hi[1], hi[2], hi[3]);
                 *reinterpret_cast<uint4*>(set + kOffV + tile_off(et, 128 + 8 * m)) =
@@ -566,7 +509,8 @@ __device__ __forceinline__ void query_role(const PrefillParams& p, const TcCta& 
             named_bar(2, 128);
             if (u >= 1) mbar_wait(bars + kBarAEmpty, (uint32_t)((u - 1) & 1), err);
             tc_fence_after();
-            float rs0 = 0.f, rs1 = 0.f;
+            float2 rs2 = make_float2(0.f, 0.f);
+            const float2 m1 = make_float2(-1.f, -1.f);
 #pragma unroll
             for (int cc = 0; cc < 8; ++cc) {
                 uint32_t hi[8], lo[8];
@@ -574,21 +518,20 @@ __device__ __forceinline__ void query_role(const PrefillParams& p, const TcCta& 
                 for (int qd = 0; qd < 4; ++qd) {
                     const float4 c4 = reinterpret_cast<const float4*>(cu)[4 * cc + qd];
                     const int ch = 16 * cc + 4 * qd;
-                    const float x0 = v[ch] * c4.x, x1 = v[ch + 1] * c4.y, x2 = v[ch + 2] * c4.z, x3 = v[ch + 3] * c4.w;
-                    rs0 += x0 + x1;
-                    rs1 += x2 + x3;
-                    const __half2 h01 = __floats2half2_rn(x0, x1), h23 = __floats2half2_rn(x2, x3);
-                    const float2 f01 = __half22float2(h01), f23 = __half22float2(h23);
+                    const float2 x01 = __fmul2_rn(make_float2(v[ch], v[ch + 1]), make_float2(c4.x, c4.y));
+                    const float2 x23 = __fmul2_rn(make_float2(v[ch + 2], v[ch + 3]), make_float2(c4.z, c4.w));
+                    rs2 = __fadd2_rn(rs2, __fadd2_rn(x01, x23));
+                    const __half2 h01 = __float22half2_rn(x01), h23 = __float22half2_rn(x23);
                     hi[2 * qd] = h2u(h01);
                     hi[2 * qd + 1] = h2u(h23);
-                    lo[2 * qd] = h2u(__floats2half2_rn(x0 - f01.x, x1 - f01.y));
-                    lo[2 * qd + 1] = h2u(__floats2half2_rn(x2 - f23.x, x3 - f23.y));
+                    lo[2 * qd] = h2u(__float22half2_rn(__ffma2_rn(__half22float2(h01), m1, x01)));
+                    lo[2 * qd + 1] = h2u(__float22half2_rn(__ffma2_rn(__half22float2(h23), m1, x23)));
                 }
                 tm_st8(ta + 8 * cc, hi);
                 tm_st8(ta + 64 + 8 * cc, lo);
             }
             tm_wait_st();
-            rsring[128 * (u & 3) + i] = rs0 + rs1;
+            rsring[128 * (u & 3) + i] = rs2.x + rs2.y;
             tc_fence_before();
             mbar_arrive(bars + kBarAFull + (u & 3));
         }
@@ -657,18 +600,30 @@ __device__ __forceinline__ void scale_o(uint32_t to, float f) {
 __device__ __forceinline__ void chunk_logits(const uint32_t (&r)[32], float (&w)[32], bool sealed, const float* aK,
                                              int ch, float al, float be, float sub, bool masked, int kcnt, int kbase,
                                              int pi) {
+    const float2 al2 = make_float2(al, al), ns2 = make_float2(-sub, -sub);
     if (sealed) {
+        const float2 be2 = make_float2(be, be);
 #pragma unroll
         for (int j4 = 0; j4 < 8; ++j4) {
             const float4 a4 = reinterpret_cast<const float4*>(aK)[8 * ch + j4];
-            w[4 * j4] = fmaf(a4.x, fmaf(al, __uint_as_float(r[4 * j4]), be), -sub);
-            w[4 * j4 + 1] = fmaf(a4.y, fmaf(al, __uint_as_float(r[4 * j4 + 1]), be), -sub);
-            w[4 * j4 + 2] = fmaf(a4.z, fmaf(al, __uint_as_float(r[4 * j4 + 2]), be), -sub);
-            w[4 * j4 + 3] = fmaf(a4.w, fmaf(al, __uint_as_float(r[4 * j4 + 3]), be), -sub);
+            const float2 s01 = __ffma2_rn(al2, make_float2(__uint_as_float(r[4 * j4]), __uint_as_float(r[4 * j4 + 1])), be2);
+            const float2 s23 =
+                __ffma2_rn(al2, make_float2(__uint_as_float(r[4 * j4 + 2]), __uint_as_float(r[4 * j4 + 3])), be2);
+            const float2 w01 = __ffma2_rn(make_float2(a4.x, a4.y), s01, ns2);
+            const float2 w23 = __ffma2_rn(make_float2(a4.z, a4.w), s23, ns2);
+            w[4 * j4] = w01.x;
+            w[4 * j4 + 1] = w01.y;
+            w[4 * j4 + 2] = w23.x;
+            w[4 * j4 + 3] = w23.y;
         }
     } else {
 #pragma unroll
-        for (int j = 0; j < 32; ++j) w[j] = fmaf(__uint_as_float(r[j]), al, -sub);
+        for (int j2 = 0; j2 < 16; ++j2) {
+            const float2 w2 =
+                __ffma2_rn(make_float2(__uint_as_float(r[2 * j2]), __uint_as_float(r[2 * j2 + 1])), al2, ns2);
+            w[2 * j2] = w2.x;
+            w[2 * j2 + 1] = w2.y;
+        }
     }
     if (masked) {
 #pragma unroll
@@ -679,22 +634,133 @@ __device__ __forceinline__ void chunk_logits(const uint32_t (&r)[32], float (&w)
 
 // Weights of 16 keys (one k-step) as f16 high parts then the f16 rounding of the residuals.
 __device__ __forceinline__ void split16(const float* w, uint32_t* o) {
+    const float2 m1 = make_float2(-1.f, -1.f);
 #pragma unroll
     for (int q = 0; q < 8; ++q) {
-        const __half2 hv = __floats2half2_rn(w[2 * q], w[2 * q + 1]);
-        const float2 hf = __half22float2(hv);
+        const float2 x = make_float2(w[2 * q], w[2 * q + 1]);
+        const __half2 hv = __float22half2_rn(x);
         o[q] = h2u(hv);
-        o[8 + q] = h2u(__floats2half2_rn(w[2 * q] - hf.x, w[2 * q + 1] - hf.y));
+        o[8 + q] = h2u(__float22half2_rn(__ffma2_rn(__half22float2(hv), m1, x)));
+    }
+}
+
+// ---- WG2: the K tile and the K-side tables of unit u (thread et = 0..127) ----
+template <int KB, int VB>
+__device__ __forceinline__ void expand_k_unit(const PrefillParams& p, const TcCta& c, uint8_t* smem, uint64_t* bars,
+                                              int32_t* err, int et, int u) {
+    float* red_all = reinterpret_cast<float*>(smem + kOffRed);
+    const int b = u & 1;
+    const Unit x = unit_of(c, u);
+    uint8_t* set = smem + b * kSetBytes;
+    float* kt = reinterpret_cast<float*>(smem + kOffKtab + (u & 3) * kKtabBytes);
+    if (x.sealed) {
+        const uint8_t* kr = tc_group_src(p, c, x.g);
+        const uint8_t* vr = kr + p.rec_k;
+        uint32_t ks_[4 * KB];
+#pragma unroll
+        for (int i = 0; i < KB; ++i) {
+            const uint4 v4 = reinterpret_cast<const uint4*>(kr + 528 + et * 16 * KB)[i];
+            ks_[4 * i] = v4.x; ks_[4 * i + 1] = v4.y; ks_[4 * i + 2] = v4.z; ks_[4 * i + 3] = v4.w;
+        }
+        const float aK = __half2float(reinterpret_cast<const __half*>(kr + 16)[et]);
+        const float aV = __half2float(reinterpret_cast<const __half*>(vr + 16)[et]);
+        const float cV = __half2float(reinterpret_cast<const __half*>(vr + 272)[et]);
+        const float dK = *reinterpret_cast<const float*>(kr), mK = *reinterpret_cast<const float*>(kr + 4);
+        const float dV = *reinterpret_cast<const float*>(vr), mV = *reinterpret_cast<const float*>(vr + 4);
+        // the set's K tile is free once QK(u - 2) has completed; the table slot u % 4 once
+        // the softmax of unit u - 4 is done, which QK(u - 2) being issued implies
+        if (u >= 2) mbar_wait(bars + kBarKEmpty + b, (uint32_t)(((u >> 1) - 1) & 1), err);
+        const int e = group_exponent<VB>(aV, cV, dV, mV, red_all + 8 * b, et, 5);
+#pragma unroll
+        for (int m = 0; m < 16; ++m)
+            *reinterpret_cast<uint4*>(set + kOffK + tile_off(et, 8 * m)) = codes8<KB>(ks_, m);
+        kt[et] = aK;
+        if (et == 0) {
+            kt[128] = dK;
+            kt[129] = mK;
+            kt[130] = (float)e;
+        }
+    } else {
+        // exact block: the K rows as they are (rows past the block's end are zeros)
+        const bool live = et < x.cnt;
+        const uint4* src = live ? exact_row(p, c, x.tail, 0, x.kp0 + et) : nullptr;
+        if (u >= 2) mbar_wait(bars + kBarKEmpty + b, (uint32_t)(((u >> 1) - 1) & 1), err);
+#pragma unroll 1
+        for (int i0 = 0; i0 < 16; i0 += 4) {
+            uint4 kr[4];
+#pragma unroll
+            for (int i = 0; i < 4; ++i) kr[i] = live ? src[i0 + i] : make_uint4(0u, 0u, 0u, 0u);
+#pragma unroll
+            for (int i = 0; i < 4; ++i) *reinterpret_cast<uint4*>(set + kOffK + tile_off(et, 8 * (i0 + i))) = kr[i];
+        }
+    }
+    fence_proxy_async_smem();
+    mbar_arrive(bars + kBarKFull + (u & 3));
+}
+
+// ---- WG2: the logits of unit v for row i (once QK(v) has completed): written back
+// over S as fp32 (log2 units, masked keys -inf), the row maximum into the ring ----
+__device__ __forceinline__ void logits_unit(const PrefillParams& p, const TcCta& c, uint8_t* smem, uint64_t* bars,
+                                            uint32_t tmem, int32_t* err, int i, uint32_t lane_off, int v) {
+    const int b = v & 1;
+    const Unit x = unit_of(c, v);
+    const int pi = reinterpret_cast<const int*>(smem + kOffPos)[i];
+    const float* kt = reinterpret_cast<const float*>(smem + kOffKtab + (v & 3) * kKtabBytes);
+    mbar_wait(bars + kBarSFull + b, (uint32_t)((v >> 1) & 1), err);
+    float al = p.scale_log2, be = 0.f;
+    int kbase, kcnt;
+    if (x.sealed) {
+        mbar_wait(bars + kBarAFull + (v & 3), (uint32_t)((v >> 2) & 1), err);
+        const float qm = reinterpret_cast<const float*>(smem + kOffQm)[i];
+        al = p.scale_log2 * qm * kt[128];
+        be = p.scale_log2 * qm * kt[129] * reinterpret_cast<const float*>(smem + kOffRs)[128 * (v & 3) + i];
+        kbase = kSink + kGroup * x.g;
+        kcnt = kGroup;
+    } else {
+        kbase = x.kp0;
+        kcnt = x.cnt;
+    }
+    tc_fence_after();
+    const uint32_t ts = tmem + lane_off + kColS + 128u * b;
+    const bool masked = kcnt < kGroup || kbase + kGroup - 1 > c.pmin;
+    float mx = kNegInfT;
+#pragma unroll 1
+    for (int ch = 0; ch < 4; ++ch) {
+        uint32_t r[32];
+        tm_ld32(ts + 32 * ch, r);
+        tm_wait_ld();
+        float w[32];
+        chunk_logits(r, w, x.sealed, kt, ch, al, be, 0.f, masked, kcnt, kbase, pi);
+#pragma unroll
+        for (int j = 0; j < 32; ++j) {
+            mx = fmaxf(mx, w[j]);
+            r[j] = __float_as_uint(w[j]);
+        }
+        tm_st32(ts + 32 * ch, r);
+    }
+    reinterpret_cast<float*>(smem + kOffMx)[128 * (v & 3) + i] = mx;
+    tm_wait_st();
+    tc_fence_before();
+    mbar_arrive(bars + kBarMFull + (v & 3));
+}
+
+// WG2's loop: the K tiles of units 0 and 1, then per unit v the logits of v (as soon as
+// QK(v) completes) followed by the K tile of v + 2 (whose slot QK(v) has just freed).
+template <int KB, int VB>
+__device__ __forceinline__ void k_role(const PrefillParams& p, const TcCta& c, uint8_t* smem, uint64_t* bars,
+                                       uint32_t tmem, int32_t* err, int et, uint32_t lane_off) {
+    for (int u = 0; u < 2 && u < c.units; ++u) expand_k_unit<KB, VB>(p, c, smem, bars, err, et, u);
+    for (int v = 0; v < c.units; ++v) {
+        logits_unit(p, c, smem, bars, tmem, err, et, lane_off, v);
+        if (v + 2 < c.units) expand_k_unit<KB, VB>(p, c, smem, bars, err, et, v + 2);
     }
 }
 
 // ---- WG0: softmax, rescaling and the output (thread i = row i) ----
 __device__ __forceinline__ void softmax_role(const PrefillParams& p, const TcCta& c, uint8_t* smem, uint64_t* bars,
                                              uint32_t tmem, int32_t* err, int i, uint32_t lane_off) {
-    const int pi = reinterpret_cast<const int*>(smem + kOffPos)[i];
-    const float* rsring = reinterpret_cast<const float*>(smem + kOffRs);
     const uint32_t to = tmem + lane_off + kColO;
-    float m_used = kNegInfT, l = 0.f, qm = 0.f;
+    float m_used = kNegInfT, l = 0.f;
     for (int u = 0; u < c.units; ++u) {
         const int b = u & 1;
         const Unit x = unit_of(c, u);
@@ -705,38 +771,12 @@ __device__ __forceinline__ void softmax_role(const PrefillParams& p, const TcCta
             named_bar(4, 256);
             tc_fence_after();
         }
-        mbar_wait(bars + kBarSFull + b, (uint32_t)((u >> 1) & 1), err);
-        float al = p.scale_log2, be = 0.f, e = 0.f;
-        const float* kt = reinterpret_cast<const float*>(smem + kOffKtab + (u & 3) * kKtabBytes);
-        int kbase, kcnt;
-        if (x.sealed) {
-            mbar_wait(bars + kBarKFull + (u & 3), (uint32_t)((u >> 2) & 1), err);
-            mbar_wait(bars + kBarAFull + (u & 3), (uint32_t)((u >> 2) & 1), err);
-            if (u == 0) qm = reinterpret_cast<const float*>(smem + kOffQm)[i];
-            al = p.scale_log2 * qm * kt[128];
-            be = p.scale_log2 * qm * kt[129] * rsring[128 * (u & 3) + i];
-            e = kt[130];
-            kbase = kSink + kGroup * x.g;
-            kcnt = kGroup;
-        } else {
-            kbase = x.kp0;
-            kcnt = x.cnt;
-        }
+        // the unit's logits (over S) and row maximum, from the K warpgroup
+        mbar_wait(bars + kBarMFull + (u & 3), (uint32_t)((u >> 2) & 1), err);
+        const float e = x.sealed ? reinterpret_cast<const float*>(smem + kOffKtab + (u & 3) * kKtabBytes)[130] : 0.f;
+        const float mx = reinterpret_cast<const float*>(smem + kOffMx)[128 * (u & 3) + i];
         tc_fence_after();
         const uint32_t ts = tmem + lane_off + kColS + 128u * b;
-        const bool masked = kcnt < kGroup || kbase + kGroup - 1 > c.pmin;
-        // pass 1: the unit's row maximum
-        float mx = kNegInfT;
-#pragma unroll 1
-        for (int ch = 0; ch < 4; ++ch) {
-            uint32_t r[32];
-            tm_ld32(ts + 32 * ch, r);
-            tm_wait_ld();
-            float w[32];
-            chunk_logits(r, w, x.sealed, kt, ch, al, be, 0.f, masked, kcnt, kbase, pi);
-#pragma unroll
-            for (int j = 0; j < 32; ++j) mx = fmaxf(mx, w[j]);
-        }
         // raise the reference maximum where it grew by more than 8; O and l follow (O
         // holds PV of every earlier unit). Tensor-memory accesses are warp-wide: the
         // whole warp rescales, by 1 in the rows that keep their maximum.
@@ -751,10 +791,11 @@ __device__ __forceinline__ void softmax_role(const PrefillParams& p, const TcCta
             tc_fence_after();
             scale_o(to, corr);
         }
-        // pass 2: weights W = 2^(logit - m + e) as f16 high and low parts, written over the
+        // weights W = 2^(logit - m + e) as f16 high and low parts, written over the
         // chunk's own columns: k-step ks (16 tokens) holds the high parts in columns
         // 16 ks .. 16 ks + 7 and the low parts in 16 ks + 8 .. 16 ks + 15
         const float sub = (m_used == kNegInfT ? 0.f : m_used) - e;
+        const float2 ns2 = make_float2(-sub, -sub);
         float ws0 = 0.f, ws1 = 0.f;
 #pragma unroll 1
         for (int ch = 0; ch < 4; ++ch) {
@@ -762,12 +803,16 @@ __device__ __forceinline__ void softmax_role(const PrefillParams& p, const TcCta
             tm_ld32(ts + 32 * ch, r);
             tm_wait_ld();
             float w[32];
-            chunk_logits(r, w, x.sealed, kt, ch, al, be, sub, masked, kcnt, kbase, pi);
+            float2 ws2 = make_float2(0.f, 0.f);
 #pragma unroll
-            for (int j = 0; j < 32; ++j) {
-                w[j] = ex2f(w[j]);
-                if (j & 1) ws1 += w[j]; else ws0 += w[j];
+            for (int j2 = 0; j2 < 16; ++j2) {
+                const float2 d = __fadd2_rn(make_float2(__uint_as_float(r[2 * j2]), __uint_as_float(r[2 * j2 + 1])), ns2);
+                w[2 * j2] = ex2f(d.x);
+                w[2 * j2 + 1] = ex2f(d.y);
+                ws2 = __fadd2_rn(ws2, make_float2(w[2 * j2], w[2 * j2 + 1]));
             }
+            ws0 += ws2.x;
+            ws1 += ws2.y;
             uint32_t o[32];
             split16(w, o);
             split16(w + 16, o + 16);
@@ -848,6 +893,7 @@ __global__ void __launch_bounds__(kTcThreads, 1) prefill_tc_kernel(const __grid_
         for (int k = 0; k < 4; ++k) {
             mbar_init(bars + kBarKFull + k, 128);
             mbar_init(bars + kBarAFull + k, 128);
+            mbar_init(bars + kBarMFull + k, 128);
         }
         for (int k = 0; k < 2; ++k) {
             mbar_init(bars + kBarKEmpty + k, 1);
@@ -880,7 +926,7 @@ __global__ void __launch_bounds__(kTcThreads, 1) prefill_tc_kernel(const __grid_
         query_role(p, c, smem, bars, tmem, err, t - 128, lane_off);
     } else if (wg == 2) {
         asm volatile("setmaxnreg.dec.sync.aligned.u32 %0;" ::"n"(kRegsExpandK));
-        expand_k_role<KB, VB>(p, c, smem, bars, err, t - 256);
+        k_role<KB, VB>(p, c, smem, bars, tmem, err, t - 256, lane_off);
     } else if (wg == 3) {
         asm volatile("setmaxnreg.dec.sync.aligned.u32 %0;" ::"n"(kRegsExpandV));
         expand_v_role<VB>(p, c, smem, bars, err, t - 384);
