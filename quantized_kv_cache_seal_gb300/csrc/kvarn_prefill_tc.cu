@@ -83,7 +83,8 @@ constexpr int kOffCq = kOffRed + 128;           // float[2][128] channel scales 
 constexpr int kOffMx = kOffCq + 1024;           // float[4][128] row maxima of the logits, ring by unit
 constexpr int kOffPos = kOffMx + 2048;          // int[128] row positions
 constexpr int kOffQm = kOffPos + 512;           // float[128] row maxima of the rotated query
-constexpr int kOffBars = kOffQm + 512;
+constexpr int kOffVst = kOffQm + 512;           // uint32[32][128] the V expansion's code words (word k of thread t at k 128 + t)
+constexpr int kOffBars = kOffVst + 32 * 128 * 4;
 // barriers: k_full[4], k_empty[2], v_full[2], v_empty[2], a_full[4], a_empty, s_full[2],
 // p_full[2], o_done[2], drain, m_full[4]
 constexpr int kNumBars = 26;
@@ -182,6 +183,25 @@ __device__ __forceinline__ uint4 codes8(const uint32_t (&s)[4 * B], int m) {
     for (int k = 0; k < 4; ++k) {
         const uint32_t f = bits_of(s, (8 * m + 2 * k) * B, 2 * B);
         // 0x6400 | c is the half 1024 + c; subtracting 1024 leaves c exactly
+        const uint32_t w = ((f & mask) | ((f >> B) << 16)) | 0x64006400u;
+        o[k] = h2u(__hsub2(u2h(w), __halves2half2(__ushort_as_half(0x6400), __ushort_as_half(0x6400))));
+    }
+    return make_uint4(o[0], o[1], o[2], o[3]);
+}
+
+// Codes 8 m .. 8 m + 7 of a row of 128 B-bit codes staged as words k at col[128 k], as
+// four words of two f16 integers each (exact); m may vary at run time.
+template <int B>
+__device__ __forceinline__ uint4 codes8_staged(const uint32_t* col, int m) {
+    constexpr uint32_t mask = (1u << B) - 1u;
+    const int pos = 8 * B * m, lo = pos >> 5, sh = pos & 31;
+    uint64_t bits = col[128 * lo];
+    if (sh + 8 * B > 32) bits |= (uint64_t)col[128 * (lo + 1)] << 32;
+    bits >>= sh;
+    uint32_t o[4];
+#pragma unroll
+    for (int k = 0; k < 4; ++k) {
+        const uint32_t f = (uint32_t)(bits >> (2 * B * k)) & ((1u << (2 * B)) - 1u);
         const uint32_t w = ((f & mask) | ((f >> B) << 16)) | 0x64006400u;
         o[k] = h2u(__hsub2(u2h(w), __halves2half2(__ushort_as_half(0x6400), __ushort_as_half(0x6400))));
     }
@@ -363,27 +383,47 @@ __device__ __forceinline__ int group_exponent(float aV, float cV, float dV, floa
     return e;
 }
 
+// What a thread of an expansion warpgroup reads of one record: its row of 128 codes
+// (B bits each) and the scales of its token / channel index.
+template <int B>
+struct RecRow {
+    uint32_t w[4 * B];
+    float a, cV, aV, d, m, dV, mV;
+};
+
+// Loads of unit u's V record for thread et, issued a unit ahead of their use.
+template <int VB>
+__device__ __forceinline__ void load_v(const PrefillParams& p, const TcCta& c, int u, int et, RecRow<VB>& L) {
+    if (u >= c.n_sealed) return;
+    const uint8_t* vr = tc_group_src(p, c, u) + p.rec_k;
+#pragma unroll
+    for (int i = 0; i < VB; ++i) {
+        const uint4 v4 = reinterpret_cast<const uint4*>(vr + 528 + et * 16 * VB)[i];
+        L.w[4 * i] = v4.x; L.w[4 * i + 1] = v4.y; L.w[4 * i + 2] = v4.z; L.w[4 * i + 3] = v4.w;
+    }
+    L.aV = __half2float(reinterpret_cast<const __half*>(vr + 16)[et]);
+    L.cV = __half2float(reinterpret_cast<const __half*>(vr + 272)[et]);
+    L.dV = *reinterpret_cast<const float*>(vr);
+    L.mV = *reinterpret_cast<const float*>(vr + 4);
+}
+
 // ---- WG3: the V tile of every unit (thread et = 0..127) ----
 template <int VB>
 __device__ __forceinline__ void expand_v_role(const PrefillParams& p, const TcCta& c, uint8_t* smem, uint64_t* bars,
                                               int32_t* err, int et) {
     const int lane = et & 31, wv = et >> 5;
     float* red_all = reinterpret_cast<float*>(smem + kOffRed) + 16;
+    RecRow<VB> nx;
+    load_v<VB>(p, c, 0, et, nx);
     for (int u = 0; u < c.units; ++u) {
         const int b = u & 1;
         const Unit x = unit_of(c, u);
         uint8_t* set = smem + b * kSetBytes;
         if (x.sealed) {
-            const uint8_t* vr = tc_group_src(p, c, x.g) + p.rec_k;
-            uint32_t vs_[4 * VB];
-#pragma unroll
-            for (int i = 0; i < VB; ++i) {
-                const uint4 v4 = reinterpret_cast<const uint4*>(vr + 528 + et * 16 * VB)[i];
-                vs_[4 * i] = v4.x; vs_[4 * i + 1] = v4.y; vs_[4 * i + 2] = v4.z; vs_[4 * i + 3] = v4.w;
-            }
-            const float aV = __half2float(reinterpret_cast<const __half*>(vr + 16)[et]);
-            const float cV = __half2float(reinterpret_cast<const __half*>(vr + 272)[et]);
-            const float dV = *reinterpret_cast<const float*>(vr), mV = *reinterpret_cast<const float*>(vr + 4);
+            const RecRow<VB> L = nx;
+            load_v<VB>(p, c, u + 1, et, nx);
+            const uint32_t(&vs_)[4 * VB] = L.w;
+            const float aV = L.aV, cV = L.cV, dV = L.dV, mV = L.mV;
             if (u >= 2) mbar_wait(bars + kBarVEmpty + b, (uint32_t)(((u >> 1) - 1) & 1), err);
             // B = the dequantised value in the rotated frame, c_j aV_t (deltaV q_tj + mV), times 2^-e
             float* alpha = reinterpret_cast<float*>(set + kOffAlpha);
@@ -398,9 +438,12 @@ __device__ __forceinline__ void expand_v_role(const PrefillParams& p, const TcCt
             // residuals in k-steps 8..15
             const float2* al2 = reinterpret_cast<const float2*>(alpha);
             const float2* be2 = reinterpret_cast<const float2*>(beta);
-#pragma unroll 4
+            uint32_t* vst = reinterpret_cast<uint32_t*>(smem + kOffVst) + et;
+#pragma unroll
+            for (int k = 0; k < 4 * VB; ++k) vst[128 * k] = vs_[k];
+#pragma unroll 1
             for (int m = 0; m < 16; ++m) {
-                const uint4 q4 = codes8<VB>(vs_, m);
+                const uint4 q4 = codes8_staged<VB>(vst, m);
                 const uint32_t qw[4] = {q4.x, q4.y, q4.z, q4.w};
                 uint32_t hi[4], lo[4];
 #pragma unroll
@@ -644,40 +687,48 @@ __device__ __forceinline__ void split16(const float* w, uint32_t* o) {
     }
 }
 
+// Loads of unit u's K record (and the V header the group's power of two needs) for
+// thread et, issued ahead of their use.
+template <int KB>
+__device__ __forceinline__ void load_k(const PrefillParams& p, const TcCta& c, int u, int et, RecRow<KB>& L) {
+    if (u >= c.n_sealed) return;
+    const uint8_t* kr = tc_group_src(p, c, u);
+    const uint8_t* vr = kr + p.rec_k;
+#pragma unroll
+    for (int i = 0; i < KB; ++i) {
+        const uint4 v4 = reinterpret_cast<const uint4*>(kr + 528 + et * 16 * KB)[i];
+        L.w[4 * i] = v4.x; L.w[4 * i + 1] = v4.y; L.w[4 * i + 2] = v4.z; L.w[4 * i + 3] = v4.w;
+    }
+    L.a = __half2float(reinterpret_cast<const __half*>(kr + 16)[et]);
+    L.d = *reinterpret_cast<const float*>(kr);
+    L.m = *reinterpret_cast<const float*>(kr + 4);
+    L.aV = __half2float(reinterpret_cast<const __half*>(vr + 16)[et]);
+    L.cV = __half2float(reinterpret_cast<const __half*>(vr + 272)[et]);
+    L.dV = *reinterpret_cast<const float*>(vr);
+    L.mV = *reinterpret_cast<const float*>(vr + 4);
+}
+
 // ---- WG2: the K tile and the K-side tables of unit u (thread et = 0..127) ----
 template <int KB, int VB>
 __device__ __forceinline__ void expand_k_unit(const PrefillParams& p, const TcCta& c, uint8_t* smem, uint64_t* bars,
-                                              int32_t* err, int et, int u) {
+                                              int32_t* err, int et, int u, const RecRow<KB>& L) {
     float* red_all = reinterpret_cast<float*>(smem + kOffRed);
     const int b = u & 1;
     const Unit x = unit_of(c, u);
     uint8_t* set = smem + b * kSetBytes;
     float* kt = reinterpret_cast<float*>(smem + kOffKtab + (u & 3) * kKtabBytes);
     if (x.sealed) {
-        const uint8_t* kr = tc_group_src(p, c, x.g);
-        const uint8_t* vr = kr + p.rec_k;
-        uint32_t ks_[4 * KB];
-#pragma unroll
-        for (int i = 0; i < KB; ++i) {
-            const uint4 v4 = reinterpret_cast<const uint4*>(kr + 528 + et * 16 * KB)[i];
-            ks_[4 * i] = v4.x; ks_[4 * i + 1] = v4.y; ks_[4 * i + 2] = v4.z; ks_[4 * i + 3] = v4.w;
-        }
-        const float aK = __half2float(reinterpret_cast<const __half*>(kr + 16)[et]);
-        const float aV = __half2float(reinterpret_cast<const __half*>(vr + 16)[et]);
-        const float cV = __half2float(reinterpret_cast<const __half*>(vr + 272)[et]);
-        const float dK = *reinterpret_cast<const float*>(kr), mK = *reinterpret_cast<const float*>(kr + 4);
-        const float dV = *reinterpret_cast<const float*>(vr), mV = *reinterpret_cast<const float*>(vr + 4);
         // the set's K tile is free once QK(u - 2) has completed; the table slot u % 4 once
         // the softmax of unit u - 4 is done, which QK(u - 2) being issued implies
         if (u >= 2) mbar_wait(bars + kBarKEmpty + b, (uint32_t)(((u >> 1) - 1) & 1), err);
-        const int e = group_exponent<VB>(aV, cV, dV, mV, red_all + 8 * b, et, 5);
+        const int e = group_exponent<VB>(L.aV, L.cV, L.dV, L.mV, red_all + 8 * b, et, 5);
 #pragma unroll
         for (int m = 0; m < 16; ++m)
-            *reinterpret_cast<uint4*>(set + kOffK + tile_off(et, 8 * m)) = codes8<KB>(ks_, m);
-        kt[et] = aK;
+            *reinterpret_cast<uint4*>(set + kOffK + tile_off(et, 8 * m)) = codes8<KB>(L.w, m);
+        kt[et] = L.a;
         if (et == 0) {
-            kt[128] = dK;
-            kt[129] = mK;
+            kt[128] = L.d;
+            kt[129] = L.m;
             kt[130] = (float)e;
         }
     } else {
@@ -745,14 +796,21 @@ __device__ __forceinline__ void logits_unit(const PrefillParams& p, const TcCta&
 }
 
 // WG2's loop: the K tiles of units 0 and 1, then per unit v the logits of v (as soon as
-// QK(v) completes) followed by the K tile of v + 2 (whose slot QK(v) has just freed).
+// QK(v) completes) followed by the K tile of v + 2 (whose slot QK(v) has just freed),
+// that tile's loads issued before the logits.
 template <int KB, int VB>
 __device__ __forceinline__ void k_role(const PrefillParams& p, const TcCta& c, uint8_t* smem, uint64_t* bars,
                                        uint32_t tmem, int32_t* err, int et, uint32_t lane_off) {
-    for (int u = 0; u < 2 && u < c.units; ++u) expand_k_unit<KB, VB>(p, c, smem, bars, err, et, u);
+    for (int u = 0; u < 2 && u < c.units; ++u) {
+        RecRow<KB> L;
+        load_k<KB>(p, c, u, et, L);
+        expand_k_unit<KB, VB>(p, c, smem, bars, err, et, u, L);
+    }
     for (int v = 0; v < c.units; ++v) {
+        RecRow<KB> L;
+        load_k<KB>(p, c, v + 2, et, L);
         logits_unit(p, c, smem, bars, tmem, err, et, lane_off, v);
-        if (v + 2 < c.units) expand_k_unit<KB, VB>(p, c, smem, bars, err, et, v + 2);
+        if (v + 2 < c.units) expand_k_unit<KB, VB>(p, c, smem, bars, err, et, v + 2, L);
     }
 }
 
