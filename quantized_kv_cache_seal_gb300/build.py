@@ -19,7 +19,7 @@ CSRC = os.path.join(HERE, "csrc")
 BUILD = os.path.join(HERE, "_build")
 LIB = os.path.join(BUILD, "libkvarn.so")
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
-SOURCES = ["kvarn_host.cpp", "kvarn_seal.cu", "kvarn_decode.cu", "kvarn_prefill.cu", "kvarn_prefill_tc.cu"]
+SOURCES = ["kvarn_host.cpp", "kvarn_seal.cu", "kvarn_decode.cu", "kvarn_prefill.cu"]
 HEADERS = ["kvarn_internal.h", "kvarn_dev.cuh"]
 
 

@@ -443,7 +443,7 @@ kvarn_status check_prefill(const kvarn_cache* c, int32_t layer, int32_t n_seqs, 
     }
     if (rows > 0 && (!q || !out)) return KVARN_EINVAL;
     if (rows * c->cfg.num_q_heads >= (1ll << 31) || ctas >= (1ll << 31)) return KVARN_ECAPACITY;
-    if (!c->host_only && prefill_tc_smem_bytes() > c->max_smem) return KVARN_ECAPACITY;
+    if (!c->host_only && prefill_smem_bytes() > c->max_smem) return KVARN_ECAPACITY;
     return KVARN_OK;
 }
 
@@ -490,13 +490,10 @@ kvarn_status run_prefill(kvarn_cache* c, int32_t layer, int32_t n_seqs, const in
     }
     if (ctas == 0) return KVARN_OK;
     p.grid = (int32_t)ctas;
-    int stages = 8;
-    while (stages > 1 && prefill_smem_bytes(cfg.k_bits, cfg.v_bits, stages) > c->max_smem) --stages;
-    p.stages = stages;
     if (c->host_only) return KVARN_OK;
     kvarn_status st = ensure_init(c, stream);
     if (st) return st;
-    const int rc = launch_prefill_tc(p, stream);
+    const int rc = launch_prefill(p, stream);
     if (rc) { set_cuda_error(rc, "prefill launch"); return KVARN_ECUDA; }
     return KVARN_OK;
 }

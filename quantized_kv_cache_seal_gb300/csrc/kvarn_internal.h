@@ -24,7 +24,6 @@ constexpr int kPartialFloats = 528;  // [0] epoch bits, [4..8) m, [8..12) l, [12
 constexpr int kDecodeThreads = 512;  // 3 compute warpgroups + 1 copy-issuing warpgroup
 constexpr int kExactRows = 16;       // tokens of an exact (sink or tail) sub-group of the decode stream
 constexpr int kSealThreads = 256;
-constexpr int kPrefillThreads = 256;  // 8 warps, one 16-row MMA tile each
 constexpr int kPrefillRows = 128;     // query rows (token, head) of a prefill CTA
 
 // device error word bits
@@ -106,8 +105,7 @@ struct PrefillParams {
     uint16_t* out;
     int32_t n_seqs, hq, hkv, r, k_bits, v_bits, layer, num_layers, max_groups;
     int32_t rec_k, rec_v, slot_bytes, tail_cap;
-    int32_t stages;     // record ring stages
-    int32_t grid;
+    int32_t grid;       // CTAs: one per (sequence, KV head, query tile)
     float scale_log2;
     PrefillSeq seqs[kMaxBatch];
 };
@@ -155,10 +153,8 @@ struct AppendParams {
 
 // Launchers (defined in the .cu files). Return 0 on success, else a cudaError_t value.
 int launch_decode(const DecodeParams& p, int smem_bytes, void* stream);
-int launch_prefill(const PrefillParams& p, int smem_bytes, void* stream);
-int prefill_smem_bytes(int k_bits, int v_bits, int stages);
-int launch_prefill_tc(const PrefillParams& p, void* stream);  // tcgen05 kernel (kvarn_prefill_tc.cu)
-int prefill_tc_smem_bytes();
+int launch_prefill(const PrefillParams& p, void* stream);
+int prefill_smem_bytes();
 int launch_seal_jobs(const SealParams& p, void* stream);
 int launch_append(const AppendParams& p, void* stream);
 int launch_seal_groups(const void* x, int n, int bits, int which, int iters, void* records, float* scales,

@@ -1,33 +1,51 @@
-// KVarN prefill (many-query) attention for sm_103a.
+// KVarN prefill (many-query) attention for sm_103a on the 5th-generation tensor cores.
 //
 // Method (anbeeld.com "KVarN KV Cache: Implementation and Benchmarks", sections 1 and
-// 2.1): the cache is read the way the decode path reads it. The sink and the exact tail
-// are fp16 and meet the unrotated query; every sealed group is read from its record with
-// the query rotated by the record's Hadamard matrix, the sealed part of the output is
-// summed in the rotated frame and rotated back once per output row. Each query token of
-// a prompt chunk attends causally (keys at positions up to its own) to the cache as it
-// stands after the chunk's append, so tokens of the chunk that already sit in a sealed
-// group are read sealed.
+// 2.1): the cache is read the way the decode path reads it. Every sealed group is read
+// from its record with the query rotated by the record's Hadamard matrix and the sealed
+// part of the output is summed in the rotated frame; the sink and the exact tail are
+// fp16 and meet the unrotated query, after the output has been rotated back (the scaled
+// Sylvester matrix is its own inverse). Each query token of a prompt chunk attends
+// causally (keys at positions up to its own) to the cache as it stands after the
+// chunk's append.
 //
-// Work split. One CTA of 8 warps per (sequence, KV head, tile of 128 / r query tokens):
-// its 128 query rows are (token, query head) pairs, token-major, and warp w owns rows
-// 16 w .. 16 w + 15, the M side of mma.sync m16n8k16 (f16 in, f32 accumulate). Each key
-// block is staged once in shared memory and read by all 8 warps:
-//   * exact blocks of 64 fp16 tokens (the sink, then the tail), loaded cooperatively;
-//   * sealed group pairs, copied with cp.async.bulk into a ring of stages and expanded
-//     by all threads into f16 operand tiles: code c becomes the subnormal half c 2^-24
-//     (exact), the K tile token-major and the V tile channel-major, as in the records.
-// For a group with codes q, token scales a, channel scales c and grid (m, delta), the
-// score of row i and token t is
-//   scale * qm_i * a_t * (delta * sum_j (v_ij c_j) q_tj + m * sum_j v_ij c_j),
-// v_i = q'_i / qm_i the rotated query scaled to |v| <= 1; v c enters as an f16 high
-// part and an f16 low part (two MMAs into one accumulator), which keeps the logits at
-// about fp32 accuracy. The rotated output of row i gains
-//   c_j * (delta_V * sum_t w_it qV_tj + m_V * sum_t w_it),  w_it = p_it aV_t,
-// with w scaled by a power of two rho into [0, 2) and rounded to f16. The row sums come
-// from the same MMAs with an all-ones operand. The accumulator is unrotated over the
-// exact blocks, rotated once into the record frame, summed over the groups and rotated
-// back at the end (the scaled Sylvester matrix is its own inverse).
+// One CTA per (sequence, KV head, tile of 128 / r query tokens): 128 query rows
+// (token, head), token-major, M = 128 of tcgen05.mma kind::f16 (f16 operands, f32
+// accumulators in tensor memory). The CTA walks its units: the visible sealed groups
+// in order, then the exact blocks (the sink, then the tail, 128 tokens each). For a
+// group with codes q, token scales a, channel scales c and grid (m, delta):
+//   QK  S_it = sum_j A_ij q_tj, A = v c_K as f16 high and low parts (two passes), v the
+//       rotated query of row i over max|v|; the logit is
+//       scale * qm_i * aK_t * (deltaK * S_it + mK * sum_j v_ij c_j).
+//   PV  O_ij += sum_t W_it B_jt, W = p 2^e, B = 2^-e c_j aV_t (deltaV q_tj + mV) (the
+//       dequantised value in the rotated frame; e = 0 unless it would reach 2^15): O
+//       accumulates across groups in place. W and B are fp32 values carried as an f16
+//       high part plus the f16 rounding of the residual; three passes (W high x B high,
+//       W high x B low, W low x B high) keep the products to about 22 bits.
+// Exact blocks: S = q . k on the raw fp16 query; W = p (high and low parts) against the
+// fp16 values (transposed), two passes.
+//
+// Warp roles (640 threads, 5 warpgroups; warp w reaches tensor-memory lanes
+// 32 (w % 4) .. 32 (w % 4) + 31, so thread 32 (w % 4) + lane of a warpgroup owns query
+// row 32 (w % 4) + lane):
+//   WG0  softmax: one thread per row; loads S in 32-column chunks (a pass for the
+//        maximum, a pass for the weights), keeps the running maximum (raised only when
+//        it grows by more than 8 in log2 units, with O and l rescaled then), writes W
+//        (high and low f16 parts) over S, and at the end normalises O and writes the
+//        output.
+//   WG1  query operand: rotates and scales its row once, then per group writes A (high
+//        and low parts) into tensor memory and the row sum sum_j v_ij c_j into shared
+//        memory; before the exact blocks it writes the raw query and rotates O back.
+//   WG2  K expansion: the K codes of each group as f16 integers (or the exact K rows) in
+//        a canonical K-major tile (no swizzle) and the group's token scales.
+//   WG3  V expansion: the dequantised V values of each group as high and low parts (or
+//        the exact V rows, transposed) in a canonical K-major tile.
+//   WG4  warp 16 owns tensor memory and one of its threads issues every MMA, QK or PV,
+//        whichever is ready first.
+// Tensor memory (512 columns): A [0, 128), S0 [128, 256), S1 [256, 384), O [384, 512).
+// QK of unit u + 1 runs while the softmax of unit u does; the K tiles, V tiles and S are
+// double-buffered and released separately (a K tile when its QK completes, a V tile when
+// its PV does). Every wait is bounded (2 s) and sets the error word when it gives up.
 #include <cuda_fp16.h>
 #include <cuda_runtime.h>
 
@@ -37,428 +55,870 @@ namespace kvarn {
 
 namespace {
 
-constexpr int kPfWarps = kPrefillThreads / 32;
-constexpr int kPfRows = 16 * kPfWarps;  // query rows of a CTA
-static_assert(kPfRows == kPrefillRows, "one 16-row MMA tile per warp");
-constexpr int kPitch = 272;             // bytes per shared row of 128 halves (ldmatrix without bank conflicts)
-constexpr int kTileBytes = 128 * kPitch;
-constexpr int kExactBlock = 64;         // tokens of an exact block
-constexpr int kQfragBytes = kPfWarps * 8 * 32 * 16;  // one query operand table (high or low parts)
-constexpr uint32_t kOnes = 0x3c003c00u;  // half2(1, 1)
-#define kNegInfP (-__int_as_float(0x7f800000))
+constexpr int kTcThreads = 640;      // five warpgroups
+constexpr int kRows = kPrefillRows;  // 128 query rows per CTA
+// registers a thread: 96 at launch (65536 / 640 rounded down to a multiple of 8), then
+// re-split per warpgroup (per scheduler: one warp of each warpgroup)
+constexpr int kRegsLaunch = 96, kRegsSoftmax = 112, kRegsQuery = 176, kRegsExpandK = 96, kRegsExpandV = 72,
+              kRegsIssue = 24;
+static_assert(kRegsSoftmax + kRegsQuery + kRegsExpandK + kRegsExpandV + kRegsIssue <= 5 * kRegsLaunch,
+              "register split exceeds what a sub-partition holds at launch");
+static_assert(kRegsLaunch * kTcThreads <= 65536, "launch registers");
 
-// Shared memory (bytes):
-//   [0, 2 T)            sealed phase: K operand tile, V operand tile (T = kTileBytes)
-//                       exact phase: K rows [0, 64 pitch), V rows after them; the staged
-//                       fp16 queries (128 rows) in [T, 2 T)
-//   [2 T, 2 T + 2 Q)    query operand tables, high then low parts (Q = kQfragBytes)
-//   ring                stages x (K record + V record), 16-byte aligned
-//   bars, positions, query maxima
-constexpr int kOffTiles = 0;
-constexpr int kOffQraw = kTileBytes;
-constexpr int kOffQhi = 2 * kTileBytes;
-constexpr int kOffQlo = kOffQhi + kQfragBytes;
-constexpr int kOffRing = kOffQlo + kQfragBytes;
-static_assert(kOffRing % 128 == 0, "ring alignment");
-static_assert(2 * kExactBlock * kPitch <= kTileBytes, "exact blocks fit below the staged queries");
+// tensor memory columns
+constexpr uint32_t kColA = 0, kColS = 128, kColO = 384;
 
-__device__ __forceinline__ void mma_f16(float (&d)[4], uint32_t a0, uint32_t a1, uint32_t a2, uint32_t a3,
-                                        uint32_t b0, uint32_t b1) {
+// shared memory: two operand sets (K tile, V tile, the V expansion's token factors),
+// the K-side tables of the last four units, then the small tables
+constexpr int kKTile = 128 * 128 * 2;           // N = 128 tokens, K = 128 channels
+constexpr int kVTile = 128 * 256 * 2;           // N = 128 channels, K = 128 tokens (high parts), 128 (low)
+constexpr int kOffK = 0, kOffV = kKTile;
+constexpr int kOffAlpha = kOffV + kVTile, kOffBeta = kOffAlpha + 512;  // deltaV aV_t, mV aV_t
+constexpr int kSetBytes = kOffBeta + 512;
+constexpr int kOffKtab = 2 * kSetBytes;         // [4][aK float[128], deltaK, mK, e, pad]
+constexpr int kKtabBytes = 512 + 16;
+constexpr int kOffRs = kOffKtab + 4 * kKtabBytes;  // float[4][128] row sums, ring by unit
+constexpr int kOffRed = kOffRs + 4 * 128 * 4;   // float[2][2][8] expansion reductions (K, V warpgroups)
+constexpr int kOffCq = kOffRed + 128;           // float[2][128] channel scales of the next query operand
+constexpr int kOffMx = kOffCq + 1024;           // float[4][128] row maxima of the logits, ring by unit
+constexpr int kOffPos = kOffMx + 2048;          // int[128] row positions
+constexpr int kOffQm = kOffPos + 512;           // float[128] row maxima of the rotated query
+constexpr int kOffVst = kOffQm + 512;           // uint32[32][128] the V expansion's code words (word k of thread t at k 128 + t)
+constexpr int kOffBars = kOffVst + 32 * 128 * 4;
+// barriers: k_full[4], k_empty[2], v_full[2], v_empty[2], a_full[4], a_empty, s_full[2],
+// p_full[2], o_done[2], drain, m_full[4]
+constexpr int kNumBars = 26;
+constexpr int kOffTmem = kOffBars + 8 * kNumBars;
+constexpr int kSmemTc = kOffTmem + 16;
+static_assert(kSmemTc <= 227 * 1024, "shared memory of one CTA");
+static_assert(kSetBytes % 128 == 0 && kOffV % 128 == 0 && kOffKtab % 16 == 0 && kKtabBytes % 16 == 0,
+              "operand tiles stay 128-byte aligned");
+
+__device__ __forceinline__ void tc_fence_before() { asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory"); }
+__device__ __forceinline__ void tc_fence_after() { asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory"); }
+__device__ __forceinline__ void fence_proxy_async_smem() { asm volatile("fence.proxy.async.shared::cta;" ::: "memory"); }
+
+// Canonical K-major operand without swizzle: 8-row x 16-byte core matrices, the two of
+// a 16-element k-step 128 bytes apart (leading offset), 8-row groups 256 bytes apart
+// (stride offset); a k-step of a tile of R rows spans R / 8 * 256 bytes.
+__device__ __forceinline__ uint64_t smem_desc(uint32_t addr) {
+    return (uint64_t)((addr >> 4) & 0x3FFFu) | ((uint64_t)(128 >> 4) << 16) | ((uint64_t)(256 >> 4) << 32) |
+           ((uint64_t)1 << 46);
+}
+// byte offset of element (row, k) in such a tile of 128 rows
+__device__ __forceinline__ int tile_off(int row, int k) {
+    return (((k >> 4) * 16 + (row >> 3)) * 2 + ((k >> 3) & 1)) * 128 + (row & 7) * 16 + (k & 7) * 2;
+}
+// kind::f16 instruction descriptor: f32 accumulator, f16 A and B, both K-major, M = 128, N = 128
+constexpr uint32_t kIdesc = (1u << 4) | ((128u >> 3) << 17) | ((128u >> 4) << 24);
+
+// A from tensor memory
+__device__ __forceinline__ void mma_ts(uint32_t d, uint32_t a, uint64_t b, uint32_t acc) {
     asm volatile(
-        "mma.sync.aligned.m16n8k16.row.col.f32.f16.f16.f32 {%0,%1,%2,%3}, {%4,%5,%6,%7}, {%8,%9}, "
-        "{%0,%1,%2,%3};\n"
-        : "+f"(d[0]), "+f"(d[1]), "+f"(d[2]), "+f"(d[3])
-        : "r"(a0), "r"(a1), "r"(a2), "r"(a3), "r"(b0), "r"(b1));
+        "{\n .reg .pred p;\n setp.ne.b32 p, %4, 0;\n"
+        " tcgen05.mma.cta_group::1.kind::f16 [%0], [%1], %2, %3, p;\n}\n" ::"r"(d),
+        "r"(a), "l"(b), "r"(kIdesc), "r"(acc)
+        : "memory");
+}
+// arrive on bar once every MMA issued so far by this thread has completed
+__device__ __forceinline__ void mma_commit(uint64_t* bar) {
+    asm volatile("tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(smem_addr(bar))
+                 : "memory");
 }
 
-// ldmatrix of four 8 x 8 b16 matrices; lanes 8 i .. 8 i + 7 give the row addresses of matrix i.
-__device__ __forceinline__ void ldsm4(uint32_t addr, uint32_t (&r)[4]) {
-    asm volatile("ldmatrix.sync.aligned.m8n8.x4.shared.b16 {%0,%1,%2,%3}, [%4];"
-                 : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3])
-                 : "r"(addr));
+// 32 consecutive columns of the warp's 32 lanes: thread lane gets lane's row
+__device__ __forceinline__ void tm_ld32(uint32_t taddr, uint32_t (&r)[32]) {
+    asm volatile(
+        "tcgen05.ld.sync.aligned.32x32b.x32.b32 {%0,%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15,"
+        "%16,%17,%18,%19,%20,%21,%22,%23,%24,%25,%26,%27,%28,%29,%30,%31}, [%32];"
+        : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]), "=r"(r[7]),
+          "=r"(r[8]), "=r"(r[9]), "=r"(r[10]), "=r"(r[11]), "=r"(r[12]), "=r"(r[13]), "=r"(r[14]), "=r"(r[15]),
+          "=r"(r[16]), "=r"(r[17]), "=r"(r[18]), "=r"(r[19]), "=r"(r[20]), "=r"(r[21]), "=r"(r[22]), "=r"(r[23]),
+          "=r"(r[24]), "=r"(r[25]), "=r"(r[26]), "=r"(r[27]), "=r"(r[28]), "=r"(r[29]), "=r"(r[30]), "=r"(r[31])
+        : "r"(taddr));
 }
-__device__ __forceinline__ void ldsm4t(uint32_t addr, uint32_t (&r)[4]) {
-    asm volatile("ldmatrix.sync.aligned.m8n8.x4.trans.shared.b16 {%0,%1,%2,%3}, [%4];"
-                 : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3])
-                 : "r"(addr));
+__device__ __forceinline__ void tm_wait_ld() { asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory"); }
+__device__ __forceinline__ void tm_st8(uint32_t taddr, const uint32_t (&r)[8]) {
+    asm volatile("tcgen05.st.sync.aligned.32x32b.x8.b32 [%0], {%1,%2,%3,%4,%5,%6,%7,%8};" ::"r"(taddr), "r"(r[0]),
+                 "r"(r[1]), "r"(r[2]), "r"(r[3]), "r"(r[4]), "r"(r[5]), "r"(r[6]), "r"(r[7])
+                 : "memory");
 }
+__device__ __forceinline__ void tm_st32(uint32_t taddr, const uint32_t (&r)[32]) {
+    asm volatile(
+        "tcgen05.st.sync.aligned.32x32b.x32.b32 [%0], {%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15,%16,"
+        "%17,%18,%19,%20,%21,%22,%23,%24,%25,%26,%27,%28,%29,%30,%31,%32};" ::"r"(taddr),
+        "r"(r[0]), "r"(r[1]), "r"(r[2]), "r"(r[3]), "r"(r[4]), "r"(r[5]), "r"(r[6]), "r"(r[7]), "r"(r[8]), "r"(r[9]),
+        "r"(r[10]), "r"(r[11]), "r"(r[12]), "r"(r[13]), "r"(r[14]), "r"(r[15]), "r"(r[16]), "r"(r[17]), "r"(r[18]),
+        "r"(r[19]), "r"(r[20]), "r"(r[21]), "r"(r[22]), "r"(r[23]), "r"(r[24]), "r"(r[25]), "r"(r[26]), "r"(r[27]),
+        "r"(r[28]), "r"(r[29]), "r"(r[30]), "r"(r[31])
+        : "memory");
+}
+__device__ __forceinline__ void tm_wait_st() { asm volatile("tcgen05.wait::st.sync.aligned;" ::: "memory"); }
 
-__device__ __forceinline__ float ex2(float x) {
+__device__ __forceinline__ float ex2f(float x) {
     float y;
     asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
     return y;
 }
-
-__device__ __forceinline__ uint32_t u32_of(__half2 h) { return *reinterpret_cast<uint32_t*>(&h); }
-__device__ __forceinline__ __half2 h2_of(uint32_t u) { return *reinterpret_cast<__half2*>(&u); }
-__device__ __forceinline__ float2 f2_of(uint32_t u) { return __half22float2(h2_of(u)); }
+__device__ __forceinline__ uint32_t h2u(__half2 h) { return *reinterpret_cast<uint32_t*>(&h); }
+__device__ __forceinline__ __half2 u2h(uint32_t u) { return *reinterpret_cast<__half2*>(&u); }
+#define kNegInfT (-__int_as_float(0x7f800000))
 
 // Bits pos .. pos + width - 1 (width <= 16) of a little-endian stream of N words.
 template <int N>
-__device__ __forceinline__ uint32_t bits_at(const uint32_t (&s)[N], int pos, int width) {
+__device__ __forceinline__ uint32_t bits_of(const uint32_t (&s)[N], int pos, int width) {
     const int lo = pos / 32, sh = pos % 32;
     uint32_t v = s[lo] >> sh;
-    if (sh + width > 32) v |= s[lo + 1] << (32 - sh);
+    if (sh + width > 32 && lo + 1 < N) v |= s[lo + 1] << (32 - sh);
     return v & ((1u << width) - 1u);
 }
 
-// 32 codes of width B (LSB-first from src, 4-byte aligned) -> 16 words of two f16
-// operands each: word k holds codes 2 k and 2 k + 1 as the subnormals code * 2^-24.
+// Codes 8 m .. 8 m + 7 of a row of 128 B-bit codes held in s (4 B words) as four words
+// of two f16 integers each (exact).
 template <int B>
-__device__ __forceinline__ void expand_chunk(const uint8_t* src, uint8_t* dst) {
-    uint32_t s[B];
-    if constexpr (B == 2) {
-        const uint2 v = *reinterpret_cast<const uint2*>(src);
-        s[0] = v.x; s[1] = v.y;
-    } else if constexpr (B == 4) {
-        const uint4 v = *reinterpret_cast<const uint4*>(src);
-        s[0] = v.x; s[1] = v.y; s[2] = v.z; s[3] = v.w;
-    } else if constexpr (B == 8) {
-        const uint4 v0 = reinterpret_cast<const uint4*>(src)[0], v1 = reinterpret_cast<const uint4*>(src)[1];
-        s[0] = v0.x; s[1] = v0.y; s[2] = v0.z; s[3] = v0.w;
-        s[4] = v1.x; s[5] = v1.y; s[6] = v1.z; s[7] = v1.w;
-    } else {
+__device__ __forceinline__ uint4 codes8(const uint32_t (&s)[4 * B], int m) {
+    constexpr uint32_t mask = (1u << B) - 1u;
+    uint32_t o[4];
 #pragma unroll
-        for (int k = 0; k < B; ++k) s[k] = reinterpret_cast<const uint32_t*>(src)[k];
+    for (int k = 0; k < 4; ++k) {
+        const uint32_t f = bits_of(s, (8 * m + 2 * k) * B, 2 * B);
+        // 0x6400 | c is the half 1024 + c; subtracting 1024 leaves c exactly
+        const uint32_t w = ((f & mask) | ((f >> B) << 16)) | 0x64006400u;
+        o[k] = h2u(__hsub2(u2h(w), __halves2half2(__ushort_as_half(0x6400), __ushort_as_half(0x6400))));
     }
-    constexpr uint32_t m = (1u << B) - 1u;
-    uint32_t o[16];
-#pragma unroll
-    for (int k = 0; k < 16; ++k) {
-        const uint32_t f = bits_at(s, 2 * k * B, 2 * B);
-        o[k] = (f & m) | ((f >> B) << 16);
-    }
-    uint4* d = reinterpret_cast<uint4*>(dst);
-#pragma unroll
-    for (int k = 0; k < 4; ++k) d[k] = make_uint4(o[4 * k], o[4 * k + 1], o[4 * k + 2], o[4 * k + 3]);
+    return make_uint4(o[0], o[1], o[2], o[3]);
 }
 
-// 128-point Hadamard transform, scaled by 1/sqrt(128), of every row of a warp's 16 x 128
-// accumulator in the m16n8 C layout: lane (g, tq) holds in x[nt][e] row g (e < 2) or
-// g + 8 (e >= 2), column 8 nt + 2 tq + (e & 1). Column bit 0 is e & 1, bits 1-2 are
-// lane bits 0-1, bits 3-6 the tile index. The lower column of a pair takes a + b.
-__device__ __forceinline__ void rows_fwht128(float (&x)[16][4], int lane) {
+// Codes 8 m .. 8 m + 7 of a row of 128 B-bit codes staged as words k at col[128 k], as
+// four words of two f16 integers each (exact); m may vary at run time.
+template <int B>
+__device__ __forceinline__ uint4 codes8_staged(const uint32_t* col, int m) {
+    constexpr uint32_t mask = (1u << B) - 1u;
+    const int pos = 8 * B * m, lo = pos >> 5, sh = pos & 31;
+    uint64_t bits = col[128 * lo];
+    if (sh + 8 * B > 32) bits |= (uint64_t)col[128 * (lo + 1)] << 32;
+    bits >>= sh;
+    uint32_t o[4];
 #pragma unroll
-    for (int nt = 0; nt < 16; ++nt) {
-#pragma unroll
-        for (int rb = 0; rb < 4; rb += 2) {
-            const float a = x[nt][rb], b = x[nt][rb + 1];
-            x[nt][rb] = a + b;
-            x[nt][rb + 1] = a - b;
-        }
+    for (int k = 0; k < 4; ++k) {
+        const uint32_t f = (uint32_t)(bits >> (2 * B * k)) & ((1u << (2 * B)) - 1u);
+        const uint32_t w = ((f & mask) | ((f >> B) << 16)) | 0x64006400u;
+        o[k] = h2u(__hsub2(u2h(w), __halves2half2(__ushort_as_half(0x6400), __ushort_as_half(0x6400))));
     }
-#pragma unroll
-    for (int bt = 1; bt < 4; bt <<= 1) {
-        const bool upper = (lane & bt) != 0;
-#pragma unroll
-        for (int nt = 0; nt < 16; ++nt) {
-#pragma unroll
-            for (int e = 0; e < 4; ++e) {
-                const float o = __shfl_xor_sync(0xffffffffu, x[nt][e], bt);
-                x[nt][e] = upper ? o - x[nt][e] : x[nt][e] + o;
-            }
-        }
-    }
-#pragma unroll
-    for (int len = 1; len < 16; len <<= 1) {
-#pragma unroll
-        for (int nt = 0; nt < 16; ++nt) {
-            if (nt & len) continue;
-#pragma unroll
-            for (int e = 0; e < 4; ++e) {
-                const float a = x[nt][e], b = x[nt + len][e];
-                x[nt][e] = a + b;
-                x[nt + len][e] = a - b;
-            }
-        }
-    }
-#pragma unroll
-    for (int nt = 0; nt < 16; ++nt)
-#pragma unroll
-        for (int e = 0; e < 4; ++e) x[nt][e] *= kInvSqrt128;
+    return make_uint4(o[0], o[1], o[2], o[3]);
 }
 
-// Same transform of one 128-vector held by a warp, channel 4 lane + e in v[e].
-__device__ __forceinline__ void vec_fwht128(float (&v)[4], int lane) {
-    float a0 = v[0] + v[1], a1 = v[0] - v[1], a2 = v[2] + v[3], a3 = v[2] - v[3];
-    v[0] = a0 + a2; v[2] = a0 - a2; v[1] = a1 + a3; v[3] = a1 - a3;
-#pragma unroll
-    for (int b = 1; b < 32; b <<= 1) {
-#pragma unroll
-        for (int e = 0; e < 4; ++e) {
-            const float o = __shfl_xor_sync(0xffffffffu, v[e], b);
-            v[e] = (lane & b) ? (o - v[e]) : (v[e] + o);
-        }
-    }
-#pragma unroll
-    for (int e = 0; e < 4; ++e) v[e] *= kInvSqrt128;
-}
-
-// Online-softmax state of the two rows a thread holds (g and g + 8 of its warp's tile).
-struct RowState {
-    float m[2], l[2];  // running maximum (log2 domain) and this thread's partial sum
-    float acc[16][4];
-};
-
-// Row maxima of a score tile S (nt tiles) over the 4 lanes of a row, the new running
-// maxima, the correction factors; p = 2^(S - m) in place; partial sums and accumulator
-// rescaled.
-template <int NT>
-__device__ __forceinline__ void softmax_update(float (&S)[NT][4], RowState& st) {
-    float mx0 = kNegInfP, mx1 = kNegInfP;
-#pragma unroll
-    for (int nt = 0; nt < NT; ++nt) {
-        mx0 = fmaxf(mx0, fmaxf(S[nt][0], S[nt][1]));
-        mx1 = fmaxf(mx1, fmaxf(S[nt][2], S[nt][3]));
-    }
-#pragma unroll
-    for (int o = 1; o < 4; o <<= 1) {
-        mx0 = fmaxf(mx0, __shfl_xor_sync(0xffffffffu, mx0, o));
-        mx1 = fmaxf(mx1, __shfl_xor_sync(0xffffffffu, mx1, o));
-    }
-    // the first block is the sink's first, which every row sees: st.m is finite after it
-    const float n0 = fmaxf(st.m[0], mx0), n1 = fmaxf(st.m[1], mx1);
-    const float c0 = ex2(st.m[0] - n0), c1 = ex2(st.m[1] - n1);
-    st.m[0] = n0;
-    st.m[1] = n1;
-    float s0 = 0.f, s1 = 0.f;
-#pragma unroll
-    for (int nt = 0; nt < NT; ++nt) {
-        S[nt][0] = ex2(S[nt][0] - n0);
-        S[nt][1] = ex2(S[nt][1] - n0);
-        S[nt][2] = ex2(S[nt][2] - n1);
-        S[nt][3] = ex2(S[nt][3] - n1);
-        s0 += S[nt][0] + S[nt][1];
-        s1 += S[nt][2] + S[nt][3];
-    }
-    st.l[0] = fmaf(st.l[0], c0, s0);
-    st.l[1] = fmaf(st.l[1], c1, s1);
-#pragma unroll
-    for (int nt = 0; nt < 16; ++nt) {
-        st.acc[nt][0] *= c0;
-        st.acc[nt][1] *= c0;
-        st.acc[nt][2] *= c1;
-        st.acc[nt][3] *= c1;
-    }
-}
-
-struct Cta {
+struct TcCta {
     const PrefillSeq* e;
-    int kvh, r, t0;      // KV head, query heads per KV head, first query token of the tile
-    int first_pos;       // position of query token 0 of the sequence's chunk
-    int pmax;            // largest valid query position of the tile
-    int n_vis;           // sealed groups with a token at or before pmax
-    size_t blk;          // (sequence, layer, KV head) index of the exact regions
+    int kvh, t0;        // KV head, first query token of the tile
+    int pmin, pmax;     // smallest and largest position among the tile's valid rows
+    int n_sealed;       // sealed groups with a token at or before pmax
+    int nb_sink;        // 1 when the sink has a visible token
+    int sink_vis;       // visible sink tokens
+    int tail_start, tail_vis;
+    int units;          // n_sealed + exact blocks
+    size_t blk;         // (sequence, layer, KV head) index of the exact regions
 };
 
-// One exact block: keys at positions kp0 .. kp0 + cnt - 1 (rows >= cnt are zeros),
-// K rows at sK, V rows at sV (pitch kPitch), queries (unrotated fp16) at sQ.
-__device__ __forceinline__ void exact_block(uint32_t sK, uint32_t sV, uint32_t sQ, int kp0, int cnt, int p0, int p1,
-                                            float scale_log2, RowState& st, int lane) {
-    const int tq = lane & 3;
-    float S[8][4];
-#pragma unroll
-    for (int nt = 0; nt < 8; ++nt) S[nt][0] = S[nt][1] = S[nt][2] = S[nt][3] = 0.f;
-    const uint32_t qa = sQ + (lane & 15) * kPitch + 16 * (lane >> 4);
-    const uint32_t ka = sK + ((lane & 7) + 8 * (lane >> 4)) * kPitch + 16 * ((lane >> 3) & 1);
-#pragma unroll
-    for (int ks = 0; ks < 8; ++ks) {
-        uint32_t a[4];
-        ldsm4(qa + 32 * ks, a);
-#pragma unroll
-        for (int np = 0; np < 4; ++np) {
-            uint32_t b[4];
-            ldsm4(ka + 16 * np * kPitch + 32 * ks, b);
-            mma_f16(S[2 * np], a[0], a[1], a[2], a[3], b[0], b[1]);
-            mma_f16(S[2 * np + 1], a[0], a[1], a[2], a[3], b[2], b[3]);
+struct Unit {
+    bool sealed;
+    int g;              // sealed group
+    int kp0, cnt;       // exact block: first position, tokens
+    bool tail;
+};
+
+__device__ __forceinline__ Unit unit_of(const TcCta& c, int u) {
+    Unit x;
+    x.sealed = u < c.n_sealed;
+    x.g = u;
+    x.tail = false;
+    x.kp0 = 0;
+    x.cnt = 0;
+    if (!x.sealed) {
+        const int e = u - c.n_sealed;
+        if (e < c.nb_sink) {
+            x.cnt = c.sink_vis;
+        } else {
+            x.tail = true;
+            x.kp0 = c.tail_start + kGroup * (e - c.nb_sink);
+            x.cnt = min(kGroup, c.tail_start + c.tail_vis - x.kp0);
         }
     }
-#pragma unroll
-    for (int nt = 0; nt < 8; ++nt) {
-#pragma unroll
-        for (int e = 0; e < 4; ++e) {
-            const int j = 8 * nt + 2 * tq + (e & 1);
-            const int P = e < 2 ? p0 : p1;
-            S[nt][e] = (j < cnt && kp0 + j <= P) ? S[nt][e] * scale_log2 : kNegInfP;
-        }
-    }
-    softmax_update<8>(S, st);
-    // P V with the weights split into f16 high and low parts
-    uint32_t ph[4][4], pl[4][4];
-#pragma unroll
-    for (int kk = 0; kk < 4; ++kk) {
-#pragma unroll
-        for (int h = 0; h < 2; ++h) {
-            const float* s = S[2 * kk + h];
-            const __half2 h01 = __floats2half2_rn(s[0], s[1]), h23 = __floats2half2_rn(s[2], s[3]);
-            const float2 f01 = __half22float2(h01), f23 = __half22float2(h23);
-            ph[kk][2 * h] = u32_of(h01);
-            ph[kk][2 * h + 1] = u32_of(h23);
-            pl[kk][2 * h] = u32_of(__floats2half2_rn(s[0] - f01.x, s[1] - f01.y));
-            pl[kk][2 * h + 1] = u32_of(__floats2half2_rn(s[2] - f23.x, s[3] - f23.y));
-        }
-    }
-    // matrix i of an ldmatrix: keys 16 kk + 8 (i & 1), channels 8 nt + 8 (i >> 1), transposed
-    const uint32_t va = sV + ((lane & 7) + 8 * ((lane >> 3) & 1)) * kPitch + 16 * (lane >> 4);
-#pragma unroll
-    for (int np = 0; np < 8; ++np) {
-#pragma unroll
-        for (int kk = 0; kk < 4; ++kk) {
-            uint32_t b[4];
-            ldsm4t(va + 16 * kk * kPitch + 32 * np, b);
-            // A fragment order: (row g, k lo), (row g + 8, k lo), (row g, k hi), (row g + 8, k hi)
-            mma_f16(st.acc[2 * np], ph[kk][0], ph[kk][1], ph[kk][2], ph[kk][3], b[0], b[1]);
-            mma_f16(st.acc[2 * np], pl[kk][0], pl[kk][1], pl[kk][2], pl[kk][3], b[0], b[1]);
-            mma_f16(st.acc[2 * np + 1], ph[kk][0], ph[kk][1], ph[kk][2], ph[kk][3], b[2], b[3]);
-            mma_f16(st.acc[2 * np + 1], pl[kk][0], pl[kk][1], pl[kk][2], pl[kk][3], b[2], b[3]);
-        }
-    }
+    return x;
 }
 
-// One sealed group pair: operand tiles at sK (token-major) and sV (channel-major), the
-// records' headers at krec / vrec, the warp's query tables at qhi / qlo.
-__device__ __forceinline__ void sealed_group(uint32_t sK, uint32_t sV, const uint8_t* krec, const uint8_t* vrec,
-                                             const uint4* qhi, const uint4* qlo, float qm0, float qm1, int gp0,
-                                             bool masked, int p0, int p1, float scale_log2, RowState& st, int lane) {
-    const int tq = lane & 3;
-    const uint32_t* cK = reinterpret_cast<const uint32_t*>(krec + 272);
-    float S[16][4];
-#pragma unroll
-    for (int nt = 0; nt < 16; ++nt) S[nt][0] = S[nt][1] = S[nt][2] = S[nt][3] = 0.f;
-    float rs[4] = {0.f, 0.f, 0.f, 0.f};
-    const uint32_t ka = sK + ((lane & 7) + 8 * (lane >> 4)) * kPitch + 16 * ((lane >> 3) & 1);
-#pragma unroll 2
-    for (int ks = 0; ks < 8; ++ks) {
-        const uint4 vh = qhi[ks * 32 + lane], vl = qlo[ks * 32 + lane];
-        const __half2 c01 = h2_of(cK[8 * ks + tq]), c89 = h2_of(cK[8 * ks + 4 + tq]);
-        const uint32_t vhs[4] = {vh.x, vh.y, vh.z, vh.w}, vls[4] = {vl.x, vl.y, vl.z, vl.w};
-        uint32_t ah[4], al[4];
-#pragma unroll
-        for (int i = 0; i < 4; ++i) {
-            const __half2 c = i < 2 ? c01 : c89;
-            const __half2 hi = __hmul2(h2_of(vhs[i]), c);
-            const __half2 res = __hfma2(h2_of(vhs[i]), c, __hneg2(hi));  // exact residual of the product
-            ah[i] = u32_of(hi);
-            al[i] = u32_of(__hfma2(h2_of(vls[i]), c, res));
-        }
-        mma_f16(rs, ah[0], ah[1], ah[2], ah[3], kOnes, kOnes);
-        mma_f16(rs, al[0], al[1], al[2], al[3], kOnes, kOnes);
-#pragma unroll
-        for (int np = 0; np < 8; ++np) {
-            uint32_t b[4];
-            ldsm4(ka + 16 * np * kPitch + 32 * ks, b);
-            mma_f16(S[2 * np], ah[0], ah[1], ah[2], ah[3], b[0], b[1]);
-            mma_f16(S[2 * np], al[0], al[1], al[2], al[3], b[0], b[1]);
-            mma_f16(S[2 * np + 1], ah[0], ah[1], ah[2], ah[3], b[2], b[3]);
-            mma_f16(S[2 * np + 1], al[0], al[1], al[2], al[3], b[2], b[3]);
-        }
-    }
-    {
-        const float dK = *reinterpret_cast<const float*>(krec);
-        const float mK = *reinterpret_cast<const float*>(krec + 4);
-        const uint32_t* aK = reinterpret_cast<const uint32_t*>(krec + 16);
-        // codes entered as code * 2^-24
-        const float al0 = scale_log2 * qm0 * dK * 16777216.0f, al1 = scale_log2 * qm1 * dK * 16777216.0f;
-        const float be0 = scale_log2 * qm0 * mK * rs[0], be1 = scale_log2 * qm1 * mK * rs[2];
-#pragma unroll
-        for (int nt = 0; nt < 16; ++nt) {
-            const float2 a = f2_of(aK[4 * nt + tq]);
-            S[nt][0] = a.x * fmaf(al0, S[nt][0], be0);
-            S[nt][1] = a.y * fmaf(al0, S[nt][1], be0);
-            S[nt][2] = a.x * fmaf(al1, S[nt][2], be1);
-            S[nt][3] = a.y * fmaf(al1, S[nt][3], be1);
-        }
-        if (masked) {
-#pragma unroll
-            for (int nt = 0; nt < 16; ++nt) {
-                const int pos = gp0 + 8 * nt + 2 * tq;
-                if (pos > p0) S[nt][0] = kNegInfP;
-                if (pos + 1 > p0) S[nt][1] = kNegInfP;
-                if (pos > p1) S[nt][2] = kNegInfP;
-                if (pos + 1 > p1) S[nt][3] = kNegInfP;
-            }
-        }
-    }
-    softmax_update<16>(S, st);
-    // weights w = p aV rho in f16; rho = 2^(15 - e) with e the biased exponent of the
-    // group's largest aV, so that every aV rho lies in [0, 2)
-    const uint32_t* aV = reinterpret_cast<const uint32_t*>(vrec + 16);
-    float rho;
-    {
-        const uint2 ab = reinterpret_cast<const uint2*>(vrec + 16)[lane];
-        uint32_t amaxb = __vmaxu2(ab.x, ab.y);
-        amaxb = max(amaxb & 0xffffu, amaxb >> 16);
-#pragma unroll
-        for (int o = 1; o < 32; o <<= 1) amaxb = max(amaxb, __shfl_xor_sync(0xffffffffu, amaxb, o));
-        const int ebits = max((int)(amaxb >> 10) & 31, 1);
-        rho = __int_as_float((127 + 15 - ebits) << 23);
-    }
-    uint32_t pw[8][4];
-#pragma unroll
-    for (int kk = 0; kk < 8; ++kk) {
-#pragma unroll
-        for (int h = 0; h < 2; ++h) {
-            const int nt = 2 * kk + h;
-            const float2 a = f2_of(aV[4 * nt + tq]);
-            const float wx = a.x * rho, wy = a.y * rho;
-            pw[kk][2 * h] = u32_of(__floats2half2_rn(S[nt][0] * wx, S[nt][1] * wy));
-            pw[kk][2 * h + 1] = u32_of(__floats2half2_rn(S[nt][2] * wx, S[nt][3] * wy));
-        }
-    }
-    float ws[4] = {0.f, 0.f, 0.f, 0.f};
-#pragma unroll
-    for (int kk = 0; kk < 8; ++kk) mma_f16(ws, pw[kk][0], pw[kk][1], pw[kk][2], pw[kk][3], kOnes, kOnes);
-    const float dV = *reinterpret_cast<const float*>(vrec);
-    const float mV = *reinterpret_cast<const float*>(vrec + 4);
-    const uint32_t* cV = reinterpret_cast<const uint32_t*>(vrec + 272);
-    const float irho = 1.0f / rho;  // a power of two: exact
-    const float gam = dV * 16777216.0f * irho;
-    const float de0 = mV * ws[0] * irho, de1 = mV * ws[2] * irho;
-    // matrix i of an ldmatrix: channels 16 np + 8 (i >> 1), tokens 16 kk + 8 (i & 1)
-    const uint32_t va = sV + ((lane & 7) + 8 * (lane >> 4)) * kPitch + 16 * ((lane >> 3) & 1);
-#pragma unroll
-    for (int np = 0; np < 8; ++np) {
-        float raw[2][4] = {{0.f, 0.f, 0.f, 0.f}, {0.f, 0.f, 0.f, 0.f}};
-#pragma unroll
-        for (int kk = 0; kk < 8; ++kk) {
-            uint32_t b[4];
-            ldsm4(va + 16 * np * kPitch + 32 * kk, b);
-            mma_f16(raw[0], pw[kk][0], pw[kk][1], pw[kk][2], pw[kk][3], b[0], b[1]);
-            mma_f16(raw[1], pw[kk][0], pw[kk][1], pw[kk][2], pw[kk][3], b[2], b[3]);
-        }
-#pragma unroll
-        for (int h = 0; h < 2; ++h) {
-            const int nt = 2 * np + h;
-            const float2 c = f2_of(cV[4 * nt + tq]);
-            st.acc[nt][0] = fmaf(c.x, fmaf(gam, raw[h][0], de0), st.acc[nt][0]);
-            st.acc[nt][1] = fmaf(c.y, fmaf(gam, raw[h][1], de0), st.acc[nt][1]);
-            st.acc[nt][2] = fmaf(c.x, fmaf(gam, raw[h][2], de1), st.acc[nt][2]);
-            st.acc[nt][3] = fmaf(c.y, fmaf(gam, raw[h][3], de1), st.acc[nt][3]);
-        }
-    }
-}
-
-__device__ __forceinline__ const uint8_t* group_src(const PrefillParams& p, const Cta& c, int g) {
+__device__ __forceinline__ const uint8_t* tc_group_src(const PrefillParams& p, const TcCta& c, int g) {
     const int32_t* table = reinterpret_cast<const int32_t*>(p.base + p.lay.block_table) +
                            ((size_t)c.e->seq * p.num_layers + p.layer) * p.max_groups;
     const int slot = table[g];
     return p.base + p.lay.pool + (size_t)slot * p.slot_bytes + (size_t)c.kvh * (p.rec_k + p.rec_v);
 }
 
+// fp16 row of an exact block (side 0 = K, 1 = V) at position pos
+__device__ __forceinline__ const uint4* exact_row(const PrefillParams& p, const TcCta& c, bool tail, int side, int pos) {
+    size_t off;
+    if (tail)
+        off = (side ? p.lay.tail_v : p.lay.tail_k) + (c.blk * p.tail_cap + (size_t)((pos - kSink) % p.tail_cap)) * 256;
+    else
+        off = (side ? p.lay.sink_v : p.lay.sink_k) + (c.blk * kSink + pos) * 256;
+    return reinterpret_cast<const uint4*>(p.base + off);
+}
+
+// bars: [0, 4) k_full (by unit % 4), [4, 6) k_empty, [6, 8) v_full, [8, 10) v_empty,
+// [10, 14) a_full (by unit % 4), 14 a_empty, [15, 17) s_full, [17, 19) p_full,
+// [19, 21) o_done (PV of unit v completes phase v / 2 of o_done[v % 2]), 21 drain (once),
+// [22, 26) m_full (by unit % 4: the unit's logits and row maxima are in place).
+// A barrier is indexed so that its previous phase has always completed when a thread
+// waits for the next: a parity wait cannot then be satisfied by an older phase. For
+// o_done this follows from tcgen05.mma completing in issue order: every wait for PV(v)
+// comes after its thread has seen QK(v) or a later MMA complete, and PV(v - 2) is issued
+// before QK(v) (QK(v) reuses the S buffer of PV(v - 2)'s weights).
+constexpr int kBarKFull = 0, kBarKEmpty = 4, kBarVFull = 6, kBarVEmpty = 8, kBarAFull = 10, kBarAEmpty = 14,
+              kBarSFull = 15, kBarPFull = 17, kBarODone = 19, kBarDrain = 21, kBarMFull = 22;
+
+// wait until PV of unit v has completed
+__device__ __forceinline__ void wait_pv(uint64_t* bars, int v, int32_t* err) {
+    mbar_wait(bars + kBarODone + (v & 1), (uint32_t)((v >> 1) & 1), err);
+}
+
+// ---- WG4: the MMA issuer (one thread) ----
+// QK(u) into S[u % 2] once the K tile and the query operand of unit u are in place and
+// PV(u - 2), the last reader of that S buffer, has been issued; PV(u) into O once the
+// weights of unit u and its V tile are in place. Whichever is ready is issued first.
+__device__ __forceinline__ void issue_qk(const TcCta& c, uint32_t sbase, uint64_t* bars, uint32_t tmem, int u) {
+    const int b = u & 1;
+    const bool sealed = u < c.n_sealed;
+    tc_fence_after();
+    const uint32_t d = tmem + kColS + 128u * b;
+    const uint32_t kt = sbase + b * kSetBytes + kOffK;
+#pragma unroll
+    for (int ks = 0; ks < 8; ++ks) mma_ts(d, tmem + kColA + 8 * ks, smem_desc(kt + ks * 4096), ks > 0);
+    if (sealed) {
+#pragma unroll
+        for (int ks = 0; ks < 8; ++ks) mma_ts(d, tmem + kColA + 64 + 8 * ks, smem_desc(kt + ks * 4096), 1u);
+    }
+    mma_commit(bars + kBarSFull + b);
+    mma_commit(bars + kBarKEmpty + b);
+    if (sealed) mma_commit(bars + kBarAEmpty);
+}
+
+__device__ __forceinline__ void issue_pv(const TcCta& c, uint32_t sbase, uint64_t* bars, uint32_t tmem, int v) {
+    const int b = v & 1;
+    tc_fence_after();
+    const uint32_t a = tmem + kColS + 128u * b;
+    const uint32_t vt = sbase + b * kSetBytes + kOffV;
+    // W high x B high, W high x B low (sealed only), W low x B high; the weights of
+    // k-step ks sit in columns 16 ks (high) and 16 ks + 8 (low)
+    const int passes = v < c.n_sealed ? 3 : 2;
+    for (int ps = 0; ps < passes; ++ps) {
+        const uint32_t alo = ps == passes - 1 ? 8u : 0u;
+        const uint32_t bks = ps == 1 && passes == 3 ? 8u : 0u;
+#pragma unroll
+        for (int ks = 0; ks < 8; ++ks)
+            mma_ts(tmem + kColO, a + 16 * ks + alo, smem_desc(vt + (bks + ks) * 4096),
+                   (v > 0 || ps > 0 || ks > 0) ? 1u : 0u);
+    }
+    mma_commit(bars + kBarVEmpty + b);
+    mma_commit(bars + kBarODone + b);
+}
+
+// non-blocking test of a barrier phase (try_wait may suspend the thread for a while)
+__device__ __forceinline__ bool mbar_test(uint64_t* bar, uint32_t parity) {
+    uint32_t ok;
+    asm volatile(
+        "{\n .reg .pred p;\n mbarrier.test_wait.parity.acquire.cta.shared::cta.b64 p, [%1], %2;\n"
+        " selp.u32 %0, 1, 0, p;\n}\n"
+        : "=r"(ok)
+        : "r"(smem_addr(bar)), "r"(parity)
+        : "memory");
+    return ok != 0;
+}
+
+__device__ __forceinline__ void issue_role(const TcCta& c, uint8_t* smem, uint64_t* bars, uint32_t tmem,
+                                           int32_t* err) {
+    const uint32_t sbase = smem_addr(smem);
+    int nq = 0, np = 0;  // next QK, next PV
+    uint64_t t0 = global_ns();
+    while (np < c.units) {
+        bool did = false;
+        if (nq < c.units && nq <= np + 1 && mbar_test(bars + kBarKFull + (nq & 3), (uint32_t)((nq >> 2) & 1)) &&
+            (nq > c.n_sealed || mbar_test(bars + kBarAFull + (nq & 3), (uint32_t)((nq >> 2) & 1)))) {
+            issue_qk(c, sbase, bars, tmem, nq);
+            ++nq;
+            did = true;
+        } else if (np < nq && mbar_test(bars + kBarPFull + (np & 1), (uint32_t)((np >> 1) & 1)) &&
+                   mbar_test(bars + kBarVFull + (np & 1), (uint32_t)((np >> 1) & 1))) {
+            issue_pv(c, sbase, bars, tmem, np);
+            ++np;
+            did = true;
+        }
+        if (did) {
+            t0 = global_ns();
+        } else if (global_ns() - t0 > kWaitLimitNs || (*reinterpret_cast<volatile int32_t*>(err) & kErrTimeout)) {
+            atomicOr(err, kErrTimeout);
+            return;
+        } else {
+            __nanosleep(32);  // leave the scheduler's issue slots to the softmax warp
+        }
+    }
+}
+
+__device__ __forceinline__ float wg_max(float x, float* red, int et, int id) {
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) x = fmaxf(x, __shfl_xor_sync(0xffffffffu, x, o));
+    if ((et & 31) == 0) red[et >> 5] = x;
+    named_bar(id, 128);
+    return fmaxf(fmaxf(red[0], red[1]), fmaxf(red[2], red[3]));
+}
+
+// The group's power of two e (its dequantised values times 2^-e stay below 2^15; the
+// weights take 2^e), computed alike by both expansion warpgroups from the V header.
+template <int VB>
+__device__ __forceinline__ int group_exponent(float aV, float cV, float dV, float mV, float* red, int et, int id) {
+    const float amax = wg_max(aV, red, et, id);
+    const float cmax = wg_max(cV, red + 4, et, id);
+    const float bound = amax * cmax * (fabsf(mV) + fabsf(dV) * (float)((1 << VB) - 1));
+    int e = 0;
+    if (bound > 32768.f) frexpf(bound * (1.0f / 32768.f), &e);
+    return e;
+}
+
+// What a thread of an expansion warpgroup reads of one record: its row of 128 codes
+// (B bits each) and the scales of its token / channel index.
+template <int B>
+struct RecRow {
+    uint32_t w[4 * B];
+    float a, cV, aV, d, m, dV, mV;
+};
+
+// Loads of unit u's V record for thread et, issued a unit ahead of their use.
+template <int VB>
+__device__ __forceinline__ void load_v(const PrefillParams& p, const TcCta& c, int u, int et, RecRow<VB>& L) {
+    if (u >= c.n_sealed) return;
+    const uint8_t* vr = tc_group_src(p, c, u) + p.rec_k;
+#pragma unroll
+    for (int i = 0; i < VB; ++i) {
+        const uint4 v4 = reinterpret_cast<const uint4*>(vr + 528 + et * 16 * VB)[i];
+        L.w[4 * i] = v4.x; L.w[4 * i + 1] = v4.y; L.w[4 * i + 2] = v4.z; L.w[4 * i + 3] = v4.w;
+    }
+    L.aV = __half2float(reinterpret_cast<const __half*>(vr + 16)[et]);
+    L.cV = __half2float(reinterpret_cast<const __half*>(vr + 272)[et]);
+    L.dV = *reinterpret_cast<const float*>(vr);
+    L.mV = *reinterpret_cast<const float*>(vr + 4);
+}
+
+// ---- WG3: the V tile of every unit (thread et = 0..127) ----
+template <int VB>
+__device__ __forceinline__ void expand_v_role(const PrefillParams& p, const TcCta& c, uint8_t* smem, uint64_t* bars,
+                                              int32_t* err, int et) {
+    const int lane = et & 31, wv = et >> 5;
+    float* red_all = reinterpret_cast<float*>(smem + kOffRed) + 16;
+    RecRow<VB> nx;
+    load_v<VB>(p, c, 0, et, nx);
+    for (int u = 0; u < c.units; ++u) {
+        const int b = u & 1;
+        const Unit x = unit_of(c, u);
+        uint8_t* set = smem + b * kSetBytes;
+        if (x.sealed) {
+            const RecRow<VB> L = nx;
+            load_v<VB>(p, c, u + 1, et, nx);
+            const uint32_t(&vs_)[4 * VB] = L.w;
+            const float aV = L.aV, cV = L.cV, dV = L.dV, mV = L.mV;
+            if (u >= 2) mbar_wait(bars + kBarVEmpty + b, (uint32_t)(((u >> 1) - 1) & 1), err);
+            // B = the dequantised value in the rotated frame, c_j aV_t (deltaV q_tj + mV), times 2^-e
+            float* alpha = reinterpret_cast<float*>(set + kOffAlpha);
+            float* beta = reinterpret_cast<float*>(set + kOffBeta);
+            alpha[et] = dV * aV;
+            beta[et] = mV * aV;
+            // (the reductions' barriers also publish alpha and beta)
+            const int e = group_exponent<VB>(aV, cV, dV, mV, red_all + 8 * b, et, 1);
+            const float cs = ldexpf(cV, -e);
+            const float2 cs2 = make_float2(cs, cs), m1 = make_float2(-1.f, -1.f);
+            // row = channel et: f16 high parts in k-steps 0..7, the f16 rounding of the
+            // residuals in k-steps 8..15
+            const float2* al2 = reinterpret_cast<const float2*>(alpha);
+            const float2* be2 = reinterpret_cast<const float2*>(beta);
+            uint32_t* vst = reinterpret_cast<uint32_t*>(smem + kOffVst) + et;
+#pragma unroll
+            for (int k = 0; k < 4 * VB; ++k) vst[128 * k] = vs_[k];
+#pragma unroll 1
+            for (int m = 0; m < 16; ++m) {
+                const uint4 q4 = codes8_staged<VB>(vst, m);
+                const uint32_t qw[4] = {q4.x, q4.y, q4.z, q4.w};
+                uint32_t hi[4], lo[4];
+#pragma unroll
+                for (int j = 0; j < 4; ++j) {
+                    const float2 x = __fmul2_rn(cs2, __ffma2_rn(__half22float2(u2h(qw[j])), al2[4 * m + j], be2[4 * m + j]));
+                    const __half2 h = __float22half2_rn(x);
+                    hi[j] = h2u(h);
+                    lo[j] = h2u(__float22half2_rn(__ffma2_rn(__half22float2(h), m1, x)));
+                }
+                *reinterpret_cast<uint4*>(set + kOffV + tile_off(et, 8 * m)) = make_uint4(hi[0], hi[1], hi[2], hi[3]);
+                *reinterpret_cast<uint4*>(set + kOffV + tile_off(et, 128 + 8 * m)) =
+                    make_uint4(lo[0], lo[1], lo[2], lo[3]);
+            }
+        } else {
+            // exact block: V rows transposed (movmatrix) into channel rows; core matrix
+            // cm = (ks 16 + rg) 2 + kc holds channels 8 rg .., tokens 16 ks + 8 kc ..
+            if (u >= 2) mbar_wait(bars + kBarVEmpty + b, (uint32_t)(((u >> 1) - 1) & 1), err);
+#pragma unroll 1
+            for (int hh = 0; hh < 2; ++hh) {
+                uint32_t a[32];
+#pragma unroll
+                for (int i = 0; i < 32; ++i) {
+                    const int cm = wv + 4 * (32 * hh + i);
+                    const int ks = cm >> 5, rg = (cm >> 1) & 15, kc = cm & 1;
+                    const int tt = 16 * ks + 8 * kc + (lane >> 2);
+                    a[i] = 0u;
+                    if (tt < x.cnt)
+                        a[i] = reinterpret_cast<const uint32_t*>(exact_row(p, c, x.tail, 1, x.kp0 + tt))[4 * rg + (lane & 3)];
+                }
+#pragma unroll
+                for (int i = 0; i < 32; ++i) {
+                    const int cm = wv + 4 * (32 * hh + i);
+                    uint32_t d;
+                    asm volatile("movmatrix.sync.aligned.m8n8.trans.b16 %0, %1;" : "=r"(d) : "r"(a[i]));
+                    *reinterpret_cast<uint32_t*>(set + kOffV + cm * 128 + 4 * lane) = d;
+                }
+            }
+        }
+        fence_proxy_async_smem();
+        mbar_arrive(bars + kBarVFull + b);
+    }
+}
+
+// 128-point Hadamard transform of a row held by one thread, scaled by 1 / sqrt(128);
+// the lower index of each pair takes a + b (the Sylvester order of the records).
+__device__ __forceinline__ void fwht_row(float (&v)[128]) {
+#pragma unroll
+    for (int len = 1; len < 128; len <<= 1) {
+#pragma unroll
+        for (int i = 0; i < 128; ++i) {
+            if (i & len) continue;
+            const float a = v[i], b = v[i + len];
+            v[i] = a + b;
+            v[i + len] = a - b;
+        }
+    }
+#pragma unroll
+    for (int i = 0; i < 128; ++i) v[i] *= kInvSqrt128;
+}
+
+// Row i of the tile: its query vector (null when the row is past the chunk).
+__device__ __forceinline__ const uint4* query_row(const PrefillParams& p, const TcCta& c, int i) {
+    const int tok = c.t0 + i / p.r;
+    if (tok >= c.e->q_len) return nullptr;
+    const size_t qrow = (size_t)(c.e->q_row + tok) * p.hq + (size_t)c.kvh * p.r + i % p.r;
+    return reinterpret_cast<const uint4*>(p.q + qrow * kHeadDim);
+}
+
+// ---- WG1: the query operand in tensor memory (thread i = row i) ----
+__device__ __forceinline__ void query_role(const PrefillParams& p, const TcCta& c, uint8_t* smem, uint64_t* bars,
+                                           uint32_t tmem, int32_t* err, int i, uint32_t lane_off) {
+    const uint4* qv = query_row(p, c, i);
+    float* rowqm = reinterpret_cast<float*>(smem + kOffQm);
+    float* rsring = reinterpret_cast<float*>(smem + kOffRs);
+    float* cq = reinterpret_cast<float*>(smem + kOffCq);
+    const uint32_t ta = tmem + lane_off + kColA;
+    if (c.n_sealed > 0) {
+        float v[128];
+#pragma unroll
+        for (int k = 0; k < 16; ++k) {
+            const uint4 r4 = qv ? qv[k] : make_uint4(0u, 0u, 0u, 0u);
+            const uint32_t w4[4] = {r4.x, r4.y, r4.z, r4.w};
+#pragma unroll
+            for (int j = 0; j < 4; ++j) {
+                const float2 f = __half22float2(u2h(w4[j]));
+                v[8 * k + 2 * j] = f.x;
+                v[8 * k + 2 * j + 1] = f.y;
+            }
+        }
+        fwht_row(v);
+        float qm = 0.f;
+#pragma unroll
+        for (int k = 0; k < 128; ++k) qm = fmaxf(qm, fabsf(v[k]));
+        const float inv = qm > 0.f ? 1.0f / qm : 0.f;
+#pragma unroll
+        for (int k = 0; k < 128; ++k) v[k] *= inv;
+        rowqm[i] = qm;
+        // channel i of the next group's c_K, fetched one group ahead
+        float cnext = __half2float(reinterpret_cast<const __half*>(tc_group_src(p, c, 0) + 272)[i]);
+        for (int u = 0; u < c.n_sealed; ++u) {
+            const float cme = cnext;
+            if (u + 1 < c.n_sealed)
+                cnext = __half2float(reinterpret_cast<const __half*>(tc_group_src(p, c, u + 1) + 272)[i]);
+            float* cu = cq + 128 * (u & 1);
+            cu[i] = cme;
+            named_bar(2, 128);
+            if (u >= 1) mbar_wait(bars + kBarAEmpty, (uint32_t)((u - 1) & 1), err);
+            tc_fence_after();
+            float2 rs2 = make_float2(0.f, 0.f);
+            const float2 m1 = make_float2(-1.f, -1.f);
+#pragma unroll
+            for (int cc = 0; cc < 8; ++cc) {
+                uint32_t hi[8], lo[8];
+#pragma unroll
+                for (int qd = 0; qd < 4; ++qd) {
+                    const float4 c4 = reinterpret_cast<const float4*>(cu)[4 * cc + qd];
+                    const int ch = 16 * cc + 4 * qd;
+                    const float2 x01 = __fmul2_rn(make_float2(v[ch], v[ch + 1]), make_float2(c4.x, c4.y));
+                    const float2 x23 = __fmul2_rn(make_float2(v[ch + 2], v[ch + 3]), make_float2(c4.z, c4.w));
+                    rs2 = __fadd2_rn(rs2, __fadd2_rn(x01, x23));
+                    const __half2 h01 = __float22half2_rn(x01), h23 = __float22half2_rn(x23);
+                    hi[2 * qd] = h2u(h01);
+                    hi[2 * qd + 1] = h2u(h23);
+                    lo[2 * qd] = h2u(__float22half2_rn(__ffma2_rn(__half22float2(h01), m1, x01)));
+                    lo[2 * qd + 1] = h2u(__float22half2_rn(__ffma2_rn(__half22float2(h23), m1, x23)));
+                }
+                tm_st8(ta + 8 * cc, hi);
+                tm_st8(ta + 64 + 8 * cc, lo);
+            }
+            tm_wait_st();
+            rsring[128 * (u & 3) + i] = rs2.x + rs2.y;
+            tc_fence_before();
+            mbar_arrive(bars + kBarAFull + (u & 3));
+        }
+        mbar_wait(bars + kBarAEmpty, (uint32_t)((c.n_sealed - 1) & 1), err);
+        tc_fence_after();
+    }
+    // the raw query for the exact blocks
+    uint32_t raw[32];
+#pragma unroll
+    for (int hh = 0; hh < 2; ++hh) {
+#pragma unroll
+        for (int k = 0; k < 8; ++k) {
+            const uint4 r4 = qv ? qv[8 * hh + k] : make_uint4(0u, 0u, 0u, 0u);
+            raw[4 * k] = r4.x; raw[4 * k + 1] = r4.y; raw[4 * k + 2] = r4.z; raw[4 * k + 3] = r4.w;
+        }
+        tm_st32(ta + 32 * hh, raw);
+    }
+    tm_wait_st();
+    tc_fence_before();
+    mbar_arrive(bars + kBarAFull + (c.n_sealed & 3));
+    if (c.n_sealed > 0) {
+        // once the last sealed group is in O, rotate row i of O back to the original frame
+        // for the exact blocks, then release the softmax warpgroups
+        wait_pv(bars, c.n_sealed - 1, err);
+        tc_fence_after();
+        const uint32_t to = tmem + lane_off + kColO;
+        float o[128];
+#pragma unroll
+        for (int ch = 0; ch < 4; ++ch) {
+            uint32_t r[32];
+            tm_ld32(to + 32 * ch, r);
+            tm_wait_ld();
+#pragma unroll
+            for (int j = 0; j < 32; ++j) o[32 * ch + j] = __uint_as_float(r[j]);
+        }
+        fwht_row(o);
+#pragma unroll
+        for (int ch = 0; ch < 4; ++ch) {
+            uint32_t r[32];
+#pragma unroll
+            for (int j = 0; j < 32; ++j) r[j] = __float_as_uint(o[32 * ch + j]);
+            tm_st32(to + 32 * ch, r);
+        }
+        tm_wait_st();
+        tc_fence_before();
+        named_bar(4, 256);
+    }
+}
+
+// O *= f over the thread's row (O complete up to the last PV issued)
+__device__ __forceinline__ void scale_o(uint32_t to, float f) {
+#pragma unroll 1
+    for (int ch = 0; ch < 4; ++ch) {
+        uint32_t r[32];
+        tm_ld32(to + 32 * ch, r);
+        tm_wait_ld();
+#pragma unroll
+        for (int j = 0; j < 32; ++j) r[j] = __float_as_uint(__uint_as_float(r[j]) * f);
+        tm_st32(to + 32 * ch, r);
+    }
+    tm_wait_st();
+}
+
+// Logits (log2 units) of 32 keys of a chunk, minus `sub`: sealed aK_t (al S + be) - sub,
+// exact S al - sub; keys past the block's end or the row's position are -inf.
+__device__ __forceinline__ void chunk_logits(const uint32_t (&r)[32], float (&w)[32], bool sealed, const float* aK,
+                                             int ch, float al, float be, float sub, bool masked, int kcnt, int kbase,
+                                             int pi) {
+    const float2 al2 = make_float2(al, al), ns2 = make_float2(-sub, -sub);
+    if (sealed) {
+        const float2 be2 = make_float2(be, be);
+#pragma unroll
+        for (int j4 = 0; j4 < 8; ++j4) {
+            const float4 a4 = reinterpret_cast<const float4*>(aK)[8 * ch + j4];
+            const float2 s01 = __ffma2_rn(al2, make_float2(__uint_as_float(r[4 * j4]), __uint_as_float(r[4 * j4 + 1])), be2);
+            const float2 s23 =
+                __ffma2_rn(al2, make_float2(__uint_as_float(r[4 * j4 + 2]), __uint_as_float(r[4 * j4 + 3])), be2);
+            const float2 w01 = __ffma2_rn(make_float2(a4.x, a4.y), s01, ns2);
+            const float2 w23 = __ffma2_rn(make_float2(a4.z, a4.w), s23, ns2);
+            w[4 * j4] = w01.x;
+            w[4 * j4 + 1] = w01.y;
+            w[4 * j4 + 2] = w23.x;
+            w[4 * j4 + 3] = w23.y;
+        }
+    } else {
+#pragma unroll
+        for (int j2 = 0; j2 < 16; ++j2) {
+            const float2 w2 =
+                __ffma2_rn(make_float2(__uint_as_float(r[2 * j2]), __uint_as_float(r[2 * j2 + 1])), al2, ns2);
+            w[2 * j2] = w2.x;
+            w[2 * j2 + 1] = w2.y;
+        }
+    }
+    if (masked) {
+#pragma unroll
+        for (int j = 0; j < 32; ++j)
+            if (32 * ch + j >= kcnt || kbase + 32 * ch + j > pi) w[j] = kNegInfT;
+    }
+}
+
+// Weights of 16 keys (one k-step) as f16 high parts then the f16 rounding of the residuals.
+__device__ __forceinline__ void split16(const float* w, uint32_t* o) {
+    const float2 m1 = make_float2(-1.f, -1.f);
+#pragma unroll
+    for (int q = 0; q < 8; ++q) {
+        const float2 x = make_float2(w[2 * q], w[2 * q + 1]);
+        const __half2 hv = __float22half2_rn(x);
+        o[q] = h2u(hv);
+        o[8 + q] = h2u(__float22half2_rn(__ffma2_rn(__half22float2(hv), m1, x)));
+    }
+}
+
+// Loads of unit u's K record (and the V header the group's power of two needs) for
+// thread et, issued ahead of their use.
+template <int KB>
+__device__ __forceinline__ void load_k(const PrefillParams& p, const TcCta& c, int u, int et, RecRow<KB>& L) {
+    if (u >= c.n_sealed) return;
+    const uint8_t* kr = tc_group_src(p, c, u);
+    const uint8_t* vr = kr + p.rec_k;
+#pragma unroll
+    for (int i = 0; i < KB; ++i) {
+        const uint4 v4 = reinterpret_cast<const uint4*>(kr + 528 + et * 16 * KB)[i];
+        L.w[4 * i] = v4.x; L.w[4 * i + 1] = v4.y; L.w[4 * i + 2] = v4.z; L.w[4 * i + 3] = v4.w;
+    }
+    L.a = __half2float(reinterpret_cast<const __half*>(kr + 16)[et]);
+    L.d = *reinterpret_cast<const float*>(kr);
+    L.m = *reinterpret_cast<const float*>(kr + 4);
+    L.aV = __half2float(reinterpret_cast<const __half*>(vr + 16)[et]);
+    L.cV = __half2float(reinterpret_cast<const __half*>(vr + 272)[et]);
+    L.dV = *reinterpret_cast<const float*>(vr);
+    L.mV = *reinterpret_cast<const float*>(vr + 4);
+}
+
+// ---- WG2: the K tile and the K-side tables of unit u (thread et = 0..127) ----
 template <int KB, int VB>
-__global__ void __launch_bounds__(kPrefillThreads, 1) prefill_kernel(const __grid_constant__ PrefillParams p) {
-    extern __shared__ __align__(128) uint8_t smem[];
-    const int t = threadIdx.x, lane = t & 31, w = t >> 5;
-    const int g = lane >> 2;
-    const int pair = p.rec_k + p.rec_v;
-    uint8_t* ring = smem + kOffRing;
-    uint64_t* full = reinterpret_cast<uint64_t*>(ring + (size_t)p.stages * pair);
-    int* rowpos = reinterpret_cast<int*>(full + p.stages);
-    float* rowqm = reinterpret_cast<float*>(rowpos + kPfRows);
+__device__ __forceinline__ void expand_k_unit(const PrefillParams& p, const TcCta& c, uint8_t* smem, uint64_t* bars,
+                                              int32_t* err, int et, int u, const RecRow<KB>& L) {
+    float* red_all = reinterpret_cast<float*>(smem + kOffRed);
+    const int b = u & 1;
+    const Unit x = unit_of(c, u);
+    uint8_t* set = smem + b * kSetBytes;
+    float* kt = reinterpret_cast<float*>(smem + kOffKtab + (u & 3) * kKtabBytes);
+    if (x.sealed) {
+        // the set's K tile is free once QK(u - 2) has completed; the table slot u % 4 once
+        // the softmax of unit u - 4 is done, which QK(u - 2) being issued implies
+        if (u >= 2) mbar_wait(bars + kBarKEmpty + b, (uint32_t)(((u >> 1) - 1) & 1), err);
+        const int e = group_exponent<VB>(L.aV, L.cV, L.dV, L.mV, red_all + 8 * b, et, 5);
+#pragma unroll
+        for (int m = 0; m < 16; ++m)
+            *reinterpret_cast<uint4*>(set + kOffK + tile_off(et, 8 * m)) = codes8<KB>(L.w, m);
+        kt[et] = L.a;
+        if (et == 0) {
+            kt[128] = L.d;
+            kt[129] = L.m;
+            kt[130] = (float)e;
+        }
+    } else {
+        // exact block: the K rows as they are (rows past the block's end are zeros)
+        const bool live = et < x.cnt;
+        const uint4* src = live ? exact_row(p, c, x.tail, 0, x.kp0 + et) : nullptr;
+        if (u >= 2) mbar_wait(bars + kBarKEmpty + b, (uint32_t)(((u >> 1) - 1) & 1), err);
+#pragma unroll 1
+        for (int i0 = 0; i0 < 16; i0 += 4) {
+            uint4 kr[4];
+#pragma unroll
+            for (int i = 0; i < 4; ++i) kr[i] = live ? src[i0 + i] : make_uint4(0u, 0u, 0u, 0u);
+#pragma unroll
+            for (int i = 0; i < 4; ++i) *reinterpret_cast<uint4*>(set + kOffK + tile_off(et, 8 * (i0 + i))) = kr[i];
+        }
+    }
+    fence_proxy_async_smem();
+    mbar_arrive(bars + kBarKFull + (u & 3));
+}
+
+// ---- WG2: the logits of unit v for row i (once QK(v) has completed): written back
+// over S as fp32 (log2 units, masked keys -inf), the row maximum into the ring ----
+__device__ __forceinline__ void logits_unit(const PrefillParams& p, const TcCta& c, uint8_t* smem, uint64_t* bars,
+                                            uint32_t tmem, int32_t* err, int i, uint32_t lane_off, int v) {
+    const int b = v & 1;
+    const Unit x = unit_of(c, v);
+    const int pi = reinterpret_cast<const int*>(smem + kOffPos)[i];
+    const float* kt = reinterpret_cast<const float*>(smem + kOffKtab + (v & 3) * kKtabBytes);
+    mbar_wait(bars + kBarSFull + b, (uint32_t)((v >> 1) & 1), err);
+    float al = p.scale_log2, be = 0.f;
+    int kbase, kcnt;
+    if (x.sealed) {
+        mbar_wait(bars + kBarAFull + (v & 3), (uint32_t)((v >> 2) & 1), err);
+        const float qm = reinterpret_cast<const float*>(smem + kOffQm)[i];
+        al = p.scale_log2 * qm * kt[128];
+        be = p.scale_log2 * qm * kt[129] * reinterpret_cast<const float*>(smem + kOffRs)[128 * (v & 3) + i];
+        kbase = kSink + kGroup * x.g;
+        kcnt = kGroup;
+    } else {
+        kbase = x.kp0;
+        kcnt = x.cnt;
+    }
+    tc_fence_after();
+    const uint32_t ts = tmem + lane_off + kColS + 128u * b;
+    const bool masked = kcnt < kGroup || kbase + kGroup - 1 > c.pmin;
+    float mx = kNegInfT;
+#pragma unroll 1
+    for (int ch = 0; ch < 4; ++ch) {
+        uint32_t r[32];
+        tm_ld32(ts + 32 * ch, r);
+        tm_wait_ld();
+        float w[32];
+        chunk_logits(r, w, x.sealed, kt, ch, al, be, 0.f, masked, kcnt, kbase, pi);
+#pragma unroll
+        for (int j = 0; j < 32; ++j) {
+            mx = fmaxf(mx, w[j]);
+            r[j] = __float_as_uint(w[j]);
+        }
+        tm_st32(ts + 32 * ch, r);
+    }
+    reinterpret_cast<float*>(smem + kOffMx)[128 * (v & 3) + i] = mx;
+    tm_wait_st();
+    tc_fence_before();
+    mbar_arrive(bars + kBarMFull + (v & 3));
+}
+
+// WG2's loop: the K tiles of units 0 and 1, then per unit v the logits of v (as soon as
+// QK(v) completes) followed by the K tile of v + 2 (whose slot QK(v) has just freed),
+// that tile's loads issued before the logits.
+template <int KB, int VB>
+__device__ __forceinline__ void k_role(const PrefillParams& p, const TcCta& c, uint8_t* smem, uint64_t* bars,
+                                       uint32_t tmem, int32_t* err, int et, uint32_t lane_off) {
+    for (int u = 0; u < 2 && u < c.units; ++u) {
+        RecRow<KB> L;
+        load_k<KB>(p, c, u, et, L);
+        expand_k_unit<KB, VB>(p, c, smem, bars, err, et, u, L);
+    }
+    for (int v = 0; v < c.units; ++v) {
+        RecRow<KB> L;
+        load_k<KB>(p, c, v + 2, et, L);
+        logits_unit(p, c, smem, bars, tmem, err, et, lane_off, v);
+        if (v + 2 < c.units) expand_k_unit<KB, VB>(p, c, smem, bars, err, et, v + 2, L);
+    }
+}
+
+// ---- WG0: softmax, rescaling and the output (thread i = row i) ----
+__device__ __forceinline__ void softmax_role(const PrefillParams& p, const TcCta& c, uint8_t* smem, uint64_t* bars,
+                                             uint32_t tmem, int32_t* err, int i, uint32_t lane_off) {
+    const uint32_t to = tmem + lane_off + kColO;
+    float m_used = kNegInfT, l = 0.f;
+    for (int u = 0; u < c.units; ++u) {
+        const int b = u & 1;
+        const Unit x = unit_of(c, u);
+        if (!x.sealed && u == c.n_sealed && u > 0) {
+            // all sealed groups are in O: the query warpgroup rotates it back to the
+            // original frame before any thread here touches O again
+            tc_fence_before();
+            named_bar(4, 256);
+            tc_fence_after();
+        }
+        // the unit's logits (over S) and row maximum, from the K warpgroup
+        mbar_wait(bars + kBarMFull + (u & 3), (uint32_t)((u >> 2) & 1), err);
+        const float e = x.sealed ? reinterpret_cast<const float*>(smem + kOffKtab + (u & 3) * kKtabBytes)[130] : 0.f;
+        const float mx = reinterpret_cast<const float*>(smem + kOffMx)[128 * (u & 3) + i];
+        tc_fence_after();
+        const uint32_t ts = tmem + lane_off + kColS + 128u * b;
+        // raise the reference maximum where it grew by more than 8; O and l follow (O
+        // holds PV of every earlier unit). Tensor-memory accesses are warp-wide: the
+        // whole warp rescales, by 1 in the rows that keep their maximum.
+        const bool raise = mx > m_used + 8.0f;
+        const float corr = raise ? ex2f(m_used - mx) : 1.0f;
+        if (raise) {
+            l *= corr;
+            m_used = mx;
+        }
+        if (u > 0 && __any_sync(0xffffffffu, raise)) {
+            wait_pv(bars, u - 1, err);
+            tc_fence_after();
+            scale_o(to, corr);
+        }
+        // weights W = 2^(logit - m + e) as f16 high and low parts, written over the
+        // chunk's own columns: k-step ks (16 tokens) holds the high parts in columns
+        // 16 ks .. 16 ks + 7 and the low parts in 16 ks + 8 .. 16 ks + 15
+        const float sub = (m_used == kNegInfT ? 0.f : m_used) - e;
+        const float2 ns2 = make_float2(-sub, -sub);
+        float ws0 = 0.f, ws1 = 0.f;
+#pragma unroll 1
+        for (int ch = 0; ch < 4; ++ch) {
+            uint32_t r[32];
+            tm_ld32(ts + 32 * ch, r);
+            tm_wait_ld();
+            float w[32];
+            float2 ws2 = make_float2(0.f, 0.f);
+#pragma unroll
+            for (int j2 = 0; j2 < 16; ++j2) {
+                const float2 d = __fadd2_rn(make_float2(__uint_as_float(r[2 * j2]), __uint_as_float(r[2 * j2 + 1])), ns2);
+                w[2 * j2] = ex2f(d.x);
+                w[2 * j2 + 1] = ex2f(d.y);
+                ws2 = __fadd2_rn(ws2, make_float2(w[2 * j2], w[2 * j2 + 1]));
+            }
+            ws0 += ws2.x;
+            ws1 += ws2.y;
+            uint32_t o[32];
+            split16(w, o);
+            split16(w + 16, o + 16);
+            tm_st32(ts + 32 * ch, o);
+        }
+        l += ldexpf(ws0 + ws1, -(int)e);
+        tm_wait_st();
+        tc_fence_before();
+        mbar_arrive(bars + kBarPFull + b);
+    }
+    // normalise and write the row
+    wait_pv(bars, c.units - 1, err);
+    tc_fence_after();
+    const int tok = c.t0 + i / p.r;
+    const float inv = l > 0.f ? 1.0f / l : 0.f;
+    uint4* dst = nullptr;
+    if (tok < c.e->q_len) {
+        const size_t orow = (size_t)(c.e->q_row + tok) * p.hq + (size_t)c.kvh * p.r + i % p.r;
+        dst = reinterpret_cast<uint4*>(p.out + orow * kHeadDim);
+    }
+#pragma unroll 1
+    for (int ch = 0; ch < 4; ++ch) {
+        uint32_t r[32];
+        tm_ld32(to + 32 * ch, r);
+        tm_wait_ld();
+        if (dst) {
+#pragma unroll
+            for (int k = 0; k < 4; ++k) {
+                uint32_t o4[4];
+#pragma unroll
+                for (int j = 0; j < 4; ++j)
+                    o4[j] = h2u(__floats2half2_rn(__uint_as_float(r[8 * k + 2 * j]) * inv,
+                                                  __uint_as_float(r[8 * k + 2 * j + 1]) * inv));
+                dst[4 * ch + k] = make_uint4(o4[0], o4[1], o4[2], o4[3]);
+            }
+        }
+    }
+}
+
+template <int KB, int VB>
+__global__ void __launch_bounds__(kTcThreads, 1) prefill_kernel(const __grid_constant__ PrefillParams p) {
+    extern __shared__ __align__(1024) uint8_t smem[];
+    const int t = threadIdx.x, w = t >> 5, lane = t & 31, wg = w >> 2;
     int32_t* err = reinterpret_cast<int32_t*>(p.base + p.lay.err);
+    uint64_t* bars = reinterpret_cast<uint64_t*>(smem + kOffBars);
 
     // the CTA's (sequence, KV head, tile): the heaviest tiles (latest tokens) first
-    Cta c;
+    TcCta c;
     {
         int lo = 0, up = p.n_seqs - 1;
         while (lo < up) {
@@ -469,231 +929,121 @@ __global__ void __launch_bounds__(kPrefillThreads, 1) prefill_kernel(const __gri
         const int local = (int)blockIdx.x - c.e->cta_begin;
         c.kvh = local % p.hkv;
         const int tile = c.e->n_tiles - 1 - local / p.hkv;
-        c.r = p.r;
-        const int qt = kPfRows / p.r;
+        const int qt = kRows / p.r;
         c.t0 = tile * qt;
-        c.first_pos = c.e->n - c.e->q_len;
-        c.pmax = c.first_pos + min(c.t0 + qt, c.e->q_len) - 1;
+        const int first_pos = c.e->n - c.e->q_len;
+        c.pmin = first_pos + c.t0;
+        c.pmax = first_pos + min(c.t0 + qt, c.e->q_len) - 1;
         const int vis = c.pmax >= kSink ? (c.pmax - kSink) / kGroup + 1 : 0;
-        c.n_vis = min(c.e->n_groups, vis);
+        c.n_sealed = min(c.e->n_groups, vis);
         c.blk = ((size_t)c.e->seq * p.num_layers + p.layer) * p.hkv + c.kvh;
+        c.sink_vis = min(min(c.e->n, kSink), c.pmax + 1);
+        c.nb_sink = c.sink_vis > 0 ? 1 : 0;
+        c.tail_start = kSink + kGroup * c.e->n_groups;
+        c.tail_vis = max(0, min(c.e->n, c.pmax + 1) - c.tail_start);
+        c.units = c.n_sealed + c.nb_sink + (c.tail_vis + kGroup - 1) / kGroup;
+        if (t < kRows) {
+            const int tok = c.t0 + t / p.r;
+            reinterpret_cast<int*>(smem + kOffPos)[t] = tok < c.e->q_len ? first_pos + tok : c.e->n - 1;
+        }
     }
-    const int n_vis = c.n_vis;
     if (t == 0) {
-        for (int s = 0; s < p.stages; ++s) mbar_init(full + s, 1);
+        for (int k = 0; k < 4; ++k) {
+            mbar_init(bars + kBarKFull + k, 128);
+            mbar_init(bars + kBarAFull + k, 128);
+            mbar_init(bars + kBarMFull + k, 128);
+        }
+        for (int k = 0; k < 2; ++k) {
+            mbar_init(bars + kBarKEmpty + k, 1);
+            mbar_init(bars + kBarVFull + k, 128);
+            mbar_init(bars + kBarVEmpty + k, 1);
+            mbar_init(bars + kBarSFull + k, 1);
+            mbar_init(bars + kBarPFull + k, 128);
+            mbar_init(bars + kBarODone + k, 1);
+        }
+        mbar_init(bars + kBarAEmpty, 1);
+        mbar_init(bars + kBarDrain, 1);
         asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
-        for (int gi = 0; gi < min(n_vis, p.stages); ++gi) {
-            mbar_arrive_expect_tx(full + gi, (uint32_t)pair);
-            bulk_g2s(ring + (size_t)gi * pair, group_src(p, c, gi), (uint32_t)pair, full + gi);
-        }
     }
-    // stage the tile's queries (fp16 rows; rows past the chunk are zeros) and positions
-    {
-        uint8_t* qraw = smem + kOffQraw;
-#pragma unroll
-        for (int it = 0; it < kPfRows * 16 / kPrefillThreads; ++it) {
-            const int idx = t + kPrefillThreads * it;
-            const int row = idx >> 4, col = idx & 15;
-            const int tok = c.t0 + row / c.r;
-            uint4 v = make_uint4(0u, 0u, 0u, 0u);
-            if (tok < c.e->q_len) {
-                const size_t qrow = ((size_t)(c.e->q_row + tok) * p.hq + (size_t)c.kvh * c.r + row % c.r);
-                v = reinterpret_cast<const uint4*>(p.q + qrow * kHeadDim)[col];
-            }
-            *reinterpret_cast<uint4*>(qraw + row * kPitch + 16 * col) = v;
-        }
-        if (t < kPfRows) {
-            const int tok = c.t0 + t / c.r;
-            rowpos[t] = tok < c.e->q_len ? c.first_pos + tok : c.e->n - 1;
-        }
+    if (w == 16) {
+        asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], 512;" ::"r"(
+                         smem_addr(smem + kOffTmem))
+                     : "memory");
+        asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;" ::: "memory");
     }
-    RowState st;
-    st.m[0] = st.m[1] = kNegInfP;
-    st.l[0] = st.l[1] = 0.f;
-#pragma unroll
-    for (int nt = 0; nt < 16; ++nt) st.acc[nt][0] = st.acc[nt][1] = st.acc[nt][2] = st.acc[nt][3] = 0.f;
+    tc_fence_before();
     __syncthreads();
-    const int p0 = rowpos[16 * w + g], p1 = rowpos[16 * w + g + 8];
-
-    // ---- exact phase: the sink, then the tail, in blocks of 64 tokens
-    {
-        const int n_sink = min(c.e->n, kSink);
-        const int sink_vis = min(n_sink, c.pmax + 1);
-        const int tail_start = kSink + kGroup * c.e->n_groups;
-        const int tail_vis = max(0, min(c.e->n, c.pmax + 1) - tail_start);
-        const int nb_sink = (sink_vis + kExactBlock - 1) / kExactBlock;
-        const int nb = nb_sink + (tail_vis + kExactBlock - 1) / kExactBlock;
-        const uint32_t sK = smem_addr(smem + kOffTiles), sV = sK + kExactBlock * kPitch;
-        const uint32_t sQ = smem_addr(smem + kOffQraw) + 16 * w * kPitch;
-        for (int b = 0; b < nb; ++b) {
-            const bool tail = b >= nb_sink;
-            const int kp0 = tail ? tail_start + kExactBlock * (b - nb_sink) : kExactBlock * b;
-            const int cnt = tail ? min(kExactBlock, tail_start + tail_vis - kp0) : min(kExactBlock, sink_vis - kp0);
-            if (b > 0) __syncthreads();  // every warp is done with the previous block
-#pragma unroll
-            for (int it = 0; it < 2 * kExactBlock * 16 / kPrefillThreads; ++it) {
-                const int idx = t + kPrefillThreads * it;
-                const int side = idx / (kExactBlock * 16);
-                const int row = (idx >> 4) % kExactBlock, col = idx & 15;
-                uint4 v = make_uint4(0u, 0u, 0u, 0u);
-                if (row < cnt) {
-                    const int pos = kp0 + row;
-                    size_t off;
-                    if (tail)
-                        off = (side ? p.lay.tail_v : p.lay.tail_k) +
-                              (c.blk * p.tail_cap + (size_t)((pos - kSink) % p.tail_cap)) * 256;
-                    else
-                        off = (side ? p.lay.sink_v : p.lay.sink_k) + (c.blk * kSink + pos) * 256;
-                    v = reinterpret_cast<const uint4*>(p.base + off)[col];
-                }
-                *reinterpret_cast<uint4*>(smem + kOffTiles + (side * kExactBlock + row) * kPitch + 16 * col) = v;
-            }
-            __syncthreads();
-            exact_block(sK, sV, sQ, kp0, cnt, p0, p1, p.scale_log2, st, lane);
-        }
-    }
-
-    if (n_vis > 0) {
-        // ---- the warp's query operand tables: v = q H / qm split into f16 high and low parts
-        {
-            const uint8_t* qraw = smem + kOffQraw;
-            uint32_t* qhi = reinterpret_cast<uint32_t*>(smem + kOffQhi) + w * 8 * 32 * 4;
-            uint32_t* qlo = reinterpret_cast<uint32_t*>(smem + kOffQlo) + w * 8 * 32 * 4;
-            for (int rr = 0; rr < 16; ++rr) {
-                const uint2 raw = *reinterpret_cast<const uint2*>(qraw + (16 * w + rr) * kPitch + 8 * lane);
-                const float2 x01 = f2_of(raw.x), x23 = f2_of(raw.y);
-                float v[4] = {x01.x, x01.y, x23.x, x23.y};
-                vec_fwht128(v, lane);
-                float qm = fmaxf(fmaxf(fabsf(v[0]), fabsf(v[1])), fmaxf(fabsf(v[2]), fabsf(v[3])));
-#pragma unroll
-                for (int o = 1; o < 32; o <<= 1) qm = fmaxf(qm, __shfl_xor_sync(0xffffffffu, qm, o));
-                const float inv = qm > 0.f ? 1.0f / qm : 0.f;
-                if (lane == 0) rowqm[16 * w + rr] = qm;
-                // channels 4 lane + 2 j, + 1 -> fragment (k-step ks, lane 4 (rr % 8) + tq, register rb + 2 h)
-#pragma unroll
-                for (int j = 0; j < 2; ++j) {
-                    const int ch = 4 * lane + 2 * j;
-                    const int ks = ch >> 4, h = (ch >> 3) & 1, tq = (ch & 7) >> 1;
-                    const int reg = (rr >> 3) + 2 * h;
-                    const int dst = (ks * 32 + 4 * (rr & 7) + tq) * 4 + reg;
-                    const float a = v[2 * j] * inv, b = v[2 * j + 1] * inv;
-                    const __half2 hi = __floats2half2_rn(a, b);
-                    const float2 hf = __half22float2(hi);
-                    qhi[dst] = u32_of(hi);
-                    qlo[dst] = u32_of(__floats2half2_rn(a - hf.x, b - hf.y));
-                }
+    tc_fence_after();
+    const uint32_t tmem = *reinterpret_cast<volatile uint32_t*>(smem + kOffTmem);
+    const uint32_t lane_off = (uint32_t)(32 * (w & 3)) << 16;
+    if (wg == 0) {
+        asm volatile("setmaxnreg.inc.sync.aligned.u32 %0;" ::"n"(kRegsSoftmax));
+        softmax_role(p, c, smem, bars, tmem, err, t, lane_off);
+    } else if (wg == 1) {
+        asm volatile("setmaxnreg.inc.sync.aligned.u32 %0;" ::"n"(kRegsQuery));
+        query_role(p, c, smem, bars, tmem, err, t - 128, lane_off);
+    } else if (wg == 2) {
+        asm volatile("setmaxnreg.dec.sync.aligned.u32 %0;" ::"n"(kRegsExpandK));
+        k_role<KB, VB>(p, c, smem, bars, tmem, err, t - 256, lane_off);
+    } else if (wg == 3) {
+        asm volatile("setmaxnreg.dec.sync.aligned.u32 %0;" ::"n"(kRegsExpandV));
+        expand_v_role<VB>(p, c, smem, bars, err, t - 384);
+    } else {
+        asm volatile("setmaxnreg.dec.sync.aligned.u32 %0;" ::"n"(kRegsIssue));
+        if (w == 16 && lane == 0) {
+            issue_role(c, smem, bars, tmem, err);
+            // every MMA has completed before tensor memory is released (bounded even
+            // after another wait gave up)
+            mma_commit(bars + kBarDrain);
+            const uint64_t t0 = global_ns();
+            while (!mbar_try_wait(bars + kBarDrain, 0u) && global_ns() - t0 < kWaitLimitNs) {
             }
         }
-        rows_fwht128(st.acc, lane);  // into the records' frame
-        __syncthreads();
-        const float qm0 = rowqm[16 * w + g], qm1 = rowqm[16 * w + g + 8];
-        const int pmin = __shfl_sync(0xffffffffu, min(p0, p1), 0);  // rows are in position order
-        const uint4* qhi = reinterpret_cast<const uint4*>(smem + kOffQhi) + w * 8 * 32;
-        const uint4* qlo = reinterpret_cast<const uint4*>(smem + kOffQlo) + w * 8 * 32;
-        const uint32_t sK = smem_addr(smem + kOffTiles), sV = sK + kTileBytes;
-        for (int gi = 0; gi < n_vis; ++gi) {
-            const int s = gi % p.stages;
-            const uint8_t* stage = ring + (size_t)s * pair;
-            if (gi > 0) {
-                __syncthreads();  // every warp is done with group gi - 1 (tiles and its stage)
-                if (t == 0 && gi - 1 + p.stages < n_vis) {
-                    const int sp = (gi - 1) % p.stages;
-                    mbar_arrive_expect_tx(full + sp, (uint32_t)pair);
-                    bulk_g2s(ring + (size_t)sp * pair, group_src(p, c, gi - 1 + p.stages), (uint32_t)pair, full + sp);
-                }
-            }
-            mbar_wait(full + s, (uint32_t)((gi / p.stages) & 1), err);
-            // expand the codes: 2 records x 128 rows x 4 chunks of 32 codes
-#pragma unroll
-            for (int it = 0; it < 4; ++it) {
-                const int idx = t + kPrefillThreads * it;
-                const int side = idx >> 9, row = (idx >> 2) & 127, ch = idx & 3;
-                uint8_t* dst = smem + kOffTiles + side * kTileBytes + row * kPitch + 64 * ch;
-                if (side == 0)
-                    expand_chunk<KB>(stage + 528 + row * 16 * KB + ch * 4 * KB, dst);
-                else
-                    expand_chunk<VB>(stage + p.rec_k + 528 + row * 16 * VB + ch * 4 * VB, dst);
-            }
-            __syncthreads();
-            const int gp0 = kSink + kGroup * gi;
-            sealed_group(sK, sV, stage, stage + p.rec_k, qhi, qlo, qm0, qm1, gp0, gp0 + kGroup - 1 > pmin, p0, p1,
-                         p.scale_log2, st, lane);
-        }
-        rows_fwht128(st.acc, lane);  // back to the original frame
     }
-
-    // ---- normalise and write the valid rows
-    float l0 = st.l[0], l1 = st.l[1];
-#pragma unroll
-    for (int o = 1; o < 4; o <<= 1) {
-        l0 += __shfl_xor_sync(0xffffffffu, l0, o);
-        l1 += __shfl_xor_sync(0xffffffffu, l1, o);
-    }
-    const float i0 = 1.0f / l0, i1 = 1.0f / l1;
-    const int tq = lane & 3;
-#pragma unroll
-    for (int half = 0; half < 2; ++half) {
-        const int row = 16 * w + g + 8 * half;
-        const int tok = c.t0 + row / c.r;
-        if (tok < c.e->q_len) {
-            const size_t orow = (size_t)(c.e->q_row + tok) * p.hq + (size_t)c.kvh * c.r + row % c.r;
-            uint32_t* o = reinterpret_cast<uint32_t*>(p.out + orow * kHeadDim);
-            const float inv = half ? i1 : i0;
-#pragma unroll
-            for (int nt = 0; nt < 16; ++nt)
-                o[4 * nt + tq] = u32_of(__floats2half2_rn(st.acc[nt][2 * half] * inv, st.acc[nt][2 * half + 1] * inv));
-        }
-    }
-    // Normally every copy was waited for. After a wait that gave up, let the copies in
-    // flight land (bounded) before the CTA's shared memory goes away.
+    tc_fence_before();
     __syncthreads();
-    if (t == 0 && (*reinterpret_cast<volatile int32_t*>(err) & kErrTimeout)) {
-        const uint64_t t0 = global_ns();
-        for (int k = max(0, n_vis - p.stages); k < n_vis; ++k)  // every group below n_vis was issued
-            while (!mbar_try_wait(full + (k % p.stages), (uint32_t)((k / p.stages) & 1)) &&
-                   global_ns() - t0 < kWaitLimitNs) {
-            }
+    tc_fence_after();
+    if (w == 16) {
+        __syncwarp();
+        asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, 512;" ::"r"(tmem) : "memory");
     }
 }
 
 template <int KB, int VB>
-int launch_pf(const PrefillParams& p, int smem, cudaStream_t s) {
+int launch_tc(const PrefillParams& p, cudaStream_t s) {
     static bool attr = false;
     if (!attr) {
         cudaError_t e = cudaFuncSetAttribute(prefill_kernel<KB, VB>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                             max_optin_smem());
+                                             kSmemTc);
         if (e != cudaSuccess) return (int)e;
         attr = true;
     }
-    prefill_kernel<KB, VB><<<p.grid, kPrefillThreads, smem, s>>>(p);
+    prefill_kernel<KB, VB><<<p.grid, kTcThreads, kSmemTc, s>>>(p);
     return (int)cudaGetLastError();
 }
 
 }  // namespace
 
-int prefill_smem_bytes(int k_bits, int v_bits, int stages) {
-    const size_t pair = record_bytes(k_bits) + record_bytes(v_bits);
-    return (int)(kOffRing + (size_t)stages * pair + (size_t)stages * 8 + kPrefillRows * 8);
-}
+int prefill_smem_bytes() { return kSmemTc; }
 
-int launch_prefill(const PrefillParams& p, int smem, void* stream) {
+int launch_prefill(const PrefillParams& p, void* stream) {
     cudaStream_t s = (cudaStream_t)stream;
     switch (p.k_bits * 16 + p.v_bits) {
-        case 0x22: return launch_pf<2, 2>(p, smem, s);
-        case 0x24: return launch_pf<2, 4>(p, smem, s);
-        case 0x28: return launch_pf<2, 8>(p, smem, s);
-        case 0x42: return launch_pf<4, 2>(p, smem, s);
-        case 0x44: return launch_pf<4, 4>(p, smem, s);
-        case 0x48: return launch_pf<4, 8>(p, smem, s);
-        case 0x82: return launch_pf<8, 2>(p, smem, s);
-        case 0x84: return launch_pf<8, 4>(p, smem, s);
-        case 0x88: return launch_pf<8, 8>(p, smem, s);
-        case 0x33: return launch_pf<3, 3>(p, smem, s);
-        case 0x55: return launch_pf<5, 5>(p, smem, s);
-        case 0x66: return launch_pf<6, 6>(p, smem, s);
-        case 0x65: return launch_pf<6, 5>(p, smem, s);
-        case 0x54: return launch_pf<5, 4>(p, smem, s);
-        case 0x32: return launch_pf<3, 2>(p, smem, s);
+        case 0x22: return launch_tc<2, 2>(p, s);
+        case 0x24: return launch_tc<2, 4>(p, s);
+        case 0x28: return launch_tc<2, 8>(p, s);
+        case 0x42: return launch_tc<4, 2>(p, s);
+        case 0x44: return launch_tc<4, 4>(p, s);
+        case 0x48: return launch_tc<4, 8>(p, s);
+        case 0x82: return launch_tc<8, 2>(p, s);
+        case 0x84: return launch_tc<8, 4>(p, s);
+        case 0x88: return launch_tc<8, 8>(p, s);
+        case 0x33: return launch_tc<3, 3>(p, s);
+        case 0x55: return launch_tc<5, 5>(p, s);
+        case 0x66: return launch_tc<6, 6>(p, s);
+        case 0x65: return launch_tc<6, 5>(p, s);
+        case 0x54: return launch_tc<5, 4>(p, s);
+        case 0x32: return launch_tc<3, 2>(p, s);
     }
     return (int)cudaErrorInvalidValue;
 }
