@@ -83,6 +83,24 @@ def test_prompt_from_scratch_every_position(hq, hkv):
     _check(cache, 0, q.cpu().numpy(), out.float().cpu().numpy(), 2, 2, label=f"r {hq // hkv}")
 
 
+def test_prompt_tiles_with_one_to_six_sealed_groups():
+    """A 900-token prompt: its query tiles see 0 to 6 sealed groups, so the switch from
+    sealed groups to the exact blocks (where the output is rotated back) falls after an
+    odd and after an even number of groups, with PV of earlier groups still in flight.
+    A completion barrier that a late wait could mistake for an older phase gave errors
+    of O(1) in the tiles with an even count; every row is checked."""
+    hq, hkv = 8, 2
+    cache = _cache(hq, hkv, 2, 2)
+    n = 900
+    k, v = _tokens(48, 0, 0, n, hkv)
+    cache.append(0, [0], [n], k, v)
+    q = _queries(49, n, hq)
+    out = cache.prefill_attention(0, [0], [n], q)
+    torch.cuda.synchronize()
+    assert cache.check_device_error() == 0
+    _check(cache, 0, q.cpu().numpy(), out.float().cpu().numpy(), 2, 2, label="900")
+
+
 @pytest.mark.parametrize("kb,vb", [(4, 2), (3, 3), (8, 8), (6, 5), (5, 4), (3, 2), (2, 8)])
 def test_chunks_on_a_cache_at_every_width(kb, vb):
     """Three sequences in one call: a chunk on top of a longer cache (ragged tile), a
