@@ -173,37 +173,62 @@ __device__ __forceinline__ uint32_t bits_of(const uint32_t (&s)[N], int pos, int
     return v & ((1u << width) - 1u);
 }
 
+// The codes enter the tensor cores as f16 subnormals: the bit pattern of a code c in
+// the low bits of a half is c 2^-24, exact, so no conversion is needed; the 2^24 is
+// folded into the group's scale (deltaK in the logits, deltaV aV_t in the V tile).
+constexpr float kCodeUnit = 16777216.0f;  // 2^24
+
+// Two codes at bits 0 .. B - 1 and B .. 2 B - 1 of f as a word of two f16 subnormals.
+template <int B>
+__device__ __forceinline__ uint32_t code_pair(uint32_t f) {
+    constexpr uint32_t mask = (1u << B) - 1u;
+    return (f & mask) | (((f >> B) & mask) << 16);
+}
+
+// Codes of one 16-bit field x (16 / B of them, B = 2, 4 or 8) as 8 / B words: with
+// y = x | x << (16 - B), word k is (y >> 2 B k) masked to B bits in each half (the low
+// half never reaches bit 16 - B, the high half reads only the shifted copy).
+template <int B>
+__device__ __forceinline__ void code_words16(uint32_t x, uint32_t* o) {
+    constexpr uint32_t mask = ((1u << B) - 1u) * 0x00010001u;
+    const uint32_t y = x | (x << (16 - B));
+#pragma unroll
+    for (int k = 0; k < 8 / B; ++k) o[k] = (y >> (2 * B * k)) & mask;
+}
+
 // Codes 8 m .. 8 m + 7 of a row of 128 B-bit codes held in s (4 B words) as four words
-// of two f16 integers each (exact).
+// of two f16 subnormals each.
 template <int B>
 __device__ __forceinline__ uint4 codes8(const uint32_t (&s)[4 * B], int m) {
-    constexpr uint32_t mask = (1u << B) - 1u;
     uint32_t o[4];
+    if constexpr (B == 2 || B == 4 || B == 8) {
 #pragma unroll
-    for (int k = 0; k < 4; ++k) {
-        const uint32_t f = bits_of(s, (8 * m + 2 * k) * B, 2 * B);
-        // 0x6400 | c is the half 1024 + c; subtracting 1024 leaves c exactly
-        const uint32_t w = ((f & mask) | ((f >> B) << 16)) | 0x64006400u;
-        o[k] = h2u(__hsub2(u2h(w), __halves2half2(__ushort_as_half(0x6400), __ushort_as_half(0x6400))));
+        for (int h = 0; h < B / 2; ++h) {
+            const int pos = 8 * B * m + 16 * h;
+            code_words16<B>((s[pos >> 5] >> (pos & 31)) & 0xffffu, o + h * (8 / B));
+        }
+    } else {
+#pragma unroll
+        for (int k = 0; k < 4; ++k) o[k] = code_pair<B>(bits_of(s, (8 * m + 2 * k) * B, 2 * B));
     }
     return make_uint4(o[0], o[1], o[2], o[3]);
 }
 
 // Codes 8 m .. 8 m + 7 of a row of 128 B-bit codes staged as words k at col[128 k], as
-// four words of two f16 integers each (exact); m may vary at run time.
+// four words of two f16 subnormals each; m may vary at run time.
 template <int B>
 __device__ __forceinline__ uint4 codes8_staged(const uint32_t* col, int m) {
-    constexpr uint32_t mask = (1u << B) - 1u;
     const int pos = 8 * B * m, lo = pos >> 5, sh = pos & 31;
     uint64_t bits = col[128 * lo];
     if (sh + 8 * B > 32) bits |= (uint64_t)col[128 * (lo + 1)] << 32;
     bits >>= sh;
     uint32_t o[4];
+    if constexpr (B == 2 || B == 4 || B == 8) {
 #pragma unroll
-    for (int k = 0; k < 4; ++k) {
-        const uint32_t f = (uint32_t)(bits >> (2 * B * k)) & ((1u << (2 * B)) - 1u);
-        const uint32_t w = ((f & mask) | ((f >> B) << 16)) | 0x64006400u;
-        o[k] = h2u(__hsub2(u2h(w), __halves2half2(__ushort_as_half(0x6400), __ushort_as_half(0x6400))));
+        for (int h = 0; h < B / 2; ++h) code_words16<B>((uint32_t)(bits >> (16 * h)) & 0xffffu, o + h * (8 / B));
+    } else {
+#pragma unroll
+        for (int k = 0; k < 4; ++k) o[k] = code_pair<B>((uint32_t)(bits >> (2 * B * k)));
     }
     return make_uint4(o[0], o[1], o[2], o[3]);
 }
@@ -428,7 +453,7 @@ __device__ __forceinline__ void expand_v_role(const PrefillParams& p, const TcCt
             // B = the dequantised value in the rotated frame, c_j aV_t (deltaV q_tj + mV), times 2^-e
             float* alpha = reinterpret_cast<float*>(set + kOffAlpha);
             float* beta = reinterpret_cast<float*>(set + kOffBeta);
-            alpha[et] = dV * aV;
+            alpha[et] = dV * aV * kCodeUnit;  // the codes are c 2^-24
             beta[et] = mV * aV;
             // (the reductions' barriers also publish alpha and beta)
             const int e = group_exponent<VB>(aV, cV, dV, mV, red_all + 8 * b, et, 1);
@@ -727,7 +752,7 @@ __device__ __forceinline__ void expand_k_unit(const PrefillParams& p, const TcCt
             *reinterpret_cast<uint4*>(set + kOffK + tile_off(et, 8 * m)) = codes8<KB>(L.w, m);
         kt[et] = L.a;
         if (et == 0) {
-            kt[128] = L.d;
+            kt[128] = L.d * kCodeUnit;  // the codes are c 2^-24
             kt[129] = L.m;
             kt[130] = (float)e;
         }
