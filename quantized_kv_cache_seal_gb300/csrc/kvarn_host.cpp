@@ -447,7 +447,8 @@ kvarn_status check_prefill(const kvarn_cache* c, int32_t layer, int32_t n_seqs, 
     return KVARN_OK;
 }
 
-// Prefill attention after check_prefill: one CTA per (sequence, KV head, query tile).
+// Prefill attention after check_prefill: one CTA per (sequence, KV head, query tile),
+// adjacent tiles paired in clusters of two (a padding tile completes an odd count).
 kvarn_status run_prefill(kvarn_cache* c, int32_t layer, int32_t n_seqs, const int32_t* seq_ids,
                          const int32_t* q_lens, const void* q, void* out, float scale, void* stream) {
     const kvarn_config& cfg = c->cfg;
@@ -484,7 +485,8 @@ kvarn_status run_prefill(kvarn_cache* c, int32_t layer, int32_t n_seqs, const in
             e.n_groups = (int32_t)groups_sealed(n, cfg.tail_floor);
             e.n_tiles = (q_lens[i] + qt - 1) / qt;
             e.cta_begin = (int32_t)ctas;
-            ctas += (int64_t)e.n_tiles * cfg.num_kv_heads;
+            // CTA pairs of adjacent tiles (a cluster of two), so an even count per sequence
+            ctas += (int64_t)((e.n_tiles + 1) / 2) * 2 * cfg.num_kv_heads;
         }
         row += q_lens[i];
     }

@@ -95,7 +95,7 @@ struct PrefillSeq {
     int32_t q_row;
     int32_t n_groups;   // sealed groups of the sequence
     int32_t n_tiles;    // query tiles (kPrefillRows / r tokens each)
-    int32_t cta_begin;  // first CTA of this sequence (n_tiles * Hkv CTAs)
+    int32_t cta_begin;  // first CTA of this sequence ((n_tiles + 1) / 2 * 2 * Hkv CTAs: tile pairs)
 };
 
 struct PrefillParams {
@@ -105,7 +105,7 @@ struct PrefillParams {
     uint16_t* out;
     int32_t n_seqs, hq, hkv, r, k_bits, v_bits, layer, num_layers, max_groups;
     int32_t rec_k, rec_v, slot_bytes, tail_cap;
-    int32_t grid;       // CTAs: one per (sequence, KV head, query tile)
+    int32_t grid;       // CTAs: one per (sequence, KV head, query tile), tiles padded to pairs
     float scale_log2;
     PrefillSeq seqs[kMaxBatch];
 };

@@ -11,8 +11,13 @@
 //
 // One CTA per (sequence, KV head, tile of 128 / r query tokens): 128 query rows
 // (token, head), token-major, M = 128 of tcgen05.mma kind::f16 (f16 operands, f32
-// accumulators in tensor memory). The CTA walks its units: the visible sealed groups
-// in order, then the exact blocks (the sink, then the tail, 128 tokens each). For a
+// accumulators in tensor memory). Adjacent tiles run as a cluster of two CTAs that walk
+// the same units (those of the later tile): the visible sealed groups in order, then the
+// exact blocks (the sink, then the tail, 128 tokens each). Each CTA of the pair expands
+// half of every sealed group's K tile (64 channels) and V tile (64 tokens) and sends it
+// to the same place in the other CTA's shared memory with one bulk copy, which completes
+// on the other CTA's full barrier; the tensor cores release a tile in both CTAs
+// (multicast commit), since both write it. For a
 // group with codes q, token scales a, channel scales c and grid (m, delta):
 //   QK  S_it = sum_j A_ij q_tj, A = v c_K as f16 high and low parts (two passes), v the
 //       rotated query of row i over max|v|; the logit is
@@ -28,18 +33,18 @@
 // Warp roles (640 threads, 5 warpgroups; warp w reaches tensor-memory lanes
 // 32 (w % 4) .. 32 (w % 4) + 31, so thread 32 (w % 4) + lane of a warpgroup owns query
 // row 32 (w % 4) + lane):
-//   WG0  softmax: one thread per row; loads S in 32-column chunks (a pass for the
-//        maximum, a pass for the weights), keeps the running maximum (raised only when
-//        it grows by more than 8 in log2 units, with O and l rescaled then), writes W
-//        (high and low f16 parts) over S, and at the end normalises O and writes the
-//        output.
+//   WG0  softmax: one thread per row; takes the unit's logits and row maximum, keeps the
+//        running maximum (raised only when it grows by more than 8 in log2 units, with O
+//        and l rescaled then), writes W (high and low f16 parts) over S in 32-column
+//        chunks, and at the end normalises O and writes the output.
 //   WG1  query operand: rotates and scales its row once, then per group writes A (high
 //        and low parts) into tensor memory and the row sum sum_j v_ij c_j into shared
 //        memory; before the exact blocks it writes the raw query and rotates O back.
-//   WG2  K expansion: the K codes of each group as f16 integers (or the exact K rows) in
-//        a canonical K-major tile (no swizzle) and the group's token scales.
-//   WG3  V expansion: the dequantised V values of each group as high and low parts (or
-//        the exact V rows, transposed) in a canonical K-major tile.
+//   WG2  K expansion: this CTA's half of the K codes of each group as f16 subnormals (or
+//        the exact K rows) in a canonical K-major tile (no swizzle), the group's token
+//        scales; and each unit's logits and row maxima, written over S.
+//   WG3  V expansion: this CTA's half of the dequantised V values of each group as high
+//        and low parts (or the exact V rows, transposed) in a canonical K-major tile.
 //   WG4  warp 16 owns tensor memory and one of its threads issues every MMA, QK or PV,
 //        whichever is ready first.
 // Tensor memory (512 columns): A [0, 128), S0 [128, 256), S1 [256, 384), O [384, 512).
@@ -123,6 +128,39 @@ __device__ __forceinline__ void mma_ts(uint32_t d, uint32_t a, uint64_t b, uint3
 // arrive on bar once every MMA issued so far by this thread has completed
 __device__ __forceinline__ void mma_commit(uint64_t* bar) {
     asm volatile("tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(smem_addr(bar))
+                 : "memory");
+}
+// the same, arriving on the barrier at bar's offset in both CTAs of the pair
+__device__ __forceinline__ void mma_commit_pair(uint64_t* bar) {
+    asm volatile(
+        "tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.multicast::cluster.b64 [%0], %1;" ::"r"(
+            smem_addr(bar)),
+        "h"((uint16_t)3)
+        : "memory");
+}
+
+// ---- the CTA pair (a cluster of two: adjacent query tiles of one sequence and KV head) ----
+__device__ __forceinline__ uint32_t pair_rank() {
+    uint32_t r;
+    asm volatile("mov.u32 %0, %%cluster_ctarank;" : "=r"(r));
+    return r;
+}
+// address in the other CTA's shared memory of the object at `local` in this one's
+__device__ __forceinline__ uint32_t peer_addr(uint32_t local) {
+    uint32_t a;
+    asm volatile("mapa.shared::cluster.u32 %0, %1, %2;" : "=r"(a) : "r"(local), "r"(pair_rank() ^ 1u));
+    return a;
+}
+// every thread of both CTAs (also orders barrier initialisation before remote arrivals)
+__device__ __forceinline__ void pair_sync() {
+    asm volatile("barrier.cluster.arrive.release.aligned;\n\tbarrier.cluster.wait.acquire.aligned;" ::: "memory");
+}
+// bytes of this CTA's shared memory at `src` to the same offset in the other CTA's,
+// completing (as transaction bytes) on the other CTA's barrier at bar's offset
+__device__ __forceinline__ void copy_to_peer(const void* src, uint32_t bytes, uint64_t* bar) {
+    asm volatile("cp.async.bulk.shared::cluster.shared::cta.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];" ::"r"(
+                     peer_addr(smem_addr(src))),
+                 "r"(smem_addr(src)), "r"(bytes), "r"(peer_addr(smem_addr(bar)))
                  : "memory");
 }
 
@@ -243,6 +281,7 @@ struct TcCta {
     int tail_start, tail_vis;
     int units;          // n_sealed + exact blocks
     size_t blk;         // (sequence, layer, KV head) index of the exact regions
+    int rank;           // in the CTA pair: expands K channel chunks and V token chunks 8 rank .. 8 rank + 7
 };
 
 struct Unit {
@@ -323,7 +362,7 @@ __device__ __forceinline__ void issue_qk(const TcCta& c, uint32_t sbase, uint64_
         for (int ks = 0; ks < 8; ++ks) mma_ts(d, tmem + kColA + 64 + 8 * ks, smem_desc(kt + ks * 4096), 1u);
     }
     mma_commit(bars + kBarSFull + b);
-    mma_commit(bars + kBarKEmpty + b);
+    mma_commit_pair(bars + kBarKEmpty + b);  // both CTAs write this CTA's K tile
     if (sealed) mma_commit(bars + kBarAEmpty);
 }
 
@@ -343,7 +382,7 @@ __device__ __forceinline__ void issue_pv(const TcCta& c, uint32_t sbase, uint64_
             mma_ts(tmem + kColO, a + 16 * ks + alo, smem_desc(vt + (bks + ks) * 4096),
                    (v > 0 || ps > 0 || ks > 0) ? 1u : 0u);
     }
-    mma_commit(bars + kBarVEmpty + b);
+    mma_commit_pair(bars + kBarVEmpty + b);  // both CTAs write this CTA's V tile
     mma_commit(bars + kBarODone + b);
 }
 
@@ -466,8 +505,10 @@ __device__ __forceinline__ void expand_v_role(const PrefillParams& p, const TcCt
             uint32_t* vst = reinterpret_cast<uint32_t*>(smem + kOffVst) + et;
 #pragma unroll
             for (int k = 0; k < 4 * VB; ++k) vst[128 * k] = vs_[k];
+            // this CTA's half: tokens 64 rank .. 64 rank + 63 (k-steps 4 rank .. 4 rank + 3 of
+            // the high parts and 8 + 4 rank .. of the low parts); the other CTA sends the rest
 #pragma unroll 1
-            for (int m = 0; m < 16; ++m) {
+            for (int m = 8 * c.rank; m < 8 * c.rank + 8; ++m) {
                 const uint4 q4 = codes8_staged<VB>(vst, m);
                 const uint32_t qw[4] = {q4.x, q4.y, q4.z, q4.w};
                 uint32_t hi[4], lo[4];
@@ -508,7 +549,18 @@ __device__ __forceinline__ void expand_v_role(const PrefillParams& p, const TcCt
             }
         }
         fence_proxy_async_smem();
-        mbar_arrive(bars + kBarVFull + b);
+        if (x.sealed) {
+            named_bar(7, 128);
+            if (et == 0) {
+                copy_to_peer(set + kOffV + 4 * c.rank * 4096, 4 * 4096, bars + kBarVFull + b);
+                copy_to_peer(set + kOffV + (8 + 4 * c.rank) * 4096, 4 * 4096, bars + kBarVFull + b);
+                mbar_arrive_expect_tx(bars + kBarVFull + b, 8 * 4096);
+            } else {
+                mbar_arrive(bars + kBarVFull + b);
+            }
+        } else {
+            mbar_arrive(bars + kBarVFull + b);
+        }
     }
 }
 
@@ -747,9 +799,14 @@ __device__ __forceinline__ void expand_k_unit(const PrefillParams& p, const TcCt
         // the softmax of unit u - 4 is done, which QK(u - 2) being issued implies
         if (u >= 2) mbar_wait(bars + kBarKEmpty + b, (uint32_t)(((u >> 1) - 1) & 1), err);
         const int e = group_exponent<VB>(L.aV, L.cV, L.dV, L.mV, red_all + 8 * b, et, 5);
+        // this CTA's half of the tile: channels 64 rank .. 64 rank + 63 (k-steps 4 rank ..
+        // 4 rank + 3, 16 KB in one piece); the other CTA sends the rest
+        uint32_t hw[4 * KB];  // the half's code words first (selected, not indexed at run time)
 #pragma unroll
-        for (int m = 0; m < 16; ++m)
-            *reinterpret_cast<uint4*>(set + kOffK + tile_off(et, 8 * m)) = codes8<KB>(L.w, m);
+        for (int k = 0; k < 4 * KB; ++k) hw[k] = k < 2 * KB ? (c.rank ? L.w[2 * KB + k] : L.w[k]) : 0u;
+#pragma unroll
+        for (int mm = 0; mm < 8; ++mm)
+            *reinterpret_cast<uint4*>(set + kOffK + tile_off(et, 8 * (8 * c.rank + mm))) = codes8<KB>(hw, mm);
         kt[et] = L.a;
         if (et == 0) {
             kt[128] = L.d * kCodeUnit;  // the codes are c 2^-24
@@ -771,7 +828,19 @@ __device__ __forceinline__ void expand_k_unit(const PrefillParams& p, const TcCt
         }
     }
     fence_proxy_async_smem();
-    mbar_arrive(bars + kBarKFull + (u & 3));
+    if (x.sealed) {
+        // the half goes to the same place in the other CTA once all of it is written;
+        // this CTA's k_full also waits for the 16 KB coming the other way
+        named_bar(6, 128);
+        if (et == 0) {
+            copy_to_peer(set + kOffK + 4 * c.rank * 4096, 4 * 4096, bars + kBarKFull + (u & 3));
+            mbar_arrive_expect_tx(bars + kBarKFull + (u & 3), 4 * 4096);
+        } else {
+            mbar_arrive(bars + kBarKFull + (u & 3));
+        }
+    } else {
+        mbar_arrive(bars + kBarKFull + (u & 3));
+    }
 }
 
 // ---- WG2: the logits of unit v for row i (once QK(v) has completed): written back
@@ -936,13 +1005,18 @@ __device__ __forceinline__ void softmax_role(const PrefillParams& p, const TcCta
 }
 
 template <int KB, int VB>
-__global__ void __launch_bounds__(kTcThreads, 1) prefill_kernel(const __grid_constant__ PrefillParams p) {
+__global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kTcThreads, 1)
+    prefill_kernel(const __grid_constant__ PrefillParams p) {
     extern __shared__ __align__(1024) uint8_t smem[];
     const int t = threadIdx.x, w = t >> 5, lane = t & 31, wg = w >> 2;
     int32_t* err = reinterpret_cast<int32_t*>(p.base + p.lay.err);
     uint64_t* bars = reinterpret_cast<uint64_t*>(smem + kOffBars);
 
-    // the CTA's (sequence, KV head, tile): the heaviest tiles (latest tokens) first
+    // the CTA's (sequence, KV head, tile): pairs of adjacent tiles (2 k, 2 k + 1) share a
+    // cluster, the heaviest pairs (latest tokens) first; a sequence with an odd number of
+    // tiles pads its last pair with a tile past its queries (no valid row). Both CTAs of a
+    // pair walk the units of the later tile (the earlier one's rows mask what they do not
+    // see), so that each expands half of every K and V tile for both.
     TcCta c;
     {
         int lo = 0, up = p.n_seqs - 1;
@@ -951,14 +1025,15 @@ __global__ void __launch_bounds__(kTcThreads, 1) prefill_kernel(const __grid_con
             if (p.seqs[mid].cta_begin <= (int)blockIdx.x) lo = mid; else up = mid - 1;
         }
         c.e = &p.seqs[lo];
-        const int local = (int)blockIdx.x - c.e->cta_begin;
-        c.kvh = local % p.hkv;
-        const int tile = c.e->n_tiles - 1 - local / p.hkv;
+        const int local = (int)blockIdx.x - c.e->cta_begin;  // cta_begin is even
+        c.rank = (int)pair_rank();
+        c.kvh = (local >> 1) % p.hkv;
+        const int pair = (c.e->n_tiles + 1) / 2 - 1 - (local >> 1) / p.hkv;
         const int qt = kRows / p.r;
-        c.t0 = tile * qt;
+        c.t0 = (2 * pair + c.rank) * qt;
         const int first_pos = c.e->n - c.e->q_len;
         c.pmin = first_pos + c.t0;
-        c.pmax = first_pos + min(c.t0 + qt, c.e->q_len) - 1;
+        c.pmax = first_pos + min((2 * pair + 2) * qt, c.e->q_len) - 1;  // the later tile's last row
         const int vis = c.pmax >= kSink ? (c.pmax - kSink) / kGroup + 1 : 0;
         c.n_sealed = min(c.e->n_groups, vis);
         c.blk = ((size_t)c.e->seq * p.num_layers + p.layer) * p.hkv + c.kvh;
@@ -979,9 +1054,9 @@ __global__ void __launch_bounds__(kTcThreads, 1) prefill_kernel(const __grid_con
             mbar_init(bars + kBarMFull + k, 128);
         }
         for (int k = 0; k < 2; ++k) {
-            mbar_init(bars + kBarKEmpty + k, 1);
+            mbar_init(bars + kBarKEmpty + k, 2);  // the QK of both CTAs
             mbar_init(bars + kBarVFull + k, 128);
-            mbar_init(bars + kBarVEmpty + k, 1);
+            mbar_init(bars + kBarVEmpty + k, 2);  // the PV of both CTAs
             mbar_init(bars + kBarSFull + k, 1);
             mbar_init(bars + kBarPFull + k, 128);
             mbar_init(bars + kBarODone + k, 1);
@@ -997,7 +1072,7 @@ __global__ void __launch_bounds__(kTcThreads, 1) prefill_kernel(const __grid_con
         asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;" ::: "memory");
     }
     tc_fence_before();
-    __syncthreads();
+    pair_sync();  // the other CTA's barriers are initialised before anything arrives on them
     tc_fence_after();
     const uint32_t tmem = *reinterpret_cast<volatile uint32_t*>(smem + kOffTmem);
     const uint32_t lane_off = (uint32_t)(32 * (w & 3)) << 16;
@@ -1026,7 +1101,8 @@ __global__ void __launch_bounds__(kTcThreads, 1) prefill_kernel(const __grid_con
         }
     }
     tc_fence_before();
-    __syncthreads();
+    // neither CTA leaves while the other may still copy into it or commit to its barriers
+    pair_sync();
     tc_fence_after();
     if (w == 16) {
         __syncwarp();
