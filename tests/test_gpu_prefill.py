@@ -7,10 +7,11 @@ runs over the GPU's own records and exact regions (the decoupled protocol of
 tests/parity.py), so seal parity and attention parity are checked apart; the records
 themselves are checked against the oracle's seal in the seal and decode tests.
 Cases: prompts from scratch (queries in the sink, inside sealed groups, in the tail),
-chunks on top of a cache, every query head ratio (1, 2, 4), widths 2..8 with the odd
-ones and the presets, a tail floor, empty query lists, the fused append + attention,
-a second layer with interleaved pool slots and norm spikes at the Phi-4 shape, and
-sampled rows of the Qwen3-4B 4096-token prefill.
+chunks on top of a cache (also one whose paired query tiles see different units),
+every query head ratio (1, 2, 4), widths 2..8 with the odd ones and the presets, a
+tail floor, empty query lists, the fused append + attention, a second layer with
+interleaved pool slots and norm spikes at the Phi-4 shape, and sampled rows of the
+Qwen3-4B 4096-token prefill.
 """
 import math
 
@@ -99,6 +100,26 @@ def test_prompt_tiles_with_one_to_six_sealed_groups():
     torch.cuda.synchronize()
     assert cache.check_device_error() == 0
     _check(cache, 0, q.cpu().numpy(), out.float().cpu().numpy(), 2, 2, label="900")
+
+
+@pytest.mark.parametrize("hq,hkv", [(8, 2), (2, 2)])
+def test_chunk_whose_tile_pairs_see_different_units(hq, hkv):
+    """Adjacent query tiles run as one CTA pair over the units of the later tile. A chunk
+    of 280 queries at positions 200 .. 479 of a 480-token cache (two sealed groups, the
+    tail from 384): with 32-token tiles (r = 4) the first pair's tiles see one and two
+    sealed groups, so the earlier tile walks a group that every one of its rows masks,
+    and the tile count is odd (a padding tile without valid rows completes the last
+    pair); with 128-token tiles (r = 1) the first pair's earlier tile sees none of the
+    tail its partner sees. Every row is checked."""
+    cache = _cache(hq, hkv, 2, 2)
+    k, v = _tokens(70 + hq, 0, 0, 480, hkv)
+    cache.append(0, [0], [200], k[:200].contiguous(), v[:200].contiguous())
+    cache.append(0, [0], [280], k[200:].contiguous(), v[200:].contiguous())
+    q = _queries(71 + hq, 280, hq)
+    out = cache.prefill_attention(0, [0], [280], q)
+    torch.cuda.synchronize()
+    assert cache.check_device_error() == 0
+    _check(cache, 0, q.cpu().numpy(), out.float().cpu().numpy(), 2, 2, label=f"pairs r {hq // hkv}")
 
 
 @pytest.mark.parametrize("kb,vb", [(4, 2), (3, 3), (8, 8), (6, 5), (5, 4), (3, 2), (2, 8)])
