@@ -22,7 +22,9 @@ struct PtrRows {
     __device__ const uint16_t* operator()(int i) const { return base + 128 * i; }
 };
 
-__global__ void __launch_bounds__(256) seal_groups_kernel(const uint16_t* x, int bits, int which, int iters,
+// Two CTAs per SM (at most 128 registers a thread; 73 KB of shared memory each): a
+// prompt's few hundred group matrices then take two rounds of the GPU instead of four.
+__global__ void __launch_bounds__(256, 2) seal_groups_kernel(const uint16_t* x, int bits, int which, int iters,
                                                           uint8_t* records, float* scales) {
     extern __shared__ __align__(16) uint8_t smem_raw[];
     SealSmem& S = *reinterpret_cast<SealSmem*>(smem_raw);
@@ -46,7 +48,7 @@ struct JobRows {
     }
 };
 
-__global__ void __launch_bounds__(256) seal_jobs_kernel(const __grid_constant__ SealParams p) {
+__global__ void __launch_bounds__(256, 2) seal_jobs_kernel(const __grid_constant__ SealParams p) {
     extern __shared__ __align__(16) uint8_t smem_raw[];
     SealSmem& S = *reinterpret_cast<SealSmem*>(smem_raw);
     const int job = blockIdx.x;
