@@ -388,7 +388,6 @@ kvarn_status run_decode(kvarn_cache* c, int32_t layer, int32_t n_seqs, const int
         for (int32_t s : taken) c->free_slots.push_back(s);
         return st;
     }
-    int pair = (int)(c->rec_k + c->rec_v);
     int stages = 32;
     while (stages > 1 && decode_smem_bytes(cfg.k_bits, cfg.v_bits, stages, any_seal) > c->max_smem) --stages;
     if (decode_smem_bytes(cfg.k_bits, cfg.v_bits, stages, any_seal) > c->max_smem) {
